@@ -1,0 +1,223 @@
+"""Seeded synthetic decode-attention inputs.
+
+This module only draws random numbers and lays them out; it holds none of the
+attention arithmetic, so both the CUDA path and the CPU oracle can take their
+inputs from it.  Everything is generated on the CPU with
+``torch.Generator().manual_seed(seed)`` so that both sides see identical bits.
+
+Cache layouts (``H`` = KV heads, ``D`` = head dim, bf16):
+
+* contiguous: ``[B, Lmax, H, D]``; row b's entry t is ``cache[b, t]``
+* paged:      ``[num_pages, P, H, D]`` + ``table int32[B, width]``; entry t of
+              row b is ``cache[table[b, t // P], t % P]``; unused table slots
+              hold -1
+* indexed:    ``[num_slots, H, D]`` + ``table int32[B, width]`` of slot indices
+              (a row's top-k list); entries past the row's length hold -1
+
+The named workloads follow the five configurations the pages' problem
+statement is measured on (tiny dense, GQA paged, MLA-style sparse, ragged
+invariance sweep, long context); sizes are spelled out in each function.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import torch
+
+CONTIGUOUS = "contiguous"
+PAGED = "paged"
+INDEXED = "indexed"
+
+
+@dataclasses.dataclass
+class Workload:
+    name: str
+    layout: str
+    q: torch.Tensor                 # [B, H_q, D_qk] bf16
+    k: torch.Tensor                 # key cache (or shared latent cache), bf16
+    v: Optional[torch.Tensor]       # value cache, or None when V = k[..., :D_v]
+    lengths: torch.Tensor           # int32 [B]
+    table: Optional[torch.Tensor]   # int32 [B, width] page table / indices
+    page_size: int
+    H_q: int
+    H_kv: int
+    D_qk: int
+    D_v: int
+    scale: float
+
+    @property
+    def B(self):
+        return self.q.shape[0]
+
+    @property
+    def width(self):
+        """Contiguous: Lmax; paged: page-table width; indexed: index width."""
+        if self.layout == CONTIGUOUS:
+            return self.k.shape[1]
+        return self.table.shape[1]
+
+    @property
+    def num_blocks(self):
+        """Pages (paged) or slots (indexed) in the cache; rows*Lmax otherwise."""
+        if self.layout == CONTIGUOUS:
+            return self.k.shape[0] * self.k.shape[1]
+        return self.k.shape[0]
+
+    def kv_bytes(self):
+        """Bytes of K and V the rows actually attend over (the algorithmic payload)."""
+        n = int(self.lengths.to(torch.int64).sum())
+        per_entry_k = self.H_kv * self.D_qk * 2
+        per_entry_v = 0 if self.v is None else self.H_kv * self.D_v * 2
+        return n * (per_entry_k + per_entry_v)
+
+    def to(self, device):
+        def mv(t):
+            return None if t is None else t.to(device)
+        return dataclasses.replace(self, q=mv(self.q), k=mv(self.k), v=mv(self.v),
+                                   lengths=mv(self.lengths), table=mv(self.table))
+
+
+def _randn(shape, g):
+    return torch.randn(shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
+
+
+def page_table(lengths, page_size, g, width=None, spare_pages=0):
+    """Random page ids for each row: every row gets ceil(L/P) distinct pages
+    drawn from a shuffled pool.  Returns (table[B, width], num_pages)."""
+    need = [-(-int(L) // page_size) for L in lengths]
+    width = max(max(need), 1) if width is None else width
+    num_pages = sum(need) + spare_pages
+    perm = torch.randperm(max(num_pages, 1), generator=g)[:num_pages].to(torch.int32)
+    table = torch.full((len(need), width), -1, dtype=torch.int32)
+    off = 0
+    for b, n in enumerate(need):
+        table[b, :n] = perm[off:off + n]
+        off += n
+    return table, max(num_pages, 1)
+
+
+def make(layout, lengths, *, H_q, H_kv, D_qk, D_v=None, page_size=16, width=None,
+         num_slots=None, latent=False, seed=0, scale=None, name="custom",
+         identity_table=False):
+    """General seeded workload.  q, K, V ~ N(0, 1) rounded to bf16.
+
+    latent=True makes one shared latent cache with V = K[..., :D_v] (MLA-style).
+    identity_table=True lays paged rows out in consecutive pages (no shuffle).
+    """
+    g = torch.Generator().manual_seed(seed)
+    lengths = torch.as_tensor(lengths, dtype=torch.int32)
+    B = lengths.numel()
+    D_v = D_qk if D_v is None else D_v
+    scale = 1.0 / math.sqrt(D_qk) if scale is None else scale
+    q = _randn((B, H_q, D_qk), g)
+    table = None
+    if layout == CONTIGUOUS:
+        Lmax = max(int(lengths.max()) if B else 0, 1) if width is None else width
+        kshape = (B, Lmax, H_kv, D_qk)
+        vshape = (B, Lmax, H_kv, D_v)
+    elif layout == PAGED:
+        if identity_table:
+            need = [-(-int(L) // page_size) for L in lengths]
+            w = max(max(need), 1) if width is None else width
+            table = torch.full((B, w), -1, dtype=torch.int32)
+            off = 0
+            for b, n in enumerate(need):
+                table[b, :n] = torch.arange(off, off + n, dtype=torch.int32)
+                off += n
+            num_pages = max(off, 1)
+        else:
+            table, num_pages = page_table(lengths.tolist(), page_size, g, width)
+        kshape = (num_pages, page_size, H_kv, D_qk)
+        vshape = (num_pages, page_size, H_kv, D_v)
+    elif layout == INDEXED:
+        w = max(int(lengths.max()) if B else 0, 1) if width is None else width
+        n_slots = max(w, 1) if num_slots is None else num_slots
+        table = torch.full((B, w), -1, dtype=torch.int32)
+        for b in range(B):
+            L = int(lengths[b])
+            table[b, :L] = torch.randperm(n_slots, generator=g)[:L].to(torch.int32)
+        kshape = (n_slots, H_kv, D_qk)
+        vshape = (n_slots, H_kv, D_v)
+    else:
+        raise ValueError(layout)
+    k = _randn(kshape, g)
+    v = None if latent else _randn(vshape, g)
+    return Workload(name, layout, q, k, v, lengths, table, page_size,
+                    H_q, H_kv, D_qk, D_v, scale)
+
+
+# --------------------------------------------------------------------------
+# The five named configurations.
+# --------------------------------------------------------------------------
+
+def tiny(seed=1000):
+    """Tiny dense decode: 4 rows, 8 q heads sharing 1 KV head, head_dim 64,
+    KV lengths {17, 100, 256, 1000}, contiguous cache, scale 1/sqrt(64)."""
+    return make(CONTIGUOUS, [17, 100, 256, 1000], H_q=8, H_kv=1, D_qk=64,
+                seed=seed, name="tiny_dense_b4_h8x1_d64")
+
+
+def gqa_paged(seed=1001, B=32):
+    """GQA paged decode: 32 rows, 32 q / 8 KV heads, head_dim 128, page 16,
+    shuffled page table, lengths uniform in [512, 8192]."""
+    g = torch.Generator().manual_seed(seed)
+    lengths = torch.randint(512, 8193, (B,), generator=g, dtype=torch.int64)
+    return make(PAGED, lengths.tolist(), H_q=32, H_kv=8, D_qk=128, page_size=16,
+                width=8192 // 16, seed=seed + 7919, name="gqa_paged_b32_h32x8_d128_p16")
+
+
+def mla_sparse(seed=1002, B=64, num_slots=65536, max_topk=2048):
+    """MLA-style sparse decode: 64 rows, 128 q heads sharing one latent KV row
+    of 576 dims (the first 512 are V), 65536 cache slots, per-row distinct
+    uniform top-k indices, topk_length uniform in [256, 2048], scale 576^-0.5."""
+    g = torch.Generator().manual_seed(seed)
+    lengths = torch.randint(256, max_topk + 1, (B,), generator=g, dtype=torch.int64)
+    return make(INDEXED, lengths.tolist(), H_q=128, H_kv=1, D_qk=576, D_v=512,
+                width=max_topk, num_slots=num_slots, latent=True, seed=seed + 7919,
+                name="mla_sparse_b64_h128_d576v512_topk2048")
+
+
+def long_context(seed=1004, B=8, L=131072, page_size=64, identity_table=False):
+    """Long-context decode: 8 rows of 131072 entries each, 32 q / 8 KV heads,
+    head_dim 128, paged with page 64 (shuffled table unless identity_table)."""
+    return make(PAGED, [L] * B, H_q=32, H_kv=8, D_qk=128, page_size=page_size,
+                seed=seed, identity_table=identity_table,
+                name=f"long_context_b{B}_l{L}_h32x8_d128_p{page_size}")
+
+
+# Ragged invariance sweep: one fixed target row (length 4096, GQA 32/8,
+# d=128, page 16) embedded at random positions in batches of 1..256 rows whose
+# other rows have log-uniform lengths in [1, 131072].
+RAGGED_TARGET_LEN = 4096
+RAGGED_MAX_LEN = 131072
+
+
+def ragged_target(seed=1003):
+    """The target row's own data: q [32, 128], K and V [4096, 8, 128] (bf16)."""
+    g = torch.Generator().manual_seed(seed)
+    q = _randn((32, 128), g)
+    k = _randn((RAGGED_TARGET_LEN, 8, 128), g)
+    v = _randn((RAGGED_TARGET_LEN, 8, 128), g)
+    return q, k, v
+
+
+def ragged_batch_lengths(B, seed):
+    """Lengths of a ragged batch and the target's position in it.
+
+    Batchmates: L = clamp(floor(2 ** (17 * U)), 1, 131072), U ~ U[0, 1).
+    Returns (lengths list with the target's 4096 at `pos`, pos)."""
+    g = torch.Generator().manual_seed(seed)
+    u = torch.rand(B, generator=g, dtype=torch.float64)
+    lens = torch.clamp(torch.floor(torch.exp2(17.0 * u)), 1, RAGGED_MAX_LEN).to(torch.int64)
+    pos = int(torch.randint(0, B, (1,), generator=g))
+    lens[pos] = RAGGED_TARGET_LEN
+    return lens.tolist(), pos
+
+
+def ragged_page_table(lengths, seed, page_size=16, width=None):
+    """Shuffled page table for a ragged batch: (table[B, width], num_pages)."""
+    g = torch.Generator().manual_seed(seed + 1)
+    return page_table(lengths, page_size, g, width)

@@ -1,0 +1,100 @@
+"""Pins of the oracle's split plans: hand-computed examples, coverage
+invariants and the defining batch-invariance property.  CPU only."""
+
+import random
+
+import pytest
+
+from oracle import plan as P
+
+FMA = P.VARIANT_CONSTANTS["fma"]
+
+
+def test_invariant_hand_examples():
+    # tile 64, >= 8 tiles per split, <= 64 splits (the FMA variant's constants)
+    T, mn, mx = FMA
+    assert (T, mn, mx) == (64, 8, 64)
+    cases = {
+        0: [0, 0],                    # empty row: one empty split
+        1: [0, 1],
+        64: [0, 1],
+        512: [0, 8],                  # 8 tiles: exactly one minimum split
+        513: [0, 8, 9],               # 9 tiles: a full split and a 1-tile tail
+        4096: list(range(0, 65, 8)),  # 64 tiles -> 8 splits of 8
+        # 2048 tiles: tps = max(8, ceil(2048 / 64)) = 32 -> 64 splits of 32
+        131072: list(range(0, 2049, 32)),
+        # 2049 tiles: tps = ceil(2049 / 64) = 33 -> 63 splits of 33 + 2 tiles
+        131073: list(range(0, 2049, 33)) + [2049],
+    }
+    for L, want in cases.items():
+        assert P.plan_invariant([L], T, mn, mx) == [want], L
+
+
+def test_invariant_coverage_and_limits():
+    T, mn, mx = FMA
+    for L in list(range(0, 3000)) + [131071, 131072, 131073, 1 << 20, 1 << 24]:
+        (cuts,) = P.plan_invariant([L], T, mn, mx)
+        n_tiles = -(-L // T)
+        assert cuts[0] == 0 and cuts[-1] == n_tiles
+        n = len(cuts) - 1
+        assert 1 <= n <= mx
+        sizes = [b - a for a, b in zip(cuts[:-1], cuts[1:])]
+        if L == 0:
+            assert sizes == [0]
+            continue
+        assert all(s > 0 for s in sizes)
+        tps = sizes[0]
+        assert tps >= mn or n == 1
+        assert all(s == tps for s in sizes[:-1]) and sizes[-1] <= tps
+
+
+def test_invariant_plan_of_a_row_does_not_depend_on_its_batch():
+    # the defining property: a row's splits are a function of its own length
+    rng = random.Random(0)
+    T, mn, mx = FMA
+    target = 4096
+    solo = P.plan_invariant([target], T, mn, mx)[0]
+    for B in (1, 2, 7, 64, 256):
+        lens = [int(2 ** (17 * rng.random())) for _ in range(B)]
+        pos = rng.randrange(B)
+        lens[pos] = target
+        assert P.plan_invariant(lens, T, mn, mx)[pos] == solo
+
+
+def test_balanced_hand_example():
+    # 3 rows of 10, 1, 20 tiles (tile 1), overhead 2, 4 parts:
+    # total = 12 + 3 + 22 = 37, payload = ceil(37 / 4) + 2 = 12.
+    # part 0: row 0 (10 + 2 = 12) fills it exactly.
+    # part 1: row 1 (1 + 2) leaves room 9; row 2 takes 9 - 2 = 7 tiles, cut at 7.
+    # part 2: row 2's remaining 13 + 2 > 12: takes 10 tiles, cut at 17.
+    # part 3: remaining 3 + 2 fits.
+    got = P.plan_balanced([10, 1, 20], 1, 64, 4, 2)
+    assert got == [[0, 10], [0, 1], [0, 7, 17, 20]]
+
+
+def test_balanced_coverage_and_split_cap():
+    rng = random.Random(1)
+    for _ in range(200):
+        B = rng.randint(1, 40)
+        lens = [rng.choice([0, 1, rng.randint(1, 200000)]) for _ in range(B)]
+        parts = rng.randint(1, 300)
+        mx = rng.choice([1, 2, 8, 64])
+        bounds = P.plan_balanced(lens, 64, mx, parts, 2)
+        for L, cuts in zip(lens, bounds):
+            n_tiles = -(-L // 64)
+            assert cuts[0] == 0 and cuts[-1] == n_tiles
+            assert 1 <= len(cuts) - 1 <= mx
+            assert all(b > a for a, b in zip(cuts[:-1], cuts[1:])) or n_tiles == 0
+
+
+def test_balanced_split_depends_on_batchmates():
+    # the counter-example the page describes: the same row is cut
+    # differently when its batchmates change
+    solo = P.plan_balanced([4096 // 64], 1, 64, 100, 2)[0]
+    mixed = P.plan_balanced([4096 // 64] + [2000] * 50, 1, 64, 100, 2)[0]
+    assert solo != mixed
+
+
+def test_work_list_order():
+    bounds = [[0, 1], [0, 2, 3, 4], [0, 0]]
+    assert P.work_list(bounds, 64) == [0, 64, 65, 66, 128]
