@@ -1,0 +1,444 @@
+"""Decode-attention benchmark: KV GB/s, rows/s and HBM-roofline fraction.
+
+One step = one pass of the whole hot path over one batch: split plan, split
+kernel, combine (three launches through the C ABI), inputs resident in HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload gqa_paged|long_context|tiny|ragged]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
+of the workload (rows are independent; no collective on the data path) and
+the step time is the max over ranks.  ``--impl reference`` times the fp64 CPU
+oracle on the host cores on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+# numpy's BLAS threads for the CPU oracle leg: all host cores, stated in the output
+_CORES = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(_CORES))
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "decode-attn KV GB/s (% of GB300 HBM peak), rows/s; invariant vs balanced split"
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+KERNEL_SOURCES = {
+    "split_fma": ["invariant_decode_attention_gb300/csrc/split_fma.cu",
+                  "invariant_decode_attention_gb300/csrc/common.cuh"],
+}
+
+
+# ----------------------------------------------------------------- helpers
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def source_hash(kernel):
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(PROFILE_DIR, "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    r = rec.get(f"{kernel}:{workload}")
+    if not r or r.get("src_sha") != source_hash(kernel):
+        return None
+    return r.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons through NVML while running."""
+
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device_index=0, period=0.005):
+        self.period = period
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self._stop = threading.Event()
+        self._nvml = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() == 0:
+                h = ctypes.c_void_p()
+                if nv.nvmlDeviceGetHandleByIndex_v2(device_index, ctypes.byref(h)) == 0:
+                    self._nvml, self._h = nv, h
+                    mx = ctypes.c_uint()
+                    if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                        self.max_mhz = mx.value
+        except OSError:
+            pass
+
+    def _run(self):
+        nv, h = self._nvml, self._h
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                self.samples.append(clk.value)
+            if nv.nvmlDeviceGetCurrentClocksEventReasons(h, ctypes.byref(rs)) == 0:
+                for bit, name in self.REASONS.items():
+                    if rs.value & bit:
+                        self.reasons.add(name)
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self._nvml is not None:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self._nvml is not None:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                    "samples": 0}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ----------------------------------------------------------------- workloads
+
+def build_workload(name, rank=0):
+    from invariant_decode_attention_gb300 import workloads as W
+    seed_shift = 100 * rank  # every rank its own replica batch (weak scaling)
+    if name == "gqa_paged":
+        return W.gqa_paged(seed=1001 + seed_shift)
+    if name == "long_context":
+        return W.long_context(seed=1004 + seed_shift)
+    if name == "tiny":
+        return W.tiny(seed=1000 + seed_shift)
+    raise ValueError(name)
+
+
+class GpuCase:
+    """A workload resident on the device plus its plan/run/combine step."""
+
+    def __init__(self, wl_cpu, device, policy):
+        from invariant_decode_attention_gb300 import api
+        self.api = api
+        self.cpu = wl_cpu
+        self.wl = wl_cpu.to(device)
+        self.policy = policy
+        self.prob = api.problem_for(self.wl)
+        self.ws = api.workspace(self.prob, device)
+        self.out = torch.empty((self.wl.B, self.wl.H_q, self.wl.D_v), dtype=torch.bfloat16,
+                               device=device)
+        self.lse = torch.empty((self.wl.B, self.wl.H_q), dtype=torch.float32, device=device)
+
+    def step(self, ev_run=None):
+        a, w = self.api, self.wl
+        pl = a.plan(self.prob, self.policy, w.lengths, self.ws)
+        if ev_run is not None:
+            ev_run[0].record()
+        a.run(pl, w.q, w.k, w.v, w.table, w.lengths, self.out, self.lse)
+        if ev_run is not None:
+            ev_run[1].record()
+        a.combine(pl, self.out, self.lse)
+
+
+def time_steps(case, steps, warmup, split_events=True):
+    """Device time per step (ms) and of the split kernel alone, CUDA events on
+    the launching stream, synchronised on both sides."""
+    for _ in range(warmup):
+        case.step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    runs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(steps)] if split_events else [None] * steps
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record()
+    for i in range(steps):
+        starts[i].record()
+        case.step(runs[i])
+        ends[i].record()
+    t1.record()
+    torch.cuda.synchronize()
+    per_step = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    split = [r[0].elapsed_time(r[1]) for r in runs] if split_events else []
+    return t0.elapsed_time(t1), per_step, split
+
+
+def e2e_steps(case, steps, warmup):
+    """Same step through the public C entry point with host buffers: per step
+    the step inputs (q, lengths, page table) go host->device from pinned
+    memory and (out, lse) come back; the KV cache stays resident."""
+    api, w = case.api, case.wl
+    h_q = case.cpu.q.pin_memory()
+    h_len = case.cpu.lengths.pin_memory()
+    h_tab = None if case.cpu.table is None else case.cpu.table.pin_memory()
+    h_out = torch.empty(case.out.shape, dtype=torch.bfloat16).pin_memory()
+    h_lse = torch.empty(case.lse.shape, dtype=torch.float32).pin_memory()
+    d_q, d_len = torch.empty_like(w.q), torch.empty_like(w.lengths)
+    d_tab = None if w.table is None else torch.empty_like(w.table)
+    h2d = h_q.numel() * 2 + h_len.numel() * 4 + (0 if h_tab is None else h_tab.numel() * 4)
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+
+    def one():
+        d_q.copy_(h_q, non_blocking=True)
+        d_len.copy_(h_len, non_blocking=True)
+        if d_tab is not None:
+            d_tab.copy_(h_tab, non_blocking=True)
+        api.forward(case.prob, case.policy, d_q, w.k, w.v, d_tab, d_len, case.ws, case.out,
+                    case.lse)
+        h_out.copy_(case.out, non_blocking=True)
+        h_lse.copy_(case.lse, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps, h2d, d2h
+
+
+# ----------------------------------------------------------------- CPU oracle
+
+def cpu_oracle_rate(wl, budget_s=15.0, max_rows=None):
+    """Time the fp64 oracle, as it stands, on whole rows of the workload until
+    the budget is spent.  Returns (GB/s, rows/s, rows done, seconds)."""
+    from oracle import attention as A
+    q = wl.q.double().numpy()
+    table = None if wl.table is None else wl.table.numpy()
+
+    class View:  # fp64 reads of the bf16 cache, row by row
+        def __init__(self, t):
+            self.t, self.shape = t, tuple(t.shape)
+
+        def __getitem__(self, idx):
+            idx = idx if isinstance(idx, tuple) else (idx,)
+            idx = tuple(torch.as_tensor(np.asarray(i)) if not isinstance(i, (int, slice)) else i
+                        for i in idx)
+            return self.t[idx].double().numpy()
+
+    K, V = View(wl.k), (None if wl.v is None else View(wl.v))
+    per_entry = wl.H_kv * (wl.D_qk + (0 if wl.v is None else wl.D_v)) * 2
+    done, nbytes = 0, 0
+    t0 = time.perf_counter()
+    for b in range(wl.B if max_rows is None else min(wl.B, max_rows)):
+        A.attend(q, K, V, wl.lengths.numpy(), scale=wl.scale, layout=wl.layout, table=table,
+                 page_size=wl.page_size, d_v=wl.D_v, rows=[b])
+        done += 1
+        nbytes += int(wl.lengths[b]) * per_entry
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return nbytes / dt / 1e9, done / dt, done, dt
+
+
+# ----------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="gqa_paged",
+                    choices=["gqa_paged", "long_context", "tiny"])
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the secondary workloads and the CPU baseline")
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from invariant_decode_attention_gb300 import api
+    api.lib()
+    peak, peak_kind = measured_peaks()
+
+    wl = build_workload(args.workload, rank)
+    case = GpuCase(wl, dev, api.INVARIANT)
+    kv_bytes = wl.kv_bytes()
+    io_bytes = wl.q.numel() * 2 + wl.B * wl.H_q * (wl.D_v * 2 + 4)
+    alg_bytes = kv_bytes + io_bytes
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        total_ms, per_step, split_ms = time_steps(case, args.steps, args.warmup)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+        dist.barrier()
+    ms_per_step = total_ms / args.steps
+    value = world * kv_bytes / (ms_per_step * 1e-3) / 1e9
+    split_avg = sum(split_ms) / len(split_ms)
+    achieved = alg_bytes / (split_avg * 1e-3) / 1e9
+
+    if rank != 0:
+        return
+
+    # INVARIANT vs BALANCED on the same inputs
+    n_bal = max(20, args.steps // 4)
+    case.policy = api.BALANCED
+    bal_ms, _, _ = time_steps(case, n_bal, args.warmup, split_events=False)
+    bal_ms /= n_bal
+    case.policy = api.INVARIANT
+
+    e2e_ms, h2d, d2h = e2e_steps(case, max(20, args.steps // 4), args.warmup)
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "math": "fp32",
+        "data": "synthetic",
+        "config": {
+            "workload": wl.name, "rows": wl.B, "H_q": wl.H_q, "H_kv": wl.H_kv,
+            "head_dim": wl.D_qk, "layout": wl.layout, "page_size": wl.page_size,
+            "kv_bytes_per_step": kv_bytes, "policy": "invariant",
+            "l2": f"inputs larger than L2 ({kv_bytes / 1e6:.0f} MB of KV per step)",
+            "parallelism": f"replicas x{world}",
+        },
+        "rows_per_s": round(world * wl.B / (ms_per_step * 1e-3), 1),
+        "hbm_frac_of_" + peak_kind: round(value / world / peak, 4),
+        "balanced": {"ms_per_step": round(bal_ms, 5),
+                     "value": round(kv_bytes / (bal_ms * 1e-3) / 1e9, 2),
+                     "invariant_over_balanced_time": round(ms_per_step / bal_ms, 4)},
+        "roofline": {
+            "kernel": "split_fma", "bound": "hbm", "achieved": round(achieved, 1),
+            "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "peak_kind": peak_kind,
+            "traffic": recorded_traffic("split_fma", wl.name),
+            "alg_bytes_per_launch": alg_bytes,
+            "split_ms_avg": round(split_avg, 5),
+        },
+        "e2e": {"value": round(kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "resident": "KV cache"},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if not args.no_extra:
+        extra = {}
+        for name in ("long_context", "tiny"):
+            if name == args.workload:
+                continue
+            w2 = build_workload(name)
+            c2 = GpuCase(w2, dev, api.INVARIANT)
+            n = 20 if name == "long_context" else 200
+            ms2, _, sp2 = time_steps(c2, n, 5)
+            ms2 /= n
+            kvb = w2.kv_bytes()
+            c2.policy = api.BALANCED
+            bms, _, _ = time_steps(c2, n, 5, split_events=False)
+            bms /= n
+            extra[w2.name] = {
+                "ms_per_step": round(ms2, 5), "kv_gbs": round(kvb / (ms2 * 1e-3) / 1e9, 1),
+                "rows_per_s": round(w2.B / (ms2 * 1e-3), 1),
+                "hbm_frac": round(kvb / (ms2 * 1e-3) / 1e9 / peak, 4),
+                "split_ms_avg": round(sum(sp2) / len(sp2), 5),
+                "balanced_ms_per_step": round(bms, 5),
+            }
+            del c2, w2
+            torch.cuda.empty_cache()
+        line["other_workloads"] = extra
+        gbs, rps, done, dt = cpu_oracle_rate(wl)
+        line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": _CORES,
+                                "kind": "oracle", "rows_per_s": round(rps, 3),
+                                "sample": f"{done} of {wl.B} rows of {wl.name}, all heads, "
+                                          f"{dt:.1f} s, numpy fp64"}
+    print(json.dumps(line), flush=True)
+
+
+def reference_arm(args, rank, world):
+    """The oracle as it stands, on host cores, on the same workload: each step
+    is a bounded sample (whole rows) of the workload."""
+    if rank != 0:
+        return
+    wl = build_workload(args.workload)
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    for _ in range(args.warmup):
+        cpu_oracle_rate(wl, budget_s=budget, max_rows=1)
+    rates, rows = [], 0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        gbs, rps, done, dt = cpu_oracle_rate(wl, budget_s=budget, max_rows=1)
+        rates.append(gbs)
+        rows += done
+    elapsed = time.perf_counter() - t0
+    value = statistics.median(rates)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * elapsed / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "rows": wl.B, "policy": "oracle (exact softmax)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": _CORES,
+                         "kind": "oracle",
+                         "sample": f"one row of {wl.name} per step, numpy fp64"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,356 @@
+// C ABI of the decode attention library: argument checks, workspace layout,
+// plan construction and kernel launches.  Allocates nothing; synchronises the
+// host only in the two documented read-back calls.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace da {
+bool mla_supported(int H_q);
+}
+
+namespace {
+
+using namespace da;
+
+struct Variant {
+  int id, tile, min_tps, max_splits;
+};
+
+struct WsLayout {
+  size_t n_splits, split_begin, work, lse_part, o_part, total;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int check_problem(const da_problem* p) {
+  if (!p) return DA_ERR_INVALID_ARG;
+  if (p->batch < 0 || p->num_q_heads < 1 || p->num_kv_heads < 1) return DA_ERR_INVALID_ARG;
+  if (p->num_q_heads % p->num_kv_heads) return DA_ERR_INVALID_ARG;
+  if (p->head_dim_qk < 1 || p->head_dim_v < 1) return DA_ERR_INVALID_ARG;
+  if (p->layout < DA_KV_CONTIGUOUS || p->layout > DA_KV_INDEXED) return DA_ERR_INVALID_ARG;
+  if (p->layout == DA_KV_PAGED && p->page_size < 1) return DA_ERR_INVALID_ARG;
+  if (p->width < 0) return DA_ERR_INVALID_ARG;
+  if (p->layout != DA_KV_CONTIGUOUS && p->num_blocks < 0) return DA_ERR_INVALID_ARG;
+  if (!std::isfinite(p->scale)) return DA_ERR_INVALID_ARG;
+  if (p->flags != 0) return DA_ERR_INVALID_ARG;
+  if (p->shared_latent != 0 && p->shared_latent != 1) return DA_ERR_INVALID_ARG;
+  if (p->shared_latent && p->head_dim_v > p->head_dim_qk) return DA_ERR_INVALID_ARG;
+  if (row_capacity(p->layout, p->width, p->page_size) > 0x7fffffffLL) return DA_ERR_INVALID_ARG;
+  return DA_OK;
+}
+
+// The kernel variant follows from the head configuration alone -- never from
+// the batch size or the lengths.
+int select_variant(const da_problem* p, Variant* v) {
+  if (p->shared_latent) {
+    if (p->head_dim_qk == 576 && p->head_dim_v == 512 && p->num_kv_heads == 1 &&
+        mla_supported(p->num_q_heads)) {
+      *v = {DA_VARIANT_MLA, kMlaTile, kMlaMinTilesPerSplit, kMlaMaxSplits};
+      return DA_OK;
+    }
+    return DA_ERR_UNSUPPORTED;
+  }
+  const int G = p->num_q_heads / p->num_kv_heads;
+  if (p->head_dim_qk == p->head_dim_v && fma_supported(G, p->head_dim_qk)) {
+    *v = {DA_VARIANT_FMA, kFmaTile, kFmaMinTilesPerSplit, kFmaMaxSplits};
+    return DA_OK;
+  }
+  return DA_ERR_UNSUPPORTED;
+}
+
+bool layout_fits(const da_problem* p, int max_splits) {
+  // work-list entries b * max_splits + s must fit in int32
+  return (long long)p->batch * (max_splits + 1) < 0x7fffffffLL;
+}
+
+WsLayout ws_layout(const da_problem* p, int max_splits) {
+  const size_t B = (size_t)p->batch, ms = (size_t)max_splits;
+  const size_t Hq = (size_t)p->num_q_heads, Dv = (size_t)p->head_dim_v;
+  WsLayout L;
+  size_t off = kHdrBytes;
+  L.n_splits = off;
+  off = align256(off + 4 * B);
+  L.split_begin = off;
+  off = align256(off + 4 * B * (ms + 1));
+  L.work = off;
+  off = align256(off + 4 * B * ms);
+  L.lse_part = off;
+  off = align256(off + 4 * B * ms * Hq);
+  L.o_part = off;
+  off = align256(off + 4 * B * ms * Hq * Dv);
+  L.total = off;
+  return L;
+}
+
+int sm_count(int dev) {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 0 || dev >= 64) return 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+Launch make_launch(const da_plan* plan) {
+  const da_problem& pr = plan->prob;
+  uint8_t* ws = static_cast<uint8_t*>(plan->ws);
+  Launch L;
+  std::memset(&L, 0, sizeof(L));
+  L.hdr = reinterpret_cast<int32_t*>(ws);
+  L.n_splits = reinterpret_cast<const int32_t*>(ws + plan->off_n_splits);
+  L.split_begin = reinterpret_cast<const int32_t*>(ws + plan->off_split_begin);
+  L.work = reinterpret_cast<const int32_t*>(ws + plan->off_work);
+  L.lse_part = reinterpret_cast<float*>(ws + plan->off_lse_part);
+  L.o_part = reinterpret_cast<float*>(ws + plan->off_o_part);
+  L.num_blocks = pr.num_blocks;
+  L.B = pr.batch;
+  L.H_q = pr.num_q_heads;
+  L.H_kv = pr.num_kv_heads;
+  L.D_qk = pr.head_dim_qk;
+  L.D_v = pr.head_dim_v;
+  L.layout = pr.layout;
+  L.page_size = pr.page_size;
+  L.width = pr.width;
+  L.capacity = (int)row_capacity(pr.layout, pr.width, pr.page_size);
+  L.max_splits = plan->max_splits;
+  L.scale_log2 = pr.scale * kLog2e;
+  return L;
+}
+
+int check_plan(const da_plan* plan) {
+  if (!plan) return DA_ERR_INVALID_ARG;
+  int rc = check_problem(&plan->prob);
+  if (rc != DA_OK) return rc;
+  Variant v;
+  rc = select_variant(&plan->prob, &v);
+  if (rc != DA_OK) return rc;
+  if (plan->variant != v.id || plan->max_splits != v.max_splits) return DA_ERR_INVALID_ARG;
+  if (plan->prob.batch > 0) {
+    if (!plan->ws || !aligned(plan->ws, 256)) return DA_ERR_WORKSPACE;
+    if (plan->ws_bytes < ws_layout(&plan->prob, v.max_splits).total) return DA_ERR_WORKSPACE;
+  }
+  return DA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* decode_attn_version(void) {
+  static char buf[256];
+  static std::once_flag once;
+  std::call_once(once, [] {
+    std::snprintf(buf, sizeof(buf),
+                  "decode_attn 0.1 sm_103a; fma: tile=%d min_tiles=%d max_splits=%d; "
+                  "mla: tile=%d min_tiles=%d max_splits=%d; balanced fixed_overhead=%d",
+                  kFmaTile, kFmaMinTilesPerSplit, kFmaMaxSplits, kMlaTile, kMlaMinTilesPerSplit,
+                  kMlaMaxSplits, kBalancedFixedOverhead);
+  });
+  return buf;
+}
+
+const char* decode_attn_status_string(int status) {
+  switch (status) {
+    case DA_OK: return "ok";
+    case DA_ERR_INVALID_ARG: return "invalid argument";
+    case DA_ERR_UNSUPPORTED: return "unsupported head configuration";
+    case DA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case DA_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+int decode_attn_split_constants(const da_problem* prob, int32_t* variant, int32_t* tile_tokens,
+                                int32_t* min_tiles_per_split, int32_t* max_splits) {
+  int rc = check_problem(prob);
+  if (rc != DA_OK) return rc;
+  Variant v;
+  rc = select_variant(prob, &v);
+  if (rc != DA_OK) return rc;
+  if (variant) *variant = v.id;
+  if (tile_tokens) *tile_tokens = v.tile;
+  if (min_tiles_per_split) *min_tiles_per_split = v.min_tps;
+  if (max_splits) *max_splits = v.max_splits;
+  return DA_OK;
+}
+
+int decode_attn_workspace_bytes(const da_problem* prob, size_t* bytes) {
+  int rc = check_problem(prob);
+  if (rc != DA_OK) return rc;
+  if (!bytes) return DA_ERR_INVALID_ARG;
+  Variant v;
+  rc = select_variant(prob, &v);
+  if (rc != DA_OK) return rc;
+  if (!layout_fits(prob, v.max_splits)) return DA_ERR_INVALID_ARG;
+  *bytes = ws_layout(prob, v.max_splits).total;
+  return DA_OK;
+}
+
+int decode_attn_plan(const da_problem* prob, int32_t policy, const int32_t* d_lengths,
+                     void* d_ws, size_t ws_bytes, da_plan* plan, void* stream) {
+  int rc = check_problem(prob);
+  if (rc != DA_OK) return rc;
+  if (!plan || (policy != DA_POLICY_INVARIANT && policy != DA_POLICY_BALANCED))
+    return DA_ERR_INVALID_ARG;
+  Variant v;
+  rc = select_variant(prob, &v);
+  if (rc != DA_OK) return rc;
+  if (!layout_fits(prob, v.max_splits)) return DA_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(prob, v.max_splits);
+  if (prob->batch > 0) {
+    if (!d_lengths) return DA_ERR_INVALID_ARG;
+    if (!d_ws || !aligned(d_ws, 256) || ws_bytes < L.total) return DA_ERR_WORKSPACE;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DA_ERR_CUDA;
+  const int sms = sm_count(dev);
+  if (sms <= 0) return DA_ERR_CUDA;
+  const int per_sm = (v.id == DA_VARIANT_MLA)
+                         ? mla_ctas_per_sm()
+                         : fma_ctas_per_sm(prob->num_q_heads / prob->num_kv_heads, prob->head_dim_qk);
+  // CTAs that one (row, split) item occupies: one per KV head (CUDA-core
+  // variant) or a pair splitting D_v (tensor-core variant).
+  const int per_item = (v.id == DA_VARIANT_MLA) ? 2 : prob->num_kv_heads;
+  const long long slots = (long long)sms * per_sm;
+  const long long max_units = (long long)prob->batch * v.max_splits * per_item;
+
+  da_plan P;
+  std::memset(&P, 0, sizeof(P));
+  P.prob = *prob;
+  P.policy = policy;
+  P.variant = v.id;
+  P.tile_tokens = v.tile;
+  P.min_tiles_per_split = v.min_tps;
+  P.max_splits = v.max_splits;
+  P.num_parts = (int)(slots / per_item > 0 ? slots / per_item : 1);
+  P.fixed_overhead = kBalancedFixedOverhead;
+  P.grid = (int)(max_units < slots ? (max_units > 0 ? max_units : 1) : slots);
+  P.device = dev;
+  P.ws = d_ws;
+  P.ws_bytes = ws_bytes;
+  P.off_n_splits = L.n_splits;
+  P.off_split_begin = L.split_begin;
+  P.off_work = L.work;
+  P.off_lse_part = L.lse_part;
+  P.off_o_part = L.o_part;
+  *plan = P;
+  if (prob->batch == 0) return DA_OK;
+
+  uint8_t* ws = static_cast<uint8_t*>(d_ws);
+  PlanLaunch pl;
+  pl.lengths = d_lengths;
+  pl.hdr = reinterpret_cast<int32_t*>(ws);
+  pl.n_splits = reinterpret_cast<int32_t*>(ws + L.n_splits);
+  pl.split_begin = reinterpret_cast<int32_t*>(ws + L.split_begin);
+  pl.work = reinterpret_cast<int32_t*>(ws + L.work);
+  pl.B = prob->batch;
+  pl.tile = v.tile;
+  pl.min_tps = v.min_tps;
+  pl.max_splits = v.max_splits;
+  pl.capacity = (int)row_capacity(prob->layout, prob->width, prob->page_size);
+  pl.policy = policy;
+  pl.num_parts = P.num_parts;
+  pl.fixed_overhead = P.fixed_overhead;
+  if (launch_plan(pl, static_cast<cudaStream_t>(stream)) != cudaSuccess) return DA_ERR_CUDA;
+  return DA_OK;
+}
+
+int decode_attn_run(const da_plan* plan, const void* q, const void* k, const void* v,
+                    const int32_t* table, const int32_t* lengths, void* out, float* lse,
+                    void* stream) {
+  int rc = check_plan(plan);
+  if (rc != DA_OK) return rc;
+  const da_problem& pr = plan->prob;
+  if (pr.batch == 0) return DA_OK;
+  if (!q || !k || !lengths || !out || !lse) return DA_ERR_INVALID_ARG;
+  if (!pr.shared_latent && !v) return DA_ERR_INVALID_ARG;
+  if (pr.layout != DA_KV_CONTIGUOUS && !table) return DA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || (v && !aligned(v, 16)) || !aligned(out, 16) ||
+      !aligned(lse, 4) || !aligned(lengths, 4) || (table && !aligned(table, 4)))
+    return DA_ERR_INVALID_ARG;
+  Launch L = make_launch(plan);
+  L.q = static_cast<const __nv_bfloat16*>(q);
+  L.k = static_cast<const __nv_bfloat16*>(k);
+  L.v = static_cast<const __nv_bfloat16*>(pr.shared_latent ? k : v);
+  L.table = table;
+  L.lengths = lengths;
+  L.out = static_cast<__nv_bfloat16*>(out);
+  L.lse = lse;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = (plan->variant == DA_VARIANT_MLA) ? launch_split_mla(L, plan->grid, s)
+                                                          : launch_split_fma(L, plan->grid, s);
+  return e == cudaSuccess ? DA_OK : DA_ERR_CUDA;
+}
+
+int decode_attn_combine(const da_plan* plan, void* out, float* lse, void* stream) {
+  int rc = check_plan(plan);
+  if (rc != DA_OK) return rc;
+  if (plan->prob.batch == 0) return DA_OK;
+  if (!out || !lse || !aligned(out, 16) || !aligned(lse, 4)) return DA_ERR_INVALID_ARG;
+  Launch L = make_launch(plan);
+  L.out = static_cast<__nv_bfloat16*>(out);
+  L.lse = lse;
+  return launch_combine(L, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DA_OK
+                                                                               : DA_ERR_CUDA;
+}
+
+int decode_attn_forward(const da_problem* prob, int32_t policy, const void* q, const void* k,
+                        const void* v, const int32_t* table, const int32_t* lengths,
+                        void* d_ws, size_t ws_bytes, void* out, float* lse, void* stream) {
+  da_plan plan;
+  int rc = decode_attn_plan(prob, policy, lengths, d_ws, ws_bytes, &plan, stream);
+  if (rc != DA_OK) return rc;
+  rc = decode_attn_run(&plan, q, k, v, table, lengths, out, lse, stream);
+  if (rc != DA_OK) return rc;
+  return decode_attn_combine(&plan, out, lse, stream);
+}
+
+int decode_attn_read_error(const da_plan* plan, int32_t* code, void* stream) {
+  if (!plan || !code) return DA_ERR_INVALID_ARG;
+  *code = 0;
+  if (plan->prob.batch == 0) return DA_OK;
+  if (!plan->ws) return DA_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(code, static_cast<const int32_t*>(plan->ws) + kHdrError, sizeof(int32_t),
+                      cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return DA_ERR_CUDA;
+  return cudaStreamSynchronize(s) == cudaSuccess ? DA_OK : DA_ERR_CUDA;
+}
+
+int decode_attn_copy_plan(const da_plan* plan, int32_t* n_splits, int32_t* split_begin,
+                          int32_t* n_work, int32_t* work, void* stream) {
+  if (!plan) return DA_ERR_INVALID_ARG;
+  const size_t B = (size_t)plan->prob.batch, ms = (size_t)plan->max_splits;
+  if (B == 0) {
+    if (n_work) *n_work = 0;
+    return DA_OK;
+  }
+  if (!plan->ws) return DA_ERR_WORKSPACE;
+  const uint8_t* ws = static_cast<const uint8_t*>(plan->ws);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (n_splits && e == cudaSuccess)
+    e = cudaMemcpyAsync(n_splits, ws + plan->off_n_splits, 4 * B, cudaMemcpyDeviceToHost, s);
+  if (split_begin && e == cudaSuccess)
+    e = cudaMemcpyAsync(split_begin, ws + plan->off_split_begin, 4 * B * (ms + 1),
+                        cudaMemcpyDeviceToHost, s);
+  if (n_work && e == cudaSuccess)
+    e = cudaMemcpyAsync(n_work, reinterpret_cast<const int32_t*>(ws) + kHdrNWork, 4,
+                        cudaMemcpyDeviceToHost, s);
+  if (work && e == cudaSuccess)
+    e = cudaMemcpyAsync(work, ws + plan->off_work, 4 * B * ms, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  return e == cudaSuccess ? DA_OK : DA_ERR_CUDA;
+}
+
+}  // extern "C"

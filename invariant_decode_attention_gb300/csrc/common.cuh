@@ -1,0 +1,211 @@
+// Shared device helpers and launch descriptors of the decode attention library.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "decode_attn.h"
+
+namespace da {
+
+// ---------------------------------------------------------------------------
+// Split constants.  They fix the bits of every output, so they are compile
+// time only (never derived from the batch or the GPU).  Per variant:
+// tokens per tile, minimum tiles per split, maximum splits per row.
+// ---------------------------------------------------------------------------
+constexpr int kFmaTile = 64;
+constexpr int kFmaMinTilesPerSplit = 8;
+constexpr int kFmaMaxSplits = 64;
+
+constexpr int kMlaTile = 64;
+constexpr int kMlaMinTilesPerSplit = 8;
+constexpr int kMlaMaxSplits = 32;
+
+// BALANCED quota: tiles charged per split on top of its own tiles.
+constexpr int kBalancedFixedOverhead = 2;
+
+// Header words at the start of the workspace.
+constexpr int kHdrError = 0;  // DA_DEVERR_* bits
+constexpr int kHdrNWork = 1;  // number of (row, split) work items
+constexpr size_t kHdrBytes = 256;
+
+// Longest a pipeline wait may spin before the kernel gives up (ns).
+constexpr unsigned long long kWaitLimitNs = 4000000000ull;
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Everything a split / combine kernel needs, by value.
+struct Launch {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  const int32_t* table;
+  const int32_t* lengths;
+  __nv_bfloat16* out;
+  float* lse;
+  int32_t* hdr;
+  const int32_t* n_splits;
+  const int32_t* split_begin;
+  const int32_t* work;
+  float* lse_part;
+  float* o_part;
+  long long num_blocks;
+  int B, H_q, H_kv, D_qk, D_v;
+  int layout, page_size, width, capacity;
+  int max_splits;
+  float scale_log2;  // softmax scale * log2(e)
+};
+
+struct PlanLaunch {
+  const int32_t* lengths;
+  int32_t* hdr;
+  int32_t* n_splits;
+  int32_t* split_begin;
+  int32_t* work;
+  int B, tile, min_tps, max_splits, capacity;
+  int policy, num_parts, fixed_overhead;
+};
+
+// Host launchers (each in its own translation unit).
+cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t stream);
+cudaError_t launch_split_fma(const Launch& p, int grid, cudaStream_t stream);
+cudaError_t launch_combine(const Launch& p, cudaStream_t stream);
+cudaError_t launch_split_mla(const Launch& p, int grid, cudaStream_t stream);
+// Persistent CTAs that fit on one SM for the variant's split kernel.
+int fma_ctas_per_sm(int G, int D);
+int mla_ctas_per_sm();
+bool fma_supported(int G, int D);
+
+// Capacity of a row (largest valid length) for a layout.
+inline long long row_capacity(int layout, int width, int page_size) {
+  if (layout == DA_KV_PAGED) return (long long)width * page_size;
+  return width;
+}
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+#ifdef __CUDACC__
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// bf16 pair (as one 32-bit word) -> two floats, exactly.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---- mbarrier -------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of `parity` to complete; false if the time limit ran out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// ---- bulk async copy global -> shared (TMA engine, non-tensor form) --------
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Barrier over `n` threads that also returns the OR of `pred` across them.
+__device__ __forceinline__ bool named_bar_or(int id, int n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void set_error(int32_t* hdr, int bits) {
+  atomicOr(reinterpret_cast<int*>(hdr + kHdrError), bits);
+}
+
+// A row's length after the same clamp the plan applies.
+__device__ __forceinline__ int clamp_len(int L, int capacity) {
+  return L < 0 ? 0 : (L > capacity ? capacity : L);
+}
+
+#endif  // __CUDACC__
+
+}  // namespace da

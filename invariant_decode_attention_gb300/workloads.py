@@ -221,3 +221,63 @@ def ragged_page_table(lengths, seed, page_size=16, width=None):
     """Shuffled page table for a ragged batch: (table[B, width], num_pages)."""
     g = torch.Generator().manual_seed(seed + 1)
     return page_table(lengths, page_size, g, width)
+
+
+class RaggedSweep:
+    """Batches of the ragged invariance sweep, assembled on a device.
+
+    All batches share one page pool whose content is random filler (drawn on
+    the device: batchmates are never compared with anything).  For each batch
+    the target row's q, K and V are written into its own freshly shuffled
+    pages, so the target attends over identical data at a different position,
+    with different page ids and different batchmates every time.
+    """
+
+    def __init__(self, sizes, device="cuda", seed=1003, page_size=16):
+        self.sizes = list(sizes)
+        self.page_size = page_size
+        self.device = device
+        self.q_t, self.k_t, self.v_t = ragged_target(seed)
+        self.batches = []
+        max_pages = 1
+        for B in self.sizes:
+            lens, pos = ragged_batch_lengths(B, seed=seed * 1000 + B)
+            table, num_pages = ragged_page_table(lens, seed=seed * 1000 + B,
+                                                 page_size=page_size,
+                                                 width=RAGGED_MAX_LEN // page_size)
+            self.batches.append((B, lens, pos, table))
+            max_pages = max(max_pages, num_pages)
+        self.num_pages = max_pages
+        g = torch.Generator(device=device).manual_seed(seed)
+        shape = (max_pages, page_size, 8, 128)
+        self.k_pool = torch.randn(shape, generator=g, device=device, dtype=torch.bfloat16)
+        self.v_pool = torch.randn(shape, generator=g, device=device, dtype=torch.bfloat16)
+        n_tp = RAGGED_TARGET_LEN // page_size
+        self._kt = self.k_t.view(n_tp, page_size, 8, 128).to(device)
+        self._vt = self.v_t.view(n_tp, page_size, 8, 128).to(device)
+        self._qt = self.q_t.to(device)
+
+    def solo(self):
+        """The target row alone, in its own 256 pages."""
+        n_tp = RAGGED_TARGET_LEN // self.page_size
+        table = torch.full((1, RAGGED_MAX_LEN // self.page_size), -1, dtype=torch.int32)
+        table[0, :n_tp] = torch.arange(n_tp, dtype=torch.int32)
+        return Workload("ragged_solo", PAGED, self._qt[None].contiguous(), self._kt.contiguous(),
+                        self._vt.contiguous(), torch.tensor([RAGGED_TARGET_LEN], dtype=torch.int32,
+                                                            device=self.device),
+                        table.to(self.device), self.page_size, 32, 8, 128, 128, 128 ** -0.5)
+
+    def batch(self, i):
+        """(Workload on the device, target position) of the i-th batch."""
+        B, lens, pos, table = self.batches[i]
+        n_tp = RAGGED_TARGET_LEN // self.page_size
+        pages = table[pos, :n_tp].to(device=self.device, dtype=torch.int64)
+        self.k_pool[pages] = self._kt
+        self.v_pool[pages] = self._vt
+        g = torch.Generator(device=self.device).manual_seed(7 * B + 1)
+        q = torch.randn((B, 32, 128), generator=g, device=self.device, dtype=torch.bfloat16)
+        q[pos] = self._qt
+        wl = Workload(f"ragged_b{B}", PAGED, q, self.k_pool, self.v_pool,
+                      torch.tensor(lens, dtype=torch.int32, device=self.device),
+                      table.to(self.device), self.page_size, 32, 8, 128, 128, 128 ** -0.5)
+        return wl, pos

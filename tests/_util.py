@@ -1,0 +1,60 @@
+"""Helpers shared by the tests: oracle evaluation on workload tensors and the
+parity tolerance.  No attention arithmetic lives here -- only marshalling."""
+
+import numpy as np
+import torch
+
+from oracle import attention as A
+from oracle import bf16 as OB
+
+# Parity bar (out): |gpu - oracle| <= max(1e-2, one bf16 ULP of the oracle
+# value).  A correctly rounded bf16 result is within half a ULP of the exact
+# value; for |o| < 4 that is <= 0.0078 < 1e-2, leaving >= 0.002 for fp32
+# accumulation error; for |o| >= 4 half a ULP alone exceeds 1e-2, so the bar
+# there is one ULP.  LSE (fp32, natural log): |gpu - oracle| <= 1e-4.
+OUT_ATOL = 1e-2
+LSE_ATOL = 1e-4
+
+
+class Bf16Cache:
+    """Read-only view of a bf16 torch cache that the oracle can index like a
+    numpy array; every read comes back as exact fp64."""
+
+    def __init__(self, t):
+        self.t = t
+        self.shape = tuple(t.shape)
+
+    def __getitem__(self, idx):
+        if not isinstance(idx, tuple):
+            idx = (idx,)
+        idx = tuple(torch.as_tensor(np.asarray(i)) if not isinstance(i, (int, slice)) else i
+                    for i in idx)
+        return self.t[idx].double().numpy()
+
+
+def oracle_for(wl, rows=None, heads=None):
+    """fp64 oracle (out, lse) of a CPU workload, optionally on a subset."""
+    table = None if wl.table is None else wl.table.numpy()
+    return A.attend(wl.q.double().numpy(), Bf16Cache(wl.k),
+                    None if wl.v is None else Bf16Cache(wl.v), wl.lengths.numpy(),
+                    scale=wl.scale, layout=wl.layout, table=table, page_size=wl.page_size,
+                    d_v=wl.D_v, rows=rows, heads=heads)
+
+
+def assert_parity(out_gpu, lse_gpu, ref_out, ref_lse, rows=None, heads=None):
+    """Element-wise parity of GPU (bf16 out, fp32 lse) against the oracle."""
+    o = out_gpu.double().cpu().numpy()
+    l = lse_gpu.double().cpu().numpy()
+    rows = range(o.shape[0]) if rows is None else rows
+    heads = range(o.shape[1]) if heads is None else heads
+    ri = np.ix_(list(rows), list(heads))
+    o, l, ro, rl = o[ri], l[ri], ref_out[ri], ref_lse[ri]
+    tol = np.maximum(OUT_ATOL, OB.ulp(ro))
+    err = np.abs(o - ro)
+    bad = ~(err <= tol)
+    assert not bad.any(), (f"out mismatch at {np.argwhere(bad)[:5].tolist()}: "
+                           f"max err {np.nanmax(err):.4g}")
+    both_inf = np.isneginf(l) & np.isneginf(rl)
+    lerr = np.where(both_inf, 0.0, np.abs(l - rl))
+    assert np.all(lerr <= LSE_ATOL), f"lse max err {np.nanmax(lerr):.4g}"
+    return float(np.max(err)) if err.size else 0.0, float(np.max(lerr)) if lerr.size else 0.0

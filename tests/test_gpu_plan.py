@@ -1,0 +1,61 @@
+"""The device split plans are bit-exact against the oracle's plans."""
+
+import random
+
+import pytest
+import torch
+
+from oracle import plan as OP
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def api():
+    from invariant_decode_attention_gb300 import api as _api
+    _api.lib()
+    return _api
+
+
+def _device_plan(api, lengths, policy, capacity):
+    prob = api.problem(batch=len(lengths), num_q_heads=1, num_kv_heads=1, head_dim_qk=64,
+                       layout="indexed", scale=1.0, width=capacity, num_blocks=1)
+    ws = api.workspace(prob)
+    d_len = torch.tensor(lengths, dtype=torch.int32, device="cuda")
+    pl = api.plan(prob, policy, d_len, ws)
+    n_splits, split_begin, work = api.copy_plan(pl)
+    bounds = [split_begin[b, :int(n_splits[b]) + 1].tolist() for b in range(len(lengths))]
+    return pl, bounds, work.tolist()
+
+
+@pytest.mark.parametrize("start", range(0, 131073, 16384))
+def test_invariant_plan_all_lengths_up_to_131072(api, start):
+    lengths = list(range(start, min(start + 16384, 131073)))
+    T, mn, mx = OP.VARIANT_CONSTANTS["fma"]
+    pl, bounds, work = _device_plan(api, lengths, api.INVARIANT, 131072)
+    want = OP.plan_invariant(lengths, T, mn, mx)
+    assert bounds == want
+    assert work == OP.work_list(want, mx)
+
+
+def test_invariant_and_balanced_random_batches(api):
+    rng = random.Random(5)
+    T, mn, mx = OP.VARIANT_CONSTANTS["fma"]
+    for trial in range(20):
+        B = rng.randint(1, 300)
+        lengths = [rng.choice([0, 1, rng.randint(1, 131072), int(2 ** (17 * rng.random()))])
+                   for _ in range(B)]
+        pl, bounds, work = _device_plan(api, lengths, api.INVARIANT, 131072)
+        want = OP.plan_invariant(lengths, T, mn, mx)
+        assert bounds == want and work == OP.work_list(want, mx)
+        pl, bounds, work = _device_plan(api, lengths, api.BALANCED, 131072)
+        want = OP.plan_balanced(lengths, T, mx, pl.num_parts, pl.fixed_overhead)
+        assert pl.fixed_overhead == OP.BALANCED_FIXED_OVERHEAD
+        assert bounds == want and work == OP.work_list(want, mx)
+
+
+def test_lengths_are_clamped_like_the_oracle_reads_them(api):
+    T, mn, mx = OP.VARIANT_CONSTANTS["fma"]
+    pl, bounds, _ = _device_plan(api, [-5, 100, 10 ** 7], api.INVARIANT, 5000)
+    assert bounds == OP.plan_invariant([0, 100, 5000], T, mn, mx)
+    assert api.read_error(pl) & api.DEVERR_LENGTH
