@@ -116,6 +116,9 @@ typedef struct da_plan {
   uint64_t off_n_splits;       /* int32[B]: splits of row b                    */
   uint64_t off_split_begin;    /* int32[B][max_splits+1]: boundaries, tiles    */
   uint64_t off_work;           /* int32[B*max_splits]: b*max_splits + s list   */
+  uint64_t off_item_desc;      /* int32[B*max_splits][4]: per work item        */
+                               /* {slot (~slot if the row has one split),      */
+                               /*  first tile, end tile, clamped length}       */
   uint64_t off_lse_part;       /* float[B*max_splits][H_q]: split LSE (log2)   */
   uint64_t off_o_part;         /* float[B*max_splits][H_q][D_v]: split output  */
 } da_plan;

@@ -68,6 +68,7 @@ class DaPlan(ctypes.Structure):
         ("off_n_splits", ctypes.c_uint64),
         ("off_split_begin", ctypes.c_uint64),
         ("off_work", ctypes.c_uint64),
+        ("off_item_desc", ctypes.c_uint64),
         ("off_lse_part", ctypes.c_uint64),
         ("off_o_part", ctypes.c_uint64),
     ]

@@ -21,7 +21,7 @@ struct Variant {
 };
 
 struct WsLayout {
-  size_t n_splits, split_begin, work, lse_part, o_part, total;
+  size_t n_splits, split_begin, work, item_desc, lse_part, o_part, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -78,6 +78,8 @@ WsLayout ws_layout(const da_problem* p, int max_splits) {
   off = align256(off + 4 * B * (ms + 1));
   L.work = off;
   off = align256(off + 4 * B * ms);
+  L.item_desc = off;
+  off = align256(off + 16 * B * ms);
   L.lse_part = off;
   off = align256(off + 4 * B * ms * Hq);
   L.o_part = off;
@@ -110,6 +112,7 @@ Launch make_launch(const da_plan* plan) {
   L.n_splits = reinterpret_cast<const int32_t*>(ws + plan->off_n_splits);
   L.split_begin = reinterpret_cast<const int32_t*>(ws + plan->off_split_begin);
   L.work = reinterpret_cast<const int32_t*>(ws + plan->off_work);
+  L.item_desc = reinterpret_cast<const int32_t*>(ws + plan->off_item_desc);
   L.lse_part = reinterpret_cast<float*>(ws + plan->off_lse_part);
   L.o_part = reinterpret_cast<float*>(ws + plan->off_o_part);
   L.num_blocks = pr.num_blocks;
@@ -241,6 +244,7 @@ int decode_attn_plan(const da_problem* prob, int32_t policy, const int32_t* d_le
   P.off_n_splits = L.n_splits;
   P.off_split_begin = L.split_begin;
   P.off_work = L.work;
+  P.off_item_desc = L.item_desc;
   P.off_lse_part = L.lse_part;
   P.off_o_part = L.o_part;
   *plan = P;
@@ -253,6 +257,7 @@ int decode_attn_plan(const da_problem* prob, int32_t policy, const int32_t* d_le
   pl.n_splits = reinterpret_cast<int32_t*>(ws + L.n_splits);
   pl.split_begin = reinterpret_cast<int32_t*>(ws + L.split_begin);
   pl.work = reinterpret_cast<int32_t*>(ws + L.work);
+  pl.item_desc = reinterpret_cast<int32_t*>(ws + L.item_desc);
   pl.B = prob->batch;
   pl.tile = v.tile;
   pl.min_tps = v.min_tps;

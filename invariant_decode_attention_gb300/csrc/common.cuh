@@ -49,6 +49,7 @@ struct Launch {
   const int32_t* n_splits;
   const int32_t* split_begin;
   const int32_t* work;
+  const int32_t* item_desc;  // int4 per work item: {slot or ~slot if single, tb, te, L}
   float* lse_part;
   float* o_part;
   long long num_blocks;
@@ -64,6 +65,7 @@ struct PlanLaunch {
   int32_t* n_splits;
   int32_t* split_begin;
   int32_t* work;
+  int32_t* item_desc;
   int B, tile, min_tps, max_splits, capacity;
   int policy, num_parts, fixed_overhead;
 };
@@ -154,6 +156,21 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
+}
+
+// ---- cp.async (16 bytes, L2 only) ------------------------------------------
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Wait until at most N of this thread's committed groups are still pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // ---- bulk async copy global -> shared (TMA engine, non-tensor form) --------

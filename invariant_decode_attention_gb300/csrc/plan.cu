@@ -74,7 +74,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_invariant_kernel(PlanLaunch
     }
     int total;
     const int off = block_exclusive_scan(n, &total);
-    for (int s = 0; s < n; ++s) p.work[work_base + off + s] = b * p.max_splits + s;
+    const int Lc = (b < p.B) ? clamp_len(p.lengths[b], p.capacity) : 0;
+    for (int s = 0; s < n; ++s) {
+      const int slot = b * p.max_splits + s;
+      p.work[work_base + off + s] = slot;
+      reinterpret_cast<int4*>(p.item_desc)[work_base + off + s] =
+          make_int4(n == 1 ? ~slot : slot, min(s * tps, n_tiles), min((s + 1) * tps, n_tiles), Lc);
+    }
     work_base += total;
   }
   if (threadIdx.x == 0) p.hdr[kHdrNWork] = work_base;
@@ -119,7 +125,13 @@ __global__ void plan_balanced_kernel(PlanLaunch p) {
     }
     sb[n_cuts] = n_tiles;
     p.n_splits[b] = n_cuts;
-    for (int s = 0; s < n_cuts; ++s) p.work[n_work++] = b * p.max_splits + s;
+    const int Lc = clamp_len(p.lengths[b], p.capacity);
+    for (int s = 0; s < n_cuts; ++s) {
+      const int slot = b * p.max_splits + s;
+      reinterpret_cast<int4*>(p.item_desc)[n_work] =
+          make_int4(n_cuts == 1 ? ~slot : slot, sb[s], sb[s + 1], Lc);
+      p.work[n_work++] = slot;
+    }
   }
   p.hdr[kHdrNWork] = n_work;
 }

@@ -7,22 +7,18 @@
 // the combine merges.  Work placement is persistent: CTA c takes units c,
 // c + grid, ...; which CTA runs a unit never changes what the unit computes.
 //
-// Inside a CTA (warp-specialised):
-//   * one producer warp streams each tile's K and V rows (and the query group
-//     at a unit's first tile) into a ring of shared-memory stages with bulk
-//     asynchronous copies (TMA engine), completing on an mbarrier per stage.
-//     Per-row copies serve all three cache layouts: a row of one KV head is
-//     D_qk*2 contiguous bytes in each of them.
-//   * four consumer warps each own 16 of a tile's 64 entries.  Eight lanes
-//     share an entry (16-byte chunks of the row each), so a score is an
-//     8-lane butterfly reduction, and a lane keeps fp32 accumulators for the
-//     G heads over its own dims.  Online softmax runs in the log2 domain with
-//     a warp-uniform running max.
-//   * at the end of a unit the lane groups and warps merge in a fixed order.
-// Every reduction has a fixed shape and order, so a unit's bits depend only
-// on its inputs and its split boundaries.
+// Inside a CTA, four warps share each unit.  Warp w owns entries
+// [16w, 16w + 16) of every 64-entry tile and streams exactly those K and V
+// rows with 16-byte cp.async into its own three-slot shared-memory ring, so
+// a warp never waits for another warp inside the tile loop.  Eight lanes
+// share an entry (two 16-byte chunks of a 128-dim row each), so a score is an
+// 8-lane butterfly sum, and a lane keeps fp32 accumulators for the G heads
+// over its own dims.  Online softmax runs in the log2 domain with a
+// warp-uniform running max.  At the end of a unit the lane groups and then the
+// warps merge in a fixed order.  Every reduction has a fixed shape and order,
+// so a unit's bits depend only on its inputs and its split boundaries.
 //
-// Softmax attention and the split/merge are the computation the FlashMLA
+// Softmax attention and its split/merge are the computation the FlashMLA
 // issue #212 page ("Sparse MLA decode is not batch-invariant") reports on; the
 // kernel design here is this library's own.
 #include "common.cuh"
@@ -30,51 +26,53 @@
 namespace da {
 namespace {
 
-// Register cap: two 160-thread CTAs per SM.
-constexpr int kFmaMaxRegs = 200;
-
 template <int G, int D>
 struct FmaShape {
   static constexpr int kTile = kFmaTile;               // entries per tile
-  static constexpr int kWarps = 4;                      // consumer warps
-  static constexpr int kThreads = (kWarps + 1) * 32;    // + one producer warp
+  static constexpr int kWarps = 4;
+  static constexpr int kThreads = kWarps * 32;
   static constexpr int kTokPerWarp = kTile / kWarps;    // 16
   static constexpr int kSteps = kTokPerWarp / 4;        // 4 entries per warp step
   static constexpr int kChunks = D / 64;                // 16-byte chunks per lane per row
   static constexpr int kDpl = kChunks * 8;              // dims per lane
-  static constexpr int kStages = 3;
+  static constexpr int kStages = 3;                     // ring slots per warp
   static constexpr int kRowBytes = D * 2;
-  static constexpr int kKVBytes = kTile * kRowBytes;    // K (or V) bytes per stage
+  static constexpr int kSliceBytes = kTokPerWarp * kRowBytes;  // K (or V) of one warp
+  static constexpr int kWarpSlotBytes = 2 * kSliceBytes;
+  static constexpr int kRingBytes = kStages * kWarps * kWarpSlotBytes;
   static constexpr int kQBytes = G * D * 2;
   static constexpr int kQPad = (kQBytes + 127) / 128 * 128;
-  static constexpr int kStageBytes = 2 * kKVBytes + kQPad;
-  // Per (warp, head) merge record: D accumulators, then m and l; the row is
-  // padded to a multiple of 4 floats so float4 stores stay 16-byte aligned.
+  static constexpr int kQOffset = kRingBytes;
+  static constexpr int kScratchOffset = kQOffset + kStages * kQPad;
+  // Per (warp, head) merge record: D accumulators, then m and l; rows padded
+  // to a multiple of 4 floats so float4 stores stay 16-byte aligned.
   static constexpr int kSRow = D + 4;
   static constexpr int kScratchFloats = kWarps * G * kSRow;
-  static constexpr int kBarOffset = kStages * kStageBytes + kScratchFloats * 4;
-  static constexpr int kSmemBytes = kBarOffset + 2 * kStages * 8 + 16;
-  // Two CTAs per SM when the q + accumulator registers leave room for it.
-  static_assert(kFmaMaxRegs * kThreads * 2 <= 65536, "two CTAs per SM");
+  static constexpr int kSmemBytes = kScratchOffset + kScratchFloats * 4;
+  static constexpr int kQChunks = kQBytes / 16;         // 16-byte chunks of a query group
   static_assert(D % 64 == 0, "head dim must be a multiple of 64");
-  static_assert(kTile == 64, "two entries per producer lane");
+  static_assert(kQChunks <= kThreads, "one q chunk per thread at most");
 };
 
+// A work unit as the kernel sees it: the plan's item descriptor plus a head.
 struct Unit {
-  int b, h, slot, L, tb, te;
+  int slot, tb, te, L, b, h;
+  bool single;
 };
 
-__device__ __forceinline__ Unit decode_unit(const Launch& p, int u) {
+__device__ __forceinline__ int4 load_desc(const Launch& p, int u) {
+  return __ldg(reinterpret_cast<const int4*>(p.item_desc) + u / p.H_kv);
+}
+
+__device__ __forceinline__ Unit make_unit(const Launch& p, int u, int4 d) {
   Unit x;
-  const int item = u / p.H_kv;
-  x.h = u - item * p.H_kv;
-  x.slot = p.work[item];
+  x.single = d.x < 0;
+  x.slot = x.single ? ~d.x : d.x;
+  x.tb = d.y;
+  x.te = d.z;
+  x.L = d.w;
   x.b = x.slot / p.max_splits;
-  const int s = x.slot - x.b * p.max_splits;
-  x.L = clamp_len(p.lengths[x.b], p.capacity);
-  const int32_t* sb = p.split_begin + (size_t)x.b * (p.max_splits + 1);
-  x.tb = sb[s];
-  x.te = sb[s + 1];
+  x.h = u % p.H_kv;
   return x;
 }
 
@@ -94,124 +92,112 @@ __device__ __forceinline__ bool entry_row(const Launch& p, int b, int tok, long 
   return slot >= 0 && slot < p.num_blocks;
 }
 
-// Wait that also gives up when another warp has raised the abort flag.
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
-                                              volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+// Position of the prefetch stream: a (unit, tile) pair, units with no tiles
+// skipped.  The descriptor of the next unit is loaded one unit ahead.
+struct Cursor {
+  Unit x;
+  int u, k;
+  int4 next;
+  bool valid;
+};
+
+__device__ __forceinline__ void cursor_seek(const Launch& p, Cursor& c, int u, int4 d,
+                                            int n_units) {
+  for (;;) {
+    if (u >= n_units) {
+      c.valid = false;
+      return;
     }
+    const int un = u + gridDim.x;
+    c.next = (un < n_units) ? load_desc(p, un) : make_int4(0, 0, 0, 0);
+    if (d.z > d.y) break;
+    u = un;
+    d = c.next;
   }
+  c.u = u;
+  c.x = make_unit(p, u, d);
+  c.k = c.x.tb;
+  c.valid = true;
 }
 
+__device__ __forceinline__ void cursor_next(const Launch& p, Cursor& c, int n_units) {
+  if (!c.valid) return;
+  if (++c.k < c.x.te) return;
+  cursor_seek(p, c, c.u + gridDim.x, c.next, n_units);
+}
+
+// Issue this warp's copies for the cursor's tile into ring slot `slot`, then
+// close the cp.async group (always, so group counting stays uniform).
 template <int G, int D>
-__device__ void producer(const Launch& p, uint8_t* stages, uint64_t* full, uint64_t* empty,
-                         volatile int* abort_flag, int n_units) {
+__device__ __forceinline__ void load_slice(const Launch& p, const Cursor& c, uint8_t* smem,
+                                           int slot, int warp, int lane) {
   using S = FmaShape<G, D>;
-  const int lane = threadIdx.x & 31;
-  const uint64_t pol_kv = policy_evict_first();
-  int stage = 0;
-  uint32_t phase = 0;
-  int issued = 0;
-  bool ok = true;
-  for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-    const Unit x = decode_unit(p, u);
-    for (int k = x.tb; k < x.te; ++k) {
-      if (!wait_or_abort(smem_addr(&empty[stage]), phase ^ 1, abort_flag)) {
-        if (lane == 0) {
-          set_error(p.hdr, DA_DEVERR_TIMEOUT);
-          *abort_flag = 1;
-        }
-        ok = false;
-        break;
-      }
-      const int t0 = k * S::kTile;
-      const int n_valid = min(S::kTile, x.L - t0);
-      long long off[2];
-      bool go[2], bad = false;
+  if (c.valid) {
+    const int grp = lane >> 3, sub = lane & 7;
+    uint8_t* ks = smem + (slot * S::kWarps + warp) * S::kWarpSlotBytes;
+    uint8_t* vs = ks + S::kSliceBytes;
+    const int t0 = c.k * S::kTile + warp * S::kTokPerWarp;
+    bool bad = false;
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int t = lane + 32 * i;
-        go[i] = false;
-        off[i] = 0;
-        if (t < n_valid) {
-          long long row;
-          go[i] = entry_row(p, x.b, t0 + t, &row);
-          bad |= !go[i];
-          off[i] = (row * p.H_kv + x.h) * D;
-        }
-      }
-      const unsigned m0 = __ballot_sync(0xffffffffu, go[0]);
-      const unsigned m1 = __ballot_sync(0xffffffffu, go[1]);
-      if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(p.hdr, DA_DEVERR_INDEX);
-      const bool first = (k == x.tb);
-      const uint32_t bytes =
-          (uint32_t)(__popc(m0) + __popc(m1)) * 2u * S::kRowBytes + (first ? S::kQBytes : 0u);
-      const uint32_t bar = smem_addr(&full[stage]);
-      if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
-      __syncwarp();
-      uint8_t* st = stages + (size_t)stage * S::kStageBytes;
+    for (int j = 0; j < S::kSteps; ++j) {
+      const int tl = 4 * j + grp;
+      const int tok = t0 + tl;
+      if (tok < c.x.L) {
+        long long row;
+        const bool ok = entry_row(p, c.x.b, tok, &row);
+        bad |= !ok;
+        if (ok) {
+          const size_t off = ((size_t)row * p.H_kv + c.x.h) * D;
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        if (go[i]) {
-          const int t = lane + 32 * i;
-          bulk_g2s(smem_addr(st + t * S::kRowBytes), p.k + off[i], S::kRowBytes, bar, pol_kv);
-          bulk_g2s(smem_addr(st + S::kKVBytes + t * S::kRowBytes), p.v + off[i], S::kRowBytes,
-                   bar, pol_kv);
+          for (int ch = 0; ch < S::kChunks; ++ch) {
+            const int e = (sub + 8 * ch) * 8;  // element offset of this 16-byte chunk
+            cp_async16(smem_addr(ks + tl * S::kRowBytes + e * 2), p.k + off + e);
+            cp_async16(smem_addr(vs + tl * S::kRowBytes + e * 2), p.v + off + e);
+          }
         }
       }
-      if (first && lane == 0) {
-        const __nv_bfloat16* qsrc = p.q + ((size_t)x.b * p.H_q + (size_t)x.h * G) * D;
-        bulk_g2s(smem_addr(st + 2 * S::kKVBytes), qsrc, S::kQBytes, bar, pol_kv);
-      }
-      ++issued;
-      if (++stage == S::kStages) {
-        stage = 0;
-        phase ^= 1;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(p.hdr, DA_DEVERR_INDEX);
+    if (c.k == c.x.tb) {
+      // the unit's query group: one 16-byte chunk per thread of the CTA
+      const int id = warp * 32 + lane;
+      if (id < S::kQChunks) {
+        const __nv_bfloat16* q = p.q + ((size_t)c.x.b * p.H_q + (size_t)c.x.h * G) * D;
+        cp_async16(smem_addr(smem + S::kQOffset + slot * S::kQPad + id * 16), q + id * 8);
       }
     }
   }
-  // Do not leave while copies this warp issued may still be landing: wait
-  // (bounded) for the fills of the last stages it used.
-  const int pending = min(issued, S::kStages);
-  for (int i = 0; i < pending; ++i) {
-    if (--stage < 0) {
-      stage = S::kStages - 1;
-      phase ^= 1;
-    }
-    mbar_wait(smem_addr(&full[stage]), phase);
+  cp_async_commit();
+}
+
+template <int D>
+__device__ __forceinline__ void unpack_row(const uint8_t* row, int sub, float* f) {
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) {
+    const uint4 w = reinterpret_cast<const uint4*>(row)[sub + 8 * c];
+    f[c * 8 + 0] = bf16_lo(w.x); f[c * 8 + 1] = bf16_hi(w.x);
+    f[c * 8 + 2] = bf16_lo(w.y); f[c * 8 + 3] = bf16_hi(w.y);
+    f[c * 8 + 4] = bf16_lo(w.z); f[c * 8 + 5] = bf16_hi(w.z);
+    f[c * 8 + 6] = bf16_lo(w.w); f[c * 8 + 7] = bf16_hi(w.w);
   }
 }
 
+// One warp's 16 entries of one tile: scores, online-softmax update, P.V.
 template <int G, int D, bool kPartial>
-__device__ __forceinline__ void consume_tile(const uint8_t* st, int warp, int lane, int n_valid,
-                                             const float (&qf)[G][FmaShape<G, D>::kDpl],
-                                             float (&m)[G], float (&l)[G],
-                                             float (&acc)[G][FmaShape<G, D>::kDpl],
-                                             float scale_log2) {
+__device__ __forceinline__ void consume_slice(const uint8_t* ks, int lane, int n_valid,
+                                              const float (&qf)[G][FmaShape<G, D>::kDpl],
+                                              float (&m)[G], float (&l)[G],
+                                              float (&acc)[G][FmaShape<G, D>::kDpl],
+                                              float scale_log2) {
   using S = FmaShape<G, D>;
   const int grp = lane >> 3, sub = lane & 7;
-  const uint8_t* sK = st;
-  const uint8_t* sV = st + S::kKVBytes;
+  const uint8_t* vs = ks + S::kSliceBytes;
 
   float s[S::kSteps][G];
 #pragma unroll
   for (int j = 0; j < S::kSteps; ++j) {
-    const int t = warp * S::kTokPerWarp + j * 4 + grp;
-    const uint4* kr = reinterpret_cast<const uint4*>(sK + t * S::kRowBytes);
     float kf[S::kDpl];
-#pragma unroll
-    for (int c = 0; c < S::kChunks; ++c) {
-      const uint4 w = kr[sub + 8 * c];
-      kf[c * 8 + 0] = bf16_lo(w.x); kf[c * 8 + 1] = bf16_hi(w.x);
-      kf[c * 8 + 2] = bf16_lo(w.y); kf[c * 8 + 3] = bf16_hi(w.y);
-      kf[c * 8 + 4] = bf16_lo(w.z); kf[c * 8 + 5] = bf16_hi(w.z);
-      kf[c * 8 + 6] = bf16_lo(w.w); kf[c * 8 + 7] = bf16_hi(w.w);
-    }
+    unpack_row<D>(ks + (4 * j + grp) * S::kRowBytes, sub, kf);
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       float a = 0.f;
@@ -230,7 +216,7 @@ __device__ __forceinline__ void consume_tile(const uint8_t* st, int warp, int la
   }
 #pragma unroll
   for (int j = 0; j < S::kSteps; ++j) {
-    const bool valid = !kPartial || (warp * S::kTokPerWarp + j * 4 + grp) < n_valid;
+    const bool valid = !kPartial || (4 * j + grp) < n_valid;
 #pragma unroll
     for (int h = 0; h < G; ++h) s[j][h] = valid ? s[j][h] * scale_log2 : -INFINITY;
   }
@@ -268,18 +254,9 @@ __device__ __forceinline__ void consume_tile(const uint8_t* st, int warp, int la
   }
 #pragma unroll
   for (int j = 0; j < S::kSteps; ++j) {
-    const int t = warp * S::kTokPerWarp + j * 4 + grp;
-    if (kPartial && t >= n_valid) continue;  // stale shared memory: never touch it
-    const uint4* vr = reinterpret_cast<const uint4*>(sV + t * S::kRowBytes);
+    if (kPartial && (4 * j + grp) >= n_valid) continue;  // never read unfilled rows
     float vf[S::kDpl];
-#pragma unroll
-    for (int c = 0; c < S::kChunks; ++c) {
-      const uint4 w = vr[sub + 8 * c];
-      vf[c * 8 + 0] = bf16_lo(w.x); vf[c * 8 + 1] = bf16_hi(w.x);
-      vf[c * 8 + 2] = bf16_lo(w.y); vf[c * 8 + 3] = bf16_hi(w.y);
-      vf[c * 8 + 4] = bf16_lo(w.z); vf[c * 8 + 5] = bf16_hi(w.z);
-      vf[c * 8 + 6] = bf16_lo(w.w); vf[c * 8 + 7] = bf16_hi(w.w);
-    }
+    unpack_row<D>(vs + (4 * j + grp) * S::kRowBytes, sub, vf);
 #pragma unroll
     for (int h = 0; h < G; ++h)
 #pragma unroll
@@ -288,16 +265,30 @@ __device__ __forceinline__ void consume_tile(const uint8_t* st, int warp, int la
 }
 
 template <int G, int D>
-__device__ void consumer(const Launch& p, uint8_t* stages, float* scratch, uint64_t* full,
-                         uint64_t* empty, volatile int* abort_flag, int n_units) {
+__global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Launch p) {
   using S = FmaShape<G, D>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  float* scratch = reinterpret_cast<float*>(smem + S::kScratchOffset);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = lane >> 3, sub = lane & 7;
-  int stage = 0;
-  uint32_t phase = 0;
+  const int n_units = p.hdr[kHdrNWork] * p.H_kv;
+  if ((int)blockIdx.x >= n_units) return;  // uniform across the CTA
+
+  // prologue: fill kStages - 1 slots
+  Cursor pf;
+  cursor_seek(p, pf, blockIdx.x, load_desc(p, blockIdx.x), n_units);
+#pragma unroll
+  for (int s = 0; s < S::kStages - 1; ++s) {
+    load_slice<G, D>(p, pf, smem, s, warp, lane);
+    cursor_next(p, pf, n_units);
+  }
+
+  int slot = 0;
   float qf[G][S::kDpl];
+  int4 d_next = load_desc(p, blockIdx.x);
   for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-    const Unit x = decode_unit(p, u);
+    const Unit x = make_unit(p, u, d_next);
+    if (u + (int)gridDim.x < n_units) d_next = load_desc(p, u + gridDim.x);
     float m[G], l[G], acc[G][S::kDpl];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
@@ -306,41 +297,28 @@ __device__ void consumer(const Launch& p, uint8_t* stages, float* scratch, uint6
 #pragma unroll
       for (int i = 0; i < S::kDpl; ++i) acc[h][i] = 0.f;
     }
-    bool alive = !*abort_flag;
-    for (int k = x.tb; k < x.te && alive; ++k) {
-      if (!wait_or_abort(smem_addr(&full[stage]), phase, abort_flag)) {
-        if (lane == 0) {
-          set_error(p.hdr, DA_DEVERR_TIMEOUT);
-          *abort_flag = 1;
-        }
-        alive = false;
-        break;
-      }
-      const uint8_t* st = stages + (size_t)stage * S::kStageBytes;
+    for (int k = x.tb; k < x.te; ++k) {
+      cp_async_wait<S::kStages - 2>();
       if (k == x.tb) {
-        const uint8_t* sq = st + 2 * S::kKVBytes;
+        // the query group was copied by threads of every warp: all four must
+        // have waited on their copies before anyone reads it, and all must
+        // have read it before any slot holding it can be refilled
+        named_bar_sync(1, S::kThreads);
+        const uint8_t* sq = smem + S::kQOffset + slot * S::kQPad;
 #pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-          for (int c = 0; c < S::kChunks; ++c) {
-            const uint4 w = reinterpret_cast<const uint4*>(sq + h * S::kRowBytes)[sub + 8 * c];
-            qf[h][c * 8 + 0] = bf16_lo(w.x); qf[h][c * 8 + 1] = bf16_hi(w.x);
-            qf[h][c * 8 + 2] = bf16_lo(w.y); qf[h][c * 8 + 3] = bf16_hi(w.y);
-            qf[h][c * 8 + 4] = bf16_lo(w.z); qf[h][c * 8 + 5] = bf16_hi(w.z);
-            qf[h][c * 8 + 6] = bf16_lo(w.w); qf[h][c * 8 + 7] = bf16_hi(w.w);
-          }
+        for (int h = 0; h < G; ++h) unpack_row<D>(sq + h * S::kRowBytes, sub, qf[h]);
+        named_bar_sync(1, S::kThreads);
       }
-      const int n_valid = min(S::kTile, x.L - k * S::kTile);
-      if (n_valid == S::kTile)
-        consume_tile<G, D, false>(st, warp, lane, n_valid, qf, m, l, acc, p.scale_log2);
+      // refill the slot consumed in the previous iteration
+      load_slice<G, D>(p, pf, smem, (slot + S::kStages - 1) % S::kStages, warp, lane);
+      cursor_next(p, pf, n_units);
+      const uint8_t* ks = smem + (slot * S::kWarps + warp) * S::kWarpSlotBytes;
+      const int n_valid = min(S::kTokPerWarp, x.L - k * S::kTile - warp * S::kTokPerWarp);
+      if (n_valid >= S::kTokPerWarp)
+        consume_slice<G, D, false>(ks, lane, n_valid, qf, m, l, acc, p.scale_log2);
       else
-        consume_tile<G, D, true>(st, warp, lane, n_valid, qf, m, l, acc, p.scale_log2);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&empty[stage]));
-      if (++stage == S::kStages) {
-        stage = 0;
-        phase ^= 1;
-      }
+        consume_slice<G, D, true>(ks, lane, n_valid, qf, m, l, acc, p.scale_log2);
+      slot = (slot + 1 == S::kStages) ? 0 : slot + 1;
     }
 
     // ---- merge: lane groups (entries) within the warp, then warps ------------
@@ -370,8 +348,7 @@ __device__ void consumer(const Launch& p, uint8_t* stages, float* scratch, uint6
         }
       }
     }
-    named_bar_sync(1, S::kWarps * 32);
-    const bool single = p.n_splits[x.b] == 1;
+    named_bar_sync(1, S::kThreads);
     for (int h = warp; h < G; h += S::kWarps) {
       float M = -INFINITY;
 #pragma unroll
@@ -393,48 +370,21 @@ __device__ void consumer(const Launch& p, uint8_t* stages, float* scratch, uint6
 #pragma unroll
         for (int w = 0; w < S::kWarps; ++w) o = fmaf(scratch[(w * G + h) * S::kSRow + d], wgt[w], o);
         o = (lt > 0.f) ? o / lt : 0.f;
-        if (single)
+        if (x.single)
           p.out[((size_t)x.b * p.H_q + hq) * D + d] = __float2bfloat16_rn(o);
         else
           p.o_part[((size_t)x.slot * p.H_q + hq) * D + d] = o;
       }
       if (lane == 0) {
-        if (single)
+        if (x.single)
           p.lse[(size_t)x.b * p.H_q + hq] = (lt > 0.f) ? lse2 * kLn2 : -INFINITY;
         else
           p.lse_part[(size_t)x.slot * p.H_q + hq] = lse2;
       }
     }
-    // Leave together: the OR over all consumer threads of the abort flag is
-    // the same value in every warp, so no warp waits alone at a barrier.
-    if (named_bar_or(1, S::kWarps * 32, *abort_flag != 0)) return;
+    named_bar_sync(1, S::kThreads);
   }
-}
-
-template <int G, int D>
-__global__ void __maxnreg__(kFmaMaxRegs)
-    split_fma_kernel(Launch p) {
-  using S = FmaShape<G, D>;
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* stages = smem;
-  float* scratch = reinterpret_cast<float*>(smem + S::kStages * S::kStageBytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBarOffset);
-  uint64_t* empty = full + S::kStages;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + S::kStages);
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S::kStages; ++s) {
-      mbar_init(smem_addr(&full[s]), 1);
-      mbar_init(smem_addr(&empty[s]), S::kWarps);
-    }
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-  const int n_units = p.hdr[kHdrNWork] * p.H_kv;
-  if ((threadIdx.x >> 5) == S::kWarps)
-    producer<G, D>(p, stages, full, empty, abort_flag, n_units);
-  else
-    consumer<G, D>(p, stages, scratch, full, empty, abort_flag, n_units);
+  cp_async_wait<0>();  // leave no copy in flight
 }
 
 template <int G, int D>
