@@ -175,6 +175,31 @@ int decode_attn_forward(const da_problem* prob, int32_t policy, const void* q, c
                         const void* v, const int32_t* table, const int32_t* lengths,
                         void* d_ws, size_t ws_bytes, void* out, float* lse, void* stream);
 
+/* The forward pass without a caller-supplied workspace, for callers that
+ * cannot allocate device memory (for example a plugin whose host process owns
+ * every device allocation, or a latency-critical path that cannot afford the
+ * synchronisation a cudaMalloc may bring).  The pages have no counterpart to
+ * this entry point; it only changes where the scratch lives.
+ *
+ * Same arguments and results as decode_attn_forward minus the workspace.
+ * The scratch is one file-scope device array of DA_STATIC_WORKSPACE_BYTES
+ * (64 MiB) per device, held until the process exits from the time the
+ * library's code is loaded on that device.  The first call on a device looks
+ * up the array's device address (cudaGetSymbolAddress, with that device
+ * current); make that first call before any stream capture.  Nothing is
+ * allocated, here or later.  A problem whose workspace
+ * (decode_attn_workspace_bytes) exceeds DA_STATIC_WORKSPACE_BYTES is
+ * rejected with DA_ERR_WORKSPACE before anything is enqueued.  All calls on a
+ * device share the one array and it keeps the last call's contents (the plan
+ * rewrites everything a call reads, including the error word), so calls whose
+ * work overlaps on the GPU -- different streams without ordering, or
+ * concurrent host threads -- race and corrupt each other's results:
+ * serialise them. */
+#define DA_STATIC_WORKSPACE_BYTES (64u << 20)
+int decode_attn_forward_static(const da_problem* prob, int32_t policy, const void* q,
+                               const void* k, const void* v, const int32_t* table,
+                               const int32_t* lengths, void* out, float* lse, void* stream);
+
 /* Synchronise `stream`, then read the device error word (DA_DEVERR_* bits)
  * written since the last decode_attn_plan on this workspace. */
 int decode_attn_read_error(const da_plan* plan, int32_t* code, void* stream);

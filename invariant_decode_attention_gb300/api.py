@@ -29,8 +29,11 @@ EXPORTS = (
     "decode_attn_version", "decode_attn_status_string", "decode_attn_split_constants",
     "decode_attn_workspace_bytes", "decode_attn_plan", "decode_attn_run",
     "decode_attn_combine", "decode_attn_forward", "decode_attn_read_error",
-    "decode_attn_copy_plan",
+    "decode_attn_copy_plan", "decode_attn_forward_static",
 )
+
+# Size of the fixed device array decode_attn_forward_static uses as scratch.
+STATIC_WORKSPACE_BYTES = 64 << 20
 
 
 class DaProblem(ctypes.Structure):
@@ -112,6 +115,8 @@ def lib():
     L.decode_attn_forward.argtypes = [P(DaProblem), i32, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
     L.decode_attn_read_error.restype = ctypes.c_int
     L.decode_attn_read_error.argtypes = [P(DaPlan), P(i32), vp]
+    L.decode_attn_forward_static.restype = ctypes.c_int
+    L.decode_attn_forward_static.argtypes = [P(DaProblem), i32, vp, vp, vp, vp, vp, vp, vp, vp]
     L.decode_attn_copy_plan.restype = ctypes.c_int
     L.decode_attn_copy_plan.argtypes = [P(DaPlan), vp, vp, P(i32), vp, vp]
     _LIB = L
@@ -225,6 +230,23 @@ def forward(prob: DaProblem, policy, q, k, v, table, lengths, ws, out, lse, stre
                                      _dev_ptr(out, "out", torch.bfloat16),
                                      _dev_ptr(lse, "lse", torch.float32), _stream(stream)),
            "forward")
+
+
+def forward_static(prob: DaProblem, policy, q, k, v, table, lengths, out, lse, stream=None):
+    """The forward pass with the library's own fixed device scratch array, for
+    callers that cannot allocate device memory (see the header): no workspace
+    argument, nothing allocated.  Raises DecodeAttnError(ERR_WORKSPACE) for a
+    problem whose workspace exceeds STATIC_WORKSPACE_BYTES.  Calls sharing a
+    device must not overlap on the GPU."""
+    _check(lib().decode_attn_forward_static(ctypes.byref(prob), policy,
+                                            _dev_ptr(q, "q", torch.bfloat16),
+                                            _dev_ptr(k, "k", torch.bfloat16),
+                                            _dev_ptr(v, "v", torch.bfloat16),
+                                            _dev_ptr(table, "table", torch.int32),
+                                            _dev_ptr(lengths, "lengths", torch.int32),
+                                            _dev_ptr(out, "out", torch.bfloat16),
+                                            _dev_ptr(lse, "lse", torch.float32), _stream(stream)),
+           "forward_static")
 
 
 def read_error(pl: DaPlan, stream=None) -> int:
