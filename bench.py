@@ -54,6 +54,14 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def tensor_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"])
+    return 1900.0
+
+
 def source_hash(kernel):
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES[kernel]:
@@ -148,6 +156,8 @@ def build_workload(name, rank=0):
         return W.long_context(seed=1004 + seed_shift)
     if name == "tiny":
         return W.tiny(seed=1000 + seed_shift)
+    if name == "mla_sparse":
+        return W.mla_sparse(seed=1002 + seed_shift)
     raise ValueError(name)
 
 
@@ -177,9 +187,22 @@ class GpuCase:
         a.combine(pl, self.out, self.lse)
 
 
-def time_steps(case, steps, warmup, split_events=True):
+_FLUSH = None
+
+
+def flush_l2():
+    """Write a buffer twice the size of L2 so the next step starts cold."""
+    global _FLUSH
+    if _FLUSH is None:
+        _FLUSH = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    _FLUSH.fill_(1)
+
+
+def time_steps(case, steps, warmup, split_events=True, flush=False):
     """Device time per step (ms) and of the split kernel alone, CUDA events on
-    the launching stream, synchronised on both sides."""
+    the launching stream, synchronised on both sides.  With flush=True, L2 is
+    flushed between steps (outside the events) and the total is the sum of
+    the per-step event times."""
     for _ in range(warmup):
         case.step()
     torch.cuda.synchronize()
@@ -192,6 +215,8 @@ def time_steps(case, steps, warmup, split_events=True):
     torch.cuda.synchronize()
     t0.record()
     for i in range(steps):
+        if flush:
+            flush_l2()
         starts[i].record()
         case.step(runs[i])
         ends[i].record()
@@ -199,7 +224,8 @@ def time_steps(case, steps, warmup, split_events=True):
     torch.cuda.synchronize()
     per_step = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     split = [r[0].elapsed_time(r[1]) for r in runs] if split_events else []
-    return t0.elapsed_time(t1), per_step, split
+    total = sum(per_step) if flush else t0.elapsed_time(t1)
+    return total, per_step, split
 
 
 def e2e_steps(case, steps, warmup):
@@ -282,7 +308,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gqa_paged",
-                    choices=["gqa_paged", "long_context", "tiny"])
+                    choices=["gqa_paged", "long_context", "tiny", "mla_sparse"])
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the secondary workloads and the CPU baseline")
     args = ap.parse_args()
@@ -378,25 +404,37 @@ def main():
     }
     if not args.no_extra:
         extra = {}
-        for name in ("long_context", "tiny"):
+        for name in ("long_context", "mla_sparse", "tiny"):
             if name == args.workload:
                 continue
             w2 = build_workload(name)
             c2 = GpuCase(w2, dev, api.INVARIANT)
             n = 20 if name == "long_context" else 200
-            ms2, _, sp2 = time_steps(c2, n, 5)
+            # the MLA cache (75.5 MB) fits in L2: flush it between steps
+            fl = name == "mla_sparse"
+            ms2, _, sp2 = time_steps(c2, n, 5, flush=fl)
             ms2 /= n
             kvb = w2.kv_bytes()
             c2.policy = api.BALANCED
-            bms, _, _ = time_steps(c2, n, 5, split_events=False)
+            bms, _, _ = time_steps(c2, n, 5, split_events=False, flush=fl)
             bms /= n
-            extra[w2.name] = {
+            sp = sum(sp2) / len(sp2)
+            rec = {
                 "ms_per_step": round(ms2, 5), "kv_gbs": round(kvb / (ms2 * 1e-3) / 1e9, 1),
                 "rows_per_s": round(w2.B / (ms2 * 1e-3), 1),
                 "hbm_frac": round(kvb / (ms2 * 1e-3) / 1e9 / peak, 4),
-                "split_ms_avg": round(sum(sp2) / len(sp2), 5),
+                "split_ms_avg": round(sp, 5),
                 "balanced_ms_per_step": round(bms, 5),
+                "l2": "flushed between steps" if fl else "inputs larger than L2",
             }
+            if name == "mla_sparse":
+                n_ent = int(w2.lengths.to(torch.int64).sum())
+                flops = n_ent * w2.H_q * (w2.D_qk + w2.D_v) * 2
+                rec["tensor_tflops_split"] = round(flops / (sp * 1e-3) / 1e12, 1)
+                rec["tensor_frac_split_of_measured_bf16"] = round(
+                    flops / (sp * 1e-3) / 1e12 / tensor_peak(), 4)
+                rec["hbm_frac_split"] = round(kvb / (sp * 1e-3) / 1e9 / peak, 4)
+            extra[w2.name] = rec
             del c2, w2
             torch.cuda.empty_cache()
         line["other_workloads"] = extra

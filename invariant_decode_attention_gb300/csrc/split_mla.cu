@@ -1,11 +1,461 @@
-// Split kernel, tensor-core variant for a shared latent KV (D_qk 576, D_v 512).
-// Not built yet: every MLA-shaped problem reports DA_ERR_UNSUPPORTED.
+// Split kernel, tensor-core variant: up to 128 query heads sharing one latent
+// KV row of 576 dims whose first 512 dims are the value (MLA-style sparse
+// decode, the case "Sparse MLA decode is not batch-invariant" -- FlashMLA
+// issue #212 -- reports on).
+//
+// Both contractions run on tcgen05 tensor cores with fp32 accumulators in
+// tensor memory:
+//     S = Q K^T      M = 128 heads, N = 32 entries, K = 576   (36 MMAs of K=16)
+//     O += P V_half  M = 128 heads, N = 256 dims,   K = 32    (2 MMAs)
+// O for 128 heads x 512 dims in fp32 would fill all of one SM's tensor memory,
+// so a (row, split) item runs as two units, one per half of the value dims;
+// each unit computes the full S itself (the same instructions on the same
+// data, so both halves see the same bits).
+//
+// Roles inside a CTA (288 threads):
+//   warps 0-3  softmax: thread i owns head i = tensor-memory lane i.  It reads
+//              its row of S, keeps the running max and sum in fp32, writes P
+//              (bf16) into shared memory and rescales its row of O when the
+//              max it uses moves by more than 2^8.
+//   warps 4-7  producer: gathers each entry's 1152-byte latent row with
+//              16-byte cp.async into the 128-byte-swizzled K-major layout the
+//              tensor core reads (and the unit's Q at its start).
+//   warp 8     MMA issue (one thread) and tensor-memory allocation.
+// Every wait on an mbarrier is bounded; on time-out the kernel records
+// DA_DEVERR_TIMEOUT, every role leaves its loop, outstanding tensor-core work
+// is drained (bounded) and tensor memory is freed.
 #include "common.cuh"
+#include "tcgen05.cuh"
 
 namespace da {
+namespace {
 
-bool mla_supported(int) { return false; }
+constexpr int kHeads = 128;       // MMA M (query heads, zero-padded)
+constexpr int kDqk = 576;
+constexpr int kDvHalf = 256;      // value dims per unit
+constexpr int kSub = 32;          // entries per sub-tile
+constexpr int kRegions = kDqk / 64;  // 64-dim swizzle regions of a row
+constexpr int kRowChunks = kDqk / 8; // 16-byte chunks of a row (72)
+
+// shared memory map (bytes)
+constexpr int kQBytes = kRegions * kHeads * 128;           // 147456
+constexpr int kStageRegion = kSub * 128;                    // 4096
+constexpr int kStageBytes = kRegions * kStageRegion;        // 36864
+constexpr int kStageOffset = kQBytes;
+constexpr int kPOffset = kStageOffset + 2 * kStageBytes;    // 221184
+constexpr int kPBytes = kHeads * kSub * 2;                  // 8192 (64-byte swizzle)
+constexpr int kBarOffset = kPOffset + kPBytes;              // 229376
+enum { kFull0 = 0, kFull1, kEmpty0, kEmpty1, kSFull0, kSFull1, kSFree0, kSFree1,
+       kPFull, kODone, kOFree, kQFull, kQFree, kDrain, kNumBars };
+constexpr int kTmemSlot = kBarOffset + kNumBars * 8;
+constexpr int kAbortSlot = kTmemSlot + 4;
+constexpr int kSmemBytes = kAbortSlot + 12;
+static_assert(kSmemBytes <= 232448, "fits the 227 KB per-block limit");
+
+constexpr int kThreads = 288;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kOCol = 256;   // O accumulator columns [256, 512)
+constexpr float kRescaleLog2 = 8.f;
+
+constexpr uint32_t kIdescS = umma::idesc_bf16_f32(kHeads, kSub, false);
+constexpr uint32_t kIdescO = umma::idesc_bf16_f32(kHeads, kDvHalf, true);
+
+__device__ __forceinline__ void cp_async16_zero(uint32_t dst, const void* any_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, 0;" ::"r"(dst), "l"(any_src)
+               : "memory");
+}
+
+// The mbarrier receives one arrive once all earlier cp.async of this thread land.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+struct Ctx {
+  uint8_t* smem;
+  uint32_t sbase;  // shared address of smem[0]
+  volatile int* abort_flag;
+  int32_t* hdr;
+};
+
+__device__ __forceinline__ uint32_t bar_addr(const Ctx& c, int i) {
+  return c.sbase + kBarOffset + 8 * i;
+}
+
+// Bounded wait that also gives up when the abort flag is raised.
+__device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity) {
+  const uint32_t bar = bar_addr(c, i);
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*c.abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        set_error(c.hdr, DA_DEVERR_TIMEOUT);
+        *c.abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// A unit: one half of the value dims of one (row, split) item.
+struct MlaUnit {
+  int slot, b, half, t_begin, t_end;  // entry range [t_begin, t_end)
+  bool single, empty;
+};
+
+__device__ __forceinline__ MlaUnit mla_unit(const Launch& p, int u) {
+  const int4 d = __ldg(reinterpret_cast<const int4*>(p.item_desc) + (u >> 1));
+  MlaUnit x;
+  x.single = d.x < 0;
+  x.slot = x.single ? ~d.x : d.x;
+  x.b = x.slot / p.max_splits;
+  x.half = u & 1;
+  x.t_begin = d.y * kMlaTile;
+  x.t_end = min(d.z * kMlaTile, d.w);
+  x.empty = x.t_end <= x.t_begin;
+  return x;
+}
+
+// Latent-cache row holding entry `tok` of row b (H_kv = 1).
+__device__ __forceinline__ bool latent_row(const Launch& p, int b, int tok, long long* row) {
+  if (p.layout == DA_KV_CONTIGUOUS) {
+    *row = (long long)b * p.width + tok;
+    return true;
+  }
+  if (p.layout == DA_KV_PAGED) {
+    const int page = __ldg(p.table + (size_t)b * p.width + tok / p.page_size);
+    *row = (long long)page * p.page_size + tok % p.page_size;
+    return page >= 0 && page < p.num_blocks;
+  }
+  const int slot = __ldg(p.table + (size_t)b * p.width + tok);
+  *row = slot;
+  return slot >= 0 && slot < p.num_blocks;
+}
+
+// 128-byte swizzle inside a 1024-byte-aligned region of 128-byte rows.
+__device__ __forceinline__ uint32_t sw128(int row, int chunk) {
+  return row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
+// ---------------------------------------------------------------- producer
+__device__ void producer(const Launch& p, const Ctx& c, int n_units) {
+  const int pt = threadIdx.x - 128;  // 0..127
+  uint32_t g = 0, n_ne = 0;
+  bool alive = true;
+  bool bad = false;
+  for (int u = blockIdx.x; u < n_units && alive; u += gridDim.x) {
+    const MlaUnit x = mla_unit(p, u);
+    if (x.empty) continue;
+    // Q of row b (zero rows past H_q), once the previous unit's S MMAs are done
+    if (!wait_bar(c, kQFree, (n_ne & 1) ^ 1)) break;
+    for (int i = 0; i < kHeads * kRowChunks / 128; ++i) {
+      const int q = pt + 128 * i;
+      const int r = q / kRowChunks, j = q % kRowChunks;
+      const uint32_t dst = c.sbase + (j >> 3) * (kHeads * 128) + sw128(r, j & 7);
+      if (r < p.H_q)
+        cp_async16(dst, p.q + ((size_t)x.b * p.H_q + r) * kDqk + j * 8);
+      else
+        cp_async16_zero(dst, p.q);
+    }
+    cp_async_arrive_noinc(bar_addr(c, kQFull));
+    for (int t0 = x.t_begin; t0 < x.t_end; t0 += kSub, ++g) {
+      const int stage = g & 1;
+      if (!wait_bar(c, kEmpty0 + stage, ((g >> 1) & 1) ^ 1)) {
+        alive = false;
+        break;
+      }
+      const int n_valid = min(kSub, x.t_end - t0);
+      const uint32_t sb = c.sbase + kStageOffset + stage * kStageBytes;
+      for (int i = 0; i < kSub * kRowChunks / 128; ++i) {
+        const int q = pt + 128 * i;
+        const int r = q / kRowChunks, j = q % kRowChunks;
+        const uint32_t dst = sb + (j >> 3) * kStageRegion + sw128(r, j & 7);
+        long long row = 0;
+        bool ok = false;
+        if (r < n_valid) {
+          ok = latent_row(p, x.b, t0 + r, &row);
+          bad |= !ok;
+        }
+        if (ok)
+          cp_async16(dst, p.k + (size_t)row * kDqk + j * 8);
+        else
+          cp_async16_zero(dst, p.k);  // masked entries read as zeros, never garbage
+      }
+      cp_async_arrive_noinc(bar_addr(c, kFull0 + stage));
+    }
+    ++n_ne;
+  }
+  if (bad) set_error(p.hdr, DA_DEVERR_INDEX);
+  cp_async_wait<0>();
+}
+
+// ---------------------------------------------------------------- MMA issue
+__device__ void mma_issuer(const Launch& p, const Ctx& c, uint32_t tmem, int n_units) {
+  uint32_t g = 0, n_ne = 0;
+  for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+    const MlaUnit x = mla_unit(p, u);
+    if (x.empty) continue;
+    const int n_sub = (x.t_end - x.t_begin + kSub - 1) / kSub;
+    if (!wait_bar(c, kQFull, n_ne & 1)) return;
+    fence_proxy_async();
+    umma::fence_after_sync();
+    auto pv = [&](uint32_t gp, bool first) -> bool {
+      if (!wait_bar(c, kPFull, gp & 1)) return false;
+      if (first && !wait_bar(c, kOFree, (n_ne & 1) ^ 1)) return false;
+      umma::fence_after_sync();
+      const uint32_t stage_base = c.sbase + kStageOffset + (gp & 1) * kStageBytes;
+#pragma unroll
+      for (int kk = 0; kk < kSub / 16; ++kk) {
+        const uint64_t a = umma::smem_desc(c.sbase + kPOffset + kk * 32, 16, 512, umma::kSwizzle64B);
+        const uint64_t b = umma::smem_desc(stage_base + (4 * x.half) * kStageRegion + kk * 2048,
+                                           kStageRegion, 1024, umma::kSwizzle128B);
+        umma::mma_bf16(tmem + kOCol, a, b, kIdescO, (first && kk == 0) ? 0u : 1u);
+      }
+      umma::commit(bar_addr(c, kODone));
+      umma::commit(bar_addr(c, kEmpty0 + (gp & 1)));
+      return true;
+    };
+    for (int i = 0; i < n_sub; ++i, ++g) {
+      const int stage = g & 1;
+      if (!wait_bar(c, kFull0 + stage, (g >> 1) & 1)) return;
+      fence_proxy_async();
+      if (!wait_bar(c, kSFree0 + stage, ((g >> 1) & 1) ^ 1)) return;
+      umma::fence_after_sync();
+      const uint32_t stage_base = c.sbase + kStageOffset + stage * kStageBytes;
+      const uint32_t d_s = tmem + stage * kSub;
+#pragma unroll 1
+      for (int r = 0; r < kRegions; ++r) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t a = umma::smem_desc(c.sbase + r * (kHeads * 128) + kk * 32, 16, 1024,
+                                             umma::kSwizzle128B);
+          const uint64_t b = umma::smem_desc(stage_base + r * kStageRegion + kk * 32, 16, 1024,
+                                             umma::kSwizzle128B);
+          umma::mma_bf16(d_s, a, b, kIdescS, (r | kk) ? 1u : 0u);
+        }
+      }
+      umma::commit(bar_addr(c, kSFull0 + stage));
+      if (i == n_sub - 1) umma::commit(bar_addr(c, kQFree));
+      if (i > 0 && !pv(g - 1, i == 1)) return;
+    }
+    if (!pv(g - 1, n_sub == 1)) return;
+    ++n_ne;
+  }
+}
+
+// ---------------------------------------------------------------- softmax + epilogue
+__device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int n_units) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = threadIdx.x;  // head = tensor-memory lane
+  const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+  uint32_t g = 0;
+  // warp-uniform bounded wait (lane 0 waits, everyone follows its verdict)
+  auto wait_w = [&](int bar, uint32_t parity) -> bool {
+    int ok = 1;
+    if (lane == 0) ok = wait_bar(c, bar, parity) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+  };
+  auto arrive_w = [&](int bar) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_addr(c, bar));
+  };
+  for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+    const MlaUnit x = mla_unit(p, u);
+    const bool head_ok = row < p.H_q;
+    const size_t out_row = ((size_t)x.b * p.H_q + row) * 512 + x.half * kDvHalf;
+    if (x.empty) {  // empty row: out = 0, lse = -inf (always a single split)
+      if (head_ok) {
+        for (int d = 0; d < kDvHalf; ++d) p.out[out_row + d] = __float2bfloat16_rn(0.f);
+        if (x.half == 0) p.lse[(size_t)x.b * p.H_q + row] = -INFINITY;
+      }
+      continue;
+    }
+    const int n_sub = (x.t_end - x.t_begin + kSub - 1) / kSub;
+    float m_used = -INFINITY, l = 0.f;
+    for (int i = 0; i < n_sub; ++i, ++g) {
+      const int sb = g & 1;
+      if (!wait_w(kSFull0 + sb, (g >> 1) & 1)) return;
+      umma::fence_after_sync();
+      float s[32];
+      umma::ld_32x32b_x32(lane_base + sb * kSub, s);
+      umma::wait_ld();
+      umma::fence_before_sync();
+      arrive_w(kSFree0 + sb);
+      const int n_valid = min(kSub, x.t_end - (x.t_begin + i * kSub));
+      float mt = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        s[j] = (j < n_valid) ? s[j] * p.scale_log2 : -INFINITY;
+        mt = fmaxf(mt, s[j]);
+      }
+      // the max used for the exponentials moves only when the tile max
+      // exceeds it by more than 2^8 (fewer O rescales; P stays <= 256)
+      const float m_new = (i == 0 || mt > m_used + kRescaleLog2) ? mt : m_used;
+      const float alpha = (i == 0) ? 1.f : ex2(m_used - m_new);
+      float sum = 0.f;
+      uint32_t pk[16];
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        const float p0 = ex2(s[j] - m_new), p1 = ex2(s[j + 1] - m_new);
+        sum += p0;
+        sum += p1;
+        const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+        pk[j / 2] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      l = (i == 0) ? sum : fmaf(l, alpha, sum);
+      if (i > 0) {  // PV of the previous sub-tile must be done with P and O
+        if (!wait_w(kODone, (g - 1) & 1)) return;
+        umma::fence_after_sync();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+          for (int ch = 0; ch < kDvHalf / 32; ++ch) {
+            float o[32];
+            umma::ld_32x32b_x32(lane_base + kOCol + ch * 32, o);
+            umma::wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] *= alpha;
+            umma::st_32x32b_x32(lane_base + kOCol + ch * 32, o);
+          }
+          umma::wait_st();
+        }
+      }
+      m_used = m_new;
+      // P row (32 bf16 = 64 bytes) into the 64-byte-swizzled K-major tile
+      uint8_t* prow = c.smem + kPOffset + row * 64;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc)
+        *reinterpret_cast<uint4*>(prow + ((cc ^ ((row >> 1) & 3)) << 4)) =
+            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+      fence_proxy_async();
+      umma::fence_before_sync();
+      arrive_w(kPFull);
+    }
+    // epilogue: O / l for this half of the value dims
+    if (!wait_w(kODone, (g - 1) & 1)) return;
+    umma::fence_after_sync();
+    const float inv = (l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll 1
+    for (int ch = 0; ch < kDvHalf / 32; ++ch) {
+      float o[32];
+      umma::ld_32x32b_x32(lane_base + kOCol + ch * 32, o);
+      umma::wait_ld();
+      if (head_ok) {
+        if (x.single) {
+          uint4* dst = reinterpret_cast<uint4*>(p.out + out_row + ch * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __nv_bfloat162 h =
+                  __floats2bfloat162_rn(o[v * 8 + 2 * e] * inv, o[v * 8 + 2 * e + 1] * inv);
+              w[e] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(
+              p.o_part + ((size_t)x.slot * p.H_q + row) * 512 + x.half * kDvHalf + ch * 32);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            dst[v] = make_float4(o[4 * v] * inv, o[4 * v + 1] * inv, o[4 * v + 2] * inv,
+                                 o[4 * v + 3] * inv);
+        }
+      }
+    }
+    umma::fence_before_sync();
+    arrive_w(kOFree);
+    if (head_ok && x.half == 0) {
+      const float lse2 = (l > 0.f) ? m_used + lg2(l) : -INFINITY;
+      if (x.single)
+        p.lse[(size_t)x.b * p.H_q + row] = (l > 0.f) ? lse2 * kLn2 : -INFINITY;
+      else
+        p.lse_part[(size_t)x.slot * p.H_q + row] = lse2;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) split_mla_kernel(Launch p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  Ctx c;
+  c.smem = smem;
+  c.sbase = smem_addr(smem);
+  c.abort_flag = reinterpret_cast<volatile int*>(smem + kAbortSlot);
+  c.hdr = p.hdr;
+  const int warp = threadIdx.x >> 5;
+  const int n_units = p.hdr[kHdrNWork] * 2;
+  if ((int)blockIdx.x >= n_units) return;  // uniform across the CTA
+  // the swizzled layouts assume 1024-byte-aligned shared addresses
+  if (c.sbase & 1023u) {
+    if (threadIdx.x == 0) set_error(p.hdr, DA_DEVERR_TIMEOUT);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNumBars; ++i) {
+      uint32_t count = 1;
+      if (i == kFull0 || i == kFull1 || i == kQFull) count = 128;  // producer threads
+      if (i == kSFree0 || i == kSFree1 || i == kPFull || i == kOFree) count = 4;  // softmax warps
+      mbar_init(bar_addr(c, i), count);
+    }
+    *c.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 8) {
+    umma::tmem_alloc(c.sbase + kTmemSlot, kTmemCols);
+    umma::tmem_relinquish();
+  }
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kTmemSlot);
+
+  if (warp < 4) {
+    softmax_warps(p, c, tmem, n_units);
+  } else if (warp < 8) {
+    producer(p, c, n_units);
+  } else if ((threadIdx.x & 31) == 0) {
+    mma_issuer(p, c, tmem, n_units);
+    // drain: one more commit; its arrival means every MMA issued before it
+    // has completed, so tensor memory can be freed
+    umma::commit(bar_addr(c, kDrain));
+  }
+  umma::fence_before_sync();
+  __syncthreads();
+  if (warp == 8) {
+    umma::fence_after_sync();
+    if ((threadIdx.x & 31) == 0) {
+      const uint32_t bar = bar_addr(c, kDrain);
+      const unsigned long long t0 = globaltimer_ns();
+      while (!mbar_try_wait(bar, 0)) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          set_error(p.hdr, DA_DEVERR_TIMEOUT);
+          break;
+        }
+      }
+    }
+    __syncwarp();
+    umma::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+bool mla_supported(int H_q) { return H_q >= 16 && H_q <= kHeads; }
+
 int mla_ctas_per_sm() { return 1; }
-cudaError_t launch_split_mla(const Launch&, int, cudaStream_t) { return cudaErrorNotSupported; }
+
+cudaError_t launch_split_mla(const Launch& p, int grid, cudaStream_t stream) {
+  static const cudaError_t attr = cudaFuncSetAttribute(
+      split_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (attr != cudaSuccess) return attr;
+  split_mla_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
 
 }  // namespace da

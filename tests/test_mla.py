@@ -1,0 +1,125 @@
+"""Tensor-core (MLA-style) variant: 16..128 query heads sharing one latent KV
+row of 576 dims whose first 512 are the value -- the sparse decode case of
+"Sparse MLA decode is not batch-invariant" (FlashMLA issue #212).  Parity
+against the fp64 oracle, bitwise batch invariance, and the variant's split
+constants."""
+
+import pytest
+import torch
+
+from _util import assert_parity, oracle_for
+from invariant_decode_attention_gb300 import workloads as W
+from oracle import plan as OP
+
+gpu = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def api():
+    import os
+    from invariant_decode_attention_gb300 import api as _api
+    if not os.path.exists(_api.LIB_PATH):
+        from invariant_decode_attention_gb300 import build
+        build.build()
+    _api.lib()
+    return _api
+
+
+# ---------------------------------------------------------------- CPU: constants
+
+@pytest.mark.parametrize("h_q", [16, 64, 128])
+def test_mla_split_constants_match_oracle(api, h_q):
+    prob = api.problem(batch=2, num_q_heads=h_q, num_kv_heads=1, head_dim_qk=576,
+                       head_dim_v=512, layout="indexed", scale=576 ** -0.5, width=2048,
+                       num_blocks=65536, shared_latent=True)
+    variant, *consts = api.split_constants(prob)
+    assert variant == api.VARIANT_MLA
+    assert tuple(consts) == OP.VARIANT_CONSTANTS["mla"]
+
+
+def test_mla_unsupported_shapes(api):
+    for h_q, h_kv, d_qk, d_v in [(8, 1, 576, 512), (256, 1, 576, 512), (128, 2, 576, 512),
+                                 (128, 1, 512, 512), (128, 1, 576, 448)]:
+        prob = api.problem(batch=1, num_q_heads=h_q, num_kv_heads=h_kv, head_dim_qk=d_qk,
+                           head_dim_v=d_v, layout="indexed", scale=0.1, width=8,
+                           num_blocks=64, shared_latent=True)
+        with pytest.raises(api.DecodeAttnError) as e:
+            api.split_constants(prob)
+        assert e.value.status == api.ERR_UNSUPPORTED
+
+
+# ---------------------------------------------------------------- GPU: parity
+
+@gpu
+@pytest.mark.parametrize("layout", [W.INDEXED, W.PAGED, W.CONTIGUOUS])
+def test_mla_small_all_layouts(api, layout):
+    lens = [1, 31, 32, 33, 64, 700, 0, 2048]
+    wl = W.make(layout, lens, H_q=128, H_kv=1, D_qk=576, D_v=512, latent=True,
+                page_size=64, num_slots=5000, width=2048 if layout != W.PAGED else None,
+                seed=40)
+    out, lse = api.run_workload(wl.to("cuda"))
+    ro, rl = oracle_for(wl)
+    assert_parity(out, lse, ro, rl)
+
+
+@gpu
+@pytest.mark.parametrize("h_q", [16, 64, 100])
+def test_mla_fewer_heads(api, h_q):
+    wl = W.make(W.INDEXED, [300, 1500], H_q=h_q, H_kv=1, D_qk=576, D_v=512, latent=True,
+                num_slots=4000, width=2048, seed=h_q)
+    out, lse = api.run_workload(wl.to("cuda"))
+    ro, rl = oracle_for(wl)
+    assert_parity(out, lse, ro, rl)
+
+
+@gpu
+def test_mla_config_full(api):
+    wl = W.mla_sparse()
+    out, lse = api.run_workload(wl.to("cuda"))
+    ro, rl = oracle_for(wl)
+    assert_parity(out, lse, ro, rl)
+
+
+@gpu
+def test_mla_balanced_is_correct(api):
+    wl = W.mla_sparse()
+    out, lse = api.run_workload(wl.to("cuda"), policy=api.BALANCED)
+    rows = list(range(0, 64, 7))
+    ro, rl = oracle_for(wl, rows=rows)
+    assert_parity(out, lse, ro, rl, rows=rows)
+
+
+@gpu
+def test_mla_out_of_range_index_sets_error(api):
+    wl = W.make(W.INDEXED, [40, 300], H_q=128, H_kv=1, D_qk=576, D_v=512, latent=True,
+                num_slots=1000, width=512, seed=77)
+    wl.table[1, 5] = 5000
+    g = wl.to("cuda")
+    prob = api.problem_for(g)
+    ws = api.workspace(prob)
+    out = torch.empty((2, 128, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((2, 128), dtype=torch.float32, device="cuda")
+    pl = api.plan(prob, api.INVARIANT, g.lengths, ws)
+    api.run(pl, g.q, g.k, None, g.table, g.lengths, out, lse)
+    api.combine(pl, out, lse)
+    assert api.read_error(pl) & api.DEVERR_INDEX
+    assert not api.read_error(pl) & api.DEVERR_TIMEOUT
+    ro, rl = oracle_for(wl, rows=[0])
+    assert_parity(out, lse, ro, rl, rows=[0])
+
+
+# ---------------------------------------------------------------- GPU: invariance
+
+@gpu
+def test_mla_row_solo_vs_batch(api):
+    wl = W.mla_sparse()
+    g = wl.to("cuda")
+    o, l = api.run_workload(g)
+    for r in (0, 21, 63):
+        solo = W.Workload("solo", W.INDEXED, g.q[r:r + 1].contiguous(), g.k, None,
+                          g.lengths[r:r + 1].contiguous(), g.table[r:r + 1].contiguous(),
+                          0, 128, 1, 576, 512, wl.scale)
+        o1, l1 = api.run_workload(solo)
+        assert torch.equal(o1[0], o[r]) and torch.equal(l1[0], l[r])
+    o2, l2 = api.run_workload(g)
+    assert torch.equal(o2, o) and torch.equal(l2, l)
