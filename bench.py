@@ -35,10 +35,14 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
+L2_FLUSH_BELOW = 256 << 20  # bytes; GB300 L2 is ~126 MB
 METRIC = "decode-attn KV GB/s (% of GB300 HBM peak), rows/s; invariant vs balanced split"
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = {
     "split_fma": ["invariant_decode_attention_gb300/csrc/split_fma.cu",
+                  "invariant_decode_attention_gb300/csrc/common.cuh"],
+    "split_mla": ["invariant_decode_attention_gb300/csrc/split_mla.cu",
+                  "invariant_decode_attention_gb300/csrc/tcgen05.cuh",
                   "invariant_decode_attention_gb300/csrc/common.cuh"],
 }
 
@@ -337,8 +341,10 @@ def main():
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
+    # inputs smaller than twice L2 are flushed out of it between steps
+    flush = kv_bytes < L2_FLUSH_BELOW
     with ClockSampler(local) as clocks:
-        total_ms, per_step, split_ms = time_steps(case, args.steps, args.warmup)
+        total_ms, per_step, split_ms = time_steps(case, args.steps, args.warmup, flush=flush)
     if world > 1:
         import torch.distributed as dist
         t = torch.tensor([total_ms], device=dev)
@@ -354,9 +360,10 @@ def main():
         return
 
     # INVARIANT vs BALANCED on the same inputs
+    kernel = "split_mla" if wl.v is None else "split_fma"
     n_bal = max(20, args.steps // 4)
     case.policy = api.BALANCED
-    bal_ms, _, _ = time_steps(case, n_bal, args.warmup, split_events=False)
+    bal_ms, _, _ = time_steps(case, n_bal, args.warmup, split_events=False, flush=flush)
     bal_ms /= n_bal
     case.policy = api.INVARIANT
 
@@ -380,7 +387,8 @@ def main():
             "workload": wl.name, "rows": wl.B, "H_q": wl.H_q, "H_kv": wl.H_kv,
             "head_dim": wl.D_qk, "layout": wl.layout, "page_size": wl.page_size,
             "kv_bytes_per_step": kv_bytes, "policy": "invariant",
-            "l2": f"inputs larger than L2 ({kv_bytes / 1e6:.0f} MB of KV per step)",
+            "l2": (f"L2 flushed between steps ({kv_bytes / 1e6:.0f} MB of KV per step)" if flush
+                   else f"inputs larger than L2 ({kv_bytes / 1e6:.0f} MB of KV per step)"),
             "parallelism": f"replicas x{world}",
         },
         "rows_per_s": round(world * wl.B / (ms_per_step * 1e-3), 1),
@@ -389,10 +397,10 @@ def main():
                      "value": round(kv_bytes / (bal_ms * 1e-3) / 1e9, 2),
                      "invariant_over_balanced_time": round(ms_per_step / bal_ms, 4)},
         "roofline": {
-            "kernel": "split_fma", "bound": "hbm", "achieved": round(achieved, 1),
+            "kernel": kernel, "bound": "hbm", "achieved": round(achieved, 1),
             "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
             "peak_kind": peak_kind,
-            "traffic": recorded_traffic("split_fma", wl.name),
+            "traffic": recorded_traffic(kernel, wl.name),
             "alg_bytes_per_launch": alg_bytes,
             "split_ms_avg": round(split_avg, 5),
         },
@@ -410,8 +418,8 @@ def main():
             w2 = build_workload(name)
             c2 = GpuCase(w2, dev, api.INVARIANT)
             n = 20 if name == "long_context" else 200
-            # the MLA cache (75.5 MB) fits in L2: flush it between steps
-            fl = name == "mla_sparse"
+            # inputs that fit in L2 (the MLA cache is 75.5 MB) are flushed between steps
+            fl = w2.kv_bytes() < L2_FLUSH_BELOW
             ms2, _, sp2 = time_steps(c2, n, 5, flush=fl)
             ms2 /= n
             kvb = w2.kv_bytes()

@@ -125,6 +125,12 @@ Launch make_launch(const da_plan* plan) {
   L.page_size = pr.page_size;
   L.width = pr.width;
   L.capacity = (int)row_capacity(pr.layout, pr.width, pr.page_size);
+  L.page_shift = -1;
+  if (pr.layout == DA_KV_PAGED && pr.page_size > 0 && (pr.page_size & (pr.page_size - 1)) == 0) {
+    int sh = 0;
+    while ((1 << sh) < pr.page_size) ++sh;
+    L.page_shift = sh;
+  }
   L.max_splits = plan->max_splits;
   L.scale_log2 = pr.scale * kLog2e;
   return L;

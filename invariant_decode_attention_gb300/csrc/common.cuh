@@ -55,6 +55,7 @@ struct Launch {
   long long num_blocks;
   int B, H_q, H_kv, D_qk, D_v;
   int layout, page_size, width, capacity;
+  int page_shift;  // log2(page_size) when it is a power of two, else -1
   int max_splits;
   float scale_log2;  // softmax scale * log2(e)
 };
@@ -105,6 +106,35 @@ __device__ __forceinline__ float lg2(float x) {
   float y;
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// ---- packed fp32 pairs (one 64-bit register = {lo, hi}) -------------------
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// d = a * b + c on both halves (round to nearest even, no contraction change)
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// bf16 pair (one 32-bit word) -> packed fp32 pair {lo, hi}, exactly.
+__device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t w) {
+  return pack2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
 // bf16 pair (as one 32-bit word) -> two floats, exactly.

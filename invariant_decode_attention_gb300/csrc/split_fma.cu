@@ -13,9 +13,9 @@
 // a warp never waits for another warp inside the tile loop.  Eight lanes
 // share an entry (two 16-byte chunks of a 128-dim row each), so a score is an
 // 8-lane butterfly sum, and a lane keeps fp32 accumulators for the G heads
-// over its own dims.  Online softmax runs in the log2 domain with a
-// warp-uniform running max.  At the end of a unit the lane groups and then the
-// warps merge in a fixed order.  Every reduction has a fixed shape and order,
+// over its own dims, as packed pairs updated with two-wide FMAs.  Online
+// softmax runs in the log2 domain with a warp-uniform running max.  At the end
+// of a unit the lane groups and then the warps merge in a fixed order.  Every reduction has a fixed shape and order,
 // so a unit's bits depend only on its inputs and its split boundaries.
 //
 // Softmax attention and its split/merge are the computation the FlashMLA
@@ -136,15 +136,31 @@ __device__ __forceinline__ void load_slice(const Launch& p, const Cursor& c, uin
     const int grp = lane >> 3, sub = lane & 7;
     uint8_t* ks = smem + (slot * S::kWarps + warp) * S::kWarpSlotBytes;
     uint8_t* vs = ks + S::kSliceBytes;
-    const int t0 = c.k * S::kTile + warp * S::kTokPerWarp;
+    const int t0 = c.k * S::kTile + warp * S::kTokPerWarp;  // a multiple of 16
+    // Contiguous rows, and pages of a multiple of 16 entries, put the warp's
+    // 16 entries in consecutive cache rows: one page lookup per slice.
+    bool uniform = false, base_ok = true;
+    long long base_row = 0;
+    if (t0 < c.x.L) {
+      if (p.layout == DA_KV_CONTIGUOUS) {
+        uniform = true;
+        base_row = (long long)c.x.b * p.width + t0;
+      } else if (p.layout == DA_KV_PAGED && (p.page_size & 15) == 0) {
+        uniform = true;
+        const int pi = (p.page_shift >= 0) ? (t0 >> p.page_shift) : (t0 / p.page_size);
+        const int page = __ldg(p.table + (size_t)c.x.b * p.width + pi);
+        base_ok = page >= 0 && page < p.num_blocks;
+        base_row = (long long)page * p.page_size + (t0 - pi * p.page_size);
+      }
+    }
     bool bad = false;
 #pragma unroll
     for (int j = 0; j < S::kSteps; ++j) {
       const int tl = 4 * j + grp;
       const int tok = t0 + tl;
       if (tok < c.x.L) {
-        long long row;
-        const bool ok = entry_row(p, c.x.b, tok, &row);
+        long long row = base_row + tl;
+        const bool ok = uniform ? base_ok : entry_row(p, c.x.b, tok, &row);
         bad |= !ok;
         if (ok) {
           const size_t off = ((size_t)row * p.H_kv + c.x.h) * D;
@@ -170,40 +186,47 @@ __device__ __forceinline__ void load_slice(const Launch& p, const Cursor& c, uin
   cp_async_commit();
 }
 
+// A lane's dims of one row as packed fp32 pairs: pair 4c + e holds dims
+// 64c + 8*sub + 2e and 64c + 8*sub + 2e + 1.
 template <int D>
-__device__ __forceinline__ void unpack_row(const uint8_t* row, int sub, float* f) {
+__device__ __forceinline__ void unpack_row2(const uint8_t* row, int sub, uint64_t* f) {
 #pragma unroll
   for (int c = 0; c < D / 64; ++c) {
     const uint4 w = reinterpret_cast<const uint4*>(row)[sub + 8 * c];
-    f[c * 8 + 0] = bf16_lo(w.x); f[c * 8 + 1] = bf16_hi(w.x);
-    f[c * 8 + 2] = bf16_lo(w.y); f[c * 8 + 3] = bf16_hi(w.y);
-    f[c * 8 + 4] = bf16_lo(w.z); f[c * 8 + 5] = bf16_hi(w.z);
-    f[c * 8 + 6] = bf16_lo(w.w); f[c * 8 + 7] = bf16_hi(w.w);
+    f[c * 4 + 0] = bf16x2_to_f2(w.x);
+    f[c * 4 + 1] = bf16x2_to_f2(w.y);
+    f[c * 4 + 2] = bf16x2_to_f2(w.z);
+    f[c * 4 + 3] = bf16x2_to_f2(w.w);
   }
 }
 
 // One warp's 16 entries of one tile: scores, online-softmax update, P.V.
+// Dot products and the P.V update use packed fp32 pairs (two FMAs per
+// instruction); a score is the sum of its even-dim and odd-dim halves.
 template <int G, int D, bool kPartial>
 __device__ __forceinline__ void consume_slice(const uint8_t* ks, int lane, int n_valid,
-                                              const float (&qf)[G][FmaShape<G, D>::kDpl],
+                                              const uint64_t (&q2)[G][FmaShape<G, D>::kDpl / 2],
                                               float (&m)[G], float (&l)[G],
-                                              float (&acc)[G][FmaShape<G, D>::kDpl],
+                                              uint64_t (&acc2)[G][FmaShape<G, D>::kDpl / 2],
                                               float scale_log2) {
   using S = FmaShape<G, D>;
+  constexpr int kP = S::kDpl / 2;  // packed pairs per lane
   const int grp = lane >> 3, sub = lane & 7;
   const uint8_t* vs = ks + S::kSliceBytes;
 
   float s[S::kSteps][G];
 #pragma unroll
   for (int j = 0; j < S::kSteps; ++j) {
-    float kf[S::kDpl];
-    unpack_row<D>(ks + (4 * j + grp) * S::kRowBytes, sub, kf);
+    uint64_t k2[kP];
+    unpack_row2<D>(ks + (4 * j + grp) * S::kRowBytes, sub, k2);
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      float a = 0.f;
+      uint64_t a = ffma2(q2[h][0], k2[0], 0ull);
 #pragma unroll
-      for (int i = 0; i < S::kDpl; ++i) a = fmaf(qf[h][i], kf[i], a);
-      s[j][h] = a;
+      for (int i = 1; i < kP; ++i) a = ffma2(q2[h][i], k2[i], a);
+      float lo, hi;
+      unpack2(a, lo, hi);
+      s[j][h] = lo + hi;
     }
   }
   // Sum the 8 lanes of each entry (butterfly: every lane ends with the same bits).
@@ -248,19 +271,23 @@ __device__ __forceinline__ void consume_slice(const uint8_t* ks, int lane, int n
   }
   if (rescale) {
 #pragma unroll
-    for (int h = 0; h < G; ++h)
+    for (int h = 0; h < G; ++h) {
+      const uint64_t a2 = pack2(alpha[h], alpha[h]);
 #pragma unroll
-      for (int i = 0; i < S::kDpl; ++i) acc[h][i] *= alpha[h];
+      for (int i = 0; i < kP; ++i) acc2[h][i] = fmul2(acc2[h][i], a2);
+    }
   }
 #pragma unroll
   for (int j = 0; j < S::kSteps; ++j) {
     if (kPartial && (4 * j + grp) >= n_valid) continue;  // never read unfilled rows
-    float vf[S::kDpl];
-    unpack_row<D>(vs + (4 * j + grp) * S::kRowBytes, sub, vf);
+    uint64_t v2[kP];
+    unpack_row2<D>(vs + (4 * j + grp) * S::kRowBytes, sub, v2);
 #pragma unroll
-    for (int h = 0; h < G; ++h)
+    for (int h = 0; h < G; ++h) {
+      const uint64_t p2 = pack2(pr[j][h], pr[j][h]);
 #pragma unroll
-      for (int i = 0; i < S::kDpl; ++i) acc[h][i] = fmaf(pr[j][h], vf[i], acc[h][i]);
+      for (int i = 0; i < kP; ++i) acc2[h][i] = ffma2(p2, v2[i], acc2[h][i]);
+    }
   }
 }
 
@@ -284,18 +311,19 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
   }
 
   int slot = 0;
-  float qf[G][S::kDpl];
+  uint64_t q2[G][S::kDpl / 2];
   int4 d_next = load_desc(p, blockIdx.x);
   for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
     const Unit x = make_unit(p, u, d_next);
     if (u + (int)gridDim.x < n_units) d_next = load_desc(p, u + gridDim.x);
-    float m[G], l[G], acc[G][S::kDpl];
+    float m[G], l[G];
+    uint64_t acc2[G][S::kDpl / 2];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       m[h] = -INFINITY;
       l[h] = 0.f;
 #pragma unroll
-      for (int i = 0; i < S::kDpl; ++i) acc[h][i] = 0.f;
+      for (int i = 0; i < S::kDpl / 2; ++i) acc2[h][i] = 0ull;
     }
     for (int k = x.tb; k < x.te; ++k) {
       cp_async_wait<S::kStages - 2>();
@@ -306,7 +334,7 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
         named_bar_sync(1, S::kThreads);
         const uint8_t* sq = smem + S::kQOffset + slot * S::kQPad;
 #pragma unroll
-        for (int h = 0; h < G; ++h) unpack_row<D>(sq + h * S::kRowBytes, sub, qf[h]);
+        for (int h = 0; h < G; ++h) unpack_row2<D>(sq + h * S::kRowBytes, sub, q2[h]);
         named_bar_sync(1, S::kThreads);
       }
       // refill the slot consumed in the previous iteration
@@ -315,13 +343,18 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
       const uint8_t* ks = smem + (slot * S::kWarps + warp) * S::kWarpSlotBytes;
       const int n_valid = min(S::kTokPerWarp, x.L - k * S::kTile - warp * S::kTokPerWarp);
       if (n_valid >= S::kTokPerWarp)
-        consume_slice<G, D, false>(ks, lane, n_valid, qf, m, l, acc, p.scale_log2);
+        consume_slice<G, D, false>(ks, lane, n_valid, q2, m, l, acc2, p.scale_log2);
       else
-        consume_slice<G, D, true>(ks, lane, n_valid, qf, m, l, acc, p.scale_log2);
+        consume_slice<G, D, true>(ks, lane, n_valid, q2, m, l, acc2, p.scale_log2);
       slot = (slot + 1 == S::kStages) ? 0 : slot + 1;
     }
 
     // ---- merge: lane groups (entries) within the warp, then warps ------------
+    float acc[G][S::kDpl];
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int i = 0; i < S::kDpl / 2; ++i) unpack2(acc2[h][i], acc[h][2 * i], acc[h][2 * i + 1]);
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       l[h] += __shfl_xor_sync(0xffffffffu, l[h], 8);

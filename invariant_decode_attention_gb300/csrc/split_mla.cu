@@ -146,6 +146,7 @@ __device__ __forceinline__ uint32_t sw128(int row, int chunk) {
 // ---------------------------------------------------------------- producer
 __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
   const int pt = threadIdx.x - 128;  // 0..127
+  const int pw = pt >> 5, pl = pt & 31;
   uint32_t g = 0, n_ne = 0;
   bool alive = true;
   bool bad = false;
@@ -172,16 +173,21 @@ __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
       }
       const int n_valid = min(kSub, x.t_end - t0);
       const uint32_t sb = c.sbase + kStageOffset + stage * kStageBytes;
-      for (int i = 0; i < kSub * kRowChunks / 128; ++i) {
-        const int q = pt + 128 * i;
-        const int r = q / kRowChunks, j = q % kRowChunks;
-        const uint32_t dst = sb + (j >> 3) * kStageRegion + sw128(r, j & 7);
-        long long row = 0;
-        bool ok = false;
-        if (r < n_valid) {
-          ok = latent_row(p, x.b, t0 + r, &row);
-          bad |= !ok;
-        }
+      // producer warp pw copies entries 8*pw .. 8*pw+7 of the sub-tile: lanes
+      // 0-7 look up those rows once, the copy lanes take them by shuffle
+      long long my_row = 0;
+      int my_ok = 0;
+      if (pl < 8 && 8 * pw + pl < n_valid) {
+        my_ok = latent_row(p, x.b, t0 + 8 * pw + pl, &my_row) ? 1 : 0;
+        bad |= !my_ok;
+      }
+#pragma unroll
+      for (int i = 0; i < 8 * kRowChunks / 32; ++i) {
+        const int q = pl + 32 * i;
+        const int e = q / kRowChunks, j = q % kRowChunks;
+        const long long row = __shfl_sync(0xffffffffu, my_row, e);
+        const int ok = __shfl_sync(0xffffffffu, my_ok, e);
+        const uint32_t dst = sb + (j >> 3) * kStageRegion + sw128(8 * pw + e, j & 7);
         if (ok)
           cp_async16(dst, p.k + (size_t)row * kDqk + j * 8);
         else
