@@ -142,6 +142,24 @@ class ClockSampler:
                 "reasons": sorted(self.reasons), "samples": len(self.samples)}
 
 
+def max_over_ranks(x, device="cpu"):
+    """The largest value of x over all ranks (x itself when not distributed);
+    a barrier follows so no rank runs ahead into the next phase."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.barrier()
+    return float(t.item())
+
+
+def replica_value(per_rank_units, world, ms_per_step):
+    """Whole-job throughput: units all ranks processed per second of the
+    slowest rank's step (weak scaling: every rank runs its own batch)."""
+    return world * per_rank_units / (ms_per_step * 1e-3)
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -345,14 +363,9 @@ def main():
     flush = kv_bytes < L2_FLUSH_BELOW
     with ClockSampler(local) as clocks:
         total_ms, per_step, split_ms = time_steps(case, args.steps, args.warmup, flush=flush)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-        dist.barrier()
+    total_ms = max_over_ranks(total_ms, dev)
     ms_per_step = total_ms / args.steps
-    value = world * kv_bytes / (ms_per_step * 1e-3) / 1e9
+    value = replica_value(kv_bytes, world, ms_per_step) / 1e9
     split_avg = sum(split_ms) / len(split_ms)
     achieved = alg_bytes / (split_avg * 1e-3) / 1e9
 

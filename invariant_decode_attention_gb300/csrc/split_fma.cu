@@ -200,9 +200,33 @@ __device__ __forceinline__ void unpack_row2(const uint8_t* row, int sub, uint64_
   }
 }
 
+// Lane-dependent orders that let the 8 lanes of an entry group reduce their
+// partial dot products by halving (each level: v[i] += shfl_xor(v[i + half]))
+// with no data-dependent selects.  For G >= 2 a lane with sub-lane bits
+// (b2 b1 b0) keeps, in entry slot js, the entry js ^ tperm and, in head slot
+// hs, the head hs ^ hperm:
+//     tperm = 2*b2 + b1,  hperm = b0 * G/2.
+// The permutation is applied where rows are addressed (K, V, q, outputs);
+// values in registers are never shuffled into place.  For G == 1 both are 0
+// and an 8-lane butterfly is used instead.
+template <int G>
+__device__ __forceinline__ int tperm_of(int sub) {
+  return G >= 2 ? (((sub >> 2) & 1) << 1 | ((sub >> 1) & 1)) : 0;
+}
+template <int G>
+__device__ __forceinline__ int hperm_of(int sub) {
+  return G >= 2 ? (sub & 1) * (G / 2) : 0;
+}
+
 // One warp's 16 entries of one tile: scores, online-softmax update, P.V.
 // Dot products and the P.V update use packed fp32 pairs (two FMAs per
-// instruction); a score is the sum of its even-dim and odd-dim halves.
+// instruction); a partial score is the sum of its even-dim and odd-dim halves.
+//
+// G >= 2: after the halving reduction a lane holds the full scores of its own
+// entry (slot 0) for head slots 0 .. G/2-1.  l[i] (i < G/2) sums p over the
+// lane's own entries only; lanes are summed at the end of the unit.
+// G == 1: every lane of a group ends with the group's scores (butterfly) and
+// l[0] counts the group's entries.
 template <int G, int D, bool kPartial>
 __device__ __forceinline__ void consume_slice(const uint8_t* ks, int lane, int n_valid,
                                               const uint64_t (&q2)[G][FmaShape<G, D>::kDpl / 2],
@@ -211,82 +235,130 @@ __device__ __forceinline__ void consume_slice(const uint8_t* ks, int lane, int n
                                               float scale_log2) {
   using S = FmaShape<G, D>;
   constexpr int kP = S::kDpl / 2;  // packed pairs per lane
+  constexpr int kV = S::kSteps * G;  // partial scores per lane
   const int grp = lane >> 3, sub = lane & 7;
+  const int tp = tperm_of<G>(sub);
   const uint8_t* vs = ks + S::kSliceBytes;
 
-  float s[S::kSteps][G];
+  // ---- partial scores v[js * G + hs] over this lane's dims
+  float v[kV];
 #pragma unroll
-  for (int j = 0; j < S::kSteps; ++j) {
+  for (int js = 0; js < S::kSteps; ++js) {
     uint64_t k2[kP];
-    unpack_row2<D>(ks + (4 * j + grp) * S::kRowBytes, sub, k2);
+    unpack_row2<D>(ks + (4 * (js ^ tp) + grp) * S::kRowBytes, sub, k2);
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      uint64_t a = ffma2(q2[h][0], k2[0], 0ull);
+    for (int hs = 0; hs < G; ++hs) {
+      uint64_t a = ffma2(q2[hs][0], k2[0], 0ull);
 #pragma unroll
-      for (int i = 1; i < kP; ++i) a = ffma2(q2[h][i], k2[i], a);
+      for (int i = 1; i < kP; ++i) a = ffma2(q2[hs][i], k2[i], a);
       float lo, hi;
       unpack2(a, lo, hi);
-      s[j][h] = lo + hi;
+      v[js * G + hs] = lo + hi;
     }
   }
-  // Sum the 8 lanes of each entry (butterfly: every lane ends with the same bits).
-#pragma unroll
-  for (int o = 1; o < 8; o <<= 1) {
-#pragma unroll
-    for (int j = 0; j < S::kSteps; ++j)
-#pragma unroll
-      for (int h = 0; h < G; ++h) s[j][h] += __shfl_xor_sync(0xffffffffu, s[j][h], o);
-  }
-#pragma unroll
-  for (int j = 0; j < S::kSteps; ++j) {
-    const bool valid = !kPartial || (4 * j + grp) < n_valid;
-#pragma unroll
-    for (int h = 0; h < G; ++h) s[j][h] = valid ? s[j][h] * scale_log2 : -INFINITY;
-  }
-  // Warp-wide running max per head.
+
+  float alpha[G];
   bool rescale = false;
-  float alpha[G], mnew[G];
+  float pfull[S::kSteps][G];  // p of entry slot js, head slot hs
+  if constexpr (G >= 2) {
+    // ---- halving reduction over the 8 lanes of the group
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    float mx = s[0][h];
+    for (int i = 0; i < kV / 2; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i + kV / 2], 4);
 #pragma unroll
-    for (int j = 1; j < S::kSteps; ++j) mx = fmaxf(mx, s[j][h]);
+    for (int i = 0; i < kV / 4; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i + kV / 4], 2);
+#pragma unroll
+    for (int i = 0; i < kV / 8; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i + kV / 8], 1);
+    // v[0 .. G/2-1]: own entry (4 * tp + grp), head slots 0 .. G/2-1
+    const bool own_valid = !kPartial || (4 * tp + grp) < n_valid;
+    float sc[G / 2], tmax[G];
+#pragma unroll
+    for (int i = 0; i < G / 2; ++i) {
+      sc[i] = own_valid ? v[i] * scale_log2 : -INFINITY;
+      float mx = sc[i];
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      tmax[i] = mx;
+    }
+#pragma unroll
+    for (int i = 0; i < G / 2; ++i) tmax[i + G / 2] = __shfl_xor_sync(0xffffffffu, tmax[i], 1);
+    float mnew[G];
+#pragma unroll
+    for (int hs = 0; hs < G; ++hs) {
+      mnew[hs] = fmaxf(m[hs], tmax[hs]);
+      alpha[hs] = (mnew[hs] == -INFINITY) ? 1.f : ex2(m[hs] - mnew[hs]);
+      rescale |= (alpha[hs] != 1.f);
+      m[hs] = mnew[hs];
+    }
+    // ---- own probabilities, own share of l
+    float pown[G / 2];
+#pragma unroll
+    for (int i = 0; i < G / 2; ++i) {
+      pown[i] = (mnew[i] == -INFINITY) ? 0.f : ex2(sc[i] - mnew[i]);
+      l[i] = fmaf(l[i], alpha[i], pown[i]);
+    }
+    // ---- all-gather p to the 8 lanes of the group (reverse of the halving)
+#pragma unroll
+    for (int i = 0; i < G / 2; ++i) {
+      pfull[0][i] = pown[i];
+      pfull[0][i + G / 2] = __shfl_xor_sync(0xffffffffu, pown[i], 1);
+    }
+#pragma unroll
+    for (int hs = 0; hs < G; ++hs) pfull[1][hs] = __shfl_xor_sync(0xffffffffu, pfull[0][hs], 2);
+#pragma unroll
+    for (int js = 0; js < 2; ++js)
+#pragma unroll
+      for (int hs = 0; hs < G; ++hs)
+        pfull[js + 2][hs] = __shfl_xor_sync(0xffffffffu, pfull[js][hs], 4);
+  } else {
+    // ---- G == 1: 8-lane butterfly, every lane of the group gets the sums
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+#pragma unroll
+      for (int i = 0; i < kV; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
+    }
+    float mx = -INFINITY;
+#pragma unroll
+    for (int js = 0; js < S::kSteps; ++js) {
+      const bool valid = !kPartial || (4 * js + grp) < n_valid;
+      v[js] = valid ? v[js] * scale_log2 : -INFINITY;
+      mx = fmaxf(mx, v[js]);
+    }
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-    mnew[h] = fmaxf(m[h], mx);
-    alpha[h] = (mnew[h] == -INFINITY) ? 1.f : ex2(m[h] - mnew[h]);
-    rescale |= (alpha[h] != 1.f);
-    m[h] = mnew[h];
-  }
-  float pr[S::kSteps][G];
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
+    const float mn = fmaxf(m[0], mx);
+    alpha[0] = (mn == -INFINITY) ? 1.f : ex2(m[0] - mn);
+    rescale = alpha[0] != 1.f;
+    m[0] = mn;
     float sum = 0.f;
 #pragma unroll
-    for (int j = 0; j < S::kSteps; ++j) {
-      pr[j][h] = (mnew[h] == -INFINITY) ? 0.f : ex2(s[j][h] - mnew[h]);
-      sum += pr[j][h];
+    for (int js = 0; js < S::kSteps; ++js) {
+      pfull[js][0] = (mn == -INFINITY) ? 0.f : ex2(v[js] - mn);
+      sum += pfull[js][0];
     }
-    l[h] = fmaf(l[h], alpha[h], sum);
+    l[0] = fmaf(l[0], alpha[0], sum);
   }
   if (rescale) {
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const uint64_t a2 = pack2(alpha[h], alpha[h]);
+    for (int hs = 0; hs < G; ++hs) {
+      const uint64_t a2 = pack2(alpha[hs], alpha[hs]);
 #pragma unroll
-      for (int i = 0; i < kP; ++i) acc2[h][i] = fmul2(acc2[h][i], a2);
+      for (int i = 0; i < kP; ++i) acc2[hs][i] = fmul2(acc2[hs][i], a2);
     }
   }
+  // ---- P.V over the group's 4 entries
 #pragma unroll
-  for (int j = 0; j < S::kSteps; ++j) {
-    if (kPartial && (4 * j + grp) >= n_valid) continue;  // never read unfilled rows
+  for (int js = 0; js < S::kSteps; ++js) {
+    const int row = 4 * (js ^ tp) + grp;
+    if (kPartial && row >= n_valid) continue;  // never read unfilled rows
     uint64_t v2[kP];
-    unpack_row2<D>(vs + (4 * j + grp) * S::kRowBytes, sub, v2);
+    unpack_row2<D>(vs + row * S::kRowBytes, sub, v2);
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const uint64_t p2 = pack2(pr[j][h], pr[j][h]);
+    for (int hs = 0; hs < G; ++hs) {
+      const uint64_t p2 = pack2(pfull[js][hs], pfull[js][hs]);
 #pragma unroll
-      for (int i = 0; i < kP; ++i) acc2[h][i] = ffma2(p2, v2[i], acc2[h][i]);
+      for (int i = 0; i < kP; ++i) acc2[hs][i] = ffma2(p2, v2[i], acc2[hs][i]);
     }
   }
 }
@@ -334,7 +406,8 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
         named_bar_sync(1, S::kThreads);
         const uint8_t* sq = smem + S::kQOffset + slot * S::kQPad;
 #pragma unroll
-        for (int h = 0; h < G; ++h) unpack_row2<D>(sq + h * S::kRowBytes, sub, q2[h]);
+        for (int hs = 0; hs < G; ++hs)
+          unpack_row2<D>(sq + (hs ^ hperm_of<G>(sub)) * S::kRowBytes, sub, q2[hs]);
         named_bar_sync(1, S::kThreads);
       }
       // refill the slot consumed in the previous iteration
@@ -349,7 +422,24 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
       slot = (slot + 1 == S::kStages) ? 0 : slot + 1;
     }
 
-    // ---- merge: lane groups (entries) within the warp, then warps ------------
+    // ---- merge: lanes within the warp, then warps --------------------------
+    // l: G >= 2 sums each lane's own entries (slots 0 .. G/2-1) over the 32
+    // lanes that share a head, then hands the other half of the heads over
+    // from the neighbouring lane; G == 1 sums the four entry groups.
+    if constexpr (G >= 2) {
+#pragma unroll
+      for (int i = 0; i < G / 2; ++i) {
+        l[i] += __shfl_xor_sync(0xffffffffu, l[i], 2);
+        l[i] += __shfl_xor_sync(0xffffffffu, l[i], 4);
+        l[i] += __shfl_xor_sync(0xffffffffu, l[i], 8);
+        l[i] += __shfl_xor_sync(0xffffffffu, l[i], 16);
+      }
+#pragma unroll
+      for (int i = 0; i < G / 2; ++i) l[i + G / 2] = __shfl_xor_sync(0xffffffffu, l[i], 1);
+    } else {
+      l[0] += __shfl_xor_sync(0xffffffffu, l[0], 8);
+      l[0] += __shfl_xor_sync(0xffffffffu, l[0], 16);
+    }
     float acc[G][S::kDpl];
 #pragma unroll
     for (int h = 0; h < G; ++h)
@@ -357,8 +447,6 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
       for (int i = 0; i < S::kDpl / 2; ++i) unpack2(acc2[h][i], acc[h][2 * i], acc[h][2 * i + 1]);
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      l[h] += __shfl_xor_sync(0xffffffffu, l[h], 8);
-      l[h] += __shfl_xor_sync(0xffffffffu, l[h], 16);
 #pragma unroll
       for (int i = 0; i < S::kDpl; ++i) {
         acc[h][i] += __shfl_xor_sync(0xffffffffu, acc[h][i], 8);
@@ -366,18 +454,19 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
       }
     }
     if (grp == 0) {
+      const int hp = hperm_of<G>(sub);
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float* dst = scratch + (warp * G + h) * S::kSRow;
+      for (int hs = 0; hs < G; ++hs) {
+        float* dst = scratch + (warp * G + (hs ^ hp)) * S::kSRow;
 #pragma unroll
         for (int c = 0; c < S::kChunks; ++c) {
           float4* d4 = reinterpret_cast<float4*>(dst + sub * 8 + c * 64);
-          d4[0] = make_float4(acc[h][c * 8 + 0], acc[h][c * 8 + 1], acc[h][c * 8 + 2], acc[h][c * 8 + 3]);
-          d4[1] = make_float4(acc[h][c * 8 + 4], acc[h][c * 8 + 5], acc[h][c * 8 + 6], acc[h][c * 8 + 7]);
+          d4[0] = make_float4(acc[hs][c * 8 + 0], acc[hs][c * 8 + 1], acc[hs][c * 8 + 2], acc[hs][c * 8 + 3]);
+          d4[1] = make_float4(acc[hs][c * 8 + 4], acc[hs][c * 8 + 5], acc[hs][c * 8 + 6], acc[hs][c * 8 + 7]);
         }
-        if (sub == 0) {
-          dst[D] = m[h];
-          dst[D + 1] = l[h];
+        if (sub == 0) {  // lane 0: hperm = 0, slot = head
+          dst[D] = m[hs];
+          dst[D + 1] = l[hs];
         }
       }
     }

@@ -165,22 +165,31 @@ __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
         cp_async16_zero(dst, p.q);
     }
     cp_async_arrive_noinc(bar_addr(c, kQFull));
+    // lanes 0-7 of producer warp pw look up the rows of entries 8*pw .. 8*pw+7
+    // of a sub-tile; the lookup for the next sub-tile is issued before the
+    // copies of the current one so its latency hides behind them
+    auto lookup = [&](int t0, long long& row, int& ok) {
+      row = 0;
+      ok = 0;
+      const int e = 8 * pw + pl;
+      if (pl < 8 && t0 + e < x.t_end) {
+        ok = latent_row(p, x.b, t0 + e, &row) ? 1 : 0;
+        bad |= !ok;
+      }
+    };
+    long long nx_row;
+    int nx_ok;
+    lookup(x.t_begin, nx_row, nx_ok);
     for (int t0 = x.t_begin; t0 < x.t_end; t0 += kSub, ++g) {
       const int stage = g & 1;
       if (!wait_bar(c, kEmpty0 + stage, ((g >> 1) & 1) ^ 1)) {
         alive = false;
         break;
       }
-      const int n_valid = min(kSub, x.t_end - t0);
       const uint32_t sb = c.sbase + kStageOffset + stage * kStageBytes;
-      // producer warp pw copies entries 8*pw .. 8*pw+7 of the sub-tile: lanes
-      // 0-7 look up those rows once, the copy lanes take them by shuffle
-      long long my_row = 0;
-      int my_ok = 0;
-      if (pl < 8 && 8 * pw + pl < n_valid) {
-        my_ok = latent_row(p, x.b, t0 + 8 * pw + pl, &my_row) ? 1 : 0;
-        bad |= !my_ok;
-      }
+      const long long my_row = nx_row;
+      const int my_ok = nx_ok;
+      if (t0 + kSub < x.t_end) lookup(t0 + kSub, nx_row, nx_ok);
 #pragma unroll
       for (int i = 0; i < 8 * kRowChunks / 32; ++i) {
         const int q = pl + 32 * i;
