@@ -76,7 +76,8 @@ def attend_row(q_row, K, V, scale):
 
 
 def attend(q, k_cache, v_cache, lengths, *, scale, layout, table=None,
-           page_size=None, d_v=None, rows=None, heads=None):
+           page_size=None, d_v=None, rows=None, heads=None,
+           extra_k=None, extra_v=None, extra_table=None, extra_lengths=None):
     """Attention of every (row, query head) over the row's own KV list.
 
     q:        ``[B, H_q, D_qk]`` (any float dtype; converted to fp64 exactly)
@@ -85,6 +86,14 @@ def attend(q, k_cache, v_cache, lengths, *, scale, layout, table=None,
               latent cache where ``V = K[..., :d_v]``
     lengths:  ``[B]`` integer KV lengths (``topk_length`` for ``indexed``)
     rows, heads: optional subsets to evaluate (others are left as NaN)
+    extra_*:  an optional second KV source, always index-gathered: row b's
+              list continues with ``extra_k[extra_table[b, t]]`` for
+              t < extra_lengths[b] (values from ``extra_v``, or the leading
+              ``d_v`` dims of ``extra_k`` for a shared latent cache).  The
+              FlashMLA issue #212 page re-runs rows with their
+              ``extra_indices_in_kvcache`` / ``extra_topk_length`` sliced
+              alongside the main indices (Measurement, item 2): the row
+              attends over both lists.
 
     Returns ``(out[B, H_q, D_v], lse[B, H_q])`` in fp64.
     """
@@ -111,6 +120,13 @@ def attend(q, k_cache, v_cache, lengths, *, scale, layout, table=None,
             V = K[..., :Dv]
         else:
             V = row_entries(v_cache, b, L, layout, table, page_size)
+        if extra_k is not None:
+            Le = int(extra_lengths[b])
+            Ke = row_entries(extra_k, b, Le, INDEXED, extra_table)
+            Ve = Ke[..., :Dv] if extra_v is None else row_entries(extra_v, b, Le, INDEXED,
+                                                                   extra_table)
+            K = np.concatenate([K, Ke], axis=0)
+            V = np.concatenate([V, Ve], axis=0)
         for j in heads:
             h = j // G
             out[b, j], lse[b, j] = attend_row(q[b, j], K[:, h, :], V[:, h, :], scale)

@@ -36,7 +36,7 @@ from __future__ import annotations
 # max splits per row).  These are restated independently of the library;
 # tests/test_abi_load.py checks that the library reports the same numbers.
 VARIANT_CONSTANTS = {
-    "fma": (64, 8, 64),
+    "fma": (64, 16, 64),
     "mla": (64, 8, 32),
 }
 
@@ -91,6 +91,21 @@ def plan_balanced(lengths, tile, max_splits, num_parts, fixed_overhead):
     return bounds
 
 
+SORT_KEYS = 256
+
+
 def work_list(bounds, max_splits):
-    """Every (row, split) pair as ``row * max_splits + split``, in batch order."""
-    return [b * max_splits + s for b, cuts in enumerate(bounds) for s in range(len(cuts) - 1)]
+    """Every (row, split) pair as ``row * max_splits + split``: items with more
+    tiles first (key = tile count capped at 255), rows and splits in batch
+    order within a key.  The order only decides which CTA takes an item; an
+    implementation may order items of equal key differently."""
+    items = [(b * max_splits + s, cuts[s + 1] - cuts[s])
+             for b, cuts in enumerate(bounds) for s in range(len(cuts) - 1)]
+    items.sort(key=lambda it: -min(it[1], SORT_KEYS - 1))  # stable: batch order within a key
+    return [slot for slot, _ in items]
+
+
+def work_key(bounds, max_splits, slot):
+    """Sort key of a work item (its tile count, capped)."""
+    b, s = divmod(slot, max_splits)
+    return min(bounds[b][s + 1] - bounds[b][s], SORT_KEYS - 1)

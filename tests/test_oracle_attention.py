@@ -277,3 +277,48 @@ def test_bf16_ulp_matches_page_figures():
     lo, hi = g["printed_range"]
     # the printed range is one ULP on [0.25, 0.5) and one ULP on [0.5, 1)
     assert abs(OB.ulp(0.3) - lo) < 1e-5 and abs(OB.ulp(0.7) - hi) < 1e-4
+
+
+# ---------------------------------------------------------------- second KV source
+
+def _two_source_case(seed=12):
+    rng = np.random.default_rng(seed)
+    B, H, D, Dv = 3, 4, 24, 16
+    q = _bf(rng.standard_normal((B, H, D)))
+    main = _bf(rng.standard_normal((40, 1, D)))
+    extra = _bf(rng.standard_normal((30, 1, D)))
+    lengths = np.array([5, 0, 12])
+    extra_lengths = np.array([3, 7, 0])
+    table = np.stack([rng.permutation(40)[:12] for _ in range(B)]).astype(np.int32)
+    extra_table = np.stack([rng.permutation(30)[:8] for _ in range(B)]).astype(np.int32)
+    return q, main, extra, lengths, extra_lengths, table, extra_table, Dv
+
+
+def test_extra_source_equals_one_concatenated_cache():
+    # the two lists read from two caches == one cache holding both, with the
+    # extra indices offset past the main cache's slots
+    q, main, extra, L, Le, t, te, Dv = _two_source_case()
+    o1, l1 = A.attend(q, main, None, L, scale=0.2, layout=A.INDEXED, table=t, d_v=Dv,
+                      extra_k=extra, extra_table=te, extra_lengths=Le)
+    cat = np.concatenate([main, extra], axis=0)
+    B = q.shape[0]
+    tt = np.full((B, 20), -1, dtype=np.int32)
+    for b in range(B):
+        tt[b, :L[b]] = t[b, :L[b]]
+        tt[b, L[b]:L[b] + Le[b]] = te[b, :Le[b]] + main.shape[0]
+    o2, l2 = A.attend(q, cat, None, L + Le, scale=0.2, layout=A.INDEXED, table=tt, d_v=Dv)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_extra_source_is_the_lse_merge_of_the_two_lists():
+    # attention over main ++ extra == LSE merge of attention over each part
+    q, main, extra, L, Le, t, te, Dv = _two_source_case(13)
+    o, l = A.attend(q, main, None, L, scale=0.3, layout=A.INDEXED, table=t, d_v=Dv,
+                    extra_k=extra, extra_table=te, extra_lengths=Le)
+    om, lm = A.attend(q, main, None, L, scale=0.3, layout=A.INDEXED, table=t, d_v=Dv)
+    oe, le = A.attend(q, extra, None, Le, scale=0.3, layout=A.INDEXED, table=te, d_v=Dv)
+    for b in range(q.shape[0]):
+        for j in range(q.shape[1]):
+            mo, ml = A.lse_merge([(om[b, j], lm[b, j]), (oe[b, j], le[b, j])])
+            assert np.allclose(o[b, j], mo, rtol=0, atol=1e-12)
+            assert (l[b, j] == ml == -np.inf) or abs(l[b, j] - ml) < 1e-12

@@ -11,23 +11,32 @@ FMA = P.VARIANT_CONSTANTS["fma"]
 
 
 def test_invariant_hand_examples():
-    # tile 64, >= 8 tiles per split, <= 64 splits (the FMA variant's constants)
+    # tile 64, >= 16 tiles per split, <= 64 splits (the FMA variant's constants)
     T, mn, mx = FMA
-    assert (T, mn, mx) == (64, 8, 64)
+    assert (T, mn, mx) == (64, 16, 64)
     cases = {
         0: [0, 0],                    # empty row: one empty split
         1: [0, 1],
         64: [0, 1],
-        512: [0, 8],                  # 8 tiles: exactly one minimum split
-        513: [0, 8, 9],               # 9 tiles: a full split and a 1-tile tail
-        4096: list(range(0, 65, 8)),  # 64 tiles -> 8 splits of 8
-        # 2048 tiles: tps = max(8, ceil(2048 / 64)) = 32 -> 64 splits of 32
+        1024: [0, 16],                # 16 tiles: exactly one minimum split
+        1025: [0, 16, 17],            # 17 tiles: a full split and a 1-tile tail
+        4096: list(range(0, 65, 16)), # 64 tiles -> 4 splits of 16
+        # 2048 tiles: tps = max(16, ceil(2048 / 64)) = 32 -> 64 splits of 32
         131072: list(range(0, 2049, 32)),
         # 2049 tiles: tps = ceil(2049 / 64) = 33 -> 63 splits of 33 + 2 tiles
         131073: list(range(0, 2049, 33)) + [2049],
     }
     for L, want in cases.items():
         assert P.plan_invariant([L], T, mn, mx) == [want], L
+
+
+def test_invariant_hand_examples_tensor_core_variant():
+    # tile 64, >= 8 tiles per split, <= 32 splits (the MLA variant's constants)
+    T, mn, mx = P.VARIANT_CONSTANTS["mla"]
+    assert (T, mn, mx) == (64, 8, 32)
+    assert P.plan_invariant([2048], T, mn, mx) == [[0, 8, 16, 24, 32]]
+    assert P.plan_invariant([513], T, mn, mx) == [[0, 8, 9]]
+    assert P.plan_invariant([256], T, mn, mx) == [[0, 4]]
 
 
 def test_invariant_coverage_and_limits():
@@ -96,5 +105,10 @@ def test_balanced_split_depends_on_batchmates():
 
 
 def test_work_list_order():
+    # sizes: row 0 split 0: 1 tile; row 1: 2, 1, 1 tiles; row 2: empty.
+    # Largest first, batch order within a size.
     bounds = [[0, 1], [0, 2, 3, 4], [0, 0]]
-    assert P.work_list(bounds, 64) == [0, 64, 65, 66, 128]
+    assert P.work_list(bounds, 64) == [64, 0, 65, 66, 128]
+    assert [P.work_key(bounds, 64, w) for w in P.work_list(bounds, 64)] == [2, 1, 1, 1, 0]
+    # keys cap at 255
+    assert P.work_list([[0, 300], [0, 400]], 8) == [0, 8]
