@@ -361,11 +361,15 @@ def main():
     torch.cuda.synchronize()
     # inputs smaller than twice L2 are flushed out of it between steps
     flush = kv_bytes < L2_FLUSH_BELOW
+    # the step as a user runs it: no events between its kernels
     with ClockSampler(local) as clocks:
-        total_ms, per_step, split_ms = time_steps(case, args.steps, args.warmup, flush=flush)
+        total_ms, per_step, _ = time_steps(case, args.steps, args.warmup, split_events=False,
+                                           flush=flush)
     total_ms = max_over_ranks(total_ms, dev)
     ms_per_step = total_ms / args.steps
     value = replica_value(kv_bytes, world, ms_per_step) / 1e9
+    # the split kernel alone: events on the launching stream around it
+    _, _, split_ms = time_steps(case, max(20, args.steps // 2), 3, flush=flush)
     split_avg = sum(split_ms) / len(split_ms)
     achieved = alg_bytes / (split_avg * 1e-3) / 1e9
 
@@ -433,8 +437,9 @@ def main():
             n = 20 if name == "long_context" else 200
             # inputs that fit in L2 (the MLA cache is 75.5 MB) are flushed between steps
             fl = w2.kv_bytes() < L2_FLUSH_BELOW
-            ms2, _, sp2 = time_steps(c2, n, 5, flush=fl)
+            ms2, _, _ = time_steps(c2, n, 5, split_events=False, flush=fl)
             ms2 /= n
+            _, _, sp2 = time_steps(c2, n, 3, flush=fl)
             kvb = w2.kv_bytes()
             c2.policy = api.BALANCED
             bms, _, _ = time_steps(c2, n, 5, split_events=False, flush=fl)

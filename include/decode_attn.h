@@ -92,6 +92,11 @@ typedef struct da_problem {
   float scale;           /* softmax scale, applied in fp32 to the fp32 dot    */
   int32_t shared_latent; /* 1: one latent cache, v == NULL, V = K[..., :D_v]  */
   uint32_t flags;        /* reserved, must be 0                               */
+  /* Optional second KV source (the *_extra entry points): an index-gathered */
+  /* cache [extra_num_blocks, H_kv, D] whose entries continue each row's     */
+  /* list after its main entries.  0 / 0 when unused.                         */
+  int32_t extra_width;      /* extra index row width (max extra entries)      */
+  int64_t extra_num_blocks; /* slots in the extra cache                       */
 } da_problem;
 
 /* A plan: filled by decode_attn_plan, read by run/combine.  Host memory,
@@ -110,7 +115,7 @@ typedef struct da_plan {
   int32_t fixed_overhead;      /* BALANCED: tiles charged per split            */
   int32_t grid;                /* persistent CTAs decode_attn_run launches     */
   int32_t device;              /* CUDA device the plan was made on             */
-  int32_t reserved;
+  int32_t has_extra;           /* 1: built by decode_attn_plan_extra           */
   void* ws;                    /* the workspace given to decode_attn_plan      */
   size_t ws_bytes;
   uint64_t off_n_splits;       /* int32[B]: splits of row b                    */
@@ -199,6 +204,34 @@ int decode_attn_forward(const da_problem* prob, int32_t policy, const void* q, c
 int decode_attn_forward_static(const da_problem* prob, int32_t policy, const void* q,
                                const void* k, const void* v, const int32_t* table,
                                const int32_t* lengths, void* out, float* lse, void* stream);
+
+/* The same three steps over two KV sources per row.  Row b attends over its
+ * main list (as above) followed by extra_lengths[b] entries gathered from a
+ * second cache: entry t of that part is extra_k[extra_indices[b, t]] (values
+ * extra_v[...], or the leading D_v dims of extra_k when shared_latent).  This
+ * is the sparse decode call of FlashMLA issue #212 with
+ * extra_indices_in_kvcache / extra_topk_length (Measurement, item 2, and the
+ * Environment's "sparse decode path with extra_k_cache").  The row's split
+ * plan is the INVARIANT (or BALANCED) rule on its total length, so the extra
+ * part changes nothing else: a row's bits still depend only on its own two
+ * lists.  prob->extra_width and prob->extra_num_blocks describe the extra
+ * cache; extra_indices is int32 [B, extra_width]; extra lengths beyond
+ * extra_width are clamped and flagged DA_DEVERR_LENGTH, indices out of
+ * [0, extra_num_blocks) flag DA_DEVERR_INDEX and are not read.  A plan made
+ * by decode_attn_plan_extra must be run by decode_attn_run_extra (and the
+ * other plans by decode_attn_run); anything else is DA_ERR_INVALID_ARG. */
+int decode_attn_plan_extra(const da_problem* prob, int32_t policy, const int32_t* d_lengths,
+                           const int32_t* d_extra_lengths, void* d_ws, size_t ws_bytes,
+                           da_plan* plan, void* stream);
+int decode_attn_run_extra(const da_plan* plan, const void* q, const void* k, const void* v,
+                          const int32_t* table, const int32_t* lengths, const void* extra_k,
+                          const void* extra_v, const int32_t* extra_indices,
+                          const int32_t* extra_lengths, void* out, float* lse, void* stream);
+int decode_attn_forward_extra(const da_problem* prob, int32_t policy, const void* q,
+                              const void* k, const void* v, const int32_t* table,
+                              const int32_t* lengths, const void* extra_k, const void* extra_v,
+                              const int32_t* extra_indices, const int32_t* extra_lengths,
+                              void* d_ws, size_t ws_bytes, void* out, float* lse, void* stream);
 
 /* Synchronise `stream`, then read the device error word (DA_DEVERR_* bits)
  * written since the last decode_attn_plan on this workspace. */

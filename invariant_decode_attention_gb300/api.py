@@ -29,7 +29,8 @@ EXPORTS = (
     "decode_attn_version", "decode_attn_status_string", "decode_attn_split_constants",
     "decode_attn_workspace_bytes", "decode_attn_plan", "decode_attn_run",
     "decode_attn_combine", "decode_attn_forward", "decode_attn_read_error",
-    "decode_attn_copy_plan", "decode_attn_forward_static",
+    "decode_attn_copy_plan", "decode_attn_forward_static", "decode_attn_plan_extra",
+    "decode_attn_run_extra", "decode_attn_forward_extra",
 )
 
 # Size of the fixed device array decode_attn_forward_static uses as scratch.
@@ -50,6 +51,8 @@ class DaProblem(ctypes.Structure):
         ("scale", ctypes.c_float),
         ("shared_latent", ctypes.c_int32),
         ("flags", ctypes.c_uint32),
+        ("extra_width", ctypes.c_int32),
+        ("extra_num_blocks", ctypes.c_int64),
     ]
 
 
@@ -65,7 +68,7 @@ class DaPlan(ctypes.Structure):
         ("fixed_overhead", ctypes.c_int32),
         ("grid", ctypes.c_int32),
         ("device", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("has_extra", ctypes.c_int32),
         ("ws", ctypes.c_void_p),
         ("ws_bytes", ctypes.c_size_t),
         ("off_n_splits", ctypes.c_uint64),
@@ -115,6 +118,13 @@ def lib():
     L.decode_attn_forward.argtypes = [P(DaProblem), i32, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
     L.decode_attn_read_error.restype = ctypes.c_int
     L.decode_attn_read_error.argtypes = [P(DaPlan), P(i32), vp]
+    L.decode_attn_plan_extra.restype = ctypes.c_int
+    L.decode_attn_plan_extra.argtypes = [P(DaProblem), i32, vp, vp, vp, sz, P(DaPlan), vp]
+    L.decode_attn_run_extra.restype = ctypes.c_int
+    L.decode_attn_run_extra.argtypes = [P(DaPlan), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.decode_attn_forward_extra.restype = ctypes.c_int
+    L.decode_attn_forward_extra.argtypes = [P(DaProblem), i32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                            vp, sz, vp, vp, vp]
     L.decode_attn_forward_static.restype = ctypes.c_int
     L.decode_attn_forward_static.argtypes = [P(DaProblem), i32, vp, vp, vp, vp, vp, vp, vp, vp]
     L.decode_attn_copy_plan.restype = ctypes.c_int
@@ -153,21 +163,26 @@ def _stream(stream):
 
 
 def problem(*, batch, num_q_heads, num_kv_heads, head_dim_qk, head_dim_v=None, layout,
-            scale, page_size=0, width=0, num_blocks=0, shared_latent=False) -> DaProblem:
+            scale, page_size=0, width=0, num_blocks=0, shared_latent=False, extra_width=0,
+            extra_num_blocks=0) -> DaProblem:
     """Fill a ``da_problem``.  ``layout`` is a name or a DA_KV_* code."""
     if isinstance(layout, str):
         layout = LAYOUT_CODES[layout]
     return DaProblem(batch, num_q_heads, num_kv_heads, head_dim_qk,
                      head_dim_qk if head_dim_v is None else head_dim_v, layout, page_size,
-                     width, num_blocks, scale, int(bool(shared_latent)), 0)
+                     width, num_blocks, scale, int(bool(shared_latent)), 0, extra_width,
+                     extra_num_blocks)
 
 
 def problem_for(wl) -> DaProblem:
     """The ``da_problem`` of a ``workloads.Workload``."""
+    extra = getattr(wl, "extra_k", None) is not None
     return problem(batch=wl.B, num_q_heads=wl.H_q, num_kv_heads=wl.H_kv, head_dim_qk=wl.D_qk,
                    head_dim_v=wl.D_v, layout=wl.layout, scale=wl.scale,
                    page_size=wl.page_size if wl.layout == "paged" else 0, width=wl.width,
-                   num_blocks=wl.num_blocks, shared_latent=wl.v is None)
+                   num_blocks=wl.num_blocks, shared_latent=wl.v is None,
+                   extra_width=wl.extra_table.shape[1] if extra else 0,
+                   extra_num_blocks=wl.extra_k.shape[0] if extra else 0)
 
 
 def version() -> str:
@@ -249,6 +264,44 @@ def forward_static(prob: DaProblem, policy, q, k, v, table, lengths, out, lse, s
            "forward_static")
 
 
+def plan_extra(prob: DaProblem, policy: int, lengths, extra_lengths, ws, stream=None) -> DaPlan:
+    pl = DaPlan()
+    _check(lib().decode_attn_plan_extra(ctypes.byref(prob), policy,
+                                        _dev_ptr(lengths, "lengths", torch.int32),
+                                        _dev_ptr(extra_lengths, "extra_lengths", torch.int32),
+                                        _dev_ptr(ws, "workspace"), ws.numel() * ws.element_size(),
+                                        ctypes.byref(pl), _stream(stream)), "plan_extra")
+    return pl
+
+
+def run_extra(pl: DaPlan, q, k, v, table, lengths, extra_k, extra_v, extra_indices,
+              extra_lengths, out, lse, stream=None):
+    _check(lib().decode_attn_run_extra(
+        ctypes.byref(pl), _dev_ptr(q, "q", torch.bfloat16), _dev_ptr(k, "k", torch.bfloat16),
+        _dev_ptr(v, "v", torch.bfloat16), _dev_ptr(table, "table", torch.int32),
+        _dev_ptr(lengths, "lengths", torch.int32), _dev_ptr(extra_k, "extra_k", torch.bfloat16),
+        _dev_ptr(extra_v, "extra_v", torch.bfloat16),
+        _dev_ptr(extra_indices, "extra_indices", torch.int32),
+        _dev_ptr(extra_lengths, "extra_lengths", torch.int32),
+        _dev_ptr(out, "out", torch.bfloat16), _dev_ptr(lse, "lse", torch.float32),
+        _stream(stream)), "run_extra")
+
+
+def forward_extra(prob: DaProblem, policy, q, k, v, table, lengths, extra_k, extra_v,
+                  extra_indices, extra_lengths, ws, out, lse, stream=None):
+    """plan + run + combine over a main and a second (index-gathered) KV source."""
+    _check(lib().decode_attn_forward_extra(
+        ctypes.byref(prob), policy, _dev_ptr(q, "q", torch.bfloat16),
+        _dev_ptr(k, "k", torch.bfloat16), _dev_ptr(v, "v", torch.bfloat16),
+        _dev_ptr(table, "table", torch.int32), _dev_ptr(lengths, "lengths", torch.int32),
+        _dev_ptr(extra_k, "extra_k", torch.bfloat16), _dev_ptr(extra_v, "extra_v", torch.bfloat16),
+        _dev_ptr(extra_indices, "extra_indices", torch.int32),
+        _dev_ptr(extra_lengths, "extra_lengths", torch.int32),
+        _dev_ptr(ws, "workspace"), ws.numel() * ws.element_size(),
+        _dev_ptr(out, "out", torch.bfloat16), _dev_ptr(lse, "lse", torch.float32),
+        _stream(stream)), "forward_extra")
+
+
 def read_error(pl: DaPlan, stream=None) -> int:
     code = ctypes.c_int32()
     _check(lib().decode_attn_read_error(ctypes.byref(pl), ctypes.byref(code), _stream(stream)),
@@ -312,5 +365,9 @@ def run_workload(wl, policy=INVARIANT, ws=None, out=None, lse=None, stream=None)
         out = torch.empty((wl.B, wl.H_q, wl.D_v), dtype=torch.bfloat16, device=wl.q.device)
     if lse is None:
         lse = torch.empty((wl.B, wl.H_q), dtype=torch.float32, device=wl.q.device)
-    forward(prob, policy, wl.q, wl.k, wl.v, wl.table, wl.lengths, ws, out, lse, stream)
+    if getattr(wl, "extra_k", None) is not None:
+        forward_extra(prob, policy, wl.q, wl.k, wl.v, wl.table, wl.lengths, wl.extra_k, wl.extra_v,
+                      wl.extra_table, wl.extra_lengths, ws, out, lse, stream)
+    else:
+        forward(prob, policy, wl.q, wl.k, wl.v, wl.table, wl.lengths, ws, out, lse, stream)
     return out, lse

@@ -39,7 +39,9 @@ int check_problem(const da_problem* p) {
   if (p->flags != 0) return DA_ERR_INVALID_ARG;
   if (p->shared_latent != 0 && p->shared_latent != 1) return DA_ERR_INVALID_ARG;
   if (p->shared_latent && p->head_dim_v > p->head_dim_qk) return DA_ERR_INVALID_ARG;
-  if (row_capacity(p->layout, p->width, p->page_size) > 0x7fffffffLL) return DA_ERR_INVALID_ARG;
+  if (p->extra_width < 0 || p->extra_num_blocks < 0) return DA_ERR_INVALID_ARG;
+  if (row_capacity(p->layout, p->width, p->page_size) + p->extra_width > 0x7fffffffLL)
+    return DA_ERR_INVALID_ARG;
   return DA_OK;
 }
 
@@ -205,8 +207,9 @@ int decode_attn_workspace_bytes(const da_problem* prob, size_t* bytes) {
   return DA_OK;
 }
 
-int decode_attn_plan(const da_problem* prob, int32_t policy, const int32_t* d_lengths,
-                     void* d_ws, size_t ws_bytes, da_plan* plan, void* stream) {
+static int plan_impl(const da_problem* prob, int32_t policy, const int32_t* d_lengths,
+                     const int32_t* d_extra_lengths, void* d_ws, size_t ws_bytes, da_plan* plan,
+                     void* stream) {
   int rc = check_problem(prob);
   if (rc != DA_OK) return rc;
   if (!plan || (policy != DA_POLICY_INVARIANT && policy != DA_POLICY_BALANCED))
@@ -245,6 +248,7 @@ int decode_attn_plan(const da_problem* prob, int32_t policy, const int32_t* d_le
   P.fixed_overhead = kBalancedFixedOverhead;
   P.grid = (int)(max_units < slots ? (max_units > 0 ? max_units : 1) : slots);
   P.device = dev;
+  P.has_extra = d_extra_lengths != nullptr;
   P.ws = d_ws;
   P.ws_bytes = ws_bytes;
   P.off_n_splits = L.n_splits;
@@ -259,6 +263,8 @@ int decode_attn_plan(const da_problem* prob, int32_t policy, const int32_t* d_le
   uint8_t* ws = static_cast<uint8_t*>(d_ws);
   PlanLaunch pl;
   pl.lengths = d_lengths;
+  pl.extra_lengths = d_extra_lengths;
+  pl.extra_capacity = prob->extra_width;
   pl.hdr = reinterpret_cast<int32_t*>(ws);
   pl.n_splits = reinterpret_cast<int32_t*>(ws + L.n_splits);
   pl.split_begin = reinterpret_cast<int32_t*>(ws + L.split_begin);
@@ -276,13 +282,37 @@ int decode_attn_plan(const da_problem* prob, int32_t policy, const int32_t* d_le
   return DA_OK;
 }
 
-int decode_attn_run(const da_plan* plan, const void* q, const void* k, const void* v,
-                    const int32_t* table, const int32_t* lengths, void* out, float* lse,
-                    void* stream) {
+int decode_attn_plan(const da_problem* prob, int32_t policy, const int32_t* d_lengths,
+                     void* d_ws, size_t ws_bytes, da_plan* plan, void* stream) {
+  return plan_impl(prob, policy, d_lengths, nullptr, d_ws, ws_bytes, plan, stream);
+}
+
+int decode_attn_plan_extra(const da_problem* prob, int32_t policy, const int32_t* d_lengths,
+                           const int32_t* d_extra_lengths, void* d_ws, size_t ws_bytes,
+                           da_plan* plan, void* stream) {
+  if (!prob || prob->extra_width < 1) return DA_ERR_INVALID_ARG;
+  if (prob->batch > 0 && !d_extra_lengths) return DA_ERR_INVALID_ARG;
+  static const int32_t dummy = 0;  // B = 0: any non-null marker will do
+  return plan_impl(prob, policy, d_lengths, prob->batch > 0 ? d_extra_lengths : &dummy, d_ws,
+                   ws_bytes, plan, stream);
+}
+
+static int run_impl(const da_plan* plan, const void* q, const void* k, const void* v,
+                    const int32_t* table, const int32_t* lengths, const void* extra_k,
+                    const void* extra_v, const int32_t* extra_indices,
+                    const int32_t* extra_lengths, void* out, float* lse, void* stream) {
   int rc = check_plan(plan);
   if (rc != DA_OK) return rc;
   const da_problem& pr = plan->prob;
+  if ((extra_k != nullptr) != (plan->has_extra != 0)) return DA_ERR_INVALID_ARG;
   if (pr.batch == 0) return DA_OK;
+  if (extra_k) {
+    if (!extra_indices || !extra_lengths || (!pr.shared_latent && !extra_v))
+      return DA_ERR_INVALID_ARG;
+    if (!aligned(extra_k, 16) || (extra_v && !aligned(extra_v, 16)) ||
+        !aligned(extra_indices, 4) || !aligned(extra_lengths, 4))
+      return DA_ERR_INVALID_ARG;
+  }
   if (!q || !k || !lengths || !out || !lse) return DA_ERR_INVALID_ARG;
   if (!pr.shared_latent && !v) return DA_ERR_INVALID_ARG;
   if (pr.layout != DA_KV_CONTIGUOUS && !table) return DA_ERR_INVALID_ARG;
@@ -297,10 +327,34 @@ int decode_attn_run(const da_plan* plan, const void* q, const void* k, const voi
   L.lengths = lengths;
   L.out = static_cast<__nv_bfloat16*>(out);
   L.lse = lse;
+  if (extra_k) {
+    L.extra_k = static_cast<const __nv_bfloat16*>(extra_k);
+    L.extra_v = static_cast<const __nv_bfloat16*>(pr.shared_latent ? extra_k : extra_v);
+    L.extra_table = extra_indices;
+    L.extra_lengths = extra_lengths;
+    L.extra_num_blocks = pr.extra_num_blocks;
+    L.extra_width = pr.extra_width;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const cudaError_t e = (plan->variant == DA_VARIANT_MLA) ? launch_split_mla(L, plan->grid, s)
                                                           : launch_split_fma(L, plan->grid, s);
   return e == cudaSuccess ? DA_OK : DA_ERR_CUDA;
+}
+
+int decode_attn_run(const da_plan* plan, const void* q, const void* k, const void* v,
+                    const int32_t* table, const int32_t* lengths, void* out, float* lse,
+                    void* stream) {
+  return run_impl(plan, q, k, v, table, lengths, nullptr, nullptr, nullptr, nullptr, out, lse,
+                  stream);
+}
+
+int decode_attn_run_extra(const da_plan* plan, const void* q, const void* k, const void* v,
+                          const int32_t* table, const int32_t* lengths, const void* extra_k,
+                          const void* extra_v, const int32_t* extra_indices,
+                          const int32_t* extra_lengths, void* out, float* lse, void* stream) {
+  if (!extra_k) return DA_ERR_INVALID_ARG;
+  return run_impl(plan, q, k, v, table, lengths, extra_k, extra_v, extra_indices, extra_lengths,
+                  out, lse, stream);
 }
 
 int decode_attn_combine(const da_plan* plan, void* out, float* lse, void* stream) {
@@ -322,6 +376,21 @@ int decode_attn_forward(const da_problem* prob, int32_t policy, const void* q, c
   int rc = decode_attn_plan(prob, policy, lengths, d_ws, ws_bytes, &plan, stream);
   if (rc != DA_OK) return rc;
   rc = decode_attn_run(&plan, q, k, v, table, lengths, out, lse, stream);
+  if (rc != DA_OK) return rc;
+  return decode_attn_combine(&plan, out, lse, stream);
+}
+
+int decode_attn_forward_extra(const da_problem* prob, int32_t policy, const void* q,
+                              const void* k, const void* v, const int32_t* table,
+                              const int32_t* lengths, const void* extra_k, const void* extra_v,
+                              const int32_t* extra_indices, const int32_t* extra_lengths,
+                              void* d_ws, size_t ws_bytes, void* out, float* lse, void* stream) {
+  da_plan plan;
+  int rc = decode_attn_plan_extra(prob, policy, lengths, extra_lengths, d_ws, ws_bytes, &plan,
+                                  stream);
+  if (rc != DA_OK) return rc;
+  rc = decode_attn_run_extra(&plan, q, k, v, table, lengths, extra_k, extra_v, extra_indices,
+                             extra_lengths, out, lse, stream);
   if (rc != DA_OK) return rc;
   return decode_attn_combine(&plan, out, lse, stream);
 }

@@ -25,6 +25,7 @@ static_assert(kMaxSplitsAny <= 64, "two split weights per lane of warp 0");
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Launch p) {
   __shared__ float coef[kMaxSplitsAny];
   __shared__ float lse_out;
+  wait_prior_grid();  // the split kernel's partials
   const int b = blockIdx.x / p.H_q, j = blockIdx.x % p.H_q;
   const int n = p.n_splits[b];
   if (n <= 1) return;  // written final by the split kernel
@@ -75,8 +76,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Launch p) {
 cudaError_t launch_combine(const Launch& p, cudaStream_t stream) {
   const long long blocks = (long long)p.B * p.H_q;
   if (blocks == 0) return cudaSuccess;
-  combine_kernel<<<(unsigned)blocks, kCombineThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_after(combine_kernel, dim3((unsigned)blocks), dim3(kCombineThreads), 0, stream, p);
 }
 
 }  // namespace da

@@ -15,7 +15,7 @@ namespace da {
 // tokens per tile, minimum tiles per split, maximum splits per row.
 // ---------------------------------------------------------------------------
 constexpr int kFmaTile = 64;
-constexpr int kFmaMinTilesPerSplit = 8;
+constexpr int kFmaMinTilesPerSplit = 16;
 constexpr int kFmaMaxSplits = 64;
 
 constexpr int kMlaTile = 64;
@@ -53,6 +53,14 @@ struct Launch {
   float* lse_part;
   float* o_part;
   long long num_blocks;
+  // optional second, index-gathered KV source continuing each row's list
+  // (extra_k == nullptr: none)
+  const __nv_bfloat16* extra_k;
+  const __nv_bfloat16* extra_v;
+  const int32_t* extra_table;
+  const int32_t* extra_lengths;
+  long long extra_num_blocks;
+  int extra_width;
   int B, H_q, H_kv, D_qk, D_v;
   int layout, page_size, width, capacity;
   int page_shift;  // log2(page_size) when it is a power of two, else -1
@@ -62,14 +70,34 @@ struct Launch {
 
 struct PlanLaunch {
   const int32_t* lengths;
+  const int32_t* extra_lengths;  // nullptr: no second source
   int32_t* hdr;
   int32_t* n_splits;
   int32_t* split_begin;
   int32_t* work;
   int32_t* item_desc;
-  int B, tile, min_tps, max_splits, capacity;
+  int B, tile, min_tps, max_splits, capacity, extra_capacity;
   int policy, num_parts, fixed_overhead;
 };
+
+// Launch `kernel` on `stream` so that it may be scheduled while the previous
+// kernel on the stream is still running (programmatic dependent launch); the
+// kernel calls wait_prior_grid() before reading that kernel's results.
+template <typename... Args>
+inline cudaError_t launch_after(void (*kernel)(Args...), dim3 grid, dim3 block, size_t smem,
+                                cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 
 // Host launchers (each in its own translation unit).
 cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t stream);
@@ -242,6 +270,20 @@ __device__ __forceinline__ bool named_bar_or(int id, int n, bool pred) {
       : "r"((uint32_t)pred), "r"(id), "r"(n)
       : "memory");
   return r != 0;
+}
+
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start before the previous kernel on the stream ends; it
+// must wait here before touching anything that kernel writes.  Without such
+// a predecessor the wait returns at once.
+__device__ __forceinline__ void wait_prior_grid() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Let the next kernel on the stream (if launched with programmatic stream
+// serialisation) be scheduled now; it still waits for this grid to finish.
+__device__ __forceinline__ void allow_next_grid() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ void set_error(int32_t* hdr, int bits) {

@@ -3,8 +3,9 @@
 // INVARIANT: the split count and boundaries of a row come from its own length
 // and compile-time constants -- the opt-in mode proposed in "Sparse MLA decode
 // is not batch-invariant" (FlashMLA issue #212, section "Question").  The
-// batch enters only through the work list (a prefix sum that places items; it
-// changes where a split runs, never what it computes).
+// batch enters only through the work list (which items exist and in which
+// order the persistent CTAs take them); it changes where a split runs, never
+// what it computes.
 //
 // BALANCED: the batch-wide quota of the same page's "Where it comes from"
 // section -- payload = ceil(total / parts) + fixed overhead, with total summed
@@ -19,10 +20,25 @@ constexpr int kPlanThreads = 1024;
 
 __device__ __forceinline__ int ceil_div_i(int a, int b) { return a / b + (a % b != 0); }
 
+// A row's list length: its main entries plus, when a second source is given,
+// its extra entries (each part clamped to its own capacity).
 __device__ __forceinline__ int row_length(const PlanLaunch& p, int b) {
   const int L = p.lengths[b];
-  const int Lc = clamp_len(L, p.capacity);
-  if (Lc != L) set_error(p.hdr, DA_DEVERR_LENGTH);
+  int Lc = clamp_len(L, p.capacity);
+  bool bad = Lc != L;
+  if (p.extra_lengths) {
+    const int Le = p.extra_lengths[b];
+    const int Lec = clamp_len(Le, p.extra_capacity);
+    bad |= Lec != Le;
+    Lc += Lec;
+  }
+  if (bad) set_error(p.hdr, DA_DEVERR_LENGTH);
+  return Lc;
+}
+
+__device__ __forceinline__ int row_length_quiet(const PlanLaunch& p, int b) {
+  int Lc = clamp_len(p.lengths[b], p.capacity);
+  if (p.extra_lengths) Lc += clamp_len(p.extra_lengths[b], p.extra_capacity);
   return Lc;
 }
 
@@ -54,41 +70,66 @@ __device__ int block_exclusive_scan(int x, int* total) {
   return warp_base + incl - x;
 }
 
+// Work-list order: items with more tiles first (bucket key = tile count,
+// capped at kSortKeys - 1), so that the round-robin placement of persistent
+// CTAs hands out the long items before the short ones.  Placement only: an
+// item's arithmetic never depends on where it lands in the list.
+constexpr int kSortKeys = 256;
+
+__device__ __forceinline__ int sort_key(int tiles) { return min(tiles, kSortKeys - 1); }
+
 __global__ void __launch_bounds__(kPlanThreads) plan_invariant_kernel(PlanLaunch p) {
+  __shared__ int bucket[kSortKeys];
+  allow_next_grid();  // the split kernel may be staged now; it waits for us
   if (threadIdx.x == 0) p.hdr[kHdrError] = 0;
+  for (int k = threadIdx.x; k < kSortKeys; k += kPlanThreads) bucket[k] = 0;
   __syncthreads();
   const int stride = p.max_splits + 1;
-  int work_base = 0;
-  for (int base = 0; base < p.B; base += kPlanThreads) {
-    const int b = base + threadIdx.x;
-    int n = 0, n_tiles = 0, tps = 1;
-    if (b < p.B) {
-      const int L = row_length(p, b);
-      n_tiles = ceil_div_i(L, p.tile);
-      tps = max(p.min_tps, ceil_div_i(n_tiles, p.max_splits));
-      n = max(1, ceil_div_i(n_tiles, tps));
-      p.n_splits[b] = n;
-      int32_t* sb = p.split_begin + (size_t)b * stride;
-      for (int s = 0; s < n; ++s) sb[s] = min(s * tps, n_tiles);
-      sb[n] = n_tiles;
+  // pass 1: every row's splits; count items per key
+  for (int b = threadIdx.x; b < p.B; b += kPlanThreads) {
+    const int L = row_length(p, b);
+    const int n_tiles = ceil_div_i(L, p.tile);
+    const int tps = max(p.min_tps, ceil_div_i(n_tiles, p.max_splits));
+    const int n = max(1, ceil_div_i(n_tiles, tps));
+    p.n_splits[b] = n;
+    int32_t* sb = p.split_begin + (size_t)b * stride;
+    for (int s = 0; s < n; ++s) sb[s] = min(s * tps, n_tiles);
+    sb[n] = n_tiles;
+    const int last = n_tiles - (n - 1) * tps;  // tiles of the last split
+    if (n > 1) atomicAdd(&bucket[sort_key(tps)], n - 1);
+    atomicAdd(&bucket[sort_key(last)], 1);
+  }
+  __syncthreads();
+  // bucket starts, largest key first (thread 0: 256 entries)
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int k = kSortKeys - 1; k >= 0; --k) {
+      const int c = bucket[k];
+      bucket[k] = acc;
+      acc += c;
     }
-    int total;
-    const int off = block_exclusive_scan(n, &total);
-    const int Lc = (b < p.B) ? clamp_len(p.lengths[b], p.capacity) : 0;
+    p.hdr[kHdrNWork] = acc;
+  }
+  __syncthreads();
+  // pass 2: place every item in its bucket (order within a bucket is free)
+  for (int b = threadIdx.x; b < p.B; b += kPlanThreads) {
+    const int n = p.n_splits[b];
+    const int32_t* sb = p.split_begin + (size_t)b * stride;
+    const int Lc = row_length_quiet(p, b);
     for (int s = 0; s < n; ++s) {
       const int slot = b * p.max_splits + s;
-      p.work[work_base + off + s] = slot;
-      reinterpret_cast<int4*>(p.item_desc)[work_base + off + s] =
-          make_int4(n == 1 ? ~slot : slot, min(s * tps, n_tiles), min((s + 1) * tps, n_tiles), Lc);
+      const int pos = atomicAdd(&bucket[sort_key(sb[s + 1] - sb[s])], 1);
+      p.work[pos] = slot;
+      reinterpret_cast<int4*>(p.item_desc)[pos] =
+          make_int4(n == 1 ? ~slot : slot, sb[s], sb[s + 1], Lc);
     }
-    work_base += total;
   }
-  if (threadIdx.x == 0) p.hdr[kHdrNWork] = work_base;
 }
 
 // One thread: the packing is sequential by definition (each row's cuts depend
 // on how full the current part is after every earlier row).
 __global__ void plan_balanced_kernel(PlanLaunch p) {
+  allow_next_grid();
   if (threadIdx.x != 0) return;
   p.hdr[kHdrError] = 0;
   const int stride = p.max_splits + 1;
@@ -100,7 +141,7 @@ __global__ void plan_balanced_kernel(PlanLaunch p) {
   long long room = payload;
   int n_work = 0;
   for (int b = 0; b < p.B; ++b) {
-    const int n_tiles = ceil_div_i(clamp_len(p.lengths[b], p.capacity), p.tile);
+    const int n_tiles = ceil_div_i(row_length_quiet(p, b), p.tile);
     int32_t* sb = p.split_begin + (size_t)b * stride;
     int n_cuts = 1;  // entries written to sb so far
     sb[0] = 0;
@@ -125,15 +166,35 @@ __global__ void plan_balanced_kernel(PlanLaunch p) {
     }
     sb[n_cuts] = n_tiles;
     p.n_splits[b] = n_cuts;
-    const int Lc = clamp_len(p.lengths[b], p.capacity);
-    for (int s = 0; s < n_cuts; ++s) {
-      const int slot = b * p.max_splits + s;
-      reinterpret_cast<int4*>(p.item_desc)[n_work] =
-          make_int4(n_cuts == 1 ? ~slot : slot, sb[s], sb[s + 1], Lc);
-      p.work[n_work++] = slot;
-    }
+    n_work += n_cuts;
   }
   p.hdr[kHdrNWork] = n_work;
+  // work list: largest items first, rows and splits in order within a key
+  // (a stable counting sort; placement only, as for INVARIANT)
+  __shared__ int start[kSortKeys];
+  for (int k = 0; k < kSortKeys; ++k) start[k] = 0;
+  for (int b = 0; b < p.B; ++b) {
+    const int32_t* sb = p.split_begin + (size_t)b * stride;
+    for (int s = 0; s < p.n_splits[b]; ++s) ++start[sort_key(sb[s + 1] - sb[s])];
+  }
+  int acc = 0;
+  for (int k = kSortKeys - 1; k >= 0; --k) {
+    const int c = start[k];
+    start[k] = acc;
+    acc += c;
+  }
+  for (int b = 0; b < p.B; ++b) {
+    const int n = p.n_splits[b];
+    const int32_t* sb = p.split_begin + (size_t)b * stride;
+    const int Lc = row_length_quiet(p, b);
+    for (int s = 0; s < n; ++s) {
+      const int slot = b * p.max_splits + s;
+      const int pos = start[sort_key(sb[s + 1] - sb[s])]++;
+      reinterpret_cast<int4*>(p.item_desc)[pos] =
+          make_int4(n == 1 ? ~slot : slot, sb[s], sb[s + 1], Lc);
+      p.work[pos] = slot;
+    }
+  }
 }
 
 }  // namespace

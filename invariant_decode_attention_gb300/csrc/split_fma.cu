@@ -57,6 +57,7 @@ struct FmaShape {
 // A work unit as the kernel sees it: the plan's item descriptor plus a head.
 struct Unit {
   int slot, tb, te, L, b, h;
+  int l_main;  // entries before the second source starts
   bool single;
 };
 
@@ -64,6 +65,9 @@ __device__ __forceinline__ int4 load_desc(const Launch& p, int u) {
   return __ldg(reinterpret_cast<const int4*>(p.item_desc) + u / p.H_kv);
 }
 
+// X: the call has a second KV source (a separate instantiation, so that the
+// single-source loop carries none of its checks).
+template <bool X>
 __device__ __forceinline__ Unit make_unit(const Launch& p, int u, int4 d) {
   Unit x;
   x.single = d.x < 0;
@@ -73,11 +77,22 @@ __device__ __forceinline__ Unit make_unit(const Launch& p, int u, int4 d) {
   x.L = d.w;
   x.b = x.slot / p.max_splits;
   x.h = u % p.H_kv;
+  x.l_main = X ? clamp_len(__ldg(p.lengths + x.b), p.capacity) : 0x7fffffff;
   return x;
 }
 
-// Cache row (in units of [H_kv, D] records) holding entry `tok` of row b.
-__device__ __forceinline__ bool entry_row(const Launch& p, int b, int tok, long long* row) {
+// Cache row (in units of [H_kv, D] records) holding entry `tok` of row b;
+// entries from l_main on come from the second source (*src = 1).
+template <bool X>
+__device__ __forceinline__ bool entry_row(const Launch& p, int b, int tok, int l_main,
+                                          long long* row, int* src) {
+  *src = 0;
+  if (X && tok >= l_main) {
+    const int slot = __ldg(p.extra_table + (size_t)b * p.extra_width + (tok - l_main));
+    *row = slot;
+    *src = 1;
+    return slot >= 0 && slot < p.extra_num_blocks;
+  }
   if (p.layout == DA_KV_CONTIGUOUS) {
     *row = (long long)b * p.width + tok;
     return true;
@@ -101,6 +116,7 @@ struct Cursor {
   bool valid;
 };
 
+template <bool X>
 __device__ __forceinline__ void cursor_seek(const Launch& p, Cursor& c, int u, int4 d,
                                             int n_units) {
   for (;;) {
@@ -115,20 +131,21 @@ __device__ __forceinline__ void cursor_seek(const Launch& p, Cursor& c, int u, i
     d = c.next;
   }
   c.u = u;
-  c.x = make_unit(p, u, d);
+  c.x = make_unit<X>(p, u, d);
   c.k = c.x.tb;
   c.valid = true;
 }
 
+template <bool X>
 __device__ __forceinline__ void cursor_next(const Launch& p, Cursor& c, int n_units) {
   if (!c.valid) return;
   if (++c.k < c.x.te) return;
-  cursor_seek(p, c, c.u + gridDim.x, c.next, n_units);
+  cursor_seek<X>(p, c, c.u + gridDim.x, c.next, n_units);
 }
 
 // Issue this warp's copies for the cursor's tile into ring slot `slot`, then
 // close the cp.async group (always, so group counting stays uniform).
-template <int G, int D>
+template <int G, int D, bool X>
 __device__ __forceinline__ void load_slice(const Launch& p, const Cursor& c, uint8_t* smem,
                                            int slot, int warp, int lane) {
   using S = FmaShape<G, D>;
@@ -141,7 +158,8 @@ __device__ __forceinline__ void load_slice(const Launch& p, const Cursor& c, uin
     // 16 entries in consecutive cache rows: one page lookup per slice.
     bool uniform = false, base_ok = true;
     long long base_row = 0;
-    if (t0 < c.x.L) {
+    // (only when every live entry of the slice comes from the main source)
+    if (t0 < c.x.L && (!X || min(t0 + S::kTokPerWarp, c.x.L) <= c.x.l_main)) {
       if (p.layout == DA_KV_CONTIGUOUS) {
         uniform = true;
         base_row = (long long)c.x.b * p.width + t0;
@@ -160,15 +178,18 @@ __device__ __forceinline__ void load_slice(const Launch& p, const Cursor& c, uin
       const int tok = t0 + tl;
       if (tok < c.x.L) {
         long long row = base_row + tl;
-        const bool ok = uniform ? base_ok : entry_row(p, c.x.b, tok, &row);
+        int src = 0;
+        const bool ok = uniform ? base_ok : entry_row<X>(p, c.x.b, tok, c.x.l_main, &row, &src);
         bad |= !ok;
         if (ok) {
           const size_t off = ((size_t)row * p.H_kv + c.x.h) * D;
+          const __nv_bfloat16* kb = (X && src) ? p.extra_k : p.k;
+          const __nv_bfloat16* vb = (X && src) ? p.extra_v : p.v;
 #pragma unroll
           for (int ch = 0; ch < S::kChunks; ++ch) {
             const int e = (sub + 8 * ch) * 8;  // element offset of this 16-byte chunk
-            cp_async16(smem_addr(ks + tl * S::kRowBytes + e * 2), p.k + off + e);
-            cp_async16(smem_addr(vs + tl * S::kRowBytes + e * 2), p.v + off + e);
+            cp_async16(smem_addr(ks + tl * S::kRowBytes + e * 2), kb + off + e);
+            cp_async16(smem_addr(vs + tl * S::kRowBytes + e * 2), vb + off + e);
           }
         }
       }
@@ -363,30 +384,32 @@ __device__ __forceinline__ void consume_slice(const uint8_t* ks, int lane, int n
   }
 }
 
-template <int G, int D>
+template <int G, int D, bool X>
 __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Launch p) {
   using S = FmaShape<G, D>;
   extern __shared__ __align__(128) uint8_t smem[];
   float* scratch = reinterpret_cast<float*>(smem + S::kScratchOffset);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = lane >> 3, sub = lane & 7;
+  wait_prior_grid();  // the plan kernel's outputs
+  allow_next_grid();
   const int n_units = p.hdr[kHdrNWork] * p.H_kv;
   if ((int)blockIdx.x >= n_units) return;  // uniform across the CTA
 
   // prologue: fill kStages - 1 slots
   Cursor pf;
-  cursor_seek(p, pf, blockIdx.x, load_desc(p, blockIdx.x), n_units);
+  cursor_seek<X>(p, pf, blockIdx.x, load_desc(p, blockIdx.x), n_units);
 #pragma unroll
   for (int s = 0; s < S::kStages - 1; ++s) {
-    load_slice<G, D>(p, pf, smem, s, warp, lane);
-    cursor_next(p, pf, n_units);
+    load_slice<G, D, X>(p, pf, smem, s, warp, lane);
+    cursor_next<X>(p, pf, n_units);
   }
 
   int slot = 0;
   uint64_t q2[G][S::kDpl / 2];
   int4 d_next = load_desc(p, blockIdx.x);
   for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-    const Unit x = make_unit(p, u, d_next);
+    const Unit x = make_unit<X>(p, u, d_next);
     if (u + (int)gridDim.x < n_units) d_next = load_desc(p, u + gridDim.x);
     float m[G], l[G];
     uint64_t acc2[G][S::kDpl / 2];
@@ -411,8 +434,8 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
         named_bar_sync(1, S::kThreads);
       }
       // refill the slot consumed in the previous iteration
-      load_slice<G, D>(p, pf, smem, (slot + S::kStages - 1) % S::kStages, warp, lane);
-      cursor_next(p, pf, n_units);
+      load_slice<G, D, X>(p, pf, smem, (slot + S::kStages - 1) % S::kStages, warp, lane);
+      cursor_next<X>(p, pf, n_units);
       const uint8_t* ks = smem + (slot * S::kWarps + warp) * S::kWarpSlotBytes;
       const int n_valid = min(S::kTokPerWarp, x.L - k * S::kTile - warp * S::kTokPerWarp);
       if (n_valid >= S::kTokPerWarp)
@@ -509,24 +532,29 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
   cp_async_wait<0>();  // leave no copy in flight
 }
 
-template <int G, int D>
-cudaError_t launch_one(const Launch& p, int grid, cudaStream_t stream) {
+template <int G, int D, bool X>
+cudaError_t launch_x(const Launch& p, int grid, cudaStream_t stream) {
   using S = FmaShape<G, D>;
   static const cudaError_t attr = cudaFuncSetAttribute(
-      split_fma_kernel<G, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+      split_fma_kernel<G, D, X>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
   if (attr != cudaSuccess) return attr;
-  split_fma_kernel<G, D><<<grid, S::kThreads, S::kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  return launch_after(split_fma_kernel<G, D, X>, dim3(grid), dim3(S::kThreads), S::kSmemBytes,
+                      stream, p);
+}
+
+template <int G, int D>
+cudaError_t launch_one(const Launch& p, int grid, cudaStream_t stream) {
+  return p.extra_k ? launch_x<G, D, true>(p, grid, stream) : launch_x<G, D, false>(p, grid, stream);
 }
 
 template <int G, int D>
 int ctas_one() {
   using S = FmaShape<G, D>;
   static int n = [] {
-    cudaFuncSetAttribute(split_fma_kernel<G, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         S::kSmemBytes);
+    cudaFuncSetAttribute(split_fma_kernel<G, D, false>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
     int c = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, split_fma_kernel<G, D>, S::kThreads,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, split_fma_kernel<G, D, false>, S::kThreads,
                                                       S::kSmemBytes) != cudaSuccess)
       c = 1;
     return c < 1 ? 1 : c;

@@ -4,7 +4,7 @@
 // issue #212 -- reports on).
 //
 // Both contractions run on tcgen05 tensor cores with fp32 accumulators in
-// tensor memory:
+// tensor memory (TMEM):
 //     S = Q K^T      M = 128 heads, N = 32 entries, K = 576   (36 MMAs of K=16)
 //     O += P V_half  M = 128 heads, N = 256 dims,   K = 32    (2 MMAs)
 // O for 128 heads x 512 dims in fp32 would fill all of one SM's tensor memory,
@@ -12,18 +12,26 @@
 // each unit computes the full S itself (the same instructions on the same
 // data, so both halves see the same bits).
 //
+// Operand placement.  The first 384 dims of Q live in TMEM (192 columns) and
+// feed 24 of the 36 S MMAs as the A operand, so those read only the K tile
+// from shared memory; dims 384..575 of Q stay in shared memory (48 KB).  TMEM
+// columns: Q [0,192), S as two K-half partial accumulators [192,224) and
+// [224,256) (two independent MMA chains), O [256,512).
+// Shared memory: Q tail, four 32-entry KV stages (36 KB each), P (8 KB).
+//
 // Roles inside a CTA (288 threads):
-//   warps 0-3  softmax: thread i owns head i = tensor-memory lane i.  It reads
-//              its row of S, keeps the running max and sum in fp32, writes P
-//              (bf16) into shared memory and rescales its row of O when the
-//              max it uses moves by more than 2^8.
+//   warps 0-3  softmax: thread i owns head i = TMEM lane i.  It loads its row
+//              of Q into TMEM at the start of a unit, reads its row of S,
+//              keeps the running max and sum in fp32, writes P (bf16) into
+//              shared memory and rescales its row of O when the max it uses
+//              moves by more than 2^8.
 //   warps 4-7  producer: gathers each entry's 1152-byte latent row with
 //              16-byte cp.async into the 128-byte-swizzled K-major layout the
-//              tensor core reads (and the unit's Q at its start).
-//   warp 8     MMA issue (one thread) and tensor-memory allocation.
+//              tensor core reads (and the unit's Q tail at its start).
+//   warp 8     MMA issue (one thread) and TMEM allocation.
 // Every wait on an mbarrier is bounded; on time-out the kernel records
 // DA_DEVERR_TIMEOUT, every role leaves its loop, outstanding tensor-core work
-// is drained (bounded) and tensor memory is freed.
+// is drained (bounded) and TMEM is freed.
 #include "common.cuh"
 #include "tcgen05.cuh"
 
@@ -33,28 +41,36 @@ namespace {
 constexpr int kHeads = 128;       // MMA M (query heads, zero-padded)
 constexpr int kDqk = 576;
 constexpr int kDvHalf = 256;      // value dims per unit
-constexpr int kSub = 32;          // entries per sub-tile
+constexpr int kSub = 64;          // entries per sub-tile (MMA N of S, K of P.V)
 constexpr int kRegions = kDqk / 64;  // 64-dim swizzle regions of a row
 constexpr int kRowChunks = kDqk / 8; // 16-byte chunks of a row (72)
+constexpr int kQT = 384;          // dims of Q held in TMEM (A operand)
+constexpr int kQTCols = kQT / 2;  // 192 TMEM columns (two bf16 per column)
+constexpr int kQSRegions = (kDqk - kQT) / 64;  // 3 smem regions of Q (dims 384..575)
+constexpr int kStages = 2;
 
 // shared memory map (bytes)
-constexpr int kQBytes = kRegions * kHeads * 128;           // 147456
-constexpr int kStageRegion = kSub * 128;                    // 4096
-constexpr int kStageBytes = kRegions * kStageRegion;        // 36864
-constexpr int kStageOffset = kQBytes;
-constexpr int kPOffset = kStageOffset + 2 * kStageBytes;    // 221184
-constexpr int kPBytes = kHeads * kSub * 2;                  // 8192 (64-byte swizzle)
-constexpr int kBarOffset = kPOffset + kPBytes;              // 229376
-enum { kFull0 = 0, kFull1, kEmpty0, kEmpty1, kSFull0, kSFull1, kSFree0, kSFree1,
-       kPFull, kODone, kOFree, kQFull, kQFree, kDrain, kNumBars };
+constexpr int kQSBytes = kQSRegions * kHeads * 128;        // 49152
+constexpr int kStageRegion = kSub * 128;                    // 8192
+constexpr int kStageBytes = kRegions * kStageRegion;        // 73728
+constexpr int kStageOffset = kQSBytes;
+constexpr int kPOffset = kStageOffset + kStages * kStageBytes;  // 196608
+constexpr int kPBytes = kHeads * kSub * 2;                  // 16384 (128-byte swizzle)
+constexpr int kBarOffset = kPOffset + kPBytes;              // 212992
+enum { kFull0 = 0, kEmpty0 = kFull0 + kStages, kSFull = kEmpty0 + kStages, kSFree, kPFull,
+       kODone, kOFree, kQFull, kQTFull, kQFree, kDrain, kNumBars };
 constexpr int kTmemSlot = kBarOffset + kNumBars * 8;
+static_assert(kPOffset % 1024 == 0 && kStageOffset % 1024 == 0, "swizzle atoms 1024-aligned");
 constexpr int kAbortSlot = kTmemSlot + 4;
 constexpr int kSmemBytes = kAbortSlot + 12;
 static_assert(kSmemBytes <= 232448, "fits the 227 KB per-block limit");
 
 constexpr int kThreads = 288;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kOCol = 256;   // O accumulator columns [256, 512)
+constexpr uint32_t kSCol = kQTCols;  // S partial accumulators at [192, 256)
+constexpr int kKSteps = kDqk / 16;   // 36 MMAs of K = 16 per S tile
+constexpr int kEntPerWarp = kSub / 4;  // entries each producer warp gathers
+constexpr uint32_t kOCol = 256;      // O accumulator columns [256, 512)
 constexpr float kRescaleLog2 = 8.f;
 
 constexpr uint32_t kIdescS = umma::idesc_bf16_f32(kHeads, kSub, false);
@@ -106,6 +122,7 @@ __device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity) {
 // A unit: one half of the value dims of one (row, split) item.
 struct MlaUnit {
   int slot, b, half, t_begin, t_end;  // entry range [t_begin, t_end)
+  int l_main;                         // entries before the second source starts
   bool single, empty;
 };
 
@@ -119,11 +136,21 @@ __device__ __forceinline__ MlaUnit mla_unit(const Launch& p, int u) {
   x.t_begin = d.y * kMlaTile;
   x.t_end = min(d.z * kMlaTile, d.w);
   x.empty = x.t_end <= x.t_begin;
+  x.l_main = p.extra_k ? clamp_len(__ldg(p.lengths + x.b), p.capacity) : 0x7fffffff;
   return x;
 }
 
-// Latent-cache row holding entry `tok` of row b (H_kv = 1).
-__device__ __forceinline__ bool latent_row(const Launch& p, int b, int tok, long long* row) {
+// Latent-cache row holding entry `tok` of row b (H_kv = 1); entries from
+// l_main on come from the second source (*src = 1).
+__device__ __forceinline__ bool latent_row(const Launch& p, int b, int tok, int l_main,
+                                           long long* row, int* src) {
+  *src = 0;
+  if (tok >= l_main) {
+    const int slot = __ldg(p.extra_table + (size_t)b * p.extra_width + (tok - l_main));
+    *row = slot;
+    *src = 1;
+    return slot >= 0 && slot < p.extra_num_blocks;
+  }
   if (p.layout == DA_KV_CONTIGUOUS) {
     *row = (long long)b * p.width + tok;
     return true;
@@ -153,36 +180,49 @@ __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
   for (int u = blockIdx.x; u < n_units && alive; u += gridDim.x) {
     const MlaUnit x = mla_unit(p, u);
     if (x.empty) continue;
-    // Q of row b (zero rows past H_q), once the previous unit's S MMAs are done
+    // Q dims 384..575 of row b (zero rows past H_q) into shared memory, once
+    // the previous unit's S MMAs are done
     if (!wait_bar(c, kQFree, (n_ne & 1) ^ 1)) break;
-    for (int i = 0; i < kHeads * kRowChunks / 128; ++i) {
+    for (int i = 0; i < kHeads * (kQSRegions * 8) / 128; ++i) {
       const int q = pt + 128 * i;
-      const int r = q / kRowChunks, j = q % kRowChunks;
+      const int r = q / (kQSRegions * 8), j = q % (kQSRegions * 8);
       const uint32_t dst = c.sbase + (j >> 3) * (kHeads * 128) + sw128(r, j & 7);
       if (r < p.H_q)
-        cp_async16(dst, p.q + ((size_t)x.b * p.H_q + r) * kDqk + j * 8);
+        cp_async16(dst, p.q + ((size_t)x.b * p.H_q + r) * kDqk + kQT + j * 8);
       else
         cp_async16_zero(dst, p.q);
     }
     cp_async_arrive_noinc(bar_addr(c, kQFull));
+    // warm L2 with the next unit's query rows (its softmax warps load them
+    // into tensor memory at its start)
+    if (u + (int)gridDim.x < n_units) {
+      const MlaUnit nx = mla_unit(p, u + gridDim.x);
+      const char* qn = reinterpret_cast<const char*>(p.q + (size_t)nx.b * p.H_q * kDqk);
+      const int lines = min(p.H_q, kHeads) * kDqk * 2 / 128;
+      for (int i = pt; i < lines; i += 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(qn + (size_t)i * 128));
+    }
     // lanes 0-7 of producer warp pw look up the rows of entries 8*pw .. 8*pw+7
     // of a sub-tile; the lookup for the next sub-tile is issued before the
     // copies of the current one so its latency hides behind them
+    // ok: 0 = masked / bad index, 1 = main source, 2 = second source
     auto lookup = [&](int t0, long long& row, int& ok) {
       row = 0;
       ok = 0;
-      const int e = 8 * pw + pl;
-      if (pl < 8 && t0 + e < x.t_end) {
-        ok = latent_row(p, x.b, t0 + e, &row) ? 1 : 0;
-        bad |= !ok;
+      const int e = kEntPerWarp * pw + pl;
+      if (pl < kEntPerWarp && t0 + e < x.t_end) {
+        int src;
+        const bool good = latent_row(p, x.b, t0 + e, x.l_main, &row, &src);
+        ok = good ? 1 + src : 0;
+        bad |= !good;
       }
     };
     long long nx_row;
     int nx_ok;
     lookup(x.t_begin, nx_row, nx_ok);
     for (int t0 = x.t_begin; t0 < x.t_end; t0 += kSub, ++g) {
-      const int stage = g & 1;
-      if (!wait_bar(c, kEmpty0 + stage, ((g >> 1) & 1) ^ 1)) {
+      const int stage = g % kStages;
+      if (!wait_bar(c, kEmpty0 + stage, ((g / kStages) & 1) ^ 1)) {
         alive = false;
         break;
       }
@@ -190,15 +230,15 @@ __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
       const long long my_row = nx_row;
       const int my_ok = nx_ok;
       if (t0 + kSub < x.t_end) lookup(t0 + kSub, nx_row, nx_ok);
-#pragma unroll
-      for (int i = 0; i < 8 * kRowChunks / 32; ++i) {
+#pragma unroll 4
+      for (int i = 0; i < kEntPerWarp * kRowChunks / 32; ++i) {
         const int q = pl + 32 * i;
         const int e = q / kRowChunks, j = q % kRowChunks;
         const long long row = __shfl_sync(0xffffffffu, my_row, e);
         const int ok = __shfl_sync(0xffffffffu, my_ok, e);
-        const uint32_t dst = sb + (j >> 3) * kStageRegion + sw128(8 * pw + e, j & 7);
+        const uint32_t dst = sb + (j >> 3) * kStageRegion + sw128(kEntPerWarp * pw + e, j & 7);
         if (ok)
-          cp_async16(dst, p.k + (size_t)row * kDqk + j * 8);
+          cp_async16(dst, (ok == 1 ? p.k : p.extra_k) + (size_t)row * kDqk + j * 8);
         else
           cp_async16_zero(dst, p.k);  // masked entries read as zeros, never garbage
       }
@@ -213,51 +253,62 @@ __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
 // ---------------------------------------------------------------- MMA issue
 __device__ void mma_issuer(const Launch& p, const Ctx& c, uint32_t tmem, int n_units) {
   uint32_t g = 0, n_ne = 0;
+  // base descriptors; per-MMA ones differ only by a constant start offset
+  const uint64_t b_stage0 =  // K tile, K-major, 128-byte swizzle
+      umma::smem_desc(c.sbase + kStageOffset, 16, 1024, umma::kSwizzle128B);
+  const uint64_t a_q0 =      // Q tail, K-major, 128-byte swizzle
+      umma::smem_desc(c.sbase, 16, 1024, umma::kSwizzle128B);
+  const uint64_t a_p0 =      // P, K-major, 128-byte swizzle
+      umma::smem_desc(c.sbase + kPOffset, 16, 1024, umma::kSwizzle128B);
+  const uint64_t b_v0 =      // V = leading dims of the K tile, MN-major
+      umma::smem_desc(c.sbase + kStageOffset, kStageRegion, 1024, umma::kSwizzle128B);
   for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
     const MlaUnit x = mla_unit(p, u);
     if (x.empty) continue;
     const int n_sub = (x.t_end - x.t_begin + kSub - 1) / kSub;
-    if (!wait_bar(c, kQFull, n_ne & 1)) return;
+    if (!wait_bar(c, kQFull, n_ne & 1)) return;   // Q tail in shared memory
     fence_proxy_async();
+    if (!wait_bar(c, kQTFull, n_ne & 1)) return;  // Q head dims in TMEM
     umma::fence_after_sync();
     auto pv = [&](uint32_t gp, bool first) -> bool {
       if (!wait_bar(c, kPFull, gp & 1)) return false;
       if (first && !wait_bar(c, kOFree, (n_ne & 1) ^ 1)) return false;
       umma::fence_after_sync();
-      const uint32_t stage_base = c.sbase + kStageOffset + (gp & 1) * kStageBytes;
+      const uint64_t bv = b_v0 + (uint64_t)(((gp % kStages) * kStageBytes +
+                                             4 * x.half * kStageRegion) >> 4);
 #pragma unroll
-      for (int kk = 0; kk < kSub / 16; ++kk) {
-        const uint64_t a = umma::smem_desc(c.sbase + kPOffset + kk * 32, 16, 512, umma::kSwizzle64B);
-        const uint64_t b = umma::smem_desc(stage_base + (4 * x.half) * kStageRegion + kk * 2048,
-                                           kStageRegion, 1024, umma::kSwizzle128B);
-        umma::mma_bf16(tmem + kOCol, a, b, kIdescO, (first && kk == 0) ? 0u : 1u);
-      }
+      for (int kk = 0; kk < kSub / 16; ++kk)
+        umma::mma_bf16(tmem + kOCol, a_p0 + (uint64_t)((kk * 32) >> 4),
+                       bv + (uint64_t)((kk * 2048) >> 4), kIdescO,
+                       (first && kk == 0) ? 0u : 1u);
       umma::commit(bar_addr(c, kODone));
-      umma::commit(bar_addr(c, kEmpty0 + (gp & 1)));
+      umma::commit(bar_addr(c, kEmpty0 + (gp % kStages)));
       return true;
     };
+    // Issue order PV(g-1), S(g): the PV that frees stage g-1 is queued before
+    // the S of tile g, so the producer refills that stage while S(g) runs.
     for (int i = 0; i < n_sub; ++i, ++g) {
-      const int stage = g & 1;
-      if (!wait_bar(c, kFull0 + stage, (g >> 1) & 1)) return;
-      fence_proxy_async();
-      if (!wait_bar(c, kSFree0 + stage, ((g >> 1) & 1) ^ 1)) return;
-      umma::fence_after_sync();
-      const uint32_t stage_base = c.sbase + kStageOffset + stage * kStageBytes;
-      const uint32_t d_s = tmem + stage * kSub;
-#pragma unroll 1
-      for (int r = 0; r < kRegions; ++r) {
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t a = umma::smem_desc(c.sbase + r * (kHeads * 128) + kk * 32, 16, 1024,
-                                             umma::kSwizzle128B);
-          const uint64_t b = umma::smem_desc(stage_base + r * kStageRegion + kk * 32, 16, 1024,
-                                             umma::kSwizzle128B);
-          umma::mma_bf16(d_s, a, b, kIdescS, (r | kk) ? 1u : 0u);
-        }
-      }
-      umma::commit(bar_addr(c, kSFull0 + stage));
-      if (i == n_sub - 1) umma::commit(bar_addr(c, kQFree));
       if (i > 0 && !pv(g - 1, i == 1)) return;
+      const int stage = g % kStages;
+      if (!wait_bar(c, kFull0 + stage, (g / kStages) & 1)) return;
+      fence_proxy_async();
+      if (!wait_bar(c, kSFree, (g & 1) ^ 1)) return;  // softmax has read S(g-1)
+      umma::fence_after_sync();
+      // S = Q K^T: 36 MMAs of M = 128, N = 64, K = 16 into columns [192, 256)
+      const uint64_t b0 = b_stage0 + (uint64_t)((stage * kStageBytes) >> 4);
+      const uint32_t d_s = tmem + kSCol;
+#pragma unroll
+      for (int k = 0; k < kKSteps; ++k) {  // K step k: dims 16k .. 16k+15
+        const uint64_t b = b0 + (uint64_t)(((k / 4) * kStageRegion + (k % 4) * 32) >> 4);
+        if (k < kQT / 16)  // A = Q rows in TMEM (8 columns per 16 dims)
+          umma::mma_bf16_ta(d_s, tmem + k * 8, b, kIdescS, k ? 1u : 0u);
+        else               // A = Q tail in shared memory
+          umma::mma_bf16(d_s, a_q0 + (uint64_t)((((k - kQT / 16) / 4) * kHeads * 128 +
+                                                   (k % 4) * 32) >> 4),
+                         b, kIdescS, 1u);
+      }
+      umma::commit(bar_addr(c, kSFull));
+      if (i == n_sub - 1) umma::commit(bar_addr(c, kQFree));
     }
     if (!pv(g - 1, n_sub == 1)) return;
     ++n_ne;
@@ -269,7 +320,7 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = threadIdx.x;  // head = tensor-memory lane
   const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-  uint32_t g = 0;
+  uint32_t g = 0, n_ne = 0;
   // warp-uniform bounded wait (lane 0 waits, everyone follows its verdict)
   auto wait_w = [&](int bar, uint32_t parity) -> bool {
     int ok = 1;
@@ -280,6 +331,34 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_addr(c, bar));
   };
+  // Q dims 0..383 of head `row` of row b into TMEM columns [0, 192): two bf16
+  // per column, the lower dim in the low half; then signal the MMA thread.
+  auto load_q = [&](int b) {
+    const bool ok = row < p.H_q;
+    const uint4* qrow = reinterpret_cast<const uint4*>(p.q + ((size_t)b * p.H_q + row) * kDqk);
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+      uint4 w[24];
+#pragma unroll
+      for (int i = 0; i < 24; ++i) w[i] = ok ? __ldg(qrow + half * 24 + i) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int ch = 0; ch < 3; ++ch) {
+        uint32_t r32[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          r32[4 * i + 0] = w[ch * 8 + i].x;
+          r32[4 * i + 1] = w[ch * 8 + i].y;
+          r32[4 * i + 2] = w[ch * 8 + i].z;
+          r32[4 * i + 3] = w[ch * 8 + i].w;
+        }
+        umma::st_32x32b_x32_u(lane_base + (half * 3 + ch) * 32, r32);
+      }
+    }
+    umma::wait_st();
+    umma::fence_before_sync();
+    arrive_w(kQTFull);
+  };
+  bool q_ready = false;  // Q of the coming unit already in TMEM
   for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
     const MlaUnit x = mla_unit(p, u);
     const bool head_ok = row < p.H_q;
@@ -292,20 +371,33 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
       continue;
     }
     const int n_sub = (x.t_end - x.t_begin + kSub - 1) / kSub;
+    if (!q_ready) {
+      // (first unit only: later units get their Q while the previous unit's
+      // epilogue is still ahead, see below)
+      if (!wait_w(kQFree, (n_ne & 1) ^ 1)) return;
+      umma::fence_after_sync();
+      load_q(x.b);
+    }
+    q_ready = false;
     float m_used = -INFINITY, l = 0.f;
     for (int i = 0; i < n_sub; ++i, ++g) {
-      const int sb = g & 1;
-      if (!wait_w(kSFull0 + sb, (g >> 1) & 1)) return;
+      if (!wait_w(kSFull, g & 1)) return;
       umma::fence_after_sync();
-      float s[32];
-      umma::ld_32x32b_x32(lane_base + sb * kSub, s);
-      umma::wait_ld();
+      float s[64];
+      {
+        float s_hi[32];
+        umma::ld_32x32b_x32(lane_base + kSCol, *reinterpret_cast<float(*)[32]>(s));
+        umma::ld_32x32b_x32(lane_base + kSCol + 32, s_hi);
+        umma::wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) s[32 + j] = s_hi[j];
+      }
       umma::fence_before_sync();
-      arrive_w(kSFree0 + sb);
+      arrive_w(kSFree);
       const int n_valid = min(kSub, x.t_end - (x.t_begin + i * kSub));
       float mt = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
+      for (int j = 0; j < kSub; ++j) {
         s[j] = (j < n_valid) ? s[j] * p.scale_log2 : -INFINITY;
         mt = fmaxf(mt, s[j]);
       }
@@ -314,9 +406,9 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
       const float m_new = (i == 0 || mt > m_used + kRescaleLog2) ? mt : m_used;
       const float alpha = (i == 0) ? 1.f : ex2(m_used - m_new);
       float sum = 0.f;
-      uint32_t pk[16];
+      uint32_t pk[kSub / 2];
 #pragma unroll
-      for (int j = 0; j < 32; j += 2) {
+      for (int j = 0; j < kSub; j += 2) {
         const float p0 = ex2(s[j] - m_new), p1 = ex2(s[j + 1] - m_new);
         sum += p0;
         sum += p1;
@@ -341,15 +433,29 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
         }
       }
       m_used = m_new;
-      // P row (32 bf16 = 64 bytes) into the 64-byte-swizzled K-major tile
-      uint8_t* prow = c.smem + kPOffset + row * 64;
+      // P row (64 bf16 = 128 bytes) into the 128-byte-swizzled K-major tile
+      uint8_t* prow = c.smem + kPOffset + row * 128;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
-        *reinterpret_cast<uint4*>(prow + ((cc ^ ((row >> 1) & 3)) << 4)) =
+      for (int cc = 0; cc < 8; ++cc)
+        *reinterpret_cast<uint4*>(prow + ((cc ^ (row & 7)) << 4)) =
             make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
       fence_proxy_async();
       umma::fence_before_sync();
       arrive_w(kPFull);
+      if (i == n_sub - 1) {
+        // All S MMAs of this unit are done (S of the last tile was read), so
+        // TMEM columns [0, 192) are free: load the next unit's Q now and let
+        // the MMA thread start on it while this unit's epilogue runs.
+        for (int u2 = u + gridDim.x; u2 < n_units; u2 += gridDim.x) {
+          const MlaUnit x2 = mla_unit(p, u2);
+          if (x2.empty) continue;
+          if (!wait_w(kQFree, n_ne & 1)) return;
+          umma::fence_after_sync();
+          load_q(x2.b);
+          q_ready = true;
+          break;
+        }
+      }
     }
     // epilogue: O / l for this half of the value dims
     if (!wait_w(kODone, (g - 1) & 1)) return;
@@ -386,6 +492,7 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
     }
     umma::fence_before_sync();
     arrive_w(kOFree);
+    ++n_ne;
     if (head_ok && x.half == 0) {
       const float lse2 = (l > 0.f) ? m_used + lg2(l) : -INFINITY;
       if (x.single)
@@ -404,6 +511,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_mla_kernel(Launch p) {
   c.abort_flag = reinterpret_cast<volatile int*>(smem + kAbortSlot);
   c.hdr = p.hdr;
   const int warp = threadIdx.x >> 5;
+  wait_prior_grid();  // the plan kernel's outputs
+  allow_next_grid();
   const int n_units = p.hdr[kHdrNWork] * 2;
   if ((int)blockIdx.x >= n_units) return;  // uniform across the CTA
   // the swizzled layouts assume 1024-byte-aligned shared addresses
@@ -413,9 +522,10 @@ __global__ void __launch_bounds__(kThreads, 1) split_mla_kernel(Launch p) {
   }
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
-      uint32_t count = 1;
-      if (i == kFull0 || i == kFull1 || i == kQFull) count = 128;  // producer threads
-      if (i == kSFree0 || i == kSFree1 || i == kPFull || i == kOFree) count = 4;  // softmax warps
+      uint32_t count = 1;                                           // tcgen05.commit
+      if ((i >= kFull0 && i < kFull0 + kStages) || i == kQFull) count = 128;  // producer threads
+      if (i == kSFree || i == kPFull || i == kOFree || i == kQTFull)
+        count = 4;                                                   // softmax warps
       mbar_init(bar_addr(c, i), count);
     }
     *c.abort_flag = 0;
@@ -469,8 +579,8 @@ cudaError_t launch_split_mla(const Launch& p, int grid, cudaStream_t stream) {
   static const cudaError_t attr = cudaFuncSetAttribute(
       split_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (attr != cudaSuccess) return attr;
-  split_mla_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  return launch_after(split_mla_kernel, dim3(grid), dim3(kThreads), (size_t)kSmemBytes, stream,
+                      p);
 }
 
 }  // namespace da

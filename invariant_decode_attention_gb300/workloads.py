@@ -47,6 +47,11 @@ class Workload:
     D_qk: int
     D_v: int
     scale: float
+    # optional second, index-gathered KV source continuing each row's list
+    extra_k: Optional[torch.Tensor] = None        # [slots, H_kv, D_qk]
+    extra_v: Optional[torch.Tensor] = None        # [slots, H_kv, D_v] or None (latent)
+    extra_table: Optional[torch.Tensor] = None    # int32 [B, extra_width]
+    extra_lengths: Optional[torch.Tensor] = None  # int32 [B]
 
     @property
     def B(self):
@@ -69,6 +74,8 @@ class Workload:
     def kv_bytes(self):
         """Bytes of K and V the rows actually attend over (the algorithmic payload)."""
         n = int(self.lengths.to(torch.int64).sum())
+        if self.extra_lengths is not None:
+            n += int(self.extra_lengths.to(torch.int64).sum())
         per_entry_k = self.H_kv * self.D_qk * 2
         per_entry_v = 0 if self.v is None else self.H_kv * self.D_v * 2
         return n * (per_entry_k + per_entry_v)
@@ -77,7 +84,10 @@ class Workload:
         def mv(t):
             return None if t is None else t.to(device)
         return dataclasses.replace(self, q=mv(self.q), k=mv(self.k), v=mv(self.v),
-                                   lengths=mv(self.lengths), table=mv(self.table))
+                                   lengths=mv(self.lengths), table=mv(self.table),
+                                   extra_k=mv(self.extra_k), extra_v=mv(self.extra_v),
+                                   extra_table=mv(self.extra_table),
+                                   extra_lengths=mv(self.extra_lengths))
 
 
 def _randn(shape, g):
@@ -281,3 +291,29 @@ class RaggedSweep:
                       torch.tensor(lens, dtype=torch.int32, device=self.device),
                       table.to(self.device), self.page_size, 32, 8, 128, 128, 128 ** -0.5)
         return wl, pos
+
+
+def with_extra(wl, extra_lengths, num_slots, width=None, seed=0):
+    """The workload plus a second, index-gathered KV source: row b's list
+    continues with extra_lengths[b] distinct slots of a fresh cache of
+    `num_slots` rows (values N(0, 1) in bf16; latent when wl.v is None)."""
+    g = torch.Generator().manual_seed(seed)
+    el = torch.as_tensor(extra_lengths, dtype=torch.int32)
+    w = max(int(el.max()) if el.numel() else 0, 1) if width is None else width
+    table = torch.full((wl.B, w), -1, dtype=torch.int32)
+    for b in range(wl.B):
+        n = int(el[b])
+        table[b, :n] = torch.randperm(num_slots, generator=g)[:n].to(torch.int32)
+    ek = _randn((num_slots, wl.H_kv, wl.D_qk), g)
+    ev = None if wl.v is None else _randn((num_slots, wl.H_kv, wl.D_v), g)
+    return dataclasses.replace(wl, extra_k=ek, extra_v=ev, extra_table=table, extra_lengths=el,
+                               name=wl.name + "_extra")
+
+
+def mla_sparse_extra(seed=1005):
+    """The MLA-style sparse workload with a second latent KV source: per row
+    extra_topk uniform in [0, 512] distinct slots of a 16384-slot extra cache
+    (the sparse decode path with an extra k cache)."""
+    g = torch.Generator().manual_seed(seed)
+    el = torch.randint(0, 513, (64,), generator=g, dtype=torch.int64)
+    return with_extra(mla_sparse(), el.tolist(), 16384, width=512, seed=seed + 1)

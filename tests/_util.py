@@ -35,10 +35,15 @@ class Bf16Cache:
 def oracle_for(wl, rows=None, heads=None):
     """fp64 oracle (out, lse) of a CPU workload, optionally on a subset."""
     table = None if wl.table is None else wl.table.numpy()
+    extra = {}
+    if getattr(wl, "extra_k", None) is not None:
+        extra = dict(extra_k=Bf16Cache(wl.extra_k),
+                     extra_v=None if wl.extra_v is None else Bf16Cache(wl.extra_v),
+                     extra_table=wl.extra_table.numpy(), extra_lengths=wl.extra_lengths.numpy())
     return A.attend(wl.q.double().numpy(), Bf16Cache(wl.k),
                     None if wl.v is None else Bf16Cache(wl.v), wl.lengths.numpy(),
                     scale=wl.scale, layout=wl.layout, table=table, page_size=wl.page_size,
-                    d_v=wl.D_v, rows=rows, heads=heads)
+                    d_v=wl.D_v, rows=rows, heads=heads, **extra)
 
 
 def assert_parity(out_gpu, lse_gpu, ref_out, ref_lse, rows=None, heads=None):
