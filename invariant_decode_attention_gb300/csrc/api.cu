@@ -227,13 +227,16 @@ static int plan_impl(const da_problem* prob, int32_t policy, const int32_t* d_le
   if (cudaGetDevice(&dev) != cudaSuccess) return DA_ERR_CUDA;
   const int sms = sm_count(dev);
   if (sms <= 0) return DA_ERR_CUDA;
-  const int per_sm = (v.id == DA_VARIANT_MLA)
-                         ? mla_ctas_per_sm()
-                         : fma_ctas_per_sm(prob->num_q_heads / prob->num_kv_heads, prob->head_dim_qk);
   // CTAs that one (row, split) item occupies: one per KV head (CUDA-core
-  // variant) or a pair splitting D_v (tensor-core variant).
+  // variant) or a cluster pair splitting D_v (tensor-core variant).
   const int per_item = (v.id == DA_VARIANT_MLA) ? 2 : prob->num_kv_heads;
-  const long long slots = (long long)sms * per_sm;
+  // persistent CTAs: as many as can be resident at once (whole pairs for the
+  // tensor-core variant)
+  const long long slots =
+      (v.id == DA_VARIANT_MLA)
+          ? (long long)mla_resident_ctas(sms)
+          : (long long)sms *
+                fma_ctas_per_sm(prob->num_q_heads / prob->num_kv_heads, prob->head_dim_qk);
   const long long max_units = (long long)prob->batch * v.max_splits * per_item;
 
   da_plan P;

@@ -106,7 +106,7 @@ cudaError_t launch_combine(const Launch& p, cudaStream_t stream);
 cudaError_t launch_split_mla(const Launch& p, int grid, cudaStream_t stream);
 // Persistent CTAs that fit on one SM for the variant's split kernel.
 int fma_ctas_per_sm(int G, int D);
-int mla_ctas_per_sm();
+int mla_resident_ctas(int sms);  // persistent CTAs, an even number
 bool fma_supported(int G, int D);
 
 // Capacity of a row (largest valid length) for a layout.

@@ -5,33 +5,44 @@
 //
 // Both contractions run on tcgen05 tensor cores with fp32 accumulators in
 // tensor memory (TMEM):
-//     S = Q K^T      M = 128 heads, N = 32 entries, K = 576   (36 MMAs of K=16)
-//     O += P V_half  M = 128 heads, N = 256 dims,   K = 32    (2 MMAs)
+//     S = Q K^T      M = 128 heads, N = 64 entries, K = 576   (36 MMAs of K=16)
+//     O += P V_half  M = 128 heads, N = 256 dims,   K = 64    (4 MMAs)
 // O for 128 heads x 512 dims in fp32 would fill all of one SM's tensor memory,
 // so a (row, split) item runs as two units, one per half of the value dims;
 // each unit computes the full S itself (the same instructions on the same
 // data, so both halves see the same bits).
 //
-// Operand placement.  The first 384 dims of Q live in TMEM (192 columns) and
-// feed 24 of the 36 S MMAs as the A operand, so those read only the K tile
-// from shared memory; dims 384..575 of Q stay in shared memory (48 KB).  TMEM
-// columns: Q [0,192), S as two K-half partial accumulators [192,224) and
-// [224,256) (two independent MMA chains), O [256,512).
-// Shared memory: Q tail, four 32-entry KV stages (36 KB each), P (8 KB).
+// Operand placement.  TMEM columns: Q dims 0..255 [0,128) (the A operand of
+// 16 of the 36 S MMAs, so those read only the K tile from shared memory), two
+// S buffers [128,192) and [192,256), O [256,512).  Shared memory: Q dims
+// 256..575 (80 KB) and two 64-entry KV stages (72 KB each).  P of a tile is
+// written into its own KV stage, over the 16 KB of K dims that only S reads
+// (dims 256..383 for the low value half, dims 0..127 for the high one), so it
+// needs no buffer of its own and is released with the stage.
+//
+// Pipeline.  The MMA thread issues S(g) into buffer g % 2 before the PV of the
+// previous tile, so the softmax of tile g-1 overlaps the S MMAs of tile g.
+// The softmax touches O only to rescale it (when its running max moves by
+// more than 2^8), after the PV before it has landed.  The producer prefetches
+// the next tile's rows into L2 while the current stage is in use.
 //
 // Roles inside a CTA (288 threads):
 //   warps 0-3  softmax: thread i owns head i = TMEM lane i.  It loads its row
-//              of Q into TMEM at the start of a unit, reads its row of S,
-//              keeps the running max and sum in fp32, writes P (bf16) into
-//              shared memory and rescales its row of O when the max it uses
-//              moves by more than 2^8.
-//   warps 4-7  producer: gathers each entry's 1152-byte latent row with
-//              16-byte cp.async into the 128-byte-swizzled K-major layout the
-//              tensor core reads (and the unit's Q tail at its start).
+//              of Q dims 0..255 into TMEM at the start of a unit, reads its
+//              row of S, keeps the running max and sum in fp32, writes P
+//              (bf16) into the stage and writes its row of the result.
+//   warps 4-7  producer: looks up each entry's cache row and has the TMA unit
+//              gather the 1152-byte latent rows four at a time
+//              (tile::gather4, 64 dims x 4 rows per copy) into the
+//              128-byte-swizzled K-major layout the tensor core reads; the
+//              unit's Q dims 256..575 come by TMA tile copies at its start.
 //   warp 8     MMA issue (one thread) and TMEM allocation.
 // Every wait on an mbarrier is bounded; on time-out the kernel records
 // DA_DEVERR_TIMEOUT, every role leaves its loop, outstanding tensor-core work
 // is drained (bounded) and TMEM is freed.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "tcgen05.cuh"
 
@@ -43,47 +54,103 @@ constexpr int kDqk = 576;
 constexpr int kDvHalf = 256;      // value dims per unit
 constexpr int kSub = 64;          // entries per sub-tile (MMA N of S, K of P.V)
 constexpr int kRegions = kDqk / 64;  // 64-dim swizzle regions of a row
-constexpr int kRowChunks = kDqk / 8; // 16-byte chunks of a row (72)
-constexpr int kQT = 384;          // dims of Q held in TMEM (A operand)
-constexpr int kQTCols = kQT / 2;  // 192 TMEM columns (two bf16 per column)
-constexpr int kQSRegions = (kDqk - kQT) / 64;  // 3 smem regions of Q (dims 384..575)
+constexpr int kQT = 256;          // dims of Q held in TMEM (A operand)
+constexpr int kQTCols = kQT / 2;  // 128 TMEM columns (two bf16 per column)
+constexpr int kQSRegions = (kDqk - kQT) / 64;  // 5 smem regions of Q (dims 256..575)
 constexpr int kStages = 2;
 
 // shared memory map (bytes)
-constexpr int kQSBytes = kQSRegions * kHeads * 128;        // 49152
+constexpr int kQSBytes = kQSRegions * kHeads * 128;        // 81920
 constexpr int kStageRegion = kSub * 128;                    // 8192
 constexpr int kStageBytes = kRegions * kStageRegion;        // 73728
 constexpr int kStageOffset = kQSBytes;
-constexpr int kPOffset = kStageOffset + kStages * kStageBytes;  // 196608
 constexpr int kPBytes = kHeads * kSub * 2;                  // 16384 (128-byte swizzle)
-constexpr int kBarOffset = kPOffset + kPBytes;              // 212992
-enum { kFull0 = 0, kEmpty0 = kFull0 + kStages, kSFull = kEmpty0 + kStages, kSFree, kPFull,
-       kODone, kOFree, kQFull, kQTFull, kQFree, kDrain, kNumBars };
+constexpr int kBarOffset = kStageOffset + kStages * kStageBytes;  // 229376
+// Barriers that are signalled once per tile come in pairs indexed by the
+// tile's parity.  A parity wait is only unambiguous while the barrier is at
+// most one phase behind the phase waited for; the softmax waits for PV
+// completion only when it rescales O (and at the epilogue), so a single
+// PV-done barrier could be two phases behind there.
+enum { kFull0 = 0, kEmpty0 = kFull0 + kStages, kSFull0 = kEmpty0 + kStages,
+       kSFree0 = kSFull0 + 2, kPFull0 = kSFree0 + 2, kODone0 = kPFull0 + 2,
+       kOFree = kODone0 + 2, kQFull, kQTFull, kQFree, kDrain, kNumBars };
 constexpr int kTmemSlot = kBarOffset + kNumBars * 8;
-static_assert(kPOffset % 1024 == 0 && kStageOffset % 1024 == 0, "swizzle atoms 1024-aligned");
+static_assert(kStageOffset % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle atoms 1024-aligned");
 constexpr int kAbortSlot = kTmemSlot + 4;
 constexpr int kSmemBytes = kAbortSlot + 12;
 static_assert(kSmemBytes <= 232448, "fits the 227 KB per-block limit");
 
+// P of a tile sits in its stage over K dims that only S reads: regions 4-5
+// (dims 256..383) when the unit takes value dims 0..255, regions 0-1 when it
+// takes 256..511.
+__host__ __device__ constexpr int p_offset_in_stage(int half) {
+  return (half == 0 ? 4 : 0) * kStageRegion;
+}
+static_assert(2 * kStageRegion == kPBytes, "P fills two regions");
+
 constexpr int kThreads = 288;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSCol = kQTCols;  // S partial accumulators at [192, 256)
+constexpr uint32_t kSCol = kQTCols;  // S buffers at [128, 192) and [192, 256)
 constexpr int kKSteps = kDqk / 16;   // 36 MMAs of K = 16 per S tile
 constexpr int kEntPerWarp = kSub / 4;  // entries each producer warp gathers
 constexpr uint32_t kOCol = 256;      // O accumulator columns [256, 512)
+static_assert(kSCol + 2 * kSub == kOCol && kOCol + kDvHalf == kTmemCols, "TMEM budget");
 constexpr float kRescaleLog2 = 8.f;
 
 constexpr uint32_t kIdescS = umma::idesc_bf16_f32(kHeads, kSub, false);
 constexpr uint32_t kIdescO = umma::idesc_bf16_f32(kHeads, kDvHalf, true);
 
-__device__ __forceinline__ void cp_async16_zero(uint32_t dst, const void* any_src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, 0;" ::"r"(dst), "l"(any_src)
-               : "memory");
+// TMA copies from a 2-D tensor map (dim 0 = the 576 dims of a row, dim 1 =
+// rows), 128-byte swizzle applied by the copy engine from the shared-memory
+// address.  Each copy lands at the same shared-memory offset in both CTAs of
+// the pair (multicast) and completes its bytes on the mbarrier at offset `bar`
+// in each of them.
+constexpr uint16_t kPairMask = 0x3;
+
+// Box {64, 1} at rows r0..r3: four 128-byte rows land at dst + 128 * i.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* tm, int col, int r0,
+                                            int r1, int r2, int r3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar),
+      "h"(kPairMask)
+      : "memory");
 }
 
-// The mbarrier receives one arrive once all earlier cp.async of this thread land.
-__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+// One box of the map (its box dims) at (col, row).
+__device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap* tm, int col, int row,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(col), "r"(row), "r"(bar), "h"(kPairMask)
+      : "memory");
+}
+
+// One arrive on the mbarrier at offset `bar` in both CTAs of the pair once
+// every tensor-core operation this thread issued so far has completed.
+__device__ __forceinline__ void commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar), "h"(kPairMask)
+      : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Start pulling `bytes` (a multiple of 16) at a 16-byte-aligned address into L2.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async() {
@@ -95,7 +162,13 @@ struct Ctx {
   uint32_t sbase;  // shared address of smem[0]
   volatile int* abort_flag;
   int32_t* hdr;
+  const CUtensorMap* tm_k;  // main cache as [rows, 576], box {64, 1}
+  const CUtensorMap* tm_x;  // second source as [slots, 576], box {64, 1}
+  const CUtensorMap* tm_q;  // q as [B * H_q, 576], box {64, 16}
 };
+
+// Rows of a 16-row box of Q a unit loads (heads rounded up to 16).
+constexpr int kQBoxRows = 16;
 
 __device__ __forceinline__ uint32_t bar_addr(const Ctx& c, int i) {
   return c.sbase + kBarOffset + 8 * i;
@@ -165,34 +238,37 @@ __device__ __forceinline__ bool latent_row(const Launch& p, int b, int tok, int 
   return slot >= 0 && slot < p.num_blocks;
 }
 
-// 128-byte swizzle inside a 1024-byte-aligned region of 128-byte rows.
-__device__ __forceinline__ uint32_t sw128(int row, int chunk) {
-  return row * 128 + ((chunk ^ (row & 7)) << 4);
-}
-
 // ---------------------------------------------------------------- producer
 __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
   const int pt = threadIdx.x - 128;  // 0..127
+  const uint32_t rank = cluster_rank();
   const int pw = pt >> 5, pl = pt & 31;
   uint32_t g = 0, n_ne = 0;
   bool alive = true;
   bool bad = false;
+  // warp-uniform bounded wait (lane 0 waits, everyone follows its verdict)
+  auto wait_w = [&](int bar, uint32_t parity) -> bool {
+    int ok = 1;
+    if (pl == 0) ok = wait_bar(c, bar, parity) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+  };
+  const int q_boxes = (min(p.H_q, kHeads) + kQBoxRows - 1) / kQBoxRows;  // per region
   for (int u = blockIdx.x; u < n_units && alive; u += gridDim.x) {
     const MlaUnit x = mla_unit(p, u);
     if (x.empty) continue;
-    // Q dims 384..575 of row b (zero rows past H_q) into shared memory, once
-    // the previous unit's S MMAs are done
-    if (!wait_bar(c, kQFree, (n_ne & 1) ^ 1)) break;
-    for (int i = 0; i < kHeads * (kQSRegions * 8) / 128; ++i) {
-      const int q = pt + 128 * i;
-      const int r = q / (kQSRegions * 8), j = q % (kQSRegions * 8);
-      const uint32_t dst = c.sbase + (j >> 3) * (kHeads * 128) + sw128(r, j & 7);
-      if (r < p.H_q)
-        cp_async16(dst, p.q + ((size_t)x.b * p.H_q + r) * kDqk + kQT + j * 8);
-      else
-        cp_async16_zero(dst, p.q);
+    // Q dims 256..575 of row b into shared memory once the previous unit's S
+    // MMAs are done: q_boxes 16-row boxes per 64-dim region, spread over the
+    // four warps (rows past H_q belong to other rows or read as zeros; those
+    // heads' results are never written)
+    if (!wait_w(kQFree, (n_ne & 1) ^ 1)) break;
+    if (pt == 0) mbar_arrive_expect_tx(bar_addr(c, kQFull), kQSRegions * q_boxes * kQBoxRows * 128);
+    __syncwarp();
+    // this CTA copies every other box; each box lands in both CTAs
+    for (int i = 2 * pt + (int)rank; i < kQSRegions * q_boxes; i += 256) {
+      const int j = i / q_boxes, rb = i % q_boxes;
+      tma_tile(c.sbase + j * (kHeads * 128) + rb * (kQBoxRows * 128), c.tm_q, kQT + 64 * j,
+               x.b * p.H_q + rb * kQBoxRows, bar_addr(c, kQFull));
     }
-    cp_async_arrive_noinc(bar_addr(c, kQFull));
     // warm L2 with the next unit's query rows (its softmax warps load them
     // into tensor memory at its start)
     if (u + (int)gridDim.x < n_units) {
@@ -202,113 +278,147 @@ __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
       for (int i = pt; i < lines; i += 128)
         asm volatile("prefetch.global.L2 [%0];" ::"l"(qn + (size_t)i * 128));
     }
-    // lanes 0-7 of producer warp pw look up the rows of entries 8*pw .. 8*pw+7
-    // of a sub-tile; the lookup for the next sub-tile is issued before the
-    // copies of the current one so its latency hides behind them
-    // ok: 0 = masked / bad index, 1 = main source, 2 = second source
-    auto lookup = [&](int t0, long long& row, int& ok) {
+    // lanes 0-15 of producer warp pw look up the rows of entries 16*pw .. 16*pw+15
+    // of a tile; the lookup for the next tile is issued before the copies of
+    // the current one so its latency hides behind them.
+    // src: 0 = main cache, 1 = second source.  Masked entries (past the end
+    // of the split) and bad indices read row 0 of the main cache, so every
+    // stage byte holds real data; masked scores are dropped by the softmax.
+    auto lookup = [&](int t0, int& row, int& src, bool& live) {
       row = 0;
-      ok = 0;
+      src = 0;
+      live = false;
       const int e = kEntPerWarp * pw + pl;
       if (pl < kEntPerWarp && t0 + e < x.t_end) {
-        int src;
-        const bool good = latent_row(p, x.b, t0 + e, x.l_main, &row, &src);
-        ok = good ? 1 + src : 0;
+        long long r;
+        int sr;
+        const bool good = latent_row(p, x.b, t0 + e, x.l_main, &r, &sr);
         bad |= !good;
+        if (good) {
+          row = (int)r;
+          src = sr;
+          live = true;
+        }
       }
     };
-    long long nx_row;
-    int nx_ok;
-    lookup(x.t_begin, nx_row, nx_ok);
+    int nx_row, nx_src;
+    bool nx_live;
+    lookup(x.t_begin, nx_row, nx_src, nx_live);
     for (int t0 = x.t_begin; t0 < x.t_end; t0 += kSub, ++g) {
       const int stage = g % kStages;
-      if (!wait_bar(c, kEmpty0 + stage, ((g / kStages) & 1) ^ 1)) {
+      if (!wait_w(kEmpty0 + stage, ((g / kStages) & 1) ^ 1)) {
         alive = false;
         break;
       }
-      const uint32_t sb = c.sbase + kStageOffset + stage * kStageBytes;
-      const long long my_row = nx_row;
-      const int my_ok = nx_ok;
-      if (t0 + kSub < x.t_end) lookup(t0 + kSub, nx_row, nx_ok);
-#pragma unroll 4
-      for (int i = 0; i < kEntPerWarp * kRowChunks / 32; ++i) {
-        const int q = pl + 32 * i;
-        const int e = q / kRowChunks, j = q % kRowChunks;
-        const long long row = __shfl_sync(0xffffffffu, my_row, e);
-        const int ok = __shfl_sync(0xffffffffu, my_ok, e);
-        const uint32_t dst = sb + (j >> 3) * kStageRegion + sw128(kEntPerWarp * pw + e, j & 7);
-        if (ok)
-          cp_async16(dst, (ok == 1 ? p.k : p.extra_k) + (size_t)row * kDqk + j * 8);
-        else
-          cp_async16_zero(dst, p.k);  // masked entries read as zeros, never garbage
+      const int my_row = nx_row, my_src = nx_src;
+      if (t0 + kSub < x.t_end) lookup(t0 + kSub, nx_row, nx_src, nx_live);
+      const uint32_t full = bar_addr(c, kFull0 + stage);
+      if (pt == 0) mbar_arrive_expect_tx(full, kStageBytes);
+      // lane q < 4 copies the group of entries 16*pw + 4q .. 16*pw + 4q + 3
+      // when the group's parity is this CTA's rank; each group lands in both
+      int r[4], sr[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        r[i] = __shfl_sync(0xffffffffu, my_row, (4 * pl + i) & 31);
+        sr[i] = __shfl_sync(0xffffffffu, my_src, (4 * pl + i) & 31);
       }
-      cp_async_arrive_noinc(bar_addr(c, kFull0 + stage));
+      if (pl < 4 && (pl & 1) == (int)rank) {
+        const uint32_t dst = c.sbase + kStageOffset + stage * kStageBytes +
+                             (kEntPerWarp * pw + 4 * pl) * 128;
+        if (sr[0] == sr[1] && sr[0] == sr[2] && sr[0] == sr[3]) {
+          const CUtensorMap* tm = sr[0] ? c.tm_x : c.tm_k;
+#pragma unroll 1
+          for (int j = 0; j < kRegions; ++j)
+            tma_gather4(dst + j * kStageRegion, tm, 64 * j, r[0], r[1], r[2], r[3], full);
+        } else {  // the group straddles the two sources: one row per copy
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll 1
+            for (int j = 0; j < kRegions; ++j)
+              tma_tile(dst + i * 128 + j * kStageRegion, sr[i] ? c.tm_x : c.tm_k, 64 * j, r[i],
+                       full);
+        }
+      }
+      // the next tile's rows start towards L2 while this stage is consumed
+      if (nx_live && t0 + kSub < x.t_end)
+        prefetch_l2((nx_src ? p.extra_k : p.k) + (size_t)nx_row * kDqk, kDqk * 2);
     }
     ++n_ne;
   }
   if (bad) set_error(p.hdr, DA_DEVERR_INDEX);
-  cp_async_wait<0>();
+  // leave no copy in flight into this CTA's shared memory (on the normal path
+  // every stage was consumed and these waits return at once)
+  if (pt == 0) {
+    for (int st = 0; st < kStages; ++st) {
+      const int last = (int)g - 1 - (((int)g - 1 - st) % kStages + kStages) % kStages;
+      if (last >= 0 && !mbar_wait(bar_addr(c, kFull0 + st), (last / kStages) & 1))
+        set_error(p.hdr, DA_DEVERR_TIMEOUT);
+    }
+    if (n_ne > 0 && !mbar_wait(bar_addr(c, kQFull), (n_ne - 1) & 1))
+      set_error(p.hdr, DA_DEVERR_TIMEOUT);
+  }
 }
 
 // ---------------------------------------------------------------- MMA issue
-__device__ void mma_issuer(const Launch& p, const Ctx& c, uint32_t tmem, int n_units) {
-  uint32_t g = 0, n_ne = 0;
+__device__ void mma_issuer(const Launch& p, const Ctx& c, uint32_t tmem, int n_units,
+                           uint32_t& g, uint32_t& n_ne) {
   // base descriptors; per-MMA ones differ only by a constant start offset
   const uint64_t b_stage0 =  // K tile, K-major, 128-byte swizzle
       umma::smem_desc(c.sbase + kStageOffset, 16, 1024, umma::kSwizzle128B);
-  const uint64_t a_q0 =      // Q tail, K-major, 128-byte swizzle
+  const uint64_t a_q0 =      // Q dims 256..575, K-major, 128-byte swizzle
       umma::smem_desc(c.sbase, 16, 1024, umma::kSwizzle128B);
-  const uint64_t a_p0 =      // P, K-major, 128-byte swizzle
-      umma::smem_desc(c.sbase + kPOffset, 16, 1024, umma::kSwizzle128B);
   const uint64_t b_v0 =      // V = leading dims of the K tile, MN-major
       umma::smem_desc(c.sbase + kStageOffset, kStageRegion, 1024, umma::kSwizzle128B);
   for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
     const MlaUnit x = mla_unit(p, u);
     if (x.empty) continue;
     const int n_sub = (x.t_end - x.t_begin + kSub - 1) / kSub;
-    if (!wait_bar(c, kQFull, n_ne & 1)) return;   // Q tail in shared memory
+    if (!wait_bar(c, kQFull, n_ne & 1)) return;   // Q dims 256.. in shared memory
     fence_proxy_async();
-    if (!wait_bar(c, kQTFull, n_ne & 1)) return;  // Q head dims in TMEM
+    if (!wait_bar(c, kQTFull, n_ne & 1)) return;  // Q dims 0..255 in TMEM
     umma::fence_after_sync();
+    // O += P(gp) V(gp): P and V both sit in the stage of tile gp
     auto pv = [&](uint32_t gp, bool first) -> bool {
-      if (!wait_bar(c, kPFull, gp & 1)) return false;
+      if (!wait_bar(c, kPFull0 + (gp & 1), (gp >> 1) & 1)) return false;
       if (first && !wait_bar(c, kOFree, (n_ne & 1) ^ 1)) return false;
       umma::fence_after_sync();
-      const uint64_t bv = b_v0 + (uint64_t)(((gp % kStages) * kStageBytes +
-                                             4 * x.half * kStageRegion) >> 4);
+      const uint32_t st = (gp % kStages) * kStageBytes;
+      const uint64_t ap = b_stage0 + (uint64_t)((st + p_offset_in_stage(x.half)) >> 4);
+      const uint64_t bv = b_v0 + (uint64_t)((st + 4 * x.half * kStageRegion) >> 4);
 #pragma unroll
       for (int kk = 0; kk < kSub / 16; ++kk)
-        umma::mma_bf16(tmem + kOCol, a_p0 + (uint64_t)((kk * 32) >> 4),
+        umma::mma_bf16(tmem + kOCol, ap + (uint64_t)((kk * 32) >> 4),
                        bv + (uint64_t)((kk * 2048) >> 4), kIdescO,
                        (first && kk == 0) ? 0u : 1u);
-      umma::commit(bar_addr(c, kODone));
-      umma::commit(bar_addr(c, kEmpty0 + (gp % kStages)));
+      umma::commit(bar_addr(c, kODone0 + (gp & 1)));
+      commit_pair(bar_addr(c, kEmpty0 + (gp % kStages)));
       return true;
     };
-    // Issue order PV(g-1), S(g): the PV that frees stage g-1 is queued before
-    // the S of tile g, so the producer refills that stage while S(g) runs.
+    // Issue order S(g), PV(g-1): S(g) goes to the other S buffer, so it runs
+    // while the softmax of tile g-1 is still producing P(g-1).
     for (int i = 0; i < n_sub; ++i, ++g) {
-      if (i > 0 && !pv(g - 1, i == 1)) return;
       const int stage = g % kStages;
+      const int sb = g & 1;
       if (!wait_bar(c, kFull0 + stage, (g / kStages) & 1)) return;
       fence_proxy_async();
-      if (!wait_bar(c, kSFree, (g & 1) ^ 1)) return;  // softmax has read S(g-1)
+      if (!wait_bar(c, kSFree0 + sb, ((g >> 1) & 1) ^ 1)) return;  // S(g-2) was read
       umma::fence_after_sync();
-      // S = Q K^T: 36 MMAs of M = 128, N = 64, K = 16 into columns [192, 256)
+      // S = Q K^T: 36 MMAs of M = 128, N = 64, K = 16 into S buffer sb
       const uint64_t b0 = b_stage0 + (uint64_t)((stage * kStageBytes) >> 4);
-      const uint32_t d_s = tmem + kSCol;
+      const uint32_t d_s = tmem + kSCol + sb * kSub;
 #pragma unroll
       for (int k = 0; k < kKSteps; ++k) {  // K step k: dims 16k .. 16k+15
         const uint64_t b = b0 + (uint64_t)(((k / 4) * kStageRegion + (k % 4) * 32) >> 4);
         if (k < kQT / 16)  // A = Q rows in TMEM (8 columns per 16 dims)
           umma::mma_bf16_ta(d_s, tmem + k * 8, b, kIdescS, k ? 1u : 0u);
-        else               // A = Q tail in shared memory
+        else               // A = Q dims 256.. in shared memory
           umma::mma_bf16(d_s, a_q0 + (uint64_t)((((k - kQT / 16) / 4) * kHeads * 128 +
                                                    (k % 4) * 32) >> 4),
                          b, kIdescS, 1u);
       }
-      umma::commit(bar_addr(c, kSFull));
-      if (i == n_sub - 1) umma::commit(bar_addr(c, kQFree));
+      umma::commit(bar_addr(c, kSFull0 + sb));
+      if (i == n_sub - 1) commit_pair(bar_addr(c, kQFree));
+      if (i > 0 && !pv(g - 1, i == 1)) return;
     }
     if (!pv(g - 1, n_sub == 1)) return;
     ++n_ne;
@@ -331,18 +441,18 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_addr(c, bar));
   };
-  // Q dims 0..383 of head `row` of row b into TMEM columns [0, 192): two bf16
+  // Q dims 0..255 of head `row` of row b into TMEM columns [0, 128): two bf16
   // per column, the lower dim in the low half; then signal the MMA thread.
   auto load_q = [&](int b) {
     const bool ok = row < p.H_q;
     const uint4* qrow = reinterpret_cast<const uint4*>(p.q + ((size_t)b * p.H_q + row) * kDqk);
 #pragma unroll 1
     for (int half = 0; half < 2; ++half) {
-      uint4 w[24];
+      uint4 w[16];
 #pragma unroll
-      for (int i = 0; i < 24; ++i) w[i] = ok ? __ldg(qrow + half * 24 + i) : make_uint4(0, 0, 0, 0);
+      for (int i = 0; i < 16; ++i) w[i] = ok ? __ldg(qrow + half * 16 + i) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int ch = 0; ch < 3; ++ch) {
+      for (int ch = 0; ch < 2; ++ch) {
         uint32_t r32[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -351,7 +461,7 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
           r32[4 * i + 2] = w[ch * 8 + i].z;
           r32[4 * i + 3] = w[ch * 8 + i].w;
         }
-        umma::st_32x32b_x32_u(lane_base + (half * 3 + ch) * 32, r32);
+        umma::st_32x32b_x32_u(lane_base + (half * 2 + ch) * 32, r32);
       }
     }
     umma::wait_st();
@@ -381,19 +491,20 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
     q_ready = false;
     float m_used = -INFINITY, l = 0.f;
     for (int i = 0; i < n_sub; ++i, ++g) {
-      if (!wait_w(kSFull, g & 1)) return;
+      const int sb = g & 1;
+      if (!wait_w(kSFull0 + sb, (g >> 1) & 1)) return;
       umma::fence_after_sync();
       float s[64];
       {
         float s_hi[32];
-        umma::ld_32x32b_x32(lane_base + kSCol, *reinterpret_cast<float(*)[32]>(s));
-        umma::ld_32x32b_x32(lane_base + kSCol + 32, s_hi);
+        umma::ld_32x32b_x32(lane_base + kSCol + sb * kSub, *reinterpret_cast<float(*)[32]>(s));
+        umma::ld_32x32b_x32(lane_base + kSCol + sb * kSub + 32, s_hi);
         umma::wait_ld();
 #pragma unroll
         for (int j = 0; j < 32; ++j) s[32 + j] = s_hi[j];
       }
       umma::fence_before_sync();
-      arrive_w(kSFree);
+      arrive_w(kSFree0 + sb);
       const int n_valid = min(kSub, x.t_end - (x.t_begin + i * kSub));
       float mt = -INFINITY;
 #pragma unroll
@@ -416,35 +527,37 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
         pk[j / 2] = *reinterpret_cast<const uint32_t*>(&h);
       }
       l = (i == 0) ? sum : fmaf(l, alpha, sum);
-      if (i > 0) {  // PV of the previous sub-tile must be done with P and O
-        if (!wait_w(kODone, (g - 1) & 1)) return;
+      // O is rescaled only when some head's max moved; the PV of the previous
+      // tile must have landed first (PV(g) waits for this warp's P(g))
+      if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        if (!wait_w(kODone0 + ((g - 1) & 1), ((g - 1) >> 1) & 1)) return;
         umma::fence_after_sync();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-          for (int ch = 0; ch < kDvHalf / 32; ++ch) {
-            float o[32];
-            umma::ld_32x32b_x32(lane_base + kOCol + ch * 32, o);
-            umma::wait_ld();
+        for (int ch = 0; ch < kDvHalf / 32; ++ch) {
+          float o[32];
+          umma::ld_32x32b_x32(lane_base + kOCol + ch * 32, o);
+          umma::wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] *= alpha;
-            umma::st_32x32b_x32(lane_base + kOCol + ch * 32, o);
-          }
-          umma::wait_st();
+          for (int j = 0; j < 32; ++j) o[j] *= alpha;
+          umma::st_32x32b_x32(lane_base + kOCol + ch * 32, o);
         }
+        umma::wait_st();
       }
       m_used = m_new;
       // P row (64 bf16 = 128 bytes) into the 128-byte-swizzled K-major tile
-      uint8_t* prow = c.smem + kPOffset + row * 128;
+      // inside this tile's stage (S(g), the last reader of those K dims, is done)
+      uint8_t* prow = c.smem + kStageOffset + (g % kStages) * kStageBytes +
+                      p_offset_in_stage(x.half) + row * 128;
 #pragma unroll
       for (int cc = 0; cc < 8; ++cc)
         *reinterpret_cast<uint4*>(prow + ((cc ^ (row & 7)) << 4)) =
             make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
       fence_proxy_async();
       umma::fence_before_sync();
-      arrive_w(kPFull);
+      arrive_w(kPFull0 + sb);
       if (i == n_sub - 1) {
         // All S MMAs of this unit are done (S of the last tile was read), so
-        // TMEM columns [0, 192) are free: load the next unit's Q now and let
+        // TMEM columns [0, 128) are free: load the next unit's Q now and let
         // the MMA thread start on it while this unit's epilogue runs.
         for (int u2 = u + gridDim.x; u2 < n_units; u2 += gridDim.x) {
           const MlaUnit x2 = mla_unit(p, u2);
@@ -458,7 +571,7 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
       }
     }
     // epilogue: O / l for this half of the value dims
-    if (!wait_w(kODone, (g - 1) & 1)) return;
+    if (!wait_w(kODone0 + ((g - 1) & 1), ((g - 1) >> 1) & 1)) return;
     umma::fence_after_sync();
     const float inv = (l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll 1
@@ -503,13 +616,19 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) split_mla_kernel(Launch p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    split_mla_kernel(Launch p, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_x,
+                     const __grid_constant__ CUtensorMap tm_q) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Ctx c;
   c.smem = smem;
   c.sbase = smem_addr(smem);
   c.abort_flag = reinterpret_cast<volatile int*>(smem + kAbortSlot);
   c.hdr = p.hdr;
+  c.tm_k = &tm_k;
+  c.tm_x = &tm_x;
+  c.tm_q = &tm_q;
   const int warp = threadIdx.x >> 5;
   wait_prior_grid();  // the plan kernel's outputs
   allow_next_grid();
@@ -523,29 +642,33 @@ __global__ void __launch_bounds__(kThreads, 1) split_mla_kernel(Launch p) {
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t count = 1;                                           // tcgen05.commit
-      if ((i >= kFull0 && i < kFull0 + kStages) || i == kQFull) count = 128;  // producer threads
-      if (i == kSFree || i == kPFull || i == kOFree || i == kQTFull)
+      if ((i >= kSFree0 && i < kSFree0 + 2) || (i >= kPFull0 && i < kPFull0 + 2) ||
+          i == kOFree || i == kQTFull)
         count = 4;                                                   // softmax warps
+      if ((i >= kEmpty0 && i < kEmpty0 + kStages) || i == kQFree)
+        count = 2;                                                   // both CTAs' MMAs
       mbar_init(bar_addr(c, i), count);
     }
     *c.abort_flag = 0;
-    fence_mbar_init();
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 8) {
     umma::tmem_alloc(c.sbase + kTmemSlot, kTmemCols);
     umma::tmem_relinquish();
   }
+  // both CTAs' barriers exist before either copies into or arrives on them
   umma::fence_before_sync();
-  __syncthreads();
+  cluster_sync();
   umma::fence_after_sync();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kTmemSlot);
 
+  uint32_t g_done = 0, q_done = 0;  // tiles and units the MMA thread got through
   if (warp < 4) {
     softmax_warps(p, c, tmem, n_units);
   } else if (warp < 8) {
     producer(p, c, n_units);
   } else if ((threadIdx.x & 31) == 0) {
-    mma_issuer(p, c, tmem, n_units);
+    mma_issuer(p, c, tmem, n_units, g_done, q_done);
     // drain: one more commit; its arrival means every MMA issued before it
     // has completed, so tensor memory can be freed
     umma::commit(bar_addr(c, kDrain));
@@ -564,23 +687,104 @@ __global__ void __launch_bounds__(kThreads, 1) split_mla_kernel(Launch p) {
         }
       }
     }
+    // the peer's releases of this CTA's stages and Q (it commits the same
+    // sequence): wait until its last ones have landed here
+    if ((threadIdx.x & 31) == 0) {
+      for (int st = 0; st < kStages; ++st) {
+        const int last = (int)g_done - 1 - (((int)g_done - 1 - st) % kStages + kStages) % kStages;
+        if (last >= 0 && !mbar_wait(bar_addr(c, kEmpty0 + st), (last / kStages) & 1))
+          set_error(p.hdr, DA_DEVERR_TIMEOUT);
+      }
+      if (q_done > 0 && !mbar_wait(bar_addr(c, kQFree), (q_done - 1) & 1))
+        set_error(p.hdr, DA_DEVERR_TIMEOUT);
+    }
     __syncwarp();
-    umma::tmem_dealloc(tmem, kTmemCols);
   }
+  // the peer CTA no longer copies into, or arrives on, this CTA's shared
+  // memory once both have drained their copies and tensor-core work
+  cluster_sync();
+  if (warp == 8) umma::tmem_dealloc(tmem, kTmemCols);
+}
+
+// Stands in for an empty cache: dummy copies of masked entries read it.
+__device__ __nv_bfloat16 g_zero_row[kDqk];
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// `rows` rows of 576 bf16 at `base` (16-byte aligned), box {64, box_rows},
+// 128-byte swizzle.
+bool encode_rows(CUtensorMap* tm, const void* base, long long rows, int box_rows) {
+  const PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn || rows < 1 || rows > (1ll << 32)) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)kDqk, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kDqk * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  const cuuint32_t elem[2] = {1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
 
 bool mla_supported(int H_q) { return H_q >= 16 && H_q <= kHeads; }
 
-int mla_ctas_per_sm() { return 1; }
+// Persistent CTAs: pairs of CTAs that can be resident at once (one per SM).
+int mla_resident_ctas(int sms) {
+  static const int clusters = [] {
+    if (cudaFuncSetAttribute(split_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess)
+      return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, split_mla_kernel, &cfg) != cudaSuccess) n = 0;
+    return n;
+  }();
+  const int pairs = sms / 2;
+  return 2 * ((clusters > 0 && clusters < pairs) ? clusters : pairs);
+}
 
 cudaError_t launch_split_mla(const Launch& p, int grid, cudaStream_t stream) {
   static const cudaError_t attr = cudaFuncSetAttribute(
       split_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (attr != cudaSuccess) return attr;
+  // rows addressable in the main cache under its layout
+  const long long rows = (p.layout == DA_KV_CONTIGUOUS) ? (long long)p.B * p.width
+                         : (p.layout == DA_KV_PAGED)    ? p.num_blocks * p.page_size
+                                                        : p.num_blocks;
+  alignas(64) CUtensorMap tm_k, tm_x, tm_q;
+  memset(&tm_k, 0, sizeof tm_k);
+  memset(&tm_x, 0, sizeof tm_x);
+  memset(&tm_q, 0, sizeof tm_q);
+  if (rows >= 1) {
+    if (!encode_rows(&tm_k, p.k, rows, 1)) return cudaErrorInvalidValue;
+  } else {  // every entry is out of range: dummy copies read one zero row
+    void* z = nullptr;
+    if (cudaGetSymbolAddress(&z, g_zero_row) != cudaSuccess || !encode_rows(&tm_k, z, 1, 1))
+      return cudaErrorInvalidValue;
+  }
+  if (p.extra_k && p.extra_num_blocks >= 1 && !encode_rows(&tm_x, p.extra_k, p.extra_num_blocks, 1))
+    return cudaErrorInvalidValue;
+  if ((long long)p.B * p.H_q >= kQBoxRows &&
+      !encode_rows(&tm_q, p.q, (long long)p.B * p.H_q, kQBoxRows))
+    return cudaErrorInvalidValue;
+  if (grid < 2 || (grid & 1)) return cudaErrorInvalidValue;  // whole pairs only
   return launch_after(split_mla_kernel, dim3(grid), dim3(kThreads), (size_t)kSmemBytes, stream,
-                      p);
+                      p, tm_k, tm_x, tm_q);
 }
 
 }  // namespace da

@@ -95,3 +95,13 @@ def test_table_width_and_page_ids_do_not_matter(api):
     wl2 = W.Workload("moved", W.PAGED, wl.q, k2, v2, wl.lengths, t2, 16, 32, 8, 128, 128, wl.scale)
     o2, l2 = api.run_workload(wl2.to("cuda"))
     assert torch.equal(o, o2) and torch.equal(l, l2)
+
+
+def test_gqa_repeated_runs_bitwise(api):
+    """Back-to-back runs on one workspace give identical bits."""
+    wl = W.gqa_paged().to("cuda")
+    ws = api.workspace(api.problem_for(wl), "cuda")
+    out0, lse0 = [t.clone() for t in api.run_workload(wl, ws=ws)]
+    for _ in range(8):
+        out, lse = api.run_workload(wl, ws=ws)
+        assert torch.equal(out, out0) and torch.equal(lse, lse0)
