@@ -213,29 +213,37 @@ __device__ __forceinline__ MlaUnit mla_unit(const Launch& p, int u) {
   return x;
 }
 
-// Latent-cache row holding entry `tok` of row b (H_kv = 1); entries from
-// l_main on come from the second source (*src = 1).
-__device__ __forceinline__ bool latent_row(const Launch& p, int b, int tok, int l_main,
-                                           long long* row, int* src) {
+// Latent-cache row holding entry `tok` of row b (H_kv = 1), in two steps so
+// that the index load can be in flight while other work is issued:
+// latent_fetch loads the table word the entry needs (its page id or slot;
+// nothing for a contiguous cache), latent_decode turns it into the row and
+// the source (1 for entries from l_main on, which come from the second
+// source) and says whether the index is in range.
+__device__ __forceinline__ int latent_fetch(const Launch& p, int b, int tok, int l_main) {
+  if (tok >= l_main) return __ldg(p.extra_table + (size_t)b * p.extra_width + (tok - l_main));
+  if (p.layout == DA_KV_CONTIGUOUS) return 0;
+  if (p.layout == DA_KV_PAGED) return __ldg(p.table + (size_t)b * p.width + tok / p.page_size);
+  return __ldg(p.table + (size_t)b * p.width + tok);
+}
+
+__device__ __forceinline__ bool latent_decode(const Launch& p, int b, int tok, int l_main,
+                                              int word, long long* row, int* src) {
   *src = 0;
   if (tok >= l_main) {
-    const int slot = __ldg(p.extra_table + (size_t)b * p.extra_width + (tok - l_main));
-    *row = slot;
+    *row = word;
     *src = 1;
-    return slot >= 0 && slot < p.extra_num_blocks;
+    return word >= 0 && word < p.extra_num_blocks;
   }
   if (p.layout == DA_KV_CONTIGUOUS) {
     *row = (long long)b * p.width + tok;
     return true;
   }
   if (p.layout == DA_KV_PAGED) {
-    const int page = __ldg(p.table + (size_t)b * p.width + tok / p.page_size);
-    *row = (long long)page * p.page_size + tok % p.page_size;
-    return page >= 0 && page < p.num_blocks;
+    *row = (long long)word * p.page_size + tok % p.page_size;
+    return word >= 0 && word < p.num_blocks;
   }
-  const int slot = __ldg(p.table + (size_t)b * p.width + tok);
-  *row = slot;
-  return slot >= 0 && slot < p.num_blocks;
+  *row = word;
+  return word >= 0 && word < p.num_blocks;
 }
 
 // ---------------------------------------------------------------- producer
@@ -278,21 +286,27 @@ __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
       for (int i = pt; i < lines; i += 128)
         asm volatile("prefetch.global.L2 [%0];" ::"l"(qn + (size_t)i * 128));
     }
-    // lanes 0-15 of producer warp pw look up the rows of entries 16*pw .. 16*pw+15
-    // of a tile; the lookup for the next tile is issued before the copies of
-    // the current one so its latency hides behind them.
+    // Lane e < 16 of producer warp pw handles entry 16*pw + e of a tile.
+    // Table words are loaded two tiles ahead and decoded one tile ahead (the
+    // decoded rows of the next tile are prefetched into L2), so the index
+    // load's latency stays off the copy path.
     // src: 0 = main cache, 1 = second source.  Masked entries (past the end
     // of the split) and bad indices read row 0 of the main cache, so every
     // stage byte holds real data; masked scores are dropped by the softmax.
-    auto lookup = [&](int t0, int& row, int& src, bool& live) {
+    const int e_lane = kEntPerWarp * pw + pl;
+    auto fetch = [&](int t0) -> int {
+      const int tok = t0 + e_lane;
+      return (pl < kEntPerWarp && tok < x.t_end) ? latent_fetch(p, x.b, tok, x.l_main) : 0;
+    };
+    auto decode = [&](int t0, int word, int& row, int& src, bool& live) {
       row = 0;
       src = 0;
       live = false;
-      const int e = kEntPerWarp * pw + pl;
-      if (pl < kEntPerWarp && t0 + e < x.t_end) {
+      const int tok = t0 + e_lane;
+      if (pl < kEntPerWarp && tok < x.t_end) {
         long long r;
         int sr;
-        const bool good = latent_row(p, x.b, t0 + e, x.l_main, &r, &sr);
+        const bool good = latent_decode(p, x.b, tok, x.l_main, word, &r, &sr);
         bad |= !good;
         if (good) {
           row = (int)r;
@@ -301,17 +315,16 @@ __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
         }
       }
     };
-    int nx_row, nx_src;
-    bool nx_live;
-    lookup(x.t_begin, nx_row, nx_src, nx_live);
+    int my_row, my_src, nx_row = 0, nx_src = 0;
+    bool my_live, nx_live = false;
+    int nx_word = (x.t_begin + kSub < x.t_end) ? fetch(x.t_begin + kSub) : 0;
+    decode(x.t_begin, fetch(x.t_begin), my_row, my_src, my_live);
     for (int t0 = x.t_begin; t0 < x.t_end; t0 += kSub, ++g) {
       const int stage = g % kStages;
       if (!wait_w(kEmpty0 + stage, ((g / kStages) & 1) ^ 1)) {
         alive = false;
         break;
       }
-      const int my_row = nx_row, my_src = nx_src;
-      if (t0 + kSub < x.t_end) lookup(t0 + kSub, nx_row, nx_src, nx_live);
       const uint32_t full = bar_addr(c, kFull0 + stage);
       if (pt == 0) mbar_arrive_expect_tx(full, kStageBytes);
       // lane q < 4 copies the group of entries 16*pw + 4q .. 16*pw + 4q + 3
@@ -339,9 +352,15 @@ __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
                        full);
         }
       }
-      // the next tile's rows start towards L2 while this stage is consumed
+      // decode the next tile's words (loaded an iteration ago), load the
+      // words of the tile after it, and start the next tile's rows towards L2
+      if (t0 + kSub < x.t_end) decode(t0 + kSub, nx_word, nx_row, nx_src, nx_live);
+      if (t0 + 2 * kSub < x.t_end) nx_word = fetch(t0 + 2 * kSub);
       if (nx_live && t0 + kSub < x.t_end)
         prefetch_l2((nx_src ? p.extra_k : p.k) + (size_t)nx_row * kDqk, kDqk * 2);
+      my_row = nx_row;
+      my_src = nx_src;
+      my_live = nx_live;
     }
     ++n_ne;
   }
