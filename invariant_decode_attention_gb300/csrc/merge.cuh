@@ -8,8 +8,8 @@
 //     w_s = 2^(lse_s - M),   W = w_0 + w_1 + ... + w_{n-1}   (in this order)
 //     out = sum_s (w_s / W) * o_s                            (fp32, s ascending)
 //     lse = (M + log2 W) * ln 2                              (natural log)
-// The combine kernel and the split kernels' in-run merge both call these two
-// functions, so a row's bits do not depend on which of them merged it.
+// merge_weights forms the weights; the value sums are fp32 FMA chains
+// acc = fma(w_s / W, o_s, acc) from acc = 0, s ascending.
 #pragma once
 
 #include "common.cuh"
@@ -48,15 +48,6 @@ __device__ __forceinline__ float merge_weights(const float* lse, size_t stride, 
   }
   __syncwarp();
   return (W > 0.f) ? (M + lg2(W)) * kLn2 : -INFINITY;
-}
-
-// sum over s of coef[s] * o[s * stride], s ascending, one fp32 FMA chain.
-__device__ __forceinline__ float merge_value(const float* coef, const float* o, size_t stride,
-                                             int n) {
-  float acc = 0.f;
-#pragma unroll 8
-  for (int s = 0; s < n; ++s) acc = fmaf(coef[s], __ldcg(o + (size_t)s * stride), acc);
-  return acc;
 }
 
 }  // namespace da

@@ -78,6 +78,20 @@ constexpr int kSortKeys = 256;
 
 __device__ __forceinline__ int sort_key(int tiles) { return min(tiles, kSortKeys - 1); }
 
+// A row's split shape under the INVARIANT rule.
+struct RowSplits {
+  int n, tps, n_tiles, len;
+};
+
+__device__ __forceinline__ RowSplits invariant_splits(const PlanLaunch& p, int len) {
+  RowSplits r;
+  r.len = len;
+  r.n_tiles = ceil_div_i(len, p.tile);
+  r.tps = max(p.min_tps, ceil_div_i(r.n_tiles, p.max_splits));
+  r.n = max(1, ceil_div_i(r.n_tiles, r.tps));
+  return r;
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_invariant_kernel(PlanLaunch p) {
   __shared__ int bucket[kSortKeys];
   allow_next_grid();  // the split kernel may be staged now; it waits for us
@@ -85,43 +99,43 @@ __global__ void __launch_bounds__(kPlanThreads) plan_invariant_kernel(PlanLaunch
   for (int k = threadIdx.x; k < kSortKeys; k += kPlanThreads) bucket[k] = 0;
   __syncthreads();
   const int stride = p.max_splits + 1;
-  // pass 1: every row's splits; count items per key
+  // pass 1: every row's splits; count items per key.  A thread keeps its
+  // first row's shape in registers for pass 2.
+  RowSplits mine = {0, 1, 0, 0};
   for (int b = threadIdx.x; b < p.B; b += kPlanThreads) {
-    const int L = row_length(p, b);
-    const int n_tiles = ceil_div_i(L, p.tile);
-    const int tps = max(p.min_tps, ceil_div_i(n_tiles, p.max_splits));
-    const int n = max(1, ceil_div_i(n_tiles, tps));
-    p.n_splits[b] = n;
+    const RowSplits r = invariant_splits(p, row_length(p, b));
+    if (b == (int)threadIdx.x) mine = r;
+    p.n_splits[b] = r.n;
     int32_t* sb = p.split_begin + (size_t)b * stride;
-    for (int s = 0; s < n; ++s) sb[s] = min(s * tps, n_tiles);
-    sb[n] = n_tiles;
-    const int last = n_tiles - (n - 1) * tps;  // tiles of the last split
-    if (n > 1) atomicAdd(&bucket[sort_key(tps)], n - 1);
+    for (int s = 0; s < r.n; ++s) sb[s] = min(s * r.tps, r.n_tiles);
+    sb[r.n] = r.n_tiles;
+    const int last = r.n_tiles - (r.n - 1) * r.tps;  // tiles of the last split
+    if (r.n > 1) atomicAdd(&bucket[sort_key(r.tps)], r.n - 1);
     atomicAdd(&bucket[sort_key(last)], 1);
   }
   __syncthreads();
-  // bucket starts, largest key first (thread 0: 256 entries)
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int k = kSortKeys - 1; k >= 0; --k) {
-      const int c = bucket[k];
-      bucket[k] = acc;
-      acc += c;
-    }
-    p.hdr[kHdrNWork] = acc;
+  // bucket starts, largest key first: thread t < kSortKeys owns key
+  // kSortKeys - 1 - t, and a block scan in that order gives the starts
+  {
+    static_assert(kSortKeys <= kPlanThreads, "one thread per key");
+    const int key = kSortKeys - 1 - (int)threadIdx.x;
+    const int count = (key >= 0) ? bucket[key] : 0;
+    int total;
+    const int start = block_exclusive_scan(count, &total);
+    if (key >= 0) bucket[key] = start;
+    if (threadIdx.x == 0) p.hdr[kHdrNWork] = total;
   }
   __syncthreads();
   // pass 2: place every item in its bucket (order within a bucket is free)
   for (int b = threadIdx.x; b < p.B; b += kPlanThreads) {
-    const int n = p.n_splits[b];
-    const int32_t* sb = p.split_begin + (size_t)b * stride;
-    const int Lc = row_length_quiet(p, b);
-    for (int s = 0; s < n; ++s) {
+    const RowSplits r = (b == (int)threadIdx.x) ? mine
+                                                : invariant_splits(p, row_length_quiet(p, b));
+    for (int s = 0; s < r.n; ++s) {
       const int slot = b * p.max_splits + s;
-      const int pos = atomicAdd(&bucket[sort_key(sb[s + 1] - sb[s])], 1);
+      const int t0 = min(s * r.tps, r.n_tiles), t1 = min((s + 1) * r.tps, r.n_tiles);
+      const int pos = atomicAdd(&bucket[sort_key(t1 - t0)], 1);
       p.work[pos] = slot;
-      reinterpret_cast<int4*>(p.item_desc)[pos] =
-          make_int4(n == 1 ? ~slot : slot, sb[s], sb[s + 1], Lc);
+      reinterpret_cast<int4*>(p.item_desc)[pos] = make_int4(r.n == 1 ? ~slot : slot, t0, t1, r.len);
     }
   }
 }
