@@ -289,6 +289,31 @@ def e2e_steps(case, steps, warmup):
 
 # ----------------------------------------------------------------- CPU oracle
 
+def invariance_sweep(api, sizes=(1, 2, 4, 8, 16, 32, 64, 128)):
+    """The ragged sweep's target row (length 4096, GQA 32/8, d = 128) at a random
+    position among log-uniform batchmates, against its solo run, under each
+    policy: how many batches move any bit of its output or LSE, and the
+    largest output difference."""
+    from invariant_decode_attention_gb300 import workloads as W
+    sweep = W.RaggedSweep(sizes)
+    res = {}
+    for name, pol in (("invariant", api.INVARIANT), ("balanced", api.BALANCED)):
+        o_solo, l_solo = api.run_workload(sweep.solo(), policy=pol)
+        moved, max_abs = 0, 0.0
+        for i in range(len(sizes)):
+            wl, pos = sweep.batch(i)
+            o, l = api.run_workload(wl, policy=pol)
+            same = torch.equal(o[pos], o_solo[0]) and torch.equal(l[pos], l_solo[0])
+            moved += 0 if same else 1
+            max_abs = max(max_abs, (o[pos].float() - o_solo[0].float()).abs().max().item())
+        res[name] = {"batches_moving_target_row": moved, "batches": len(sizes),
+                     "max_absdiff_out": max_abs}
+    res["batch_sizes"] = list(sizes)
+    del sweep
+    torch.cuda.empty_cache()
+    return res
+
+
 def cpu_oracle_rate(wl, budget_s=15.0, max_rows=None):
     """Time the fp64 oracle, as it stands, on whole rows of the workload until
     the budget is spent.  Returns (GB/s, rows/s, rows done, seconds)."""
@@ -464,6 +489,7 @@ def main():
             del c2, w2
             torch.cuda.empty_cache()
         line["other_workloads"] = extra
+        line["invariance_sweep"] = invariance_sweep(api)
         gbs, rps, done, dt = cpu_oracle_rate(wl)
         line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": _CORES,
                                 "kind": "oracle", "rows_per_s": round(rps, 3),

@@ -192,6 +192,17 @@ __device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity) {
   }
 }
 
+// The units a CTA takes.  Unit 2i + h is value half h of work item i; CTA
+// pair q (CTAs 2q, 2q + 1) takes item k * pairs + q in even rounds k and
+// k * pairs + (pairs - 1 - q) in odd ones.  The list is sorted largest
+// first, so this serpentine deal evens out the pairs' sums.  Placement
+// only: no unit's arithmetic depends on its CTA.
+__device__ __forceinline__ int next_unit(int u) {
+  const int pairs = gridDim.x >> 1, q = blockIdx.x >> 1;
+  const int k = (u >> 1) / pairs + 1;
+  return 2 * (k * pairs + ((k & 1) ? pairs - 1 - q : q)) + (u & 1);
+}
+
 // A unit: one half of the value dims of one (row, split) item.
 struct MlaUnit {
   int slot, b, half, t_begin, t_end;  // entry range [t_begin, t_end)
@@ -261,7 +272,7 @@ __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
   };
   const int q_boxes = (min(p.H_q, kHeads) + kQBoxRows - 1) / kQBoxRows;  // per region
-  for (int u = blockIdx.x; u < n_units && alive; u += gridDim.x) {
+  for (int u = blockIdx.x; u < n_units && alive; u = next_unit(u)) {
     const MlaUnit x = mla_unit(p, u);
     if (x.empty) continue;
     // Q dims 256..575 of row b into shared memory once the previous unit's S
@@ -279,8 +290,8 @@ __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
     }
     // warm L2 with the next unit's query rows (its softmax warps load them
     // into tensor memory at its start)
-    if (u + (int)gridDim.x < n_units) {
-      const MlaUnit nx = mla_unit(p, u + gridDim.x);
+    if (next_unit(u) < n_units) {
+      const MlaUnit nx = mla_unit(p, next_unit(u));
       const char* qn = reinterpret_cast<const char*>(p.q + (size_t)nx.b * p.H_q * kDqk);
       const int lines = min(p.H_q, kHeads) * kDqk * 2 / 128;
       for (int i = pt; i < lines; i += 128)
@@ -388,7 +399,7 @@ __device__ void mma_issuer(const Launch& p, const Ctx& c, uint32_t tmem, int n_u
       umma::smem_desc(c.sbase, 16, 1024, umma::kSwizzle128B);
   const uint64_t b_v0 =      // V = leading dims of the K tile, MN-major
       umma::smem_desc(c.sbase + kStageOffset, kStageRegion, 1024, umma::kSwizzle128B);
-  for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+  for (int u = blockIdx.x; u < n_units; u = next_unit(u)) {
     const MlaUnit x = mla_unit(p, u);
     if (x.empty) continue;
     const int n_sub = (x.t_end - x.t_begin + kSub - 1) / kSub;
@@ -488,7 +499,7 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
     arrive_w(kQTFull);
   };
   bool q_ready = false;  // Q of the coming unit already in TMEM
-  for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+  for (int u = blockIdx.x; u < n_units; u = next_unit(u)) {
     const MlaUnit x = mla_unit(p, u);
     const bool head_ok = row < p.H_q;
     const size_t out_row = ((size_t)x.b * p.H_q + row) * 512 + x.half * kDvHalf;
@@ -578,7 +589,7 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
         // All S MMAs of this unit are done (S of the last tile was read), so
         // TMEM columns [0, 128) are free: load the next unit's Q now and let
         // the MMA thread start on it while this unit's epilogue runs.
-        for (int u2 = u + gridDim.x; u2 < n_units; u2 += gridDim.x) {
+        for (int u2 = next_unit(u); u2 < n_units; u2 = next_unit(u2)) {
           const MlaUnit x2 = mla_unit(p, u2);
           if (x2.empty) continue;
           if (!wait_w(kQFree, n_ne & 1)) return;
