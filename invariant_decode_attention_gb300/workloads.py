@@ -14,6 +14,10 @@ Cache layouts (``H`` = KV heads, ``D`` = head dim, bf16):
 * indexed:    ``[num_slots, H, D]`` + ``table int32[B, width]`` of slot indices
               (a row's top-k list); entries past the row's length hold -1
 
+A quantized workload (``kv_fp8``) holds K and V as E4M3 bytes (uint8) with
+one fp32 scale per cache; ``quantize_fp8`` makes one from a bf16 workload by
+torch's own float8_e4m3fn conversion of value / scale.
+
 The named workloads follow the five configurations the pages' problem
 statement is measured on (tiny dense, GQA paged, MLA-style sparse, ragged
 invariance sweep, long context); sizes are spelled out in each function.
@@ -52,6 +56,10 @@ class Workload:
     extra_v: Optional[torch.Tensor] = None        # [slots, H_kv, D_v] or None (latent)
     extra_table: Optional[torch.Tensor] = None    # int32 [B, extra_width]
     extra_lengths: Optional[torch.Tensor] = None  # int32 [B]
+    # quantized cache: k and v are E4M3 bytes (uint8), value = scale * e4m3
+    kv_fp8: bool = False
+    k_scale: float = 1.0
+    v_scale: float = 1.0
 
     @property
     def B(self):
@@ -76,8 +84,9 @@ class Workload:
         n = int(self.lengths.to(torch.int64).sum())
         if self.extra_lengths is not None:
             n += int(self.extra_lengths.to(torch.int64).sum())
-        per_entry_k = self.H_kv * self.D_qk * 2
-        per_entry_v = 0 if self.v is None else self.H_kv * self.D_v * 2
+        eb = 1 if self.kv_fp8 else 2
+        per_entry_k = self.H_kv * self.D_qk * eb
+        per_entry_v = 0 if self.v is None else self.H_kv * self.D_v * eb
         return n * (per_entry_k + per_entry_v)
 
     def to(self, device):
@@ -317,3 +326,28 @@ def mla_sparse_extra(seed=1005):
     g = torch.Generator().manual_seed(seed)
     el = torch.randint(0, 513, (64,), generator=g, dtype=torch.int64)
     return with_extra(mla_sparse(), el.tolist(), 16384, width=512, seed=seed + 1)
+
+
+def quantize_fp8(wl, k_scale=1.0 / 64, v_scale=1.0 / 64, name=None):
+    """The same workload with its K and V caches stored as E4M3 bytes:
+    ``bytes = float8_e4m3fn(value / scale)`` (torch's conversion, round to
+    nearest even).  With N(0, 1) data and scale 1/64 every value stays far
+    inside the format's range (|value / scale| < 448)."""
+    assert wl.v is not None and wl.extra_k is None, "separate K and V, one source"
+    def q8(t, scale):
+        return (t.float() / scale).to(torch.float8_e4m3fn).view(torch.uint8)
+    return dataclasses.replace(wl, k=q8(wl.k, k_scale), v=q8(wl.v, v_scale), kv_fp8=True,
+                               k_scale=float(k_scale), v_scale=float(v_scale),
+                               name=name or wl.name + "_fp8")
+
+
+def gqa_paged_fp8(seed=1001):
+    """The GQA paged workload (32 rows, 32/8 heads, d = 128, page 16, lengths
+    512..8192) with an E4M3 KV cache, scales 1/64."""
+    return quantize_fp8(gqa_paged(seed), name="gqa_paged_fp8_b32_h32x8_d128_p16")
+
+
+def long_context_fp8(seed=1004):
+    """The long-context workload (8 x 131072, 32/8 heads, d = 128, page 64)
+    with an E4M3 KV cache, scales 1/64."""
+    return quantize_fp8(long_context(seed), name="long_context_fp8_b8_l131072_h32x8_d128_p64")

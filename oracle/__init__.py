@@ -22,6 +22,9 @@ What it computes and where that is stated:
 * ``plan.plan_balanced`` -- batch-wide quota + greedy packing.  Source: same
   page, "Where it comes from" (``payload = ceil_div(total_num_blocks,
   num_sm_parts) + fixed_overhead_num_blocks`` and the greedy packing loop).
+* ``fp8`` -- exact fp64 decode of an FP8 E4M3 key/value cache with one
+  scale per cache (the reading of the pages' low-precision checkpoints,
+  stated in the module).
 * ``bf16`` -- exact fp64 -> bf16 round-to-nearest-even, used to state the
   output rounding and the tolerance in units of bf16 ULP (same page,
   Measurement: "1-2 ULP of bf16 near 1.0").
@@ -30,4 +33,4 @@ Parity pins (``tests/test_oracle_*.py``) tie every function to closed forms,
 brute force and invariants; no function here is "parity unpinned".
 """
 
-from . import attention, plan, bf16  # noqa: F401
+from . import attention, plan, bf16, fp8  # noqa: F401

@@ -6,6 +6,7 @@ import torch
 
 from oracle import attention as A
 from oracle import bf16 as OB
+from oracle import fp8 as OF
 
 # Parity bar (out): |gpu - oracle| <= max(1e-2, one bf16 ULP of the oracle
 # value).  A correctly rounded bf16 result is within half a ULP of the exact
@@ -32,9 +33,31 @@ class Bf16Cache:
         return self.t[idx].double().numpy()
 
 
+class Fp8Cache:
+    """Read-only view of an E4M3 byte cache (uint8 torch tensor) with its
+    scale; every read is decoded by the oracle (exact fp64)."""
+
+    def __init__(self, t, scale):
+        self.t = t
+        self.scale = scale
+        self.shape = tuple(t.shape)
+
+    def __getitem__(self, idx):
+        if not isinstance(idx, tuple):
+            idx = (idx,)
+        idx = tuple(torch.as_tensor(np.asarray(i)) if not isinstance(i, (int, slice)) else i
+                    for i in idx)
+        return OF.dequantize(self.t[idx].numpy(), self.scale)
+
+
 def oracle_for(wl, rows=None, heads=None):
     """fp64 oracle (out, lse) of a CPU workload, optionally on a subset."""
     table = None if wl.table is None else wl.table.numpy()
+    if getattr(wl, "kv_fp8", False):
+        return A.attend(wl.q.double().numpy(), Fp8Cache(wl.k, wl.k_scale),
+                        Fp8Cache(wl.v, wl.v_scale), wl.lengths.numpy(), scale=wl.scale,
+                        layout=wl.layout, table=table, page_size=wl.page_size, d_v=wl.D_v,
+                        rows=rows, heads=heads)
     extra = {}
     if getattr(wl, "extra_k", None) is not None:
         extra = dict(extra_k=Bf16Cache(wl.extra_k),
