@@ -180,6 +180,10 @@ def build_workload(name, rank=0):
         return W.tiny(seed=1000 + seed_shift)
     if name == "mla_sparse":
         return W.mla_sparse(seed=1002 + seed_shift)
+    if name == "gqa_paged_fp8":
+        return W.gqa_paged_fp8(seed=1001 + seed_shift)
+    if name == "long_context_fp8":
+        return W.long_context_fp8(seed=1004 + seed_shift)
     raise ValueError(name)
 
 
@@ -355,7 +359,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gqa_paged",
-                    choices=["gqa_paged", "long_context", "tiny", "mla_sparse"])
+                    choices=["gqa_paged", "long_context", "tiny", "mla_sparse", "gqa_paged_fp8",
+                             "long_context_fp8"])
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the secondary workloads and the CPU baseline")
     args = ap.parse_args()
@@ -454,12 +459,12 @@ def main():
     }
     if not args.no_extra:
         extra = {}
-        for name in ("long_context", "mla_sparse", "tiny"):
+        for name in ("long_context", "mla_sparse", "tiny", "gqa_paged_fp8", "long_context_fp8"):
             if name == args.workload:
                 continue
             w2 = build_workload(name)
             c2 = GpuCase(w2, dev, api.INVARIANT)
-            n = 20 if name == "long_context" else 200
+            n = 20 if name.startswith("long_context") else 200
             # inputs that fit in L2 (the MLA cache is 75.5 MB) are flushed between steps
             fl = w2.kv_bytes() < L2_FLUSH_BELOW
             ms2, _, _ = time_steps(c2, n, 5, split_events=False, flush=fl)
@@ -475,6 +480,7 @@ def main():
                 "rows_per_s": round(w2.B / (ms2 * 1e-3), 1),
                 "hbm_frac": round(kvb / (ms2 * 1e-3) / 1e9 / peak, 4),
                 "split_ms_avg": round(sp, 5),
+                "hbm_frac_split": round(kvb / (sp * 1e-3) / 1e9 / peak, 4),
                 "balanced_ms_per_step": round(bms, 5),
                 "l2": "flushed between steps" if fl else "inputs larger than L2",
             }
@@ -484,7 +490,6 @@ def main():
                 rec["tensor_tflops_split"] = round(flops / (sp * 1e-3) / 1e12, 1)
                 rec["tensor_frac_split_of_measured_bf16"] = round(
                     flops / (sp * 1e-3) / 1e12 / tensor_peak(), 4)
-                rec["hbm_frac_split"] = round(kvb / (sp * 1e-3) / 1e9 / peak, 4)
             extra[w2.name] = rec
             del c2, w2
             torch.cuda.empty_cache()

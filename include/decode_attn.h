@@ -67,6 +67,19 @@ extern "C" {
  * entries at t >= length are never read                                   */
 #define DA_KV_INDEXED 2
 
+/* ---- KV element types (da_problem.kv_dtype) ------------------------- */
+#define DA_KV_BF16 0     /* bf16 K and V                                      */
+/* One byte per element in the 8-bit E4M3 floating-point layout (bias 7,
+ * subnormals, no infinities, S.1111.111 = NaN) with one fp32 scale per cache:
+ * element value = scale * e4m3(byte).  The pages run low-precision
+ * checkpoints (FlashMLA issue #212, Environment: NVFP4 DeepSeek-V4-Flash;
+ * gllm issue #98, Observation: NVFP4 Nemotron) but name no cache format;
+ * this is the library's reading.  The kernel converts each byte exactly to
+ * fp32, applies k_scale to the softmax scale and v_scale to a unit's output
+ * (fixed roundings, independent of the batch).  CUDA-core variant, one KV
+ * source only; other combinations return DA_ERR_UNSUPPORTED.              */
+#define DA_KV_FP8_E4M3 1
+
 /* ---- kernel variants (chosen from the head config only, never B) ----- */
 #define DA_VARIANT_FMA 0 /* CUDA-core fp32 FMA, H_q/H_kv in {1,2,4,8}, D in {64,128} */
 #define DA_VARIANT_MLA 1 /* tcgen05 tensor cores, shared latent 576/512, 16..128 heads */
@@ -97,6 +110,9 @@ typedef struct da_problem {
   /* list after its main entries.  0 / 0 when unused.                         */
   int32_t extra_width;      /* extra index row width (max extra entries)      */
   int64_t extra_num_blocks; /* slots in the extra cache                       */
+  int32_t kv_dtype;         /* DA_KV_BF16 (0) or DA_KV_FP8_E4M3               */
+  float k_scale;            /* DA_KV_FP8_E4M3: K element scale (finite, > 0)  */
+  float v_scale;            /* DA_KV_FP8_E4M3: V element scale (finite, > 0)  */
 } da_problem;
 
 /* A plan: filled by decode_attn_plan, read by run/combine.  Host memory,

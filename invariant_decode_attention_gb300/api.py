@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libd
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA = 0, 1, 2, 3, 4
 INVARIANT, BALANCED = 0, 1
+KV_BF16, KV_FP8_E4M3 = 0, 1
 CONTIGUOUS, PAGED, INDEXED = 0, 1, 2
 VARIANT_FMA, VARIANT_MLA = 0, 1
 DEVERR_LENGTH, DEVERR_INDEX, DEVERR_TIMEOUT = 1, 2, 4
@@ -53,6 +54,9 @@ class DaProblem(ctypes.Structure):
         ("flags", ctypes.c_uint32),
         ("extra_width", ctypes.c_int32),
         ("extra_num_blocks", ctypes.c_int64),
+        ("kv_dtype", ctypes.c_int32),
+        ("k_scale", ctypes.c_float),
+        ("v_scale", ctypes.c_float),
     ]
 
 
@@ -144,6 +148,11 @@ def _ptr(t: Optional[torch.Tensor]):
     return ctypes.c_void_p(t.data_ptr())
 
 
+# cache tensors: bf16, or E4M3 bytes (uint8 / float8_e4m3fn) for DA_KV_FP8_E4M3
+_KV = (torch.bfloat16, torch.uint8) + ((torch.float8_e4m3fn,)
+                                        if hasattr(torch, "float8_e4m3fn") else ())
+
+
 def _dev_ptr(t: Optional[torch.Tensor], name: str, dtype=None):
     if t is None:
         return None
@@ -151,7 +160,7 @@ def _dev_ptr(t: Optional[torch.Tensor], name: str, dtype=None):
         raise ValueError(f"{name} must be a CUDA tensor (no CPU path)")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
-    if dtype is not None and t.dtype != dtype:
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     return ctypes.c_void_p(t.data_ptr())
 
@@ -164,14 +173,14 @@ def _stream(stream):
 
 def problem(*, batch, num_q_heads, num_kv_heads, head_dim_qk, head_dim_v=None, layout,
             scale, page_size=0, width=0, num_blocks=0, shared_latent=False, extra_width=0,
-            extra_num_blocks=0) -> DaProblem:
+            extra_num_blocks=0, kv_dtype=KV_BF16, k_scale=1.0, v_scale=1.0) -> DaProblem:
     """Fill a ``da_problem``.  ``layout`` is a name or a DA_KV_* code."""
     if isinstance(layout, str):
         layout = LAYOUT_CODES[layout]
     return DaProblem(batch, num_q_heads, num_kv_heads, head_dim_qk,
                      head_dim_qk if head_dim_v is None else head_dim_v, layout, page_size,
                      width, num_blocks, scale, int(bool(shared_latent)), 0, extra_width,
-                     extra_num_blocks)
+                     extra_num_blocks, kv_dtype, k_scale, v_scale)
 
 
 def problem_for(wl) -> DaProblem:
@@ -182,7 +191,9 @@ def problem_for(wl) -> DaProblem:
                    page_size=wl.page_size if wl.layout == "paged" else 0, width=wl.width,
                    num_blocks=wl.num_blocks, shared_latent=wl.v is None,
                    extra_width=wl.extra_table.shape[1] if extra else 0,
-                   extra_num_blocks=wl.extra_k.shape[0] if extra else 0)
+                   extra_num_blocks=wl.extra_k.shape[0] if extra else 0,
+                   kv_dtype=KV_FP8_E4M3 if getattr(wl, "kv_fp8", False) else KV_BF16,
+                   k_scale=getattr(wl, "k_scale", 1.0), v_scale=getattr(wl, "v_scale", 1.0))
 
 
 def version() -> str:
@@ -221,7 +232,7 @@ def plan(prob: DaProblem, policy: int, lengths: torch.Tensor, ws: torch.Tensor,
 
 def run(pl: DaPlan, q, k, v, table, lengths, out, lse, stream=None):
     _check(lib().decode_attn_run(ctypes.byref(pl), _dev_ptr(q, "q", torch.bfloat16),
-                                 _dev_ptr(k, "k", torch.bfloat16), _dev_ptr(v, "v", torch.bfloat16),
+                                 _dev_ptr(k, "k", _KV), _dev_ptr(v, "v", _KV),
                                  _dev_ptr(table, "table", torch.int32),
                                  _dev_ptr(lengths, "lengths", torch.int32),
                                  _dev_ptr(out, "out", torch.bfloat16),
@@ -237,8 +248,8 @@ def combine(pl: DaPlan, out, lse, stream=None):
 def forward(prob: DaProblem, policy, q, k, v, table, lengths, ws, out, lse, stream=None):
     """plan + run + combine through the single C entry point."""
     _check(lib().decode_attn_forward(ctypes.byref(prob), policy, _dev_ptr(q, "q", torch.bfloat16),
-                                     _dev_ptr(k, "k", torch.bfloat16),
-                                     _dev_ptr(v, "v", torch.bfloat16),
+                                     _dev_ptr(k, "k", _KV),
+                                     _dev_ptr(v, "v", _KV),
                                      _dev_ptr(table, "table", torch.int32),
                                      _dev_ptr(lengths, "lengths", torch.int32),
                                      _dev_ptr(ws, "workspace"), ws.numel() * ws.element_size(),
@@ -255,8 +266,8 @@ def forward_static(prob: DaProblem, policy, q, k, v, table, lengths, out, lse, s
     device must not overlap on the GPU."""
     _check(lib().decode_attn_forward_static(ctypes.byref(prob), policy,
                                             _dev_ptr(q, "q", torch.bfloat16),
-                                            _dev_ptr(k, "k", torch.bfloat16),
-                                            _dev_ptr(v, "v", torch.bfloat16),
+                                            _dev_ptr(k, "k", _KV),
+                                            _dev_ptr(v, "v", _KV),
                                             _dev_ptr(table, "table", torch.int32),
                                             _dev_ptr(lengths, "lengths", torch.int32),
                                             _dev_ptr(out, "out", torch.bfloat16),
@@ -277,8 +288,8 @@ def plan_extra(prob: DaProblem, policy: int, lengths, extra_lengths, ws, stream=
 def run_extra(pl: DaPlan, q, k, v, table, lengths, extra_k, extra_v, extra_indices,
               extra_lengths, out, lse, stream=None):
     _check(lib().decode_attn_run_extra(
-        ctypes.byref(pl), _dev_ptr(q, "q", torch.bfloat16), _dev_ptr(k, "k", torch.bfloat16),
-        _dev_ptr(v, "v", torch.bfloat16), _dev_ptr(table, "table", torch.int32),
+        ctypes.byref(pl), _dev_ptr(q, "q", torch.bfloat16), _dev_ptr(k, "k", _KV),
+        _dev_ptr(v, "v", _KV), _dev_ptr(table, "table", torch.int32),
         _dev_ptr(lengths, "lengths", torch.int32), _dev_ptr(extra_k, "extra_k", torch.bfloat16),
         _dev_ptr(extra_v, "extra_v", torch.bfloat16),
         _dev_ptr(extra_indices, "extra_indices", torch.int32),
@@ -292,7 +303,7 @@ def forward_extra(prob: DaProblem, policy, q, k, v, table, lengths, extra_k, ext
     """plan + run + combine over a main and a second (index-gathered) KV source."""
     _check(lib().decode_attn_forward_extra(
         ctypes.byref(prob), policy, _dev_ptr(q, "q", torch.bfloat16),
-        _dev_ptr(k, "k", torch.bfloat16), _dev_ptr(v, "v", torch.bfloat16),
+        _dev_ptr(k, "k", _KV), _dev_ptr(v, "v", _KV),
         _dev_ptr(table, "table", torch.int32), _dev_ptr(lengths, "lengths", torch.int32),
         _dev_ptr(extra_k, "extra_k", torch.bfloat16), _dev_ptr(extra_v, "extra_v", torch.bfloat16),
         _dev_ptr(extra_indices, "extra_indices", torch.int32),

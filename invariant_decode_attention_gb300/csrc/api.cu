@@ -42,12 +42,20 @@ int check_problem(const da_problem* p) {
   if (p->extra_width < 0 || p->extra_num_blocks < 0) return DA_ERR_INVALID_ARG;
   if (row_capacity(p->layout, p->width, p->page_size) + p->extra_width > 0x7fffffffLL)
     return DA_ERR_INVALID_ARG;
+  if (p->kv_dtype != DA_KV_BF16 && p->kv_dtype != DA_KV_FP8_E4M3) return DA_ERR_INVALID_ARG;
+  if (p->kv_dtype == DA_KV_FP8_E4M3 &&
+      !(std::isfinite(p->k_scale) && p->k_scale > 0.f && std::isfinite(p->v_scale) &&
+        p->v_scale > 0.f))
+    return DA_ERR_INVALID_ARG;
   return DA_OK;
 }
 
 // The kernel variant follows from the head configuration alone -- never from
 // the batch size or the lengths.
 int select_variant(const da_problem* p, Variant* v) {
+  // E4M3 caches: CUDA-core variant, one KV source
+  if (p->kv_dtype == DA_KV_FP8_E4M3 && (p->shared_latent || p->extra_width > 0))
+    return DA_ERR_UNSUPPORTED;
   if (p->shared_latent) {
     if (p->head_dim_qk == 576 && p->head_dim_v == 512 && p->num_kv_heads == 1 &&
         mla_supported(p->num_q_heads)) {
@@ -135,6 +143,11 @@ Launch make_launch(const da_plan* plan) {
   }
   L.max_splits = plan->max_splits;
   L.scale_log2 = pr.scale * kLog2e;
+  if (pr.kv_dtype == DA_KV_FP8_E4M3) {  // scores of E4M3 keys: scale * k_scale
+    L.kv_fp8 = 1;
+    L.scale_log2 *= pr.k_scale;
+    L.v_scale = pr.v_scale;
+  }
   return L;
 }
 

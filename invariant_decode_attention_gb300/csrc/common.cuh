@@ -65,7 +65,9 @@ struct Launch {
   int layout, page_size, width, capacity;
   int page_shift;  // log2(page_size) when it is a power of two, else -1
   int max_splits;
-  float scale_log2;  // softmax scale * log2(e)
+  float scale_log2;  // softmax scale * log2(e) (* k_scale for an E4M3 cache)
+  int kv_fp8;        // K and V are E4M3 bytes
+  float v_scale;     // E4M3 cache: multiplies each unit's output
 };
 
 struct PlanLaunch {

@@ -26,7 +26,8 @@
 namespace da {
 namespace {
 
-template <int G, int D>
+// F8: the K and V caches hold E4M3 bytes (DA_KV_FP8_E4M3) instead of bf16.
+template <int G, int D, bool F8 = false>
 struct FmaShape {
   static constexpr int kTile = kFmaTile;               // entries per tile
   static constexpr int kWarps = 4;
@@ -36,7 +37,10 @@ struct FmaShape {
   static constexpr int kChunks = D / 64;                // 16-byte chunks per lane per row
   static constexpr int kDpl = kChunks * 8;              // dims per lane
   static constexpr int kStages = 3;                     // ring slots per warp
-  static constexpr int kRowBytes = D * 2;
+  static constexpr int kRowBytes = D * (F8 ? 1 : 2);
+  // 16-byte copies per lane per row (8 lanes per row; an E4M3 row of 64 dims
+  // is four copies, made by lanes 0-3)
+  static constexpr int kCopies = F8 ? (D + 127) / 128 : D / 64;
   static constexpr int kSliceBytes = kTokPerWarp * kRowBytes;  // K (or V) of one warp
   static constexpr int kWarpSlotBytes = 2 * kSliceBytes;
   static constexpr int kRingBytes = kStages * kWarps * kWarpSlotBytes;
@@ -145,10 +149,10 @@ __device__ __forceinline__ void cursor_next(const Launch& p, Cursor& c, int n_un
 
 // Issue this warp's copies for the cursor's tile into ring slot `slot`, then
 // close the cp.async group (always, so group counting stays uniform).
-template <int G, int D, bool X>
+template <int G, int D, bool X, bool F8>
 __device__ __forceinline__ void load_slice(const Launch& p, const Cursor& c, uint8_t* smem,
                                            int slot, int warp, int lane) {
-  using S = FmaShape<G, D>;
+  using S = FmaShape<G, D, F8>;
   if (c.valid) {
     const int grp = lane >> 3, sub = lane & 7;
     uint8_t* ks = smem + (slot * S::kWarps + warp) * S::kWarpSlotBytes;
@@ -182,14 +186,16 @@ __device__ __forceinline__ void load_slice(const Launch& p, const Cursor& c, uin
         const bool ok = uniform ? base_ok : entry_row<X>(p, c.x.b, tok, c.x.l_main, &row, &src);
         bad |= !ok;
         if (ok) {
-          const size_t off = ((size_t)row * p.H_kv + c.x.h) * D;
-          const __nv_bfloat16* kb = (X && src) ? p.extra_k : p.k;
-          const __nv_bfloat16* vb = (X && src) ? p.extra_v : p.v;
+          // byte offset of the row of KV head h
+          const size_t off = ((size_t)row * p.H_kv + c.x.h) * S::kRowBytes;
+          const char* kb = reinterpret_cast<const char*>((X && src) ? p.extra_k : p.k);
+          const char* vb = reinterpret_cast<const char*>((X && src) ? p.extra_v : p.v);
 #pragma unroll
-          for (int ch = 0; ch < S::kChunks; ++ch) {
-            const int e = (sub + 8 * ch) * 8;  // element offset of this 16-byte chunk
-            cp_async16(smem_addr(ks + tl * S::kRowBytes + e * 2), kb + off + e);
-            cp_async16(smem_addr(vs + tl * S::kRowBytes + e * 2), vb + off + e);
+          for (int ch = 0; ch < S::kCopies; ++ch) {
+            const int e = (sub + 8 * ch) * 16;  // byte offset of this 16-byte copy
+            if (F8 && e >= S::kRowBytes) continue;
+            cp_async16(smem_addr(ks + tl * S::kRowBytes + e), kb + off + e);
+            cp_async16(smem_addr(vs + tl * S::kRowBytes + e), vb + off + e);
           }
         }
       }
@@ -221,6 +227,36 @@ __device__ __forceinline__ void unpack_row2(const uint8_t* row, int sub, uint64_
   }
 }
 
+// The same for an E4M3 row: 8 bytes per lane per 64 dims, each byte converted
+// exactly to fp32 (E4M3 values are all representable in f16, and f16 in fp32).
+template <int D>
+__device__ __forceinline__ void unpack_row2_f8(const uint8_t* row, int sub, uint64_t* f) {
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) {
+    const uint2 w = reinterpret_cast<const uint2*>(row)[sub + 8 * c];
+    const uint32_t words[2] = {w.x, w.y};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const unsigned short two = (unsigned short)(words[h] >> (16 * e));
+        uint32_t h2;
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
+        const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
+        f[c * 4 + h * 2 + e] = pack2(__low2float(hv), __high2float(hv));
+      }
+    }
+  }
+}
+
+template <int D, bool F8>
+__device__ __forceinline__ void unpack_kv2(const uint8_t* row, int sub, uint64_t* f) {
+  if constexpr (F8)
+    unpack_row2_f8<D>(row, sub, f);
+  else
+    unpack_row2<D>(row, sub, f);
+}
+
 // Lane-dependent orders that let the 8 lanes of an entry group reduce their
 // partial dot products by halving (each level: v[i] += shfl_xor(v[i + half]))
 // with no data-dependent selects.  For G >= 2 a lane with sub-lane bits
@@ -248,13 +284,13 @@ __device__ __forceinline__ int hperm_of(int sub) {
 // lane's own entries only; lanes are summed at the end of the unit.
 // G == 1: every lane of a group ends with the group's scores (butterfly) and
 // l[0] counts the group's entries.
-template <int G, int D, bool kPartial>
+template <int G, int D, bool F8, bool kPartial>
 __device__ __forceinline__ void consume_slice(const uint8_t* ks, int lane, int n_valid,
                                               const uint64_t (&q2)[G][FmaShape<G, D>::kDpl / 2],
                                               float (&m)[G], float (&l)[G],
                                               uint64_t (&acc2)[G][FmaShape<G, D>::kDpl / 2],
                                               float scale_log2) {
-  using S = FmaShape<G, D>;
+  using S = FmaShape<G, D, F8>;
   constexpr int kP = S::kDpl / 2;  // packed pairs per lane
   constexpr int kV = S::kSteps * G;  // partial scores per lane
   const int grp = lane >> 3, sub = lane & 7;
@@ -266,7 +302,7 @@ __device__ __forceinline__ void consume_slice(const uint8_t* ks, int lane, int n
 #pragma unroll
   for (int js = 0; js < S::kSteps; ++js) {
     uint64_t k2[kP];
-    unpack_row2<D>(ks + (4 * (js ^ tp) + grp) * S::kRowBytes, sub, k2);
+    unpack_kv2<D, F8>(ks + (4 * (js ^ tp) + grp) * S::kRowBytes, sub, k2);
 #pragma unroll
     for (int hs = 0; hs < G; ++hs) {
       uint64_t a = ffma2(q2[hs][0], k2[0], 0ull);
@@ -374,7 +410,7 @@ __device__ __forceinline__ void consume_slice(const uint8_t* ks, int lane, int n
     const int row = 4 * (js ^ tp) + grp;
     if (kPartial && row >= n_valid) continue;  // never read unfilled rows
     uint64_t v2[kP];
-    unpack_row2<D>(vs + row * S::kRowBytes, sub, v2);
+    unpack_kv2<D, F8>(vs + row * S::kRowBytes, sub, v2);
 #pragma unroll
     for (int hs = 0; hs < G; ++hs) {
       const uint64_t p2 = pack2(pfull[js][hs], pfull[js][hs]);
@@ -384,9 +420,9 @@ __device__ __forceinline__ void consume_slice(const uint8_t* ks, int lane, int n
   }
 }
 
-template <int G, int D, bool X>
+template <int G, int D, bool X, bool F8>
 __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Launch p) {
-  using S = FmaShape<G, D>;
+  using S = FmaShape<G, D, F8>;
   extern __shared__ __align__(128) uint8_t smem[];
   float* scratch = reinterpret_cast<float*>(smem + S::kScratchOffset);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -401,7 +437,7 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
   cursor_seek<X>(p, pf, blockIdx.x, load_desc(p, blockIdx.x), n_units);
 #pragma unroll
   for (int s = 0; s < S::kStages - 1; ++s) {
-    load_slice<G, D, X>(p, pf, smem, s, warp, lane);
+    load_slice<G, D, X, F8>(p, pf, smem, s, warp, lane);
     cursor_next<X>(p, pf, n_units);
   }
 
@@ -430,18 +466,18 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
         const uint8_t* sq = smem + S::kQOffset + slot * S::kQPad;
 #pragma unroll
         for (int hs = 0; hs < G; ++hs)
-          unpack_row2<D>(sq + (hs ^ hperm_of<G>(sub)) * S::kRowBytes, sub, q2[hs]);
+          unpack_row2<D>(sq + (hs ^ hperm_of<G>(sub)) * (D * 2), sub, q2[hs]);  // bf16 q
         named_bar_sync(1, S::kThreads);
       }
       // refill the slot consumed in the previous iteration
-      load_slice<G, D, X>(p, pf, smem, (slot + S::kStages - 1) % S::kStages, warp, lane);
+      load_slice<G, D, X, F8>(p, pf, smem, (slot + S::kStages - 1) % S::kStages, warp, lane);
       cursor_next<X>(p, pf, n_units);
       const uint8_t* ks = smem + (slot * S::kWarps + warp) * S::kWarpSlotBytes;
       const int n_valid = min(S::kTokPerWarp, x.L - k * S::kTile - warp * S::kTokPerWarp);
       if (n_valid >= S::kTokPerWarp)
-        consume_slice<G, D, false>(ks, lane, n_valid, q2, m, l, acc2, p.scale_log2);
+        consume_slice<G, D, F8, false>(ks, lane, n_valid, q2, m, l, acc2, p.scale_log2);
       else
-        consume_slice<G, D, true>(ks, lane, n_valid, q2, m, l, acc2, p.scale_log2);
+        consume_slice<G, D, F8, true>(ks, lane, n_valid, q2, m, l, acc2, p.scale_log2);
       slot = (slot + 1 == S::kStages) ? 0 : slot + 1;
     }
 
@@ -515,6 +551,7 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
 #pragma unroll
         for (int w = 0; w < S::kWarps; ++w) o = fmaf(scratch[(w * G + h) * S::kSRow + d], wgt[w], o);
         o = (lt > 0.f) ? o / lt : 0.f;
+        if constexpr (F8) o *= p.v_scale;  // E4M3 values: scale once, at the output
         if (x.single)
           p.out[((size_t)x.b * p.H_q + hq) * D + d] = __float2bfloat16_rn(o);
         else
@@ -532,29 +569,36 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
   cp_async_wait<0>();  // leave no copy in flight
 }
 
-template <int G, int D, bool X>
+template <int G, int D, bool X, bool F8>
 cudaError_t launch_x(const Launch& p, int grid, cudaStream_t stream) {
-  using S = FmaShape<G, D>;
+  using S = FmaShape<G, D, F8>;
   static const cudaError_t attr = cudaFuncSetAttribute(
-      split_fma_kernel<G, D, X>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+      split_fma_kernel<G, D, X, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
   if (attr != cudaSuccess) return attr;
-  return launch_after(split_fma_kernel<G, D, X>, dim3(grid), dim3(S::kThreads), S::kSmemBytes,
+  return launch_after(split_fma_kernel<G, D, X, F8>, dim3(grid), dim3(S::kThreads), S::kSmemBytes,
                       stream, p);
 }
 
+// Instantiations: bf16 with one or two KV sources; E4M3 with one source.
 template <int G, int D>
 cudaError_t launch_one(const Launch& p, int grid, cudaStream_t stream) {
-  return p.extra_k ? launch_x<G, D, true>(p, grid, stream) : launch_x<G, D, false>(p, grid, stream);
+  if (p.kv_fp8) {
+    if (p.extra_k) return cudaErrorInvalidValue;
+    return launch_x<G, D, false, true>(p, grid, stream);
+  }
+  return p.extra_k ? launch_x<G, D, true, false>(p, grid, stream)
+                   : launch_x<G, D, false, false>(p, grid, stream);
 }
 
 template <int G, int D>
 int ctas_one() {
   using S = FmaShape<G, D>;
   static int n = [] {
-    cudaFuncSetAttribute(split_fma_kernel<G, D, false>,
+    cudaFuncSetAttribute(split_fma_kernel<G, D, false, false>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
     int c = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, split_fma_kernel<G, D, false>, S::kThreads,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, split_fma_kernel<G, D, false, false>,
+                                                      S::kThreads,
                                                       S::kSmemBytes) != cudaSuccess)
       c = 1;
     return c < 1 ? 1 : c;
