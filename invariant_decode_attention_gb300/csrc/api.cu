@@ -142,6 +142,7 @@ Launch make_launch(const da_plan* plan) {
     L.page_shift = sh;
   }
   L.max_splits = plan->max_splits;
+  L.o_part_mla = plan->variant == DA_VARIANT_MLA;
   L.scale_log2 = pr.scale * kLog2e;
   if (pr.kv_dtype == DA_KV_FP8_E4M3) {  // scores of E4M3 keys: scale * k_scale
     L.kv_fp8 = 1;

@@ -55,9 +55,72 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Launch p) {
   if (threadIdx.x == 0) p.lse[(size_t)b * p.H_q + j] = lse_out;
 }
 
+// The tensor-core variant's partials are head-interleaved: value dims in
+// groups of four, heads innermost -- element (slot, head j, dim d) at
+// ((slot * 128 + d / 4) * H_q + j) * 4 + d % 4 -- so that its epilogue's
+// stores coalesce.  Its combine takes one CTA per (row, value half, 32 dims)
+// and one thread per head: each thread forms its head's weights alone with
+// the same operations in the same order as merge_weights, and its loads of a
+// split's 4-dim group coalesce across the heads.
+constexpr int kMlaGroupsPerCta = 8;  // 4-dim groups: 32 value dims
+
+__global__ void __launch_bounds__(kCombineThreads) combine_mla_kernel(Launch p) {
+  wait_prior_grid();  // the split kernel's partials
+  constexpr int kBlocksPerRow = 512 / 4 / kMlaGroupsPerCta;  // 16
+  const int b = blockIdx.x / kBlocksPerRow, cb = blockIdx.x % kBlocksPerRow;
+  const int n = p.n_splits[b];
+  const int j = threadIdx.x;
+  if (n <= 1 || j >= p.H_q) return;
+  const size_t slot0 = (size_t)b * p.max_splits;
+  float coef[kMlaMaxSplits];
+  float M = -INFINITY;
+  for (int s = 0; s < n; ++s) {
+    coef[s] = __ldcg(p.lse_part + (slot0 + s) * p.H_q + j);
+    M = fmaxf(M, coef[s]);
+  }
+  float W = 0.f;
+  for (int s = 0; s < n; ++s) {
+    coef[s] = (M == -INFINITY) ? 0.f : ex2(coef[s] - M);
+    W += coef[s];
+  }
+  for (int s = 0; s < n; ++s) coef[s] = (W > 0.f) ? coef[s] / W : 0.f;
+  const float4* op = reinterpret_cast<const float4*>(p.o_part);
+  float4 acc[kMlaGroupsPerCta];
+#pragma unroll
+  for (int gi = 0; gi < kMlaGroupsPerCta; ++gi) acc[gi] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4* base = op + (slot0 * 128 + cb * kMlaGroupsPerCta) * p.H_q + j;
+  for (int s = 0; s < n; ++s) {
+    const float c = coef[s];
+    const float4* src = base + (size_t)s * 128 * p.H_q;
+#pragma unroll
+    for (int gi = 0; gi < kMlaGroupsPerCta; ++gi) {
+      const float4 v = __ldcg(src + gi * p.H_q);
+      acc[gi].x = fmaf(c, v.x, acc[gi].x);
+      acc[gi].y = fmaf(c, v.y, acc[gi].y);
+      acc[gi].z = fmaf(c, v.z, acc[gi].z);
+      acc[gi].w = fmaf(c, v.w, acc[gi].w);
+    }
+  }
+  __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(
+      p.out + ((size_t)b * p.H_q + j) * 512 + cb * kMlaGroupsPerCta * 4);
+#pragma unroll
+  for (int gi = 0; gi < kMlaGroupsPerCta; ++gi) {
+    dst[2 * gi] = __floats2bfloat162_rn(acc[gi].x, acc[gi].y);
+    dst[2 * gi + 1] = __floats2bfloat162_rn(acc[gi].z, acc[gi].w);
+  }
+  if (cb == 0) p.lse[(size_t)b * p.H_q + j] = (W > 0.f) ? (M + lg2(W)) * kLn2 : -INFINITY;
+}
+
 }  // namespace
 
 cudaError_t launch_combine(const Launch& p, cudaStream_t stream) {
+  if (p.o_part_mla) {
+    if (p.D_v != 512 || p.H_q > kCombineThreads) return cudaErrorInvalidValue;
+    const long long blocks = (long long)p.B * (512 / 4 / kMlaGroupsPerCta);
+    if (blocks == 0) return cudaSuccess;
+    return launch_after(combine_mla_kernel, dim3((unsigned)blocks), dim3(kCombineThreads), 0,
+                        stream, p);
+  }
   if (p.D_v > kCombineThreads * kMaxDimsPerThread) return cudaErrorInvalidValue;
   const long long blocks = (long long)p.B * p.H_q;
   if (blocks == 0) return cudaSuccess;

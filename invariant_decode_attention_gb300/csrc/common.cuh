@@ -67,6 +67,7 @@ struct Launch {
   int max_splits;
   float scale_log2;  // softmax scale * log2(e) (* k_scale for an E4M3 cache)
   int kv_fp8;        // K and V are E4M3 bytes
+  int o_part_mla;    // partials in the tensor-core variant's head-interleaved layout
   float v_scale;     // E4M3 cache: multiplies each unit's output
 };
 

@@ -624,12 +624,14 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
             dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
           }
         } else {
-          float4* dst = reinterpret_cast<float4*>(
-              p.o_part + ((size_t)x.slot * p.H_q + row) * 512 + x.half * kDvHalf + ch * 32);
+          // partials in the head-interleaved layout (4-dim groups, heads
+          // innermost): a warp's store covers 32 consecutive heads, 512 bytes
+          const int c0 = (x.half * kDvHalf + ch * 32) / 4;
 #pragma unroll
           for (int v = 0; v < 8; ++v)
-            dst[v] = make_float4(o[4 * v] * inv, o[4 * v + 1] * inv, o[4 * v + 2] * inv,
-                                 o[4 * v + 3] * inv);
+            reinterpret_cast<float4*>(p.o_part)[((size_t)x.slot * 128 + c0 + v) * p.H_q + row] =
+                make_float4(o[4 * v] * inv, o[4 * v + 1] * inv, o[4 * v + 2] * inv,
+                            o[4 * v + 3] * inv);
         }
       }
     }
