@@ -293,26 +293,31 @@ def e2e_steps(case, steps, warmup):
 
 # ----------------------------------------------------------------- CPU oracle
 
-def invariance_sweep(api, sizes=(1, 2, 4, 8, 16, 32, 64, 128)):
+def invariance_sweep(api, sizes=(1, 2, 4, 8, 16, 32, 64, 128), steps=10):
     """The ragged sweep's target row (length 4096, GQA 32/8, d = 128) at a random
     position among log-uniform batchmates, against its solo run, under each
-    policy: how many batches move any bit of its output or LSE, and the
-    largest output difference."""
+    policy: how many batches move any bit of its output or LSE, the largest
+    output difference, and the step time of every batch (the occupancy cost
+    of the per-row split rule on ragged batches)."""
     from invariant_decode_attention_gb300 import workloads as W
     sweep = W.RaggedSweep(sizes)
-    res = {}
+    res = {"batch_sizes": list(sizes)}
     for name, pol in (("invariant", api.INVARIANT), ("balanced", api.BALANCED)):
         o_solo, l_solo = api.run_workload(sweep.solo(), policy=pol)
-        moved, max_abs = 0, 0.0
+        moved, max_abs, ms, gbs = 0, 0.0, [], []
         for i in range(len(sizes)):
             wl, pos = sweep.batch(i)
-            o, l = api.run_workload(wl, policy=pol)
+            case = GpuCase(wl, wl.q.device, pol)  # already on the device: no copy
+            tot, _, _ = time_steps(case, steps, 3, split_events=False)
+            ms.append(round(tot / steps, 5))
+            gbs.append(round(wl.kv_bytes() / (tot / steps * 1e-3) / 1e9, 1))
+            o, l = case.out, case.lse
             same = torch.equal(o[pos], o_solo[0]) and torch.equal(l[pos], l_solo[0])
             moved += 0 if same else 1
             max_abs = max(max_abs, (o[pos].float() - o_solo[0].float()).abs().max().item())
+            del case
         res[name] = {"batches_moving_target_row": moved, "batches": len(sizes),
-                     "max_absdiff_out": max_abs}
-    res["batch_sizes"] = list(sizes)
+                     "max_absdiff_out": max_abs, "ms_per_step": ms, "kv_gbs": gbs}
     del sweep
     torch.cuda.empty_cache()
     return res
