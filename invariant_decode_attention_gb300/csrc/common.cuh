@@ -28,6 +28,9 @@ constexpr int kBalancedFixedOverhead = 2;
 // Header words at the start of the workspace.
 constexpr int kHdrError = 0;  // DA_DEVERR_* bits
 constexpr int kHdrNWork = 1;  // number of (row, split) work items
+constexpr int kHdrQueue = 2;  // CUDA-core split kernel: units handed out so far
+constexpr int kHdrExits = 3;  // CUDA-core split kernel: CTAs that have finished
+constexpr int kHdrNEmpty = 4; // work items with no tiles (empty rows); listed last
 constexpr size_t kHdrBytes = 256;
 
 // Longest a pipeline wait may spin before the kernel gives up (ns).

@@ -95,7 +95,11 @@ __device__ __forceinline__ RowSplits invariant_splits(const PlanLaunch& p, int l
 __global__ void __launch_bounds__(kPlanThreads) plan_invariant_kernel(PlanLaunch p) {
   __shared__ int bucket[kSortKeys];
   allow_next_grid();  // the split kernel may be staged now; it waits for us
-  if (threadIdx.x == 0) p.hdr[kHdrError] = 0;
+  if (threadIdx.x == 0) {
+    p.hdr[kHdrError] = 0;
+    p.hdr[kHdrQueue] = 0;
+    p.hdr[kHdrExits] = 0;
+  }
   for (int k = threadIdx.x; k < kSortKeys; k += kPlanThreads) bucket[k] = 0;
   __syncthreads();
   const int stride = p.max_splits + 1;
@@ -123,6 +127,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_invariant_kernel(PlanLaunch
     int total;
     const int start = block_exclusive_scan(count, &total);
     if (key >= 0) bucket[key] = start;
+    if (key == 0) p.hdr[kHdrNEmpty] = count;  // items with no tiles: key 0, listed last
     if (threadIdx.x == 0) p.hdr[kHdrNWork] = total;
   }
   __syncthreads();
@@ -146,6 +151,8 @@ __global__ void plan_balanced_kernel(PlanLaunch p) {
   allow_next_grid();
   if (threadIdx.x != 0) return;
   p.hdr[kHdrError] = 0;
+  p.hdr[kHdrQueue] = 0;
+  p.hdr[kHdrExits] = 0;
   const int stride = p.max_splits + 1;
   const int ovh = p.fixed_overhead;
   long long total = 0;
@@ -197,6 +204,7 @@ __global__ void plan_balanced_kernel(PlanLaunch p) {
     start[k] = acc;
     acc += c;
   }
+  p.hdr[kHdrNEmpty] = n_work - start[0];  // items with no tiles: key 0, listed last
   for (int b = 0; b < p.B; ++b) {
     const int n = p.n_splits[b];
     const int32_t* sb = p.split_begin + (size_t)b * stride;

@@ -111,40 +111,61 @@ __device__ __forceinline__ bool entry_row(const Launch& p, int b, int tok, int l
   return slot >= 0 && slot < p.num_blocks;
 }
 
-// Position of the prefetch stream: a (unit, tile) pair, units with no tiles
-// skipped.  The descriptor of the next unit is loaded one unit ahead.
+// Work queue.  Units with tiles are taken in work-list order (largest first).
+// While every CTA still has a full round, CTA c takes unit k * grid + c in
+// round k: the KV heads of one item (consecutive units) then run at the same
+// time on neighbouring CTAs and read the same cache records together.  The
+// remaining units -- less than one round -- come from an atomic counter in the
+// workspace header, so the CTAs that finish first take them.  Thread 0 takes
+// ids kAhead units ahead into a ring in shared memory (kRing slots).  While the compute works
+// on tile t of unit ordinal o, a warp's prefetch cursor has loaded tile t + 2
+// and stands on tile t + 3 -- at most ordinal o + 3 when units have one tile
+// -- and reads the id of the ordinal after it, o + 4: ids up to o + 4 must be
+// known, so the ring is filled five ahead (and slot o + 5 - kRing = o - 3,
+// long finished, is the one reused).  Which CTA runs a unit never changes
+// what the unit computes.
+constexpr int kRing = 8;
+constexpr int kAhead = 5;
+static_assert(kAhead < kRing - 2, "the reused slot is behind the compute");
+
+// The unit id of this CTA's ordinal `ord` (ids >= n_units: no more work).
+__device__ __forceinline__ int unit_of(const Launch& p, int ord, int n_static) {
+  const int s = ord * (int)gridDim.x + (int)blockIdx.x;
+  return (s < n_static) ? s : n_static + atomicAdd(p.hdr + kHdrQueue, 1);
+}
+
+// Position of the prefetch stream: a (unit, tile) pair; ord is the unit's
+// ordinal in this CTA's sequence.  The descriptor of the next unit is loaded
+// one unit ahead.
 struct Cursor {
   Unit x;
-  int u, k;
+  int ord, k;
   int4 next;
   bool valid;
 };
 
 template <bool X>
-__device__ __forceinline__ void cursor_seek(const Launch& p, Cursor& c, int u, int4 d,
-                                            int n_units) {
-  for (;;) {
-    if (u >= n_units) {
-      c.valid = false;
-      return;
-    }
-    const int un = u + gridDim.x;
-    c.next = (un < n_units) ? load_desc(p, un) : make_int4(0, 0, 0, 0);
-    if (d.z > d.y) break;
-    u = un;
-    d = c.next;
+__device__ __forceinline__ void cursor_seek(const Launch& p, Cursor& c, int ord, int4 d,
+                                            const volatile int* ring, int n_units) {
+  const int u = ring[ord % kRing];
+  if (u >= n_units) {
+    c.valid = false;
+    return;
   }
-  c.u = u;
+  const int un = ring[(ord + 1) % kRing];
+  c.next = (un < n_units) ? load_desc(p, un) : make_int4(0, 0, 0, 0);
+  c.ord = ord;
   c.x = make_unit<X>(p, u, d);
   c.k = c.x.tb;
   c.valid = true;
 }
 
 template <bool X>
-__device__ __forceinline__ void cursor_next(const Launch& p, Cursor& c, int n_units) {
+__device__ __forceinline__ void cursor_next(const Launch& p, Cursor& c, const volatile int* ring,
+                                            int n_units) {
   if (!c.valid) return;
   if (++c.k < c.x.te) return;
-  cursor_seek<X>(p, c, c.u + gridDim.x, c.next, n_units);
+  cursor_seek<X>(p, c, c.ord + 1, c.next, ring, n_units);
 }
 
 // Issue this warp's copies for the cursor's tile into ring slot `slot`, then
@@ -429,24 +450,43 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
   const int grp = lane >> 3, sub = lane & 7;
   wait_prior_grid();  // the plan kernel's outputs
   allow_next_grid();
-  const int n_units = p.hdr[kHdrNWork] * p.H_kv;
-  if ((int)blockIdx.x >= n_units) return;  // uniform across the CTA
+  __shared__ int ring[kRing];  // unit ids of this CTA's ordinals, kAhead ahead
+  const int n_items = p.hdr[kHdrNWork], n_empty = p.hdr[kHdrNEmpty];
+  const int n_units = (n_items - n_empty) * p.H_kv;  // units with tiles, listed first
+  // units of empty rows (listed last): out = 0, lse = -inf, dealt round-robin
+  for (int e = n_units + blockIdx.x; e < n_items * p.H_kv; e += gridDim.x) {
+    const int4 d = load_desc(p, e);
+    const int b = (~d.x) / p.max_splits, hq0 = (e % p.H_kv) * G;  // an empty row has one split
+    for (int i = threadIdx.x; i < G * D; i += S::kThreads)
+      p.out[((size_t)b * p.H_q + hq0) * D + i] = __float2bfloat16_rn(0.f);
+    if (threadIdx.x < G) p.lse[(size_t)b * p.H_q + hq0 + threadIdx.x] = -INFINITY;
+  }
+  const int n_static = n_units / (int)gridDim.x * (int)gridDim.x;  // whole rounds
+  if (threadIdx.x == 0)
+    for (int i = 0; i < kAhead; ++i) ring[i] = unit_of(p, i, n_static);
+  __syncthreads();
 
   // prologue: fill kStages - 1 slots
   Cursor pf;
-  cursor_seek<X>(p, pf, blockIdx.x, load_desc(p, blockIdx.x), n_units);
+  if (ring[0] < n_units)
+    cursor_seek<X>(p, pf, 0, load_desc(p, ring[0]), ring, n_units);
+  else
+    pf.valid = false;
 #pragma unroll
   for (int s = 0; s < S::kStages - 1; ++s) {
     load_slice<G, D, X, F8>(p, pf, smem, s, warp, lane);
-    cursor_next<X>(p, pf, n_units);
+    cursor_next<X>(p, pf, ring, n_units);
   }
 
   int slot = 0;
   uint64_t q2[G][S::kDpl / 2];
-  int4 d_next = load_desc(p, blockIdx.x);
-  for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+  int4 d_next = (ring[0] < n_units) ? load_desc(p, ring[0]) : make_int4(0, 0, 0, 0);
+  for (int ord = 0;; ++ord) {
+    const int u = ring[ord % kRing];
+    if (u >= n_units) break;
     const Unit x = make_unit<X>(p, u, d_next);
-    if (u + (int)gridDim.x < n_units) d_next = load_desc(p, u + gridDim.x);
+    const int un = ring[(ord + 1) % kRing];
+    if (un < n_units) d_next = load_desc(p, un);
     float m[G], l[G];
     uint64_t acc2[G][S::kDpl / 2];
 #pragma unroll
@@ -471,7 +511,7 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
       }
       // refill the slot consumed in the previous iteration
       load_slice<G, D, X, F8>(p, pf, smem, (slot + S::kStages - 1) % S::kStages, warp, lane);
-      cursor_next<X>(p, pf, n_units);
+      cursor_next<X>(p, pf, ring, n_units);
       const uint8_t* ks = smem + (slot * S::kWarps + warp) * S::kWarpSlotBytes;
       const int n_valid = min(S::kTokPerWarp, x.L - k * S::kTile - warp * S::kTokPerWarp);
       if (n_valid >= S::kTokPerWarp)
@@ -564,9 +604,20 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
           p.lse_part[(size_t)x.slot * p.H_q + hq] = lse2;
       }
     }
+    // the id of ordinal ord + kAhead; the barrier publishes it
+    if (threadIdx.x == 0) ring[(ord + kAhead) % kRing] = unit_of(p, ord + kAhead, n_static);
     named_bar_sync(1, S::kThreads);
   }
   cp_async_wait<0>();  // leave no copy in flight
+  // the last CTA to finish resets the queue for the next call on this plan
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(p.hdr + kHdrExits, 1) == (int)gridDim.x - 1) {
+      p.hdr[kHdrQueue] = 0;
+      p.hdr[kHdrExits] = 0;
+    }
+  }
 }
 
 template <int G, int D, bool X, bool F8>

@@ -105,3 +105,25 @@ def test_gqa_repeated_runs_bitwise(api):
     for _ in range(8):
         out, lse = api.run_workload(wl, ws=ws)
         assert torch.equal(out, out0) and torch.equal(lse, lse0)
+
+
+def test_one_plan_many_runs(api):
+    """One plan, several run + combine calls: the split kernel's work queue is
+    back at its start after every call, so every call computes every unit."""
+    wl = W.make(W.PAGED, [0, 5000, 1, 0, 70000, 640, 3000], H_q=32, H_kv=8, D_qk=128,
+                page_size=16, seed=71).to("cuda")
+    prob = api.problem_for(wl)
+    ws = api.workspace(prob, "cuda")
+    pl = api.plan(prob, api.INVARIANT, wl.lengths, ws)
+    outs = []
+    for _ in range(3):
+        out = torch.full((wl.B, wl.H_q, wl.D_v), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((wl.B, wl.H_q), float("nan"), dtype=torch.float32, device="cuda")
+        api.run(pl, wl.q, wl.k, wl.v, wl.table, wl.lengths, out, lse)
+        api.combine(pl, out, lse)
+        outs.append((out, lse))
+    for out, lse in outs:
+        assert not torch.isnan(out).any() and not torch.isnan(lse).any()
+        assert torch.equal(out, outs[0][0]) and torch.equal(lse, outs[0][1])
+    o_ref, l_ref = api.run_workload(wl)
+    assert torch.equal(outs[0][0], o_ref) and torch.equal(outs[0][1], l_ref)
