@@ -351,3 +351,79 @@ def long_context_fp8(seed=1004):
     """The long-context workload (8 x 131072, 32/8 heads, d = 128, page 64)
     with an E4M3 KV cache, scales 1/64."""
     return quantize_fp8(long_context(seed), name="long_context_fp8_b8_l131072_h32x8_d128_p64")
+
+
+# ----------------------------------------------------------------- NVFP4 weight matmul
+
+@dataclasses.dataclass
+class Nvfp4Matmul:
+    """Inputs of one weight matmul y = bf16(x) @ W^T with an NVFP4 weight.
+
+    ``codes`` uint8 [N, K / 2]: two E2M1 codes per byte, element 2j of a row
+    in the low nibble of byte j; ``scales`` uint8 [N, K / 16]: one E4M3 code
+    per 16 consecutive weights of a row; ``global_scale``: one fp32 factor
+    for the whole matrix; ``x`` fp32 [n, K]: the activations before rounding.
+    """
+    name: str
+    x: torch.Tensor
+    codes: torch.Tensor
+    scales: torch.Tensor
+    global_scale: float
+
+    @property
+    def n(self):
+        return int(self.x.shape[0])
+
+    @property
+    def N(self):
+        return int(self.codes.shape[0])
+
+    @property
+    def K(self):
+        return int(self.x.shape[1])
+
+    def weight_bytes(self):
+        return self.codes.numel() + self.scales.numel()
+
+    def to(self, device):
+        return dataclasses.replace(self, x=self.x.to(device), codes=self.codes.to(device),
+                                   scales=self.scales.to(device))
+
+    def with_rows(self, x):
+        """The same weight with other activation rows."""
+        return dataclasses.replace(self, x=x)
+
+
+def nvfp4_weight(N, K, seed, global_scale=1.0 / 128):
+    """A random NVFP4 weight: every byte of ``codes`` uniform over 0..255 (all
+    sixteen E2M1 codes in both nibbles, both zeros included) and positive
+    E4M3 block scales with exponent field 4..10 and a uniform fraction, i.e.
+    values 2^-3 .. 15 (no NaN code)."""
+    if N <= 0 or K <= 0 or K % 16:
+        raise ValueError("N > 0 and K a positive multiple of 16")
+    g = torch.Generator().manual_seed(seed)
+    codes = torch.randint(0, 256, (N, K // 2), generator=g, dtype=torch.int32).to(torch.uint8)
+    e = torch.randint(4, 11, (N, K // 16), generator=g, dtype=torch.int32)
+    f = torch.randint(0, 8, (N, K // 16), generator=g, dtype=torch.int32)
+    scales = ((e << 3) | f).to(torch.uint8)
+    return codes, scales, float(global_scale)
+
+
+def nvfp4_activations(n, K, seed):
+    """n activation rows of N(0, 1) fp32 values (full fp32 fraction bits, so
+    rounding to bf16 changes almost every one)."""
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn((n, K), generator=g, dtype=torch.float32)
+
+
+def nvfp4_matmul(n, N, K, seed, name=None):
+    codes, scales, gs = nvfp4_weight(N, K, seed)
+    x = nvfp4_activations(n, K, seed + 7919)
+    return Nvfp4Matmul(name or f"nvfp4_n{n}_N{N}_K{K}", x, codes, scales, gs)
+
+
+def nvfp4_proj(n=32, seed=1006):
+    """A dense projection-sized NVFP4 weight (N = 8192 outputs, K = 4096
+    inputs: 16.8 MB of codes + 2.1 MB of scales) with n activation rows;
+    n = 32 is the largest row count the pages' GEMV path takes."""
+    return nvfp4_matmul(n, 8192, 4096, seed, name=f"nvfp4_proj_n{n}_N8192_K4096")

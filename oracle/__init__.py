@@ -25,6 +25,11 @@ What it computes and where that is stated:
 * ``fp8`` -- exact fp64 decode of an FP8 E4M3 key/value cache with one
   scale per cache (the reading of the pages' low-precision checkpoints,
   stated in the module).
+* ``nvfp4`` -- exact fp64 decode of an NVFP4 weight matrix (E2M1 codes, one
+  E4M3 scale per 16 weights, one fp32 scale per matrix) and the product
+  ``bf16(x) @ W^T`` that both kernel shapes of a weight matmul agree on.
+  Source: "Greedy outputs depend on batch composition" (gllm issue #98),
+  Candidate cause and Next steps.
 * ``bf16`` -- exact fp64 -> bf16 round-to-nearest-even, used to state the
   output rounding and the tolerance in units of bf16 ULP (same page,
   Measurement: "1-2 ULP of bf16 near 1.0").
@@ -33,4 +38,4 @@ Parity pins (``tests/test_oracle_*.py``) tie every function to closed forms,
 brute force and invariants; no function here is "parity unpinned".
 """
 
-from . import attention, plan, bf16, fp8  # noqa: F401
+from . import attention, plan, bf16, fp8, nvfp4  # noqa: F401
