@@ -1,4 +1,5 @@
-"""Thin Python binding of the C ABI in ``include/decode_attn.h``.
+"""Thin Python binding of the C ABI in ``include/decode_attn.h`` and
+``include/nvfp4_mm.h``.
 
 Argument marshalling only: every step of the computation runs in the CUDA
 library.  torch tensors supply device memory and the current CUDA stream.  If
@@ -32,7 +33,12 @@ EXPORTS = (
     "decode_attn_combine", "decode_attn_forward", "decode_attn_read_error",
     "decode_attn_copy_plan", "decode_attn_forward_static", "decode_attn_plan_extra",
     "decode_attn_run_extra", "decode_attn_forward_extra",
+    "nvfp4_mm_workspace_bytes", "nvfp4_mm", "nvfp4_mm_read_error",
 )
+
+# NVFP4 weight matmul (include/nvfp4_mm.h)
+NVFP4_TILE_N, NVFP4_ROW_TILE, NVFP4_K_CHUNK = 128, 32, 1024
+NVFP4_X_F32, NVFP4_X_BF16 = 0, 1
 
 # Size of the fixed device array decode_attn_forward_static uses as scratch.
 STATIC_WORKSPACE_BYTES = 64 << 20
@@ -133,6 +139,12 @@ def lib():
     L.decode_attn_forward_static.argtypes = [P(DaProblem), i32, vp, vp, vp, vp, vp, vp, vp, vp]
     L.decode_attn_copy_plan.restype = ctypes.c_int
     L.decode_attn_copy_plan.argtypes = [P(DaPlan), vp, vp, P(i32), vp, vp]
+    L.nvfp4_mm_workspace_bytes.restype = sz
+    L.nvfp4_mm_workspace_bytes.argtypes = [i32, i32, i32]
+    L.nvfp4_mm.restype = ctypes.c_int
+    L.nvfp4_mm.argtypes = [vp, i32, vp, vp, ctypes.c_float, i32, i32, i32, vp, vp, vp, sz, vp]
+    L.nvfp4_mm_read_error.restype = ctypes.c_int
+    L.nvfp4_mm_read_error.argtypes = [vp, P(i32), vp]
     _LIB = L
     return L
 
@@ -382,3 +394,58 @@ def run_workload(wl, policy=INVARIANT, ws=None, out=None, lse=None, stream=None)
     else:
         forward(prob, policy, wl.q, wl.k, wl.v, wl.table, wl.lengths, ws, out, lse, stream)
     return out, lse
+
+
+# ----------------------------------------------------------------- NVFP4 weight matmul
+
+def nvfp4_workspace_bytes(n: int, N: int, K: int) -> int:
+    """Workspace bytes of one ``nvfp4_mm`` call (0: shape not supported)."""
+    return int(lib().nvfp4_mm_workspace_bytes(n, N, K))
+
+
+def nvfp4_workspace(n: int, N: int, K: int, device="cuda") -> torch.Tensor:
+    nb = nvfp4_workspace_bytes(n, N, K)
+    if nb == 0:
+        raise DecodeAttnError(ERR_UNSUPPORTED, f"nvfp4 shape n={n} N={N} K={K}")
+    return torch.empty(nb, dtype=torch.uint8, device=device)
+
+
+def nvfp4_mm(x, codes, scales, global_scale, *, y=None, y_bf16=None, ws=None, stream=None):
+    """y = global_scale * bf16(x) @ W^T for an NVFP4 weight (nvfp4_mm.h).
+
+    x: fp32 or bf16 [n, K]; codes: uint8 [N, K / 2]; scales: uint8 (or
+    float8_e4m3fn) [N, K / 16]; returns y fp32 [n, N] (and fills ``y_bf16``
+    when given).  Every row's result is independent of n and of the other rows.
+    """
+    n, K = x.shape
+    N = codes.shape[0]
+    if codes.shape != (N, K // 2) or scales.shape != (N, K // 16):
+        raise ValueError(f"codes {tuple(codes.shape)} / scales {tuple(scales.shape)} "
+                         f"do not match x {tuple(x.shape)}")
+    x_dtype = {torch.float32: NVFP4_X_F32, torch.bfloat16: NVFP4_X_BF16}.get(x.dtype)
+    if x_dtype is None:
+        raise ValueError(f"x must be float32 or bfloat16, got {x.dtype}")
+    if y is None:
+        y = torch.empty((n, N), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = nvfp4_workspace(n, N, K, x.device)
+    _check(lib().nvfp4_mm(_dev_ptr(x, "x"), x_dtype, _dev_ptr(codes, "codes", torch.uint8),
+                          _dev_ptr(scales, "scales", _KV[1:]), ctypes.c_float(global_scale),
+                          n, N, K, _dev_ptr(y, "y", torch.float32),
+                          _dev_ptr(y_bf16, "y_bf16", torch.bfloat16), _dev_ptr(ws, "ws"),
+                          ws.numel(), _stream(stream)), "nvfp4_mm")
+    return y
+
+
+def nvfp4_read_error(ws: torch.Tensor, stream=None) -> int:
+    """Device error bits (DEVERR_*) of the last ``nvfp4_mm`` call on ``ws``."""
+    code = ctypes.c_int32()
+    _check(lib().nvfp4_mm_read_error(_dev_ptr(ws, "ws"), ctypes.byref(code), _stream(stream)),
+           "nvfp4_read_error")
+    return code.value
+
+
+def run_nvfp4(m, ws=None, y=None, y_bf16=None, stream=None):
+    """nvfp4_mm on a ``workloads.Nvfp4Matmul`` whose tensors are on the GPU."""
+    return nvfp4_mm(m.x, m.codes, m.scales, m.global_scale, y=y, y_bf16=y_bf16, ws=ws,
+                    stream=stream)

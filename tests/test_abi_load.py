@@ -11,7 +11,7 @@ import pytest
 from oracle import plan as OP
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "decode_attn.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("decode_attn.h", "nvfp4_mm.h")]
 
 
 @pytest.fixture(scope="module")
@@ -25,8 +25,17 @@ def api():
 
 
 def header_functions():
-    text = open(HEADER).read()
-    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(decode_attn_\w+)\s*\(", text, re.M)))
+    names = set()
+    for h in HEADERS:
+        text = open(h).read()
+        names |= set(re.findall(r"^[A-Za-z_][\w \*]*?\b((?:decode_attn|nvfp4_mm)\w*)\s*\(",
+                                text, re.M))
+    return sorted(names)
+
+
+def test_every_header_is_covered():
+    assert sorted(os.listdir(os.path.join(ROOT, "include"))) == sorted(
+        os.path.basename(h) for h in HEADERS)
 
 
 def test_exports_every_declared_symbol(api):
