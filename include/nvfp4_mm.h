@@ -63,8 +63,9 @@ extern "C" {
 
 /* Device workspace bytes for one call with n activation rows, N outputs and
  * reduction length K (0 when the shape is not supported).  It holds a 256-byte
- * header, the rounded activations (n rounded up to NVFP4_MM_ROW_TILE rows)
- * and, when K > NVFP4_MM_K_CHUNK, the fp32 partial sums. */
+ * header, one counter per output tile, the rounded activations (n rounded up
+ * to NVFP4_MM_ROW_TILE rows) and, when K > NVFP4_MM_K_CHUNK, the fp32 partial
+ * sums P_c.  Its contents need no initialisation. */
 size_t nvfp4_mm_workspace_bytes(int32_t n, int32_t N, int32_t K);
 
 /* y = global_scale * bf16(x) @ W^T as defined above.

@@ -9,25 +9,38 @@
 // added in chunk order.  A row's bits therefore depend on its own activations
 // and the weight only.
 //
-// Tile: 128 output features (MMA M, one per tensor-memory lane) x 32
-// activation rows (MMA N) x one K chunk; the MMA is D[o, i] += W[o, k] x[i, k]
-// ("swap AB": the weight is the 128-row operand, so a small n wastes nothing
-// of the weight stream).  Per 64-wide K step of the chunk:
-//   warp 0     TMA: the step's 128 x 32 bytes of E2M1 codes into a 6-deep
-//              ring (no swizzle), the step's 32 x 64 bf16 activations into a
-//              4-deep ring (128-byte swizzle, K-major);
-//   warps 2-5  dequantize: thread r owns weight row r of the tile, decodes
-//              its 64 codes with the row's four E4M3 block scales into bf16
-//              (exact: an E2M1 value times an E4M3 scale has at most six
-//              significant bits) and writes them into a 3-deep ring in the
-//              128-byte-swizzled K-major layout the tensor core reads;
-//   warp 1     MMA issue (one thread): four M128 N32 K16 MMAs into a 32-column
-//              fp32 accumulator in tensor memory.
-// After the chunk, warps 2-5 read the accumulator (thread r = lane r) and
-// write the chunk's partial sums, or y itself when K is a single chunk.
+// Work unit ("tile"): 128 output features (MMA M, one per tensor-memory lane)
+// x 32 activation rows (MMA N) x one K chunk; the MMA is D[o, i] += W[o, k]
+// x[i, k] ("swap AB": the weight is the 128-row operand, so a small n wastes
+// nothing of the weight stream).  The kernel is persistent, one CTA per SM,
+// each CTA taking tiles blockIdx.x, + gridDim.x, ...; its rings run on across
+// tiles, so the next tile's copies and dequantization overlap the current
+// tile's MMAs and epilogue.  Per 64-wide K step:
+//   warps 0, 22 TMA (one thread each): the step's 128 x 32 bytes of E2M1
+//               codes into a 12-deep ring (no swizzle); the step's 32 x 64
+//               bf16 activations into a 6-deep ring (128-byte swizzle,
+//               K-major);
+//   warps 6-21  dequantize: thread (r, g) owns weight row r of the tile and
+//               the 16 weights of block g of the step; it decodes them with
+//               the block's E4M3 scale into bf16 (exact: an E2M1 value times
+//               an E4M3 scale has at most six significant bits) and writes
+//               them into a 4-deep ring in the 128-byte-swizzled K-major layout
+//               the tensor core reads;
+//   warp 1      MMA issue (one thread): four M128 N32 K16 MMAs per step into
+//               one of two 32-column fp32 accumulators in tensor memory
+//               (tiles alternate between them);
+//   warps 2-5   epilogue: read a finished accumulator (warp w reads lanes
+//               32 (w % 4)..), free it, and write y when K is one chunk, else
+//               the chunk's partial sums; the last of a tile's chunk CTAs to
+//               finish (a counter per output tile) adds the partials in chunk
+//               order and writes y.
+// One CTA per SM: two CTAs of this kernel sharing an SM were measured to
+// corrupt the accumulators of one of them now and then (cause not found; see
+// the design notes), so the shared-memory request keeps the second one out.
 // Every mbarrier wait is bounded; on time-out the kernel records
-// DA_DEVERR_TIMEOUT, all roles leave their loops, the copies in flight and
-// the tensor-core work are drained (bounded) and tensor memory is freed.
+// DA_DEVERR_TIMEOUT, all roles leave their loops together, the copies in
+// flight and the tensor-core work are drained (bounded) and tensor memory is
+// freed.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -45,32 +58,43 @@ namespace {
 constexpr int kTileN = NVFP4_MM_TILE_N;     // weight rows per tile (MMA M)
 constexpr int kRowTile = NVFP4_MM_ROW_TILE; // activation rows per tile (MMA N)
 constexpr int kKChunk = NVFP4_MM_K_CHUNK;   // K per partial sum
-constexpr int kStep = 64;                   // K per pipeline step (one swizzle row)
-constexpr int kStepsPerChunk = kKChunk / kStep;
-constexpr int kRawStages = 6, kXStages = 4, kAStages = 3;
-constexpr int kRawBytes = kTileN * kStep / 2;   // 4096: E2M1 codes of a step
-constexpr int kXBytes = kRowTile * kStep * 2;   // 4096: bf16 activations of a step
-constexpr int kABytes = kTileN * kStep * 2;     // 16384: bf16 weights of a step
-constexpr int kScaleStride = kStepsPerChunk * 4 + 4;  // 68 bytes per row: no bank conflicts
+constexpr int kStep = 128;                  // K per pipeline step: two 64-wide swizzle regions
+constexpr int kRegion = 64;                 // K of one 128-byte swizzle row of bf16
+constexpr int kRawStages = 6, kStages = 3;  // code ring; operand ring (weights + activations)
+constexpr int kRawBytes = kTileN * kStep / 2;       // 8192: E2M1 codes of a step
+constexpr int kXRegionBytes = kRowTile * kRegion * 2;  // 4096
+constexpr int kXBytes = 2 * kXRegionBytes;          // 8192: bf16 activations of a step
+constexpr int kARegionBytes = kTileN * kRegion * 2;  // 16384
+constexpr int kABytes = 2 * kARegionBytes;          // 32768: bf16 weights of a step
+constexpr int kScaleStride = kKChunk / 16 + 4;      // 68 bytes per row: no bank conflicts
+constexpr int kScaleBytes = kTileN * kScaleStride;  // one tile's block scales
 
 constexpr int kAOff = 0;
-constexpr int kXOff = kAOff + kAStages * kABytes;        // 49152
-constexpr int kRawOff = kXOff + kXStages * kXBytes;      // 65536
-constexpr int kScaleOff = kRawOff + kRawStages * kRawBytes;  // 90112
-constexpr int kBarOff = kScaleOff + kTileN * kScaleStride;   // 98816
-enum { kRawFull0 = 0, kRawEmpty0 = kRawFull0 + kRawStages, kXFull0 = kRawEmpty0 + kRawStages,
-       kXEmpty0 = kXFull0 + kXStages, kAFull0 = kXEmpty0 + kXStages,
-       kAEmpty0 = kAFull0 + kAStages, kDFull = kAEmpty0 + kAStages, kDrain, kNumBars };
+constexpr int kXOff = kAOff + kStages * kABytes;             // 98304
+constexpr int kRawOff = kXOff + kStages * kXBytes;           // 122880
+constexpr int kScaleOff = kRawOff + kRawStages * kRawBytes;  // 172032
+constexpr int kBarOff = kScaleOff + 2 * kScaleBytes;         // 189440
+enum { kRawFull0 = 0, kRawEmpty0 = kRawFull0 + kRawStages, kFull0 = kRawEmpty0 + kRawStages,
+       kEmpty0 = kFull0 + kStages, kDFull0 = kEmpty0 + kStages, kDEmpty0 = kDFull0 + 2,
+       kDrain = kDEmpty0 + 2, kNumBars };
 constexpr int kTmemSlot = kBarOff + kNumBars * 8;
 constexpr int kAbortSlot = kTmemSlot + 4;
-constexpr int kSmemBytes = kAbortSlot + 4;
-static_assert(kXOff % 1024 == 0 && kABytes % 1024 == 0 && kXBytes % 1024 == 0,
+constexpr int kLastSlot = kAbortSlot + 4;
+constexpr int kSmemBytes = kLastSlot + 4;
+static_assert(kXOff % 1024 == 0 && kARegionBytes % 1024 == 0 && kXRegionBytes % 1024 == 0,
               "swizzled tiles start on 1024-byte boundaries");
 static_assert(kBarOff % 8 == 0, "mbarriers are 8-byte aligned");
-static_assert(2 * (kSmemBytes + 1024) <= 233472, "two CTAs per SM");
+static_assert(kSmemBytes <= 232448 && 2 * (kSmemBytes + 1024) > 233472,
+              "fits one CTA per SM and keeps a second one out");
 
-constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 32;
+constexpr int kEpWarp0 = 2, kEpWarps = 4;    // warps 2..5
+constexpr int kDqWarp0 = 6, kDqWarps = 16;   // warps 6..21
+constexpr int kDqThreads = kDqWarps * 32;
+constexpr int kEpThreads = kEpWarps * 32;
+constexpr int kXWarp = kDqWarp0 + kDqWarps;            // warp 22: activation producer
+constexpr int kThreads = (kXWarp + 1) * 32;            // 736
+constexpr int kDqBarrier = 1, kEpBarrier = 2;         // named barriers of the two groups
+constexpr uint32_t kTmemCols = 2 * kRowTile;           // two accumulators
 constexpr uint32_t kIdesc = umma::idesc_bf16_f32(kTileN, kRowTile, false);
 
 struct MmArgs {
@@ -79,9 +103,32 @@ struct MmArgs {
   float* y;               // [n, N]
   __nv_bfloat16* y_bf16;  // [n, N] or null
   int32_t* hdr;           // workspace header (error word)
+  int32_t* tile_count;    // [N / 128, n_itiles] chunk CTAs finished per tile (n_chunks > 1)
   float global_scale;
-  int n, N, K, n_chunks, n_itiles;
+  int n, N, K, n_chunks, n_itiles, n_tiles;
+  int raw_box;            // bytes of a code row per copy: 64, or 32 when K = 64
 };
+
+// Tile t -> (activation tile, chunk, weight tile); activation tiles of one
+// weight chunk are neighbours, so they run together and share it in L2.
+struct Tile {
+  int o0, i0, k0, k_len, chunk, n_steps, out_tile;  // k_len: K of the chunk (64 .. 1024)
+};
+
+__device__ __forceinline__ Tile tile_of(const MmArgs& a, int t) {
+  Tile x;
+  const int it = t % a.n_itiles;
+  const int rest = t / a.n_itiles;
+  x.chunk = rest % a.n_chunks;
+  const int ot = rest / a.n_chunks;
+  x.o0 = ot * kTileN;
+  x.i0 = it * kRowTile;
+  x.k0 = x.chunk * kKChunk;
+  x.k_len = min(a.K, x.k0 + kKChunk) - x.k0;
+  x.n_steps = (x.k_len + kStep - 1) / kStep;
+  x.out_tile = ot * a.n_itiles + it;
+  return x;
+}
 
 // ---------------------------------------------------------------- helpers
 
@@ -165,135 +212,265 @@ __device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity) {
 
 // ---------------------------------------------------------------- roles
 
-__device__ void producer(const Ctx& c, const CUtensorMap* tm_w, const CUtensorMap* tm_x,
-                         int o0, int i0, int k0, int n_steps) {
-  int w_issued = 0, x_issued = 0;
-  auto issue_w = [&](int j) -> bool {
-    const int s = j % kRawStages;
-    if (j >= kRawStages && !wait_bar(c, kRawEmpty0 + s, ((j / kRawStages) - 1) & 1)) return false;
-    mbar_arrive_expect_tx(bar_addr(c, kRawFull0 + s), kRawBytes);
-    tma_load_2d(c.sbase + kRawOff + s * kRawBytes, tm_w, (k0 + j * kStep) / 2, o0,
-                bar_addr(c, kRawFull0 + s));
-    w_issued = j + 1;
-    return true;
-  };
-  // The weight does not come from the previous kernel on the stream: start
-  // streaming it before waiting for that kernel (which writes the activations).
-  bool ok = true;
-  for (int j = 0; j < n_steps && j < kRawStages && ok; ++j) ok = issue_w(j);
-  wait_prior_grid();
-  for (int j = 0; j < n_steps && ok; ++j) {
-    const int s = j % kXStages;
-    if (j >= kXStages && !wait_bar(c, kXEmpty0 + s, ((j / kXStages) - 1) & 1)) break;
-    mbar_arrive_expect_tx(bar_addr(c, kXFull0 + s), kXBytes);
-    tma_load_2d(c.sbase + kXOff + s * kXBytes, tm_x, k0 + j * kStep, i0, bar_addr(c, kXFull0 + s));
-    x_issued = j + 1;
-    if (j + kRawStages < n_steps) ok = issue_w(j + kRawStages);
+// Two producer threads, one per stream, each blocking on its own ring's free
+// slots: warp 0 streams the weight codes over the CTA's whole tile sequence,
+// warp 22 the activations.  The weight does not come from the previous kernel
+// on the stream, so it streams from the start; the activation producer first
+// waits for that kernel (which writes them).  A step's activations land on
+// the same "full" barrier as its dequantized weights (16 warp arrivals + this
+// thread's arrive with the copy's byte count), so the MMA thread waits once
+// per step.
+__device__ void producer_w(const Ctx& c, const MmArgs& a, const CUtensorMap* tm_w) {
+  int g = 0;
+  for (int t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
+    const Tile x = tile_of(a, t);
+    for (int j = 0; j < x.n_steps; ++j, ++g) {
+      const int s = g % kRawStages;
+      if (g >= kRawStages && !wait_bar(c, kRawEmpty0 + s, ((g / kRawStages) - 1) & 1)) {
+        t = a.n_tiles;
+        break;
+      }
+      // a half step at the end of K reads past the row: the copy fills zeros
+      mbar_arrive_expect_tx(bar_addr(c, kRawFull0 + s), kTileN * a.raw_box);
+      tma_load_2d(c.sbase + kRawOff + s * kRawBytes, tm_w, (x.k0 + j * kStep) / 2, x.o0,
+                  bar_addr(c, kRawFull0 + s));
+    }
   }
   // Copies still in flight must land before the CTA's shared memory goes away.
   for (int s = 0; s < kRawStages; ++s) {
-    const int last = w_issued - 1 - ((w_issued - 1 - s) % kRawStages + kRawStages) % kRawStages;
+    const int last = g - 1 - ((g - 1 - s) % kRawStages + kRawStages) % kRawStages;
     if (last >= 0 && !mbar_wait(bar_addr(c, kRawFull0 + s), (last / kRawStages) & 1))
       set_error(c.hdr, DA_DEVERR_TIMEOUT);
   }
-  for (int s = 0; s < kXStages; ++s) {
-    const int last = x_issued - 1 - ((x_issued - 1 - s) % kXStages + kXStages) % kXStages;
-    if (last >= 0 && !mbar_wait(bar_addr(c, kXFull0 + s), (last / kXStages) & 1))
+}
+
+__device__ void producer_x(const Ctx& c, const MmArgs& a, const CUtensorMap* tm_x) {
+  wait_prior_grid();
+  int g = 0;
+  for (int t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
+    const Tile x = tile_of(a, t);
+    for (int j = 0; j < x.n_steps; ++j, ++g) {
+      const int s = g % kStages;
+      if (g >= kStages && !wait_bar(c, kEmpty0 + s, ((g / kStages) - 1) & 1)) {
+        t = a.n_tiles;
+        break;
+      }
+      const int regions = min(kStep, x.k_len - j * kStep) / kRegion;  // 1 or 2
+      mbar_arrive_expect_tx(bar_addr(c, kFull0 + s), regions * kXRegionBytes);
+      for (int rg = 0; rg < regions; ++rg)
+        tma_load_2d(c.sbase + kXOff + s * kXBytes + rg * kXRegionBytes, tm_x,
+                    x.k0 + j * kStep + rg * kRegion, x.i0, bar_addr(c, kFull0 + s));
+    }
+  }
+  // Copies still in flight must land before the CTA's shared memory goes away
+  // (normally the MMA thread has waited for every one already).
+  for (int s = 0; s < kStages; ++s) {
+    const int last = g - 1 - ((g - 1 - s) % kStages + kStages) % kStages;
+    if (last >= 0 && !mbar_wait(bar_addr(c, kFull0 + s), (last / kStages) & 1))
       set_error(c.hdr, DA_DEVERR_TIMEOUT);
   }
 }
 
-__device__ void mma_issuer(const Ctx& c, uint32_t tmem, int n_steps) {
-  for (int j = 0; j < n_steps; ++j) {
-    const int sa = j % kAStages, sx = j % kXStages;
-    if (!wait_bar(c, kAFull0 + sa, (j / kAStages) & 1)) return;
-    if (!wait_bar(c, kXFull0 + sx, (j / kXStages) & 1)) return;
+// Tiles alternate between the two accumulators; an accumulator is reused once
+// the epilogue has read it.  Returns the number of steps whose MMAs were
+// issued and committed.
+__device__ int mma_issuer(const Ctx& c, const MmArgs& a, uint32_t tmem) {
+  int g = 0, k = 0;
+  for (int t = blockIdx.x; t < a.n_tiles; t += gridDim.x, ++k) {
+    const Tile x = tile_of(a, t);
+    const int tb = k & 1;
+    if (k >= 2 && !wait_bar(c, kDEmpty0 + tb, ((k >> 1) - 1) & 1)) return g;
     umma::fence_after_sync();
+    const uint32_t d = tmem + tb * kRowTile;
+    for (int j = 0; j < x.n_steps; ++j, ++g) {
+      const int s = g % kStages;
+      if (!wait_bar(c, kFull0 + s, (g / kStages) & 1)) return g;
+      umma::fence_after_sync();
+      const int n_mma = min(kStep, x.k_len - j * kStep) / 16;  // 4 or 8
+      const uint32_t a0 = c.sbase + kAOff + s * kABytes, b0 = c.sbase + kXOff + s * kXBytes;
 #pragma unroll
-    for (int kk = 0; kk < kStep / 16; ++kk) {  // K = 16 per MMA: 32 bytes along the row
-      const uint64_t a = umma::smem_desc(c.sbase + kAOff + sa * kABytes + kk * 32, 16, 1024,
-                                         umma::kSwizzle128B);
-      const uint64_t b = umma::smem_desc(c.sbase + kXOff + sx * kXBytes + kk * 32, 16, 1024,
-                                         umma::kSwizzle128B);
-      umma::mma_bf16(tmem, a, b, kIdesc, (j | kk) ? 1u : 0u);
+      for (int kk = 0; kk < kStep / 16; ++kk) {  // K = 16 per MMA: 32 bytes of a region row
+        if (kk < n_mma) {
+          const uint32_t off = (kk % 4) * 32;
+          const uint64_t ad = umma::smem_desc(a0 + (kk / 4) * kARegionBytes + off, 16, 1024,
+                                              umma::kSwizzle128B);
+          const uint64_t bd = umma::smem_desc(b0 + (kk / 4) * kXRegionBytes + off, 16, 1024,
+                                              umma::kSwizzle128B);
+          umma::mma_bf16(d, ad, bd, kIdesc, (j | kk) ? 1u : 0u);
+        }
+      }
+      umma::commit(bar_addr(c, kEmpty0 + s));
     }
-    umma::commit(bar_addr(c, kAEmpty0 + sa));
-    umma::commit(bar_addr(c, kXEmpty0 + sx));
+    umma::commit(bar_addr(c, kDFull0 + tb));
   }
-  umma::commit(bar_addr(c, kDFull));
+  return g;
 }
 
-// Thread r (0..127) of warps 2-5: weight row r of the tile, which is also
-// tensor-memory lane r for the epilogue (a warp reads lanes 32 (warp % 4)..).
-__device__ void dequant_and_store(const Ctx& c, const MmArgs& a, uint32_t tmem, int o0, int i0,
-                                  int chunk, int k0, int n_steps) {
+// The arrive of a tcgen05.commit lands some time after the MMAs it tracks;
+// before the CTA's shared memory is handed on, the last arrive on every ring
+// slot's release barrier must have landed.
+__device__ void drain_commits(const Ctx& c, int n_done) {
+  for (int s = 0; s < kStages; ++s) {
+    const int last = n_done - 1 - ((n_done - 1 - s) % kStages + kStages) % kStages;
+    if (last >= 0 && !mbar_wait(bar_addr(c, kEmpty0 + s), (last / kStages) & 1))
+      set_error(c.hdr, DA_DEVERR_TIMEOUT);
+  }
+}
+
+// Warps 6-21: warp w covers weight rows 8 (w - 6) .. +7 of the tile; lane l
+// takes row 8 (w - 6) + l / 4 and blocks 2 (l % 4), 2 (l % 4) + 1 of every step
+// (weights 32 (l % 4) .. +31), so a warp's code reads cover 512 contiguous bytes.
+__device__ void dequant(const Ctx& c, const MmArgs& a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = (warp & 3) * 32 + lane;
+  const int q = lane & 3;
+  const int r = (warp - kDqWarp0) * 8 + (lane >> 2);
   const bool leader = lane == 0;
-  // the chunk's block scales of row r: n_steps words of four E4M3 codes
-  {
-    const uint8_t* src = a.scales + (size_t)(o0 + r) * (a.K / 16) + k0 / 16;
-    const uint32_t dst = c.sbase + kScaleOff + r * kScaleStride;
-    for (int j = 0; j < n_steps; ++j) cp_async4(dst + 4 * j, src + 4 * j);
+  // lane 0 waits (one mbarrier poll per warp, not 32) and the warp follows:
+  // every lane takes the same branch, and the warp barrier orders lane 0's
+  // acquire before the other lanes' reads of the stage
+  auto wait_w = [&](int bar, uint32_t parity) -> bool {
+    int ok = 1;
+    if (leader) ok = wait_bar(c, bar, parity) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+  };
+  // a tile's block scales of row r (one word of four E4M3 codes per 64 of K):
+  // the four threads of a row load every fourth word
+  auto load_scales = [&](int t, int buf) {
+    const Tile x = tile_of(a, t);
+    const uint8_t* src = a.scales + (size_t)(x.o0 + r) * (a.K / 16) + x.k0 / 16;
+    const uint32_t dst = c.sbase + kScaleOff + buf * kScaleBytes + r * kScaleStride;
+    for (int wd = q; wd < x.k_len / 64; wd += 4) cp_async4(dst + 4 * wd, src + 4 * wd);
     cp_async_commit();
-  }
-  const uint8_t* srow = c.smem + kScaleOff + r * kScaleStride;
-  cp_async_wait<0>();
+  };
+  const int G = gridDim.x;
+  if ((int)blockIdx.x < a.n_tiles) load_scales(blockIdx.x, 0);
   bool ok = true;
-  for (int j = 0; j < n_steps && ok; ++j) {
-    const int s = j % kRawStages, sa = j % kAStages;
-    if (!wait_bar(c, kRawFull0 + s, (j / kRawStages) & 1)) { ok = false; break; }
-    const uint8_t* raw = c.smem + kRawOff + s * kRawBytes + r * (kStep / 2);
-    const uint4 w0 = *reinterpret_cast<const uint4*>(raw);
-    const uint4 w1 = *reinterpret_cast<const uint4*>(raw + 16);
-    __syncwarp();
-    if (leader) mbar_arrive(bar_addr(c, kRawEmpty0 + s));
-    const uint32_t sw = *reinterpret_cast<const uint32_t*>(srow + 4 * j);
-    const uint32_t s01 = e4m3x2_to_f16x2(sw & 0xffffu), s23 = e4m3x2_to_f16x2(sw >> 16);
-    const uint32_t sc[4] = {__byte_perm(s01, 0, 0x1010), __byte_perm(s01, 0, 0x3232),
-                            __byte_perm(s23, 0, 0x1010), __byte_perm(s23, 0, 0x3232)};
-    const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-    if (j >= kAStages && !wait_bar(c, kAEmpty0 + sa, ((j / kAStages) - 1) & 1)) { ok = false; break; }
-    uint8_t* arow = c.smem + kAOff + sa * kABytes + r * 128;
+  int g = 0, k = 0;
+  for (int t = blockIdx.x; t < a.n_tiles; t += G, ++k) {
+    cp_async_wait<0>();
+    // all dequantizing threads are done with the previous tile (so its scale
+    // buffer may be refilled) and this tile's scales are visible; a failure
+    // anywhere stops all of them here together
+    if (named_bar_or(kDqBarrier, kDqThreads, !ok)) break;
+    if (t + G < a.n_tiles) load_scales(t + G, (k + 1) & 1);
+    const Tile x = tile_of(a, t);
+    const uint8_t* srow = c.smem + kScaleOff + (k & 1) * kScaleBytes + r * kScaleStride;
+    for (int j = 0; j < x.n_steps; ++j, ++g) {
+      const int s = g % kRawStages, sa = g % kStages;
+      if (!wait_w(kRawFull0 + s, (g / kRawStages) & 1)) { ok = false; break; }
+      // code rows are raw_box bytes apart in the stage (64; 32 when K = 64, and
+      // then only the live threads' bytes are meaningful)
+      const uint4 w = *reinterpret_cast<const uint4*>(c.smem + kRawOff + s * kRawBytes +
+                                                     r * a.raw_box + (q & (a.raw_box / 16 - 1)) * 16);
+      __syncwarp();
+      if (leader) mbar_arrive(bar_addr(c, kRawEmpty0 + s));
+      // weights past the end of K (a half step) are never read by the MMAs
+      const bool live = j * kStep + 32 * q < x.k_len;
+      // the two blocks' scales as f16 pairs (s, s)
+      const uint32_t s2 =
+          e4m3x2_to_f16x2(live ? *reinterpret_cast<const uint16_t*>(srow + 8 * j + 2 * q) : 0u);
+      const uint32_t sc0 = __byte_perm(s2, 0, 0x1010), sc1 = __byte_perm(s2, 0, 0x3232);
+      if (g >= kStages && !wait_w(kEmpty0 + sa, ((g / kStages) - 1) & 1)) { ok = false; break; }
+      if (live) {
+        uint8_t* arow = c.smem + kAOff + sa * kABytes + (q >> 1) * kARegionBytes + r * 128;
+        const uint32_t words[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int cc = 0; cc < 8; ++cc) {  // 16-byte chunk cc: weights 8cc .. 8cc+7
-      uint32_t h[4], o[4];
-      e2m1x8_to_f16x2(words[cc], h);
+        for (int e = 0; e < 4; ++e) {  // 16-byte chunk 4 (q & 1) + e of the region row
+          uint32_t hv[4], o[4];
+          e2m1x8_to_f16x2(words[e], hv);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) o[q] = f16x2_to_bf16x2(hmul2(h[q], sc[cc >> 1]));
-      *reinterpret_cast<uint4*>(arow + ((cc ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          for (int u = 0; u < 4; ++u) o[u] = f16x2_to_bf16x2(hmul2(hv[u], e < 2 ? sc0 : sc1));
+          *reinterpret_cast<uint4*>(arow + (((4 * (q & 1) + e) ^ (r & 7)) << 4)) =
+              make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        fence_proxy_async();
+      }
+      __syncwarp();
+      if (leader) mbar_arrive(bar_addr(c, kFull0 + sa));
     }
-    fence_proxy_async();
-    __syncwarp();
-    if (leader) mbar_arrive(bar_addr(c, kAFull0 + sa));
   }
-  if (!ok || !wait_bar(c, kDFull, 0)) return;
-  umma::fence_after_sync();
-  float v[32];
-  umma::ld_32x32b_x32(tmem + ((uint32_t)((warp & 3) * 32) << 16), v);
-  umma::wait_ld();
-  const int o = o0 + r;
-  const int rows = min(kRowTile, a.n - i0);
-  if (a.n_chunks == 1) {
+}
+
+// Warps 2-5: thread r = weight row r of the tile = tensor-memory lane r.
+__device__ void epilogue(const Ctx& c, const MmArgs& a, uint32_t tmem) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quad = warp & 3;
+  const int r = quad * 32 + lane;
+  const bool leader = lane == 0;
+  const bool elected = threadIdx.x == kEpWarp0 * 32;
+  volatile int* last = reinterpret_cast<volatile int*>(c.smem + kLastSlot);
+  const size_t cstride = (size_t)a.n * a.N;  // between chunks of the partials
+  bool ok = true;
+  int k = 0;
+  for (int t = blockIdx.x; t < a.n_tiles; t += gridDim.x, ++k) {
+    const Tile x = tile_of(a, t);
+    const int tb = k & 1;
+    if (ok) {
+      int w_ok = 1;
+      if (leader) w_ok = wait_bar(c, kDFull0 + tb, (k >> 1) & 1) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, w_ok, 0) != 0;
+    }
+    if (named_bar_or(kEpBarrier, kEpThreads, !ok)) break;
+    umma::fence_after_sync();
+    float v[32];
+    umma::ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + tb * kRowTile, v);
+    umma::wait_ld();
+    umma::fence_before_sync();
+    __syncwarp();
+    if (leader) mbar_arrive(bar_addr(c, kDEmpty0 + tb));  // the MMAs may refill it
+    const int o = x.o0 + r;
+    const int rows = min(kRowTile, a.n - x.i0);
+    if (a.n_chunks == 1) {
 #pragma unroll
-    for (int q = 0; q < kRowTile; ++q) {
-      if (q < rows) {
-        const float yv = a.global_scale * v[q];
-        a.y[(size_t)(i0 + q) * a.N + o] = yv;
-        if (a.y_bf16) a.y_bf16[(size_t)(i0 + q) * a.N + o] = __float2bfloat16_rn(yv);
+      for (int i = 0; i < kRowTile; ++i) {
+        if (i < rows) {
+          const float yv = a.global_scale * v[i];
+          a.y[(size_t)(x.i0 + i) * a.N + o] = yv;
+          if (a.y_bf16) a.y_bf16[(size_t)(x.i0 + i) * a.N + o] = __float2bfloat16_rn(yv);
+        }
+      }
+      continue;
+    }
+    float* mine = a.part + x.chunk * cstride + (size_t)x.i0 * a.N + o;
+#pragma unroll
+    for (int i = 0; i < kRowTile; ++i)
+      if (i < rows) mine[(size_t)i * a.N] = v[i];
+    // The last chunk CTA of this output tile to get here adds all partials in
+    // chunk order.
+    __threadfence();
+    named_bar_sync(kEpBarrier, kEpThreads);
+    if (elected) *last = atomicAdd(a.tile_count + x.out_tile, 1) == a.n_chunks - 1;
+    named_bar_sync(kEpBarrier, kEpThreads);
+    if (!*last) continue;
+    __threadfence();
+    // sum = P_0, then sum += P_c for c = 1, 2, ...: all 32 rows of a chunk are
+    // loaded before they are added, so the loads overlap
+    const float* p0 = a.part + (size_t)x.i0 * a.N + o;
+#pragma unroll
+    for (int i = 0; i < kRowTile; ++i) v[i] = (i < rows) ? __ldcg(p0 + (size_t)i * a.N) : 0.f;
+    for (int ch = 1; ch < a.n_chunks; ++ch) {
+      const float* pc = p0 + ch * cstride;
+      float u[kRowTile];
+#pragma unroll
+      for (int i = 0; i < kRowTile; ++i) u[i] = (i < rows) ? __ldcg(pc + (size_t)i * a.N) : 0.f;
+#pragma unroll
+      for (int i = 0; i < kRowTile; ++i) v[i] += u[i];
+    }
+#pragma unroll
+    for (int i = 0; i < kRowTile; ++i) {
+      if (i < rows) {
+        const float yv = a.global_scale * v[i];
+        a.y[(size_t)(x.i0 + i) * a.N + o] = yv;
+        if (a.y_bf16) a.y_bf16[(size_t)(x.i0 + i) * a.N + o] = __float2bfloat16_rn(yv);
       }
     }
-  } else {
-    float* dst = a.part + ((size_t)chunk * a.n + i0) * a.N + o;
-#pragma unroll
-    for (int q = 0; q < kRowTile; ++q)
-      if (q < rows) dst[(size_t)q * a.N] = v[q];
+    if (elected) a.tile_count[x.out_tile] = 0;  // ready for the next call
   }
 }
 
-// Tile id -> (activation tile, chunk, weight tile); activation tiles of one
-// weight chunk are neighbours, so they run together and share it in L2.
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     nvfp4_mm_kernel(MmArgs a, const __grid_constant__ CUtensorMap tm_w,
                     const __grid_constant__ CUtensorMap tm_x) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -303,14 +480,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   c.abort_flag = reinterpret_cast<volatile int*>(smem + kAbortSlot);
   c.hdr = a.hdr;
   const int warp = threadIdx.x >> 5;
-  allow_next_grid();  // the combine kernel may be scheduled; it waits for this grid
-  const int id = blockIdx.x;
-  const int it = id % a.n_itiles;
-  const int rest = id / a.n_itiles;
-  const int chunk = rest % a.n_chunks;
-  const int o0 = (rest / a.n_chunks) * kTileN, i0 = it * kRowTile;
-  const int k0 = chunk * kKChunk;
-  const int n_steps = (min(a.K, k0 + kKChunk) - k0) / kStep;
+  allow_next_grid();  // the next call's first kernel may be scheduled; it waits for this grid
   if (c.sbase & 1023u) {  // the swizzled layouts need 1024-byte-aligned shared memory
     if (threadIdx.x == 0) set_error(a.hdr, DA_DEVERR_TIMEOUT);
     return;
@@ -318,9 +488,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t count = 1;  // TMA expect_tx arrive or tcgen05.commit
-      if ((i >= kRawEmpty0 && i < kRawEmpty0 + kRawStages) ||
-          (i >= kAFull0 && i < kAFull0 + kAStages))
-        count = 4;         // one arrive per dequantizing warp
+      if (i >= kRawEmpty0 && i < kRawEmpty0 + kRawStages) count = kDqWarps;  // per warp
+      if (i >= kFull0 && i < kFull0 + kStages) count = kDqWarps + 1;  // + the activation copy
+      if (i == kDEmpty0 || i == kDEmpty0 + 1) count = kEpWarps;
       mbar_init(bar_addr(c, i), count);
     }
     *c.abort_flag = 0;
@@ -335,39 +505,49 @@ __global__ void __launch_bounds__(kThreads, 2)
   umma::fence_after_sync();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kTmemSlot);
 
+  int n_done = 0;  // steps the MMA thread committed
   if (warp == 0) {
-    if ((threadIdx.x & 31) == 0) producer(c, &tm_w, &tm_x, o0, i0, k0, n_steps);
+    if ((threadIdx.x & 31) == 0) producer_w(c, a, &tm_w);
+  } else if (warp == kXWarp) {
+    if ((threadIdx.x & 31) == 0) producer_x(c, a, &tm_x);
   } else if (warp == 1) {
     if ((threadIdx.x & 31) == 0) {
-      mma_issuer(c, tmem, n_steps);
+      n_done = mma_issuer(c, a, tmem);
       umma::commit(bar_addr(c, kDrain));  // arrives once every MMA above has completed
     }
-  } else {
+  } else if (warp < kDqWarp0) {
     // Its stores come after the MMAs, which come after the producer's wait
-    // for the previous kernel: they never overtake that kernel's reads.
-    dequant_and_store(c, a, tmem, o0, i0, chunk, k0, n_steps);
+    // for the previous kernel: they never overtake that kernel's accesses.
+    epilogue(c, a, tmem);
+  } else {
+    dequant(c, a);
   }
   umma::fence_before_sync();
   __syncthreads();
   if (warp == 1) {
     umma::fence_after_sync();
-    if ((threadIdx.x & 31) == 0 && !mbar_wait(bar_addr(c, kDrain), 0))
-      set_error(a.hdr, DA_DEVERR_TIMEOUT);
+    if ((threadIdx.x & 31) == 0) {
+      if (!mbar_wait(bar_addr(c, kDrain), 0)) set_error(a.hdr, DA_DEVERR_TIMEOUT);
+      drain_commits(c, n_done);
+    }
     __syncwarp();
     umma::tmem_dealloc(tmem, kTmemCols);
   }
 }
 
 // fp32 / bf16 activations [n, K] -> bf16 [n_pad, K] (round to nearest even),
-// rows n .. n_pad - 1 zero.  Eight elements per thread and step.
+// rows n .. n_pad - 1 zero, eight elements per thread and step; also clears
+// the call's error word and the per-tile chunk counters.
 __global__ void nvfp4_round_kernel(const void* x, int x_dtype, __nv_bfloat16* xr, int32_t* hdr,
-                                   int n, int n_pad, int K) {
+                                   int32_t* tile_count, int n_tiles, int n, int n_pad, int K) {
   wait_prior_grid();
   allow_next_grid();  // after the wait: the next kernel may read the weight early
-  if (blockIdx.x == 0 && threadIdx.x == 0) hdr[kHdrError] = 0;  // errors of this call only
+  const size_t tid = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  const size_t nthreads = (size_t)gridDim.x * blockDim.x;
+  if (tid == 0) hdr[kHdrError] = 0;  // errors of this call only
+  for (size_t t = tid; t < (size_t)n_tiles; t += nthreads) tile_count[t] = 0;
   const size_t total = (size_t)n_pad * K / 8, valid = (size_t)n * K / 8;
-  for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < total;
-       v += (size_t)gridDim.x * blockDim.x) {
+  for (size_t v = tid; v < total; v += nthreads) {
     uint4 o = make_uint4(0, 0, 0, 0);
     if (v < valid) {
       if (x_dtype == NVFP4_X_F32) {
@@ -382,34 +562,6 @@ __global__ void nvfp4_round_kernel(const void* x, int x_dtype, __nv_bfloat16* xr
       }
     }
     reinterpret_cast<uint4*>(xr)[v] = o;
-  }
-}
-
-// y = global_scale * (((P_0 + P_1) + P_2) + ...), four outputs per thread.
-__global__ void nvfp4_combine_kernel(const float* part, float* y, __nv_bfloat16* y_bf16,
-                                     float global_scale, int n_chunks, size_t count) {
-  wait_prior_grid();
-  const size_t n4 = count / 4;
-  for (size_t v = blockIdx.x * (size_t)blockDim.x + threadIdx.x; v < n4;
-       v += (size_t)gridDim.x * blockDim.x) {
-    float4 s = __ldg(reinterpret_cast<const float4*>(part) + v);
-    for (int ch = 1; ch < n_chunks; ++ch) {
-      const float4 p = __ldg(reinterpret_cast<const float4*>(part + (size_t)ch * count) + v);
-      s.x += p.x;
-      s.y += p.y;
-      s.z += p.z;
-      s.w += p.w;
-    }
-    s.x *= global_scale;
-    s.y *= global_scale;
-    s.z *= global_scale;
-    s.w *= global_scale;
-    reinterpret_cast<float4*>(y)[v] = s;
-    if (y_bf16) {
-      __nv_bfloat162 b0 = __floats2bfloat162_rn(s.x, s.y), b1 = __floats2bfloat162_rn(s.z, s.w);
-      reinterpret_cast<uint2*>(y_bf16)[v] =
-          make_uint2(*reinterpret_cast<uint32_t*>(&b0), *reinterpret_cast<uint32_t*>(&b1));
-    }
   }
 }
 
@@ -428,14 +580,33 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 constexpr size_t kHdr = 256;
 
+// Multiprocessors of the current device (cached per device).
+int sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  if (dev >= 64) {
+    int v = 0;
+    return cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess ? v : 0;
+  }
+  if (cache[dev] == 0 &&
+      cudaDeviceGetAttribute(&cache[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    cache[dev] = 0;
+  return cache[dev];
+}
+
 size_t round_up(size_t v, size_t m) { return (v + m - 1) / m * m; }
 
 int n_chunks_of(int K) { return (K + kKChunk - 1) / kKChunk; }
 
 size_t xr_bytes(int n, int K) { return round_up((size_t)round_up(n, kRowTile) * K * 2, 256); }
 
+int n_tiles_of(int n, int N) { return (N / kTileN) * (int)(round_up(n, kRowTile) / kRowTile); }
+
+size_t counter_bytes(int n, int N) { return round_up((size_t)n_tiles_of(n, N) * 4, 256); }
+
 bool shape_ok(int n, int N, int K) {
-  if (n < 0 || N <= 0 || K <= 0 || N % kTileN || K % kStep) return false;
+  if (n < 0 || N <= 0 || K <= 0 || N % kTileN || K % kRegion) return false;
   if ((long long)round_up(n, kRowTile) * K >= (1ll << 31) || (long long)n * N >= (1ll << 31))
     return false;
   return true;
@@ -451,7 +622,7 @@ extern "C" {
 size_t nvfp4_mm_workspace_bytes(int32_t n, int32_t N, int32_t K) {
   if (!shape_ok(n, N, K)) return 0;
   const int nc = n_chunks_of(K);
-  size_t b = kHdr + xr_bytes(n, K);
+  size_t b = kHdr + counter_bytes(n, N) + xr_bytes(n, K);
   if (nc > 1) b += round_up((size_t)nc * n * N * 4, 256);
   return b;
 }
@@ -476,14 +647,17 @@ int nvfp4_mm(const void* x, int32_t x_dtype, const uint8_t* codes, const uint8_t
   const int n_pad = (int)round_up(n, kRowTile);
   const int nc = n_chunks_of(K);
   uint8_t* base = static_cast<uint8_t*>(ws);
-  __nv_bfloat16* xr = reinterpret_cast<__nv_bfloat16*>(base + kHdr);
-  float* part = nc > 1 ? reinterpret_cast<float*>(base + kHdr + xr_bytes(n, K)) : nullptr;
+  int32_t* tile_count = reinterpret_cast<int32_t*>(base + kHdr);
+  __nv_bfloat16* xr = reinterpret_cast<__nv_bfloat16*>(base + kHdr + counter_bytes(n, N));
+  float* part = nc > 1 ? reinterpret_cast<float*>(base + kHdr + counter_bytes(n, N) +
+                                                  xr_bytes(n, K))
+                       : nullptr;
 
   alignas(64) CUtensorMap tm_w, tm_x;
   {
     const cuuint64_t dims[2] = {(cuuint64_t)K / 2, (cuuint64_t)N};
     const cuuint64_t strides[1] = {(cuuint64_t)K / 2};
-    const cuuint32_t box[2] = {kStep / 2, kTileN};
+    const cuuint32_t box[2] = {(cuuint32_t)std::min(kStep / 2, K / 2), kTileN};
     const cuuint32_t elem[2] = {1, 1};
     if (enc(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(codes), dims, strides,
             box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -493,7 +667,7 @@ int nvfp4_mm(const void* x, int32_t x_dtype, const uint8_t* codes, const uint8_t
   {
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)n_pad};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {kStep, kRowTile};
+    const cuuint32_t box[2] = {kRegion, kRowTile};
     const cuuint32_t elem[2] = {1, 1};
     if (enc(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xr, dims, strides, box, elem,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -510,30 +684,29 @@ int nvfp4_mm(const void* x, int32_t x_dtype, const uint8_t* codes, const uint8_t
   a.y = y;
   a.y_bf16 = static_cast<__nv_bfloat16*>(y_bf16);
   a.hdr = static_cast<int32_t*>(ws);
+  a.tile_count = tile_count;
   a.global_scale = global_scale;
   a.n = n;
   a.N = N;
   a.K = K;
   a.n_chunks = nc;
   a.n_itiles = n_pad / kRowTile;
+  a.raw_box = std::min(kStep / 2, (int)K / 2);
 
   const size_t vec = (size_t)n_pad * K / 8;
   const int round_blocks = (int)std::min<size_t>((vec + 255) / 256, 4096);
   if (launch_after(nvfp4_round_kernel, dim3(round_blocks), dim3(256), 0, st, x, (int)x_dtype, xr,
-                   a.hdr, (int)n, n_pad, (int)K) != cudaSuccess)
+                   a.hdr, tile_count, n_tiles_of(n, N), (int)n, n_pad, (int)K) != cudaSuccess)
     return DA_ERR_CUDA;
   const long long tiles = (long long)(N / kTileN) * nc * a.n_itiles;
   if (tiles >= (1ll << 31)) return DA_ERR_UNSUPPORTED;
-  if (launch_after(nvfp4_mm_kernel, dim3((unsigned)tiles), dim3(kThreads), (size_t)kSmemBytes, st,
-                   a, tm_w, tm_x) != cudaSuccess)
+  a.n_tiles = (int)tiles;
+  const int sms = sm_count();
+  if (sms <= 0) return DA_ERR_CUDA;
+  const int grid = (int)std::min<long long>(tiles, sms);  // persistent: one CTA per SM
+  if (launch_after(nvfp4_mm_kernel, dim3(grid), dim3(kThreads), (size_t)kSmemBytes, st, a, tm_w,
+                   tm_x) != cudaSuccess)
     return DA_ERR_CUDA;
-  if (nc > 1) {
-    const size_t count = (size_t)n * N;
-    const int blocks = (int)std::min<size_t>((count / 4 + 255) / 256, 4096);
-    if (launch_after(nvfp4_combine_kernel, dim3(blocks), dim3(256), 0, st, (const float*)part, y,
-                     a.y_bf16, global_scale, nc, count) != cudaSuccess)
-      return DA_ERR_CUDA;
-  }
   return DA_OK;
 }
 

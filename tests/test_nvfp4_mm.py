@@ -148,8 +148,10 @@ def test_argument_rules(api):
     fake = vp(1 << 20)  # never dereferenced: every case fails before any device work
     assert L.nvfp4_mm_workspace_bytes(1, 100, 64) == 0
     assert L.nvfp4_mm_workspace_bytes(1, 128, 48) == 0
-    assert L.nvfp4_mm_workspace_bytes(32, 128, 1024) == 256 + 32 * 1024 * 2
-    assert L.nvfp4_mm_workspace_bytes(33, 128, 2048) == 256 + 64 * 2048 * 2 + 2 * 33 * 128 * 4
+    # header, tile counters (256-byte rounded), rounded activations, partials
+    assert L.nvfp4_mm_workspace_bytes(32, 128, 1024) == 256 + 256 + 32 * 1024 * 2
+    assert L.nvfp4_mm_workspace_bytes(33, 128, 2048) == (256 + 256 + 64 * 2048 * 2 +
+                                                         2 * 33 * 128 * 4)
     def call(x=fake, xd=0, codes=fake, scales=fake, gs=1.0, n=4, N=128, K=64, y=fake, yb=None,
              ws=fake, wsb=1 << 30):
         return L.nvfp4_mm(x, xd, codes, scales, ctypes.c_float(gs), n, N, K, y, yb, ws, wsb, None)
