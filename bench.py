@@ -291,6 +291,64 @@ def e2e_steps(case, steps, warmup):
     return a.elapsed_time(b) / steps, h2d, d2h
 
 
+# ----------------------------------------------------------------- NVFP4 weight matmul
+
+def nvfp4_section(api, peak, sizes=(1, 32, 33, 256), reps=30):
+    """The NVFP4 weight matmul on the 8192 x 4096 projection: per row count n,
+    the median device time of one call (rounding kernel + matmul kernel,
+    captured once in a CUDA graph and replayed after an L2 flush), the
+    weight-stream rate against the HBM copy peak and the matmul rate against
+    the bf16 tensor peak; and whether one row's bits are the same at every n."""
+    from invariant_decode_attention_gb300 import workloads as W
+    codes, scales, gs = W.nvfp4_weight(8192, 4096, seed=1006)
+    dc, ds = codes.cuda(), scales.cuda()
+    wbytes = codes.numel() + scales.numel()
+    pool = W.nvfp4_activations(max(sizes), 4096, seed=1006 + 7919).cuda()
+    out, ref = {}, None
+    for n in sizes:
+        x = pool[:n].contiguous()
+        ws = api.nvfp4_workspace(n, 8192, 4096)
+        y = torch.empty((n, 8192), dtype=torch.float32, device="cuda")
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                api.nvfp4_mm(x, dc, ds, gs, y=y, ws=ws)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            api.nvfp4_mm(x, dc, ds, gs, y=y, ws=ws)
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(reps):
+            flush_l2()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            graph.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times)
+        flops = 2.0 * n * 8192 * 4096
+        row = y[0].clone()
+        ref = row if ref is None else ref
+        out[f"n{n}"] = {
+            "ms": round(ms, 5),
+            "weight_gbs": round(wbytes / (ms * 1e-3) / 1e9, 1),
+            "hbm_frac": round(wbytes / (ms * 1e-3) / 1e9 / peak, 4),
+            "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+            "tensor_frac_of_measured_bf16": round(flops / (ms * 1e-3) / 1e12 / tensor_peak(), 4),
+            "row0_bits_equal_to_n1": bool(torch.equal(row, ref)),
+        }
+        del graph, ws, y
+    return {"workload": "nvfp4_proj_N8192_K4096", "weight_bytes": wbytes,
+            "timing": "CUDA graph of one call (rounding + matmul kernels), L2 flushed before "
+                      "each replay, median of %d" % reps, "by_rows": out}
+
+
 # ----------------------------------------------------------------- CPU oracle
 
 def invariance_sweep(api, sizes=(1, 2, 4, 8, 16, 32, 64, 128), steps=10):
@@ -500,6 +558,7 @@ def main():
             torch.cuda.empty_cache()
         line["other_workloads"] = extra
         line["invariance_sweep"] = invariance_sweep(api)
+        line["nvfp4_mm"] = nvfp4_section(api, peak)
         gbs, rps, done, dt = cpu_oracle_rate(wl)
         line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": _CORES,
                                 "kind": "oracle", "rows_per_s": round(rps, 3),

@@ -15,32 +15,34 @@
 // nothing of the weight stream).  The kernel is persistent, one CTA per SM,
 // each CTA taking tiles blockIdx.x, + gridDim.x, ...; its rings run on across
 // tiles, so the next tile's copies and dequantization overlap the current
-// tile's MMAs and epilogue.  Per 64-wide K step:
-//   warps 0, 22 TMA (one thread each): the step's 128 x 32 bytes of E2M1
-//               codes into a 12-deep ring (no swizzle); the step's 32 x 64
-//               bf16 activations into a 6-deep ring (128-byte swizzle,
-//               K-major);
-//   warps 6-21  dequantize: thread (r, g) owns weight row r of the tile and
-//               the 16 weights of block g of the step; it decodes them with
-//               the block's E4M3 scale into bf16 (exact: an E2M1 value times
-//               an E4M3 scale has at most six significant bits) and writes
-//               them into a 4-deep ring in the 128-byte-swizzled K-major layout
-//               the tensor core reads;
-//   warp 1      MMA issue (one thread): four M128 N32 K16 MMAs per step into
-//               one of two 32-column fp32 accumulators in tensor memory
-//               (tiles alternate between them);
-//   warps 2-5   epilogue: read a finished accumulator (warp w reads lanes
+// tile's MMAs and epilogue.  Per 128-wide K step:
+//   16 warps    dequantize: thread (r, b) owns weight row r of the tile and two
+//               16-weight blocks; it fetches its own 16 bytes of codes and its
+//               word of block scales with cp.async five steps ahead (a ring
+//               only it reads), decodes them exactly to bf16 (an E2M1 value
+//               times an E4M3 scale has at most six significant bits) and
+//               writes them into a 3-deep ring in the 128-byte-swizzled
+//               K-major layout the tensor core reads;
+//   warp 5      TMA (one thread): the step's 32 x 128 bf16 activations into a
+//               6-deep ring (128-byte swizzle, K-major);
+//   warp 1      MMA issue (one thread): eight M128 N32 K16 MMAs per step into
+//               one of two 32-column fp32 accumulators in tensor memory (tiles
+//               alternate between them); a step's weights and activations
+//               complete one barrier, and one commit frees both slots;
+//   warps 21-24 epilogue: read a finished accumulator (warp w reads lanes
 //               32 (w % 4)..), free it, and write y when K is one chunk, else
 //               the chunk's partial sums; the last of a tile's chunk CTAs to
 //               finish (a counter per output tile) adds the partials in chunk
 //               order and writes y.
-// One CTA per SM: two CTAs of this kernel sharing an SM were measured to
-// corrupt the accumulators of one of them now and then (cause not found; see
-// the design notes), so the shared-memory request keeps the second one out.
+// Warp w issues on scheduler w % 4: the pacing single-thread roles (MMA issue,
+// activation copies) have scheduler 1 to themselves, the dequantizing warps
+// fill the other three.
+// One CTA per SM: two CTAs of an earlier version of this kernel sharing an SM
+// were measured to corrupt the accumulators of one of them now and then
+// (cause not found), so the shared-memory request keeps a second one out.
 // Every mbarrier wait is bounded; on time-out the kernel records
-// DA_DEVERR_TIMEOUT, all roles leave their loops together, the copies in
-// flight and the tensor-core work are drained (bounded) and tensor memory is
-// freed.
+// DA_DEVERR_TIMEOUT, all roles leave their loops, the copies in flight and
+// the tensor-core work are drained (bounded) and tensor memory is freed.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -60,23 +62,26 @@ constexpr int kRowTile = NVFP4_MM_ROW_TILE; // activation rows per tile (MMA N)
 constexpr int kKChunk = NVFP4_MM_K_CHUNK;   // K per partial sum
 constexpr int kStep = 128;                  // K per pipeline step: two 64-wide swizzle regions
 constexpr int kRegion = 64;                 // K of one 128-byte swizzle row of bf16
-constexpr int kRawStages = 6, kStages = 3;  // code ring; operand ring (weights + activations)
+constexpr int kRawStages = 6;               // per-thread code ring (cp.async)
+constexpr int kAStages = 3, kXStages = 6;   // weight and activation operand rings
+static_assert(kXStages % kAStages == 0, "a step's barriers index both rings");
 constexpr int kRawBytes = kTileN * kStep / 2;       // 8192: E2M1 codes of a step
+constexpr int kSBytes = 512 * 4;                    // 2048: a 4-byte scale word per dequantizing thread
 constexpr int kXRegionBytes = kRowTile * kRegion * 2;  // 4096
 constexpr int kXBytes = 2 * kXRegionBytes;          // 8192: bf16 activations of a step
 constexpr int kARegionBytes = kTileN * kRegion * 2;  // 16384
 constexpr int kABytes = 2 * kARegionBytes;          // 32768: bf16 weights of a step
-constexpr int kScaleStride = kKChunk / 16 + 4;      // 68 bytes per row: no bank conflicts
-constexpr int kScaleBytes = kTileN * kScaleStride;  // one tile's block scales
 
 constexpr int kAOff = 0;
-constexpr int kXOff = kAOff + kStages * kABytes;             // 98304
-constexpr int kRawOff = kXOff + kStages * kXBytes;           // 122880
-constexpr int kScaleOff = kRawOff + kRawStages * kRawBytes;  // 172032
-constexpr int kBarOff = kScaleOff + 2 * kScaleBytes;         // 189440
-enum { kRawFull0 = 0, kRawEmpty0 = kRawFull0 + kRawStages, kFull0 = kRawEmpty0 + kRawStages,
-       kEmpty0 = kFull0 + kStages, kDFull0 = kEmpty0 + kStages, kDEmpty0 = kDFull0 + 2,
-       kDrain = kDEmpty0 + 2, kNumBars };
+constexpr int kXOff = kAOff + kAStages * kABytes;            // 98304
+constexpr int kRawOff = kXOff + kXStages * kXBytes;          // 147456
+constexpr int kSOff = kRawOff + kRawStages * kRawBytes;      // 196608
+constexpr int kBarOff = kSOff + kRawStages * kSBytes;        // 208896
+// Step g: its activations (slot g % kXStages) and its weights (slot
+// g % kAStages) complete full[g % kXStages]; one commit to empty[g % kXStages]
+// frees both slots.
+enum { kFull0 = 0, kEmpty0 = kFull0 + kXStages, kDFull0 = kEmpty0 + kXStages,
+       kDEmpty0 = kDFull0 + 2, kDrain = kDEmpty0 + 2, kNumBars };
 constexpr int kTmemSlot = kBarOff + kNumBars * 8;
 constexpr int kAbortSlot = kTmemSlot + 4;
 constexpr int kLastSlot = kAbortSlot + 4;
@@ -87,17 +92,28 @@ static_assert(kBarOff % 8 == 0, "mbarriers are 8-byte aligned");
 static_assert(kSmemBytes <= 232448 && 2 * (kSmemBytes + 1024) > 233472,
               "fits one CTA per SM and keeps a second one out");
 
-constexpr int kEpWarp0 = 2, kEpWarps = 4;    // warps 2..5
-constexpr int kDqWarp0 = 6, kDqWarps = 16;   // warps 6..21
-constexpr int kDqThreads = kDqWarps * 32;
+// Warp w issues on scheduler w % 4.  The single-thread roles that set the
+// pace (MMA issue, activation copies) get scheduler 1 to themselves; the 16
+// dequantizing warps fill schedulers 0, 2 and 3 (ids 0..20 with w % 4 != 1);
+// the epilogue needs one warp per tensor-memory lane quarter (w % 4 = 0..3).
+constexpr int kMmaWarp = 1, kXWarp = 5;
+constexpr int kDqWarps = 16, kDqLastWarp = 20;
+constexpr int kEpWarp0 = 21, kEpWarps = 4;   // warps 21..24
+static_assert(kRawBytes == kDqWarps * 32 * 16 && kSBytes == kDqWarps * 32 * 4,
+              "per-thread code and scale slots fill their stages exactly");
 constexpr int kEpThreads = kEpWarps * 32;
-constexpr int kXWarp = kDqWarp0 + kDqWarps;            // warp 22: activation producer
-constexpr int kThreads = (kXWarp + 1) * 32;            // 736
-constexpr int kDqBarrier = 1, kEpBarrier = 2;         // named barriers of the two groups
+constexpr int kThreads = (kEpWarp0 + kEpWarps) * 32;  // 800 (warps 9, 13, 17 idle)
+__host__ __device__ constexpr bool is_dq_warp(int w) { return w <= kDqLastWarp && (w & 3) != 1; }
+// index 0..15 of a dequantizing warp: its id less the scheduler-1 ids below it
+__host__ __device__ constexpr int dq_index(int w) { return w - (w + 3) / 4; }
+static_assert(dq_index(0) == 0 && dq_index(2) == 1 && dq_index(kDqLastWarp) == kDqWarps - 1,
+              "dequantizing warps are numbered 0..15");
+constexpr int kEpBarrier = 2;                          // named barrier of the epilogue warps
 constexpr uint32_t kTmemCols = 2 * kRowTile;           // two accumulators
 constexpr uint32_t kIdesc = umma::idesc_bf16_f32(kTileN, kRowTile, false);
 
 struct MmArgs {
+  const uint8_t* codes;   // [N, K / 2]
   const uint8_t* scales;  // [N, K / 16]
   float* part;            // [n_chunks, n, N] partial sums (n_chunks > 1)
   float* y;               // [n, N]
@@ -106,7 +122,6 @@ struct MmArgs {
   int32_t* tile_count;    // [N / 128, n_itiles] chunk CTAs finished per tile (n_chunks > 1)
   float global_scale;
   int n, N, K, n_chunks, n_itiles, n_tiles;
-  int raw_box;            // bytes of a code row per copy: 64, or 32 when K = 64
 };
 
 // Tile t -> (activation tile, chunk, weight tile); activation tiles of one
@@ -212,46 +227,17 @@ __device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity) {
 
 // ---------------------------------------------------------------- roles
 
-// Two producer threads, one per stream, each blocking on its own ring's free
-// slots: warp 0 streams the weight codes over the CTA's whole tile sequence,
-// warp 22 the activations.  The weight does not come from the previous kernel
-// on the stream, so it streams from the start; the activation producer first
-// waits for that kernel (which writes them).  A step's activations land on
-// the same "full" barrier as its dequantized weights (16 warp arrivals + this
-// thread's arrive with the copy's byte count), so the MMA thread waits once
-// per step.
-__device__ void producer_w(const Ctx& c, const MmArgs& a, const CUtensorMap* tm_w) {
-  int g = 0;
-  for (int t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
-    const Tile x = tile_of(a, t);
-    for (int j = 0; j < x.n_steps; ++j, ++g) {
-      const int s = g % kRawStages;
-      if (g >= kRawStages && !wait_bar(c, kRawEmpty0 + s, ((g / kRawStages) - 1) & 1)) {
-        t = a.n_tiles;
-        break;
-      }
-      // a half step at the end of K reads past the row: the copy fills zeros
-      mbar_arrive_expect_tx(bar_addr(c, kRawFull0 + s), kTileN * a.raw_box);
-      tma_load_2d(c.sbase + kRawOff + s * kRawBytes, tm_w, (x.k0 + j * kStep) / 2, x.o0,
-                  bar_addr(c, kRawFull0 + s));
-    }
-  }
-  // Copies still in flight must land before the CTA's shared memory goes away.
-  for (int s = 0; s < kRawStages; ++s) {
-    const int last = g - 1 - ((g - 1 - s) % kRawStages + kRawStages) % kRawStages;
-    if (last >= 0 && !mbar_wait(bar_addr(c, kRawFull0 + s), (last / kRawStages) & 1))
-      set_error(c.hdr, DA_DEVERR_TIMEOUT);
-  }
-}
-
+// The activation producer (one thread of warp 9) first waits for the previous
+// kernel on the stream, which writes the rounded activations, then keeps the
+// 6-deep activation ring full over the CTA's whole tile sequence.
 __device__ void producer_x(const Ctx& c, const MmArgs& a, const CUtensorMap* tm_x) {
   wait_prior_grid();
   int g = 0;
   for (int t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
     const Tile x = tile_of(a, t);
     for (int j = 0; j < x.n_steps; ++j, ++g) {
-      const int s = g % kStages;
-      if (g >= kStages && !wait_bar(c, kEmpty0 + s, ((g / kStages) - 1) & 1)) {
+      const int s = g % kXStages;
+      if (g >= kXStages && !wait_bar(c, kEmpty0 + s, ((g / kXStages) - 1) & 1)) {
         t = a.n_tiles;
         break;
       }
@@ -264,17 +250,19 @@ __device__ void producer_x(const Ctx& c, const MmArgs& a, const CUtensorMap* tm_
   }
   // Copies still in flight must land before the CTA's shared memory goes away
   // (normally the MMA thread has waited for every one already).
-  for (int s = 0; s < kStages; ++s) {
-    const int last = g - 1 - ((g - 1 - s) % kStages + kStages) % kStages;
-    if (last >= 0 && !mbar_wait(bar_addr(c, kFull0 + s), (last / kStages) & 1))
+  for (int s = 0; s < kXStages; ++s) {
+    const int last = g - 1 - ((g - 1 - s) % kXStages + kXStages) % kXStages;
+    if (last >= 0 && !mbar_wait(bar_addr(c, kFull0 + s), (last / kXStages) & 1))
       set_error(c.hdr, DA_DEVERR_TIMEOUT);
   }
 }
 
 // Tiles alternate between the two accumulators; an accumulator is reused once
-// the epilogue has read it.  Returns the number of steps whose MMAs were
-// issued and committed.
+// the epilogue has read it.  One wait and one commit per step.  Returns the
+// number of steps whose MMAs were issued and committed.
 __device__ int mma_issuer(const Ctx& c, const MmArgs& a, uint32_t tmem) {
+  const uint64_t a_desc0 = umma::smem_desc(c.sbase + kAOff, 16, 1024, umma::kSwizzle128B);
+  const uint64_t b_desc0 = umma::smem_desc(c.sbase + kXOff, 16, 1024, umma::kSwizzle128B);
   int g = 0, k = 0;
   for (int t = blockIdx.x; t < a.n_tiles; t += gridDim.x, ++k) {
     const Tile x = tile_of(a, t);
@@ -283,23 +271,24 @@ __device__ int mma_issuer(const Ctx& c, const MmArgs& a, uint32_t tmem) {
     umma::fence_after_sync();
     const uint32_t d = tmem + tb * kRowTile;
     for (int j = 0; j < x.n_steps; ++j, ++g) {
-      const int s = g % kStages;
-      if (!wait_bar(c, kFull0 + s, (g / kStages) & 1)) return g;
+      const int sx = g % kXStages, sa = g % kAStages;
+      if (!wait_bar(c, kFull0 + sx, (g / kXStages) & 1)) return g;
       umma::fence_after_sync();
       const int n_mma = min(kStep, x.k_len - j * kStep) / 16;  // 4 or 8
-      const uint32_t a0 = c.sbase + kAOff + s * kABytes, b0 = c.sbase + kXOff + s * kXBytes;
+      // descriptors of this step's operands; each MMA adds a constant offset
+      // (K = 16 is 32 bytes of a 128-byte region row; the start address field
+      // holds bytes / 16 and never carries out at these offsets)
+      const uint64_t ad0 = a_desc0 + (uint64_t)(sa * (kABytes >> 4));
+      const uint64_t bd0 = b_desc0 + (uint64_t)(sx * (kXBytes >> 4));
+      umma::mma_bf16(d, ad0, bd0, kIdesc, j ? 1u : 0u);
 #pragma unroll
-      for (int kk = 0; kk < kStep / 16; ++kk) {  // K = 16 per MMA: 32 bytes of a region row
-        if (kk < n_mma) {
-          const uint32_t off = (kk % 4) * 32;
-          const uint64_t ad = umma::smem_desc(a0 + (kk / 4) * kARegionBytes + off, 16, 1024,
-                                              umma::kSwizzle128B);
-          const uint64_t bd = umma::smem_desc(b0 + (kk / 4) * kXRegionBytes + off, 16, 1024,
-                                              umma::kSwizzle128B);
-          umma::mma_bf16(d, ad, bd, kIdesc, (j | kk) ? 1u : 0u);
-        }
+      for (int kk = 1; kk < kStep / 16; ++kk) {
+        if (kk < n_mma)
+          umma::mma_bf16(d, ad0 + (uint64_t)(((kk / 4) * kARegionBytes + (kk % 4) * 32) >> 4),
+                         bd0 + (uint64_t)(((kk / 4) * kXRegionBytes + (kk % 4) * 32) >> 4), kIdesc,
+                         1u);
       }
-      umma::commit(bar_addr(c, kEmpty0 + s));
+      umma::commit(bar_addr(c, kEmpty0 + sx));
     }
     umma::commit(bar_addr(c, kDFull0 + tb));
   }
@@ -310,24 +299,28 @@ __device__ int mma_issuer(const Ctx& c, const MmArgs& a, uint32_t tmem) {
 // before the CTA's shared memory is handed on, the last arrive on every ring
 // slot's release barrier must have landed.
 __device__ void drain_commits(const Ctx& c, int n_done) {
-  for (int s = 0; s < kStages; ++s) {
-    const int last = n_done - 1 - ((n_done - 1 - s) % kStages + kStages) % kStages;
-    if (last >= 0 && !mbar_wait(bar_addr(c, kEmpty0 + s), (last / kStages) & 1))
+  for (int s = 0; s < kXStages; ++s) {
+    const int last = n_done - 1 - ((n_done - 1 - s) % kXStages + kXStages) % kXStages;
+    if (last >= 0 && !mbar_wait(bar_addr(c, kEmpty0 + s), (last / kXStages) & 1))
       set_error(c.hdr, DA_DEVERR_TIMEOUT);
   }
 }
 
-// Warps 6-21: warp w covers weight rows 8 (w - 6) .. +7 of the tile; lane l
-// takes row 8 (w - 6) + l / 4 and blocks 2 (l % 4), 2 (l % 4) + 1 of every step
-// (weights 32 (l % 4) .. +31), so a warp's code reads cover 512 contiguous bytes.
+// Dequantizing warp d (0..15) covers weight rows 8d .. 8d + 7 of the tile; lane
+// l takes row 8d + l / 4 and blocks 2 (l % 4), 2 (l % 4) + 1 of every step
+// (weights 32 (l % 4) .. +31).  Each thread fetches its own 16 bytes of codes
+// and the 4-byte word of block scales holding its two blocks with cp.async,
+// kRawStages - 1 steps ahead, into a ring only it reads, so the weight stream
+// needs no barrier and no copy engine.
 __device__ void dequant(const Ctx& c, const MmArgs& a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = lane & 3;
-  const int r = (warp - kDqWarp0) * 8 + (lane >> 2);
+  const int tid = dq_index(warp) * 32 + lane;
+  const int r = dq_index(warp) * 8 + (lane >> 2);
   const bool leader = lane == 0;
+  const int G = gridDim.x;
   // lane 0 waits (one mbarrier poll per warp, not 32) and the warp follows:
-  // every lane takes the same branch, and the warp barrier orders lane 0's
-  // acquire before the other lanes' reads of the stage
+  // every lane takes the same branch
   auto wait_w = [&](int bar, uint32_t parity) -> bool {
     int ok = 1;
     if (leader) ok = wait_bar(c, bar, parity) ? 1 : 0;
@@ -335,44 +328,50 @@ __device__ void dequant(const Ctx& c, const MmArgs& a) {
     __syncwarp();
     return ok != 0;
   };
-  // a tile's block scales of row r (one word of four E4M3 codes per 64 of K):
-  // the four threads of a row load every fourth word
-  auto load_scales = [&](int t, int buf) {
-    const Tile x = tile_of(a, t);
-    const uint8_t* src = a.scales + (size_t)(x.o0 + r) * (a.K / 16) + x.k0 / 16;
-    const uint32_t dst = c.sbase + kScaleOff + buf * kScaleBytes + r * kScaleStride;
-    for (int wd = q; wd < x.k_len / 64; wd += 4) cp_async4(dst + 4 * wd, src + 4 * wd);
-    cp_async_commit();
+  // prefetch cursor over the CTA's steps
+  int tf = blockIdx.x, jf = 0, gf = 0;
+  Tile xf = tile_of(a, tf);
+  auto prefetch = [&]() {
+    if (tf < a.n_tiles) {
+      const int slot = gf % kRawStages;
+      if (jf * kStep + 32 * q < xf.k_len) {  // weights past the end of K are never fetched
+        const size_t row = (size_t)(xf.o0 + r);
+        const int kb = xf.k0 + jf * kStep;
+        cp_async16(c.sbase + kRawOff + slot * kRawBytes + tid * 16,
+                   a.codes + row * (a.K / 2) + kb / 2 + 16 * q);
+        cp_async4(c.sbase + kSOff + slot * kSBytes + tid * 4,
+                  a.scales + row * (a.K / 16) + kb / 16 + 4 * (q >> 1));
+      }
+      ++gf;
+      if (++jf == xf.n_steps) {
+        jf = 0;
+        tf += G;
+        if (tf < a.n_tiles) xf = tile_of(a, tf);
+      }
+    }
+    cp_async_commit();  // one group per step, empty past the last step
   };
-  const int G = gridDim.x;
-  if ((int)blockIdx.x < a.n_tiles) load_scales(blockIdx.x, 0);
+  for (int i = 0; i < kRawStages - 1; ++i) prefetch();
   bool ok = true;
-  int g = 0, k = 0;
-  for (int t = blockIdx.x; t < a.n_tiles; t += G, ++k) {
-    cp_async_wait<0>();
-    // all dequantizing threads are done with the previous tile (so its scale
-    // buffer may be refilled) and this tile's scales are visible; a failure
-    // anywhere stops all of them here together
-    if (named_bar_or(kDqBarrier, kDqThreads, !ok)) break;
-    if (t + G < a.n_tiles) load_scales(t + G, (k + 1) & 1);
+  int g = 0;
+  for (int t = blockIdx.x; t < a.n_tiles && ok; t += G) {
     const Tile x = tile_of(a, t);
-    const uint8_t* srow = c.smem + kScaleOff + (k & 1) * kScaleBytes + r * kScaleStride;
     for (int j = 0; j < x.n_steps; ++j, ++g) {
-      const int s = g % kRawStages, sa = g % kStages;
-      if (!wait_w(kRawFull0 + s, (g / kRawStages) & 1)) { ok = false; break; }
-      // code rows are raw_box bytes apart in the stage (64; 32 when K = 64, and
-      // then only the live threads' bytes are meaningful)
-      const uint4 w = *reinterpret_cast<const uint4*>(c.smem + kRawOff + s * kRawBytes +
-                                                     r * a.raw_box + (q & (a.raw_box / 16 - 1)) * 16);
-      __syncwarp();
-      if (leader) mbar_arrive(bar_addr(c, kRawEmpty0 + s));
-      // weights past the end of K (a half step) are never read by the MMAs
+      prefetch();                       // step g + kRawStages - 1
+      cp_async_wait<kRawStages - 1>();  // this thread's copies of step g have landed
+      const int slot = g % kRawStages, sa = g % kAStages, sx = g % kXStages;
       const bool live = j * kStep + 32 * q < x.k_len;
-      // the two blocks' scales as f16 pairs (s, s)
-      const uint32_t s2 =
-          e4m3x2_to_f16x2(live ? *reinterpret_cast<const uint16_t*>(srow + 8 * j + 2 * q) : 0u);
+      const uint4 w = *reinterpret_cast<const uint4*>(c.smem + kRawOff + slot * kRawBytes + tid * 16);
+      const uint32_t sw = *reinterpret_cast<const uint32_t*>(c.smem + kSOff + slot * kSBytes + tid * 4);
+      // the two blocks' scales (bytes 2 (q & 1), +1 of the word) as f16 pairs (s, s)
+      const uint32_t s2 = e4m3x2_to_f16x2(live ? ((q & 1) ? sw >> 16 : sw & 0xffffu) : 0u);
       const uint32_t sc0 = __byte_perm(s2, 0, 0x1010), sc1 = __byte_perm(s2, 0, 0x3232);
-      if (g >= kStages && !wait_w(kEmpty0 + sa, ((g / kStages) - 1) & 1)) { ok = false; break; }
+      // the weight slot is free once the MMAs of step g - kAStages are done
+      if (g >= kAStages &&
+          !wait_w(kEmpty0 + (g - kAStages) % kXStages, ((g - kAStages) / kXStages) & 1)) {
+        ok = false;
+        break;
+      }
       if (live) {
         uint8_t* arow = c.smem + kAOff + sa * kABytes + (q >> 1) * kARegionBytes + r * 128;
         const uint32_t words[4] = {w.x, w.y, w.z, w.w};
@@ -388,12 +387,14 @@ __device__ void dequant(const Ctx& c, const MmArgs& a) {
         fence_proxy_async();
       }
       __syncwarp();
-      if (leader) mbar_arrive(bar_addr(c, kFull0 + sa));
+      if (leader) mbar_arrive(bar_addr(c, kFull0 + sx));
     }
   }
+  cp_async_wait<0>();  // none of this thread's copies may still be in flight at exit
 }
 
-// Warps 2-5: thread r = weight row r of the tile = tensor-memory lane r.
+// Warps 21-24: thread r = weight row r of the tile = tensor-memory lane r
+// (warp w reads lanes 32 (w % 4) ..).
 __device__ void epilogue(const Ctx& c, const MmArgs& a, uint32_t tmem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;
@@ -471,8 +472,7 @@ __device__ void epilogue(const Ctx& c, const MmArgs& a, uint32_t tmem) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    nvfp4_mm_kernel(MmArgs a, const __grid_constant__ CUtensorMap tm_w,
-                    const __grid_constant__ CUtensorMap tm_x) {
+    nvfp4_mm_kernel(MmArgs a, const __grid_constant__ CUtensorMap tm_x) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Ctx c;
   c.smem = smem;
@@ -488,15 +488,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t count = 1;  // TMA expect_tx arrive or tcgen05.commit
-      if (i >= kRawEmpty0 && i < kRawEmpty0 + kRawStages) count = kDqWarps;  // per warp
-      if (i >= kFull0 && i < kFull0 + kStages) count = kDqWarps + 1;  // + the activation copy
+      if (i >= kFull0 && i < kFull0 + kXStages) count = kDqWarps + 1;  // + the activation copy
       if (i == kDEmpty0 || i == kDEmpty0 + 1) count = kEpWarps;
       mbar_init(bar_addr(c, i), count);
     }
     *c.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     umma::tmem_alloc(c.sbase + kTmemSlot, kTmemCols);
     umma::tmem_relinquish();
   }
@@ -506,25 +505,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kTmemSlot);
 
   int n_done = 0;  // steps the MMA thread committed
-  if (warp == 0) {
-    if ((threadIdx.x & 31) == 0) producer_w(c, a, &tm_w);
-  } else if (warp == kXWarp) {
+  if (warp == kXWarp) {
     if ((threadIdx.x & 31) == 0) producer_x(c, a, &tm_x);
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     if ((threadIdx.x & 31) == 0) {
       n_done = mma_issuer(c, a, tmem);
       umma::commit(bar_addr(c, kDrain));  // arrives once every MMA above has completed
     }
-  } else if (warp < kDqWarp0) {
+  } else if (warp >= kEpWarp0) {
     // Its stores come after the MMAs, which come after the producer's wait
     // for the previous kernel: they never overtake that kernel's accesses.
     epilogue(c, a, tmem);
-  } else {
+  } else if (is_dq_warp(warp)) {
     dequant(c, a);
   }
   umma::fence_before_sync();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     umma::fence_after_sync();
     if ((threadIdx.x & 31) == 0) {
       if (!mbar_wait(bar_addr(c, kDrain), 0)) set_error(a.hdr, DA_DEVERR_TIMEOUT);
@@ -653,17 +650,7 @@ int nvfp4_mm(const void* x, int32_t x_dtype, const uint8_t* codes, const uint8_t
                                                   xr_bytes(n, K))
                        : nullptr;
 
-  alignas(64) CUtensorMap tm_w, tm_x;
-  {
-    const cuuint64_t dims[2] = {(cuuint64_t)K / 2, (cuuint64_t)N};
-    const cuuint64_t strides[1] = {(cuuint64_t)K / 2};
-    const cuuint32_t box[2] = {(cuuint32_t)std::min(kStep / 2, K / 2), kTileN};
-    const cuuint32_t elem[2] = {1, 1};
-    if (enc(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(codes), dims, strides,
-            box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return DA_ERR_CUDA;
-  }
+  alignas(64) CUtensorMap tm_x;
   {
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)n_pad};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
@@ -679,6 +666,7 @@ int nvfp4_mm(const void* x, int32_t x_dtype, const uint8_t* codes, const uint8_t
   if (attr != cudaSuccess) return DA_ERR_CUDA;
 
   MmArgs a;
+  a.codes = codes;
   a.scales = scales;
   a.part = part;
   a.y = y;
@@ -691,7 +679,6 @@ int nvfp4_mm(const void* x, int32_t x_dtype, const uint8_t* codes, const uint8_t
   a.K = K;
   a.n_chunks = nc;
   a.n_itiles = n_pad / kRowTile;
-  a.raw_box = std::min(kStep / 2, (int)K / 2);
 
   const size_t vec = (size_t)n_pad * K / 8;
   const int round_blocks = (int)std::min<size_t>((vec + 255) / 256, 4096);
@@ -704,8 +691,7 @@ int nvfp4_mm(const void* x, int32_t x_dtype, const uint8_t* codes, const uint8_t
   const int sms = sm_count();
   if (sms <= 0) return DA_ERR_CUDA;
   const int grid = (int)std::min<long long>(tiles, sms);  // persistent: one CTA per SM
-  if (launch_after(nvfp4_mm_kernel, dim3(grid), dim3(kThreads), (size_t)kSmemBytes, st, a, tm_w,
-                   tm_x) != cudaSuccess)
+  if (launch_after(nvfp4_mm_kernel, dim3(grid), dim3(kThreads), (size_t)kSmemBytes, st, a, tm_x) != cudaSuccess)
     return DA_ERR_CUDA;
   return DA_OK;
 }
