@@ -426,6 +426,10 @@ def main():
                              "long_context_fp8"])
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the secondary workloads and the CPU baseline")
+    ap.add_argument("--nvfp4-only", type=int, nargs="+", metavar="ROWS",
+                    help="time only the NVFP4 weight matmul at these row counts and print "
+                         "its JSON")
+    ap.add_argument("--nvfp4-reps", type=int, default=30)
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
@@ -441,6 +445,11 @@ def main():
     from invariant_decode_attention_gb300 import api
     api.lib()
     peak, peak_kind = measured_peaks()
+    if args.nvfp4_only:
+        if rank == 0:
+            print(json.dumps(nvfp4_section(api, peak, sizes=tuple(args.nvfp4_only),
+                                           reps=args.nvfp4_reps)), flush=True)
+        return
 
     wl = build_workload(args.workload, rank)
     case = GpuCase(wl, dev, api.INVARIANT)
