@@ -12,7 +12,7 @@ writes that definition out, with no tiling, splitting or reordering:
     lse   = m + log sum_i exp(s_i - m)              (natural log)
     out   = sum_i exp(s_i - m) * V[i, :] / sum_i exp(s_i - m)
 
-Readings of points the pages leave open (each is also listed in the design doc):
+Readings of points the pages leave open:
 
 * GQA head map: query head ``j`` reads KV head ``j // (H_q / H_kv)``.
 * Latent (MLA-style) KV: when no separate V cache is given, ``V = K[..., :D_v]``
