@@ -21,10 +21,10 @@
 //               word of block scales with cp.async five steps ahead (a ring
 //               only it reads), decodes them exactly to bf16 (an E2M1 value
 //               times an E4M3 scale has at most six significant bits) and
-//               writes them into a 3-deep ring in the 128-byte-swizzled
+//               writes them into a 4-deep ring in the 128-byte-swizzled
 //               K-major layout the tensor core reads;
 //   warp 5      TMA (one thread): the step's 32 x 128 bf16 activations into a
-//               6-deep ring (128-byte swizzle, K-major);
+//               4-deep ring (128-byte swizzle, K-major);
 //   warp 1      MMA issue (one thread): eight M128 N32 K16 MMAs per step into
 //               one of two 32-column fp32 accumulators in tensor memory (tiles
 //               alternate between them); a step's weights and activations
@@ -63,7 +63,7 @@ constexpr int kKChunk = NVFP4_MM_K_CHUNK;   // K per partial sum
 constexpr int kStep = 128;                  // K per pipeline step: two 64-wide swizzle regions
 constexpr int kRegion = 64;                 // K of one 128-byte swizzle row of bf16
 constexpr int kRawStages = 6;               // per-thread code ring (cp.async)
-constexpr int kAStages = 3, kXStages = 6;   // weight and activation operand rings
+constexpr int kAStages = 4, kXStages = 4;   // weight and activation operand rings
 static_assert(kXStages % kAStages == 0, "a step's barriers index both rings");
 constexpr int kRawBytes = kTileN * kStep / 2;       // 8192: E2M1 codes of a step
 constexpr int kSBytes = 512 * 4;                    // 2048: a 4-byte scale word per dequantizing thread
@@ -73,10 +73,10 @@ constexpr int kARegionBytes = kTileN * kRegion * 2;  // 16384
 constexpr int kABytes = 2 * kARegionBytes;          // 32768: bf16 weights of a step
 
 constexpr int kAOff = 0;
-constexpr int kXOff = kAOff + kAStages * kABytes;            // 98304
-constexpr int kRawOff = kXOff + kXStages * kXBytes;          // 147456
-constexpr int kSOff = kRawOff + kRawStages * kRawBytes;      // 196608
-constexpr int kBarOff = kSOff + kRawStages * kSBytes;        // 208896
+constexpr int kXOff = kAOff + kAStages * kABytes;            // 131072
+constexpr int kRawOff = kXOff + kXStages * kXBytes;          // 163840
+constexpr int kSOff = kRawOff + kRawStages * kRawBytes;      // 212992
+constexpr int kBarOff = kSOff + kRawStages * kSBytes;        // 225280
 // Step g: its activations (slot g % kXStages) and its weights (slot
 // g % kAStages) complete full[g % kXStages]; one commit to empty[g % kXStages]
 // frees both slots.
@@ -227,9 +227,9 @@ __device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity) {
 
 // ---------------------------------------------------------------- roles
 
-// The activation producer (one thread of warp 9) first waits for the previous
+// The activation producer (one thread of warp 5) first waits for the previous
 // kernel on the stream, which writes the rounded activations, then keeps the
-// 6-deep activation ring full over the CTA's whole tile sequence.
+// 4-deep activation ring full over the CTA's whole tile sequence.
 __device__ void producer_x(const Ctx& c, const MmArgs& a, const CUtensorMap* tm_x) {
   wait_prior_grid();
   int g = 0;
