@@ -15,17 +15,17 @@
 // nothing of the weight stream).  The kernel is persistent, one CTA per SM,
 // each CTA taking tiles blockIdx.x, + gridDim.x, ...; its rings run on across
 // tiles, so the next tile's copies and dequantization overlap the current
-// tile's MMAs and epilogue.  Per 128-wide K step:
+// tile's MMAs and epilogue.  Per 256-wide K step:
 //   16 warps    dequantize: thread (r, b) owns weight row r of the tile and two
-//               16-weight blocks; it fetches its own 16 bytes of codes and its
-//               word of block scales with cp.async five steps ahead (a ring
-//               only it reads), decodes them exactly to bf16 (an E2M1 value
-//               times an E4M3 scale has at most six significant bits) and
-//               writes them into a 4-deep ring in the 128-byte-swizzled
-//               K-major layout the tensor core reads;
-//   warp 5      TMA (one thread): the step's 32 x 128 bf16 activations into a
-//               4-deep ring (128-byte swizzle, K-major);
-//   warp 1      MMA issue (one thread): eight M128 N32 K16 MMAs per step into
+//               16-weight blocks of each 128-wide half of the step; it fetches
+//               its own 2 x 16 bytes of codes and 2 words of block scales with
+//               cp.async two steps ahead (a ring only it reads), decodes them
+//               exactly to bf16 (an E2M1 value times an E4M3 scale has at most
+//               six significant bits) and writes them into a 2-deep ring in
+//               the 128-byte-swizzled K-major layout the tensor core reads;
+//   warp 5      TMA (one thread): the step's 32 x 256 bf16 activations into a
+//               2-deep ring (128-byte swizzle, K-major);
+//   warp 1      MMA issue (one thread): sixteen M128 N32 K16 MMAs per step into
 //               one of two 32-column fp32 accumulators in tensor memory (tiles
 //               alternate between them); a step's weights and activations
 //               complete one barrier, and one commit frees both slots;
@@ -60,17 +60,19 @@ namespace {
 constexpr int kTileN = NVFP4_MM_TILE_N;     // weight rows per tile (MMA M)
 constexpr int kRowTile = NVFP4_MM_ROW_TILE; // activation rows per tile (MMA N)
 constexpr int kKChunk = NVFP4_MM_K_CHUNK;   // K per partial sum
-constexpr int kStep = 128;                  // K per pipeline step: two 64-wide swizzle regions
+constexpr int kStep = 256;                  // K per pipeline step: four 64-wide swizzle regions
+constexpr int kSub = 128;                   // K a dequantizing thread covers per half step: 32
 constexpr int kRegion = 64;                 // K of one 128-byte swizzle row of bf16
-constexpr int kRawStages = 6;               // per-thread code ring (cp.async)
-constexpr int kAStages = 4, kXStages = 4;   // weight and activation operand rings
+constexpr int kRegions = kStep / kRegion;
+constexpr int kRawStages = 3;               // per-thread code ring (cp.async)
+constexpr int kAStages = 2, kXStages = 2;   // weight and activation operand rings
 static_assert(kXStages % kAStages == 0, "a step's barriers index both rings");
-constexpr int kRawBytes = kTileN * kStep / 2;       // 8192: E2M1 codes of a step
-constexpr int kSBytes = 512 * 4;                    // 2048: a 4-byte scale word per dequantizing thread
+constexpr int kRawBytes = kTileN * kStep / 2;       // 16384: E2M1 codes of a step
+constexpr int kSBytes = 512 * 8;                    // 4096: two 4-byte scale words per dequantizing thread
 constexpr int kXRegionBytes = kRowTile * kRegion * 2;  // 4096
-constexpr int kXBytes = 2 * kXRegionBytes;          // 8192: bf16 activations of a step
+constexpr int kXBytes = kRegions * kXRegionBytes;   // 16384: bf16 activations of a step
 constexpr int kARegionBytes = kTileN * kRegion * 2;  // 16384
-constexpr int kABytes = 2 * kARegionBytes;          // 32768: bf16 weights of a step
+constexpr int kABytes = kRegions * kARegionBytes;   // 65536: bf16 weights of a step
 
 constexpr int kAOff = 0;
 constexpr int kXOff = kAOff + kAStages * kABytes;            // 131072
@@ -99,7 +101,7 @@ static_assert(kSmemBytes <= 232448 && 2 * (kSmemBytes + 1024) > 233472,
 constexpr int kMmaWarp = 1, kXWarp = 5;
 constexpr int kDqWarps = 16, kDqLastWarp = 20;
 constexpr int kEpWarp0 = 21, kEpWarps = 4;   // warps 21..24
-static_assert(kRawBytes == kDqWarps * 32 * 16 && kSBytes == kDqWarps * 32 * 4,
+static_assert(kRawBytes == kDqWarps * 32 * 32 && kSBytes == kDqWarps * 32 * 8,
               "per-thread code and scale slots fill their stages exactly");
 constexpr int kEpThreads = kEpWarps * 32;
 constexpr int kThreads = (kEpWarp0 + kEpWarps) * 32;  // 800 (warps 9, 13, 17 idle)
@@ -229,7 +231,7 @@ __device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity) {
 
 // The activation producer (one thread of warp 5) first waits for the previous
 // kernel on the stream, which writes the rounded activations, then keeps the
-// 4-deep activation ring full over the CTA's whole tile sequence.
+// 2-deep activation ring full over the CTA's whole tile sequence.
 __device__ void producer_x(const Ctx& c, const MmArgs& a, const CUtensorMap* tm_x) {
   wait_prior_grid();
   int g = 0;
@@ -241,7 +243,7 @@ __device__ void producer_x(const Ctx& c, const MmArgs& a, const CUtensorMap* tm_
         t = a.n_tiles;
         break;
       }
-      const int regions = min(kStep, x.k_len - j * kStep) / kRegion;  // 1 or 2
+      const int regions = min(kStep, x.k_len - j * kStep) / kRegion;  // 1 .. 4
       mbar_arrive_expect_tx(bar_addr(c, kFull0 + s), regions * kXRegionBytes);
       for (int rg = 0; rg < regions; ++rg)
         tma_load_2d(c.sbase + kXOff + s * kXBytes + rg * kXRegionBytes, tm_x,
@@ -274,7 +276,7 @@ __device__ int mma_issuer(const Ctx& c, const MmArgs& a, uint32_t tmem) {
       const int sx = g % kXStages, sa = g % kAStages;
       if (!wait_bar(c, kFull0 + sx, (g / kXStages) & 1)) return g;
       umma::fence_after_sync();
-      const int n_mma = min(kStep, x.k_len - j * kStep) / 16;  // 4 or 8
+      const int n_mma = min(kStep, x.k_len - j * kStep) / 16;  // 4 .. 16
       // descriptors of this step's operands; each MMA adds a constant offset
       // (K = 16 is 32 bytes of a 128-byte region row; the start address field
       // holds bytes / 16 and never carries out at these offsets)
@@ -307,11 +309,12 @@ __device__ void drain_commits(const Ctx& c, int n_done) {
 }
 
 // Dequantizing warp d (0..15) covers weight rows 8d .. 8d + 7 of the tile; lane
-// l takes row 8d + l / 4 and blocks 2 (l % 4), 2 (l % 4) + 1 of every step
-// (weights 32 (l % 4) .. +31).  Each thread fetches its own 16 bytes of codes
-// and the 4-byte word of block scales holding its two blocks with cp.async,
-// kRawStages - 1 steps ahead, into a ring only it reads, so the weight stream
-// needs no barrier and no copy engine.
+// l takes row 8d + l / 4 and, in each 128-wide half h of every step, blocks
+// 2 (l % 4), 2 (l % 4) + 1 (weights 128 h + 32 (l % 4) .. +31).  For each half
+// a thread fetches its own 16 bytes of codes and the 4-byte word of block
+// scales holding its two blocks with cp.async, kRawStages - 1 steps ahead,
+// into a ring only it reads, so the weight stream needs no barrier and no
+// copy engine.
 __device__ void dequant(const Ctx& c, const MmArgs& a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = lane & 3;
@@ -334,13 +337,16 @@ __device__ void dequant(const Ctx& c, const MmArgs& a) {
   auto prefetch = [&]() {
     if (tf < a.n_tiles) {
       const int slot = gf % kRawStages;
-      if (jf * kStep + 32 * q < xf.k_len) {  // weights past the end of K are never fetched
-        const size_t row = (size_t)(xf.o0 + r);
-        const int kb = xf.k0 + jf * kStep;
-        cp_async16(c.sbase + kRawOff + slot * kRawBytes + tid * 16,
-                   a.codes + row * (a.K / 2) + kb / 2 + 16 * q);
-        cp_async4(c.sbase + kSOff + slot * kSBytes + tid * 4,
-                  a.scales + row * (a.K / 16) + kb / 16 + 4 * (q >> 1));
+      const size_t row = (size_t)(xf.o0 + r);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int kb = jf * kStep + h * kSub;  // K of the half step within the chunk
+        if (kb + 32 * q < xf.k_len) {  // weights past the end of K are never fetched
+          cp_async16(c.sbase + kRawOff + slot * kRawBytes + tid * 32 + h * 16,
+                     a.codes + row * (a.K / 2) + (xf.k0 + kb) / 2 + 16 * q);
+          cp_async4(c.sbase + kSOff + slot * kSBytes + tid * 8 + h * 4,
+                    a.scales + row * (a.K / 16) + (xf.k0 + kb) / 16 + 4 * (q >> 1));
+        }
       }
       ++gf;
       if (++jf == xf.n_steps) {
@@ -360,20 +366,26 @@ __device__ void dequant(const Ctx& c, const MmArgs& a) {
       prefetch();                       // step g + kRawStages - 1
       cp_async_wait<kRawStages - 1>();  // this thread's copies of step g have landed
       const int slot = g % kRawStages, sa = g % kAStages, sx = g % kXStages;
-      const bool live = j * kStep + 32 * q < x.k_len;
-      const uint4 w = *reinterpret_cast<const uint4*>(c.smem + kRawOff + slot * kRawBytes + tid * 16);
-      const uint32_t sw = *reinterpret_cast<const uint32_t*>(c.smem + kSOff + slot * kSBytes + tid * 4);
-      // the two blocks' scales (bytes 2 (q & 1), +1 of the word) as f16 pairs (s, s)
-      const uint32_t s2 = e4m3x2_to_f16x2(live ? ((q & 1) ? sw >> 16 : sw & 0xffffu) : 0u);
-      const uint32_t sc0 = __byte_perm(s2, 0, 0x1010), sc1 = __byte_perm(s2, 0, 0x3232);
       // the weight slot is free once the MMAs of step g - kAStages are done
       if (g >= kAStages &&
           !wait_w(kEmpty0 + (g - kAStages) % kXStages, ((g - kAStages) / kXStages) & 1)) {
         ok = false;
         break;
       }
-      if (live) {
-        uint8_t* arow = c.smem + kAOff + sa * kABytes + (q >> 1) * kARegionBytes + r * 128;
+      bool wrote = false;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // half step h: K 128 h .. 128 h + 127 of the step
+        const bool live = j * kStep + h * kSub + 32 * q < x.k_len;
+        if (!live) continue;
+        const uint4 w = *reinterpret_cast<const uint4*>(c.smem + kRawOff + slot * kRawBytes +
+                                                       tid * 32 + h * 16);
+        const uint32_t sw = *reinterpret_cast<const uint32_t*>(c.smem + kSOff + slot * kSBytes +
+                                                               tid * 8 + h * 4);
+        // the two blocks' scales (bytes 2 (q & 1), +1 of the word) as f16 pairs (s, s)
+        const uint32_t s2 = e4m3x2_to_f16x2((q & 1) ? sw >> 16 : sw & 0xffffu);
+        const uint32_t sc0 = __byte_perm(s2, 0, 0x1010), sc1 = __byte_perm(s2, 0, 0x3232);
+        uint8_t* arow = c.smem + kAOff + sa * kABytes + (2 * h + (q >> 1)) * kARegionBytes +
+                        r * 128;
         const uint32_t words[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {  // 16-byte chunk 4 (q & 1) + e of the region row
@@ -384,8 +396,9 @@ __device__ void dequant(const Ctx& c, const MmArgs& a) {
           *reinterpret_cast<uint4*>(arow + (((4 * (q & 1) + e) ^ (r & 7)) << 4)) =
               make_uint4(o[0], o[1], o[2], o[3]);
         }
-        fence_proxy_async();
+        wrote = true;
       }
+      if (wrote) fence_proxy_async();
       __syncwarp();
       if (leader) mbar_arrive(bar_addr(c, kFull0 + sx));
     }
