@@ -242,7 +242,7 @@ static int plan_impl(const da_problem* prob, int32_t policy, const int32_t* d_le
   const int sms = sm_count(dev);
   if (sms <= 0) return DA_ERR_CUDA;
   // CTAs that one (row, split) item occupies: one per KV head (CUDA-core
-  // variant) or a cluster pair splitting D_v (tensor-core variant).
+  // variant) or two, one per half of D_v (tensor-core variant).
   const int per_item = (v.id == DA_VARIANT_MLA) ? 2 : prob->num_kv_heads;
   // persistent CTAs: as many as can be resident at once (whole pairs for the
   // tensor-core variant)

@@ -101,20 +101,17 @@ constexpr uint32_t kIdescS = umma::idesc_bf16_f32(kHeads, kSub, false);
 constexpr uint32_t kIdescO = umma::idesc_bf16_f32(kHeads, kDvHalf, true);
 
 // TMA copies from a 2-D tensor map (dim 0 = the 576 dims of a row, dim 1 =
-// rows), 128-byte swizzle applied by the copy engine from the shared-memory
-// address.  Each copy lands at the same shared-memory offset in both CTAs of
-// the pair (multicast) and completes its bytes on the mbarrier at offset `bar`
-// in each of them.
-constexpr uint16_t kPairMask = 0x3;
+// rows) into this CTA's own shared memory, 128-byte swizzle applied by the
+// copy engine from the shared-memory address; each completes its bytes on the
+// mbarrier at shared address `bar`.
 
 // Box {64, 1} at rows r0..r3: four 128-byte rows land at dst + 128 * i.
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* tm, int col, int r0,
                                             int r1, int r2, int r3, uint32_t bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar),
-      "h"(kPairMask)
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
       : "memory");
 }
 
@@ -123,29 +120,9 @@ __device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap* tm, in
                                          uint32_t bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(col), "r"(row), "r"(bar), "h"(kPairMask)
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(col), "r"(row), "r"(bar)
       : "memory");
-}
-
-// One arrive on the mbarrier at offset `bar` in both CTAs of the pair once
-// every tensor-core operation this thread issued so far has completed.
-__device__ __forceinline__ void commit_pair(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar), "h"(kPairMask)
-      : "memory");
-}
-
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
-               ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
 }
 
 // Start pulling `bytes` (a multiple of 16) at a 16-byte-aligned address into L2.
@@ -195,8 +172,10 @@ __device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity) {
 // The units a CTA takes.  Unit 2i + h is value half h of work item i; CTA
 // pair q (CTAs 2q, 2q + 1) takes item k * pairs + q in even rounds k and
 // k * pairs + (pairs - 1 - q) in odd ones.  The list is sorted largest
-// first, so this serpentine deal evens out the pairs' sums.  Placement
-// only: no unit's arithmetic depends on its CTA.
+// first, so this serpentine deal evens out the pairs' sums, and the two
+// halves of an item run at the same time on neighbouring CTAs (all CTAs are
+// resident), so the second read of each latent row is served by L2.
+// Placement only: no unit's arithmetic depends on its CTA.
 __device__ __forceinline__ int next_unit(int u) {
   const int pairs = gridDim.x >> 1, q = blockIdx.x >> 1;
   const int k = (u >> 1) / pairs + 1;
@@ -260,7 +239,6 @@ __device__ __forceinline__ bool latent_decode(const Launch& p, int b, int tok, i
 // ---------------------------------------------------------------- producer
 __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
   const int pt = threadIdx.x - 128;  // 0..127
-  const uint32_t rank = cluster_rank();
   const int pw = pt >> 5, pl = pt & 31;
   uint32_t g = 0, n_ne = 0;
   bool alive = true;
@@ -282,8 +260,7 @@ __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
     if (!wait_w(kQFree, (n_ne & 1) ^ 1)) break;
     if (pt == 0) mbar_arrive_expect_tx(bar_addr(c, kQFull), kQSRegions * q_boxes * kQBoxRows * 128);
     __syncwarp();
-    // this CTA copies every other box; each box lands in both CTAs
-    for (int i = 2 * pt + (int)rank; i < kQSRegions * q_boxes; i += 256) {
+    for (int i = pt; i < kQSRegions * q_boxes; i += 128) {
       const int j = i / q_boxes, rb = i % q_boxes;
       tma_tile(c.sbase + j * (kHeads * 128) + rb * (kQBoxRows * 128), c.tm_q, kQT + 64 * j,
                x.b * p.H_q + rb * kQBoxRows, bar_addr(c, kQFull));
@@ -339,14 +316,13 @@ __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
       const uint32_t full = bar_addr(c, kFull0 + stage);
       if (pt == 0) mbar_arrive_expect_tx(full, kStageBytes);
       // lane q < 4 copies the group of entries 16*pw + 4q .. 16*pw + 4q + 3
-      // when the group's parity is this CTA's rank; each group lands in both
       int r[4], sr[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         r[i] = __shfl_sync(0xffffffffu, my_row, (4 * pl + i) & 31);
         sr[i] = __shfl_sync(0xffffffffu, my_src, (4 * pl + i) & 31);
       }
-      if (pl < 4 && (pl & 1) == (int)rank) {
+      if (pl < 4) {
         const uint32_t dst = c.sbase + kStageOffset + stage * kStageBytes +
                              (kEntPerWarp * pw + 4 * pl) * 128;
         if (sr[0] == sr[1] && sr[0] == sr[2] && sr[0] == sr[3]) {
@@ -421,7 +397,7 @@ __device__ void mma_issuer(const Launch& p, const Ctx& c, uint32_t tmem, int n_u
                        bv + (uint64_t)((kk * 2048) >> 4), kIdescO,
                        (first && kk == 0) ? 0u : 1u);
       umma::commit(bar_addr(c, kODone0 + (gp & 1)));
-      commit_pair(bar_addr(c, kEmpty0 + (gp % kStages)));
+      umma::commit(bar_addr(c, kEmpty0 + (gp % kStages)));
       return true;
     };
     // Issue order S(g), PV(g-1): S(g) goes to the other S buffer, so it runs
@@ -447,7 +423,7 @@ __device__ void mma_issuer(const Launch& p, const Ctx& c, uint32_t tmem, int n_u
                          b, kIdescS, 1u);
       }
       umma::commit(bar_addr(c, kSFull0 + sb));
-      if (i == n_sub - 1) commit_pair(bar_addr(c, kQFree));
+      if (i == n_sub - 1) umma::commit(bar_addr(c, kQFree));
       if (i > 0 && !pv(g - 1, i == 1)) return;
     }
     if (!pv(g - 1, n_sub == 1)) return;
@@ -648,7 +624,7 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
   }
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     split_mla_kernel(Launch p, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_x,
                      const __grid_constant__ CUtensorMap tm_q) {
@@ -677,20 +653,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if ((i >= kSFree0 && i < kSFree0 + 2) || (i >= kPFull0 && i < kPFull0 + 2) ||
           i == kOFree || i == kQTFull)
         count = 4;                                                   // softmax warps
-      if ((i >= kEmpty0 && i < kEmpty0 + kStages) || i == kQFree)
-        count = 2;                                                   // both CTAs' MMAs
       mbar_init(bar_addr(c, i), count);
     }
     *c.abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fence_mbar_init();
   }
   if (warp == 8) {
     umma::tmem_alloc(c.sbase + kTmemSlot, kTmemCols);
     umma::tmem_relinquish();
   }
-  // both CTAs' barriers exist before either copies into or arrives on them
+  // the barriers exist before any role copies into or arrives on them
   umma::fence_before_sync();
-  cluster_sync();
+  __syncthreads();
   umma::fence_after_sync();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kTmemSlot);
 
@@ -719,8 +693,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
     }
-    // the peer's releases of this CTA's stages and Q (it commits the same
-    // sequence): wait until its last ones have landed here
+    // the last releases of the stages and of Q (commits issued before the
+    // drain): wait until they have landed, so no arrive is still in flight
+    // when the shared memory is given up
     if ((threadIdx.x & 31) == 0) {
       for (int st = 0; st < kStages; ++st) {
         const int last = (int)g_done - 1 - (((int)g_done - 1 - st) % kStages + kStages) % kStages;
@@ -731,11 +706,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         set_error(p.hdr, DA_DEVERR_TIMEOUT);
     }
     __syncwarp();
+    umma::tmem_dealloc(tmem, kTmemCols);
   }
-  // the peer CTA no longer copies into, or arrives on, this CTA's shared
-  // memory once both have drained their copies and tensor-core work
-  cluster_sync();
-  if (warp == 8) umma::tmem_dealloc(tmem, kTmemCols);
 }
 
 // Stands in for an empty cache: dummy copies of masked entries read it.
@@ -772,22 +744,21 @@ bool encode_rows(CUtensorMap* tm, const void* base, long long rows, int box_rows
 
 bool mla_supported(int H_q) { return H_q >= 16 && H_q <= kHeads; }
 
-// Persistent CTAs: pairs of CTAs that can be resident at once (one per SM).
+// Persistent CTAs: as many as can be resident at once (one per SM), rounded
+// down to an even number (units are dealt to pairs of CTAs).
 int mla_resident_ctas(int sms) {
-  static const int clusters = [] {
+  static const int per_sm = [] {
     if (cudaFuncSetAttribute(split_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemBytes) != cudaSuccess)
-      return 0;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+      return 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, split_mla_kernel, &cfg) != cudaSuccess) n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, split_mla_kernel, kThreads,
+                                                      kSmemBytes) != cudaSuccess || n < 1)
+      n = 1;
     return n;
   }();
-  const int pairs = sms / 2;
-  return 2 * ((clusters > 0 && clusters < pairs) ? clusters : pairs);
+  const int n = per_sm * sms;
+  return n < 2 ? 2 : (n & ~1);
 }
 
 cudaError_t launch_split_mla(const Launch& p, int grid, cudaStream_t stream) {
