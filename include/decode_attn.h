@@ -207,19 +207,26 @@ int decode_attn_forward(const da_problem* prob, int32_t policy, const void* q, c
  * (64 MiB) per device, held until the process exits from the time the
  * library's code is loaded on that device.  The first call on a device looks
  * up the array's device address (cudaGetSymbolAddress, with that device
- * current); make that first call before any stream capture.  Nothing is
- * allocated, here or later.  A problem whose workspace
- * (decode_attn_workspace_bytes) exceeds DA_STATIC_WORKSPACE_BYTES is
- * rejected with DA_ERR_WORKSPACE before anything is enqueued.  All calls on a
- * device share the one array and it keeps the last call's contents (the plan
- * rewrites everything a call reads, including the error word), so calls whose
- * work overlaps on the GPU -- different streams without ordering, or
- * concurrent host threads -- race and corrupt each other's results:
- * serialise them. */
+ * current) and caches it; make that first call before any stream capture.
+ * The cached address is stale after cudaDeviceReset: do not call this entry
+ * point again in a process that reset the device.  Nothing is allocated,
+ * here or later.  A problem whose workspace (decode_attn_workspace_bytes)
+ * exceeds DA_STATIC_WORKSPACE_BYTES is rejected with DA_ERR_WORKSPACE before
+ * anything is enqueued.  All calls on a device share the one array and it
+ * keeps the last call's contents (the plan rewrites everything a call reads,
+ * including the error word), so calls whose work overlaps on the GPU --
+ * different streams without ordering, or concurrent host threads -- race and
+ * corrupt each other's results: serialise them.
+ *
+ * plan_out (host, may be NULL): on DA_OK, receives the call's plan, whose
+ * workspace is the static array; decode_attn_read_error(plan_out, ...) then
+ * reads the device input-check bits (DA_DEVERR_*) of this call, as long as no
+ * later call of this entry point on the device has overwritten them. */
 #define DA_STATIC_WORKSPACE_BYTES (64u << 20)
 int decode_attn_forward_static(const da_problem* prob, int32_t policy, const void* q,
                                const void* k, const void* v, const int32_t* table,
-                               const int32_t* lengths, void* out, float* lse, void* stream);
+                               const int32_t* lengths, void* out, float* lse, void* stream,
+                               da_plan* plan_out);
 
 /* The same three steps over two KV sources per row.  Row b attends over its
  * main list (as above) followed by extra_lengths[b] entries gathered from a

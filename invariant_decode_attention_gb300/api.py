@@ -136,7 +136,8 @@ def lib():
     L.decode_attn_forward_extra.argtypes = [P(DaProblem), i32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                             vp, sz, vp, vp, vp]
     L.decode_attn_forward_static.restype = ctypes.c_int
-    L.decode_attn_forward_static.argtypes = [P(DaProblem), i32, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.decode_attn_forward_static.argtypes = [P(DaProblem), i32, vp, vp, vp, vp, vp, vp, vp, vp,
+                                             P(DaPlan)]
     L.decode_attn_copy_plan.restype = ctypes.c_int
     L.decode_attn_copy_plan.argtypes = [P(DaPlan), vp, vp, P(i32), vp, vp]
     L.nvfp4_mm_workspace_bytes.restype = sz
@@ -270,12 +271,15 @@ def forward(prob: DaProblem, policy, q, k, v, table, lengths, ws, out, lse, stre
            "forward")
 
 
-def forward_static(prob: DaProblem, policy, q, k, v, table, lengths, out, lse, stream=None):
+def forward_static(prob: DaProblem, policy, q, k, v, table, lengths, out, lse,
+                   stream=None) -> DaPlan:
     """The forward pass with the library's own fixed device scratch array, for
     callers that cannot allocate device memory (see the header): no workspace
     argument, nothing allocated.  Raises DecodeAttnError(ERR_WORKSPACE) for a
     problem whose workspace exceeds STATIC_WORKSPACE_BYTES.  Calls sharing a
-    device must not overlap on the GPU."""
+    device must not overlap on the GPU.  Returns the call's plan, which
+    read_error accepts until the next call overwrites the array."""
+    pl = DaPlan()
     _check(lib().decode_attn_forward_static(ctypes.byref(prob), policy,
                                             _dev_ptr(q, "q", torch.bfloat16),
                                             _dev_ptr(k, "k", _KV),
@@ -283,8 +287,10 @@ def forward_static(prob: DaProblem, policy, q, k, v, table, lengths, out, lse, s
                                             _dev_ptr(table, "table", torch.int32),
                                             _dev_ptr(lengths, "lengths", torch.int32),
                                             _dev_ptr(out, "out", torch.bfloat16),
-                                            _dev_ptr(lse, "lse", torch.float32), _stream(stream)),
+                                            _dev_ptr(lse, "lse", torch.float32), _stream(stream),
+                                            ctypes.byref(pl)),
            "forward_static")
+    return pl
 
 
 def plan_extra(prob: DaProblem, policy: int, lengths, extra_lengths, ws, stream=None) -> DaPlan:

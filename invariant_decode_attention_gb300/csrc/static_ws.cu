@@ -23,7 +23,9 @@ void* g_addr[64];
 
 // Device address of g_static_workspace on the current device, looked up once
 // per device.  In host code the array's name is only a host-side stand-in,
-// so the address must come from the runtime.
+// so the address must come from the runtime.  The cached address belongs to
+// the device's current context: after cudaDeviceReset it is stale, and this
+// entry point must not be called again in that process.
 int static_workspace_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DA_ERR_CUDA;
@@ -42,7 +44,7 @@ int static_workspace_address(void** out) {
 extern "C" int decode_attn_forward_static(const da_problem* prob, int32_t policy, const void* q,
                                           const void* k, const void* v, const int32_t* table,
                                           const int32_t* lengths, void* out, float* lse,
-                                          void* stream) {
+                                          void* stream, da_plan* plan_out) {
   size_t need = 0;
   int rc = decode_attn_workspace_bytes(prob, &need);
   if (rc != DA_OK) return rc;
@@ -50,6 +52,15 @@ extern "C" int decode_attn_forward_static(const da_problem* prob, int32_t policy
   void* ws = nullptr;
   rc = static_workspace_address(&ws);
   if (rc != DA_OK) return rc;
-  return decode_attn_forward(prob, policy, q, k, v, table, lengths, ws,
-                             (size_t)DA_STATIC_WORKSPACE_BYTES, out, lse, stream);
+  da_plan plan;
+  rc = decode_attn_plan(prob, policy, lengths, ws, (size_t)DA_STATIC_WORKSPACE_BYTES, &plan,
+                        stream);
+  if (rc != DA_OK) return rc;
+  rc = decode_attn_run(&plan, q, k, v, table, lengths, out, lse, stream);
+  if (rc != DA_OK) return rc;
+  rc = decode_attn_combine(&plan, out, lse, stream);
+  // The plan names the array's device address, so decode_attn_read_error can
+  // read this call's error word from it (until the next call overwrites it).
+  if (rc == DA_OK && plan_out) *plan_out = plan;
+  return rc;
 }

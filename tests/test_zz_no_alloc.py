@@ -5,24 +5,23 @@ synchronisation).  Its scratch is one fixed device array inside the library.
 
 The test calls the entry point through the C ABI twice in a row -- two
 different problems, so the second call runs on scratch the first one left
-behind -- and checks each result against the regular entry point
-(decode_attn_forward with a caller-owned workspace) within the tolerance the
-parity tests use.  It also checks that an oversized problem is refused.
-This file is named to be collected last.
+behind -- and checks each result bit for bit against the regular entry point
+(decode_attn_forward with a caller-owned workspace): both run the same plan
+and the same kernels, so their bits must agree.  A third call repeats the
+first problem while the device's free memory and torch's allocator counters
+are watched: nothing may be allocated.  It also reads a call's device error
+word through the returned plan, and checks that an oversized problem is
+refused.  This file is named to be collected last.
 """
 
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
 from invariant_decode_attention_gb300 import workloads as W
-from oracle import bf16 as OB
 
 pytestmark = pytest.mark.gpu
-
-OUT_ATOL, LSE_ATOL = 1e-2, 1e-4
 
 
 @pytest.fixture(scope="module")
@@ -32,27 +31,60 @@ def api():
     return _api
 
 
-def _close(out, lse, ref_out, ref_lse):
-    o, ro = out.double().cpu().numpy(), ref_out.double().cpu().numpy()
-    assert np.all(np.abs(o - ro) <= np.maximum(OUT_ATOL, OB.ulp(ro)))
-    l, rl = lse.double().cpu().numpy(), ref_lse.double().cpu().numpy()
-    same_inf = np.isneginf(l) & np.isneginf(rl)
-    assert np.all(same_inf | (np.abs(l - rl) <= LSE_ATOL))
+def _cases():
+    return [W.gqa_paged(), W.make(W.PAGED, [0, 9000, 77, 131072], H_q=16, H_kv=4, D_qk=128,
+                                  page_size=64, seed=5)]
+
+
+def _static(api, g, prob):
+    out = torch.full((g.B, g.H_q, g.D_v), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((g.B, g.H_q), float("nan"), dtype=torch.float32, device="cuda")
+    return out, lse
 
 
 def test_static_entry_matches_regular_entry_on_two_calls(api):
-    cases = [W.gqa_paged(), W.make(W.PAGED, [0, 9000, 77, 131072], H_q=16, H_kv=4,
-                                   D_qk=128, page_size=64, seed=5)]
-    for wl in cases:
+    for wl in _cases():
         g = wl.to("cuda")
         prob = api.problem_for(g)
         assert api.workspace_bytes(prob) <= api.STATIC_WORKSPACE_BYTES
         ref_out, ref_lse = api.run_workload(g)  # decode_attn_forward, caller's workspace
-        out = torch.full_like(ref_out, float("nan"))
-        lse = torch.full_like(ref_lse, float("nan"))
-        api.forward_static(prob, api.INVARIANT, g.q, g.k, g.v, g.table, g.lengths, out, lse)
+        out, lse = _static(api, g, prob)
+        pl = api.forward_static(prob, api.INVARIANT, g.q, g.k, g.v, g.table, g.lengths, out, lse)
         torch.cuda.synchronize()
-        _close(out, lse, ref_out, ref_lse)
+        assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
+        assert api.read_error(pl) == 0
+
+
+def test_static_entry_allocates_nothing(api):
+    g = _cases()[0].to("cuda")
+    prob = api.problem_for(g)
+    ref_out, ref_lse = api.run_workload(g)
+    out, lse = _static(api, g, prob)
+    # first call: the library's code and its array are loaded on the device
+    api.forward_static(prob, api.INVARIANT, g.q, g.k, g.v, g.table, g.lengths, out, lse)
+    out2, lse2 = _static(api, g, prob)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    alloc0, res0 = torch.cuda.memory_allocated(), torch.cuda.memory_reserved()
+    api.forward_static(prob, api.INVARIANT, g.q, g.k, g.v, g.table, g.lengths, out2, lse2)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+    assert torch.cuda.memory_allocated() == alloc0 and torch.cuda.memory_reserved() == res0
+    assert torch.equal(out2, ref_out) and torch.equal(lse2, ref_lse)
+
+
+def test_static_entry_reports_device_errors(api):
+    wl = W.make(W.PAGED, [100, 3000], H_q=32, H_kv=8, D_qk=128, page_size=16, seed=9)
+    g = wl.to("cuda")
+    prob = api.problem_for(g)
+    bad = torch.tensor([100, 10 ** 7], dtype=torch.int32, device="cuda")  # above capacity
+    out, lse = _static(api, g, prob)
+    pl = api.forward_static(prob, api.INVARIANT, g.q, g.k, g.v, g.table, bad, out, lse)
+    assert api.read_error(pl) & api.DEVERR_LENGTH
+    # a clean call afterwards clears the word again
+    pl = api.forward_static(prob, api.INVARIANT, g.q, g.k, g.v, g.table, g.lengths, out, lse)
+    assert api.read_error(pl) == 0
 
 
 def test_static_entry_refuses_a_problem_beyond_its_array(api):
@@ -64,5 +96,6 @@ def test_static_entry_refuses_a_problem_beyond_its_array(api):
     dummy = torch.zeros(16, dtype=torch.int32, device="cuda")
     p = ctypes.c_void_p(dummy.data_ptr())
     rc = L.decode_attn_forward_static(ctypes.byref(prob), api.INVARIANT, p, p, p, p, p, p, p,
-                                      ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+                                      ctypes.c_void_p(torch.cuda.current_stream().cuda_stream),
+                                      None)
     assert rc == api.ERR_WORKSPACE
