@@ -242,6 +242,11 @@ def ragged_page_table(lengths, seed, page_size=16, width=None):
     return page_table(lengths, page_size, g, width)
 
 
+def _e4m3_bytes(t, scale):
+    """E4M3 bytes of value / scale (torch's float8_e4m3fn conversion)."""
+    return (t.float() / scale).to(torch.float8_e4m3fn).view(torch.uint8)
+
+
 class RaggedSweep:
     """Batches of the ragged invariance sweep, assembled on a device.
 
@@ -250,12 +255,25 @@ class RaggedSweep:
     the target row's q, K and V are written into its own freshly shuffled
     pages, so the target attends over identical data at a different position,
     with different page ids and different batchmates every time.
+
+    kv_fp8: the caches hold E4M3 bytes (scales 1/64), the target's bytes
+    converted once from its bf16 values.  extra: every row's list continues
+    in a second, index-gathered cache [extra_slots, 8, 128]; the target's
+    RAGGED_TARGET_EXTRA extra entries are written to fresh distinct slots per
+    batch, batchmates take uniform extra lengths in [0, extra_width] of
+    random (possibly repeated) slots.
     """
 
-    def __init__(self, sizes, device="cuda", seed=1003, page_size=16):
+    def __init__(self, sizes, device="cuda", seed=1003, page_size=16, kv_fp8=False,
+                 extra=False, extra_slots=32768, extra_width=1024):
         self.sizes = list(sizes)
         self.page_size = page_size
         self.device = device
+        self.seed = seed
+        self.kv_fp8 = kv_fp8
+        self.extra = extra
+        self.extra_slots = extra_slots
+        self.extra_width = extra_width
         self.q_t, self.k_t, self.v_t = ragged_target(seed)
         self.batches = []
         max_pages = 1
@@ -272,19 +290,67 @@ class RaggedSweep:
         self.k_pool = torch.randn(shape, generator=g, device=device, dtype=torch.bfloat16)
         self.v_pool = torch.randn(shape, generator=g, device=device, dtype=torch.bfloat16)
         n_tp = RAGGED_TARGET_LEN // page_size
-        self._kt = self.k_t.view(n_tp, page_size, 8, 128).to(device)
-        self._vt = self.v_t.view(n_tp, page_size, 8, 128).to(device)
+        kt = self.k_t.view(n_tp, page_size, 8, 128)
+        vt = self.v_t.view(n_tp, page_size, 8, 128)
+        if kv_fp8:
+            self.k_scale = self.v_scale = 1.0 / 64
+            self.k_pool = _e4m3_bytes(self.k_pool, self.k_scale)
+            self.v_pool = _e4m3_bytes(self.v_pool, self.v_scale)
+            kt, vt = _e4m3_bytes(kt, self.k_scale), _e4m3_bytes(vt, self.v_scale)
+        self.kt_cpu, self.vt_cpu = kt, vt  # the target's cache rows as stored
+        self._kt = kt.to(device)
+        self._vt = vt.to(device)
         self._qt = self.q_t.to(device)
+        if extra:
+            gx = torch.Generator().manual_seed(seed + 17)
+            self.xk_t = _randn((RAGGED_TARGET_EXTRA, 8, 128), gx)
+            self.xv_t = _randn((RAGGED_TARGET_EXTRA, 8, 128), gx)
+            xshape = (extra_slots, 8, 128)
+            self.xk_pool = torch.randn(xshape, generator=g, device=device, dtype=torch.bfloat16)
+            self.xv_pool = torch.randn(xshape, generator=g, device=device, dtype=torch.bfloat16)
+            self._xkt, self._xvt = self.xk_t.to(device), self.xv_t.to(device)
+
+    def _wl(self, name, q, k, v, lengths, table, **extra):
+        kw = {}
+        if self.kv_fp8:
+            kw = dict(kv_fp8=True, k_scale=self.k_scale, v_scale=self.v_scale)
+        return Workload(name, PAGED, q, k, v, lengths, table, self.page_size, 32, 8, 128, 128,
+                        128 ** -0.5, **extra, **kw)
 
     def solo(self):
-        """The target row alone, in its own 256 pages."""
+        """The target row alone, in its own 256 pages (and, with a second
+        source, its extra entries in slots 0 .. RAGGED_TARGET_EXTRA-1 of a
+        cache of their own)."""
         n_tp = RAGGED_TARGET_LEN // self.page_size
         table = torch.full((1, RAGGED_MAX_LEN // self.page_size), -1, dtype=torch.int32)
         table[0, :n_tp] = torch.arange(n_tp, dtype=torch.int32)
-        return Workload("ragged_solo", PAGED, self._qt[None].contiguous(), self._kt.contiguous(),
-                        self._vt.contiguous(), torch.tensor([RAGGED_TARGET_LEN], dtype=torch.int32,
-                                                            device=self.device),
-                        table.to(self.device), self.page_size, 32, 8, 128, 128, 128 ** -0.5)
+        extra = {}
+        if self.extra:
+            xt = torch.full((1, self.extra_width), -1, dtype=torch.int32)
+            xt[0, :RAGGED_TARGET_EXTRA] = torch.arange(RAGGED_TARGET_EXTRA, dtype=torch.int32)
+            extra = dict(extra_k=self._xkt.contiguous(), extra_v=self._xvt.contiguous(),
+                         extra_table=xt.to(self.device),
+                         extra_lengths=torch.tensor([RAGGED_TARGET_EXTRA], dtype=torch.int32,
+                                                    device=self.device))
+        return self._wl("ragged_solo", self._qt[None].contiguous(), self._kt.contiguous(),
+                        self._vt.contiguous(),
+                        torch.tensor([RAGGED_TARGET_LEN], dtype=torch.int32, device=self.device),
+                        table.to(self.device), **extra)
+
+    def solo_cpu(self):
+        """The solo row as a CPU workload with a contiguous cache (for the
+        oracle)."""
+        extra = {}
+        if self.extra:
+            xt = torch.arange(RAGGED_TARGET_EXTRA, dtype=torch.int32)[None]
+            extra = dict(extra_k=self.xk_t, extra_v=self.xv_t, extra_table=xt,
+                         extra_lengths=torch.tensor([RAGGED_TARGET_EXTRA], dtype=torch.int32))
+        kw = dict(kv_fp8=True, k_scale=self.k_scale, v_scale=self.v_scale) if self.kv_fp8 else {}
+        k = self.kt_cpu.reshape(RAGGED_TARGET_LEN, 8, 128)[None]
+        v = self.vt_cpu.reshape(RAGGED_TARGET_LEN, 8, 128)[None]
+        return Workload("ragged_solo_cpu", CONTIGUOUS, self.q_t[None], k, v,
+                        torch.tensor([RAGGED_TARGET_LEN], dtype=torch.int32), None, 0, 32, 8,
+                        128, 128, 128 ** -0.5, **extra, **kw)
 
     def batch(self, i):
         """(Workload on the device, target position) of the i-th batch."""
@@ -296,9 +362,114 @@ class RaggedSweep:
         g = torch.Generator(device=self.device).manual_seed(7 * B + 1)
         q = torch.randn((B, 32, 128), generator=g, device=self.device, dtype=torch.bfloat16)
         q[pos] = self._qt
-        wl = Workload(f"ragged_b{B}", PAGED, q, self.k_pool, self.v_pool,
+        extra = {}
+        if self.extra:
+            gx = torch.Generator().manual_seed(self.seed * 1000 + B + 5)
+            el = torch.randint(0, self.extra_width + 1, (B,), generator=gx, dtype=torch.int32)
+            el[pos] = RAGGED_TARGET_EXTRA
+            xt = torch.randint(0, self.extra_slots, (B, self.extra_width), generator=gx,
+                               dtype=torch.int32)
+            xt[torch.arange(self.extra_width)[None, :] >= el[:, None]] = -1
+            slots = torch.randperm(self.extra_slots, generator=gx)[:RAGGED_TARGET_EXTRA]
+            xt[pos] = -1
+            xt[pos, :RAGGED_TARGET_EXTRA] = slots.to(torch.int32)
+            sd = slots.to(self.device)
+            self.xk_pool[sd] = self._xkt
+            self.xv_pool[sd] = self._xvt
+            extra = dict(extra_k=self.xk_pool, extra_v=self.xv_pool,
+                         extra_table=xt.to(self.device), extra_lengths=el.to(self.device))
+        wl = self._wl(f"ragged_b{B}", q, self.k_pool, self.v_pool,
                       torch.tensor(lens, dtype=torch.int32, device=self.device),
-                      table.to(self.device), self.page_size, 32, 8, 128, 128, 128 ** -0.5)
+                      table.to(self.device), **extra)
+        return wl, pos
+
+
+# Ragged sweep of the shared-latent (MLA-style) variant: one target row
+# (128 heads, top-k 1536 entries of a 65536-slot latent cache, 576 dims of
+# which the first 512 are V) in batches whose other rows take top-k lengths
+# log-uniform in [1, 2048]; optionally a second latent source (target: 300
+# entries of a 16384-slot cache, batchmates uniform in [0, 512]).
+RAGGED_TARGET_EXTRA = 700
+LATENT_TARGET_LEN = 1536
+LATENT_TARGET_EXTRA = 300
+
+
+class RaggedSweepLatent:
+    """Batches of the shared-latent ragged sweep, assembled on a device.
+
+    The caches are pools of random filler drawn on the device; for every
+    batch the target row's latent entries are written into fresh distinct
+    slots (in the same order), so the target attends over identical data at
+    a new position, through new slot ids, among new batchmates whose index
+    lists are random (possibly repeated) slots."""
+
+    def __init__(self, sizes, device="cuda", seed=1008, extra=False, num_slots=65536,
+                 width=2048, extra_slots=16384, extra_width=512):
+        self.sizes = list(sizes)
+        self.device = device
+        self.seed = seed
+        self.extra = extra
+        self.num_slots, self.width = num_slots, width
+        self.extra_slots, self.extra_width = extra_slots, extra_width
+        g = torch.Generator().manual_seed(seed)
+        self.q_t = _randn((128, 576), g)
+        self.k_t = _randn((LATENT_TARGET_LEN, 1, 576), g)
+        self.xk_t = _randn((LATENT_TARGET_EXTRA, 1, 576), g) if extra else None
+        gd = torch.Generator(device=device).manual_seed(seed)
+        self.pool = torch.randn((num_slots, 1, 576), generator=gd, device=device,
+                                dtype=torch.bfloat16)
+        self.xpool = (torch.randn((extra_slots, 1, 576), generator=gd, device=device,
+                                  dtype=torch.bfloat16) if extra else None)
+        self._qt, self._kt = self.q_t.to(device), self.k_t.to(device)
+        self._xkt = self.xk_t.to(device) if extra else None
+
+    def solo_cpu(self):
+        """The target row alone with caches of its own (CPU tensors)."""
+        table = torch.arange(LATENT_TARGET_LEN, dtype=torch.int32)[None]
+        extra = {}
+        if self.extra:
+            extra = dict(extra_k=self.xk_t, extra_v=None,
+                         extra_table=torch.arange(LATENT_TARGET_EXTRA, dtype=torch.int32)[None],
+                         extra_lengths=torch.tensor([LATENT_TARGET_EXTRA], dtype=torch.int32))
+        return Workload("latent_solo", INDEXED, self.q_t[None], self.k_t, None,
+                        torch.tensor([LATENT_TARGET_LEN], dtype=torch.int32), table, 0, 128, 1,
+                        576, 512, 576 ** -0.5, **extra)
+
+    def solo(self):
+        return self.solo_cpu().to(self.device)
+
+    def batch(self, i):
+        """(Workload on the device, target position) of the i-th batch."""
+        B = self.sizes[i]
+        g = torch.Generator().manual_seed(self.seed * 1000 + B)
+        u = torch.rand(B, generator=g, dtype=torch.float64)
+        lens = torch.clamp(torch.floor(torch.exp2(11.0 * u)), 1, self.width).to(torch.int32)
+        pos = int(torch.randint(0, B, (1,), generator=g))
+        lens[pos] = LATENT_TARGET_LEN
+        table = torch.randint(0, self.num_slots, (B, self.width), generator=g, dtype=torch.int32)
+        table[torch.arange(self.width)[None, :] >= lens[:, None]] = -1
+        slots = torch.randperm(self.num_slots, generator=g)[:LATENT_TARGET_LEN]
+        table[pos] = -1
+        table[pos, :LATENT_TARGET_LEN] = slots.to(torch.int32)
+        self.pool[slots.to(self.device)] = self._kt
+        gq = torch.Generator(device=self.device).manual_seed(11 * B + 3)
+        q = torch.randn((B, 128, 576), generator=gq, device=self.device, dtype=torch.bfloat16)
+        q[pos] = self._qt
+        extra = {}
+        if self.extra:
+            el = torch.randint(0, self.extra_width + 1, (B,), generator=g, dtype=torch.int32)
+            el[pos] = LATENT_TARGET_EXTRA
+            xt = torch.randint(0, self.extra_slots, (B, self.extra_width), generator=g,
+                               dtype=torch.int32)
+            xt[torch.arange(self.extra_width)[None, :] >= el[:, None]] = -1
+            xs = torch.randperm(self.extra_slots, generator=g)[:LATENT_TARGET_EXTRA]
+            xt[pos] = -1
+            xt[pos, :LATENT_TARGET_EXTRA] = xs.to(torch.int32)
+            self.xpool[xs.to(self.device)] = self._xkt
+            extra = dict(extra_k=self.xpool, extra_v=None, extra_table=xt.to(self.device),
+                         extra_lengths=el.to(self.device))
+        wl = Workload(f"latent_ragged_b{B}", INDEXED, q, self.pool, None, lens.to(self.device),
+                      table.to(self.device), 0, 128, 1, 576, 512, 576 ** -0.5, **extra)
         return wl, pos
 
 
