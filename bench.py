@@ -4,7 +4,7 @@ One step = one pass of the whole hot path over one batch: split plan, split
 kernel, combine (three launches through the C ABI), inputs resident in HBM.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload gqa_paged|long_context|tiny|ragged]
+                    [--workload long_context|gqa_paged|mla_sparse|tiny|...]
 
 Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
 of the workload (rows are independent; no collective on the data path) and
@@ -381,9 +381,10 @@ def invariance_sweep(api, sizes=(1, 2, 4, 8, 16, 32, 64, 128), steps=10):
     return res
 
 
-def cpu_oracle_rate(wl, budget_s=15.0, max_rows=None):
+def cpu_oracle_rate(wl, budget_s=15.0, max_rows=None, group=None, first_row=0):
     """Time the fp64 oracle, as it stands, on whole rows of the workload until
-    the budget is spent.  Returns (GB/s, rows/s, rows done, seconds)."""
+    the budget is spent (group=h: only the query heads of KV head h, a
+    bounded sample of each row).  Returns (GB/s, rows/s, rows done, seconds)."""
     from oracle import attention as A
     q = wl.q.double().numpy()
     table = None if wl.table is None else wl.table.numpy()
@@ -399,12 +400,17 @@ def cpu_oracle_rate(wl, budget_s=15.0, max_rows=None):
             return self.t[idx].double().numpy()
 
     K, V = View(wl.k), (None if wl.v is None else View(wl.v))
-    per_entry = wl.H_kv * (wl.D_qk + (0 if wl.v is None else wl.D_v)) * 2
+    n_kv = 1 if group is not None else wl.H_kv
+    per_entry = n_kv * (wl.D_qk + (0 if wl.v is None else wl.D_v)) * 2
+    G = wl.H_q // wl.H_kv
+    heads = None if group is None else list(range(group * G, (group + 1) * G))
     done, nbytes = 0, 0
     t0 = time.perf_counter()
-    for b in range(wl.B if max_rows is None else min(wl.B, max_rows)):
+    n_rows = wl.B if max_rows is None else min(wl.B, max_rows)
+    for i in range(n_rows):
+        b = (first_row + i) % wl.B
         A.attend(q, K, V, wl.lengths.numpy(), scale=wl.scale, layout=wl.layout, table=table,
-                 page_size=wl.page_size, d_v=wl.D_v, rows=[b])
+                 page_size=wl.page_size, d_v=wl.D_v, rows=[b], heads=heads)
         done += 1
         nbytes += int(wl.lengths[b]) * per_entry
         if time.perf_counter() - t0 > budget_s:
@@ -415,13 +421,100 @@ def cpu_oracle_rate(wl, budget_s=15.0, max_rows=None):
 
 # ----------------------------------------------------------------- main
 
+def cpu_model():
+    """The host CPU's model name (x86: /proc/cpuinfo; Arm: lscpu), or the machine."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        import subprocess
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine()
+
+
+def alg_bytes_of(wl):
+    """Algorithmic bytes of one split-kernel launch: the rows' KV payload,
+    q, and the final out (bf16) and lse (fp32)."""
+    return wl.kv_bytes() + wl.q.numel() * 2 + wl.B * wl.H_q * (wl.D_v * 2 + 4)
+
+
+def measure(case, peak, peak_kind, steps, warmup, world=1, dev="cpu", clocks=None):
+    """Step time (INVARIANT, then BALANCED on the same inputs) and the split
+    kernel's own time and roofline for one resident workload."""
+    api, wl = case.api, case.wl
+    kv_bytes = wl.kv_bytes()
+    flush = kv_bytes < L2_FLUSH_BELOW  # inputs that fit in L2 are flushed out of it
+    case.policy = api.INVARIANT
+    if clocks is not None:
+        with clocks:
+            total_ms, _, _ = time_steps(case, steps, warmup, split_events=False, flush=flush)
+    else:
+        total_ms, _, _ = time_steps(case, steps, warmup, split_events=False, flush=flush)
+    total_ms = max_over_ranks(total_ms, dev)
+    ms = total_ms / steps
+    # the split kernel alone: events on the launching stream around it
+    _, _, split_ms = time_steps(case, max(20, steps // 2), 3, flush=flush)
+    split_avg = max_over_ranks(sum(split_ms) / len(split_ms), dev)
+    alg = alg_bytes_of(wl)
+    kernel = "split_mla" if wl.v is None else "split_fma"
+    n_bal = max(20, steps // 4)
+    case.policy = api.BALANCED
+    bal_ms, _, _ = time_steps(case, n_bal, warmup, split_events=False, flush=flush)
+    bal_ms = max_over_ranks(bal_ms, dev) / n_bal
+    case.policy = api.INVARIANT
+    rec = {
+        "ms_per_step": round(ms, 5),
+        "kv_gbs": round(replica_value(kv_bytes, world, ms) / 1e9, 2),
+        "rows_per_s": round(world * wl.B / (ms * 1e-3), 1),
+        "hbm_frac_step_of_" + peak_kind: round(kv_bytes / (ms * 1e-3) / 1e9 / peak, 4),
+        "l2": (f"L2 flushed between steps ({kv_bytes / 1e6:.0f} MB of KV per step)" if flush
+               else f"inputs larger than L2 ({kv_bytes / 1e6:.0f} MB of KV per step)"),
+        "balanced": {"ms_per_step": round(bal_ms, 5),
+                     "kv_gbs": round(kv_bytes / (bal_ms * 1e-3) / 1e9, 2),
+                     "invariant_over_balanced_time": round(ms / bal_ms, 4)},
+        "roofline": {
+            "kernel": kernel, "bound": "hbm",
+            "achieved": round(alg / (split_avg * 1e-3) / 1e9, 1),
+            "peak": peak, "unit": "GB/s",
+            "frac": round(alg / (split_avg * 1e-3) / 1e9 / peak, 4),
+            "peak_kind": peak_kind,
+            "traffic": recorded_traffic(kernel, wl.name),
+            "alg_bytes_per_launch": alg,
+            "split_ms_avg": round(split_avg, 5),
+        },
+    }
+    if kernel == "split_mla":
+        n_ent = int(wl.lengths.to(torch.int64).sum())
+        if wl.extra_lengths is not None:
+            n_ent += int(wl.extra_lengths.to(torch.int64).sum())
+        flops = n_ent * wl.H_q * (wl.D_qk + wl.D_v) * 2
+        tp = tensor_peak()
+        rec["roofline_tensor"] = {
+            "bound": "tensor", "achieved": round(flops / (split_avg * 1e-3) / 1e12, 1),
+            "peak": tp, "unit": "TFLOP/s",
+            "frac": round(flops / (split_avg * 1e-3) / 1e12 / tp, 4),
+            "flops_per_launch": flops,
+        }
+    return rec
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="gqa_paged",
+    ap.add_argument("--workload", default="long_context",
                     choices=["gqa_paged", "long_context", "tiny", "mla_sparse", "gqa_paged_fp8",
                              "long_context_fp8"])
     ap.add_argument("--no-extra", action="store_true",
@@ -454,39 +547,22 @@ def main():
     wl = build_workload(args.workload, rank)
     case = GpuCase(wl, dev, api.INVARIANT)
     kv_bytes = wl.kv_bytes()
-    io_bytes = wl.q.numel() * 2 + wl.B * wl.H_q * (wl.D_v * 2 + 4)
-    alg_bytes = kv_bytes + io_bytes
 
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
-    # inputs smaller than twice L2 are flushed out of it between steps
-    flush = kv_bytes < L2_FLUSH_BELOW
-    # the step as a user runs it: no events between its kernels
-    with ClockSampler(local) as clocks:
-        total_ms, per_step, _ = time_steps(case, args.steps, args.warmup, split_events=False,
-                                           flush=flush)
-    total_ms = max_over_ranks(total_ms, dev)
-    ms_per_step = total_ms / args.steps
+    # the step as a user runs it (no events between its kernels), NVML
+    # sampling the clocks while it runs
+    clocks = ClockSampler(local)
+    rec = measure(case, peak, peak_kind, args.steps, args.warmup, world, dev, clocks)
+    ms_per_step = rec["ms_per_step"]
     value = replica_value(kv_bytes, world, ms_per_step) / 1e9
-    # the split kernel alone: events on the launching stream around it
-    _, _, split_ms = time_steps(case, max(20, args.steps // 2), 3, flush=flush)
-    split_avg = sum(split_ms) / len(split_ms)
-    achieved = alg_bytes / (split_avg * 1e-3) / 1e9
+    e2e_ms, h2d, d2h = e2e_steps(case, max(20, args.steps // 4), args.warmup)
+    e2e_ms = max_over_ranks(e2e_ms, dev)
 
     if rank != 0:
         return
-
-    # INVARIANT vs BALANCED on the same inputs
-    kernel = "split_mla" if wl.v is None else "split_fma"
-    n_bal = max(20, args.steps // 4)
-    case.policy = api.BALANCED
-    bal_ms, _, _ = time_steps(case, n_bal, args.warmup, split_events=False, flush=flush)
-    bal_ms /= n_bal
-    case.policy = api.INVARIANT
-
-    e2e_ms, h2d, d2h = e2e_steps(case, max(20, args.steps // 4), args.warmup)
 
     line = {
         "metric": METRIC,
@@ -505,72 +581,41 @@ def main():
         "config": {
             "workload": wl.name, "rows": wl.B, "H_q": wl.H_q, "H_kv": wl.H_kv,
             "head_dim": wl.D_qk, "layout": wl.layout, "page_size": wl.page_size,
-            "kv_bytes_per_step": kv_bytes, "policy": "invariant",
-            "l2": (f"L2 flushed between steps ({kv_bytes / 1e6:.0f} MB of KV per step)" if flush
-                   else f"inputs larger than L2 ({kv_bytes / 1e6:.0f} MB of KV per step)"),
+            "kv_bytes_per_step": kv_bytes, "policy": "invariant", "l2": rec["l2"],
             "parallelism": f"replicas x{world}",
         },
-        "rows_per_s": round(world * wl.B / (ms_per_step * 1e-3), 1),
+        "rows_per_s": rec["rows_per_s"],
         "hbm_frac_of_" + peak_kind: round(value / world / peak, 4),
-        "balanced": {"ms_per_step": round(bal_ms, 5),
-                     "value": round(kv_bytes / (bal_ms * 1e-3) / 1e9, 2),
-                     "invariant_over_balanced_time": round(ms_per_step / bal_ms, 4)},
-        "roofline": {
-            "kernel": kernel, "bound": "hbm", "achieved": round(achieved, 1),
-            "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-            "peak_kind": peak_kind,
-            "traffic": recorded_traffic(kernel, wl.name),
-            "alg_bytes_per_launch": alg_bytes,
-            "split_ms_avg": round(split_avg, 5),
-        },
-        "e2e": {"value": round(kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "balanced": rec["balanced"],
+        "roofline": rec["roofline"],
+        "e2e": {"value": round(replica_value(kv_bytes, world, e2e_ms) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "resident": "KV cache"},
+                "d2h_bytes_per_step": d2h, "resident": "KV cache",
+                "api": "decode_attn_forward"},
         "gpu_launches": 3 * args.steps,
         "clocks": clocks.summary(),
     }
+    if "roofline_tensor" in rec:
+        line["roofline_tensor"] = rec["roofline_tensor"]
     if not args.no_extra:
         extra = {}
-        for name in ("long_context", "mla_sparse", "tiny", "gqa_paged_fp8", "long_context_fp8"):
+        for name in ("gqa_paged", "mla_sparse", "tiny", "gqa_paged_fp8", "long_context_fp8",
+                     "long_context"):
             if name == args.workload:
                 continue
             w2 = build_workload(name)
             c2 = GpuCase(w2, dev, api.INVARIANT)
-            n = 20 if name.startswith("long_context") else 200
-            # inputs that fit in L2 (the MLA cache is 75.5 MB) are flushed between steps
-            fl = w2.kv_bytes() < L2_FLUSH_BELOW
-            ms2, _, _ = time_steps(c2, n, 5, split_events=False, flush=fl)
-            ms2 /= n
-            _, _, sp2 = time_steps(c2, n, 3, flush=fl)
-            kvb = w2.kv_bytes()
-            c2.policy = api.BALANCED
-            bms, _, _ = time_steps(c2, n, 5, split_events=False, flush=fl)
-            bms /= n
-            sp = sum(sp2) / len(sp2)
-            rec = {
-                "ms_per_step": round(ms2, 5), "kv_gbs": round(kvb / (ms2 * 1e-3) / 1e9, 1),
-                "rows_per_s": round(w2.B / (ms2 * 1e-3), 1),
-                "hbm_frac": round(kvb / (ms2 * 1e-3) / 1e9 / peak, 4),
-                "split_ms_avg": round(sp, 5),
-                "hbm_frac_split": round(kvb / (sp * 1e-3) / 1e9 / peak, 4),
-                "balanced_ms_per_step": round(bms, 5),
-                "l2": "flushed between steps" if fl else "inputs larger than L2",
-            }
-            if name == "mla_sparse":
-                n_ent = int(w2.lengths.to(torch.int64).sum())
-                flops = n_ent * w2.H_q * (w2.D_qk + w2.D_v) * 2
-                rec["tensor_tflops_split"] = round(flops / (sp * 1e-3) / 1e12, 1)
-                rec["tensor_frac_split_of_measured_bf16"] = round(
-                    flops / (sp * 1e-3) / 1e12 / tensor_peak(), 4)
-            extra[w2.name] = rec
+            n = 40 if name.startswith("long_context") else 200
+            extra[w2.name] = measure(c2, peak, peak_kind, n, 5)
             del c2, w2
             torch.cuda.empty_cache()
         line["other_workloads"] = extra
         line["invariance_sweep"] = invariance_sweep(api)
         line["nvfp4_mm"] = nvfp4_section(api, peak)
-        gbs, rps, done, dt = cpu_oracle_rate(wl)
+        gbs, rps, done, dt = cpu_oracle_rate(wl, budget_s=20.0)
         line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": _CORES,
-                                "kind": "oracle", "rows_per_s": round(rps, 3),
+                                "cpu": cpu_model(), "kind": "oracle",
+                                "rows_per_s": round(rps, 3),
                                 "sample": f"{done} of {wl.B} rows of {wl.name}, all heads, "
                                           f"{dt:.1f} s, numpy fp64"}
     print(json.dumps(line), flush=True)
@@ -578,21 +623,23 @@ def main():
 
 def reference_arm(args, rank, world):
     """The oracle as it stands, on host cores, on the same workload: each step
-    is a bounded sample (whole rows) of the workload."""
+    is a bounded sample of it -- the query heads of one KV head of one row,
+    cycling over rows and KV heads."""
     if rank != 0:
         return
     wl = build_workload(args.workload)
-    budget = 60.0 / max(1, args.steps + args.warmup)
-    for _ in range(args.warmup):
-        cpu_oracle_rate(wl, budget_s=budget, max_rows=1)
-    rates, rows = [], 0
+    for i in range(args.warmup):
+        cpu_oracle_rate(wl, budget_s=0.0, max_rows=1, group=i % wl.H_kv, first_row=i)
+    rates = []
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        gbs, rps, done, dt = cpu_oracle_rate(wl, budget_s=budget, max_rows=1)
+    for i in range(args.steps):
+        gbs, _, _, _ = cpu_oracle_rate(wl, budget_s=0.0, max_rows=1, group=i % wl.H_kv,
+                                       first_row=i // wl.H_kv)
         rates.append(gbs)
-        rows += done
     elapsed = time.perf_counter() - t0
     value = statistics.median(rates)
+    sample = (f"per step: query heads of one KV head of one row of {wl.name} "
+              f"(1/{wl.H_kv} of a row), numpy fp64")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -600,8 +647,7 @@ def reference_arm(args, rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": wl.name, "rows": wl.B, "policy": "oracle (exact softmax)"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": _CORES,
-                         "kind": "oracle",
-                         "sample": f"one row of {wl.name} per step, numpy fp64"},
+                         "cpu": cpu_model(), "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
