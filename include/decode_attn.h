@@ -81,7 +81,7 @@ extern "C" {
 #define DA_KV_FP8_E4M3 1
 
 /* ---- kernel variants (chosen from the head config only, never B) ----- */
-#define DA_VARIANT_FMA 0 /* CUDA-core fp32 FMA, H_q/H_kv in {1,2,4,8}, D in {64,128} */
+#define DA_VARIANT_FMA 0 /* CUDA-core fp32 FMA, H_q/H_kv in 1..128, D in {64,128}    */
 #define DA_VARIANT_MLA 1 /* tcgen05 tensor cores, shared latent 576/512, 16..128 heads */
 
 /* ---- device-detected input errors (decode_attn_read_error bits) ----- */

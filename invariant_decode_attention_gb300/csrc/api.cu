@@ -241,9 +241,12 @@ static int plan_impl(const da_problem* prob, int32_t policy, const int32_t* d_le
   if (cudaGetDevice(&dev) != cudaSuccess) return DA_ERR_CUDA;
   const int sms = sm_count(dev);
   if (sms <= 0) return DA_ERR_CUDA;
-  // CTAs that one (row, split) item occupies: one per KV head (CUDA-core
-  // variant) or two, one per half of D_v (tensor-core variant).
-  const int per_item = (v.id == DA_VARIANT_MLA) ? 2 : prob->num_kv_heads;
+  // CTAs that one (row, split) item occupies: one per KV head and head chunk
+  // (CUDA-core variant) or two, one per half of D_v (tensor-core variant).
+  int gc = 1, chunks = 1;
+  if (v.id == DA_VARIANT_FMA)
+    fma_chunk_shape(prob->num_q_heads / prob->num_kv_heads, prob->head_dim_qk, &gc, &chunks);
+  const int per_item = (v.id == DA_VARIANT_MLA) ? 2 : prob->num_kv_heads * chunks;
   // persistent CTAs: as many as can be resident at once (whole pairs for the
   // tensor-core variant)
   const long long slots =

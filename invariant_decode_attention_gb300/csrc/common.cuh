@@ -18,6 +18,9 @@ constexpr int kFmaTile = 64;
 constexpr int kFmaMinTilesPerSplit = 16;
 constexpr int kFmaMaxSplits = 64;
 
+// CUDA-core variant: query heads per KV head it takes at most.
+constexpr int kFmaMaxGroup = 128;
+
 constexpr int kMlaTile = 64;
 constexpr int kMlaMinTilesPerSplit = 8;
 constexpr int kMlaMaxSplits = 32;
@@ -72,6 +75,8 @@ struct Launch {
   int kv_fp8;        // K and V are E4M3 bytes
   int o_part_mla;    // partials in the tensor-core variant's head-interleaved layout
   float v_scale;     // E4M3 cache: multiplies each unit's output
+  int fma_group;     // CUDA-core variant: query heads per KV head (G)
+  int fma_chunks;    // CUDA-core variant: units per KV head (head chunks)
 };
 
 struct PlanLaunch {
@@ -114,6 +119,7 @@ cudaError_t launch_split_mla(const Launch& p, int grid, cudaStream_t stream);
 int fma_ctas_per_sm(int G, int D);
 int mla_resident_ctas(int sms);  // persistent CTAs, an even number
 bool fma_supported(int G, int D);
+void fma_chunk_shape(int G, int D, int* gc, int* chunks);
 
 // Capacity of a row (largest valid length) for a layout.
 inline long long row_capacity(int layout, int width, int page_size) {

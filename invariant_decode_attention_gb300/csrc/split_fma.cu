@@ -1,11 +1,17 @@
-// Split kernel, CUDA-core variant (query groups of 1, 2, 4 or 8 heads per KV
-// head; head dim 64 or 128; G * D <= 512).
+// Split kernel, CUDA-core variant (any number of query heads per KV head;
+// head dim 64 or 128).
 //
-// One unit of work = (row b, split s, KV head h): the G query heads of group
-// h attend over the split's tiles of row b's KV list and produce either the
-// row's final output (single-split rows) or an fp32 partial (out, lse) that
-// the combine merges.  Work placement is persistent: CTA c takes units c,
-// c + grid, ...; which CTA runs a unit never changes what the unit computes.
+// One unit of work = (row b, split s, KV head h, head chunk c): up to Gc
+// query heads of group h (chunk c of the group; Gc = 1, 2, 4 or 8 with
+// Gc * D <= 512, fixed by the head config) attend over the split's tiles of
+// row b's KV list and produce either the row's final output (single-split
+// rows) or an fp32 partial (out, lse) that the combine merges.  A group of
+// G heads is cut into ceil(G / Gc) chunks; slots of the last chunk past the
+// group's end compute on a zero query and are never written.  The chunks of
+// one KV head are consecutive units, so they run at the same time on
+// neighbouring CTAs and their second reads of K and V come from L2.  Work
+// placement is persistent: which CTA runs a unit never changes what the unit
+// computes.
 //
 // Inside a CTA, four warps share each unit.  Warp w owns entries
 // [16w, 16w + 16) of every 64-entry tile and streams exactly those K and V
@@ -58,20 +64,35 @@ struct FmaShape {
   static_assert(kQChunks <= kThreads, "one q chunk per thread at most");
 };
 
-// A work unit as the kernel sees it: the plan's item descriptor plus a head.
+// The reference value the exponentials are taken against moves only when a
+// score exceeds it by more than 2^8 (log2 units): a warp then reduces the
+// tile maxima and rescales; otherwise p <= 2^8 is formed against the old
+// value with no cross-lane reduction.  The decision depends only on the
+// unit's own scores, so it is the same in every batch.
+constexpr float kRescaleLog2 = 8.f;
+
+// A work unit as the kernel sees it: the plan's item descriptor plus a KV
+// head and a chunk of its query heads.
 struct Unit {
   int slot, tb, te, L, b, h;
+  int hq0;     // first query head of the chunk
+  int live;    // query heads of the chunk inside the group (the rest are padding)
   int l_main;  // entries before the second source starts
   bool single;
 };
 
+// Units per (row, split) item: one per KV head and head chunk.
+__device__ __forceinline__ int units_per_item(const Launch& p) {
+  return p.H_kv * p.fma_chunks;
+}
+
 __device__ __forceinline__ int4 load_desc(const Launch& p, int u) {
-  return __ldg(reinterpret_cast<const int4*>(p.item_desc) + u / p.H_kv);
+  return __ldg(reinterpret_cast<const int4*>(p.item_desc) + u / units_per_item(p));
 }
 
 // X: the call has a second KV source (a separate instantiation, so that the
 // single-source loop carries none of its checks).
-template <bool X>
+template <int Gc, bool X>
 __device__ __forceinline__ Unit make_unit(const Launch& p, int u, int4 d) {
   Unit x;
   x.single = d.x < 0;
@@ -80,7 +101,10 @@ __device__ __forceinline__ Unit make_unit(const Launch& p, int u, int4 d) {
   x.te = d.z;
   x.L = d.w;
   x.b = x.slot / p.max_splits;
-  x.h = u % p.H_kv;
+  const int r = u % units_per_item(p), c = r % p.fma_chunks;
+  x.h = r / p.fma_chunks;
+  x.hq0 = x.h * p.fma_group + c * Gc;
+  x.live = min(Gc, p.fma_group - c * Gc);
   x.l_main = X ? clamp_len(__ldg(p.lengths + x.b), p.capacity) : 0x7fffffff;
   return x;
 }
@@ -144,7 +168,7 @@ struct Cursor {
   bool valid;
 };
 
-template <bool X>
+template <int Gc, bool X>
 __device__ __forceinline__ void cursor_seek(const Launch& p, Cursor& c, int ord, int4 d,
                                             const volatile int* ring, int n_units) {
   const int u = ring[ord % kRing];
@@ -155,17 +179,17 @@ __device__ __forceinline__ void cursor_seek(const Launch& p, Cursor& c, int ord,
   const int un = ring[(ord + 1) % kRing];
   c.next = (un < n_units) ? load_desc(p, un) : make_int4(0, 0, 0, 0);
   c.ord = ord;
-  c.x = make_unit<X>(p, u, d);
+  c.x = make_unit<Gc, X>(p, u, d);
   c.k = c.x.tb;
   c.valid = true;
 }
 
-template <bool X>
+template <int Gc, bool X>
 __device__ __forceinline__ void cursor_next(const Launch& p, Cursor& c, const volatile int* ring,
                                             int n_units) {
   if (!c.valid) return;
   if (++c.k < c.x.te) return;
-  cursor_seek<X>(p, c, c.ord + 1, c.next, ring, n_units);
+  cursor_seek<Gc, X>(p, c, c.ord + 1, c.next, ring, n_units);
 }
 
 // Issue this warp's copies for the cursor's tile into ring slot `slot`, then
@@ -223,11 +247,17 @@ __device__ __forceinline__ void load_slice(const Launch& p, const Cursor& c, uin
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(p.hdr, DA_DEVERR_INDEX);
     if (c.k == c.x.tb) {
-      // the unit's query group: one 16-byte chunk per thread of the CTA
+      // the unit's query heads: one 16-byte piece per thread of the CTA;
+      // padding slots past the group's end get zeros
       const int id = warp * 32 + lane;
       if (id < S::kQChunks) {
-        const __nv_bfloat16* q = p.q + ((size_t)c.x.b * p.H_q + (size_t)c.x.h * G) * D;
-        cp_async16(smem_addr(smem + S::kQOffset + slot * S::kQPad + id * 16), q + id * 8);
+        uint8_t* dst = smem + S::kQOffset + slot * S::kQPad + id * 16;
+        if (id / (D / 8) < c.x.live) {
+          const __nv_bfloat16* q = p.q + ((size_t)c.x.b * p.H_q + c.x.hq0) * D;
+          cp_async16(smem_addr(dst), q + id * 8);
+        } else {
+          *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+        }
       }
     }
   }
@@ -348,26 +378,43 @@ __device__ __forceinline__ void consume_slice(const uint8_t* ks, int lane, int n
     for (int i = 0; i < kV / 8; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i + kV / 8], 1);
     // v[0 .. G/2-1]: own entry (4 * tp + grp), head slots 0 .. G/2-1
     const bool own_valid = !kPartial || (4 * tp + grp) < n_valid;
-    float sc[G / 2], tmax[G];
+    float sc[G / 2];
+    bool jump = false;  // some score exceeds its running max by more than 2^8
 #pragma unroll
     for (int i = 0; i < G / 2; ++i) {
       sc[i] = own_valid ? v[i] * scale_log2 : -INFINITY;
-      float mx = sc[i];
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-      tmax[i] = mx;
+      jump |= sc[i] > m[i] + kRescaleLog2;
     }
-#pragma unroll
-    for (int i = 0; i < G / 2; ++i) tmax[i + G / 2] = __shfl_xor_sync(0xffffffffu, tmax[i], 1);
     float mnew[G];
+    if (__any_sync(0xffffffffu, jump)) {
+      // the slow path: the tile maxima of every head, then the standard
+      // online-softmax update (the reference value becomes the running max)
+      float tmax[G];
 #pragma unroll
-    for (int hs = 0; hs < G; ++hs) {
-      mnew[hs] = fmaxf(m[hs], tmax[hs]);
-      alpha[hs] = (mnew[hs] == -INFINITY) ? 1.f : ex2(m[hs] - mnew[hs]);
-      rescale |= (alpha[hs] != 1.f);
-      m[hs] = mnew[hs];
+      for (int i = 0; i < G / 2; ++i) {
+        float mx = sc[i];
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        tmax[i] = mx;
+      }
+#pragma unroll
+      for (int i = 0; i < G / 2; ++i) tmax[i + G / 2] = __shfl_xor_sync(0xffffffffu, tmax[i], 1);
+#pragma unroll
+      for (int hs = 0; hs < G; ++hs) {
+        mnew[hs] = fmaxf(m[hs], tmax[hs]);
+        alpha[hs] = (mnew[hs] == -INFINITY) ? 1.f : ex2(m[hs] - mnew[hs]);
+        rescale |= (alpha[hs] != 1.f);
+        m[hs] = mnew[hs];
+      }
+    } else {
+      // every score is at most 2^8 above its head's reference value: keep it
+#pragma unroll
+      for (int hs = 0; hs < G; ++hs) {
+        mnew[hs] = m[hs];
+        alpha[hs] = 1.f;
+      }
     }
     // ---- own probabilities, own share of l
     float pown[G / 2];
@@ -396,19 +443,26 @@ __device__ __forceinline__ void consume_slice(const uint8_t* ks, int lane, int n
 #pragma unroll
       for (int i = 0; i < kV; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
     }
-    float mx = -INFINITY;
+    bool jump = false;  // some score exceeds the running max by more than 2^8
 #pragma unroll
     for (int js = 0; js < S::kSteps; ++js) {
       const bool valid = !kPartial || (4 * js + grp) < n_valid;
       v[js] = valid ? v[js] * scale_log2 : -INFINITY;
-      mx = fmaxf(mx, v[js]);
+      jump |= v[js] > m[0] + kRescaleLog2;
     }
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-    const float mn = fmaxf(m[0], mx);
-    alpha[0] = (mn == -INFINITY) ? 1.f : ex2(m[0] - mn);
-    rescale = alpha[0] != 1.f;
-    m[0] = mn;
+    float mn = m[0];
+    alpha[0] = 1.f;
+    if (__any_sync(0xffffffffu, jump)) {
+      float mx = -INFINITY;
+#pragma unroll
+      for (int js = 0; js < S::kSteps; ++js) mx = fmaxf(mx, v[js]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      mn = fmaxf(m[0], mx);
+      alpha[0] = (mn == -INFINITY) ? 1.f : ex2(m[0] - mn);
+      rescale = alpha[0] != 1.f;
+      m[0] = mn;
+    }
     float sum = 0.f;
 #pragma unroll
     for (int js = 0; js < S::kSteps; ++js) {
@@ -452,14 +506,14 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
   allow_next_grid();
   __shared__ int ring[kRing];  // unit ids of this CTA's ordinals, kAhead ahead
   const int n_items = p.hdr[kHdrNWork], n_empty = p.hdr[kHdrNEmpty];
-  const int n_units = (n_items - n_empty) * p.H_kv;  // units with tiles, listed first
+  const int upi = units_per_item(p);
+  const int n_units = (n_items - n_empty) * upi;  // units with tiles, listed first
   // units of empty rows (listed last): out = 0, lse = -inf, dealt round-robin
-  for (int e = n_units + blockIdx.x; e < n_items * p.H_kv; e += gridDim.x) {
-    const int4 d = load_desc(p, e);
-    const int b = (~d.x) / p.max_splits, hq0 = (e % p.H_kv) * G;  // an empty row has one split
-    for (int i = threadIdx.x; i < G * D; i += S::kThreads)
-      p.out[((size_t)b * p.H_q + hq0) * D + i] = __float2bfloat16_rn(0.f);
-    if (threadIdx.x < G) p.lse[(size_t)b * p.H_q + hq0 + threadIdx.x] = -INFINITY;
+  for (int e = n_units + blockIdx.x; e < n_items * upi; e += gridDim.x) {
+    const Unit x = make_unit<G, false>(p, e, load_desc(p, e));  // an empty row has one split
+    for (int i = threadIdx.x; i < x.live * D; i += S::kThreads)
+      p.out[((size_t)x.b * p.H_q + x.hq0) * D + i] = __float2bfloat16_rn(0.f);
+    if (threadIdx.x < x.live) p.lse[(size_t)x.b * p.H_q + x.hq0 + threadIdx.x] = -INFINITY;
   }
   const int n_static = n_units / (int)gridDim.x * (int)gridDim.x;  // whole rounds
   if (threadIdx.x == 0)
@@ -469,13 +523,13 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
   // prologue: fill kStages - 1 slots
   Cursor pf;
   if (ring[0] < n_units)
-    cursor_seek<X>(p, pf, 0, load_desc(p, ring[0]), ring, n_units);
+    cursor_seek<G, X>(p, pf, 0, load_desc(p, ring[0]), ring, n_units);
   else
     pf.valid = false;
 #pragma unroll
   for (int s = 0; s < S::kStages - 1; ++s) {
     load_slice<G, D, X, F8>(p, pf, smem, s, warp, lane);
-    cursor_next<X>(p, pf, ring, n_units);
+    cursor_next<G, X>(p, pf, ring, n_units);
   }
 
   int slot = 0;
@@ -484,7 +538,7 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
   for (int ord = 0;; ++ord) {
     const int u = ring[ord % kRing];
     if (u >= n_units) break;
-    const Unit x = make_unit<X>(p, u, d_next);
+    const Unit x = make_unit<G, X>(p, u, d_next);
     const int un = ring[(ord + 1) % kRing];
     if (un < n_units) d_next = load_desc(p, un);
     float m[G], l[G];
@@ -511,7 +565,7 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
       }
       // refill the slot consumed in the previous iteration
       load_slice<G, D, X, F8>(p, pf, smem, (slot + S::kStages - 1) % S::kStages, warp, lane);
-      cursor_next<X>(p, pf, ring, n_units);
+      cursor_next<G, X>(p, pf, ring, n_units);
       const uint8_t* ks = smem + (slot * S::kWarps + warp) * S::kWarpSlotBytes;
       const int n_valid = min(S::kTokPerWarp, x.L - k * S::kTile - warp * S::kTokPerWarp);
       if (n_valid >= S::kTokPerWarp)
@@ -570,7 +624,7 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
       }
     }
     named_bar_sync(1, S::kThreads);
-    for (int h = warp; h < G; h += S::kWarps) {
+    for (int h = warp; h < x.live; h += S::kWarps) {
       float M = -INFINITY;
 #pragma unroll
       for (int w = 0; w < S::kWarps; ++w) M = fmaxf(M, scratch[(w * G + h) * S::kSRow + D]);
@@ -582,7 +636,7 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
         wgt[w] = (M == -INFINITY) ? 0.f : ex2(src[D] - M);
         lt = fmaf(src[D + 1], wgt[w], lt);
       }
-      const int hq = x.h * G + h;
+      const int hq = x.hq0 + h;
       const float lse2 = (lt > 0.f) ? M + lg2(lt) : -INFINITY;
 #pragma unroll
       for (int r = 0; r < D / 32; ++r) {
@@ -659,31 +713,48 @@ int ctas_one() {
 
 }  // namespace
 
-bool fma_supported(int G, int D) {
-  // G * D <= 512 keeps a lane's query and accumulator registers at <= 64 each.
-  return (G == 1 || G == 2 || G == 4 || G == 8) && (D == 64 || D == 128) && G * D <= 512;
+// Query heads per unit (Gc) and units per KV head for a group of G heads:
+// Gc = the power of two >= G, at most 8 for D = 64 and 4 for D = 128 (so that
+// a lane's query and accumulator registers stay at <= 64 each).
+void fma_chunk_shape(int G, int D, int* gc, int* chunks) {
+  const int gmax = (D == 64) ? 8 : 4;
+  int g = 1;
+  while (g < G && g < gmax) g <<= 1;
+  *gc = g;
+  *chunks = (G + g - 1) / g;
 }
 
-cudaError_t launch_split_fma(const Launch& p, int grid, cudaStream_t stream) {
-  const int G = p.H_q / p.H_kv, D = p.D_qk;
-  if (G == 1 && D == 64) return launch_one<1, 64>(p, grid, stream);
-  if (G == 2 && D == 64) return launch_one<2, 64>(p, grid, stream);
-  if (G == 4 && D == 64) return launch_one<4, 64>(p, grid, stream);
-  if (G == 8 && D == 64) return launch_one<8, 64>(p, grid, stream);
-  if (G == 1 && D == 128) return launch_one<1, 128>(p, grid, stream);
-  if (G == 2 && D == 128) return launch_one<2, 128>(p, grid, stream);
-  if (G == 4 && D == 128) return launch_one<4, 128>(p, grid, stream);
+bool fma_supported(int G, int D) {
+  return G >= 1 && G <= kFmaMaxGroup && (D == 64 || D == 128);
+}
+
+cudaError_t launch_split_fma(const Launch& p0, int grid, cudaStream_t stream) {
+  const int G = p0.H_q / p0.H_kv, D = p0.D_qk;
+  if (!fma_supported(G, D)) return cudaErrorInvalidValue;
+  Launch p = p0;
+  int gc = 1;
+  fma_chunk_shape(G, D, &gc, &p.fma_chunks);
+  p.fma_group = G;
+  if (gc == 1 && D == 64) return launch_one<1, 64>(p, grid, stream);
+  if (gc == 2 && D == 64) return launch_one<2, 64>(p, grid, stream);
+  if (gc == 4 && D == 64) return launch_one<4, 64>(p, grid, stream);
+  if (gc == 8 && D == 64) return launch_one<8, 64>(p, grid, stream);
+  if (gc == 1 && D == 128) return launch_one<1, 128>(p, grid, stream);
+  if (gc == 2 && D == 128) return launch_one<2, 128>(p, grid, stream);
+  if (gc == 4 && D == 128) return launch_one<4, 128>(p, grid, stream);
   return cudaErrorInvalidValue;
 }
 
 int fma_ctas_per_sm(int G, int D) {
-  if (G == 1 && D == 64) return ctas_one<1, 64>();
-  if (G == 2 && D == 64) return ctas_one<2, 64>();
-  if (G == 4 && D == 64) return ctas_one<4, 64>();
-  if (G == 8 && D == 64) return ctas_one<8, 64>();
-  if (G == 1 && D == 128) return ctas_one<1, 128>();
-  if (G == 2 && D == 128) return ctas_one<2, 128>();
-  if (G == 4 && D == 128) return ctas_one<4, 128>();
+  int gc = 1, chunks = 1;
+  fma_chunk_shape(G, D, &gc, &chunks);
+  if (gc == 1 && D == 64) return ctas_one<1, 64>();
+  if (gc == 2 && D == 64) return ctas_one<2, 64>();
+  if (gc == 4 && D == 64) return ctas_one<4, 64>();
+  if (gc == 8 && D == 64) return ctas_one<8, 64>();
+  if (gc == 1 && D == 128) return ctas_one<1, 128>();
+  if (gc == 2 && D == 128) return ctas_one<2, 128>();
+  if (gc == 4 && D == 128) return ctas_one<4, 128>();
   return 1;
 }
 

@@ -214,10 +214,10 @@ RAGGED_TARGET_LEN = 4096
 RAGGED_MAX_LEN = 131072
 
 
-def ragged_target(seed=1003):
-    """The target row's own data: q [32, 128], K and V [4096, 8, 128] (bf16)."""
+def ragged_target(seed=1003, H_q=32):
+    """The target row's own data: q [H_q, 128], K and V [4096, 8, 128] (bf16)."""
     g = torch.Generator().manual_seed(seed)
-    q = _randn((32, 128), g)
+    q = _randn((H_q, 128), g)
     k = _randn((RAGGED_TARGET_LEN, 8, 128), g)
     v = _randn((RAGGED_TARGET_LEN, 8, 128), g)
     return q, k, v
@@ -256,6 +256,7 @@ class RaggedSweep:
     pages, so the target attends over identical data at a different position,
     with different page ids and different batchmates every time.
 
+    H_q: query heads over the 8 KV heads (32 in the sweep's configuration).
     kv_fp8: the caches hold E4M3 bytes (scales 1/64), the target's bytes
     converted once from its bf16 values.  extra: every row's list continues
     in a second, index-gathered cache [extra_slots, 8, 128]; the target's
@@ -265,7 +266,7 @@ class RaggedSweep:
     """
 
     def __init__(self, sizes, device="cuda", seed=1003, page_size=16, kv_fp8=False,
-                 extra=False, extra_slots=32768, extra_width=1024):
+                 extra=False, extra_slots=32768, extra_width=1024, H_q=32):
         self.sizes = list(sizes)
         self.page_size = page_size
         self.device = device
@@ -274,7 +275,8 @@ class RaggedSweep:
         self.extra = extra
         self.extra_slots = extra_slots
         self.extra_width = extra_width
-        self.q_t, self.k_t, self.v_t = ragged_target(seed)
+        self.H_q = H_q
+        self.q_t, self.k_t, self.v_t = ragged_target(seed, H_q)
         self.batches = []
         max_pages = 1
         for B in self.sizes:
@@ -314,8 +316,8 @@ class RaggedSweep:
         kw = {}
         if self.kv_fp8:
             kw = dict(kv_fp8=True, k_scale=self.k_scale, v_scale=self.v_scale)
-        return Workload(name, PAGED, q, k, v, lengths, table, self.page_size, 32, 8, 128, 128,
-                        128 ** -0.5, **extra, **kw)
+        return Workload(name, PAGED, q, k, v, lengths, table, self.page_size, self.H_q, 8, 128,
+                        128, 128 ** -0.5, **extra, **kw)
 
     def solo(self):
         """The target row alone, in its own 256 pages (and, with a second
@@ -349,8 +351,8 @@ class RaggedSweep:
         k = self.kt_cpu.reshape(RAGGED_TARGET_LEN, 8, 128)[None]
         v = self.vt_cpu.reshape(RAGGED_TARGET_LEN, 8, 128)[None]
         return Workload("ragged_solo_cpu", CONTIGUOUS, self.q_t[None], k, v,
-                        torch.tensor([RAGGED_TARGET_LEN], dtype=torch.int32), None, 0, 32, 8,
-                        128, 128, 128 ** -0.5, **extra, **kw)
+                        torch.tensor([RAGGED_TARGET_LEN], dtype=torch.int32), None, 0, self.H_q,
+                        8, 128, 128, 128 ** -0.5, **extra, **kw)
 
     def batch(self, i):
         """(Workload on the device, target position) of the i-th batch."""
@@ -360,7 +362,7 @@ class RaggedSweep:
         self.k_pool[pages] = self._kt
         self.v_pool[pages] = self._vt
         g = torch.Generator(device=self.device).manual_seed(7 * B + 1)
-        q = torch.randn((B, 32, 128), generator=g, device=self.device, dtype=torch.bfloat16)
+        q = torch.randn((B, self.H_q, 128), generator=g, device=self.device, dtype=torch.bfloat16)
         q[pos] = self._qt
         extra = {}
         if self.extra:

@@ -9,8 +9,10 @@ the target every time; the target's bits must equal its solo run, which
 itself matches the fp64 oracle, and repeated runs must be identical.
 
 Families: the E4M3 (one-byte cache) instantiation of the CUDA-core kernel,
-the CUDA-core kernel with a second KV source, the tensor-core shared-latent
-kernel, and the tensor-core kernel with a second latent source.
+the CUDA-core kernel with a second KV source, the CUDA-core kernel on groups
+it cuts into head chunks (8 and 3 query heads per KV head at d = 128), the
+tensor-core shared-latent kernel, and the tensor-core kernel with a second
+latent source.
 """
 
 import pytest
@@ -54,6 +56,12 @@ def test_fp8_cache_ragged_sweep_bitwise(api):
 
 def test_extra_source_ragged_sweep_bitwise(api):
     sweep = W.RaggedSweep(SIZES, extra=True)
+    _sweep(api, sweep, sweep.solo_cpu())
+
+
+@pytest.mark.parametrize("h_q", [64, 24])
+def test_head_chunk_ragged_sweep_bitwise(api, h_q):
+    sweep = W.RaggedSweep(SIZES, H_q=h_q)
     _sweep(api, sweep, sweep.solo_cpu())
 
 

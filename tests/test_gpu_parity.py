@@ -38,6 +38,29 @@ def test_edge_lengths_all_layouts(api, layout, g, d):
     assert_parity(out, lse, ro, rl)
 
 
+@pytest.mark.parametrize("g,d", [(g, 128) for g in (3, 5, 6, 7, 8, 9, 12, 15, 16)] +
+                         [(g, 64) for g in (3, 5, 6, 7, 9, 12, 15, 16)])
+def test_any_group_size(api, g, d):
+    # groups the kernel takes in head chunks of 4 (d = 128) or 8 (d = 64),
+    # the last chunk padded past the group's end
+    wl = W.make(W.PAGED, EDGE_LENGTHS, H_q=2 * g, H_kv=2, D_qk=d, page_size=16,
+                seed=300 + g + d)
+    out, lse = api.run_workload(wl.to("cuda"))
+    ro, rl = oracle_for(wl)
+    assert_parity(out, lse, ro, rl)
+
+
+@pytest.mark.parametrize("g", [3, 8, 12])
+def test_any_group_size_fp8_and_extra(api, g):
+    base = W.make(W.PAGED, [0, 17, 700, 5000], H_q=2 * g, H_kv=2, D_qk=128, page_size=16,
+                  seed=400 + g)
+    for wl in (W.quantize_fp8(base, k_scale=0.5, v_scale=2.0),
+               W.with_extra(base, [3, 0, 64, 900], num_slots=1000, seed=401 + g)):
+        out, lse = api.run_workload(wl.to("cuda"))
+        ro, rl = oracle_for(wl)
+        assert_parity(out, lse, ro, rl)
+
+
 @pytest.mark.parametrize("page_size", [1, 8, 16, 64, 100])
 def test_page_sizes(api, page_size):
     wl = W.make(W.PAGED, [1, 99, 700, 2100], H_q=8, H_kv=2, D_qk=128, page_size=page_size,
