@@ -16,7 +16,10 @@ Cache layouts (``H`` = KV heads, ``D`` = head dim, bf16):
 
 A quantized workload (``kv_fp8``) holds K and V as E4M3 bytes (uint8) with
 one fp32 scale per cache; ``quantize_fp8`` makes one from a bf16 workload by
-torch's own float8_e4m3fn conversion of value / scale.
+torch's own float8_e4m3fn conversion of value / scale.  An NVFP4 workload
+(``kv_nvfp4``) holds, per cache, E2M1 codes ``[..., H, D/2]`` and E4M3 block
+scales ``[..., H, D/16]`` drawn at random (``nvfp4_kv``); on a device the two
+are views into one buffer, codes first, as the library reads them.
 
 The named workloads follow the five configurations the pages' problem
 statement is measured on (tiny dense, GQA paged, MLA-style sparse, ragged
@@ -60,6 +63,11 @@ class Workload:
     kv_fp8: bool = False
     k_scale: float = 1.0
     v_scale: float = 1.0
+    # NVFP4 cache: k / v hold the E2M1 codes [..., H, D/2] (uint8), these the
+    # E4M3 block scales [..., H, D/16] (uint8)
+    kv_nvfp4: bool = False
+    k_blocks: Optional[torch.Tensor] = None
+    v_blocks: Optional[torch.Tensor] = None
 
     @property
     def B(self):
@@ -84,6 +92,9 @@ class Workload:
         n = int(self.lengths.to(torch.int64).sum())
         if self.extra_lengths is not None:
             n += int(self.extra_lengths.to(torch.int64).sum())
+        if self.kv_nvfp4:
+            per = self.H_kv * (self.D_qk // 2 + self.D_qk // 16)
+            return n * 2 * per
         eb = 1 if self.kv_fp8 else 2
         per_entry_k = self.H_kv * self.D_qk * eb
         per_entry_v = 0 if self.v is None else self.H_kv * self.D_v * eb
@@ -92,11 +103,27 @@ class Workload:
     def to(self, device):
         def mv(t):
             return None if t is None else t.to(device)
-        return dataclasses.replace(self, q=mv(self.q), k=mv(self.k), v=mv(self.v),
+        kv = dict(k=mv(self.k), v=mv(self.v))
+        if self.kv_nvfp4:
+            kv = {}
+            for name in ("k", "v"):
+                codes, blocks = getattr(self, name), getattr(self, name + "_blocks")
+                kv[name], kv[name + "_blocks"] = nvfp4_buffer(codes, blocks, device)
+        return dataclasses.replace(self, q=mv(self.q), **kv,
                                    lengths=mv(self.lengths), table=mv(self.table),
                                    extra_k=mv(self.extra_k), extra_v=mv(self.extra_v),
                                    extra_table=mv(self.extra_table),
                                    extra_lengths=mv(self.extra_lengths))
+
+
+def nvfp4_buffer(codes, blocks, device):
+    """One buffer on `device` holding the codes, then the block scales (the
+    layout the library reads); returns (codes view, block-scales view)."""
+    n = codes.numel()
+    buf = torch.empty(n + blocks.numel(), dtype=torch.uint8, device=device)
+    buf[:n].copy_(codes.reshape(-1))
+    buf[n:].copy_(blocks.reshape(-1))
+    return buf[:n].view(codes.shape), buf[n:].view(blocks.shape)
 
 
 def _randn(shape, g):
@@ -120,11 +147,14 @@ def page_table(lengths, page_size, g, width=None, spare_pages=0):
 
 def make(layout, lengths, *, H_q, H_kv, D_qk, D_v=None, page_size=16, width=None,
          num_slots=None, latent=False, seed=0, scale=None, name="custom",
-         identity_table=False):
+         identity_table=False, draw_kv=True):
     """General seeded workload.  q, K, V ~ N(0, 1) rounded to bf16.
 
     latent=True makes one shared latent cache with V = K[..., :D_v] (MLA-style).
     identity_table=True lays paged rows out in consecutive pages (no shuffle).
+    draw_kv=False leaves K and V undrawn (uninitialised placeholders of the
+    right shapes, for a caller that replaces them); q and the table are the
+    same as with draw_kv=True.
     """
     g = torch.Generator().manual_seed(seed)
     lengths = torch.as_tensor(lengths, dtype=torch.int32)
@@ -162,8 +192,12 @@ def make(layout, lengths, *, H_q, H_kv, D_qk, D_v=None, page_size=16, width=None
         vshape = (n_slots, H_kv, D_v)
     else:
         raise ValueError(layout)
-    k = _randn(kshape, g)
-    v = None if latent else _randn(vshape, g)
+    if draw_kv:
+        k = _randn(kshape, g)
+        v = None if latent else _randn(vshape, g)
+    else:
+        k = torch.empty(kshape, dtype=torch.bfloat16)
+        v = None if latent else torch.empty(vshape, dtype=torch.bfloat16)
     return Workload(name, layout, q, k, v, lengths, table, page_size,
                     H_q, H_kv, D_qk, D_v, scale)
 
@@ -188,6 +222,17 @@ def gqa_paged(seed=1001, B=32):
                 width=8192 // 16, seed=seed + 7919, name="gqa_paged_b32_h32x8_d128_p16")
 
 
+def gqa16_paged(seed=1007, B=32):
+    """GQA paged decode with 16 query heads per KV head (the tensor-core
+    GQA variant's case): 32 rows, 128 q / 8 KV heads, head_dim 128, page 16,
+    shuffled page table, lengths uniform in [512, 8192] -- the GQA paged
+    recipe with four times the query heads."""
+    g = torch.Generator().manual_seed(seed)
+    lengths = torch.randint(512, 8193, (B,), generator=g, dtype=torch.int64)
+    return make(PAGED, lengths.tolist(), H_q=128, H_kv=8, D_qk=128, page_size=16,
+                width=8192 // 16, seed=seed + 7919, name="gqa16_paged_b32_h128x8_d128_p16")
+
+
 def mla_sparse(seed=1002, B=64, num_slots=65536, max_topk=2048):
     """MLA-style sparse decode: 64 rows, 128 q heads sharing one latent KV row
     of 576 dims (the first 512 are V), 65536 cache slots, per-row distinct
@@ -199,11 +244,11 @@ def mla_sparse(seed=1002, B=64, num_slots=65536, max_topk=2048):
                 name="mla_sparse_b64_h128_d576v512_topk2048")
 
 
-def long_context(seed=1004, B=8, L=131072, page_size=64, identity_table=False):
+def long_context(seed=1004, B=8, L=131072, page_size=64, identity_table=False, draw_kv=True):
     """Long-context decode: 8 rows of 131072 entries each, 32 q / 8 KV heads,
     head_dim 128, paged with page 64 (shuffled table unless identity_table)."""
     return make(PAGED, [L] * B, H_q=32, H_kv=8, D_qk=128, page_size=page_size,
-                seed=seed, identity_table=identity_table,
+                seed=seed, identity_table=identity_table, draw_kv=draw_kv,
                 name=f"long_context_b{B}_l{L}_h32x8_d128_p{page_size}")
 
 
@@ -258,7 +303,9 @@ class RaggedSweep:
 
     H_q: query heads over the 8 KV heads (32 in the sweep's configuration).
     kv_fp8: the caches hold E4M3 bytes (scales 1/64), the target's bytes
-    converted once from its bf16 values.  extra: every row's list continues
+    converted once from its bf16 values.  kv_nvfp4: the caches are NVFP4
+    (codes, then block scales, in one buffer per cache; global scales 1/2),
+    the target's parts drawn at random like the pool's.  extra: every row's list continues
     in a second, index-gathered cache [extra_slots, 8, 128]; the target's
     RAGGED_TARGET_EXTRA extra entries are written to fresh distinct slots per
     batch, batchmates take uniform extra lengths in [0, extra_width] of
@@ -266,12 +313,13 @@ class RaggedSweep:
     """
 
     def __init__(self, sizes, device="cuda", seed=1003, page_size=16, kv_fp8=False,
-                 extra=False, extra_slots=32768, extra_width=1024, H_q=32):
+                 extra=False, extra_slots=32768, extra_width=1024, H_q=32, kv_nvfp4=False):
         self.sizes = list(sizes)
         self.page_size = page_size
         self.device = device
         self.seed = seed
         self.kv_fp8 = kv_fp8
+        self.kv_nvfp4 = kv_nvfp4
         self.extra = extra
         self.extra_slots = extra_slots
         self.extra_width = extra_width
@@ -299,6 +347,28 @@ class RaggedSweep:
             self.k_pool = _e4m3_bytes(self.k_pool, self.k_scale)
             self.v_pool = _e4m3_bytes(self.v_pool, self.v_scale)
             kt, vt = _e4m3_bytes(kt, self.k_scale), _e4m3_bytes(vt, self.v_scale)
+        self.ktb_cpu = self.vtb_cpu = None
+        if kv_nvfp4:
+            self.k_scale = self.v_scale = 0.5
+            gn = torch.Generator().manual_seed(seed + 29)
+            shape_t = (RAGGED_TARGET_LEN, 8, 128)
+            kc, kb = nvfp4_codes(shape_t, gn)
+            vc, vb = nvfp4_codes(shape_t, gn)
+            kt, vt = kc.view(n_tp, page_size, 8, 64), vc.view(n_tp, page_size, 8, 64)
+            self.ktb_cpu = kb.view(n_tp, page_size, 8, 8)
+            self.vtb_cpu = vb.view(n_tp, page_size, 8, 8)
+            self._ktb, self._vtb = self.ktb_cpu.to(device), self.vtb_cpu.to(device)
+            pools = []
+            for _ in range(2):  # filler parts drawn on the device, codes then scales
+                nc, nb = max_pages * page_size * 8 * 64, max_pages * page_size * 8 * 8
+                buf = torch.empty(nc + nb, dtype=torch.uint8, device=device)
+                buf[:nc] = torch.randint(0, 256, (nc,), generator=g, device=device,
+                                         dtype=torch.int32).to(torch.uint8)
+                e = torch.randint(4, 8, (nb,), generator=g, device=device, dtype=torch.int32)
+                buf[nc:] = ((e << 3) | 5).to(torch.uint8)
+                pools.append((buf[:nc].view(max_pages, page_size, 8, 64),
+                              buf[nc:].view(max_pages, page_size, 8, 8)))
+            (self.k_pool, self.kb_pool), (self.v_pool, self.vb_pool) = pools
         self.kt_cpu, self.vt_cpu = kt, vt  # the target's cache rows as stored
         self._kt = kt.to(device)
         self._vt = vt.to(device)
@@ -312,10 +382,13 @@ class RaggedSweep:
             self.xv_pool = torch.randn(xshape, generator=g, device=device, dtype=torch.bfloat16)
             self._xkt, self._xvt = self.xk_t.to(device), self.xv_t.to(device)
 
-    def _wl(self, name, q, k, v, lengths, table, **extra):
+    def _wl(self, name, q, k, v, lengths, table, kb=None, vb=None, **extra):
         kw = {}
         if self.kv_fp8:
             kw = dict(kv_fp8=True, k_scale=self.k_scale, v_scale=self.v_scale)
+        if self.kv_nvfp4:
+            kw = dict(kv_nvfp4=True, k_blocks=kb, v_blocks=vb, k_scale=self.k_scale,
+                      v_scale=self.v_scale)
         return Workload(name, PAGED, q, k, v, lengths, table, self.page_size, self.H_q, 8, 128,
                         128, 128 ** -0.5, **extra, **kw)
 
@@ -334,10 +407,13 @@ class RaggedSweep:
                          extra_table=xt.to(self.device),
                          extra_lengths=torch.tensor([RAGGED_TARGET_EXTRA], dtype=torch.int32,
                                                     device=self.device))
-        return self._wl("ragged_solo", self._qt[None].contiguous(), self._kt.contiguous(),
-                        self._vt.contiguous(),
+        k, v, kb, vb = self._kt.contiguous(), self._vt.contiguous(), None, None
+        if self.kv_nvfp4:
+            k, kb = nvfp4_buffer(self._kt, self._ktb, self.device)
+            v, vb = nvfp4_buffer(self._vt, self._vtb, self.device)
+        return self._wl("ragged_solo", self._qt[None].contiguous(), k, v,
                         torch.tensor([RAGGED_TARGET_LEN], dtype=torch.int32, device=self.device),
-                        table.to(self.device), **extra)
+                        table.to(self.device), kb=kb, vb=vb, **extra)
 
     def solo_cpu(self):
         """The solo row as a CPU workload with a contiguous cache (for the
@@ -348,8 +424,13 @@ class RaggedSweep:
             extra = dict(extra_k=self.xk_t, extra_v=self.xv_t, extra_table=xt,
                          extra_lengths=torch.tensor([RAGGED_TARGET_EXTRA], dtype=torch.int32))
         kw = dict(kv_fp8=True, k_scale=self.k_scale, v_scale=self.v_scale) if self.kv_fp8 else {}
-        k = self.kt_cpu.reshape(RAGGED_TARGET_LEN, 8, 128)[None]
-        v = self.vt_cpu.reshape(RAGGED_TARGET_LEN, 8, 128)[None]
+        dk = 64 if self.kv_nvfp4 else 128
+        k = self.kt_cpu.reshape(RAGGED_TARGET_LEN, 8, dk)[None]
+        v = self.vt_cpu.reshape(RAGGED_TARGET_LEN, 8, dk)[None]
+        if self.kv_nvfp4:
+            kw = dict(kv_nvfp4=True, k_scale=self.k_scale, v_scale=self.v_scale,
+                      k_blocks=self.ktb_cpu.reshape(RAGGED_TARGET_LEN, 8, 8)[None],
+                      v_blocks=self.vtb_cpu.reshape(RAGGED_TARGET_LEN, 8, 8)[None])
         return Workload("ragged_solo_cpu", CONTIGUOUS, self.q_t[None], k, v,
                         torch.tensor([RAGGED_TARGET_LEN], dtype=torch.int32), None, 0, self.H_q,
                         8, 128, 128, 128 ** -0.5, **extra, **kw)
@@ -361,6 +442,11 @@ class RaggedSweep:
         pages = table[pos, :n_tp].to(device=self.device, dtype=torch.int64)
         self.k_pool[pages] = self._kt
         self.v_pool[pages] = self._vt
+        nv = {}
+        if self.kv_nvfp4:
+            self.kb_pool[pages] = self._ktb
+            self.vb_pool[pages] = self._vtb
+            nv = dict(kb=self.kb_pool, vb=self.vb_pool)
         g = torch.Generator(device=self.device).manual_seed(7 * B + 1)
         q = torch.randn((B, self.H_q, 128), generator=g, device=self.device, dtype=torch.bfloat16)
         q[pos] = self._qt
@@ -382,7 +468,7 @@ class RaggedSweep:
                          extra_table=xt.to(self.device), extra_lengths=el.to(self.device))
         wl = self._wl(f"ragged_b{B}", q, self.k_pool, self.v_pool,
                       torch.tensor(lens, dtype=torch.int32, device=self.device),
-                      table.to(self.device), **extra)
+                      table.to(self.device), **nv, **extra)
         return wl, pos
 
 
@@ -512,6 +598,45 @@ def quantize_fp8(wl, k_scale=1.0 / 64, v_scale=1.0 / 64, name=None):
     return dataclasses.replace(wl, k=q8(wl.k, k_scale), v=q8(wl.v, v_scale), kv_fp8=True,
                                k_scale=float(k_scale), v_scale=float(v_scale),
                                name=name or wl.name + "_fp8")
+
+
+def nvfp4_codes(shape, g):
+    """Random NVFP4 parts for a cache of bf16 shape [..., H, D]: codes uint8
+    [..., H, D/2] uniform over 0..255 (all sixteen E2M1 codes in both nibbles)
+    and block scales uint8 [..., H, D/16], positive E4M3 codes with exponent
+    field 4..7 and a uniform fraction (values 2^-3 .. 1.875)."""
+    *lead, D = shape
+    codes = torch.randint(0, 256, (*lead, D // 2), generator=g, dtype=torch.int32)
+    e = torch.randint(4, 8, (*lead, D // 16), generator=g, dtype=torch.int32)
+    f = torch.randint(0, 8, (*lead, D // 16), generator=g, dtype=torch.int32)
+    return codes.to(torch.uint8), ((e << 3) | f).to(torch.uint8)
+
+
+def nvfp4_kv(wl, k_scale=0.5, v_scale=0.5, seed=0, name=None):
+    """The workload with NVFP4 K and V caches of the same shapes, drawn at
+    random (nvfp4_codes) -- the format's values, not a rounding of wl's: with
+    global scales 1/2 the elements are 0 .. 5.6 in magnitude."""
+    assert wl.v is not None and wl.extra_k is None, "separate K and V, one source"
+    g = torch.Generator().manual_seed(seed)
+    kc, kb = nvfp4_codes(tuple(wl.k.shape), g)
+    vc, vb = nvfp4_codes(tuple(wl.v.shape), g)
+    return dataclasses.replace(wl, k=kc, v=vc, k_blocks=kb, v_blocks=vb, kv_nvfp4=True,
+                               k_scale=float(k_scale), v_scale=float(v_scale),
+                               name=name or wl.name + "_nvfp4")
+
+
+def gqa_paged_nvfp4(seed=1001):
+    """The GQA paged workload (32 rows, 32/8 heads, d = 128, page 16, lengths
+    512..8192) with NVFP4 KV caches (global scales 1/2)."""
+    return nvfp4_kv(gqa_paged(seed), seed=seed + 31,
+                    name="gqa_paged_nvfp4_b32_h32x8_d128_p16")
+
+
+def long_context_nvfp4(seed=1004):
+    """The long-context workload (8 x 131072, 32/8 heads, d = 128, page 64)
+    with NVFP4 KV caches (global scales 1/2)."""
+    return nvfp4_kv(long_context(seed, draw_kv=False), seed=seed + 31,
+                    name="long_context_nvfp4_b8_l131072_h32x8_d128_p64")
 
 
 def gqa_paged_fp8(seed=1001):

@@ -69,6 +69,25 @@ def dequantize(codes, scales, global_scale):
     return np.float64(global_scale) * block * vals
 
 
+def dequantize_cache(codes, scales, global_scale):
+    """A key or value cache stored as NVFP4, decoded to fp64.
+
+    The pages' models are NVFP4 checkpoints ("Sparse MLA decode is not
+    batch-invariant", Environment; "Greedy outputs depend on batch
+    composition", Observation) but no page names a KV cache format.  The
+    reading used here and by the library takes the weight layout above along
+    a head's row: ``codes`` uint8 ``[..., H_kv, D / 2]`` (element 2j in the low
+    nibble of byte j), ``scales`` uint8 ``[..., H_kv, D / 16]`` (one E4M3 scale
+    per 16 consecutive elements of the row), one fp32 scale per cache:
+
+        value[..., h, d] = global_scale * e4m3(scales[..., h, d // 16])
+                           * e2m1(nibble d of row h)
+
+    Returns fp64 ``[..., H_kv, D]``; ``attention.attend`` then runs unchanged.
+    """
+    return dequantize(codes, scales, global_scale)
+
+
 def round_activations(x):
     """The agreed activation precision: fp32 values rounded to bf16 (RNE)."""
     return bf16.round_to_bf16(np.asarray(x, dtype=np.float64))

@@ -7,6 +7,7 @@ import torch
 from oracle import attention as A
 from oracle import bf16 as OB
 from oracle import fp8 as OF
+from oracle import nvfp4 as ON
 
 # Parity bar (out): |gpu - oracle| <= max(1e-2, one bf16 ULP of the oracle
 # value).  A correctly rounded bf16 result is within half a ULP of the exact
@@ -50,9 +51,30 @@ class Fp8Cache:
         return OF.dequantize(self.t[idx].numpy(), self.scale)
 
 
+class Nvfp4Cache:
+    """Read-only view of an NVFP4 cache (codes and block-scale uint8 torch
+    tensors) with its global scale; every read is decoded by the oracle."""
+
+    def __init__(self, codes, blocks, scale):
+        self.codes, self.blocks, self.scale = codes, blocks, scale
+        self.shape = tuple(codes.shape[:-1]) + (codes.shape[-1] * 2,)
+
+    def __getitem__(self, idx):
+        if not isinstance(idx, tuple):
+            idx = (idx,)
+        idx = tuple(torch.as_tensor(np.asarray(i)) if not isinstance(i, (int, slice)) else i
+                    for i in idx)
+        return ON.dequantize_cache(self.codes[idx].numpy(), self.blocks[idx].numpy(), self.scale)
+
+
 def oracle_for(wl, rows=None, heads=None):
     """fp64 oracle (out, lse) of a CPU workload, optionally on a subset."""
     table = None if wl.table is None else wl.table.numpy()
+    if getattr(wl, "kv_nvfp4", False):
+        return A.attend(wl.q.double().numpy(), Nvfp4Cache(wl.k, wl.k_blocks, wl.k_scale),
+                        Nvfp4Cache(wl.v, wl.v_blocks, wl.v_scale), wl.lengths.numpy(),
+                        scale=wl.scale, layout=wl.layout, table=table,
+                        page_size=wl.page_size, d_v=wl.D_v, rows=rows, heads=heads)
     if getattr(wl, "kv_fp8", False):
         return A.attend(wl.q.double().numpy(), Fp8Cache(wl.k, wl.k_scale),
                         Fp8Cache(wl.v, wl.v_scale), wl.lengths.numpy(), scale=wl.scale,

@@ -150,3 +150,75 @@ def test_generator_layout():
     e = (m.scales.numpy() >> 3) & 0xF
     assert e.min() >= 4 and e.max() <= 10 and (m.scales.numpy() < 0x80).all()
     assert m.weight_bytes() == 10 * 32 + 10 * 4
+
+
+# ---------------------------------------------------------------- NVFP4 KV cache
+
+def test_cache_blocks_run_along_each_head_row():
+    # two heads of one entry, D = 32: a head row has two 16-element blocks;
+    # head 0 row codes 0x21 (elements 0.5, 1.0, ...), head 1 row all code 7 (6.0)
+    codes = np.zeros((1, 2, 16), dtype=np.uint8)
+    codes[0, 0] = 0x21
+    codes[0, 1] = 0x77
+    scales = np.array([[[0x38, 0x40], [0x30, 0x48]]], dtype=np.uint8)  # 1, 2 | 0.5, 4
+    got = nvfp4.dequantize_cache(codes, scales, 0.25)
+    h0 = np.array([0.5, 1.0] * 8 + [1.0, 2.0] * 8) * 0.25
+    h1 = np.array([3.0] * 16 + [24.0] * 16) * 0.25
+    assert got.shape == (1, 2, 32)
+    assert np.array_equal(got[0, 0], h0) and np.array_equal(got[0, 1], h1)
+
+
+def test_attention_over_an_nvfp4_cache_by_brute_force():
+    # a 5-entry cache of one KV head (D = 32) decoded by an independent table
+    # of E2M1 values and the E4M3 decoder (pinned in test_oracle_fp8.py);
+    # attention then by math.fsum: the oracle's view must agree to 1e-12
+    from oracle import attention as A
+    rng = np.random.default_rng(3)
+    L, D = 5, 32
+    kc = rng.integers(0, 256, (L, 1, D // 2), dtype=np.uint8)
+    vc = rng.integers(0, 256, (L, 1, D // 2), dtype=np.uint8)
+    ks = rng.integers(0x20, 0x40, (L, 1, D // 16), dtype=np.uint8)
+    vs = rng.integers(0x20, 0x40, (L, 1, D // 16), dtype=np.uint8)
+    q = rng.standard_normal((1, 2, D))
+
+    def hand(codes, scales, g):
+        out = np.zeros((L, 1, D))
+        for t in range(L):
+            for d in range(D):
+                byte = int(codes[t, 0, d // 2])
+                nib = (byte >> 4) if d % 2 else (byte & 0xF)
+                out[t, 0, d] = g * float(fp8.decode_e4m3(scales[t, 0, d // 16])) * E2M1_VALUES[nib]
+        return out
+
+    K, V = hand(kc, ks, 0.5), hand(vc, vs, 2.0)
+    scale = D ** -0.5
+    want_o = np.zeros((2, D))
+    want_l = np.zeros(2)
+    for j in range(2):
+        s = [scale * math.fsum(q[0, j, d] * K[t, 0, d] for d in range(D)) for t in range(L)]
+        m = max(s)
+        w = [math.exp(x - m) for x in s]
+        Z = math.fsum(w)
+        want_l[j] = m + math.log(Z)
+        for d in range(D):
+            want_o[j, d] = math.fsum(w[t] * V[t, 0, d] for t in range(L)) / Z
+    Kd = nvfp4.dequantize_cache(kc, ks, 0.5)[None]
+    Vd = nvfp4.dequantize_cache(vc, vs, 2.0)[None]
+    o, l = A.attend(q, Kd, Vd, np.array([L]), scale=scale, layout="contiguous")
+    assert np.allclose(o[0], want_o, rtol=0, atol=1e-12)
+    assert np.allclose(l[0], want_l, rtol=0, atol=1e-12)
+
+
+def test_nvfp4_workload_device_layout_is_codes_then_scales():
+    wl = W.nvfp4_kv(W.make(W.PAGED, [5, 40], H_q=4, H_kv=2, D_qk=64, page_size=16, seed=3),
+                    seed=4)
+    assert wl.k.shape == (wl.k.shape[0], 16, 2, 32) and wl.k_blocks.shape[-1] == 4
+    moved = wl.to("cpu")
+    base = moved.k.data_ptr()
+    assert moved.k_blocks.data_ptr() == base + moved.k.numel()
+    assert np.array_equal(moved.k.numpy(), wl.k.numpy())
+    assert np.array_equal(moved.v_blocks.numpy(), wl.v_blocks.numpy())
+    # positive scales, no NaN code; every code value appears
+    assert ((wl.k_blocks >> 3) >= 4).all() and ((wl.k_blocks & 0x80) == 0).all()
+    nib = np.concatenate([wl.k.numpy().ravel() & 0xF, wl.k.numpy().ravel() >> 4])
+    assert set(nib.tolist()) == set(range(16))
