@@ -38,6 +38,7 @@ from __future__ import annotations
 VARIANT_CONSTANTS = {
     "fma": (64, 16, 64),
     "mla": (64, 8, 32),
+    "gqa_tc": (64, 16, 64),
 }
 
 BALANCED_FIXED_OVERHEAD = 2
