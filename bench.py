@@ -41,6 +41,9 @@ PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = {
     "split_fma": ["invariant_decode_attention_gb300/csrc/split_fma.cu",
                   "invariant_decode_attention_gb300/csrc/common.cuh"],
+    "split_gqa_tc": ["invariant_decode_attention_gb300/csrc/split_gqa_tc.cu",
+                     "invariant_decode_attention_gb300/csrc/tcgen05.cuh",
+                     "invariant_decode_attention_gb300/csrc/common.cuh"],
     "split_mla": ["invariant_decode_attention_gb300/csrc/split_mla.cu",
                   "invariant_decode_attention_gb300/csrc/tcgen05.cuh",
                   "invariant_decode_attention_gb300/csrc/common.cuh"],
@@ -184,6 +187,12 @@ def build_workload(name, rank=0):
         return W.gqa_paged_fp8(seed=1001 + seed_shift)
     if name == "long_context_fp8":
         return W.long_context_fp8(seed=1004 + seed_shift)
+    if name == "gqa16_paged":
+        return W.gqa16_paged(seed=1007 + seed_shift)
+    if name == "gqa_paged_nvfp4":
+        return W.gqa_paged_nvfp4(seed=1001 + seed_shift)
+    if name == "long_context_nvfp4":
+        return W.long_context_nvfp4(seed=1004 + seed_shift)
     raise ValueError(name)
 
 
@@ -467,7 +476,9 @@ def measure(case, peak, peak_kind, steps, warmup, world=1, dev="cpu", clocks=Non
     _, _, split_ms = time_steps(case, max(20, steps // 2), 3, flush=flush)
     split_avg = max_over_ranks(sum(split_ms) / len(split_ms), dev)
     alg = alg_bytes_of(wl)
-    kernel = "split_mla" if wl.v is None else "split_fma"
+    kernel = ("split_mla" if wl.v is None else
+              "split_gqa_tc" if api.split_constants(case.prob)[0] == api.VARIANT_GQA_TC else
+              "split_fma")
     n_bal = max(20, steps // 4)
     case.policy = api.BALANCED
     bal_ms, _, _ = time_steps(case, n_bal, warmup, split_events=False, flush=flush)
@@ -494,7 +505,7 @@ def measure(case, peak, peak_kind, steps, warmup, world=1, dev="cpu", clocks=Non
             "split_ms_avg": round(split_avg, 5),
         },
     }
-    if kernel == "split_mla":
+    if kernel in ("split_mla", "split_gqa_tc"):
         n_ent = int(wl.lengths.to(torch.int64).sum())
         if wl.extra_lengths is not None:
             n_ent += int(wl.extra_lengths.to(torch.int64).sum())
@@ -517,7 +528,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="long_context",
                     choices=["gqa_paged", "long_context", "tiny", "mla_sparse", "gqa_paged_fp8",
-                             "long_context_fp8"])
+                             "long_context_fp8", "gqa_paged_nvfp4", "long_context_nvfp4",
+                             "gqa16_paged"])
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the secondary workloads and the CPU baseline")
     ap.add_argument("--nvfp4-only", type=int, nargs="+", metavar="ROWS",
@@ -600,7 +612,8 @@ def main():
         line["roofline_tensor"] = rec["roofline_tensor"]
     if not args.no_extra:
         extra = {}
-        for name in ("gqa_paged", "mla_sparse", "tiny", "gqa_paged_fp8", "long_context_fp8",
+        for name in ("gqa_paged", "mla_sparse", "gqa16_paged", "tiny", "gqa_paged_fp8",
+                     "long_context_fp8", "gqa_paged_nvfp4", "long_context_nvfp4",
                      "long_context"):
             if name == args.workload:
                 continue

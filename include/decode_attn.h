@@ -79,10 +79,26 @@ extern "C" {
  * (fixed roundings, independent of the batch).  CUDA-core variant, one KV
  * source only; other combinations return DA_ERR_UNSUPPORTED.              */
 #define DA_KV_FP8_E4M3 1
+/* NVFP4: each head's row of D elements is stored as D/2 bytes of 4-bit E2M1
+ * codes (element 2j in the low nibble of byte j; magnitudes 0, 0.5, 1, 1.5,
+ * 2, 3, 4, 6) and D/16 E4M3 block scales, one per 16 consecutive elements, with
+ * one fp32 scale per cache: element value = scale * e4m3(block) * e2m1(code).
+ * A cache buffer (k or v) holds all its codes first, laid out like a bf16
+ * cache with D/2 bytes per head row ([rows, H_kv, D/2], rows = batch*width
+ * contiguous, num_blocks*page_size paged, num_blocks indexed), and right
+ * after them, at byte offset rows*H_kv*D/2, the block scales [rows, H_kv,
+ * D/16] in the same order.  Same reading of the pages and the same rules as
+ * DA_KV_FP8_E4M3 (k_scale, v_scale; CUDA-core variant, one KV source).  The
+ * kernel turns each code and each block scale into f16 exactly, multiplies
+ * them in f16 (exact: at most six significant bits) and widens to fp32.   */
+#define DA_KV_NVFP4 2
 
 /* ---- kernel variants (chosen from the head config only, never B) ----- */
 #define DA_VARIANT_FMA 0 /* CUDA-core fp32 FMA, H_q/H_kv in 1..128, D in {64,128}    */
 #define DA_VARIANT_MLA 1 /* tcgen05 tensor cores, shared latent 576/512, 16..128 heads */
+/* tcgen05 tensor cores, separate bf16 K and V, 16..128 query heads per KV head,
+ * D = 128, one KV source (other configs of >= 16 heads: DA_VARIANT_FMA)     */
+#define DA_VARIANT_GQA_TC 2
 
 /* ---- device-detected input errors (decode_attn_read_error bits) ----- */
 #define DA_DEVERR_LENGTH 1  /* a length < 0 or above capacity; it was clamped  */
@@ -110,9 +126,9 @@ typedef struct da_problem {
   /* list after its main entries.  0 / 0 when unused.                         */
   int32_t extra_width;      /* extra index row width (max extra entries)      */
   int64_t extra_num_blocks; /* slots in the extra cache                       */
-  int32_t kv_dtype;         /* DA_KV_BF16 (0) or DA_KV_FP8_E4M3               */
-  float k_scale;            /* DA_KV_FP8_E4M3: K element scale (finite, > 0)  */
-  float v_scale;            /* DA_KV_FP8_E4M3: V element scale (finite, > 0)  */
+  int32_t kv_dtype;         /* DA_KV_BF16 (0), DA_KV_FP8_E4M3, DA_KV_NVFP4    */
+  float k_scale;            /* quantized caches: K scale (finite, > 0)        */
+  float v_scale;            /* quantized caches: V scale (finite, > 0)        */
 } da_problem;
 
 /* A plan: filled by decode_attn_plan, read by run/combine.  Host memory,

@@ -19,9 +19,9 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libd
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA = 0, 1, 2, 3, 4
 INVARIANT, BALANCED = 0, 1
-KV_BF16, KV_FP8_E4M3 = 0, 1
+KV_BF16, KV_FP8_E4M3, KV_NVFP4 = 0, 1, 2
 CONTIGUOUS, PAGED, INDEXED = 0, 1, 2
-VARIANT_FMA, VARIANT_MLA = 0, 1
+VARIANT_FMA, VARIANT_MLA, VARIANT_GQA_TC = 0, 1, 2
 DEVERR_LENGTH, DEVERR_INDEX, DEVERR_TIMEOUT = 1, 2, 4
 
 LAYOUT_CODES = {"contiguous": CONTIGUOUS, "paged": PAGED, "indexed": INDEXED}
@@ -205,7 +205,8 @@ def problem_for(wl) -> DaProblem:
                    num_blocks=wl.num_blocks, shared_latent=wl.v is None,
                    extra_width=wl.extra_table.shape[1] if extra else 0,
                    extra_num_blocks=wl.extra_k.shape[0] if extra else 0,
-                   kv_dtype=KV_FP8_E4M3 if getattr(wl, "kv_fp8", False) else KV_BF16,
+                   kv_dtype=(KV_NVFP4 if getattr(wl, "kv_nvfp4", False) else
+                             KV_FP8_E4M3 if getattr(wl, "kv_fp8", False) else KV_BF16),
                    k_scale=getattr(wl, "k_scale", 1.0), v_scale=getattr(wl, "v_scale", 1.0))
 
 

@@ -42,8 +42,9 @@ int check_problem(const da_problem* p) {
   if (p->extra_width < 0 || p->extra_num_blocks < 0) return DA_ERR_INVALID_ARG;
   if (row_capacity(p->layout, p->width, p->page_size) + p->extra_width > 0x7fffffffLL)
     return DA_ERR_INVALID_ARG;
-  if (p->kv_dtype != DA_KV_BF16 && p->kv_dtype != DA_KV_FP8_E4M3) return DA_ERR_INVALID_ARG;
-  if (p->kv_dtype == DA_KV_FP8_E4M3 &&
+  if (p->kv_dtype != DA_KV_BF16 && p->kv_dtype != DA_KV_FP8_E4M3 && p->kv_dtype != DA_KV_NVFP4)
+    return DA_ERR_INVALID_ARG;
+  if (p->kv_dtype != DA_KV_BF16 &&
       !(std::isfinite(p->k_scale) && p->k_scale > 0.f && std::isfinite(p->v_scale) &&
         p->v_scale > 0.f))
     return DA_ERR_INVALID_ARG;
@@ -53,8 +54,8 @@ int check_problem(const da_problem* p) {
 // The kernel variant follows from the head configuration alone -- never from
 // the batch size or the lengths.
 int select_variant(const da_problem* p, Variant* v) {
-  // E4M3 caches: CUDA-core variant, one KV source
-  if (p->kv_dtype == DA_KV_FP8_E4M3 && (p->shared_latent || p->extra_width > 0))
+  // quantized caches: CUDA-core variant, one KV source
+  if (p->kv_dtype != DA_KV_BF16 && (p->shared_latent || p->extra_width > 0))
     return DA_ERR_UNSUPPORTED;
   if (p->shared_latent) {
     if (p->head_dim_qk == 576 && p->head_dim_v == 512 && p->num_kv_heads == 1 &&
@@ -65,6 +66,13 @@ int select_variant(const da_problem* p, Variant* v) {
     return DA_ERR_UNSUPPORTED;
   }
   const int G = p->num_q_heads / p->num_kv_heads;
+  // groups of at least 16 heads over a bf16 cache with one source: the
+  // multi-head contractions go to the tensor cores
+  if (p->head_dim_qk == p->head_dim_v && p->kv_dtype == DA_KV_BF16 && p->extra_width == 0 &&
+      gqa_tc_supported(G, p->head_dim_qk)) {
+    *v = {DA_VARIANT_GQA_TC, kTcTile, kTcMinTilesPerSplit, kTcMaxSplits};
+    return DA_OK;
+  }
   if (p->head_dim_qk == p->head_dim_v && fma_supported(G, p->head_dim_qk)) {
     *v = {DA_VARIANT_FMA, kFmaTile, kFmaMinTilesPerSplit, kFmaMaxSplits};
     return DA_OK;
@@ -144,10 +152,13 @@ Launch make_launch(const da_plan* plan) {
   L.max_splits = plan->max_splits;
   L.o_part_mla = plan->variant == DA_VARIANT_MLA;
   L.scale_log2 = pr.scale * kLog2e;
-  if (pr.kv_dtype == DA_KV_FP8_E4M3) {  // scores of E4M3 keys: scale * k_scale
-    L.kv_fp8 = 1;
+  if (pr.kv_dtype != DA_KV_BF16) {  // scores of scaled keys: scale * k_scale
+    L.kv_type = pr.kv_dtype;
     L.scale_log2 *= pr.k_scale;
     L.v_scale = pr.v_scale;
+    L.kv_rows = (pr.layout == DA_KV_CONTIGUOUS) ? (long long)pr.batch * pr.width
+                : (pr.layout == DA_KV_PAGED)    ? pr.num_blocks * pr.page_size
+                                                : pr.num_blocks;
   }
   return L;
 }
@@ -176,10 +187,12 @@ const char* decode_attn_version(void) {
   static std::once_flag once;
   std::call_once(once, [] {
     std::snprintf(buf, sizeof(buf),
-                  "decode_attn 0.1 sm_103a; fma: tile=%d min_tiles=%d max_splits=%d; "
-                  "mla: tile=%d min_tiles=%d max_splits=%d; balanced fixed_overhead=%d",
+                  "decode_attn 0.2 sm_103a; fma: tile=%d min_tiles=%d max_splits=%d; "
+                  "mla: tile=%d min_tiles=%d max_splits=%d; "
+                  "gqa_tc: tile=%d min_tiles=%d max_splits=%d; balanced fixed_overhead=%d",
                   kFmaTile, kFmaMinTilesPerSplit, kFmaMaxSplits, kMlaTile, kMlaMinTilesPerSplit,
-                  kMlaMaxSplits, kBalancedFixedOverhead);
+                  kMlaMaxSplits, kTcTile, kTcMinTilesPerSplit, kTcMaxSplits,
+                  kBalancedFixedOverhead);
   });
   return buf;
 }
@@ -242,18 +255,20 @@ static int plan_impl(const da_problem* prob, int32_t policy, const int32_t* d_le
   const int sms = sm_count(dev);
   if (sms <= 0) return DA_ERR_CUDA;
   // CTAs that one (row, split) item occupies: one per KV head and head chunk
-  // (CUDA-core variant) or two, one per half of D_v (tensor-core variant).
+  // (CUDA-core variant), one per KV head (GQA tensor-core variant) or two, one
+  // per half of D_v (shared-latent tensor-core variant).
   int gc = 1, chunks = 1;
   if (v.id == DA_VARIANT_FMA)
     fma_chunk_shape(prob->num_q_heads / prob->num_kv_heads, prob->head_dim_qk, &gc, &chunks);
   const int per_item = (v.id == DA_VARIANT_MLA) ? 2 : prob->num_kv_heads * chunks;
   // persistent CTAs: as many as can be resident at once (whole pairs for the
-  // tensor-core variant)
+  // shared-latent variant)
   const long long slots =
-      (v.id == DA_VARIANT_MLA)
-          ? (long long)mla_resident_ctas(sms)
-          : (long long)sms *
-                fma_ctas_per_sm(prob->num_q_heads / prob->num_kv_heads, prob->head_dim_qk);
+      (v.id == DA_VARIANT_MLA)      ? (long long)mla_resident_ctas(sms)
+      : (v.id == DA_VARIANT_GQA_TC) ? (long long)gqa_tc_resident_ctas(sms)
+                                    : (long long)sms * fma_ctas_per_sm(prob->num_q_heads /
+                                                                           prob->num_kv_heads,
+                                                                       prob->head_dim_qk);
   const long long max_units = (long long)prob->batch * v.max_splits * per_item;
 
   da_plan P;
@@ -356,7 +371,8 @@ static int run_impl(const da_plan* plan, const void* q, const void* k, const voi
     L.extra_width = pr.extra_width;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = (plan->variant == DA_VARIANT_MLA) ? launch_split_mla(L, plan->grid, s)
+  const cudaError_t e = (plan->variant == DA_VARIANT_MLA)      ? launch_split_mla(L, plan->grid, s)
+                        : (plan->variant == DA_VARIANT_GQA_TC) ? launch_split_gqa_tc(L, plan->grid, s)
                                                           : launch_split_fma(L, plan->grid, s);
   return e == cudaSuccess ? DA_OK : DA_ERR_CUDA;
 }

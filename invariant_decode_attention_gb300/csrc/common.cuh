@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -24,6 +25,11 @@ constexpr int kFmaMaxGroup = 128;
 constexpr int kMlaTile = 64;
 constexpr int kMlaMinTilesPerSplit = 8;
 constexpr int kMlaMaxSplits = 32;
+
+// Tensor-core variant for groups of >= 16 query heads over separate K and V.
+constexpr int kTcTile = 64;
+constexpr int kTcMinTilesPerSplit = 16;
+constexpr int kTcMaxSplits = 64;
 
 // BALANCED quota: tiles charged per split on top of its own tiles.
 constexpr int kBalancedFixedOverhead = 2;
@@ -72,7 +78,8 @@ struct Launch {
   int page_shift;  // log2(page_size) when it is a power of two, else -1
   int max_splits;
   float scale_log2;  // softmax scale * log2(e) (* k_scale for an E4M3 cache)
-  int kv_fp8;        // K and V are E4M3 bytes
+  int kv_type;       // K and V elements: 0 bf16, 1 E4M3 bytes, 2 NVFP4 (codes + block scales)
+  long long kv_rows; // NVFP4: rows of the main cache (its block scales follow its codes)
   int o_part_mla;    // partials in the tensor-core variant's head-interleaved layout
   float v_scale;     // E4M3 cache: multiplies each unit's output
   int fma_group;     // CUDA-core variant: query heads per KV head (G)
@@ -115,6 +122,9 @@ cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t stream);
 cudaError_t launch_split_fma(const Launch& p, int grid, cudaStream_t stream);
 cudaError_t launch_combine(const Launch& p, cudaStream_t stream);
 cudaError_t launch_split_mla(const Launch& p, int grid, cudaStream_t stream);
+cudaError_t launch_split_gqa_tc(const Launch& p, int grid, cudaStream_t stream);
+bool gqa_tc_supported(int G, int D);
+int gqa_tc_resident_ctas(int sms);
 // Persistent CTAs that fit on one SM for the variant's split kernel.
 int fma_ctas_per_sm(int G, int D);
 int mla_resident_ctas(int sms);  // persistent CTAs, an even number
@@ -241,6 +251,41 @@ __device__ __forceinline__ void cp_async_commit() {
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// 8- and 4-byte copies (through L1; both addresses aligned to the size)
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// ---- low-precision element decoding (all exact) -----------------------------
+// Eight E2M1 codes (a 32-bit word, element 2j in the low nibble of byte j) to
+// four f16 pairs; pair j holds elements 2j (low half) and 2j + 1.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+}
+
+// Two E4M3 codes (low byte first) to an f16 pair.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((unsigned short)two));
+  return h;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
 }
 
 // ---- bulk async copy global -> shared (TMA engine, non-tensor form) --------

@@ -32,8 +32,14 @@
 namespace da {
 namespace {
 
-// F8: the K and V caches hold E4M3 bytes (DA_KV_FP8_E4M3) instead of bf16.
-template <int G, int D, bool F8 = false>
+// Element types of the K and V caches (template argument KT).
+enum KvType {
+  kKvBf16 = 0,  // bf16
+  kKvE4m3 = 1,  // one E4M3 byte per element (DA_KV_FP8_E4M3)
+  kKvFp4 = 2,   // E2M1 codes, two per byte, one E4M3 scale per 16 (DA_KV_NVFP4)
+};
+
+template <int G, int D, int KT = kKvBf16>
 struct FmaShape {
   static constexpr int kTile = kFmaTile;               // entries per tile
   static constexpr int kWarps = 4;
@@ -43,11 +49,16 @@ struct FmaShape {
   static constexpr int kChunks = D / 64;                // 16-byte chunks per lane per row
   static constexpr int kDpl = kChunks * 8;              // dims per lane
   static constexpr int kStages = 3;                     // ring slots per warp
-  static constexpr int kRowBytes = D * (F8 ? 1 : 2);
-  // 16-byte copies per lane per row (8 lanes per row; an E4M3 row of 64 dims
-  // is four copies, made by lanes 0-3)
-  static constexpr int kCopies = F8 ? (D + 127) / 128 : D / 64;
-  static constexpr int kSliceBytes = kTokPerWarp * kRowBytes;  // K (or V) of one warp
+  // bytes of one head's row of codes (and, for kKvFp4, of its block scales)
+  static constexpr int kRowBytes = KT == kKvBf16 ? D * 2 : KT == kKvE4m3 ? D : D / 2;
+  static constexpr int kScaleRowBytes = KT == kKvFp4 ? D / 16 : 0;
+  // 16-byte copies per lane per row (8 lanes per row; a shorter row is copied
+  // by the lanes 0 .. kRowBytes / 16 - 1 of the group)
+  static constexpr int kCopies = (kRowBytes + 127) / 128;
+  // K (or V) of one warp: 16 rows of codes, then (kKvFp4) 16 rows of scales
+  static constexpr int kScalesOffset = kTokPerWarp * kRowBytes;
+  static constexpr int kSliceBytes = kScalesOffset + kTokPerWarp * kScaleRowBytes;
+  static_assert(kSliceBytes % 16 == 0, "slices stay 16-byte aligned");
   static constexpr int kWarpSlotBytes = 2 * kSliceBytes;
   static constexpr int kRingBytes = kStages * kWarps * kWarpSlotBytes;
   static constexpr int kQBytes = G * D * 2;
@@ -194,10 +205,10 @@ __device__ __forceinline__ void cursor_next(const Launch& p, Cursor& c, const vo
 
 // Issue this warp's copies for the cursor's tile into ring slot `slot`, then
 // close the cp.async group (always, so group counting stays uniform).
-template <int G, int D, bool X, bool F8>
+template <int G, int D, bool X, int KT>
 __device__ __forceinline__ void load_slice(const Launch& p, const Cursor& c, uint8_t* smem,
                                            int slot, int warp, int lane) {
-  using S = FmaShape<G, D, F8>;
+  using S = FmaShape<G, D, KT>;
   if (c.valid) {
     const int grp = lane >> 3, sub = lane & 7;
     uint8_t* ks = smem + (slot * S::kWarps + warp) * S::kWarpSlotBytes;
@@ -238,9 +249,25 @@ __device__ __forceinline__ void load_slice(const Launch& p, const Cursor& c, uin
 #pragma unroll
           for (int ch = 0; ch < S::kCopies; ++ch) {
             const int e = (sub + 8 * ch) * 16;  // byte offset of this 16-byte copy
-            if (F8 && e >= S::kRowBytes) continue;
+            if (S::kRowBytes % 128 != 0 && e >= S::kRowBytes) continue;
             cp_async16(smem_addr(ks + tl * S::kRowBytes + e), kb + off + e);
             cp_async16(smem_addr(vs + tl * S::kRowBytes + e), vb + off + e);
+          }
+          if constexpr (KT == kKvFp4) {
+            // the row's block scales sit in the scale region after all codes
+            if (sub == 7) {
+              const size_t so = (size_t)p.kv_rows * p.H_kv * S::kRowBytes +
+                                ((size_t)row * p.H_kv + c.x.h) * S::kScaleRowBytes;
+              const uint32_t kd = smem_addr(ks + S::kScalesOffset + tl * S::kScaleRowBytes);
+              const uint32_t vd = smem_addr(vs + S::kScalesOffset + tl * S::kScaleRowBytes);
+              if constexpr (S::kScaleRowBytes == 8) {
+                cp_async8(kd, kb + so);
+                cp_async8(vd, vb + so);
+              } else {
+                cp_async4(kd, kb + so);
+                cp_async4(vd, vb + so);
+              }
+            }
           }
         }
       }
@@ -300,12 +327,41 @@ __device__ __forceinline__ void unpack_row2_f8(const uint8_t* row, int sub, uint
   }
 }
 
-template <int D, bool F8>
-__device__ __forceinline__ void unpack_kv2(const uint8_t* row, int sub, uint64_t* f) {
-  if constexpr (F8)
-    unpack_row2_f8<D>(row, sub, f);
+// The same for an NVFP4 row: 4 code bytes per lane per 64 dims (8 E2M1
+// values, low nibble first) and the lane's block scale (dims 16k .. 16k + 15
+// share byte k of the scale row).  Each code becomes an f16 exactly, the f16
+// product with the E4M3 scale is exact too (at most 2 x 4 significant bits,
+// magnitudes 2^-10 .. 2688), and f16 widens to fp32 exactly.
+template <int D>
+__device__ __forceinline__ void unpack_row2_fp4(const uint8_t* row, const uint8_t* scales,
+                                                int sub, uint64_t* f) {
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) {
+    const uint32_t w = reinterpret_cast<const uint32_t*>(row)[sub + 8 * c];
+    const uint32_t s2 = e4m3x2_to_f16x2(scales[4 * c + (sub >> 1)]);
+    const uint32_t sc = __byte_perm(s2, 0, 0x1010);  // (s, s)
+    uint32_t hv[4];
+    e2m1x8_to_f16x2(w, hv);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t h2 = hmul2(hv[e], sc);
+      const __half2 hp = *reinterpret_cast<const __half2*>(&h2);
+      f[c * 4 + e] = pack2(__low2float(hp), __high2float(hp));
+    }
+  }
+}
+
+// Row `r` of a slice (K or V part) as the lane's packed fp32 pairs.
+template <int G, int D, int KT>
+__device__ __forceinline__ void unpack_kv2(const uint8_t* part, int r, int sub, uint64_t* f) {
+  using S = FmaShape<G, D, KT>;
+  if constexpr (KT == kKvE4m3)
+    unpack_row2_f8<D>(part + r * S::kRowBytes, sub, f);
+  else if constexpr (KT == kKvFp4)
+    unpack_row2_fp4<D>(part + r * S::kRowBytes, part + S::kScalesOffset + r * S::kScaleRowBytes,
+                       sub, f);
   else
-    unpack_row2<D>(row, sub, f);
+    unpack_row2<D>(part + r * S::kRowBytes, sub, f);
 }
 
 // Lane-dependent orders that let the 8 lanes of an entry group reduce their
@@ -335,13 +391,13 @@ __device__ __forceinline__ int hperm_of(int sub) {
 // lane's own entries only; lanes are summed at the end of the unit.
 // G == 1: every lane of a group ends with the group's scores (butterfly) and
 // l[0] counts the group's entries.
-template <int G, int D, bool F8, bool kPartial>
+template <int G, int D, int KT, bool kPartial>
 __device__ __forceinline__ void consume_slice(const uint8_t* ks, int lane, int n_valid,
                                               const uint64_t (&q2)[G][FmaShape<G, D>::kDpl / 2],
                                               float (&m)[G], float (&l)[G],
                                               uint64_t (&acc2)[G][FmaShape<G, D>::kDpl / 2],
                                               float scale_log2) {
-  using S = FmaShape<G, D, F8>;
+  using S = FmaShape<G, D, KT>;
   constexpr int kP = S::kDpl / 2;  // packed pairs per lane
   constexpr int kV = S::kSteps * G;  // partial scores per lane
   const int grp = lane >> 3, sub = lane & 7;
@@ -353,7 +409,7 @@ __device__ __forceinline__ void consume_slice(const uint8_t* ks, int lane, int n
 #pragma unroll
   for (int js = 0; js < S::kSteps; ++js) {
     uint64_t k2[kP];
-    unpack_kv2<D, F8>(ks + (4 * (js ^ tp) + grp) * S::kRowBytes, sub, k2);
+    unpack_kv2<G, D, KT>(ks, 4 * (js ^ tp) + grp, sub, k2);
 #pragma unroll
     for (int hs = 0; hs < G; ++hs) {
       uint64_t a = ffma2(q2[hs][0], k2[0], 0ull);
@@ -485,7 +541,7 @@ __device__ __forceinline__ void consume_slice(const uint8_t* ks, int lane, int n
     const int row = 4 * (js ^ tp) + grp;
     if (kPartial && row >= n_valid) continue;  // never read unfilled rows
     uint64_t v2[kP];
-    unpack_kv2<D, F8>(vs + row * S::kRowBytes, sub, v2);
+    unpack_kv2<G, D, KT>(vs, row, sub, v2);
 #pragma unroll
     for (int hs = 0; hs < G; ++hs) {
       const uint64_t p2 = pack2(pfull[js][hs], pfull[js][hs]);
@@ -495,9 +551,9 @@ __device__ __forceinline__ void consume_slice(const uint8_t* ks, int lane, int n
   }
 }
 
-template <int G, int D, bool X, bool F8>
+template <int G, int D, bool X, int KT>
 __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Launch p) {
-  using S = FmaShape<G, D, F8>;
+  using S = FmaShape<G, D, KT>;
   extern __shared__ __align__(128) uint8_t smem[];
   float* scratch = reinterpret_cast<float*>(smem + S::kScratchOffset);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -528,7 +584,7 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
     pf.valid = false;
 #pragma unroll
   for (int s = 0; s < S::kStages - 1; ++s) {
-    load_slice<G, D, X, F8>(p, pf, smem, s, warp, lane);
+    load_slice<G, D, X, KT>(p, pf, smem, s, warp, lane);
     cursor_next<G, X>(p, pf, ring, n_units);
   }
 
@@ -564,14 +620,14 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
         named_bar_sync(1, S::kThreads);
       }
       // refill the slot consumed in the previous iteration
-      load_slice<G, D, X, F8>(p, pf, smem, (slot + S::kStages - 1) % S::kStages, warp, lane);
+      load_slice<G, D, X, KT>(p, pf, smem, (slot + S::kStages - 1) % S::kStages, warp, lane);
       cursor_next<G, X>(p, pf, ring, n_units);
       const uint8_t* ks = smem + (slot * S::kWarps + warp) * S::kWarpSlotBytes;
       const int n_valid = min(S::kTokPerWarp, x.L - k * S::kTile - warp * S::kTokPerWarp);
       if (n_valid >= S::kTokPerWarp)
-        consume_slice<G, D, F8, false>(ks, lane, n_valid, q2, m, l, acc2, p.scale_log2);
+        consume_slice<G, D, KT, false>(ks, lane, n_valid, q2, m, l, acc2, p.scale_log2);
       else
-        consume_slice<G, D, F8, true>(ks, lane, n_valid, q2, m, l, acc2, p.scale_log2);
+        consume_slice<G, D, KT, true>(ks, lane, n_valid, q2, m, l, acc2, p.scale_log2);
       slot = (slot + 1 == S::kStages) ? 0 : slot + 1;
     }
 
@@ -645,7 +701,7 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
 #pragma unroll
         for (int w = 0; w < S::kWarps; ++w) o = fmaf(scratch[(w * G + h) * S::kSRow + d], wgt[w], o);
         o = (lt > 0.f) ? o / lt : 0.f;
-        if constexpr (F8) o *= p.v_scale;  // E4M3 values: scale once, at the output
+        if constexpr (KT != kKvBf16) o *= p.v_scale;  // cache scale: once, at the output
         if (x.single)
           p.out[((size_t)x.b * p.H_q + hq) * D + d] = __float2bfloat16_rn(o);
         else
@@ -674,35 +730,38 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
   }
 }
 
-template <int G, int D, bool X, bool F8>
+template <int G, int D, bool X, int KT>
 cudaError_t launch_x(const Launch& p, int grid, cudaStream_t stream) {
-  using S = FmaShape<G, D, F8>;
+  using S = FmaShape<G, D, KT>;
   static const cudaError_t attr = cudaFuncSetAttribute(
-      split_fma_kernel<G, D, X, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+      split_fma_kernel<G, D, X, KT>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
   if (attr != cudaSuccess) return attr;
-  return launch_after(split_fma_kernel<G, D, X, F8>, dim3(grid), dim3(S::kThreads), S::kSmemBytes,
+  return launch_after(split_fma_kernel<G, D, X, KT>, dim3(grid), dim3(S::kThreads), S::kSmemBytes,
                       stream, p);
 }
 
-// Instantiations: bf16 with one or two KV sources; E4M3 with one source.
+// Instantiations: bf16 with one or two KV sources; E4M3 and NVFP4 caches
+// with one source.
 template <int G, int D>
 cudaError_t launch_one(const Launch& p, int grid, cudaStream_t stream) {
-  if (p.kv_fp8) {
+  if (p.kv_type != kKvBf16) {
     if (p.extra_k) return cudaErrorInvalidValue;
-    return launch_x<G, D, false, true>(p, grid, stream);
+    if (p.kv_type == kKvE4m3) return launch_x<G, D, false, kKvE4m3>(p, grid, stream);
+    if (p.kv_type == kKvFp4) return launch_x<G, D, false, kKvFp4>(p, grid, stream);
+    return cudaErrorInvalidValue;
   }
-  return p.extra_k ? launch_x<G, D, true, false>(p, grid, stream)
-                   : launch_x<G, D, false, false>(p, grid, stream);
+  return p.extra_k ? launch_x<G, D, true, kKvBf16>(p, grid, stream)
+                   : launch_x<G, D, false, kKvBf16>(p, grid, stream);
 }
 
 template <int G, int D>
 int ctas_one() {
   using S = FmaShape<G, D>;
   static int n = [] {
-    cudaFuncSetAttribute(split_fma_kernel<G, D, false, false>,
+    cudaFuncSetAttribute(split_fma_kernel<G, D, false, kKvBf16>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
     int c = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, split_fma_kernel<G, D, false, false>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, split_fma_kernel<G, D, false, kKvBf16>,
                                                       S::kThreads,
                                                       S::kSmemBytes) != cudaSuccess)
       c = 1;

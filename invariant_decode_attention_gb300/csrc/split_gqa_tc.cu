@@ -1,0 +1,659 @@
+// Split kernel, tensor-core variant for grouped-query attention with a
+// separate K and V cache: 16 to 128 query heads per KV head, head dim 128,
+// bf16 caches.
+//
+// One unit of work = (row b, split s, KV head h).  Both contractions run on
+// tcgen05 tensor cores with fp32 accumulators in tensor memory (TMEM); the
+// G query heads of the group are the MMA's M rows (padded to 128: rows past
+// the group compute on whatever the Q buffer holds there and are never
+// written -- a row of an MMA result depends only on its own row of A):
+//     S = Q K^T      M = 128, N = 64 entries, K = 128 dims   (8 MMAs of K=16)
+//     O += P V       M = 128, N = 128 dims,   K = 64 entries (4 MMAs of K=16)
+// A thread of the softmax warps owns one head (one TMEM lane), so the
+// running max and sum of a head are plain per-thread loops: no cross-lane
+// reductions.  The reference value of the exponentials moves only when a
+// score exceeds it by more than 2^8 (then O is rescaled in TMEM), a decision
+// that depends only on the unit's own scores.
+//
+// Memory.  Shared: two Q buffers (the next unit's Q loads while the current
+// one runs) and four 64-entry stages of K and V, each tile in the
+// 128-byte-swizzled layout the tensor core reads (two 64-dim regions of
+// 64 rows x 128 bytes).  P of a tile (128 heads x 64 entries, bf16) is
+// written over its stage's K tile once S has read it.  TMEM: two S buffers
+// and two O accumulators (the next unit's first P.V does not wait for the
+// previous unit's epilogue).
+//
+// Loads (TMA).  For a contiguous cache and for pages of a multiple of 16
+// entries, each 16-entry group of a tile is 16 consecutive cache rows: one
+// box copy of 16 rows x 64 dims per half of the head's row.  Other layouts
+// gather four rows per copy (tile::gather4).  Entries past the split's end,
+// and entries whose page or slot is out of range, copy cache row 0 instead
+// (their scores are masked), so no stage byte is ever uninitialised.
+//
+// Roles (192 threads): warps 0-3 softmax and epilogue; warp 4 producer (page
+// or index lookups one tile ahead, TMA issue); warp 5 MMA issue (one
+// thread) and TMEM allocation.  Every mbarrier wait is bounded; on time-out
+// the kernel records DA_DEVERR_TIMEOUT, every role leaves its loop,
+// outstanding tensor-core work is drained (bounded) and TMEM is freed.
+//
+// Softmax attention and its split/merge are the computation "Sparse MLA
+// decode is not batch-invariant" (FlashMLA issue #212) reports on; which CTA
+// runs a unit never changes what the unit computes.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "tcgen05.cuh"
+
+namespace da {
+namespace {
+
+constexpr int kRows = 128;  // MMA M: query heads of the group, padded
+constexpr int kD = 128;
+constexpr int kT = kTcTile;  // entries per tile
+static_assert(kT == 64, "one 128-byte swizzle row of P per head");
+constexpr int kStages = 4;
+constexpr int kRegion = kT * 128;           // 64 rows x 64 dims (bf16)
+constexpr int kTileBytes = 2 * kRegion;     // K (or V) of a tile: 16 KB
+constexpr int kStageBytes = 2 * kTileBytes;  // K, then V
+constexpr int kQRegion = kRows * 128;       // 128 rows x 64 dims
+constexpr int kQBytes = 2 * kQRegion;       // 32 KB
+constexpr int kStageOffset = 2 * kQBytes;
+constexpr int kBarOffset = kStageOffset + kStages * kStageBytes;
+enum {
+  kFull0 = 0, kEmpty0 = kFull0 + kStages, kQFull0 = kEmpty0 + kStages, kQFree0 = kQFull0 + 2,
+  kSFull0 = kQFree0 + 2, kSFree0 = kSFull0 + 2, kPFull0 = kSFree0 + 2, kPVDone0 = kPFull0 + 2,
+  kOFree0 = kPVDone0 + 2, kDrain = kOFree0 + 2, kNumBars
+};
+constexpr int kTmemSlot = kBarOffset + kNumBars * 8;
+constexpr int kAbortSlot = kTmemSlot + 4;
+constexpr int kSmemBytes = kAbortSlot + 12;
+static_assert(kStageOffset % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle atoms 1024-aligned");
+static_assert(kSmemBytes <= 232448, "fits the 227 KB per-block limit");
+
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSCol = 0;    // S buffers [0, 64) and [64, 128)
+constexpr uint32_t kOCol = 128;  // O accumulators [128, 256) and [256, 384)
+constexpr float kRescaleLog2 = 8.f;
+constexpr int kQBoxRows = 16;
+
+constexpr uint32_t kIdescS = umma::idesc_bf16_f32(kRows, kT, false);
+constexpr uint32_t kIdescO = umma::idesc_bf16_f32(kRows, kD, true);
+
+__device__ __forceinline__ void tma_box3(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
+                                         int c2, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_box2(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+// Box {64, 1} at rows r0..r3 of a 2-D map: four 128-byte rows at dst + 128 i.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* tm, int col, int r0,
+                                            int r1, int r2, int r3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+struct Maps {
+  CUtensorMap k3, v3;  // [rows][H_kv][128], box {64, 1, 16} (box path)
+  CUtensorMap k2, v2;  // [rows * H_kv][128], box {64, 1} (gather path)
+  CUtensorMap q;       // [B * H_q][128], box {64, 16}
+};
+
+struct Ctx {
+  uint8_t* smem;
+  uint32_t sbase;
+  volatile int* abort_flag;
+  int32_t* hdr;
+};
+
+__device__ __forceinline__ uint32_t bar_addr(const Ctx& c, int i) {
+  return c.sbase + kBarOffset + 8 * i;
+}
+
+// Bounded wait that also gives up when the abort flag is raised.
+__device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity) {
+  const uint32_t bar = bar_addr(c, i);
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*c.abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        set_error(c.hdr, DA_DEVERR_TIMEOUT);
+        *c.abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// A unit: KV head h of one (row, split) item.
+struct TcUnit {
+  int slot, b, h, t_begin, t_end;
+  bool single;
+};
+
+__device__ __forceinline__ TcUnit tc_unit(const Launch& p, int u) {
+  const int4 d = __ldg(reinterpret_cast<const int4*>(p.item_desc) + u / p.H_kv);
+  TcUnit x;
+  x.single = d.x < 0;
+  x.slot = x.single ? ~d.x : d.x;
+  x.b = x.slot / p.max_splits;
+  x.h = u % p.H_kv;
+  x.t_begin = d.y * kT;
+  x.t_end = min(d.z * kT, d.w);
+  return x;
+}
+
+// ---------------------------------------------------------------- producer
+// Warp 4.  Box path: lane j < 4 owns the 16-entry group j of each tile;
+// gather path: lane j < 16 owns the 4-entry group j.  A lane loads the table
+// word(s) of its group one tile ahead of the copies that use them.
+__device__ void producer(const Launch& p, const Ctx& c, const Maps& m, int n_units, bool box) {
+  const int lane = threadIdx.x & 31;
+  const int G = p.H_q / p.H_kv;
+  const int q_boxes = (G + kQBoxRows - 1) / kQBoxRows;
+  const int per = box ? 16 : 4;             // entries per lane-group
+  const int groups = kT / per;              // 4 or 16
+  uint32_t g = 0, nq = 0;
+  bool bad = false;
+  // cache row of entry `tok` of row b (paged: from the page word), or -1
+  // when the entry is past the split or its page / slot is out of range
+  auto word_of = [&](const TcUnit& x, int tok) -> int {
+    if (tok >= x.t_end || p.layout == DA_KV_CONTIGUOUS) return 0;
+    if (p.layout == DA_KV_PAGED) return __ldg(p.table + (size_t)x.b * p.width + tok / p.page_size);
+    return __ldg(p.table + (size_t)x.b * p.width + tok);
+  };
+  auto row_of = [&](const TcUnit& x, int tok, int word) -> long long {
+    if (tok >= x.t_end) return -1;
+    if (p.layout == DA_KV_CONTIGUOUS) return (long long)x.b * p.width + tok;
+    if (p.layout == DA_KV_PAGED) {
+      if (word < 0 || word >= p.num_blocks) {
+        bad = true;
+        return -1;
+      }
+      return (long long)word * p.page_size + tok % p.page_size;
+    }
+    if (word < 0 || word >= p.num_blocks) {
+      bad = true;
+      return -1;
+    }
+    return word;
+  };
+  auto wait_w = [&](int bar, uint32_t parity) -> bool {
+    int ok = 1;
+    if (lane == 0) ok = wait_bar(c, bar, parity) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+  };
+  bool alive = true;
+  for (int u = blockIdx.x; u < n_units && alive; u += gridDim.x, ++nq) {
+    const TcUnit x = tc_unit(p, u);
+    // Q of the unit's heads into Q buffer nq & 1 once the unit that used it
+    // last has finished its S MMAs
+    const int qb = nq & 1;
+    if (!wait_w(kQFree0 + qb, ((nq >> 1) & 1) ^ 1)) break;
+    if (lane == 0) {
+      const uint32_t qfull = bar_addr(c, kQFull0 + qb);
+      mbar_arrive_expect_tx(qfull, q_boxes * 2 * kQBoxRows * 128);
+      const uint32_t qdst = c.sbase + qb * kQBytes;
+      for (int rb = 0; rb < q_boxes; ++rb)
+        for (int half = 0; half < 2; ++half)
+          tma_box2(qdst + half * kQRegion + rb * kQBoxRows * 128, &m.q, 64 * half,
+                   x.b * p.H_q + x.h * G + rb * kQBoxRows, qfull);
+    }
+    // this lane's group of the first tile
+    int word = (lane < groups) ? word_of(x, x.t_begin + lane * per) : 0;
+    int words4[4] = {0, 0, 0, 0};
+    if (!box && lane < groups)
+      for (int i = 0; i < 4; ++i) words4[i] = word_of(x, x.t_begin + lane * per + i);
+    for (int t0 = x.t_begin; t0 < x.t_end; t0 += kT, ++g) {
+      const int st = g % kStages;
+      // the next tile's words, loaded before this tile's copies are issued
+      int nword = 0, nwords4[4] = {0, 0, 0, 0};
+      const int t1 = t0 + kT;
+      if (t1 < x.t_end && lane < groups) {
+        if (box)
+          nword = word_of(x, t1 + lane * per);
+        else
+          for (int i = 0; i < 4; ++i) nwords4[i] = word_of(x, t1 + lane * per + i);
+      }
+      if (!wait_w(kEmpty0 + st, ((g / kStages) & 1) ^ 1)) {
+        alive = false;
+        break;
+      }
+      const uint32_t full = bar_addr(c, kFull0 + st);
+      if (lane == 0) mbar_arrive_expect_tx(full, kStageBytes);
+      __syncwarp();
+      const uint32_t kdst = c.sbase + kStageOffset + st * kStageBytes;
+      const uint32_t vdst = kdst + kTileBytes;
+      if (lane < groups) {
+        if (box) {
+          const int tok = t0 + lane * per;
+          long long r = row_of(x, tok, word);
+          if (r < 0) r = 0;
+          for (int half = 0; half < 2; ++half) {
+            const uint32_t off = half * kRegion + lane * per * 128;
+            tma_box3(kdst + off, &m.k3, 64 * half, x.h, (int)r, full);
+            tma_box3(vdst + off, &m.v3, 64 * half, x.h, (int)r, full);
+          }
+        } else {
+          int rr[4];
+          for (int i = 0; i < 4; ++i) {
+            const long long r = row_of(x, t0 + lane * per + i, words4[i]);
+            rr[i] = (int)((r < 0 ? 0 : r) * p.H_kv + x.h);
+          }
+          for (int half = 0; half < 2; ++half) {
+            const uint32_t off = half * kRegion + lane * per * 128;
+            tma_gather4(kdst + off, &m.k2, 64 * half, rr[0], rr[1], rr[2], rr[3], full);
+            tma_gather4(vdst + off, &m.v2, 64 * half, rr[0], rr[1], rr[2], rr[3], full);
+          }
+        }
+      }
+      word = nword;
+      for (int i = 0; i < 4; ++i) words4[i] = nwords4[i];
+    }
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(p.hdr, DA_DEVERR_INDEX);
+  // leave no copy in flight into this CTA's shared memory (on the normal path
+  // every stage and Q buffer was consumed and these waits return at once)
+  if (lane == 0) {
+    for (int st = 0; st < kStages; ++st) {
+      const int last = (int)g - 1 - (((int)g - 1 - st) % kStages + kStages) % kStages;
+      if (last >= 0 && !mbar_wait(bar_addr(c, kFull0 + st), (last / kStages) & 1))
+        set_error(p.hdr, DA_DEVERR_TIMEOUT);
+    }
+    for (int qb = 0; qb < 2; ++qb) {
+      const int last = (int)nq - 1 - (((int)nq - 1 - qb) % 2 + 2) % 2;
+      if (last >= 0 && !mbar_wait(bar_addr(c, kQFull0 + qb), (last >> 1) & 1))
+        set_error(p.hdr, DA_DEVERR_TIMEOUT);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- MMA issue
+__device__ void mma_issuer(const Launch& p, const Ctx& c, uint32_t tmem, int n_units) {
+  // K-major tiles, 128-byte swizzle: 8-row groups 1024 bytes apart
+  const uint64_t b_k0 = umma::smem_desc(c.sbase + kStageOffset, 16, 1024, umma::kSwizzle128B);
+  const uint64_t a_q0 = umma::smem_desc(c.sbase, 16, 1024, umma::kSwizzle128B);
+  // V as an MN-major B operand: 64-dim regions kRegion apart, 8-entry groups
+  // 1024 bytes apart
+  const uint64_t b_v0 =
+      umma::smem_desc(c.sbase + kStageOffset + kTileBytes, kRegion, 1024, umma::kSwizzle128B);
+  uint32_t g = 0, nq = 0;
+  for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++nq) {
+    const TcUnit x = tc_unit(p, u);
+    const int n_sub = (x.t_end - x.t_begin + kT - 1) / kT;
+    const int qb = nq & 1, ob = nq & 1;
+    if (!wait_bar(c, kQFull0 + qb, (nq >> 1) & 1)) return;
+    fence_proxy_async();
+    // O += P(gp) V(gp): P sits over the K tile of stage gp, V after it
+    auto pv = [&](uint32_t gp, bool first) -> bool {
+      if (!wait_bar(c, kPFull0 + (gp & 1), (gp >> 1) & 1)) return false;
+      if (first && !wait_bar(c, kOFree0 + ob, ((nq >> 1) & 1) ^ 1)) return false;
+      umma::fence_after_sync();
+      const uint32_t st = (gp % kStages) * kStageBytes;
+      const uint64_t ap = b_k0 + (uint64_t)(st >> 4);
+      const uint64_t bv = b_v0 + (uint64_t)(st >> 4);
+#pragma unroll
+      for (int kk = 0; kk < kT / 16; ++kk)
+        umma::mma_bf16(tmem + kOCol + ob * kD, ap + (uint64_t)((kk * 32) >> 4),
+                       bv + (uint64_t)((kk * 2048) >> 4), kIdescO, (first && kk == 0) ? 0u : 1u);
+      umma::commit(bar_addr(c, kPVDone0 + (gp & 1)));
+      umma::commit(bar_addr(c, kEmpty0 + (gp % kStages)));
+      return true;
+    };
+    // issue order S(g), PV(g-1): S(g) goes to the other S buffer, so it runs
+    // while the softmax of tile g-1 is still producing P(g-1)
+    for (int i = 0; i < n_sub; ++i, ++g) {
+      const int st = g % kStages;
+      const int sb = g & 1;
+      if (!wait_bar(c, kFull0 + st, (g / kStages) & 1)) return;
+      fence_proxy_async();
+      if (!wait_bar(c, kSFree0 + sb, ((g >> 1) & 1) ^ 1)) return;  // S(g-2) was read
+      umma::fence_after_sync();
+      const uint64_t b0 = b_k0 + (uint64_t)((st * kStageBytes) >> 4);
+      const uint64_t a0 = a_q0 + (uint64_t)((qb * kQBytes) >> 4);
+#pragma unroll
+      for (int k = 0; k < kD / 16; ++k) {  // dims 16k .. 16k + 15
+        const uint32_t off = (k / 4) * kRegion + (k % 4) * 32;
+        const uint32_t offq = (k / 4) * kQRegion + (k % 4) * 32;
+        umma::mma_bf16(tmem + kSCol + sb * kT, a0 + (uint64_t)(offq >> 4),
+                       b0 + (uint64_t)(off >> 4), kIdescS, k ? 1u : 0u);
+      }
+      umma::commit(bar_addr(c, kSFull0 + sb));
+      if (i == n_sub - 1) umma::commit(bar_addr(c, kQFree0 + qb));
+      if (i > 0 && !pv(g - 1, i == 1)) return;
+    }
+    if (!pv(g - 1, n_sub == 1)) return;
+  }
+}
+
+// ---------------------------------------------------------------- softmax + epilogue
+__device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int n_units) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = threadIdx.x;  // head of the group = TMEM lane
+  const int G = p.H_q / p.H_kv;
+  const bool live = row < G;              // rows past the group are never written
+  const bool warp_live = warp * 32 < G;   // a warp of padding rows only keeps time
+  const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+  uint32_t g = 0, nq = 0;
+  auto wait_w = [&](int bar, uint32_t parity) -> bool {
+    int ok = 1;
+    if (lane == 0) ok = wait_bar(c, bar, parity) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+  };
+  auto arrive_w = [&](int bar) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_addr(c, bar));
+  };
+  for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++nq) {
+    const TcUnit x = tc_unit(p, u);
+    const int n_sub = (x.t_end - x.t_begin + kT - 1) / kT;
+    const int ob = nq & 1;
+    const uint32_t o_col = kOCol + ob * kD;
+    float m_used = -INFINITY, l = 0.f;
+    for (int i = 0; i < n_sub; ++i, ++g) {
+      const int sb = g & 1;
+      if (!wait_w(kSFull0 + sb, (g >> 1) & 1)) return;
+      if (!warp_live) {  // its P rows keep the stage's (finite) K bytes
+        arrive_w(kSFree0 + sb);
+        arrive_w(kPFull0 + sb);
+        continue;
+      }
+      umma::fence_after_sync();
+      float s[kT];
+      {
+        float s_hi[32];
+        umma::ld_32x32b_x32(lane_base + kSCol + sb * kT, *reinterpret_cast<float(*)[32]>(s));
+        umma::ld_32x32b_x32(lane_base + kSCol + sb * kT + 32, s_hi);
+        umma::wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) s[32 + j] = s_hi[j];
+      }
+      umma::fence_before_sync();
+      arrive_w(kSFree0 + sb);
+      const int n_valid = min(kT, x.t_end - (x.t_begin + i * kT));
+      float mt = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < kT; ++j) {
+        // padding rows score 0 everywhere (their Q rows hold arbitrary bytes)
+        s[j] = !live ? 0.f : (j < n_valid) ? s[j] * p.scale_log2 : -INFINITY;
+        mt = fmaxf(mt, s[j]);
+      }
+      const float m_new = (i == 0 || mt > m_used + kRescaleLog2) ? mt : m_used;
+      const float alpha = (i == 0) ? 1.f : ex2(m_used - m_new);
+      float sum = 0.f;
+      uint32_t pk[kT / 2];
+#pragma unroll
+      for (int j = 0; j < kT; j += 2) {
+        const float p0 = ex2(s[j] - m_new), p1 = ex2(s[j + 1] - m_new);
+        sum += p0;
+        sum += p1;
+        const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+        pk[j / 2] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      l = (i == 0) ? sum : fmaf(l, alpha, sum);
+      // rescale O when some head's reference value moved; the previous P.V
+      // must have landed first
+      if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        if (!wait_w(kPVDone0 + ((g - 1) & 1), ((g - 1) >> 1) & 1)) return;
+        umma::fence_after_sync();
+#pragma unroll 1
+        for (int ch = 0; ch < kD / 32; ++ch) {
+          float o[32];
+          umma::ld_32x32b_x32(lane_base + o_col + ch * 32, o);
+          umma::wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] *= alpha;
+          umma::st_32x32b_x32(lane_base + o_col + ch * 32, o);
+        }
+        umma::wait_st();
+      }
+      m_used = m_new;
+      // P row (64 bf16 = 128 bytes) over the K tile of this tile's stage, in
+      // the 128-byte-swizzled K-major layout (S(g), the K tile's only reader,
+      // has completed)
+      uint8_t* prow = c.smem + kStageOffset + (g % kStages) * kStageBytes + row * 128;
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc)
+        *reinterpret_cast<uint4*>(prow + ((cc ^ (row & 7)) << 4)) =
+            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+      fence_proxy_async();
+      umma::fence_before_sync();
+      arrive_w(kPFull0 + sb);
+    }
+    // epilogue: O / l
+    if (!warp_live) {
+      arrive_w(kOFree0 + ob);
+      continue;
+    }
+    if (!wait_w(kPVDone0 + ((g - 1) & 1), ((g - 1) >> 1) & 1)) return;
+    umma::fence_after_sync();
+    const int hq = x.h * G + row;
+    const float inv = (l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll 1
+    for (int ch = 0; ch < kD / 32; ++ch) {
+      float o[32];
+      umma::ld_32x32b_x32(lane_base + o_col + ch * 32, o);
+      umma::wait_ld();
+      if (live) {
+        if (x.single) {
+          uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)x.b * p.H_q + hq) * kD + ch * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __nv_bfloat162 h =
+                  __floats2bfloat162_rn(o[v * 8 + 2 * e] * inv, o[v * 8 + 2 * e + 1] * inv);
+              w[e] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(p.o_part + ((size_t)x.slot * p.H_q + hq) * kD +
+                                                  ch * 32);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            dst[v] = make_float4(o[4 * v] * inv, o[4 * v + 1] * inv, o[4 * v + 2] * inv,
+                                 o[4 * v + 3] * inv);
+        }
+      }
+    }
+    umma::fence_before_sync();
+    arrive_w(kOFree0 + ob);
+    if (live) {
+      const float lse2 = (l > 0.f) ? m_used + lg2(l) : -INFINITY;
+      if (x.single)
+        p.lse[(size_t)x.b * p.H_q + hq] = (l > 0.f) ? lse2 * kLn2 : -INFINITY;
+      else
+        p.lse_part[(size_t)x.slot * p.H_q + hq] = lse2;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    split_gqa_tc_kernel(Launch p, const __grid_constant__ Maps maps, int box) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  Ctx c;
+  c.smem = smem;
+  c.sbase = smem_addr(smem);
+  c.abort_flag = reinterpret_cast<volatile int*>(smem + kAbortSlot);
+  c.hdr = p.hdr;
+  const int warp = threadIdx.x >> 5;
+  wait_prior_grid();  // the plan kernel's outputs
+  allow_next_grid();
+  const int n_items = p.hdr[kHdrNWork], n_empty = p.hdr[kHdrNEmpty];
+  const int n_units = (n_items - n_empty) * p.H_kv;  // units with tiles, listed first
+  const int G = p.H_q / p.H_kv;
+  // units of empty rows (listed last): out = 0, lse = -inf
+  for (int e = n_units + blockIdx.x; e < n_items * p.H_kv; e += gridDim.x) {
+    const TcUnit x = tc_unit(p, e);  // an empty row has one split
+    for (int i = threadIdx.x; i < G * kD; i += kThreads)
+      p.out[((size_t)x.b * p.H_q + x.h * G) * kD + i] = __float2bfloat16_rn(0.f);
+    for (int i = threadIdx.x; i < G; i += kThreads)
+      p.lse[(size_t)x.b * p.H_q + x.h * G + i] = -INFINITY;
+  }
+  if ((int)blockIdx.x >= n_units) return;  // uniform across the CTA
+  if (c.sbase & 1023u) {  // the swizzled layouts need 1024-byte-aligned shared memory
+    if (threadIdx.x == 0) set_error(p.hdr, DA_DEVERR_TIMEOUT);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNumBars; ++i) {
+      uint32_t count = 1;  // tcgen05.commit or the producer's expect_tx arrive
+      if ((i >= kSFree0 && i < kSFree0 + 2) || (i >= kPFull0 && i < kPFull0 + 2) ||
+          (i >= kOFree0 && i < kOFree0 + 2))
+        count = 4;  // the four softmax warps
+      mbar_init(bar_addr(c, i), count);
+    }
+    *c.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    umma::tmem_alloc(c.sbase + kTmemSlot, kTmemCols);
+    umma::tmem_relinquish();
+  }
+  umma::fence_before_sync();
+  __syncthreads();
+  umma::fence_after_sync();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kTmemSlot);
+
+  if (warp < 4) {
+    softmax_warps(p, c, tmem, n_units);
+  } else if (warp == 4) {
+    producer(p, c, maps, n_units, box != 0);
+  } else if ((threadIdx.x & 31) == 0) {
+    mma_issuer(p, c, tmem, n_units);
+    // drain: its arrival means every MMA issued before it has completed
+    umma::commit(bar_addr(c, kDrain));
+  }
+  umma::fence_before_sync();
+  __syncthreads();
+  if (warp == 5) {
+    umma::fence_after_sync();
+    if ((threadIdx.x & 31) == 0) {
+      const uint32_t bar = bar_addr(c, kDrain);
+      const unsigned long long t0 = globaltimer_ns();
+      while (!mbar_try_wait(bar, 0)) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          set_error(p.hdr, DA_DEVERR_TIMEOUT);
+          break;
+        }
+      }
+    }
+    __syncwarp();
+    umma::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Stands in for an empty cache in a tensor map (never read by a live entry).
+__device__ __nv_bfloat16 g_zero_tile[16 * kD];
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// A bf16 map of `rank` dims (dim 0 = 128 elements of a head row), 128-byte
+// swizzle, zero fill past the bounds.
+bool encode(CUtensorMap* tm, const void* base, int rank, const cuuint64_t* dims,
+            const cuuint64_t* strides, const cuuint32_t* box) {
+  const PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  const cuuint32_t elem[3] = {1, 1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides,
+            box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int tc_ctas_per_sm() {
+  static const int n = [] {
+    if (cudaFuncSetAttribute(split_gqa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess)
+      return 1;
+    int c = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, split_gqa_tc_kernel, kThreads,
+                                                      kSmemBytes) != cudaSuccess || c < 1)
+      c = 1;
+    return c;
+  }();
+  return n;
+}
+
+}  // namespace
+
+bool gqa_tc_supported(int G, int D) { return G >= 16 && G <= kRows && D == kD; }
+
+int gqa_tc_resident_ctas(int sms) { return tc_ctas_per_sm() * sms; }
+
+cudaError_t launch_split_gqa_tc(const Launch& p, int grid, cudaStream_t stream) {
+  static const cudaError_t attr = cudaFuncSetAttribute(
+      split_gqa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (attr != cudaSuccess) return attr;
+  const int G = p.H_q / p.H_kv;
+  if (!gqa_tc_supported(G, p.D_qk) || p.D_v != kD || p.extra_k || p.kv_type != 0)
+    return cudaErrorInvalidValue;
+  const long long rows = (p.layout == DA_KV_CONTIGUOUS) ? (long long)p.B * p.width
+                         : (p.layout == DA_KV_PAGED)    ? p.num_blocks * p.page_size
+                                                        : p.num_blocks;
+  const bool box =
+      p.layout == DA_KV_CONTIGUOUS || (p.layout == DA_KV_PAGED && p.page_size % 16 == 0);
+  Maps m;
+  memset(&m, 0, sizeof m);
+  const void* kb = p.k;
+  const void* vb = p.v;
+  long long r = rows;
+  if (rows < 1) {  // an empty cache: every entry is masked, copies read zeros
+    void* z = nullptr;
+    if (cudaGetSymbolAddress(&z, g_zero_tile) != cudaSuccess) return cudaErrorInvalidValue;
+    kb = vb = z;
+    r = 1;
+  }
+  if (r * p.H_kv >= (1ll << 31)) return cudaErrorInvalidValue;  // signed TMA coordinates
+  const cuuint64_t d3[3] = {(cuuint64_t)kD, (cuuint64_t)p.H_kv, (cuuint64_t)r};
+  const cuuint64_t s3[2] = {(cuuint64_t)kD * 2, (cuuint64_t)p.H_kv * kD * 2};
+  const cuuint32_t b3[3] = {64, 1, 16};
+  const cuuint64_t d2[2] = {(cuuint64_t)kD, (cuuint64_t)(r * p.H_kv)};
+  const cuuint64_t s2[1] = {(cuuint64_t)kD * 2};
+  const cuuint32_t b2[2] = {64, 1};
+  const cuuint64_t dq[2] = {(cuuint64_t)kD, (cuuint64_t)p.B * p.H_q};
+  const cuuint32_t bq[2] = {64, (cuuint32_t)kQBoxRows};
+  if (!encode(&m.k3, kb, 3, d3, s3, b3) || !encode(&m.v3, vb, 3, d3, s3, b3) ||
+      !encode(&m.k2, kb, 2, d2, s2, b2) || !encode(&m.v2, vb, 2, d2, s2, b2) ||
+      !encode(&m.q, p.q, 2, dq, s2, bq))
+    return cudaErrorInvalidValue;
+  return launch_after(split_gqa_tc_kernel, dim3(grid), dim3(kThreads), (size_t)kSmemBytes, stream,
+                      p, m, box ? 1 : 0);
+}
+
+}  // namespace da
