@@ -360,31 +360,63 @@ def nvfp4_section(api, peak, sizes=(1, 32, 33, 256), reps=30):
 
 # ----------------------------------------------------------------- CPU oracle
 
-def invariance_sweep(api, sizes=(1, 2, 4, 8, 16, 32, 64, 128), steps=10):
+def time_plan(case, steps):
+    """Device time (ms) of the plan kernel alone: `steps` plan calls captured
+    in one CUDA graph (so host-side call overhead is not timed), replayed
+    between CUDA events."""
+    a, w = case.api, case.wl
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            a.plan(case.prob, case.policy, w.lengths, case.ws)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(steps):
+            a.plan(case.prob, case.policy, w.lengths, case.ws)
+    graph.replay()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    del graph
+    return e0.elapsed_time(e1) / steps
+
+
+def invariance_sweep(api, sizes=(1, 2, 4, 8, 16, 32, 64, 128, 256), steps=10):
     """The ragged sweep's target row (length 4096, GQA 32/8, d = 128) at a random
     position among log-uniform batchmates, against its solo run, under each
     policy: how many batches move any bit of its output or LSE, the largest
-    output difference, and the step time of every batch (the occupancy cost
-    of the per-row split rule on ragged batches)."""
+    output difference, the step time of every batch (the occupancy cost of
+    the per-row split rule on ragged batches) and the plan kernel's own time."""
     from invariant_decode_attention_gb300 import workloads as W
     sweep = W.RaggedSweep(sizes)
     res = {"batch_sizes": list(sizes)}
     for name, pol in (("invariant", api.INVARIANT), ("balanced", api.BALANCED)):
         o_solo, l_solo = api.run_workload(sweep.solo(), policy=pol)
-        moved, max_abs, ms, gbs = 0, 0.0, [], []
+        moved, max_abs, ms, gbs, plan_ms = 0, 0.0, [], [], []
         for i in range(len(sizes)):
             wl, pos = sweep.batch(i)
             case = GpuCase(wl, wl.q.device, pol)  # already on the device: no copy
             tot, _, _ = time_steps(case, steps, 3, split_events=False)
             ms.append(round(tot / steps, 5))
             gbs.append(round(wl.kv_bytes() / (tot / steps * 1e-3) / 1e9, 1))
+            plan_ms.append(round(time_plan(case, steps), 5))
             o, l = case.out, case.lse
             same = torch.equal(o[pos], o_solo[0]) and torch.equal(l[pos], l_solo[0])
             moved += 0 if same else 1
             max_abs = max(max_abs, (o[pos].float() - o_solo[0].float()).abs().max().item())
             del case
         res[name] = {"batches_moving_target_row": moved, "batches": len(sizes),
-                     "max_absdiff_out": max_abs, "ms_per_step": ms, "kv_gbs": gbs}
+                     "max_absdiff_out": max_abs, "ms_per_step": ms, "kv_gbs": gbs,
+                     "plan_ms": plan_ms}
+    res["invariant_over_balanced_time"] = [
+        round(a / b, 4) for a, b in zip(res["invariant"]["ms_per_step"],
+                                        res["balanced"]["ms_per_step"])]
     del sweep
     torch.cuda.empty_cache()
     return res

@@ -279,7 +279,7 @@ static int plan_impl(const da_problem* prob, int32_t policy, const int32_t* d_le
   P.tile_tokens = v.tile;
   P.min_tiles_per_split = v.min_tps;
   P.max_splits = v.max_splits;
-  P.num_parts = (int)(slots / per_item > 0 ? slots / per_item : 1);
+  P.num_parts = (int)(slots / per_item > 0 ? kBalancedPartsPerSlot * (slots / per_item) : 1);
   P.fixed_overhead = kBalancedFixedOverhead;
   P.grid = (int)(max_units < slots ? (max_units > 0 ? max_units : 1) : slots);
   P.device = dev;

@@ -31,8 +31,11 @@ constexpr int kTcTile = 64;
 constexpr int kTcMinTilesPerSplit = 16;
 constexpr int kTcMaxSplits = 64;
 
-// BALANCED quota: tiles charged per split on top of its own tiles.
+// BALANCED quota: tiles charged per split on top of its own tiles, and parts
+// the quota divides the batch into per set of CTAs that run one item at once
+// (four: every CTA takes several items, so placement can even out the parts).
 constexpr int kBalancedFixedOverhead = 2;
+constexpr int kBalancedPartsPerSlot = 4;
 
 // Header words at the start of the workspace.
 constexpr int kHdrError = 0;  // DA_DEVERR_* bits

@@ -145,73 +145,99 @@ __global__ void __launch_bounds__(kPlanThreads) plan_invariant_kernel(PlanLaunch
   }
 }
 
-// One thread: the packing is sequential by definition (each row's cuts depend
-// on how full the current part is after every earlier row).
-__global__ void plan_balanced_kernel(PlanLaunch p) {
+// BALANCED, as the page's scheduler does it: the batch-wide total by a
+// block reduction, then the greedy walk over the rows -- sequential by
+// definition, each row's cuts depend on how full the current part is after
+// every earlier row -- by one thread over tile counts staged in shared
+// memory, then every item placed in parallel.
+constexpr int kBalancedSmemRows = 8192;  // rows whose tile counts fit in shared memory
+
+__global__ void __launch_bounds__(kPlanThreads) plan_balanced_kernel(PlanLaunch p) {
+  __shared__ int bucket[kSortKeys];
+  __shared__ int tiles_s[kBalancedSmemRows];
+  __shared__ long long red[kPlanThreads / 32];
   allow_next_grid();
-  if (threadIdx.x != 0) return;
-  p.hdr[kHdrError] = 0;
-  p.hdr[kHdrQueue] = 0;
-  p.hdr[kHdrExits] = 0;
+  if (threadIdx.x == 0) {
+    p.hdr[kHdrError] = 0;
+    p.hdr[kHdrQueue] = 0;
+    p.hdr[kHdrExits] = 0;
+  }
+  for (int k = threadIdx.x; k < kSortKeys; k += kPlanThreads) bucket[k] = 0;
   const int stride = p.max_splits + 1;
   const int ovh = p.fixed_overhead;
-  long long total = 0;
-  for (int b = 0; b < p.B; ++b) total += ceil_div_i(row_length(p, b), p.tile) + ovh;
-  const int parts = max(1, p.num_parts);
-  const long long payload = (total / parts + (total % parts != 0)) + ovh;
-  long long room = payload;
-  int n_work = 0;
-  for (int b = 0; b < p.B; ++b) {
-    const int n_tiles = ceil_div_i(row_length_quiet(p, b), p.tile);
-    int32_t* sb = p.split_begin + (size_t)b * stride;
-    int n_cuts = 1;  // entries written to sb so far
-    sb[0] = 0;
-    long long begin = 0;
-    for (;;) {
-      const long long rest = n_tiles - begin;
-      if (rest + ovh <= room) {  // the rest of the row fits in this part
-        room -= rest + ovh;
-        break;
+  const bool in_smem = p.B <= kBalancedSmemRows;
+  // every row's tile count (kept in n_splits until the walk overwrites it)
+  long long part = 0;
+  for (int b = threadIdx.x; b < p.B; b += kPlanThreads) {
+    const int n = ceil_div_i(row_length(p, b), p.tile);
+    if (in_smem) tiles_s[b] = n;
+    p.n_splits[b] = n;
+    part += n + ovh;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = part;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    long long total = 0;
+    for (int w = 0; w < kPlanThreads / 32; ++w) total += red[w];
+    const int parts = max(1, p.num_parts);
+    const long long payload = (total / parts + (total % parts != 0)) + ovh;
+    long long room = payload;
+    for (int b = 0; b < p.B; ++b) {
+      const int n_tiles = in_smem ? tiles_s[b] : p.n_splits[b];
+      int32_t* sb = p.split_begin + (size_t)b * stride;
+      int n_cuts = 1;  // entries written to sb so far
+      sb[0] = 0;
+      long long begin = 0;
+      for (;;) {
+        const long long rest = n_tiles - begin;
+        if (rest + ovh <= room) {  // the rest of the row fits in this part
+          room -= rest + ovh;
+          break;
+        }
+        const long long take = room - ovh;
+        if (take > 0 && n_cuts < p.max_splits) {  // fill the part, cut the row
+          begin += take;
+          sb[n_cuts++] = (int)begin;
+        }
+        room = payload;  // open a new part
+        if (n_cuts == p.max_splits) {  // no splits left: the last one takes the rest
+          room = room - (n_tiles - begin) - ovh;
+          if (room < 0) room = 0;
+          break;
+        }
       }
-      const long long take = room - ovh;
-      if (take > 0 && n_cuts < p.max_splits) {  // fill the part, cut the row
-        begin += take;
-        sb[n_cuts++] = (int)begin;
-      }
-      room = payload;  // open a new part
-      if (n_cuts == p.max_splits) {  // no splits left: the last one takes the rest
-        room = room - (n_tiles - begin) - ovh;
-        if (room < 0) room = 0;
-        break;
-      }
+      sb[n_cuts] = n_tiles;
+      p.n_splits[b] = n_cuts;
     }
-    sb[n_cuts] = n_tiles;
-    p.n_splits[b] = n_cuts;
-    n_work += n_cuts;
   }
-  p.hdr[kHdrNWork] = n_work;
-  // work list: largest items first, rows and splits in order within a key
-  // (a stable counting sort; placement only, as for INVARIANT)
-  __shared__ int start[kSortKeys];
-  for (int k = 0; k < kSortKeys; ++k) start[k] = 0;
-  for (int b = 0; b < p.B; ++b) {
+  __syncthreads();
+  // count the items per key, then bucket starts, largest key first
+  for (int b = threadIdx.x; b < p.B; b += kPlanThreads) {
+    const int n = p.n_splits[b];
     const int32_t* sb = p.split_begin + (size_t)b * stride;
-    for (int s = 0; s < p.n_splits[b]; ++s) ++start[sort_key(sb[s + 1] - sb[s])];
+    for (int s = 0; s < n; ++s) atomicAdd(&bucket[sort_key(sb[s + 1] - sb[s])], 1);
   }
-  int acc = 0;
-  for (int k = kSortKeys - 1; k >= 0; --k) {
-    const int c = start[k];
-    start[k] = acc;
-    acc += c;
+  __syncthreads();
+  {
+    const int key = kSortKeys - 1 - (int)threadIdx.x;
+    const int count = (key >= 0) ? bucket[key] : 0;
+    int total;
+    const int start = block_exclusive_scan(count, &total);
+    if (key >= 0) bucket[key] = start;
+    if (key == 0) p.hdr[kHdrNEmpty] = count;  // items with no tiles: key 0, listed last
+    if (threadIdx.x == 0) p.hdr[kHdrNWork] = total;
   }
-  p.hdr[kHdrNEmpty] = n_work - start[0];  // items with no tiles: key 0, listed last
-  for (int b = 0; b < p.B; ++b) {
+  __syncthreads();
+  // place every item in its bucket (order within a bucket is free: placement only)
+  for (int b = threadIdx.x; b < p.B; b += kPlanThreads) {
     const int n = p.n_splits[b];
     const int32_t* sb = p.split_begin + (size_t)b * stride;
     const int Lc = row_length_quiet(p, b);
     for (int s = 0; s < n; ++s) {
       const int slot = b * p.max_splits + s;
-      const int pos = start[sort_key(sb[s + 1] - sb[s])]++;
+      const int pos = atomicAdd(&bucket[sort_key(sb[s + 1] - sb[s])], 1);
       reinterpret_cast<int4*>(p.item_desc)[pos] =
           make_int4(n == 1 ? ~slot : slot, sb[s], sb[s + 1], Lc);
       p.work[pos] = slot;
@@ -223,7 +249,7 @@ __global__ void plan_balanced_kernel(PlanLaunch p) {
 
 cudaError_t launch_plan(const PlanLaunch& p, cudaStream_t stream) {
   if (p.policy == DA_POLICY_BALANCED) {
-    plan_balanced_kernel<<<1, 32, 0, stream>>>(p);
+    plan_balanced_kernel<<<1, kPlanThreads, 0, stream>>>(p);
   } else {
     plan_invariant_kernel<<<1, kPlanThreads, 0, stream>>>(p);
   }

@@ -30,9 +30,10 @@
 // and entries whose page or slot is out of range, copy cache row 0 instead
 // (their scores are masked), so no stage byte is ever uninitialised.
 //
-// Roles (192 threads): warps 0-3 softmax and epilogue; warp 4 producer (page
-// or index lookups one tile ahead, TMA issue); warp 5 MMA issue (one
-// thread) and TMEM allocation.  Every mbarrier wait is bounded; on time-out
+// Roles (320 threads): warps 0-3 softmax; warps 4-7 epilogue (a unit's O
+// merge and output while the softmax warps go on with the next unit); warp 8
+// producer (page or index lookups ahead of the copies, TMA issue); warp 9 MMA
+// issue (one thread) and TMEM allocation.  Every mbarrier wait is bounded; on time-out
 // the kernel records DA_DEVERR_TIMEOUT, every role leaves its loop,
 // outstanding tensor-core work is drained (bounded) and TMEM is freed.
 //
@@ -63,15 +64,20 @@ constexpr int kBarOffset = kStageOffset + kStages * kStageBytes;
 enum {
   kFull0 = 0, kEmpty0 = kFull0 + kStages, kQFull0 = kEmpty0 + kStages, kQFree0 = kQFull0 + 2,
   kSFull0 = kQFree0 + 2, kSFree0 = kSFull0 + 2, kPFull0 = kSFree0 + 2, kPVDone0 = kPFull0 + 2,
-  kOFree0 = kPVDone0 + 2, kDrain = kOFree0 + 2, kNumBars
+  kODone0 = kPVDone0 + 2, kEpiReady0 = kODone0 + 2, kOFree0 = kEpiReady0 + 2,
+  kDrain = kOFree0 + 2, kNumBars
 };
 constexpr int kTmemSlot = kBarOffset + kNumBars * 8;
 constexpr int kAbortSlot = kTmemSlot + 4;
-constexpr int kSmemBytes = kAbortSlot + 12;
+// m and l of every row, per O buffer (softmax -> epilogue), then the
+// epilogue's merge scratch: one 32-column chunk of every row's O (rows padded
+// to 33 floats)
+constexpr int kMergeOffset = (kAbortSlot + 4 + 15) / 16 * 16;
+constexpr int kSmemBytes = kMergeOffset + (2 * 2 * kRows + kRows * 33) * 4;
 static_assert(kStageOffset % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle atoms 1024-aligned");
 static_assert(kSmemBytes <= 232448, "fits the 227 KB per-block limit");
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSCol = 0;    // S buffers [0, 64) and [64, 128)
 constexpr uint32_t kOCol = 128;  // O accumulators [128, 256) and [256, 384)
@@ -167,38 +173,37 @@ __device__ __forceinline__ TcUnit tc_unit(const Launch& p, int u) {
 }
 
 // ---------------------------------------------------------------- producer
-// Warp 4.  Box path: lane j < 4 owns the 16-entry group j of each tile;
-// gather path: lane j < 16 owns the 4-entry group j.  A lane loads the table
-// word(s) of its group one tile ahead of the copies that use them.
-__device__ void producer(const Launch& p, const Ctx& c, const Maps& m, int n_units, bool box) {
+// Warp 4.  Box path: a tile's 16-entry group j is copied by one lane; the
+// page words of a unit's tiles are loaded eight tiles at a time, a batch
+// ahead of the copies that use them (lane l holds the word of group l % 4 of
+// tile l / 4 of the batch), and the next unit's descriptor and first batch
+// are loaded during the current unit, so the copies never wait on a lookup.
+// Gather path: lane j < 16 owns the 4-entry group j of each tile, its words
+// loaded one tile ahead.
+__device__ void producer(const Launch& p, const Ctx& c, const Maps& m, int n_units, bool box,
+                         int R) {
   const int lane = threadIdx.x & 31;
   const int G = p.H_q / p.H_kv;
   const int q_boxes = (G + kQBoxRows - 1) / kQBoxRows;
-  const int per = box ? 16 : 4;             // entries per lane-group
-  const int groups = kT / per;              // 4 or 16
+  const int gp = kRows / R;  // rows per copy of the group
   uint32_t g = 0, nq = 0;
   bool bad = false;
-  // cache row of entry `tok` of row b (paged: from the page word), or -1
-  // when the entry is past the split or its page / slot is out of range
+  // table word holding entry `tok` (0 past the split or for a contiguous cache)
   auto word_of = [&](const TcUnit& x, int tok) -> int {
     if (tok >= x.t_end || p.layout == DA_KV_CONTIGUOUS) return 0;
     if (p.layout == DA_KV_PAGED) return __ldg(p.table + (size_t)x.b * p.width + tok / p.page_size);
     return __ldg(p.table + (size_t)x.b * p.width + tok);
   };
+  // cache row of entry `tok`, or -1 when the entry is past the split or its
+  // page / slot is out of range
   auto row_of = [&](const TcUnit& x, int tok, int word) -> long long {
     if (tok >= x.t_end) return -1;
     if (p.layout == DA_KV_CONTIGUOUS) return (long long)x.b * p.width + tok;
-    if (p.layout == DA_KV_PAGED) {
-      if (word < 0 || word >= p.num_blocks) {
-        bad = true;
-        return -1;
-      }
-      return (long long)word * p.page_size + tok % p.page_size;
-    }
     if (word < 0 || word >= p.num_blocks) {
       bad = true;
       return -1;
     }
+    if (p.layout == DA_KV_PAGED) return (long long)word * p.page_size + tok % p.page_size;
     return word;
   };
   auto wait_w = [&](int bar, uint32_t parity) -> bool {
@@ -206,37 +211,50 @@ __device__ void producer(const Launch& p, const Ctx& c, const Maps& m, int n_uni
     if (lane == 0) ok = wait_bar(c, bar, parity) ? 1 : 0;
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
   };
+  // box path: the word of lane l for batch `bt` (tiles 8 bt .. 8 bt + 7) of unit x
+  auto batch_word = [&](const TcUnit& x, int bt) -> int {
+    return word_of(x, x.t_begin + (8 * bt + (lane >> 2)) * kT + (lane & 3) * 16);
+  };
   bool alive = true;
+  TcUnit x = tc_unit(p, blockIdx.x);  // blockIdx.x < n_units (the kernel checked)
+  int w_first = box ? batch_word(x, 0) : 0;
   for (int u = blockIdx.x; u < n_units && alive; u += gridDim.x, ++nq) {
-    const TcUnit x = tc_unit(p, u);
+    const int u_next = u + (int)gridDim.x;
+    const bool has_next = u_next < n_units;
+    const TcUnit xn = has_next ? tc_unit(p, u_next) : x;  // in flight during this unit
+    const int n_sub = (x.t_end - x.t_begin + kT - 1) / kT;
     // Q of the unit's heads into Q buffer nq & 1 once the unit that used it
     // last has finished its S MMAs
     const int qb = nq & 1;
     if (!wait_w(kQFree0 + qb, ((nq >> 1) & 1) ^ 1)) break;
     if (lane == 0) {
       const uint32_t qfull = bar_addr(c, kQFull0 + qb);
-      mbar_arrive_expect_tx(qfull, q_boxes * 2 * kQBoxRows * 128);
+      mbar_arrive_expect_tx(qfull, R * q_boxes * 2 * kQBoxRows * 128);
       const uint32_t qdst = c.sbase + qb * kQBytes;
-      for (int rb = 0; rb < q_boxes; ++rb)
-        for (int half = 0; half < 2; ++half)
-          tma_box2(qdst + half * kQRegion + rb * kQBoxRows * 128, &m.q, 64 * half,
-                   x.b * p.H_q + x.h * G + rb * kQBoxRows, qfull);
+      for (int cp = 0; cp < R; ++cp)  // every copy of the group's rows
+        for (int rb = 0; rb < q_boxes; ++rb)
+          for (int half = 0; half < 2; ++half)
+            tma_box2(qdst + half * kQRegion + (cp * gp + rb * kQBoxRows) * 128, &m.q, 64 * half,
+                     x.b * p.H_q + x.h * G + rb * kQBoxRows, qfull);
     }
-    // this lane's group of the first tile
-    int word = (lane < groups) ? word_of(x, x.t_begin + lane * per) : 0;
-    int words4[4] = {0, 0, 0, 0};
-    if (!box && lane < groups)
-      for (int i = 0; i < 4; ++i) words4[i] = word_of(x, x.t_begin + lane * per + i);
-    for (int t0 = x.t_begin; t0 < x.t_end; t0 += kT, ++g) {
+    int w_cur = w_first, w_nxt = 0, w_n0 = 0;
+    if (box && n_sub > 8) w_nxt = batch_word(x, 1);
+    // gather path: this lane's four words of the current and the next tile
+    int wg[4] = {0, 0, 0, 0}, wg_n[4] = {0, 0, 0, 0};
+    if (!box && lane < 16)
+      for (int i = 0; i < 4; ++i) wg[i] = word_of(x, x.t_begin + lane * 4 + i);
+    const int last_batch = (n_sub - 1) / 8;
+    for (int i = 0; i < n_sub; ++i, ++g) {
+      const int t0 = x.t_begin + i * kT;
       const int st = g % kStages;
-      // the next tile's words, loaded before this tile's copies are issued
-      int nword = 0, nwords4[4] = {0, 0, 0, 0};
-      const int t1 = t0 + kT;
-      if (t1 < x.t_end && lane < groups) {
-        if (box)
-          nword = word_of(x, t1 + lane * per);
-        else
-          for (int i = 0; i < 4; ++i) nwords4[i] = word_of(x, t1 + lane * per + i);
+      if (box) {
+        if (i > 0 && (i & 7) == 0) {  // next batch: its words were loaded a batch ago
+          w_cur = w_nxt;
+          if ((i >> 3) + 1 <= last_batch) w_nxt = batch_word(x, (i >> 3) + 1);
+        }
+        if (i == 8 * last_batch && has_next) w_n0 = batch_word(xn, 0);  // the next unit's
+      } else if (lane < 16 && t0 + kT < x.t_end) {
+        for (int k = 0; k < 4; ++k) wg_n[k] = word_of(x, t0 + kT + lane * 4 + k);
       }
       if (!wait_w(kEmpty0 + st, ((g / kStages) & 1) ^ 1)) {
         alive = false;
@@ -247,32 +265,33 @@ __device__ void producer(const Launch& p, const Ctx& c, const Maps& m, int n_uni
       __syncwarp();
       const uint32_t kdst = c.sbase + kStageOffset + st * kStageBytes;
       const uint32_t vdst = kdst + kTileBytes;
-      if (lane < groups) {
-        if (box) {
-          const int tok = t0 + lane * per;
-          long long r = row_of(x, tok, word);
+      if (box) {
+        if ((lane >> 2) == (i & 7)) {
+          const int grp = lane & 3;
+          long long r = row_of(x, t0 + grp * 16, w_cur);
           if (r < 0) r = 0;
           for (int half = 0; half < 2; ++half) {
-            const uint32_t off = half * kRegion + lane * per * 128;
+            const uint32_t off = half * kRegion + grp * 16 * 128;
             tma_box3(kdst + off, &m.k3, 64 * half, x.h, (int)r, full);
             tma_box3(vdst + off, &m.v3, 64 * half, x.h, (int)r, full);
           }
-        } else {
-          int rr[4];
-          for (int i = 0; i < 4; ++i) {
-            const long long r = row_of(x, t0 + lane * per + i, words4[i]);
-            rr[i] = (int)((r < 0 ? 0 : r) * p.H_kv + x.h);
-          }
-          for (int half = 0; half < 2; ++half) {
-            const uint32_t off = half * kRegion + lane * per * 128;
-            tma_gather4(kdst + off, &m.k2, 64 * half, rr[0], rr[1], rr[2], rr[3], full);
-            tma_gather4(vdst + off, &m.v2, 64 * half, rr[0], rr[1], rr[2], rr[3], full);
-          }
         }
+      } else if (lane < 16) {
+        int rr[4];
+        for (int k = 0; k < 4; ++k) {
+          const long long r = row_of(x, t0 + lane * 4 + k, wg[k]);
+          rr[k] = (int)((r < 0 ? 0 : r) * p.H_kv + x.h);
+        }
+        for (int half = 0; half < 2; ++half) {
+          const uint32_t off = half * kRegion + lane * 4 * 128;
+          tma_gather4(kdst + off, &m.k2, 64 * half, rr[0], rr[1], rr[2], rr[3], full);
+          tma_gather4(vdst + off, &m.v2, 64 * half, rr[0], rr[1], rr[2], rr[3], full);
+        }
+        for (int k = 0; k < 4; ++k) wg[k] = wg_n[k];
       }
-      word = nword;
-      for (int i = 0; i < 4; ++i) words4[i] = nwords4[i];
     }
+    x = xn;
+    w_first = w_n0;
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(p.hdr, DA_DEVERR_INDEX);
   // leave no copy in flight into this CTA's shared memory (on the normal path
@@ -346,17 +365,37 @@ __device__ void mma_issuer(const Launch& p, const Ctx& c, uint32_t tmem, int n_u
       if (i > 0 && !pv(g - 1, i == 1)) return;
     }
     if (!pv(g - 1, n_sub == 1)) return;
+    umma::commit(bar_addr(c, kODone0 + ob));  // the unit's O is complete
   }
 }
 
 // ---------------------------------------------------------------- softmax + epilogue
+// The group's heads are held R = 128 / Gp times in the MMA rows (Gp = the
+// power of two >= G, at least 16): row r is head r % Gp of copy r / Gp.  The
+// tensor cores compute every row's scores for the whole tile anyway; copy c
+// takes only entries [64c/R, 64(c+1)/R) of each tile (its P row is zero
+// elsewhere), so a thread's softmax work per tile is 64/R entries and the
+// copies run on all four warps.  Each row keeps its own running reference
+// value and sum; at the unit's end the R copies of a head are merged in copy
+// order, the combine arithmetic of the split/merge step:
+//     M = max_c m_c,  L = sum_c 2^(m_c - M) l_c,  O = sum_c 2^(m_c - M) O_c / L.
+// All of it depends only on the unit's own data.
+template <int R>
 __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int n_units) {
+  constexpr int kGp = kRows / R;              // rows per copy
+  constexpr int kCpt = kT / R;                // entries of a tile per copy
+  constexpr int kCopiesPerWarp = kGp < 32 ? 32 / kGp : 1;
+  constexpr int kWarpCols = kCopiesPerWarp * kCpt;  // columns a warp loads from S
+  static_assert(kWarpCols == 16 || kWarpCols == 32 || kWarpCols == 64, "load shapes");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = threadIdx.x;  // head of the group = TMEM lane
+  const int row = threadIdx.x;  // TMEM lane
+  const int cp = row / kGp, j = row % kGp;
   const int G = p.H_q / p.H_kv;
-  const bool live = row < G;              // rows past the group are never written
-  const bool warp_live = warp * 32 < G;   // a warp of padding rows only keeps time
+  const bool live = j < G;  // rows past the group compute but are never written
+  const int wcol0 = (warp * 32 / kGp) * kCpt;  // first S column this warp loads
+  const int col0 = cp * kCpt;                  // first entry of the tile this row takes
   const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+  float* ml = reinterpret_cast<float*>(c.smem + kMergeOffset);  // [2 buffers][m, l][128]
   uint32_t g = 0, nq = 0;
   auto wait_w = [&](int bar, uint32_t parity) -> bool {
     int ok = 1;
@@ -376,45 +415,52 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
     for (int i = 0; i < n_sub; ++i, ++g) {
       const int sb = g & 1;
       if (!wait_w(kSFull0 + sb, (g >> 1) & 1)) return;
-      if (!warp_live) {  // its P rows keep the stage's (finite) K bytes
-        arrive_w(kSFree0 + sb);
-        arrive_w(kPFull0 + sb);
-        continue;
-      }
       umma::fence_after_sync();
-      float s[kT];
+      float s[kCpt];
       {
-        float s_hi[32];
-        umma::ld_32x32b_x32(lane_base + kSCol + sb * kT, *reinterpret_cast<float(*)[32]>(s));
-        umma::ld_32x32b_x32(lane_base + kSCol + sb * kT + 32, s_hi);
+        float w[kWarpCols];
+        const uint32_t a = lane_base + kSCol + sb * kT + wcol0;
+        if constexpr (kWarpCols == 16) {
+          umma::ld_32x32b_x16(a, w);
+        } else if constexpr (kWarpCols == 32) {
+          umma::ld_32x32b_x32(a, w);
+        } else {
+          umma::ld_32x32b_x32(a, *reinterpret_cast<float(*)[32]>(w));
+          umma::ld_32x32b_x32(a + 32, *reinterpret_cast<float(*)[32]>(w + 32));
+        }
         umma::wait_ld();
+        const bool upper = kCopiesPerWarp == 2 && lane >= 16;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) s[32 + j] = s_hi[j];
+        for (int k = 0; k < kCpt; ++k) s[k] = upper ? w[kCpt + k] : w[k];
       }
       umma::fence_before_sync();
       arrive_w(kSFree0 + sb);
-      const int n_valid = min(kT, x.t_end - (x.t_begin + i * kT));
+      const int n_valid = min(kT, x.t_end - (x.t_begin + i * kT)) - col0;
       float mt = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < kT; ++j) {
+      for (int k = 0; k < kCpt; ++k) {
         // padding rows score 0 everywhere (their Q rows hold arbitrary bytes)
-        s[j] = !live ? 0.f : (j < n_valid) ? s[j] * p.scale_log2 : -INFINITY;
-        mt = fmaxf(mt, s[j]);
+        s[k] = !live ? 0.f : (k < n_valid) ? s[k] * p.scale_log2 : -INFINITY;
+        mt = fmaxf(mt, s[k]);
       }
-      const float m_new = (i == 0 || mt > m_used + kRescaleLog2) ? mt : m_used;
-      const float alpha = (i == 0) ? 1.f : ex2(m_used - m_new);
+      // the reference value moves on the row's first scores and when a score
+      // exceeds it by more than 2^8
+      const bool move = mt > m_used + kRescaleLog2 || (m_used == -INFINITY && mt > -INFINITY);
+      const float m_new = move ? mt : m_used;
+      const float alpha = (move && m_used > -INFINITY) ? ex2(m_used - m_new) : 1.f;
       float sum = 0.f;
-      uint32_t pk[kT / 2];
+      uint32_t pk[kCpt / 2];
 #pragma unroll
-      for (int j = 0; j < kT; j += 2) {
-        const float p0 = ex2(s[j] - m_new), p1 = ex2(s[j + 1] - m_new);
+      for (int k = 0; k < kCpt; k += 2) {
+        const float p0 = (m_new == -INFINITY) ? 0.f : ex2(s[k] - m_new);
+        const float p1 = (m_new == -INFINITY) ? 0.f : ex2(s[k + 1] - m_new);
         sum += p0;
         sum += p1;
         const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-        pk[j / 2] = *reinterpret_cast<const uint32_t*>(&h);
+        pk[k / 2] = *reinterpret_cast<const uint32_t*>(&h);
       }
-      l = (i == 0) ? sum : fmaf(l, alpha, sum);
-      // rescale O when some head's reference value moved; the previous P.V
+      l = fmaf(l, alpha, sum);
+      // rescale the row's O when its reference value moved; the previous P.V
       // must have landed first
       if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         if (!wait_w(kPVDone0 + ((g - 1) & 1), ((g - 1) >> 1) & 1)) return;
@@ -425,74 +471,138 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
           umma::ld_32x32b_x32(lane_base + o_col + ch * 32, o);
           umma::wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] *= alpha;
+          for (int k = 0; k < 32; ++k) o[k] *= alpha;
           umma::st_32x32b_x32(lane_base + o_col + ch * 32, o);
         }
         umma::wait_st();
       }
       m_used = m_new;
-      // P row (64 bf16 = 128 bytes) over the K tile of this tile's stage, in
-      // the 128-byte-swizzled K-major layout (S(g), the K tile's only reader,
-      // has completed)
+      // P row (64 bf16 = 128 bytes: this copy's entries, zeros elsewhere) over
+      // the K tile of this tile's stage, in the 128-byte-swizzled K-major
+      // layout (S(g), the K tile's only reader, has completed)
       uint8_t* prow = c.smem + kStageOffset + (g % kStages) * kStageBytes + row * 128;
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc)
-        *reinterpret_cast<uint4*>(prow + ((cc ^ (row & 7)) << 4)) =
-            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+      for (int cc = 0; cc < 8; ++cc) {
+        uint4 v = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int q = 0; q < kCpt / 8; ++q)
+          if (cc == col0 / 8 + q) v = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        *reinterpret_cast<uint4*>(prow + ((cc ^ (row & 7)) << 4)) = v;
+      }
       fence_proxy_async();
       umma::fence_before_sync();
       arrive_w(kPFull0 + sb);
     }
-    // epilogue: O / l
-    if (!warp_live) {
-      arrive_w(kOFree0 + ob);
-      continue;
-    }
-    if (!wait_w(kPVDone0 + ((g - 1) & 1), ((g - 1) >> 1) & 1)) return;
+    // hand the rows' (m, l) to the epilogue warps once the epilogue of the
+    // unit that used this O buffer before has read its own
+    if (!wait_w(kOFree0 + ob, ((nq >> 1) & 1) ^ 1)) return;
+    ml[ob * 2 * kRows + row] = m_used;
+    ml[ob * 2 * kRows + kRows + row] = l;
+    arrive_w(kEpiReady0 + ob);
+  }
+}
+
+// ---------------------------------------------------------------- epilogue
+// Warps 4-7 (warp 4 + q reads TMEM lanes 32q .. 32q + 31, the rows of softmax
+// warp q).  Per unit: merge the R copies of each head in copy order,
+//     M = max_c m_c,  L = sum_c 2^(m_c - M) l_c,  O = sum_c 2^(m_c - M) O_c,
+// and write O / L (bf16 output of a single-split row, else the fp32 partial
+// and its LSE in log2 units).  Thread t of the group, for each 32-column
+// chunk, sums the R copies of head t % Gp over 32/R of the columns.
+template <int R>
+__device__ void epilogue_warps(const Launch& p, const Ctx& c, uint32_t tmem, int n_units) {
+  constexpr int kGp = kRows / R;
+  constexpr int kCols = 32 / R;  // columns of a chunk a thread sums
+  const int q = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
+  const int row = q * 32 + lane;  // TMEM lane = row of the MMA
+  const int G = p.H_q / p.H_kv;
+  const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+  const float* ml = reinterpret_cast<const float*>(c.smem + kMergeOffset);
+  float* ob_s = reinterpret_cast<float*>(c.smem + kMergeOffset) + 2 * 2 * kRows;  // [128][33]
+  const int jt = row % kGp, kq = row / kGp;  // the head and column slice this thread sums
+  uint32_t nq = 0;
+  auto wait_w = [&](int bar, uint32_t parity) -> bool {
+    int ok = 1;
+    if (lane == 0) ok = wait_bar(c, bar, parity) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+  };
+  for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++nq) {
+    const TcUnit x = tc_unit(p, u);
+    const int ob = nq & 1;
+    if (!wait_w(kEpiReady0 + ob, (nq >> 1) & 1)) return;
+    if (!wait_w(kODone0 + ob, (nq >> 1) & 1)) return;
     umma::fence_after_sync();
-    const int hq = x.h * G + row;
-    const float inv = (l > 0.f) ? 1.f / l : 0.f;
+    const float* m_s = ml + ob * 2 * kRows;
+    const float* l_s = m_s + kRows;
+    const uint32_t o_col = kOCol + ob * kD;
+    // the merged (M, L) of head jt; this row's weight in it
+    float M = -INFINITY, L = 0.f;
+#pragma unroll
+    for (int cq = 0; cq < R; ++cq) M = fmaxf(M, m_s[cq * kGp + jt]);
+#pragma unroll
+    for (int cq = 0; cq < R; ++cq) {
+      const float mq = m_s[cq * kGp + jt];
+      L += (mq == -INFINITY) ? 0.f : ex2(mq - M) * l_s[cq * kGp + jt];
+    }
+    // this row is copy kq of head jt: its weight in the head's merge
+    const float m_row = m_s[row];
+    const float f = (m_row == -INFINITY) ? 0.f : ex2(m_row - M);
+    const bool writer = jt < G;
+    const int hq = x.h * G + jt;
+    const float inv = (L > 0.f) ? 1.f / L : 0.f;
 #pragma unroll 1
     for (int ch = 0; ch < kD / 32; ++ch) {
       float o[32];
       umma::ld_32x32b_x32(lane_base + o_col + ch * 32, o);
       umma::wait_ld();
-      if (live) {
+      float v[kCols];
+      if constexpr (R == 1) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] = o[k];
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) ob_s[row * 33 + k] = o[k] * f;
+        named_bar_sync(1, 128);
+#pragma unroll
+        for (int k = 0; k < kCols; ++k) {
+          float a = ob_s[jt * 33 + kq * kCols + k];
+#pragma unroll
+          for (int cq = 1; cq < R; ++cq) a += ob_s[(cq * kGp + jt) * 33 + kq * kCols + k];
+          v[k] = a;
+        }
+        named_bar_sync(1, 128);
+      }
+      if (writer) {
+        const int d0 = ch * 32 + kq * kCols;
         if (x.single) {
-          uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)x.b * p.H_q + hq) * kD + ch * 32);
+          uint32_t* dst = reinterpret_cast<uint32_t*>(p.out + ((size_t)x.b * p.H_q + hq) * kD + d0);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const __nv_bfloat162 h =
-                  __floats2bfloat162_rn(o[v * 8 + 2 * e] * inv, o[v * 8 + 2 * e + 1] * inv);
-              w[e] = *reinterpret_cast<const uint32_t*>(&h);
-            }
-            dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+          for (int k = 0; k < kCols; k += 2) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(v[k] * inv, v[k + 1] * inv);
+            dst[k / 2] = *reinterpret_cast<const uint32_t*>(&h);
           }
         } else {
-          float4* dst = reinterpret_cast<float4*>(p.o_part + ((size_t)x.slot * p.H_q + hq) * kD +
-                                                  ch * 32);
+          float4* dst = reinterpret_cast<float4*>(p.o_part + ((size_t)x.slot * p.H_q + hq) * kD + d0);
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            dst[v] = make_float4(o[4 * v] * inv, o[4 * v + 1] * inv, o[4 * v + 2] * inv,
-                                 o[4 * v + 3] * inv);
+          for (int k = 0; k < kCols; k += 4)
+            dst[k / 4] = make_float4(v[k] * inv, v[k + 1] * inv, v[k + 2] * inv, v[k + 3] * inv);
         }
       }
     }
     umma::fence_before_sync();
-    arrive_w(kOFree0 + ob);
-    if (live) {
-      const float lse2 = (l > 0.f) ? m_used + lg2(l) : -INFINITY;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_addr(c, kOFree0 + ob));
+    if (writer && kq == 0) {
+      const float lse2 = (L > 0.f) ? M + lg2(L) : -INFINITY;
       if (x.single)
-        p.lse[(size_t)x.b * p.H_q + hq] = (l > 0.f) ? lse2 * kLn2 : -INFINITY;
+        p.lse[(size_t)x.b * p.H_q + hq] = (L > 0.f) ? lse2 * kLn2 : -INFINITY;
       else
         p.lse_part[(size_t)x.slot * p.H_q + hq] = lse2;
     }
   }
 }
 
+template <int R>
 __global__ void __launch_bounds__(kThreads, 1)
     split_gqa_tc_kernel(Launch p, const __grid_constant__ Maps maps, int box) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -524,14 +634,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t count = 1;  // tcgen05.commit or the producer's expect_tx arrive
       if ((i >= kSFree0 && i < kSFree0 + 2) || (i >= kPFull0 && i < kPFull0 + 2) ||
-          (i >= kOFree0 && i < kOFree0 + 2))
-        count = 4;  // the four softmax warps
+          (i >= kEpiReady0 && i < kEpiReady0 + 2) || (i >= kOFree0 && i < kOFree0 + 2))
+        count = 4;  // the four softmax (or, for kOFree, epilogue) warps
       mbar_init(bar_addr(c, i), count);
     }
     *c.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     umma::tmem_alloc(c.sbase + kTmemSlot, kTmemCols);
     umma::tmem_relinquish();
   }
@@ -541,9 +651,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kTmemSlot);
 
   if (warp < 4) {
-    softmax_warps(p, c, tmem, n_units);
-  } else if (warp == 4) {
-    producer(p, c, maps, n_units, box != 0);
+    softmax_warps<R>(p, c, tmem, n_units);
+  } else if (warp < 8) {
+    epilogue_warps<R>(p, c, tmem, n_units);
+  } else if (warp == 8) {
+    producer(p, c, maps, n_units, box != 0, R);
   } else if ((threadIdx.x & 31) == 0) {
     mma_issuer(p, c, tmem, n_units);
     // drain: its arrival means every MMA issued before it has completed
@@ -551,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   umma::fence_before_sync();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     umma::fence_after_sync();
     if ((threadIdx.x & 31) == 0) {
       const uint32_t bar = bar_addr(c, kDrain);
@@ -596,18 +708,38 @@ bool encode(CUtensorMap* tm, const void* base, int rank, const cuuint64_t* dims,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Copies of the group's rows in the MMA: 128 / (the power of two >= G, >= 16).
+int copies_for(int G) {
+  int gp = 16;
+  while (gp < G) gp <<= 1;
+  return kRows / gp;
+}
+
+template <int R>
+cudaError_t set_smem() {
+  static const cudaError_t e = cudaFuncSetAttribute(
+      split_gqa_tc_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  return e;
+}
+
 int tc_ctas_per_sm() {
   static const int n = [] {
-    if (cudaFuncSetAttribute(split_gqa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes) != cudaSuccess)
-      return 1;
+    if (set_smem<1>() != cudaSuccess) return 1;
     int c = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, split_gqa_tc_kernel, kThreads,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, split_gqa_tc_kernel<1>, kThreads,
                                                       kSmemBytes) != cudaSuccess || c < 1)
       c = 1;
     return c;
   }();
   return n;
+}
+
+template <int R>
+cudaError_t launch_r(const Launch& p, const Maps& m, int box, int grid, cudaStream_t stream) {
+  const cudaError_t e = set_smem<R>();
+  if (e != cudaSuccess) return e;
+  return launch_after(split_gqa_tc_kernel<R>, dim3(grid), dim3(kThreads), (size_t)kSmemBytes,
+                      stream, p, m, box);
 }
 
 }  // namespace
@@ -617,9 +749,6 @@ bool gqa_tc_supported(int G, int D) { return G >= 16 && G <= kRows && D == kD; }
 int gqa_tc_resident_ctas(int sms) { return tc_ctas_per_sm() * sms; }
 
 cudaError_t launch_split_gqa_tc(const Launch& p, int grid, cudaStream_t stream) {
-  static const cudaError_t attr = cudaFuncSetAttribute(
-      split_gqa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (attr != cudaSuccess) return attr;
   const int G = p.H_q / p.H_kv;
   if (!gqa_tc_supported(G, p.D_qk) || p.D_v != kD || p.extra_k || p.kv_type != 0)
     return cudaErrorInvalidValue;
@@ -652,8 +781,12 @@ cudaError_t launch_split_gqa_tc(const Launch& p, int grid, cudaStream_t stream) 
       !encode(&m.k2, kb, 2, d2, s2, b2) || !encode(&m.v2, vb, 2, d2, s2, b2) ||
       !encode(&m.q, p.q, 2, dq, s2, bq))
     return cudaErrorInvalidValue;
-  return launch_after(split_gqa_tc_kernel, dim3(grid), dim3(kThreads), (size_t)kSmemBytes, stream,
-                      p, m, box ? 1 : 0);
+  switch (copies_for(G)) {
+    case 8: return launch_r<8>(p, m, box ? 1 : 0, grid, stream);
+    case 4: return launch_r<4>(p, m, box ? 1 : 0, grid, stream);
+    case 2: return launch_r<2>(p, m, box ? 1 : 0, grid, stream);
+    default: return launch_r<1>(p, m, box ? 1 : 0, grid, stream);
+  }
 }
 
 }  // namespace da
