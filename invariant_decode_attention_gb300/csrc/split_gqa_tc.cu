@@ -30,10 +30,11 @@
 // and entries whose page or slot is out of range, copy cache row 0 instead
 // (their scores are masked), so no stage byte is ever uninitialised.
 //
-// Roles (320 threads): warps 0-3 softmax; warps 4-7 epilogue (a unit's O
-// merge and output while the softmax warps go on with the next unit); warp 8
-// producer (page or index lookups ahead of the copies, TMA issue); warp 9 MMA
-// issue (one thread) and TMEM allocation.  Every mbarrier wait is bounded; on time-out
+// Roles (352 threads): warps 0-3 softmax; warps 4-7 epilogue (a unit's O
+// merge and output while the softmax warps go on with the next unit); warps
+// 8-9 producer (page or index lookups ahead of the copies, TMA issue; the two
+// warps take alternate tiles, so one issues copies while the other waits for
+// its next stage); warp 10 MMA issue (one thread) and TMEM allocation.  Every mbarrier wait is bounded; on time-out
 // the kernel records DA_DEVERR_TIMEOUT, every role leaves its loop,
 // outstanding tensor-core work is drained (bounded) and TMEM is freed.
 //
@@ -77,7 +78,7 @@ constexpr int kSmemBytes = kMergeOffset + (2 * 2 * kRows + kRows * 33) * 4;
 static_assert(kStageOffset % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle atoms 1024-aligned");
 static_assert(kSmemBytes <= 232448, "fits the 227 KB per-block limit");
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSCol = 0;    // S buffers [0, 64) and [64, 128)
 constexpr uint32_t kOCol = 128;  // O accumulators [128, 256) and [256, 384)
@@ -173,7 +174,8 @@ __device__ __forceinline__ TcUnit tc_unit(const Launch& p, int u) {
 }
 
 // ---------------------------------------------------------------- producer
-// Warp 4.  Box path: a tile's 16-entry group j is copied by one lane; the
+// Warps 8 and 9: warp w issues the copies of the tiles g with g % 2 == w
+// (and warp 8 each unit's Q rows); both walk every unit and tile.  Box path: a tile's 16-entry group j is copied by one lane; the
 // page words of a unit's tiles are loaded eight tiles at a time, a batch
 // ahead of the copies that use them (lane l holds the word of group l % 4 of
 // tile l / 4 of the batch), and the next unit's descriptor and first batch
@@ -183,6 +185,7 @@ __device__ __forceinline__ TcUnit tc_unit(const Launch& p, int u) {
 __device__ void producer(const Launch& p, const Ctx& c, const Maps& m, int n_units, bool box,
                          int R) {
   const int lane = threadIdx.x & 31;
+  const int pw = (threadIdx.x >> 5) - 8;  // producer warp 0 or 1: tiles of its parity
   const int G = p.H_q / p.H_kv;
   const int q_boxes = (G + kQBoxRows - 1) / kQBoxRows;
   const int gp = kRows / R;  // rows per copy of the group
@@ -226,8 +229,8 @@ __device__ void producer(const Launch& p, const Ctx& c, const Maps& m, int n_uni
     // Q of the unit's heads into Q buffer nq & 1 once the unit that used it
     // last has finished its S MMAs
     const int qb = nq & 1;
-    if (!wait_w(kQFree0 + qb, ((nq >> 1) & 1) ^ 1)) break;
-    if (lane == 0) {
+    if (pw == 0 && !wait_w(kQFree0 + qb, ((nq >> 1) & 1) ^ 1)) break;
+    if (pw == 0 && lane == 0) {
       const uint32_t qfull = bar_addr(c, kQFull0 + qb);
       mbar_arrive_expect_tx(qfull, R * q_boxes * 2 * kQBoxRows * 128);
       const uint32_t qdst = c.sbase + qb * kQBytes;
@@ -255,6 +258,11 @@ __device__ void producer(const Launch& p, const Ctx& c, const Maps& m, int n_uni
         if (i == 8 * last_batch && has_next) w_n0 = batch_word(xn, 0);  // the next unit's
       } else if (lane < 16 && t0 + kT < x.t_end) {
         for (int k = 0; k < 4; ++k) wg_n[k] = word_of(x, t0 + kT + lane * 4 + k);
+      }
+      if ((int)(g & 1) != pw) {  // the other producer warp's tile
+        if (!box && lane < 16)
+          for (int k = 0; k < 4; ++k) wg[k] = wg_n[k];
+        continue;
       }
       if (!wait_w(kEmpty0 + st, ((g / kStages) & 1) ^ 1)) {
         alive = false;
@@ -641,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *c.abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == 10) {
     umma::tmem_alloc(c.sbase + kTmemSlot, kTmemCols);
     umma::tmem_relinquish();
   }
@@ -654,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     softmax_warps<R>(p, c, tmem, n_units);
   } else if (warp < 8) {
     epilogue_warps<R>(p, c, tmem, n_units);
-  } else if (warp == 8) {
+  } else if (warp < 10) {
     producer(p, c, maps, n_units, box != 0, R);
   } else if ((threadIdx.x & 31) == 0) {
     mma_issuer(p, c, tmem, n_units);
@@ -663,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   umma::fence_before_sync();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 10) {
     umma::fence_after_sync();
     if ((threadIdx.x & 31) == 0) {
       const uint32_t bar = bar_addr(c, kDrain);

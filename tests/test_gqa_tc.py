@@ -3,9 +3,11 @@
 contractions go to tcgen05; "Sparse MLA decode is not batch-invariant",
 FlashMLA issue #212, Summary: the op is per row over its own KV list, the
 head layout is the caller's).  Parity against the fp64 oracle on every
-layout (box copies for contiguous caches and pages of a multiple of 16,
-gathers otherwise), bitwise batch invariance (a ragged sweep, solo against
-batched rows, repeats), and the variant choice (CPU checks need no GPU)."""
+layout and page size (box copies for contiguous caches and pages of a
+multiple of 16 entries, gathers otherwise), runs of one-tile units (the copy
+pipeline crossing a unit boundary every tile), bitwise batch invariance (a
+ragged sweep, solo against batched rows, repeats), and the variant choice
+(CPU checks need no GPU)."""
 
 import ctypes
 
@@ -147,3 +149,23 @@ def test_tc_repeated_runs_and_solo_rows(api):
                           wl.page_size, wl.H_q, wl.H_kv, 128, 128, wl.scale)
         o1, l1 = api.run_workload(solo)
         assert torch.equal(o1[0], o0[r]) and torch.equal(l1[0], l0[r])
+
+
+@gpu
+def test_tc_runs_of_one_tile_units(api):
+    # hundreds of rows of at most one tile each: a CTA takes many one-tile
+    # units in a row, so its copy pipeline crosses unit boundaries every tile
+    lens = [1 + (37 * i) % 64 for i in range(300)] + [5000, 0, 130]
+    wl = W.make(W.PAGED, lens, H_q=64, H_kv=4, D_qk=128, page_size=16, seed=99)
+    g = wl.to("cuda")
+    prob = api.problem_for(g)
+    ws = api.workspace(prob)
+    out = torch.empty((wl.B, 64, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((wl.B, 64), dtype=torch.float32, device="cuda")
+    pl = api.plan(prob, api.INVARIANT, g.lengths, ws)
+    api.run(pl, g.q, g.k, g.v, g.table, g.lengths, out, lse)
+    api.combine(pl, out, lse)
+    assert api.read_error(pl) == 0
+    rows = [0, 1, 63, 150, 299, 300, 301, 302]
+    ro, rl = oracle_for(wl, rows=rows)
+    assert_parity(out, lse, ro, rl, rows=rows)
