@@ -20,8 +20,12 @@
 // (dims 256..383 for the low value half, dims 0..127 for the high one), so it
 // needs no buffer of its own and is released with the stage.
 //
-// Pipeline.  The MMA thread issues S(g) into buffer g % 2 before the PV of the
-// previous tile, so the softmax of tile g-1 overlaps the S MMAs of tile g.
+// Pipeline.  S(g) goes into buffer g % 2, so the softmax of tile g-1 can
+// overlap the S MMAs of tile g.  The MMA thread issues S(g) and PV(g-1) in
+// whichever order their inputs arrive: when P(g-1) is ready before tile g's
+// rows have landed, PV(g-1) goes first and releases its stage, so the copy of
+// tile g+1 starts one tile earlier (with two stages, the copy latency is
+// otherwise exposed on every tile).
 // The softmax touches O only to rescale it (when its running max moves by
 // more than 2^8), after the PV before it has landed.  The producer prefetches
 // the next tile's rows into L2 while the current stage is in use.
@@ -164,6 +168,25 @@ __device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity) {
         set_error(c.hdr, DA_DEVERR_TIMEOUT);
         *c.abort_flag = 1;
         return false;
+      }
+    }
+  }
+}
+
+// Bounded wait for whichever of two barrier phases completes first: 1 for
+// (a, pa), 2 for (b, pb), 0 on time-out or abort.
+__device__ __forceinline__ int wait_either(const Ctx& c, int a, uint32_t pa, int b, uint32_t pb) {
+  const uint32_t ba = bar_addr(c, a), bb = bar_addr(c, b);
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(ba, pa)) return 1;
+    if (mbar_try_wait(bb, pb)) return 2;
+    if ((it & 63u) == 0) {
+      if (*c.abort_flag) return 0;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        set_error(c.hdr, DA_DEVERR_TIMEOUT);
+        *c.abort_flag = 1;
+        return 0;
       }
     }
   }
@@ -400,11 +423,23 @@ __device__ void mma_issuer(const Launch& p, const Ctx& c, uint32_t tmem, int n_u
       umma::commit(bar_addr(c, kEmpty0 + (gp % kStages)));
       return true;
     };
-    // Issue order S(g), PV(g-1): S(g) goes to the other S buffer, so it runs
-    // while the softmax of tile g-1 is still producing P(g-1).
+    // S(g) goes to the other S buffer, so it can run while the softmax of
+    // tile g-1 is still producing P(g-1); PV(g-1) is issued as soon as P(g-1)
+    // is ready, before S(g) when tile g's rows are still on their way (PV
+    // releases the stage, so the copy of tile g+1 can start).
+    bool pv_due = false;  // PV(g-1) not issued yet
     for (int i = 0; i < n_sub; ++i, ++g) {
       const int stage = g % kStages;
       const int sb = g & 1;
+      if (pv_due) {
+        const int w = wait_either(c, kPFull0 + ((g - 1) & 1), ((g - 1) >> 1) & 1,
+                                  kFull0 + stage, (g / kStages) & 1);
+        if (w == 0) return;
+        if (w == 1) {
+          if (!pv(g - 1, i == 1)) return;
+          pv_due = false;
+        }
+      }
       if (!wait_bar(c, kFull0 + stage, (g / kStages) & 1)) return;
       fence_proxy_async();
       if (!wait_bar(c, kSFree0 + sb, ((g >> 1) & 1) ^ 1)) return;  // S(g-2) was read
@@ -424,7 +459,8 @@ __device__ void mma_issuer(const Launch& p, const Ctx& c, uint32_t tmem, int n_u
       }
       umma::commit(bar_addr(c, kSFull0 + sb));
       if (i == n_sub - 1) umma::commit(bar_addr(c, kQFree));
-      if (i > 0 && !pv(g - 1, i == 1)) return;
+      if (pv_due && !pv(g - 1, i == 1)) return;
+      pv_due = true;
     }
     if (!pv(g - 1, n_sub == 1)) return;
     ++n_ne;
