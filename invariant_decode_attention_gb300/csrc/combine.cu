@@ -5,9 +5,10 @@
 // so the addends and their order are the same in any batch.
 //
 // One CTA per (row, head): warp 0 forms the weights, then every thread owns up
-// to four value dims (d, d + 128, ...) and advances their FMA chains together,
-// split by split, so all their loads are in flight at once; each chain runs
-// in split order from zero, as merge.cuh states.
+// to four value dims (d, d + 128, ...).  It loads its values of a batch of
+// kBatch splits first (all those loads in flight at once: a row of 64 splits
+// costs four round trips to L2, not 64), then advances its FMA chains through
+// the batch; each chain runs in split order from zero, as merge.cuh states.
 #include "common.cuh"
 #include "merge.cuh"
 
@@ -16,6 +17,7 @@ namespace {
 
 constexpr int kCombineThreads = 128;
 constexpr int kMaxDimsPerThread = 4;  // D_v <= 512
+constexpr int kBatch = 16;            // splits whose loads are issued together
 constexpr int kMaxSplitsAny = kFmaMaxSplits > kMlaMaxSplits ? kFmaMaxSplits : kMlaMaxSplits;
 static_assert(kMaxSplitsAny <= 64, "two split weights per lane of warp 0");
 
@@ -38,13 +40,23 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Launch p) {
   float acc[kMaxDimsPerThread];
 #pragma unroll
   for (int k = 0; k < kMaxDimsPerThread; ++k) acc[k] = 0.f;
-#pragma unroll 2
-  for (int s = 0; s < n; ++s) {
-    const float c = coef[s];
+  const int nk = (Dv - (int)threadIdx.x + kCombineThreads - 1) / kCombineThreads;  // own dims
+  for (int s0 = 0; s0 < n; s0 += kBatch) {
+    float v[kBatch][kMaxDimsPerThread];
 #pragma unroll
-    for (int k = 0; k < kMaxDimsPerThread; ++k) {
-      const int d = threadIdx.x + k * kCombineThreads;
-      if (d < Dv) acc[k] = fmaf(c, __ldcg(o0 + s * stride + d), acc[k]);
+    for (int i = 0; i < kBatch; ++i)
+#pragma unroll
+      for (int k = 0; k < kMaxDimsPerThread; ++k)
+        v[i][k] = (s0 + i < n && k < nk)
+                      ? __ldcg(o0 + (size_t)(s0 + i) * stride + threadIdx.x + k * kCombineThreads)
+                      : 0.f;
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      if (s0 + i < n) {
+        const float c = coef[s0 + i];
+#pragma unroll
+        for (int k = 0; k < kMaxDimsPerThread; ++k) acc[k] = fmaf(c, v[i][k], acc[k]);
+      }
     }
   }
 #pragma unroll
@@ -60,9 +72,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Launch p) {
 // ((slot * 128 + d / 4) * H_q + j) * 4 + d % 4 -- so that its epilogue's
 // stores coalesce.  Its combine takes one CTA per (row, value half, 32 dims)
 // and one thread per head: each thread forms its head's weights alone with
-// the same operations in the same order as merge_weights, and its loads of a
-// split's 4-dim group coalesce across the heads.
+// the same operations in the same order as merge_weights (its weights sit in
+// a shared-memory column), and its loads of a split's 4-dim group coalesce
+// across the heads.  The loads of two splits are issued before their FMAs.
 constexpr int kMlaGroupsPerCta = 8;  // 4-dim groups: 32 value dims
+constexpr int kMlaBatch = 2;         // splits whose loads are issued together
 
 __global__ void __launch_bounds__(kCombineThreads) combine_mla_kernel(Launch p) {
   wait_prior_grid();  // the split kernel's partials
@@ -72,33 +86,44 @@ __global__ void __launch_bounds__(kCombineThreads) combine_mla_kernel(Launch p) 
   const int j = threadIdx.x;
   if (n <= 1 || j >= p.H_q) return;
   const size_t slot0 = (size_t)b * p.max_splits;
-  float coef[kMlaMaxSplits];
+  __shared__ float coef_s[kMlaMaxSplits][kCombineThreads];
   float M = -INFINITY;
   for (int s = 0; s < n; ++s) {
-    coef[s] = __ldcg(p.lse_part + (slot0 + s) * p.H_q + j);
-    M = fmaxf(M, coef[s]);
+    coef_s[s][j] = __ldcg(p.lse_part + (slot0 + s) * p.H_q + j);
+    M = fmaxf(M, coef_s[s][j]);
   }
   float W = 0.f;
   for (int s = 0; s < n; ++s) {
-    coef[s] = (M == -INFINITY) ? 0.f : ex2(coef[s] - M);
-    W += coef[s];
+    coef_s[s][j] = (M == -INFINITY) ? 0.f : ex2(coef_s[s][j] - M);
+    W += coef_s[s][j];
   }
-  for (int s = 0; s < n; ++s) coef[s] = (W > 0.f) ? coef[s] / W : 0.f;
+  for (int s = 0; s < n; ++s) coef_s[s][j] = (W > 0.f) ? coef_s[s][j] / W : 0.f;
   const float4* op = reinterpret_cast<const float4*>(p.o_part);
   float4 acc[kMlaGroupsPerCta];
 #pragma unroll
   for (int gi = 0; gi < kMlaGroupsPerCta; ++gi) acc[gi] = make_float4(0.f, 0.f, 0.f, 0.f);
   const float4* base = op + (slot0 * 128 + cb * kMlaGroupsPerCta) * p.H_q + j;
-  for (int s = 0; s < n; ++s) {
-    const float c = coef[s];
-    const float4* src = base + (size_t)s * 128 * p.H_q;
+  for (int s0 = 0; s0 < n; s0 += kMlaBatch) {
+    float4 v[kMlaBatch][kMlaGroupsPerCta];
 #pragma unroll
-    for (int gi = 0; gi < kMlaGroupsPerCta; ++gi) {
-      const float4 v = __ldcg(src + gi * p.H_q);
-      acc[gi].x = fmaf(c, v.x, acc[gi].x);
-      acc[gi].y = fmaf(c, v.y, acc[gi].y);
-      acc[gi].z = fmaf(c, v.z, acc[gi].z);
-      acc[gi].w = fmaf(c, v.w, acc[gi].w);
+    for (int i = 0; i < kMlaBatch; ++i) {
+      const float4* src = base + (size_t)(s0 + i) * 128 * p.H_q;
+#pragma unroll
+      for (int gi = 0; gi < kMlaGroupsPerCta; ++gi)
+        v[i][gi] = (s0 + i < n) ? __ldcg(src + gi * p.H_q) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < kMlaBatch; ++i) {
+      if (s0 + i < n) {
+        const float c = coef_s[s0 + i][j];
+#pragma unroll
+        for (int gi = 0; gi < kMlaGroupsPerCta; ++gi) {
+          acc[gi].x = fmaf(c, v[i][gi].x, acc[gi].x);
+          acc[gi].y = fmaf(c, v[i][gi].y, acc[gi].y);
+          acc[gi].z = fmaf(c, v[i][gi].z, acc[gi].z);
+          acc[gi].w = fmaf(c, v[i][gi].w, acc[gi].w);
+        }
+      }
     }
   }
   __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(
