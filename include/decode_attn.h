@@ -105,6 +105,17 @@ extern "C" {
 #define DA_DEVERR_INDEX 2   /* a page id / slot index out of range; not read   */
 #define DA_DEVERR_TIMEOUT 4 /* a pipeline wait hit its limit; kernel bailed out */
 
+/* ---- da_problem.flags ------------------------------------------------ */
+/* Test hook for the time-out path of the tensor-core variants, never for a
+ * production call: with this flag the MMA-issuing thread of every CTA of
+ * DA_VARIANT_MLA and DA_VARIANT_GQA_TC first waits on an mbarrier that
+ * nothing signals, with a 2 ms limit.  That wait runs out, the kernel records
+ * DA_DEVERR_TIMEOUT, every role leaves its loop, the copies in flight and the
+ * tensor-core work are drained and tensor memory is freed before the CTA
+ * exits, so the context stays usable; that call's outputs are unspecified.
+ * The CUDA-core variant has no such waits and ignores the flag. */
+#define DA_FLAG_TEST_STALL 1u
+
 /* Problem description.  Plain data, filled by the caller. */
 typedef struct da_problem {
   int32_t batch;         /* B >= 0 query rows                                 */
@@ -120,7 +131,7 @@ typedef struct da_problem {
                          /* contiguous: ignored                               */
   float scale;           /* softmax scale, applied in fp32 to the fp32 dot    */
   int32_t shared_latent; /* 1: one latent cache, v == NULL, V = K[..., :D_v]  */
-  uint32_t flags;        /* reserved, must be 0                               */
+  uint32_t flags;        /* 0, or DA_FLAG_TEST_STALL (tests only)             */
   /* Optional second KV source (the *_extra entry points): an index-gathered */
   /* cache [extra_num_blocks, H_kv, D] whose entries continue each row's     */
   /* list after its main entries.  0 / 0 when unused.                         */

@@ -23,6 +23,7 @@ KV_BF16, KV_FP8_E4M3, KV_NVFP4 = 0, 1, 2
 CONTIGUOUS, PAGED, INDEXED = 0, 1, 2
 VARIANT_FMA, VARIANT_MLA, VARIANT_GQA_TC = 0, 1, 2
 DEVERR_LENGTH, DEVERR_INDEX, DEVERR_TIMEOUT = 1, 2, 4
+FLAG_TEST_STALL = 1  # da_problem.flags test hook (see include/decode_attn.h)
 
 LAYOUT_CODES = {"contiguous": CONTIGUOUS, "paged": PAGED, "indexed": INDEXED}
 

@@ -36,7 +36,7 @@ int check_problem(const da_problem* p) {
   if (p->width < 0) return DA_ERR_INVALID_ARG;
   if (p->layout != DA_KV_CONTIGUOUS && p->num_blocks < 0) return DA_ERR_INVALID_ARG;
   if (!std::isfinite(p->scale)) return DA_ERR_INVALID_ARG;
-  if (p->flags != 0) return DA_ERR_INVALID_ARG;
+  if ((p->flags & ~DA_FLAG_TEST_STALL) != 0) return DA_ERR_INVALID_ARG;
   if (p->shared_latent != 0 && p->shared_latent != 1) return DA_ERR_INVALID_ARG;
   if (p->shared_latent && p->head_dim_v > p->head_dim_qk) return DA_ERR_INVALID_ARG;
   if (p->extra_width < 0 || p->extra_num_blocks < 0) return DA_ERR_INVALID_ARG;
@@ -151,6 +151,7 @@ Launch make_launch(const da_plan* plan) {
   }
   L.max_splits = plan->max_splits;
   L.o_part_mla = plan->variant == DA_VARIANT_MLA;
+  L.test_stall = (pr.flags & DA_FLAG_TEST_STALL) != 0;
   L.scale_log2 = pr.scale * kLog2e;
   if (pr.kv_dtype != DA_KV_BF16) {  // scores of scaled keys: scale * k_scale
     L.kv_type = pr.kv_dtype;

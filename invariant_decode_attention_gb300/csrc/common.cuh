@@ -47,6 +47,9 @@ constexpr size_t kHdrBytes = 256;
 
 // Longest a pipeline wait may spin before the kernel gives up (ns).
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;
+// The limit of the one wait the time-out test hook (DA_FLAG_TEST_STALL) makes
+// run out.
+constexpr unsigned long long kTestStallNs = 2000000ull;
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -87,6 +90,7 @@ struct Launch {
   float v_scale;     // E4M3 cache: multiplies each unit's output
   int fma_group;     // CUDA-core variant: query heads per KV head (G)
   int fma_chunks;    // CUDA-core variant: units per KV head (head chunks)
+  int test_stall;    // DA_FLAG_TEST_STALL: tensor-core kernels stall at start (tests)
 };
 
 struct PlanLaunch {

@@ -66,7 +66,9 @@ enum {
   kFull0 = 0, kEmpty0 = kFull0 + kStages, kQFull0 = kEmpty0 + kStages, kQFree0 = kQFull0 + 2,
   kSFull0 = kQFree0 + 2, kSFree0 = kSFull0 + 2, kPFull0 = kSFree0 + 2, kPVDone0 = kPFull0 + 2,
   kODone0 = kPVDone0 + 2, kEpiReady0 = kODone0 + 2, kOFree0 = kEpiReady0 + 2,
-  kDrain = kOFree0 + 2, kNumBars
+  kDrain = kOFree0 + 2,
+  kStall,  // never signalled: the time-out test hook waits on it
+  kNumBars
 };
 constexpr int kTmemSlot = kBarOffset + kNumBars * 8;
 constexpr int kAbortSlot = kTmemSlot + 4;
@@ -138,7 +140,8 @@ __device__ __forceinline__ uint32_t bar_addr(const Ctx& c, int i) {
 }
 
 // Bounded wait that also gives up when the abort flag is raised.
-__device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity) {
+__device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity,
+                                         unsigned long long limit_ns = kWaitLimitNs) {
   const uint32_t bar = bar_addr(c, i);
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
@@ -146,7 +149,7 @@ __device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*c.abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         set_error(c.hdr, DA_DEVERR_TIMEOUT);
         *c.abort_flag = 1;
         return false;
@@ -303,14 +306,18 @@ __device__ void producer(const Launch& p, const Ctx& c, const Maps& m, int n_uni
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(p.hdr, DA_DEVERR_INDEX);
   // leave no copy in flight into this CTA's shared memory (on the normal path
-  // every stage and Q buffer was consumed and these waits return at once)
+  // every stage and Q buffer was consumed and these waits return at once).
+  // A warp waits only for its own copies: tiles t < g of its parity (after a
+  // time-out, g is the tile it did not copy), which fill the stages of its
+  // parity; Q buffers are copied by warp 0 alone.
+  static_assert(kStages % 2 == 0, "a stage is filled by one producer warp");
   if (lane == 0) {
-    for (int st = 0; st < kStages; ++st) {
+    for (int st = pw; st < kStages; st += 2) {
       const int last = (int)g - 1 - (((int)g - 1 - st) % kStages + kStages) % kStages;
       if (last >= 0 && !mbar_wait(bar_addr(c, kFull0 + st), (last / kStages) & 1))
         set_error(p.hdr, DA_DEVERR_TIMEOUT);
     }
-    for (int qb = 0; qb < 2; ++qb) {
+    for (int qb = 0; qb < 2 && pw == 0; ++qb) {
       const int last = (int)nq - 1 - (((int)nq - 1 - qb) % 2 + 2) % 2;
       if (last >= 0 && !mbar_wait(bar_addr(c, kQFull0 + qb), (last >> 1) & 1))
         set_error(p.hdr, DA_DEVERR_TIMEOUT);
@@ -328,6 +335,8 @@ __device__ void mma_issuer(const Launch& p, const Ctx& c, uint32_t tmem, int n_u
   const uint64_t b_v0 =
       umma::smem_desc(c.sbase + kStageOffset + kTileBytes, kRegion, 1024, umma::kSwizzle128B);
   uint32_t g = 0, nq = 0;
+  // time-out test hook: a wait that runs out, then the abort path
+  if (p.test_stall && !wait_bar(c, kStall, 0, kTestStallNs)) return;
   for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++nq) {
     const TcUnit x = tc_unit(p, u);
     const int n_sub = (x.t_end - x.t_begin + kT - 1) / kT;
@@ -537,8 +546,10 @@ __device__ void epilogue_warps(const Launch& p, const Ctx& c, uint32_t tmem, int
   for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++nq) {
     const TcUnit x = tc_unit(p, u);
     const int ob = nq & 1;
-    if (!wait_w(kEpiReady0 + ob, (nq >> 1) & 1)) return;
-    if (!wait_w(kODone0 + ob, (nq >> 1) & 1)) return;
+    // the four warps leave together: one that gave up while another got
+    // through would leave the other waiting at the named barrier below
+    const bool ok = wait_w(kEpiReady0 + ob, (nq >> 1) & 1) && wait_w(kODone0 + ob, (nq >> 1) & 1);
+    if (named_bar_or(1, 128, !ok)) return;
     umma::fence_after_sync();
     const float* m_s = ml + ob * 2 * kRows;
     const float* l_s = m_s + kRows;

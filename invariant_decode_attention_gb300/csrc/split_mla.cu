@@ -77,7 +77,9 @@ constexpr int kBarOffset = kStageOffset + kStages * kStageBytes;  // 229376
 // PV-done barrier could be two phases behind there.
 enum { kFull0 = 0, kEmpty0 = kFull0 + kStages, kSFull0 = kEmpty0 + kStages,
        kSFree0 = kSFull0 + 2, kPFull0 = kSFree0 + 2, kODone0 = kPFull0 + 2,
-       kOFree = kODone0 + 2, kQFull, kQTFull, kQFree, kDrain, kNumBars };
+       kOFree = kODone0 + 2, kQFull, kQTFull, kQFree, kDrain,
+       kStall,  // never signalled: the time-out test hook waits on it
+       kNumBars };
 constexpr int kTmemSlot = kBarOffset + kNumBars * 8;
 static_assert(kStageOffset % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle atoms 1024-aligned");
 constexpr int kAbortSlot = kTmemSlot + 4;
@@ -156,7 +158,8 @@ __device__ __forceinline__ uint32_t bar_addr(const Ctx& c, int i) {
 }
 
 // Bounded wait that also gives up when the abort flag is raised.
-__device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity) {
+__device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity,
+                                         unsigned long long limit_ns = kWaitLimitNs) {
   const uint32_t bar = bar_addr(c, i);
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
@@ -164,7 +167,7 @@ __device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*c.abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         set_error(c.hdr, DA_DEVERR_TIMEOUT);
         *c.abort_flag = 1;
         return false;
@@ -398,6 +401,8 @@ __device__ void mma_issuer(const Launch& p, const Ctx& c, uint32_t tmem, int n_u
       umma::smem_desc(c.sbase, 16, 1024, umma::kSwizzle128B);
   const uint64_t b_v0 =      // V = leading dims of the K tile, MN-major
       umma::smem_desc(c.sbase + kStageOffset, kStageRegion, 1024, umma::kSwizzle128B);
+  // time-out test hook: a wait that runs out, then the abort path
+  if (p.test_stall && !wait_bar(c, kStall, 0, kTestStallNs)) return;
   for (int u = blockIdx.x; u < n_units; u = next_unit(u)) {
     const MlaUnit x = mla_unit(p, u);
     if (x.empty) continue;
