@@ -3,17 +3,20 @@
 // bf16 caches.
 //
 // One unit of work = (row b, split s, KV head h).  Both contractions run on
-// tcgen05 tensor cores with fp32 accumulators in tensor memory (TMEM); the
-// G query heads of the group are the MMA's M rows (padded to 128: rows past
-// the group compute on whatever the Q buffer holds there and are never
-// written -- a row of an MMA result depends only on its own row of A):
+// tcgen05 tensor cores with fp32 accumulators in tensor memory (TMEM):
 //     S = Q K^T      M = 128, N = 64 entries, K = 128 dims   (8 MMAs of K=16)
 //     O += P V       M = 128, N = 128 dims,   K = 64 entries (4 MMAs of K=16)
-// A thread of the softmax warps owns one head (one TMEM lane), so the
-// running max and sum of a head are plain per-thread loops: no cross-lane
-// reductions.  The reference value of the exponentials moves only when a
-// score exceeds it by more than 2^8 (then O is rescaled in TMEM), a decision
-// that depends only on the unit's own scores.
+// The G query heads of the group, padded to gp = the power of two >= G (at
+// least 16), fill the 128 MMA rows as R = 128 / gp copies; rows past the
+// group compute on whatever the Q buffer holds there and are never written
+// (a row of an MMA result depends only on its own row of A).  Copy c of the
+// group takes entries [c * 64 / R, (c + 1) * 64 / R) of every tile in the
+// softmax: a thread owns one (head, copy) row -- one TMEM lane -- with its
+// own running max and sum, P is zero outside its copy's entries, and the
+// epilogue merges the R copies' (O, max, sum) of each head.  The reference
+// value of a row's exponentials moves only when a score exceeds it by more
+// than 2^8 (then its O row is rescaled in TMEM), a decision that depends only
+// on the unit's own scores.
 //
 // Memory.  Shared: two Q buffers (the next unit's Q loads while the current
 // one runs) and four 64-entry stages of K and V, each tile in the
