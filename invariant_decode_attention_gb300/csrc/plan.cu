@@ -10,7 +10,11 @@
 // BALANCED: the batch-wide quota of the same page's "Where it comes from"
 // section -- payload = ceil(total / parts) + fixed overhead, with total summed
 // over every row, then greedy packing in batch order that cuts a row wherever
-// a part fills up.  Kept only to measure what invariance costs.
+// a part fills up.  The page's scheduler allows up to 256 splits; here a row
+// has at most the variant's max_splits, so the quota is raised, where needed,
+// to the smallest one that cuts the longest row into that many (otherwise the
+// last split of a long row would take all the rest and BALANCED would be an
+// unfairly slow opponent).  Kept only to measure what invariance costs.
 #include "common.cuh"
 
 namespace da {
@@ -156,6 +160,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_balanced_kernel(PlanLaunch 
   __shared__ int bucket[kSortKeys];
   __shared__ int tiles_s[kBalancedSmemRows];
   __shared__ long long red[kPlanThreads / 32];
+  __shared__ int red_max[kPlanThreads / 32];
   allow_next_grid();
   if (threadIdx.x == 0) {
     p.hdr[kHdrError] = 0;
@@ -168,21 +173,38 @@ __global__ void __launch_bounds__(kPlanThreads) plan_balanced_kernel(PlanLaunch 
   const bool in_smem = p.B <= kBalancedSmemRows;
   // every row's tile count (kept in n_splits until the walk overwrites it)
   long long part = 0;
+  int longest = 0;
   for (int b = threadIdx.x; b < p.B; b += kPlanThreads) {
     const int n = ceil_div_i(row_length(p, b), p.tile);
     if (in_smem) tiles_s[b] = n;
     p.n_splits[b] = n;
     part += n + ovh;
+    longest = max(longest, n);
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = part;
+  for (int o = 16; o > 0; o >>= 1) {
+    part += __shfl_xor_sync(0xffffffffu, part, o);
+    longest = max(longest, __shfl_xor_sync(0xffffffffu, longest, o));
+  }
+  if ((threadIdx.x & 31) == 0) {
+    red[threadIdx.x >> 5] = part;
+    red_max[threadIdx.x >> 5] = longest;
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
     long long total = 0;
-    for (int w = 0; w < kPlanThreads / 32; ++w) total += red[w];
+    int n_max = 0;
+    for (int w = 0; w < kPlanThreads / 32; ++w) {
+      total += red[w];
+      n_max = max(n_max, red_max[w]);
+    }
     const int parts = max(1, p.num_parts);
-    const long long payload = (total / parts + (total % parts != 0)) + ovh;
+    long long payload = (total / parts + (total % parts != 0)) + ovh;
+    // raised, where needed, so that the longest row fits in the split budget:
+    // full parts of payload - ovh tiles cut it into at most max_splits pieces
+    const int cap = max(1, p.max_splits - 1);
+    const long long fit = (long long)(n_max / cap + (n_max % cap != 0)) + ovh;
+    if (payload < fit) payload = fit;
     long long room = payload;
     for (int b = 0; b < p.B; ++b) {
       const int n_tiles = in_smem ? tiles_s[b] : p.n_splits[b];

@@ -65,6 +65,11 @@ def plan_balanced(lengths, tile, max_splits, num_parts, fixed_overhead):
     n_tiles = [ceil_div(int(L), tile) for L in lengths]
     total = sum(n + fixed_overhead for n in n_tiles)
     payload = ceil_div(total, max(1, num_parts)) + fixed_overhead
+    # the quota is raised, where needed, so that the longest row fits in the
+    # split budget: full parts of payload - fixed_overhead tiles cut it into
+    # at most max_splits pieces
+    longest = max(n_tiles, default=0)
+    payload = max(payload, ceil_div(longest, max(1, max_splits - 1)) + fixed_overhead)
     bounds = []
     room = payload  # tiles still free in the current part
     for n in n_tiles:

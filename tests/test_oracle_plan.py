@@ -81,6 +81,21 @@ def test_balanced_hand_example():
     assert got == [[0, 10], [0, 1], [0, 7, 17, 20]]
 
 
+def test_balanced_quota_raised_for_the_longest_row():
+    # one row of 4096 tiles (tile 1), 152 parts, overhead 2, 64 splits at most:
+    # the page's quota is ceil(4098 / 152) + 2 = 29, which would need 152
+    # pieces; raised to ceil(4096 / 63) + 2 = 68, full parts of 66 tiles cut
+    # the row into 63 pieces, the last one 4 tiles -- no overloaded split.
+    got = P.plan_balanced([4096], 1, 64, 152, 2)[0]
+    assert got == list(range(0, 4093, 66)) + [4096]
+    assert max(b - a for a, b in zip(got[:-1], got[1:])) == 66
+    # when the quota already fits the longest row it is the page's own:
+    # total = 100 * (40 + 2) = 4200, 7 parts -> 600 + 2 = 602 (>= 40 / 63 + 2);
+    # 14 rows fill 588 of the first part, row 14 takes 14 - 2 = 12 tiles there
+    many = P.plan_balanced([40] * 100, 1, 64, 7, 2)
+    assert many[13] == [0, 40] and many[14] == [0, 12, 40]
+
+
 def test_balanced_coverage_and_split_cap():
     rng = random.Random(1)
     for _ in range(200):
