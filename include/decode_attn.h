@@ -96,8 +96,9 @@ extern "C" {
 /* ---- kernel variants (chosen from the head config only, never B) ----- */
 #define DA_VARIANT_FMA 0 /* CUDA-core fp32 FMA, H_q/H_kv in 1..128, D in {64,128}    */
 #define DA_VARIANT_MLA 1 /* tcgen05 tensor cores, shared latent 576/512, 16..128 heads */
-/* tcgen05 tensor cores, separate bf16 K and V, 16..128 query heads per KV head,
- * D = 128, one KV source (other configs of >= 16 heads: DA_VARIANT_FMA)     */
+/* tcgen05 tensor cores, separate K and V (bf16, or E4M3 converted to f16 in
+ * shared memory), 16..128 query heads per KV head, D = 128, one KV source
+ * (other configs of >= 16 heads: DA_VARIANT_FMA)                            */
 #define DA_VARIANT_GQA_TC 2
 
 /* ---- device-detected input errors (decode_attn_read_error bits) ----- */

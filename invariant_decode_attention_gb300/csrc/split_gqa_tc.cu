@@ -57,41 +57,74 @@ constexpr int kRows = 128;  // MMA M: query heads of the group, padded
 constexpr int kD = 128;
 constexpr int kT = kTcTile;  // entries per tile
 static_assert(kT == 64, "one 128-byte swizzle row of P per head");
-constexpr int kStages = 4;
-constexpr int kRegion = kT * 128;           // 64 rows x 64 dims (bf16)
+constexpr int kRegion = kT * 128;           // 64 rows x 64 dims (16-bit elements)
 constexpr int kTileBytes = 2 * kRegion;     // K (or V) of a tile: 16 KB
 constexpr int kStageBytes = 2 * kTileBytes;  // K, then V
 constexpr int kQRegion = kRows * 128;       // 128 rows x 64 dims
 constexpr int kQBytes = 2 * kQRegion;       // 32 KB
-constexpr int kStageOffset = 2 * kQBytes;
-constexpr int kBarOffset = kStageOffset + kStages * kStageBytes;
+constexpr int kRawTileBytes = kT * kD;      // E4M3 K (or V) of a tile: 64 rows x 128 bytes
+constexpr int kRawStageBytes = 2 * kRawTileBytes;  // 16 KB: K, then V
+constexpr int kMaxStages = 8;
 enum {
-  kFull0 = 0, kEmpty0 = kFull0 + kStages, kQFull0 = kEmpty0 + kStages, kQFree0 = kQFull0 + 2,
+  kFull0 = 0, kEmpty0 = kFull0 + kMaxStages,  // operand stages: ready / free
+  kRawFull0 = kEmpty0 + kMaxStages,           // E4M3 cache: copies landed
+  kRawEmpty0 = kRawFull0 + kMaxStages,        // E4M3 cache: converted, reusable
+  kQConv0 = kRawEmpty0 + kMaxStages,          // E4M3 cache: Q written to tensor memory
+  kQFull0 = kQConv0 + 2, kQFree0 = kQFull0 + 2,
   kSFull0 = kQFree0 + 2, kSFree0 = kSFull0 + 2, kPFull0 = kSFree0 + 2, kPVDone0 = kPFull0 + 2,
   kODone0 = kPVDone0 + 2, kEpiReady0 = kODone0 + 2, kOFree0 = kEpiReady0 + 2,
   kDrain = kOFree0 + 2,
   kStall,  // never signalled: the time-out test hook waits on it
   kNumBars
 };
-constexpr int kTmemSlot = kBarOffset + kNumBars * 8;
-constexpr int kAbortSlot = kTmemSlot + 4;
-// m and l of every row, per O buffer (softmax -> epilogue), then the
-// epilogue's merge scratch: one 32-column chunk of every row's O (rows padded
-// to 33 floats)
-constexpr int kMergeOffset = (kAbortSlot + 4 + 15) / 16 * 16;
-constexpr int kSmemBytes = kMergeOffset + (2 * 2 * kRows + kRows * 33) * 4;
-static_assert(kStageOffset % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle atoms 1024-aligned");
-static_assert(kSmemBytes <= 232448, "fits the 227 KB per-block limit");
 
-constexpr int kThreads = 352;
+// Shared-memory map.  Q8: the cache holds one E4M3 byte per element.  bf16:
+// two Q buffers (TMA copies, the S MMAs' A operand) and four operand stages
+// that TMA fills directly.  E4M3: Q lives in tensor memory instead (the
+// converter writes it there), TMA copies the cache bytes into seven raw
+// stages (one producer warp: half the copies of the bf16 path per tile) and
+// the converter warpgroup writes them, as f16, into three operand stages
+// (the MMAs then run on f16 operands, see the converter).  Seven raw stages
+// keep 112 KB of the cache in flight per SM, as many entries as 224 KB of
+// bf16.
+template <bool Q8>
+struct Lay {
+  static constexpr int kStages = Q8 ? 3 : 4;     // operand stages (K, V as 16-bit)
+  static constexpr int kRawStages = Q8 ? 7 : 0;  // E4M3 copies
+  static constexpr int kStageOffset = Q8 ? 0 : 2 * kQBytes;
+  static constexpr int kRawOffset = kStageOffset + kStages * kStageBytes;
+  static constexpr int kBarOffset = kRawOffset + kRawStages * kRawStageBytes;
+  static constexpr int kTmemSlot = kBarOffset + kNumBars * 8;
+  static constexpr int kAbortSlot = kTmemSlot + 4;
+  // m and l of every row, per O buffer (softmax -> epilogue), then the
+  // epilogue's merge scratch: one 32-column chunk of every row's O (rows
+  // padded to 33 floats)
+  static constexpr int kMergeOffset = (kAbortSlot + 4 + 15) / 16 * 16;
+  static constexpr int kSmemBytes = kMergeOffset + (2 * 2 * kRows + kRows * 33) * 4;
+  // warps 0-3 softmax, 4-7 epilogue, 8-9 producer, 10 MMA, 11-14 converter
+  static constexpr int kThreads = Q8 ? 480 : 352;
+  static_assert(kStageOffset % 1024 == 0 && kRawOffset % 1024 == 0, "aligned stages");
+  static_assert(kStages <= kMaxStages && kRawStages <= kMaxStages, "barrier slots");
+  static_assert(kSmemBytes <= 232448, "fits the 227 KB per-block limit");
+};
+
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSCol = 0;    // S buffers [0, 64) and [64, 128)
 constexpr uint32_t kOCol = 128;  // O accumulators [128, 256) and [256, 384)
+constexpr uint32_t kQCol = 384;  // E4M3 cache: two f16 Q buffers [384, 448) and [448, 512)
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kQBoxRows = 16;
 
-constexpr uint32_t kIdescS = umma::idesc_bf16_f32(kRows, kT, false);
-constexpr uint32_t kIdescO = umma::idesc_bf16_f32(kRows, kD, true);
+// bf16 operands (bf16 cache); f16 operands (E4M3 cache: E4M3 values are f16
+// values, and Q is prescaled by a power of two into f16's range)
+template <bool Q8>
+__host__ __device__ constexpr uint32_t idesc_s() {
+  return Q8 ? umma::idesc_f16_f32(kRows, kT, false) : umma::idesc_bf16_f32(kRows, kT, false);
+}
+template <bool Q8>
+__host__ __device__ constexpr uint32_t idesc_o() {
+  return Q8 ? umma::idesc_f16_f32(kRows, kD, true) : umma::idesc_bf16_f32(kRows, kD, true);
+}
 
 __device__ __forceinline__ void tma_box3(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
                                          int c2, uint32_t bar) {
@@ -126,21 +159,23 @@ __device__ __forceinline__ void fence_proxy_async() {
 }
 
 struct Maps {
-  CUtensorMap k3, v3;  // [rows][H_kv][128], box {64, 1, 16} (box path)
-  CUtensorMap k2, v2;  // [rows * H_kv][128], box {64, 1} (gather path)
+  // bf16: [rows][H_kv][128] elements, box {64, 1, 16}; E4M3: bytes, box {128, 1, 16}
+  CUtensorMap k3, v3;  // (box path)
+  // bf16: [rows * H_kv][128], box {64, 1}; E4M3: bytes, box {128, 1}
+  CUtensorMap k2, v2;  // (gather path)
   CUtensorMap q;       // [B * H_q][128], box {64, 16}
 };
 
 struct Ctx {
   uint8_t* smem;
   uint32_t sbase;
+  uint32_t bars;    // shared address of the first mbarrier
+  float* merge;     // m, l per O buffer, then the epilogue's merge scratch
   volatile int* abort_flag;
   int32_t* hdr;
 };
 
-__device__ __forceinline__ uint32_t bar_addr(const Ctx& c, int i) {
-  return c.sbase + kBarOffset + 8 * i;
-}
+__device__ __forceinline__ uint32_t bar_addr(const Ctx& c, int i) { return c.bars + 8 * i; }
 
 // Bounded wait that also gives up when the abort flag is raised.
 __device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity,
@@ -159,6 +194,37 @@ __device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity,
       }
     }
   }
+}
+
+// ---- E4M3 cache: f16 operands ---------------------------------------------
+// Every E4M3 value is an f16 value, so K and V convert exactly; Q (bf16) is
+// brought into f16's range per row by a power of two: with m the row's
+// largest magnitude and 2^k <= m < 2^(k+1), the row is multiplied by
+// 2^e, e = 14 - k (clamped to [-113, 120]), so its largest element lies in
+// [2^14, 2^15).  Elements below 2^-14 of that (after scaling) become f16
+// subnormals, an absolute error of at most 2^-25 * 2^-e, far below the fp32
+// accumulation's.  The softmax divides the row's scores by 2^e again.
+__device__ __forceinline__ int q_prescale_exp(float maxabs) {
+  const uint32_t bits = __float_as_uint(maxabs);
+  const int biased = (int)((bits >> 23) & 0xff);
+  if (maxabs == 0.f || biased == 0xff) return 0;  // zero row, or inf / NaN: no scaling
+  const int k = (biased == 0) ? -127 : biased - 127;
+  return min(120, max(-113, 14 - k));
+}
+
+// 2^e for e in [-126, 127].
+__device__ __forceinline__ float exp2_int(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
+
+// Largest magnitude of eight bf16 values.
+__device__ __forceinline__ float bf16x8_absmax(uint4 w) {
+  const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    m = fmaxf(m, fabsf(__uint_as_float(v[i] << 16)));
+    m = fmaxf(m, fabsf(__uint_as_float(v[i] & 0xffff0000u)));
+  }
+  return m;
 }
 
 // A unit: KV head h of one (row, split) item.
@@ -188,10 +254,18 @@ __device__ __forceinline__ TcUnit tc_unit(const Launch& p, int u) {
 // are loaded during the current unit, so the copies never wait on a lookup.
 // Gather path: lane j < 16 owns the 4-entry group j of each tile, its words
 // loaded one tile ahead.
+template <bool Q8>
 __device__ void producer(const Launch& p, const Ctx& c, const Maps& m, int n_units, bool box,
                          int R) {
+  using L = Lay<Q8>;
+  // the stages this role fills: raw E4M3 stages, or the operand stages
+  constexpr int kNS = Q8 ? L::kRawStages : L::kStages;
+  constexpr int kFullB = Q8 ? kRawFull0 : kFull0, kEmptyB = Q8 ? kRawEmpty0 : kEmpty0;
+  // E4M3 cache: warp 8 alone copies (a tile is 8 box copies, not 16)
+  constexpr int kWarpsCopying = Q8 ? 1 : 2;
   const int lane = threadIdx.x & 31;
   const int pw = (threadIdx.x >> 5) - 8;  // producer warp 0 or 1: tiles of its parity
+  if (pw >= kWarpsCopying) return;
   const int G = p.H_q / p.H_kv;
   const int q_boxes = (G + kQBoxRows - 1) / kQBoxRows;
   const int gp = kRows / R;  // rows per copy of the group
@@ -235,8 +309,8 @@ __device__ void producer(const Launch& p, const Ctx& c, const Maps& m, int n_uni
     // Q of the unit's heads into Q buffer nq & 1 once the unit that used it
     // last has finished its S MMAs
     const int qb = nq & 1;
-    if (pw == 0 && !wait_w(kQFree0 + qb, ((nq >> 1) & 1) ^ 1)) break;
-    if (pw == 0 && lane == 0) {
+    if (!Q8 && pw == 0 && !wait_w(kQFree0 + qb, ((nq >> 1) & 1) ^ 1)) break;
+    if (!Q8 && pw == 0 && lane == 0) {
       const uint32_t qfull = bar_addr(c, kQFull0 + qb);
       mbar_arrive_expect_tx(qfull, R * q_boxes * 2 * kQBoxRows * 128);
       const uint32_t qdst = c.sbase + qb * kQBytes;
@@ -255,7 +329,7 @@ __device__ void producer(const Launch& p, const Ctx& c, const Maps& m, int n_uni
     const int last_batch = (n_sub - 1) / 8;
     for (int i = 0; i < n_sub; ++i, ++g) {
       const int t0 = x.t_begin + i * kT;
-      const int st = g % kStages;
+      const int st = g % kNS;
       if (box) {
         if (i > 0 && (i & 7) == 0) {  // next batch: its words were loaded a batch ago
           w_cur = w_nxt;
@@ -265,43 +339,67 @@ __device__ void producer(const Launch& p, const Ctx& c, const Maps& m, int n_uni
       } else if (lane < 16 && t0 + kT < x.t_end) {
         for (int k = 0; k < 4; ++k) wg_n[k] = word_of(x, t0 + kT + lane * 4 + k);
       }
-      if ((int)(g & 1) != pw) {  // the other producer warp's tile
+      if (kWarpsCopying == 2 && (int)(g & 1) != pw) {  // the other producer warp's tile
         if (!box && lane < 16)
           for (int k = 0; k < 4; ++k) wg[k] = wg_n[k];
         continue;
       }
-      if (!wait_w(kEmpty0 + st, ((g / kStages) & 1) ^ 1)) {
+      if (!wait_w(kEmptyB + st, ((g / kNS) & 1) ^ 1)) {
         alive = false;
         break;
       }
-      const uint32_t full = bar_addr(c, kFull0 + st);
-      if (lane == 0) mbar_arrive_expect_tx(full, kStageBytes);
+      const uint32_t full = bar_addr(c, kFullB + st);
+      if (lane == 0) mbar_arrive_expect_tx(full, Q8 ? kRawStageBytes : kStageBytes);
       __syncwarp();
-      const uint32_t kdst = c.sbase + kStageOffset + st * kStageBytes;
-      const uint32_t vdst = kdst + kTileBytes;
-      if (box) {
-        if ((lane >> 2) == (i & 7)) {
-          const int grp = lane & 3;
-          long long r = row_of(x, t0 + grp * 16, w_cur);
-          if (r < 0) r = 0;
-          for (int half = 0; half < 2; ++half) {
-            const uint32_t off = half * kRegion + grp * 16 * 128;
-            tma_box3(kdst + off, &m.k3, 64 * half, x.h, (int)r, full);
-            tma_box3(vdst + off, &m.v3, 64 * half, x.h, (int)r, full);
+      if constexpr (Q8) {
+        // E4M3 rows (128 bytes) into a raw stage, row-major: K then V
+        const uint32_t kdst = c.sbase + L::kRawOffset + st * kRawStageBytes;
+        const uint32_t vdst = kdst + kRawTileBytes;
+        if (box) {
+          if ((lane >> 2) == (i & 7)) {
+            const int grp = lane & 3;
+            long long r = row_of(x, t0 + grp * 16, w_cur);
+            if (r < 0) r = 0;
+            tma_box3(kdst + grp * 16 * kD, &m.k3, 0, x.h, (int)r, full);
+            tma_box3(vdst + grp * 16 * kD, &m.v3, 0, x.h, (int)r, full);
           }
+        } else if (lane < 16) {
+          int rr[4];
+          for (int k = 0; k < 4; ++k) {
+            const long long r = row_of(x, t0 + lane * 4 + k, wg[k]);
+            rr[k] = (int)((r < 0 ? 0 : r) * p.H_kv + x.h);
+          }
+          tma_gather4(kdst + lane * 4 * kD, &m.k2, 0, rr[0], rr[1], rr[2], rr[3], full);
+          tma_gather4(vdst + lane * 4 * kD, &m.v2, 0, rr[0], rr[1], rr[2], rr[3], full);
+          for (int k = 0; k < 4; ++k) wg[k] = wg_n[k];
         }
-      } else if (lane < 16) {
-        int rr[4];
-        for (int k = 0; k < 4; ++k) {
-          const long long r = row_of(x, t0 + lane * 4 + k, wg[k]);
-          rr[k] = (int)((r < 0 ? 0 : r) * p.H_kv + x.h);
+      } else {
+        const uint32_t kdst = c.sbase + L::kStageOffset + st * kStageBytes;
+        const uint32_t vdst = kdst + kTileBytes;
+        if (box) {
+          if ((lane >> 2) == (i & 7)) {
+            const int grp = lane & 3;
+            long long r = row_of(x, t0 + grp * 16, w_cur);
+            if (r < 0) r = 0;
+            for (int half = 0; half < 2; ++half) {
+              const uint32_t off = half * kRegion + grp * 16 * 128;
+              tma_box3(kdst + off, &m.k3, 64 * half, x.h, (int)r, full);
+              tma_box3(vdst + off, &m.v3, 64 * half, x.h, (int)r, full);
+            }
+          }
+        } else if (lane < 16) {
+          int rr[4];
+          for (int k = 0; k < 4; ++k) {
+            const long long r = row_of(x, t0 + lane * 4 + k, wg[k]);
+            rr[k] = (int)((r < 0 ? 0 : r) * p.H_kv + x.h);
+          }
+          for (int half = 0; half < 2; ++half) {
+            const uint32_t off = half * kRegion + lane * 4 * 128;
+            tma_gather4(kdst + off, &m.k2, 64 * half, rr[0], rr[1], rr[2], rr[3], full);
+            tma_gather4(vdst + off, &m.v2, 64 * half, rr[0], rr[1], rr[2], rr[3], full);
+          }
+          for (int k = 0; k < 4; ++k) wg[k] = wg_n[k];
         }
-        for (int half = 0; half < 2; ++half) {
-          const uint32_t off = half * kRegion + lane * 4 * 128;
-          tma_gather4(kdst + off, &m.k2, 64 * half, rr[0], rr[1], rr[2], rr[3], full);
-          tma_gather4(vdst + off, &m.v2, 64 * half, rr[0], rr[1], rr[2], rr[3], full);
-        }
-        for (int k = 0; k < 4; ++k) wg[k] = wg_n[k];
       }
     }
     x = xn;
@@ -313,14 +411,14 @@ __device__ void producer(const Launch& p, const Ctx& c, const Maps& m, int n_uni
   // A warp waits only for its own copies: tiles t < g of its parity (after a
   // time-out, g is the tile it did not copy), which fill the stages of its
   // parity; Q buffers are copied by warp 0 alone.
-  static_assert(kStages % 2 == 0, "a stage is filled by one producer warp");
+  static_assert(kNS % kWarpsCopying == 0, "a stage is filled by one producer warp");
   if (lane == 0) {
-    for (int st = pw; st < kStages; st += 2) {
-      const int last = (int)g - 1 - (((int)g - 1 - st) % kStages + kStages) % kStages;
-      if (last >= 0 && !mbar_wait(bar_addr(c, kFull0 + st), (last / kStages) & 1))
+    for (int st = pw; st < kNS; st += kWarpsCopying) {
+      const int last = (int)g - 1 - (((int)g - 1 - st) % kNS + kNS) % kNS;
+      if (last >= 0 && !mbar_wait(bar_addr(c, kFullB + st), (last / kNS) & 1))
         set_error(p.hdr, DA_DEVERR_TIMEOUT);
     }
-    for (int qb = 0; qb < 2 && pw == 0; ++qb) {
+    for (int qb = 0; qb < 2 && pw == 0 && !Q8; ++qb) {
       const int last = (int)nq - 1 - (((int)nq - 1 - qb) % 2 + 2) % 2;
       if (last >= 0 && !mbar_wait(bar_addr(c, kQFull0 + qb), (last >> 1) & 1))
         set_error(p.hdr, DA_DEVERR_TIMEOUT);
@@ -328,15 +426,131 @@ __device__ void producer(const Launch& p, const Ctx& c, const Maps& m, int n_uni
   }
 }
 
+// ---------------------------------------------------------------- converter
+// E4M3 cache only: warps 11-14.  Per unit, once the S MMAs of the unit two
+// back have released Q buffer qb (kQFree), each thread writes one MMA row of
+// Q into tensor memory -- warp w owns lanes 32 (w % 4) .. + 31 -- as f16
+// pairs, prescaled (q_prescale_exp; rows past the group are zeros), and the
+// MMA thread is told (kQConv).  Per tile, once its
+// bytes are in raw stage g % 3 and operand stage g % 3 is free (the PV three
+// tiles back completed), K and V are written as f16 into the operand stage in
+// the 128-byte-swizzled K-major layout the tensor core reads -- eight lanes
+// per 128-byte row, so every load reads four whole rows, and lanes jj and
+// jj + 4 (same chunk pair, other 64-dim region) store their two chunks in
+// opposite orders, so the eight lanes of a store phase hit eight different
+// bank groups -- and both stages are handed on.
+template <int R>
+__device__ void converter(const Launch& p, const Ctx& c, uint32_t tmem, int n_units) {
+  using L = Lay<true>;
+  constexpr int kGp = kRows / R;  // rows per copy of the group
+  const int ct = threadIdx.x - 11 * 32;  // 0..127
+  const int warp = threadIdx.x >> 5, lane = ct & 31;
+  const int qrow = 32 * (warp & 3) + lane;  // the MMA row (tensor-memory lane) of Q it writes
+  const int jq = qrow % kGp;                // that row's head in the group
+  const int G = p.H_q / p.H_kv;
+  const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+  uint32_t g = 0, nq = 0;
+  auto wait_w = [&](int bar, uint32_t parity) -> bool {
+    int ok = 1;
+    if (lane == 0) ok = wait_bar(c, bar, parity) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+  };
+  auto arrive_w = [&](int bar) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_addr(c, bar));
+  };
+  for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++nq) {
+    const TcUnit x = tc_unit(p, u);
+    const int n_sub = (x.t_end - x.t_begin + kT - 1) / kT;
+    const int qb = nq & 1;
+    // ---- Q into tensor-memory columns kQCol + 64 qb .. + 63 (dims 2c, 2c+1 in column c)
+    if (!wait_w(kQFree0 + qb, ((nq >> 1) & 1) ^ 1)) return;
+    umma::fence_after_sync();
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.q + ((size_t)x.b * p.H_q + (size_t)x.h * G + (jq < G ? jq : 0)) * kD);
+      float mx = 0.f;
+      if (jq < G) {
+#pragma unroll 4
+        for (int i = 0; i < kD / 8; ++i) mx = fmaxf(mx, bf16x8_absmax(__ldg(src + i)));
+      }
+      const float sc = exp2_int(q_prescale_exp(mx));
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        uint32_t r32[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 wi = jq < G ? __ldg(src + half * 8 + i) : make_uint4(0, 0, 0, 0);
+          const uint32_t v[4] = {wi.x, wi.y, wi.z, wi.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const __half2 hh = __floats2half2_rn(__uint_as_float(v[e] << 16) * sc,
+                                                 __uint_as_float(v[e] & 0xffff0000u) * sc);
+            r32[4 * i + e] = *reinterpret_cast<const uint32_t*>(&hh);
+          }
+        }
+        umma::st_32x32b_x32_u(lane_base + kQCol + qb * 64 + half * 32, r32);
+      }
+      umma::wait_st();
+    }
+    umma::fence_before_sync();
+    arrive_w(kQConv0 + qb);
+    // ---- K and V of every tile
+    const int jj = ct & 7;        // 16-byte piece (dims 16 jj .. 16 jj + 15) of a row
+    const int r0 = ct >> 3;       // rows r0, r0 + 16, r0 + 32, r0 + 48 of a tile
+    for (int i = 0; i < n_sub; ++i, ++g) {
+      const int rs = g % L::kRawStages, os = g % L::kStages;
+      if (!wait_w(kRawFull0 + rs, (g / L::kRawStages) & 1)) return;
+      if (!wait_w(kEmpty0 + os, ((g / L::kStages) & 1) ^ 1)) return;
+      const uint8_t* raw = c.smem + L::kRawOffset + rs * kRawStageBytes;
+      uint8_t* op = c.smem + L::kStageOffset + os * kStageBytes;
+#pragma unroll
+      for (int kv = 0; kv < 2; ++kv) {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int row = r0 + 16 * q4;
+          const uint4 b = *reinterpret_cast<const uint4*>(raw + kv * kRawTileBytes + row * kD +
+                                                          jj * 16);
+          const uint32_t wb[4] = {b.x, b.y, b.z, b.w};
+          uint32_t h[8];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            h[2 * e] = e4m3x2_to_f16x2(wb[e]);
+            h[2 * e + 1] = e4m3x2_to_f16x2(wb[e] >> 16);
+          }
+          // dims 16 jj .. +7 and +8 .. +15: region jj / 4, chunks 2 (jj % 4) and +1
+          uint8_t* rbase = op + kv * kTileBytes + (jj >> 2) * kRegion + row * 128;
+          const int ch = 2 * (jj & 3);
+          const int sw = jj >> 2;  // 0: chunk ch first, 1: chunk ch + 1 first
+          const uint4 lo = make_uint4(h[0], h[1], h[2], h[3]);
+          const uint4 hi = make_uint4(h[4], h[5], h[6], h[7]);
+          *reinterpret_cast<uint4*>(rbase + (((ch + sw) ^ (row & 7)) << 4)) = sw ? hi : lo;
+          *reinterpret_cast<uint4*>(rbase + (((ch + 1 - sw) ^ (row & 7)) << 4)) = sw ? lo : hi;
+        }
+      }
+      fence_proxy_async();
+      arrive_w(kFull0 + os);
+      arrive_w(kRawEmpty0 + rs);
+    }
+  }
+}
+
 // ---------------------------------------------------------------- MMA issue
+template <bool Q8>
 __device__ void mma_issuer(const Launch& p, const Ctx& c, uint32_t tmem, int n_units) {
+  using L = Lay<Q8>;
+  constexpr int kStages = L::kStages;
+  constexpr uint32_t kIdescS = idesc_s<Q8>(), kIdescO = idesc_o<Q8>();
+  // Q in a Q buffer is ready: copied (bf16), or copied and converted (E4M3)
+  constexpr int kQReady0 = Q8 ? kQConv0 : kQFull0;
   // K-major tiles, 128-byte swizzle: 8-row groups 1024 bytes apart
-  const uint64_t b_k0 = umma::smem_desc(c.sbase + kStageOffset, 16, 1024, umma::kSwizzle128B);
+  const uint64_t b_k0 =
+      umma::smem_desc(c.sbase + L::kStageOffset, 16, 1024, umma::kSwizzle128B);
   const uint64_t a_q0 = umma::smem_desc(c.sbase, 16, 1024, umma::kSwizzle128B);
   // V as an MN-major B operand: 64-dim regions kRegion apart, 8-entry groups
   // 1024 bytes apart
-  const uint64_t b_v0 =
-      umma::smem_desc(c.sbase + kStageOffset + kTileBytes, kRegion, 1024, umma::kSwizzle128B);
+  const uint64_t b_v0 = umma::smem_desc(c.sbase + L::kStageOffset + kTileBytes, kRegion, 1024,
+                                        umma::kSwizzle128B);
   uint32_t g = 0, nq = 0;
   // time-out test hook: a wait that runs out, then the abort path
   if (p.test_stall && !wait_bar(c, kStall, 0, kTestStallNs)) return;
@@ -344,7 +558,7 @@ __device__ void mma_issuer(const Launch& p, const Ctx& c, uint32_t tmem, int n_u
     const TcUnit x = tc_unit(p, u);
     const int n_sub = (x.t_end - x.t_begin + kT - 1) / kT;
     const int qb = nq & 1, ob = nq & 1;
-    if (!wait_bar(c, kQFull0 + qb, (nq >> 1) & 1)) return;
+    if (!wait_bar(c, kQReady0 + qb, (nq >> 1) & 1)) return;
     fence_proxy_async();
     // O += P(gp) V(gp): P sits over the K tile of stage gp, V after it
     auto pv = [&](uint32_t gp, bool first) -> bool {
@@ -376,9 +590,14 @@ __device__ void mma_issuer(const Launch& p, const Ctx& c, uint32_t tmem, int n_u
 #pragma unroll
       for (int k = 0; k < kD / 16; ++k) {  // dims 16k .. 16k + 15
         const uint32_t off = (k / 4) * kRegion + (k % 4) * 32;
-        const uint32_t offq = (k / 4) * kQRegion + (k % 4) * 32;
-        umma::mma_bf16(tmem + kSCol + sb * kT, a0 + (uint64_t)(offq >> 4),
-                       b0 + (uint64_t)(off >> 4), kIdescS, k ? 1u : 0u);
+        if constexpr (Q8) {  // A = Q in tensor memory (8 columns per 16 dims)
+          umma::mma_bf16_ta(tmem + kSCol + sb * kT, tmem + kQCol + qb * 64 + k * 8,
+                            b0 + (uint64_t)(off >> 4), kIdescS, k ? 1u : 0u);
+        } else {
+          const uint32_t offq = (k / 4) * kQRegion + (k % 4) * 32;
+          umma::mma_bf16(tmem + kSCol + sb * kT, a0 + (uint64_t)(offq >> 4),
+                         b0 + (uint64_t)(off >> 4), kIdescS, k ? 1u : 0u);
+        }
       }
       umma::commit(bar_addr(c, kSFull0 + sb));
       if (i == n_sub - 1) umma::commit(bar_addr(c, kQFree0 + qb));
@@ -400,8 +619,9 @@ __device__ void mma_issuer(const Launch& p, const Ctx& c, uint32_t tmem, int n_u
 // order, the combine arithmetic of the split/merge step:
 //     M = max_c m_c,  L = sum_c 2^(m_c - M) l_c,  O = sum_c 2^(m_c - M) O_c / L.
 // All of it depends only on the unit's own data.
-template <int R>
+template <int R, bool Q8>
 __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int n_units) {
+  using L = Lay<Q8>;
   constexpr int kGp = kRows / R;              // rows per copy
   constexpr int kCpt = kT / R;                // entries of a tile per copy
   constexpr int kCopiesPerWarp = kGp < 32 ? 32 / kGp : 1;
@@ -415,7 +635,7 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
   const int wcol0 = (warp * 32 / kGp) * kCpt;  // first S column this warp loads
   const int col0 = cp * kCpt;                  // first entry of the tile this row takes
   const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-  float* ml = reinterpret_cast<float*>(c.smem + kMergeOffset);  // [2 buffers][m, l][128]
+  float* ml = c.merge;  // [2 buffers][m, l][128]
   uint32_t g = 0, nq = 0;
   auto wait_w = [&](int bar, uint32_t parity) -> bool {
     int ok = 1;
@@ -430,6 +650,20 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
     const TcUnit x = tc_unit(p, u);
     const int n_sub = (x.t_end - x.t_begin + kT - 1) / kT;
     const int ob = nq & 1;
+    // E4M3 cache: the row's Q was prescaled by 2^e into f16 (the converter
+    // derives e from the same 128 values, see q_prescale_exp), so its scores
+    // carry that factor; the row takes it back in its softmax scale
+    float row_scale = p.scale_log2;
+    if constexpr (Q8) {
+      if (live) {
+        const uint4* qr = reinterpret_cast<const uint4*>(
+            p.q + ((size_t)x.b * p.H_q + (size_t)x.h * G + j) * kD);
+        float mx = 0.f;
+#pragma unroll 4
+        for (int i = 0; i < kD / 8; ++i) mx = fmaxf(mx, bf16x8_absmax(__ldg(qr + i)));
+        row_scale *= exp2_int(-q_prescale_exp(mx));
+      }
+    }
     const uint32_t o_col = kOCol + ob * kD;
     float m_used = -INFINITY, l = 0.f;
     for (int i = 0; i < n_sub; ++i, ++g) {
@@ -460,7 +694,7 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
 #pragma unroll
       for (int k = 0; k < kCpt; ++k) {
         // padding rows score 0 everywhere (their Q rows hold arbitrary bytes)
-        s[k] = !live ? 0.f : (k < n_valid) ? s[k] * p.scale_log2 : -INFINITY;
+        s[k] = !live ? 0.f : (k < n_valid) ? s[k] * row_scale : -INFINITY;
         mt = fmaxf(mt, s[k]);
       }
       // the reference value moves on the row's first scores and when a score
@@ -476,8 +710,13 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
         const float p1 = (m_new == -INFINITY) ? 0.f : ex2(s[k + 1] - m_new);
         sum += p0;
         sum += p1;
-        const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-        pk[k / 2] = *reinterpret_cast<const uint32_t*>(&h);
+        if constexpr (Q8) {  // f16 operands
+          const __half2 h = __floats2half2_rn(p0, p1);
+          pk[k / 2] = *reinterpret_cast<const uint32_t*>(&h);
+        } else {
+          const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+          pk[k / 2] = *reinterpret_cast<const uint32_t*>(&h);
+        }
       }
       l = fmaf(l, alpha, sum);
       // rescale the row's O when its reference value moved; the previous P.V
@@ -500,7 +739,7 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
       // P row (64 bf16 = 128 bytes: this copy's entries, zeros elsewhere) over
       // the K tile of this tile's stage, in the 128-byte-swizzled K-major
       // layout (S(g), the K tile's only reader, has completed)
-      uint8_t* prow = c.smem + kStageOffset + (g % kStages) * kStageBytes + row * 128;
+      uint8_t* prow = c.smem + L::kStageOffset + (g % L::kStages) * kStageBytes + row * 128;
 #pragma unroll
       for (int cc = 0; cc < 8; ++cc) {
         uint4 v = make_uint4(0, 0, 0, 0);
@@ -529,7 +768,7 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
 // and write O / L (bf16 output of a single-split row, else the fp32 partial
 // and its LSE in log2 units).  Thread t of the group, for each 32-column
 // chunk, sums the R copies of head t % Gp over 32/R of the columns.
-template <int R>
+template <int R, bool Q8>
 __device__ void epilogue_warps(const Launch& p, const Ctx& c, uint32_t tmem, int n_units) {
   constexpr int kGp = kRows / R;
   constexpr int kCols = 32 / R;  // columns of a chunk a thread sums
@@ -537,8 +776,8 @@ __device__ void epilogue_warps(const Launch& p, const Ctx& c, uint32_t tmem, int
   const int row = q * 32 + lane;  // TMEM lane = row of the MMA
   const int G = p.H_q / p.H_kv;
   const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-  const float* ml = reinterpret_cast<const float*>(c.smem + kMergeOffset);
-  float* ob_s = reinterpret_cast<float*>(c.smem + kMergeOffset) + 2 * 2 * kRows;  // [128][33]
+  const float* ml = c.merge;
+  float* ob_s = c.merge + 2 * 2 * kRows;  // [128][33]
   const int jt = row % kGp, kq = row / kGp;  // the head and column slice this thread sums
   uint32_t nq = 0;
   auto wait_w = [&](int bar, uint32_t parity) -> bool {
@@ -571,7 +810,8 @@ __device__ void epilogue_warps(const Launch& p, const Ctx& c, uint32_t tmem, int
     const float f = (m_row == -INFINITY) ? 0.f : ex2(m_row - M);
     const bool writer = jt < G;
     const int hq = x.h * G + jt;
-    const float inv = (L > 0.f) ? 1.f / L : 0.f;
+    // (an E4M3 cache's V scale multiplies the output once, here)
+    const float inv = ((L > 0.f) ? 1.f / L : 0.f) * (Q8 ? p.v_scale : 1.f);
 #pragma unroll 1
     for (int ch = 0; ch < kD / 32; ++ch) {
       float o[32];
@@ -624,14 +864,18 @@ __device__ void epilogue_warps(const Launch& p, const Ctx& c, uint32_t tmem, int
   }
 }
 
-template <int R>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int R, bool Q8>
+__global__ void __launch_bounds__(Lay<Q8>::kThreads, 1)
     split_gqa_tc_kernel(Launch p, const __grid_constant__ Maps maps, int box) {
+  using L = Lay<Q8>;
+  constexpr int kThreads = L::kThreads;
   extern __shared__ __align__(1024) uint8_t smem[];
   Ctx c;
   c.smem = smem;
   c.sbase = smem_addr(smem);
-  c.abort_flag = reinterpret_cast<volatile int*>(smem + kAbortSlot);
+  c.bars = c.sbase + L::kBarOffset;
+  c.merge = reinterpret_cast<float*>(smem + L::kMergeOffset);
+  c.abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbortSlot);
   c.hdr = p.hdr;
   const int warp = threadIdx.x >> 5;
   wait_prior_grid();  // the plan kernel's outputs
@@ -658,30 +902,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       if ((i >= kSFree0 && i < kSFree0 + 2) || (i >= kPFull0 && i < kPFull0 + 2) ||
           (i >= kEpiReady0 && i < kEpiReady0 + 2) || (i >= kOFree0 && i < kOFree0 + 2))
         count = 4;  // the four softmax (or, for kOFree, epilogue) warps
+      // E4M3 cache: the four converter warps fill the operand stages, free
+      // the raw stages and report each converted Q buffer
+      if (Q8 && ((i >= kFull0 && i < kFull0 + kMaxStages) ||
+                 (i >= kRawEmpty0 && i < kRawEmpty0 + kMaxStages) ||
+                 (i >= kQConv0 && i < kQConv0 + 2)))
+        count = 4;
       mbar_init(bar_addr(c, i), count);
     }
     *c.abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 10) {
-    umma::tmem_alloc(c.sbase + kTmemSlot, kTmemCols);
+    umma::tmem_alloc(c.sbase + L::kTmemSlot, kTmemCols);
     umma::tmem_relinquish();
   }
   umma::fence_before_sync();
   __syncthreads();
   umma::fence_after_sync();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kTmemSlot);
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
 
   if (warp < 4) {
-    softmax_warps<R>(p, c, tmem, n_units);
+    softmax_warps<R, Q8>(p, c, tmem, n_units);
   } else if (warp < 8) {
-    epilogue_warps<R>(p, c, tmem, n_units);
+    epilogue_warps<R, Q8>(p, c, tmem, n_units);
   } else if (warp < 10) {
-    producer(p, c, maps, n_units, box != 0, R);
-  } else if ((threadIdx.x & 31) == 0) {
-    mma_issuer(p, c, tmem, n_units);
-    // drain: its arrival means every MMA issued before it has completed
-    umma::commit(bar_addr(c, kDrain));
+    producer<Q8>(p, c, maps, n_units, box != 0, R);
+  } else if (warp == 10) {
+    if ((threadIdx.x & 31) == 0) {
+      mma_issuer<Q8>(p, c, tmem, n_units);
+      // drain: its arrival means every MMA issued before it has completed
+      umma::commit(bar_addr(c, kDrain));
+    }
+  } else if constexpr (Q8) {
+    converter<R>(p, c, tmem, n_units);
   }
   umma::fence_before_sync();
   __syncthreads();
@@ -718,15 +972,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// A bf16 map of `rank` dims (dim 0 = 128 elements of a head row), 128-byte
-// swizzle, zero fill past the bounds.
+// A map of `rank` dims (dim 0 = the 128 elements of a head row), zero fill
+// past the bounds: bf16 elements with the 128-byte swizzle (operands copied
+// straight into the tensor core's layout), or bytes without swizzle (E4M3
+// rows for the converter).
 bool encode(CUtensorMap* tm, const void* base, int rank, const cuuint64_t* dims,
-            const cuuint64_t* strides, const cuuint32_t* box) {
+            const cuuint64_t* strides, const cuuint32_t* box, bool bytes) {
   const PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return false;
   const cuuint32_t elem[3] = {1, 1, 1};
-  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides,
-            box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  return fn(tm, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
+            const_cast<void*>(base), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            bytes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -737,31 +994,46 @@ int copies_for(int G) {
   return kRows / gp;
 }
 
-template <int R>
+template <int R, bool Q8>
 cudaError_t set_smem() {
-  static const cudaError_t e = cudaFuncSetAttribute(
-      split_gqa_tc_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  static const cudaError_t e =
+      cudaFuncSetAttribute(split_gqa_tc_kernel<R, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Lay<Q8>::kSmemBytes);
   return e;
 }
 
 int tc_ctas_per_sm() {
   static const int n = [] {
-    if (set_smem<1>() != cudaSuccess) return 1;
+    if (set_smem<1, false>() != cudaSuccess) return 1;
     int c = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, split_gqa_tc_kernel<1>, kThreads,
-                                                      kSmemBytes) != cudaSuccess || c < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, split_gqa_tc_kernel<1, false>,
+                                                      Lay<false>::kThreads,
+                                                      Lay<false>::kSmemBytes) != cudaSuccess ||
+        c < 1)
       c = 1;
     return c;
   }();
   return n;
 }
+static_assert(Lay<true>::kSmemBytes > 232448 / 2 && Lay<false>::kSmemBytes > 232448 / 2,
+              "both layouts run one CTA per SM (the grid is sized from one)");
 
-template <int R>
+template <int R, bool Q8>
 cudaError_t launch_r(const Launch& p, const Maps& m, int box, int grid, cudaStream_t stream) {
-  const cudaError_t e = set_smem<R>();
+  const cudaError_t e = set_smem<R, Q8>();
   if (e != cudaSuccess) return e;
-  return launch_after(split_gqa_tc_kernel<R>, dim3(grid), dim3(kThreads), (size_t)kSmemBytes,
-                      stream, p, m, box);
+  return launch_after(split_gqa_tc_kernel<R, Q8>, dim3(grid), dim3(Lay<Q8>::kThreads),
+                      (size_t)Lay<Q8>::kSmemBytes, stream, p, m, box);
+}
+
+template <bool Q8>
+cudaError_t launch_q(const Launch& p, const Maps& m, int box, int grid, cudaStream_t stream) {
+  switch (copies_for(p.H_q / p.H_kv)) {
+    case 8: return launch_r<8, Q8>(p, m, box, grid, stream);
+    case 4: return launch_r<4, Q8>(p, m, box, grid, stream);
+    case 2: return launch_r<2, Q8>(p, m, box, grid, stream);
+    default: return launch_r<1, Q8>(p, m, box, grid, stream);
+  }
 }
 
 }  // namespace
@@ -772,8 +1044,10 @@ int gqa_tc_resident_ctas(int sms) { return tc_ctas_per_sm() * sms; }
 
 cudaError_t launch_split_gqa_tc(const Launch& p, int grid, cudaStream_t stream) {
   const int G = p.H_q / p.H_kv;
-  if (!gqa_tc_supported(G, p.D_qk) || p.D_v != kD || p.extra_k || p.kv_type != 0)
+  // bf16 or E4M3 caches (kv_type 0 or 1), one source
+  if (!gqa_tc_supported(G, p.D_qk) || p.D_v != kD || p.extra_k || (p.kv_type != 0 && p.kv_type != 1))
     return cudaErrorInvalidValue;
+  const bool q8 = p.kv_type == 1;
   const long long rows = (p.layout == DA_KV_CONTIGUOUS) ? (long long)p.B * p.width
                          : (p.layout == DA_KV_PAGED)    ? p.num_blocks * p.page_size
                                                         : p.num_blocks;
@@ -784,31 +1058,33 @@ cudaError_t launch_split_gqa_tc(const Launch& p, int grid, cudaStream_t stream) 
   const void* kb = p.k;
   const void* vb = p.v;
   long long r = rows;
+  long long heads = p.H_kv;
   if (rows < 1) {  // an empty cache: every entry is masked, copies read zeros
+    // (one zero row in the map: every other coordinate lies past its bounds
+    // and reads the zero fill)
     void* z = nullptr;
     if (cudaGetSymbolAddress(&z, g_zero_tile) != cudaSuccess) return cudaErrorInvalidValue;
     kb = vb = z;
     r = 1;
+    heads = 1;
   }
-  if (r * p.H_kv >= (1ll << 31)) return cudaErrorInvalidValue;  // signed TMA coordinates
-  const cuuint64_t d3[3] = {(cuuint64_t)kD, (cuuint64_t)p.H_kv, (cuuint64_t)r};
-  const cuuint64_t s3[2] = {(cuuint64_t)kD * 2, (cuuint64_t)p.H_kv * kD * 2};
-  const cuuint32_t b3[3] = {64, 1, 16};
-  const cuuint64_t d2[2] = {(cuuint64_t)kD, (cuuint64_t)(r * p.H_kv)};
-  const cuuint64_t s2[1] = {(cuuint64_t)kD * 2};
-  const cuuint32_t b2[2] = {64, 1};
+  if (r * heads >= (1ll << 31)) return cudaErrorInvalidValue;  // signed TMA coordinates
+  const cuuint64_t es = q8 ? 1 : 2;  // bytes per cache element
+  const cuuint64_t d3[3] = {(cuuint64_t)kD, (cuuint64_t)heads, (cuuint64_t)r};
+  const cuuint64_t s3[2] = {(cuuint64_t)kD * es, (cuuint64_t)heads * kD * es};
+  const cuuint32_t b3[3] = {q8 ? 128u : 64u, 1, 16};
+  const cuuint64_t d2[2] = {(cuuint64_t)kD, (cuuint64_t)(r * heads)};
+  const cuuint64_t s2[1] = {(cuuint64_t)kD * es};
+  const cuuint32_t b2[2] = {q8 ? 128u : 64u, 1};
   const cuuint64_t dq[2] = {(cuuint64_t)kD, (cuuint64_t)p.B * p.H_q};
+  const cuuint64_t sq[1] = {(cuuint64_t)kD * 2};
   const cuuint32_t bq[2] = {64, (cuuint32_t)kQBoxRows};
-  if (!encode(&m.k3, kb, 3, d3, s3, b3) || !encode(&m.v3, vb, 3, d3, s3, b3) ||
-      !encode(&m.k2, kb, 2, d2, s2, b2) || !encode(&m.v2, vb, 2, d2, s2, b2) ||
-      !encode(&m.q, p.q, 2, dq, s2, bq))
+  if (!encode(&m.k3, kb, 3, d3, s3, b3, q8) || !encode(&m.v3, vb, 3, d3, s3, b3, q8) ||
+      !encode(&m.k2, kb, 2, d2, s2, b2, q8) || !encode(&m.v2, vb, 2, d2, s2, b2, q8) ||
+      !encode(&m.q, p.q, 2, dq, sq, bq, false))
     return cudaErrorInvalidValue;
-  switch (copies_for(G)) {
-    case 8: return launch_r<8>(p, m, box ? 1 : 0, grid, stream);
-    case 4: return launch_r<4>(p, m, box ? 1 : 0, grid, stream);
-    case 2: return launch_r<2>(p, m, box ? 1 : 0, grid, stream);
-    default: return launch_r<1>(p, m, box ? 1 : 0, grid, stream);
-  }
+  return q8 ? launch_q<true>(p, m, box ? 1 : 0, grid, stream)
+            : launch_q<false>(p, m, box ? 1 : 0, grid, stream);
 }
 
 }  // namespace da

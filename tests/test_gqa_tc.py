@@ -10,6 +10,7 @@ ragged sweep, solo against batched rows, repeats), and the variant choice
 (CPU checks need no GPU)."""
 
 import ctypes
+import dataclasses
 
 import pytest
 import torch
@@ -46,9 +47,14 @@ def test_tensor_core_variant_for_large_groups(api, g):
     assert tuple(consts) == OP.VARIANT_CONSTANTS["gqa_tc"]
 
 
+def test_e4m3_cache_takes_the_tensor_core_variant(api):
+    prob = _prob(api, 32, kv_dtype=api.KV_FP8_E4M3, k_scale=0.5, v_scale=0.25)
+    assert api.split_constants(prob)[0] == api.VARIANT_GQA_TC
+
+
 def test_other_large_group_configs_stay_on_cuda_cores(api):
     for prob in (_prob(api, 16, d=64), _prob(api, 15),
-                 _prob(api, 16, kv_dtype=api.KV_FP8_E4M3, k_scale=1.0, v_scale=1.0),
+                 _prob(api, 16, kv_dtype=api.KV_NVFP4, k_scale=1.0, v_scale=1.0),
                  _prob(api, 16, extra_width=8, extra_num_blocks=10)):
         variant, *consts = api.split_constants(prob)
         assert variant == api.VARIANT_FMA
@@ -166,6 +172,87 @@ def test_tc_runs_of_one_tile_units(api):
     api.run(pl, g.q, g.k, g.v, g.table, g.lengths, out, lse)
     api.combine(pl, out, lse)
     assert api.read_error(pl) == 0
+    rows = [0, 1, 63, 150, 299, 300, 301, 302]
+    ro, rl = oracle_for(wl, rows=rows)
+    assert_parity(out, lse, ro, rl, rows=rows)
+
+
+# ---------------------------------------------------------------- E4M3 caches
+# The same variant on one-byte caches: the bytes are converted to f16 in
+# shared memory (exact), Q is prescaled per row by a power of two into f16's
+# range, the MMAs run on f16 operands; the oracle decodes the same bytes.
+
+@gpu
+@pytest.mark.parametrize("layout,page", [(W.PAGED, 16), (W.PAGED, 100), (W.CONTIGUOUS, 0),
+                                         (W.INDEXED, 0)])
+@pytest.mark.parametrize("g", [16, 32])
+def test_tc_fp8_parity_layouts(api, layout, page, g):
+    base = W.make(layout, EDGE, H_q=2 * g, H_kv=2, D_qk=128, page_size=page or 16,
+                  num_slots=6000, seed=700 + g + page)
+    wl = W.quantize_fp8(base, k_scale=0.37, v_scale=3.0)
+    assert api.split_constants(api.problem_for(wl))[0] == api.VARIANT_GQA_TC
+    out, lse = api.run_workload(wl.to("cuda"))
+    ro, rl = oracle_for(wl)
+    assert_parity(out, lse, ro, rl)
+
+
+@gpu
+@pytest.mark.parametrize("g", [20, 64, 128])
+def test_tc_fp8_parity_group_sizes(api, g):
+    wl = W.quantize_fp8(W.make(W.PAGED, [1, 77, 1024, 3000], H_q=g, H_kv=1, D_qk=128,
+                               page_size=32, seed=800 + g))
+    out, lse = api.run_workload(wl.to("cuda"))
+    ro, rl = oracle_for(wl)
+    assert_parity(out, lse, ro, rl)
+
+
+@gpu
+def test_tc_fp8_query_scales(api):
+    # query rows of very different magnitudes (the per-row power-of-two
+    # prescale into f16), and a row of zeros
+    wl = W.quantize_fp8(W.make(W.PAGED, [500, 2000], H_q=32, H_kv=2, D_qk=128, page_size=16,
+                               seed=901))
+    q = wl.q.float()
+    q[0, :8] *= 2.0 ** 6
+    q[0, 8:16] *= 2.0 ** -20
+    q[1, 3] = 0.0
+    wl = dataclasses.replace(wl, q=q.to(torch.bfloat16))
+    out, lse = api.run_workload(wl.to("cuda"))
+    ro, rl = oracle_for(wl)
+    assert_parity(out, lse, ro, rl)
+
+
+@gpu
+def test_tc_fp8_gqa16_config(api):
+    wl = W.quantize_fp8(W.gqa16_paged())
+    out, lse = api.run_workload(wl.to("cuda"))
+    rows = list(range(0, wl.B, 5))
+    ro, rl = oracle_for(wl, rows=rows)
+    assert_parity(out, lse, ro, rl, rows=rows)
+
+
+@gpu
+def test_tc_fp8_ragged_sweep_bitwise(api):
+    sweep = W.RaggedSweep(range(1, 257), H_q=128, kv_fp8=True)
+    o_solo, l_solo = api.run_workload(sweep.solo())
+    ro, rl = oracle_for(sweep.solo_cpu())
+    assert_parity(o_solo, l_solo, ro, rl)
+    for i in range(len(sweep.sizes)):
+        wl, pos = sweep.batch(i)
+        o, l = api.run_workload(wl)
+        assert torch.equal(o[pos], o_solo[0]), f"B={wl.B} pos={pos}"
+        assert torch.equal(l[pos], l_solo[0]), f"B={wl.B} pos={pos}"
+        if i in (0, 63, 255):
+            for _ in range(3):
+                o2, l2 = api.run_workload(wl)
+                assert torch.equal(o2, o) and torch.equal(l2, l)
+
+
+@gpu
+def test_tc_fp8_runs_of_one_tile_units(api):
+    lens = [1 + (37 * i) % 64 for i in range(300)] + [5000, 0, 130]
+    wl = W.quantize_fp8(W.make(W.PAGED, lens, H_q=64, H_kv=4, D_qk=128, page_size=16, seed=98))
+    out, lse = api.run_workload(wl.to("cuda"))
     rows = [0, 1, 63, 150, 299, 300, 301, 302]
     ro, rl = oracle_for(wl, rows=rows)
     assert_parity(out, lse, ro, rl, rows=rows)

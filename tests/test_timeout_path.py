@@ -34,6 +34,8 @@ def _workloads():
                       latent=True, num_slots=4096, seed=71),
         "gqa_tc": W.make(W.PAGED, [40, 300, 1500, 5000], H_q=64, H_kv=2, D_qk=128,
                          page_size=16, seed=72),
+        "gqa_tc_fp8": W.quantize_fp8(W.make(W.PAGED, [40, 300, 1500, 5000], H_q=64, H_kv=2,
+                                            D_qk=128, page_size=16, seed=73)),
     }
 
 
@@ -48,7 +50,7 @@ def test_flag_validation(api):
 
 
 @gpu
-@pytest.mark.parametrize("kind", ["mla", "gqa_tc"])
+@pytest.mark.parametrize("kind", ["mla", "gqa_tc", "gqa_tc_fp8"])
 def test_stall_times_out_and_context_stays_usable(api, kind):
     wl = _workloads()[kind]
     g = wl.to("cuda")
