@@ -33,13 +33,15 @@
 // and entries whose page or slot is out of range, copy cache row 0 instead
 // (their scores are masked), so no stage byte is ever uninitialised.
 //
-// Roles (352 threads): warps 0-3 softmax; warps 4-7 epilogue (a unit's O
-// merge and output while the softmax warps go on with the next unit); warps
-// 8-9 producer (page or index lookups ahead of the copies, TMA issue; the two
+// Roles: warps 0-3 softmax; warps 4-7 epilogue (a unit's O merge and output
+// while the softmax warps go on with the next unit); warps 8-9 producer (page
+// or index lookups ahead of the copies, TMA issue; for a bf16 cache the two
 // warps take alternate tiles, so one issues copies while the other waits for
-// its next stage); warp 10 MMA issue (one thread) and TMEM allocation.  Every mbarrier wait is bounded; on time-out
-// the kernel records DA_DEVERR_TIMEOUT, every role leaves its loop,
-// outstanding tensor-core work is drained (bounded) and TMEM is freed.
+// its next stage; for an E4M3 cache warp 8 alone); warp 10 the S MMAs (one
+// thread) and TMEM allocation; E4M3 cache: warps 11-14 converter; last warp
+// the P.V MMAs (one thread).  Every mbarrier wait is bounded; on time-out the
+// kernel records DA_DEVERR_TIMEOUT, every role leaves its loop, outstanding
+// tensor-core work is drained (bounded) and TMEM is freed.
 //
 // Softmax attention and its split/merge are the computation "Sparse MLA
 // decode is not batch-invariant" (FlashMLA issue #212) reports on; which CTA
@@ -71,8 +73,13 @@ enum {
   kRawEmpty0 = kRawFull0 + kMaxStages,        // E4M3 cache: converted, reusable
   kQConv0 = kRawEmpty0 + kMaxStages,          // E4M3 cache: Q written to tensor memory
   kQFull0 = kQConv0 + 2, kQFree0 = kQFull0 + 2,
-  kSFull0 = kQFree0 + 2, kSFree0 = kSFull0 + 2, kPFull0 = kSFree0 + 2, kPVDone0 = kPFull0 + 2,
-  kODone0 = kPVDone0 + 2, kEpiReady0 = kODone0 + 2, kOFree0 = kEpiReady0 + 2,
+  // P ready and P.V done: four slots each (tile g uses slot g % 4, phase
+  // g / 4).  The S and P.V MMAs are issued by two threads, so the softmax can
+  // run up to three tiles ahead of the P.V thread (S(g) needs stage g's copy,
+  // which needs P.V(g - kStages) done); four slots keep every parity wait
+  // within one phase of its barrier.
+  kSFull0 = kQFree0 + 2, kSFree0 = kSFull0 + 2, kPFull0 = kSFree0 + 2, kPVDone0 = kPFull0 + 4,
+  kODone0 = kPVDone0 + 4, kEpiReady0 = kODone0 + 2, kOFree0 = kEpiReady0 + 2,
   kDrain = kOFree0 + 2,
   kStall,  // never signalled: the time-out test hook waits on it
   kNumBars
@@ -101,8 +108,10 @@ struct Lay {
   // padded to 33 floats)
   static constexpr int kMergeOffset = (kAbortSlot + 4 + 15) / 16 * 16;
   static constexpr int kSmemBytes = kMergeOffset + (2 * 2 * kRows + kRows * 33) * 4;
-  // warps 0-3 softmax, 4-7 epilogue, 8-9 producer, 10 MMA, 11-14 converter
-  static constexpr int kThreads = Q8 ? 480 : 352;
+  // warps 0-3 softmax, 4-7 epilogue, 8-9 producer, 10 S MMAs, 11-14
+  // converter (E4M3), then the P.V MMAs' warp
+  static constexpr int kPvWarp = Q8 ? 15 : 11;
+  static constexpr int kThreads = (kPvWarp + 1) * 32;
   static_assert(kStageOffset % 1024 == 0 && kRawOffset % 1024 == 0, "aligned stages");
   static_assert(kStages <= kMaxStages && kRawStages <= kMaxStages, "barrier slots");
   static_assert(kSmemBytes <= 232448, "fits the 227 KB per-block limit");
@@ -536,48 +545,30 @@ __device__ void converter(const Launch& p, const Ctx& c, uint32_t tmem, int n_un
 }
 
 // ---------------------------------------------------------------- MMA issue
+// Two issuing threads, so that S(g+1) never waits behind PV(g), which needs
+// the softmax of tile g: warp 10 issues the S MMAs, warp kPvWarp the P.V
+// MMAs.  A tcgen05.commit tracks the MMAs of its own thread, so each thread's
+// commits free exactly what its MMAs read.
 template <bool Q8>
-__device__ void mma_issuer(const Launch& p, const Ctx& c, uint32_t tmem, int n_units) {
+__device__ void mma_s(const Launch& p, const Ctx& c, uint32_t tmem, int n_units) {
   using L = Lay<Q8>;
   constexpr int kStages = L::kStages;
-  constexpr uint32_t kIdescS = idesc_s<Q8>(), kIdescO = idesc_o<Q8>();
-  // Q in a Q buffer is ready: copied (bf16), or copied and converted (E4M3)
+  constexpr uint32_t kIdescS = idesc_s<Q8>();
+  // Q in a Q buffer is ready: copied (bf16), or written to tensor memory (E4M3)
   constexpr int kQReady0 = Q8 ? kQConv0 : kQFull0;
   // K-major tiles, 128-byte swizzle: 8-row groups 1024 bytes apart
   const uint64_t b_k0 =
       umma::smem_desc(c.sbase + L::kStageOffset, 16, 1024, umma::kSwizzle128B);
   const uint64_t a_q0 = umma::smem_desc(c.sbase, 16, 1024, umma::kSwizzle128B);
-  // V as an MN-major B operand: 64-dim regions kRegion apart, 8-entry groups
-  // 1024 bytes apart
-  const uint64_t b_v0 = umma::smem_desc(c.sbase + L::kStageOffset + kTileBytes, kRegion, 1024,
-                                        umma::kSwizzle128B);
   uint32_t g = 0, nq = 0;
   // time-out test hook: a wait that runs out, then the abort path
   if (p.test_stall && !wait_bar(c, kStall, 0, kTestStallNs)) return;
   for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++nq) {
     const TcUnit x = tc_unit(p, u);
     const int n_sub = (x.t_end - x.t_begin + kT - 1) / kT;
-    const int qb = nq & 1, ob = nq & 1;
+    const int qb = nq & 1;
     if (!wait_bar(c, kQReady0 + qb, (nq >> 1) & 1)) return;
     fence_proxy_async();
-    // O += P(gp) V(gp): P sits over the K tile of stage gp, V after it
-    auto pv = [&](uint32_t gp, bool first) -> bool {
-      if (!wait_bar(c, kPFull0 + (gp & 1), (gp >> 1) & 1)) return false;
-      if (first && !wait_bar(c, kOFree0 + ob, ((nq >> 1) & 1) ^ 1)) return false;
-      umma::fence_after_sync();
-      const uint32_t st = (gp % kStages) * kStageBytes;
-      const uint64_t ap = b_k0 + (uint64_t)(st >> 4);
-      const uint64_t bv = b_v0 + (uint64_t)(st >> 4);
-#pragma unroll
-      for (int kk = 0; kk < kT / 16; ++kk)
-        umma::mma_bf16(tmem + kOCol + ob * kD, ap + (uint64_t)((kk * 32) >> 4),
-                       bv + (uint64_t)((kk * 2048) >> 4), kIdescO, (first && kk == 0) ? 0u : 1u);
-      umma::commit(bar_addr(c, kPVDone0 + (gp & 1)));
-      umma::commit(bar_addr(c, kEmpty0 + (gp % kStages)));
-      return true;
-    };
-    // issue order S(g), PV(g-1): S(g) goes to the other S buffer, so it runs
-    // while the softmax of tile g-1 is still producing P(g-1)
     for (int i = 0; i < n_sub; ++i, ++g) {
       const int st = g % kStages;
       const int sb = g & 1;
@@ -601,9 +592,43 @@ __device__ void mma_issuer(const Launch& p, const Ctx& c, uint32_t tmem, int n_u
       }
       umma::commit(bar_addr(c, kSFull0 + sb));
       if (i == n_sub - 1) umma::commit(bar_addr(c, kQFree0 + qb));
-      if (i > 0 && !pv(g - 1, i == 1)) return;
     }
-    if (!pv(g - 1, n_sub == 1)) return;
+  }
+}
+
+// O += P(g) V(g): P sits over the K tile of stage g % kStages (the softmax
+// wrote it once S(g) had read that tile), V after it.
+template <bool Q8>
+__device__ void mma_pv(const Launch& p, const Ctx& c, uint32_t tmem, int n_units) {
+  using L = Lay<Q8>;
+  constexpr int kStages = L::kStages;
+  static_assert(kStages <= 4, "the four P slots cover the softmax's lead");
+  constexpr uint32_t kIdescO = idesc_o<Q8>();
+  const uint64_t b_k0 =
+      umma::smem_desc(c.sbase + L::kStageOffset, 16, 1024, umma::kSwizzle128B);
+  // V as an MN-major B operand: 64-dim regions kRegion apart, 8-entry groups
+  // 1024 bytes apart
+  const uint64_t b_v0 = umma::smem_desc(c.sbase + L::kStageOffset + kTileBytes, kRegion, 1024,
+                                        umma::kSwizzle128B);
+  uint32_t g = 0, nq = 0;
+  for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++nq) {
+    const TcUnit x = tc_unit(p, u);
+    const int n_sub = (x.t_end - x.t_begin + kT - 1) / kT;
+    const int ob = nq & 1;
+    for (int i = 0; i < n_sub; ++i, ++g) {
+      if (!wait_bar(c, kPFull0 + (g & 3), (g >> 2) & 1)) return;
+      if (i == 0 && !wait_bar(c, kOFree0 + ob, ((nq >> 1) & 1) ^ 1)) return;
+      umma::fence_after_sync();
+      const uint32_t st = (g % kStages) * kStageBytes;
+      const uint64_t ap = b_k0 + (uint64_t)(st >> 4);
+      const uint64_t bv = b_v0 + (uint64_t)(st >> 4);
+#pragma unroll
+      for (int kk = 0; kk < kT / 16; ++kk)
+        umma::mma_bf16(tmem + kOCol + ob * kD, ap + (uint64_t)((kk * 32) >> 4),
+                       bv + (uint64_t)((kk * 2048) >> 4), kIdescO, (i == 0 && kk == 0) ? 0u : 1u);
+      umma::commit(bar_addr(c, kPVDone0 + (g & 3)));
+      umma::commit(bar_addr(c, kEmpty0 + (g % kStages)));
+    }
     umma::commit(bar_addr(c, kODone0 + ob));  // the unit's O is complete
   }
 }
@@ -722,7 +747,7 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
       // rescale the row's O when its reference value moved; the previous P.V
       // must have landed first
       if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        if (!wait_w(kPVDone0 + ((g - 1) & 1), ((g - 1) >> 1) & 1)) return;
+        if (!wait_w(kPVDone0 + ((g - 1) & 3), ((g - 1) >> 2) & 1)) return;
         umma::fence_after_sync();
 #pragma unroll 1
         for (int ch = 0; ch < kD / 32; ++ch) {
@@ -750,7 +775,7 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
       }
       fence_proxy_async();
       umma::fence_before_sync();
-      arrive_w(kPFull0 + sb);
+      arrive_w(kPFull0 + (g & 3));
     }
     // hand the rows' (m, l) to the epilogue warps once the epilogue of the
     // unit that used this O buffer before has read its own
@@ -899,9 +924,10 @@ __global__ void __launch_bounds__(Lay<Q8>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t count = 1;  // tcgen05.commit or the producer's expect_tx arrive
-      if ((i >= kSFree0 && i < kSFree0 + 2) || (i >= kPFull0 && i < kPFull0 + 2) ||
+      if ((i >= kSFree0 && i < kSFree0 + 2) || (i >= kPFull0 && i < kPFull0 + 4) ||
           (i >= kEpiReady0 && i < kEpiReady0 + 2) || (i >= kOFree0 && i < kOFree0 + 2))
         count = 4;  // the four softmax (or, for kOFree, epilogue) warps
+      if (i == kDrain) count = 2;  // the S and the P.V issuing threads
       // E4M3 cache: the four converter warps fill the operand stages, free
       // the raw stages and report each converted Q buffer
       if (Q8 && ((i >= kFull0 && i < kFull0 + kMaxStages) ||
@@ -928,10 +954,14 @@ __global__ void __launch_bounds__(Lay<Q8>::kThreads, 1)
     epilogue_warps<R, Q8>(p, c, tmem, n_units);
   } else if (warp < 10) {
     producer<Q8>(p, c, maps, n_units, box != 0, R);
-  } else if (warp == 10) {
+  } else if (warp == 10 || warp == L::kPvWarp) {
     if ((threadIdx.x & 31) == 0) {
-      mma_issuer<Q8>(p, c, tmem, n_units);
-      // drain: its arrival means every MMA issued before it has completed
+      if (warp == 10)
+        mma_s<Q8>(p, c, tmem, n_units);
+      else
+        mma_pv<Q8>(p, c, tmem, n_units);
+      // drain (one commit per issuing thread): its arrival means every MMA
+      // this thread issued has completed
       umma::commit(bar_addr(c, kDrain));
     }
   } else if constexpr (Q8) {
