@@ -21,16 +21,15 @@
 // needs no buffer of its own and is released with the stage.
 //
 // Pipeline.  S(g) goes into buffer g % 2, so the softmax of tile g-1 can
-// overlap the S MMAs of tile g.  The MMA thread issues S(g) and PV(g-1) in
-// whichever order their inputs arrive: when P(g-1) is ready before tile g's
-// rows have landed, PV(g-1) goes first and releases its stage, so the copy of
-// tile g+1 starts one tile earlier (with two stages, the copy latency is
-// otherwise exposed on every tile).
+// overlap the S MMAs of tile g.  S and PV are issued by two threads: PV(g)
+// goes out as soon as P(g) is ready and releases its stage, so the copy of
+// tile g+2 starts without waiting for S(g+1) to be issued (with two stages,
+// the copy latency is otherwise exposed on every tile).
 // The softmax touches O only to rescale it (when its running max moves by
 // more than 2^8), after the PV before it has landed.  The producer prefetches
 // the next tile's rows into L2 while the current stage is in use.
 //
-// Roles inside a CTA (288 threads):
+// Roles inside a CTA (320 threads):
 //   warps 0-3  softmax: thread i owns head i = TMEM lane i.  It loads its row
 //              of Q dims 0..255 into TMEM at the start of a unit, reads its
 //              row of S, keeps the running max and sum in fp32, writes P
@@ -40,7 +39,8 @@
 //              (tile::gather4, 64 dims x 4 rows per copy) into the
 //              128-byte-swizzled K-major layout the tensor core reads; the
 //              unit's Q dims 256..575 come by TMA tile copies at its start.
-//   warp 8     MMA issue (one thread) and TMEM allocation.
+//   warp 8     S MMA issue (one thread) and TMEM allocation.
+//   warp 9     P.V MMA issue (one thread).
 // Every wait on an mbarrier is bounded; on time-out the kernel records
 // DA_DEVERR_TIMEOUT, every role leaves its loop, outstanding tensor-core work
 // is drained (bounded) and TMEM is freed.
@@ -94,7 +94,7 @@ __host__ __device__ constexpr int p_offset_in_stage(int half) {
 }
 static_assert(2 * kStageRegion == kPBytes, "P fills two regions");
 
-constexpr int kThreads = 288;
+constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSCol = kQTCols;  // S buffers at [128, 192) and [192, 256)
 constexpr int kKSteps = kDqk / 16;   // 36 MMAs of K = 16 per S tile
@@ -171,25 +171,6 @@ __device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity,
         set_error(c.hdr, DA_DEVERR_TIMEOUT);
         *c.abort_flag = 1;
         return false;
-      }
-    }
-  }
-}
-
-// Bounded wait for whichever of two barrier phases completes first: 1 for
-// (a, pa), 2 for (b, pb), 0 on time-out or abort.
-__device__ __forceinline__ int wait_either(const Ctx& c, int a, uint32_t pa, int b, uint32_t pb) {
-  const uint32_t ba = bar_addr(c, a), bb = bar_addr(c, b);
-  const unsigned long long t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(ba, pa)) return 1;
-    if (mbar_try_wait(bb, pb)) return 2;
-    if ((it & 63u) == 0) {
-      if (*c.abort_flag) return 0;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        set_error(c.hdr, DA_DEVERR_TIMEOUT);
-        *c.abort_flag = 1;
-        return 0;
       }
     }
   }
@@ -392,15 +373,20 @@ __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
 }
 
 // ---------------------------------------------------------------- MMA issue
-__device__ void mma_issuer(const Launch& p, const Ctx& c, uint32_t tmem, int n_units,
-                           uint32_t& g, uint32_t& n_ne) {
+// Two issuing threads: warp 8 issues the S MMAs, warp 9 the P.V MMAs, so
+// S(g+1) never waits behind P.V(g), which needs the softmax of tile g, and
+// P.V(g) goes out as soon as P(g) is ready.  A tcgen05.commit tracks the MMAs
+// of its own thread, so each thread's commits free exactly what its MMAs
+// read.  The softmax can lead the P.V thread by at most one tile (S(g) needs
+// stage g's copy, which needs P.V(g - 2) done), so the per-parity P-ready and
+// P.V-done barriers stay within one phase of every wait.
+__device__ void mma_s(const Launch& p, const Ctx& c, uint32_t tmem, int n_units, uint32_t& n_ne) {
   // base descriptors; per-MMA ones differ only by a constant start offset
   const uint64_t b_stage0 =  // K tile, K-major, 128-byte swizzle
       umma::smem_desc(c.sbase + kStageOffset, 16, 1024, umma::kSwizzle128B);
   const uint64_t a_q0 =      // Q dims 256..575, K-major, 128-byte swizzle
       umma::smem_desc(c.sbase, 16, 1024, umma::kSwizzle128B);
-  const uint64_t b_v0 =      // V = leading dims of the K tile, MN-major
-      umma::smem_desc(c.sbase + kStageOffset, kStageRegion, 1024, umma::kSwizzle128B);
+  uint32_t g = 0;
   // time-out test hook: a wait that runs out, then the abort path
   if (p.test_stall && !wait_bar(c, kStall, 0, kTestStallNs)) return;
   for (int u = blockIdx.x; u < n_units; u = next_unit(u)) {
@@ -411,40 +397,9 @@ __device__ void mma_issuer(const Launch& p, const Ctx& c, uint32_t tmem, int n_u
     fence_proxy_async();
     if (!wait_bar(c, kQTFull, n_ne & 1)) return;  // Q dims 0..255 in TMEM
     umma::fence_after_sync();
-    // O += P(gp) V(gp): P and V both sit in the stage of tile gp
-    auto pv = [&](uint32_t gp, bool first) -> bool {
-      if (!wait_bar(c, kPFull0 + (gp & 1), (gp >> 1) & 1)) return false;
-      if (first && !wait_bar(c, kOFree, (n_ne & 1) ^ 1)) return false;
-      umma::fence_after_sync();
-      const uint32_t st = (gp % kStages) * kStageBytes;
-      const uint64_t ap = b_stage0 + (uint64_t)((st + p_offset_in_stage(x.half)) >> 4);
-      const uint64_t bv = b_v0 + (uint64_t)((st + 4 * x.half * kStageRegion) >> 4);
-#pragma unroll
-      for (int kk = 0; kk < kSub / 16; ++kk)
-        umma::mma_bf16(tmem + kOCol, ap + (uint64_t)((kk * 32) >> 4),
-                       bv + (uint64_t)((kk * 2048) >> 4), kIdescO,
-                       (first && kk == 0) ? 0u : 1u);
-      umma::commit(bar_addr(c, kODone0 + (gp & 1)));
-      umma::commit(bar_addr(c, kEmpty0 + (gp % kStages)));
-      return true;
-    };
-    // S(g) goes to the other S buffer, so it can run while the softmax of
-    // tile g-1 is still producing P(g-1); PV(g-1) is issued as soon as P(g-1)
-    // is ready, before S(g) when tile g's rows are still on their way (PV
-    // releases the stage, so the copy of tile g+1 can start).
-    bool pv_due = false;  // PV(g-1) not issued yet
     for (int i = 0; i < n_sub; ++i, ++g) {
       const int stage = g % kStages;
       const int sb = g & 1;
-      if (pv_due) {
-        const int w = wait_either(c, kPFull0 + ((g - 1) & 1), ((g - 1) >> 1) & 1,
-                                  kFull0 + stage, (g / kStages) & 1);
-        if (w == 0) return;
-        if (w == 1) {
-          if (!pv(g - 1, i == 1)) return;
-          pv_due = false;
-        }
-      }
       if (!wait_bar(c, kFull0 + stage, (g / kStages) & 1)) return;
       fence_proxy_async();
       if (!wait_bar(c, kSFree0 + sb, ((g >> 1) & 1) ^ 1)) return;  // S(g-2) was read
@@ -464,10 +419,36 @@ __device__ void mma_issuer(const Launch& p, const Ctx& c, uint32_t tmem, int n_u
       }
       umma::commit(bar_addr(c, kSFull0 + sb));
       if (i == n_sub - 1) umma::commit(bar_addr(c, kQFree));
-      if (pv_due && !pv(g - 1, i == 1)) return;
-      pv_due = true;
     }
-    if (!pv(g - 1, n_sub == 1)) return;
+    ++n_ne;
+  }
+}
+
+// O += P(g) V(g): P and V both sit in the stage of tile g.
+__device__ void mma_pv(const Launch& p, const Ctx& c, uint32_t tmem, int n_units, uint32_t& g) {
+  const uint64_t b_stage0 =
+      umma::smem_desc(c.sbase + kStageOffset, 16, 1024, umma::kSwizzle128B);
+  const uint64_t b_v0 =      // V = leading dims of the K tile, MN-major
+      umma::smem_desc(c.sbase + kStageOffset, kStageRegion, 1024, umma::kSwizzle128B);
+  uint32_t n_ne = 0;
+  for (int u = blockIdx.x; u < n_units; u = next_unit(u)) {
+    const MlaUnit x = mla_unit(p, u);
+    if (x.empty) continue;
+    const int n_sub = (x.t_end - x.t_begin + kSub - 1) / kSub;
+    for (int i = 0; i < n_sub; ++i, ++g) {
+      if (!wait_bar(c, kPFull0 + (g & 1), (g >> 1) & 1)) return;
+      if (i == 0 && !wait_bar(c, kOFree, (n_ne & 1) ^ 1)) return;
+      umma::fence_after_sync();
+      const uint32_t st = (g % kStages) * kStageBytes;
+      const uint64_t ap = b_stage0 + (uint64_t)((st + p_offset_in_stage(x.half)) >> 4);
+      const uint64_t bv = b_v0 + (uint64_t)((st + 4 * x.half * kStageRegion) >> 4);
+#pragma unroll
+      for (int kk = 0; kk < kSub / 16; ++kk)
+        umma::mma_bf16(tmem + kOCol, ap + (uint64_t)((kk * 32) >> 4),
+                       bv + (uint64_t)((kk * 2048) >> 4), kIdescO, (i == 0 && kk == 0) ? 0u : 1u);
+      umma::commit(bar_addr(c, kODone0 + (g & 1)));
+      umma::commit(bar_addr(c, kEmpty0 + (g % kStages)));
+    }
     ++n_ne;
   }
 }
@@ -694,6 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if ((i >= kSFree0 && i < kSFree0 + 2) || (i >= kPFull0 && i < kPFull0 + 2) ||
           i == kOFree || i == kQTFull)
         count = 4;                                                   // softmax warps
+      if (i == kDrain) count = 2;                                    // the two issuing threads
       mbar_init(bar_addr(c, i), count);
     }
     *c.abort_flag = 0;
@@ -709,19 +691,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   umma::fence_after_sync();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kTmemSlot);
 
-  uint32_t g_done = 0, q_done = 0;  // tiles and units the MMA thread got through
+  // tiles whose P.V and units whose S MMAs the issuing threads got through
+  volatile uint32_t* done = reinterpret_cast<volatile uint32_t*>(smem + kAbortSlot + 4);
   if (warp < 4) {
     softmax_warps(p, c, tmem, n_units);
   } else if (warp < 8) {
     producer(p, c, n_units);
   } else if ((threadIdx.x & 31) == 0) {
-    mma_issuer(p, c, tmem, n_units, g_done, q_done);
-    // drain: one more commit; its arrival means every MMA issued before it
-    // has completed, so tensor memory can be freed
+    uint32_t count = 0;
+    if (warp == 8)
+      mma_s(p, c, tmem, n_units, count);
+    else
+      mma_pv(p, c, tmem, n_units, count);
+    done[warp - 8] = count;
+    // drain (one commit per issuing thread): its arrival means every MMA the
+    // thread issued has completed, so tensor memory can be freed
     umma::commit(bar_addr(c, kDrain));
   }
   umma::fence_before_sync();
   __syncthreads();
+  const uint32_t q_done = done[0], g_done = done[1];
   if (warp == 8) {
     umma::fence_after_sync();
     if ((threadIdx.x & 31) == 0) {
