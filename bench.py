@@ -191,6 +191,8 @@ def build_workload(name, rank=0):
         return W.gqa16_paged(seed=1007 + seed_shift)
     if name == "gqa16_paged_fp8":
         return W.gqa16_paged_fp8(seed=1007 + seed_shift)
+    if name == "gqa16_paged_nvfp4":
+        return W.gqa16_paged_nvfp4(seed=1007 + seed_shift)
     if name == "gqa_paged_nvfp4":
         return W.gqa_paged_nvfp4(seed=1001 + seed_shift)
     if name == "long_context_nvfp4":
@@ -563,7 +565,7 @@ def main():
     ap.add_argument("--workload", default="long_context",
                     choices=["gqa_paged", "long_context", "tiny", "mla_sparse", "gqa_paged_fp8",
                              "long_context_fp8", "gqa_paged_nvfp4", "long_context_nvfp4",
-                             "gqa16_paged", "gqa16_paged_fp8"])
+                             "gqa16_paged", "gqa16_paged_fp8", "gqa16_paged_nvfp4"])
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the secondary workloads and the CPU baseline")
     ap.add_argument("--nvfp4-only", type=int, nargs="+", metavar="ROWS",
@@ -646,7 +648,8 @@ def main():
         line["roofline_tensor"] = rec["roofline_tensor"]
     if not args.no_extra:
         extra = {}
-        for name in ("gqa_paged", "mla_sparse", "gqa16_paged", "gqa16_paged_fp8", "tiny",
+        for name in ("gqa_paged", "mla_sparse", "gqa16_paged", "gqa16_paged_fp8",
+                     "gqa16_paged_nvfp4", "tiny",
                      "gqa_paged_fp8",
                      "long_context_fp8", "gqa_paged_nvfp4", "long_context_nvfp4",
                      "long_context"):

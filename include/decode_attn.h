@@ -76,8 +76,9 @@ extern "C" {
  * gllm issue #98, Observation: NVFP4 Nemotron) but name no cache format;
  * this is the library's reading.  The kernel converts each byte exactly to
  * fp32, applies k_scale to the softmax scale and v_scale to a unit's output
- * (fixed roundings, independent of the batch).  CUDA-core variant, one KV
- * source only; other combinations return DA_ERR_UNSUPPORTED.              */
+ * (fixed roundings, independent of the batch).  One KV source only, no
+ * shared latent (DA_ERR_UNSUPPORTED otherwise); DA_VARIANT_GQA_TC for groups
+ * of 16 or more heads at D = 128, else DA_VARIANT_FMA.                     */
 #define DA_KV_FP8_E4M3 1
 /* NVFP4: each head's row of D elements is stored as D/2 bytes of 4-bit E2M1
  * codes (element 2j in the low nibble of byte j; magnitudes 0, 0.5, 1, 1.5,
@@ -88,17 +89,19 @@ extern "C" {
  * contiguous, num_blocks*page_size paged, num_blocks indexed), and right
  * after them, at byte offset rows*H_kv*D/2, the block scales [rows, H_kv,
  * D/16] in the same order.  Same reading of the pages and the same rules as
- * DA_KV_FP8_E4M3 (k_scale, v_scale; CUDA-core variant, one KV source).  The
- * kernel turns each code and each block scale into f16 exactly, multiplies
- * them in f16 (exact: at most six significant bits) and widens to fp32.   */
+ * DA_KV_FP8_E4M3 (k_scale, v_scale, one KV source; DA_VARIANT_GQA_TC only
+ * when H_kv is even as well).  The kernel turns each code and each block
+ * scale into f16 exactly and multiplies them in f16 (exact: at most six
+ * significant bits).                                                       */
 #define DA_KV_NVFP4 2
 
 /* ---- kernel variants (chosen from the head config only, never B) ----- */
 #define DA_VARIANT_FMA 0 /* CUDA-core fp32 FMA, H_q/H_kv in 1..128, D in {64,128}    */
 #define DA_VARIANT_MLA 1 /* tcgen05 tensor cores, shared latent 576/512, 16..128 heads */
-/* tcgen05 tensor cores, separate K and V (bf16, or E4M3 converted to f16 in
- * shared memory), 16..128 query heads per KV head, D = 128, one KV source
- * (other configs of >= 16 heads: DA_VARIANT_FMA)                            */
+/* tcgen05 tensor cores, separate K and V (bf16, or E4M3 or NVFP4 converted
+ * to f16 in shared memory; NVFP4 with an even H_kv), 16..128 query heads per
+ * KV head, D = 128, one KV source (other configs of >= 16 heads:
+ * DA_VARIANT_FMA)                                                           */
 #define DA_VARIANT_GQA_TC 2
 
 /* ---- device-detected input errors (decode_attn_read_error bits) ----- */

@@ -66,10 +66,12 @@ int select_variant(const da_problem* p, Variant* v) {
     return DA_ERR_UNSUPPORTED;
   }
   const int G = p->num_q_heads / p->num_kv_heads;
-  // groups of at least 16 heads over a bf16 or E4M3 cache with one source:
-  // the multi-head contractions go to the tensor cores
-  if (p->head_dim_qk == p->head_dim_v &&
-      (p->kv_dtype == DA_KV_BF16 || p->kv_dtype == DA_KV_FP8_E4M3) && p->extra_width == 0 &&
+  // groups of at least 16 heads over a bf16, E4M3 or NVFP4 cache (NVFP4: an
+  // even number of KV heads) with one source: the multi-head contractions go
+  // to the tensor cores
+  const bool tc_cache = p->kv_dtype == DA_KV_BF16 || p->kv_dtype == DA_KV_FP8_E4M3 ||
+                        (p->kv_dtype == DA_KV_NVFP4 && p->num_kv_heads % 2 == 0);
+  if (p->head_dim_qk == p->head_dim_v && tc_cache && p->extra_width == 0 &&
       gqa_tc_supported(G, p->head_dim_qk)) {
     *v = {DA_VARIANT_GQA_TC, kTcTile, kTcMinTilesPerSplit, kTcMaxSplits};
     return DA_OK;

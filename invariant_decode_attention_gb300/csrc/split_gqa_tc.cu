@@ -1,6 +1,6 @@
 // Split kernel, tensor-core variant for grouped-query attention with a
 // separate K and V cache: 16 to 128 query heads per KV head, head dim 128,
-// bf16 caches.
+// bf16, E4M3 or NVFP4 caches.
 //
 // One unit of work = (row b, split s, KV head h).  Both contractions run on
 // tcgen05 tensor cores with fp32 accumulators in tensor memory (TMEM):
@@ -37,8 +37,9 @@
 // while the softmax warps go on with the next unit); warps 8-9 producer (page
 // or index lookups ahead of the copies, TMA issue; for a bf16 cache the two
 // warps take alternate tiles, so one issues copies while the other waits for
-// its next stage; for an E4M3 cache warp 8 alone); warp 10 the S MMAs (one
-// thread) and TMEM allocation; E4M3 cache: warps 11-14 converter; last warp
+// its next stage; for a quantized cache warp 8 alone); warp 10 the S MMAs
+// (one thread) and TMEM allocation; quantized cache: warps 11-14 converter;
+// last warp
 // the P.V MMAs (one thread).  Every mbarrier wait is bounded; on time-out the
 // kernel records DA_DEVERR_TIMEOUT, every role leaves its loop, outstanding
 // tensor-core work is drained (bounded) and TMEM is freed.
@@ -64,14 +65,13 @@ constexpr int kTileBytes = 2 * kRegion;     // K (or V) of a tile: 16 KB
 constexpr int kStageBytes = 2 * kTileBytes;  // K, then V
 constexpr int kQRegion = kRows * 128;       // 128 rows x 64 dims
 constexpr int kQBytes = 2 * kQRegion;       // 32 KB
-constexpr int kRawTileBytes = kT * kD;      // E4M3 K (or V) of a tile: 64 rows x 128 bytes
-constexpr int kRawStageBytes = 2 * kRawTileBytes;  // 16 KB: K, then V
+
 constexpr int kMaxStages = 8;
 enum {
   kFull0 = 0, kEmpty0 = kFull0 + kMaxStages,  // operand stages: ready / free
-  kRawFull0 = kEmpty0 + kMaxStages,           // E4M3 cache: copies landed
-  kRawEmpty0 = kRawFull0 + kMaxStages,        // E4M3 cache: converted, reusable
-  kQConv0 = kRawEmpty0 + kMaxStages,          // E4M3 cache: Q written to tensor memory
+  kRawFull0 = kEmpty0 + kMaxStages,           // quantized cache: copies landed
+  kRawEmpty0 = kRawFull0 + kMaxStages,        // quantized cache: converted, reusable
+  kQConv0 = kRawEmpty0 + kMaxStages,          // quantized cache: Q in tensor memory
   kQFull0 = kQConv0 + 2, kQFree0 = kQFull0 + 2,
   // P ready and P.V done: four slots each (tile g uses slot g % 4, phase
   // g / 4).  The S and P.V MMAs are issued by two threads, so the softmax can
@@ -85,22 +85,35 @@ enum {
   kNumBars
 };
 
-// Shared-memory map.  Q8: the cache holds one E4M3 byte per element.  bf16:
-// two Q buffers (TMA copies, the S MMAs' A operand) and four operand stages
-// that TMA fills directly.  E4M3: Q lives in tensor memory instead (the
-// converter writes it there), TMA copies the cache bytes into seven raw
-// stages (one producer warp: half the copies of the bf16 path per tile) and
-// the converter warpgroup writes them, as f16, into three operand stages
-// (the MMAs then run on f16 operands, see the converter).  Seven raw stages
-// keep 112 KB of the cache in flight per SM, as many entries as 224 KB of
-// bf16.
-template <bool Q8>
+// Shared-memory map.  KT: 0 bf16 cache, 1 E4M3 (one byte per element), 2
+// NVFP4 (E2M1 codes and E4M3 block scales); Q8: a quantized cache (1 or 2).
+// bf16: two Q buffers (TMA copies, the S MMAs' A operand) and four operand
+// stages that TMA fills directly.  Quantized: Q lives in tensor memory
+// instead (the converter writes it there), TMA copies the cache bytes into
+// raw stages (one producer warp) and the converter warpgroup writes them, as
+// f16, into three operand stages (the MMAs then run on f16 operands, see the
+// converter).  Seven E4M3 raw stages keep 112 KB of the cache in flight per
+// SM, as many entries as 224 KB of bf16; eight NVFP4 stages keep 80 KB (512
+// entries, where the bf16 path has 256).
+template <int KT>
 struct Lay {
+  static constexpr bool Q8 = KT != 0;  // a quantized cache: the f16 converter path
   static constexpr int kStages = Q8 ? 3 : 4;     // operand stages (K, V as 16-bit)
-  static constexpr int kRawStages = Q8 ? 7 : 0;  // E4M3 copies
+  // Raw stage: E4M3 -- K rows, then V rows, 128 bytes each (16 KB); NVFP4 --
+  // K codes, V codes (64 bytes a row), then K and V block scales (16 bytes a
+  // row: the scale rows of two neighbouring heads, copied together) in 2 KB
+  // each (box copies: 16 rows a copy, rows back to back; gathers: 4 rows a
+  // copy into its own 128-byte slot, as a tensor copy's shared destination
+  // is 128-byte aligned) (12 KB)
+  static constexpr int kRawCodeBytes = KT == 2 ? kT * kD / 2 : kT * kD;  // K (or V) codes of a tile
+  static constexpr int kRawScaleBytes = KT == 2 ? (kT / 4) * 128 : 0;    // K (or V) scales
+  static constexpr int kRawStageBytes = 2 * kRawCodeBytes + 2 * kRawScaleBytes;
+  static constexpr int kRawTxBytes = 2 * kRawCodeBytes + (KT == 2 ? 2 * kT * 16 : 0);  // copied
+  static constexpr int kRawStages = KT == 2 ? 8 : Q8 ? 7 : 0;
   static constexpr int kStageOffset = Q8 ? 0 : 2 * kQBytes;
   static constexpr int kRawOffset = kStageOffset + kStages * kStageBytes;
   static constexpr int kBarOffset = kRawOffset + kRawStages * kRawStageBytes;
+  static_assert(kRawStageBytes % 1024 == 0, "raw stages keep 1 KB alignment");
   static constexpr int kTmemSlot = kBarOffset + kNumBars * 8;
   static constexpr int kAbortSlot = kTmemSlot + 4;
   // m and l of every row, per O buffer (softmax -> epilogue), then the
@@ -109,7 +122,7 @@ struct Lay {
   static constexpr int kMergeOffset = (kAbortSlot + 4 + 15) / 16 * 16;
   static constexpr int kSmemBytes = kMergeOffset + (2 * 2 * kRows + kRows * 33) * 4;
   // warps 0-3 softmax, 4-7 epilogue, 8-9 producer, 10 S MMAs, 11-14
-  // converter (E4M3), then the P.V MMAs' warp
+  // converter (quantized cache), then the P.V MMAs' warp
   static constexpr int kPvWarp = Q8 ? 15 : 11;
   static constexpr int kThreads = (kPvWarp + 1) * 32;
   static_assert(kStageOffset % 1024 == 0 && kRawOffset % 1024 == 0, "aligned stages");
@@ -120,12 +133,13 @@ struct Lay {
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSCol = 0;    // S buffers [0, 64) and [64, 128)
 constexpr uint32_t kOCol = 128;  // O accumulators [128, 256) and [256, 384)
-constexpr uint32_t kQCol = 384;  // E4M3 cache: two f16 Q buffers [384, 448) and [448, 512)
+constexpr uint32_t kQCol = 384;  // quantized cache: two f16 Q buffers [384, 448), [448, 512)
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kQBoxRows = 16;
 
-// bf16 operands (bf16 cache); f16 operands (E4M3 cache: E4M3 values are f16
-// values, and Q is prescaled by a power of two into f16's range)
+// bf16 operands (bf16 cache); f16 operands (quantized cache: E4M3 values and
+// NVFP4 code x block-scale products are f16 values, and Q is prescaled by a
+// power of two into f16's range)
 template <bool Q8>
 __host__ __device__ constexpr uint32_t idesc_s() {
   return Q8 ? umma::idesc_f16_f32(kRows, kT, false) : umma::idesc_bf16_f32(kRows, kT, false);
@@ -153,7 +167,8 @@ __device__ __forceinline__ void tma_box2(uint32_t dst, const CUtensorMap* tm, in
       : "memory");
 }
 
-// Box {64, 1} at rows r0..r3 of a 2-D map: four 128-byte rows at dst + 128 i.
+// Box {w, 1} at rows r0..r3 of a 2-D map: the four rows of the box (its w
+// elements each) back to back from dst (128-byte aligned).
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* tm, int col, int r0,
                                             int r1, int r2, int r3, uint32_t bar) {
   asm volatile(
@@ -168,10 +183,14 @@ __device__ __forceinline__ void fence_proxy_async() {
 }
 
 struct Maps {
-  // bf16: [rows][H_kv][128] elements, box {64, 1, 16}; E4M3: bytes, box {128, 1, 16}
+  // bf16: [rows][H_kv][128] elements, box {64, 1, 16}; E4M3: bytes, box
+  // {128, 1, 16}; NVFP4 codes: bytes [rows][H_kv][64], box {64, 1, 16}
   CUtensorMap k3, v3;  // (box path)
-  // bf16: [rows * H_kv][128], box {64, 1}; E4M3: bytes, box {128, 1}
+  // the same as [rows * H_kv][row], box {64 | 128 | 64, 1}
   CUtensorMap k2, v2;  // (gather path)
+  // NVFP4 block scales as bytes [rows][H_kv * 8]: box {16, 16} (box path) and
+  // {16, 1} (gather path) -- the 8-byte scale rows of heads 2i and 2i + 1
+  CUtensorMap ks, vs, ks2, vs2;
   CUtensorMap q;       // [B * H_q][128], box {64, 16}
 };
 
@@ -205,8 +224,10 @@ __device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity,
   }
 }
 
-// ---- E4M3 cache: f16 operands ---------------------------------------------
-// Every E4M3 value is an f16 value, so K and V convert exactly; Q (bf16) is
+// ---- quantized cache: f16 operands ----------------------------------------
+// Every E4M3 value is an f16 value, and so is every NVFP4 element (an E2M1
+// code, at most two significant bits, times an E4M3 block scale, at most
+// four, with magnitudes from 2^-10 to 2688), so K and V convert exactly; Q (bf16) is
 // brought into f16's range per row by a power of two: with m the row's
 // largest magnitude and 2^k <= m < 2^(k+1), the row is multiplied by
 // 2^e, e = 14 - k (clamped to [-113, 120]), so its largest element lies in
@@ -263,14 +284,16 @@ __device__ __forceinline__ TcUnit tc_unit(const Launch& p, int u) {
 // are loaded during the current unit, so the copies never wait on a lookup.
 // Gather path: lane j < 16 owns the 4-entry group j of each tile, its words
 // loaded one tile ahead.
-template <bool Q8>
+template <int KT>
 __device__ void producer(const Launch& p, const Ctx& c, const Maps& m, int n_units, bool box,
                          int R) {
-  using L = Lay<Q8>;
-  // the stages this role fills: raw E4M3 stages, or the operand stages
+  constexpr bool Q8 = KT != 0;  // a quantized cache (E4M3 or NVFP4)
+  using L = Lay<KT>;
+  // the stages this role fills: raw stages of cache bytes, or the operand stages
   constexpr int kNS = Q8 ? L::kRawStages : L::kStages;
   constexpr int kFullB = Q8 ? kRawFull0 : kFull0, kEmptyB = Q8 ? kRawEmpty0 : kEmpty0;
-  // E4M3 cache: warp 8 alone copies (a tile is 8 box copies, not 16)
+  // quantized cache: warp 8 alone copies (a tile is 8 box copies of codes,
+  // plus 8 of NVFP4 scales, not 16 of bf16 halves)
   constexpr int kWarpsCopying = Q8 ? 1 : 2;
   const int lane = threadIdx.x & 31;
   const int pw = (threadIdx.x >> 5) - 8;  // producer warp 0 or 1: tiles of its parity
@@ -358,28 +381,42 @@ __device__ void producer(const Launch& p, const Ctx& c, const Maps& m, int n_uni
         break;
       }
       const uint32_t full = bar_addr(c, kFullB + st);
-      if (lane == 0) mbar_arrive_expect_tx(full, Q8 ? kRawStageBytes : kStageBytes);
+      if (lane == 0) mbar_arrive_expect_tx(full, Q8 ? L::kRawTxBytes : kStageBytes);
       __syncwarp();
       if constexpr (Q8) {
-        // E4M3 rows (128 bytes) into a raw stage, row-major: K then V
-        const uint32_t kdst = c.sbase + L::kRawOffset + st * kRawStageBytes;
-        const uint32_t vdst = kdst + kRawTileBytes;
+        // E4M3 rows (128 bytes) or NVFP4 code rows (64 bytes) into a raw
+        // stage, row-major: K then V; NVFP4 block scales after them (the
+        // 16-byte scale rows of heads 2i and 2i + 1, i = h / 2)
+        constexpr int kRow = L::kRawCodeBytes / kT;  // code bytes a row
+        const uint32_t kdst = c.sbase + L::kRawOffset + st * L::kRawStageBytes;
+        const uint32_t vdst = kdst + L::kRawCodeBytes;
+        const uint32_t ksdst = kdst + 2 * L::kRawCodeBytes, vsdst = ksdst + L::kRawScaleBytes;
+        const int sx = (x.h & ~1) * 8;  // first scale byte of the head pair
         if (box) {
           if ((lane >> 2) == (i & 7)) {
             const int grp = lane & 3;
             long long r = row_of(x, t0 + grp * 16, w_cur);
             if (r < 0) r = 0;
-            tma_box3(kdst + grp * 16 * kD, &m.k3, 0, x.h, (int)r, full);
-            tma_box3(vdst + grp * 16 * kD, &m.v3, 0, x.h, (int)r, full);
+            tma_box3(kdst + grp * 16 * kRow, &m.k3, 0, x.h, (int)r, full);
+            tma_box3(vdst + grp * 16 * kRow, &m.v3, 0, x.h, (int)r, full);
+            if constexpr (KT == 2) {
+              tma_box2(ksdst + grp * 16 * 16, &m.ks, sx, (int)r, full);
+              tma_box2(vsdst + grp * 16 * 16, &m.vs, sx, (int)r, full);
+            }
           }
         } else if (lane < 16) {
-          int rr[4];
+          int rr[4], rs[4];
           for (int k = 0; k < 4; ++k) {
             const long long r = row_of(x, t0 + lane * 4 + k, wg[k]);
+            rs[k] = (int)(r < 0 ? 0 : r);
             rr[k] = (int)((r < 0 ? 0 : r) * p.H_kv + x.h);
           }
-          tma_gather4(kdst + lane * 4 * kD, &m.k2, 0, rr[0], rr[1], rr[2], rr[3], full);
-          tma_gather4(vdst + lane * 4 * kD, &m.v2, 0, rr[0], rr[1], rr[2], rr[3], full);
+          tma_gather4(kdst + lane * 4 * kRow, &m.k2, 0, rr[0], rr[1], rr[2], rr[3], full);
+          tma_gather4(vdst + lane * 4 * kRow, &m.v2, 0, rr[0], rr[1], rr[2], rr[3], full);
+          if constexpr (KT == 2) {
+            tma_gather4(ksdst + lane * 128, &m.ks2, sx, rs[0], rs[1], rs[2], rs[3], full);
+            tma_gather4(vsdst + lane * 128, &m.vs2, sx, rs[0], rs[1], rs[2], rs[3], full);
+          }
           for (int k = 0; k < 4; ++k) wg[k] = wg_n[k];
         }
       } else {
@@ -436,21 +473,22 @@ __device__ void producer(const Launch& p, const Ctx& c, const Maps& m, int n_uni
 }
 
 // ---------------------------------------------------------------- converter
-// E4M3 cache only: warps 11-14.  Per unit, once the S MMAs of the unit two
+// Quantized cache only: warps 11-14.  Per unit, once the S MMAs of the unit two
 // back have released Q buffer qb (kQFree), each thread writes one MMA row of
 // Q into tensor memory -- warp w owns lanes 32 (w % 4) .. + 31 -- as f16
 // pairs, prescaled (q_prescale_exp; rows past the group are zeros), and the
-// MMA thread is told (kQConv).  Per tile, once its
-// bytes are in raw stage g % 3 and operand stage g % 3 is free (the PV three
-// tiles back completed), K and V are written as f16 into the operand stage in
-// the 128-byte-swizzled K-major layout the tensor core reads -- eight lanes
-// per 128-byte row, so every load reads four whole rows, and lanes jj and
+// MMA thread is told (kQConv).  Per tile, once its bytes are in raw stage
+// g % kRawStages and operand stage g % 3 is free (the PV three tiles back
+// completed), K and V are written as f16 into the operand stage (NVFP4: each
+// code times its block scale, multiplied in f16) in the 128-byte-swizzled
+// K-major layout the tensor core reads -- eight lanes per row, so every load
+// reads four whole rows, and lanes jj and
 // jj + 4 (same chunk pair, other 64-dim region) store their two chunks in
 // opposite orders, so the eight lanes of a store phase hit eight different
 // bank groups -- and both stages are handed on.
-template <int R>
-__device__ void converter(const Launch& p, const Ctx& c, uint32_t tmem, int n_units) {
-  using L = Lay<true>;
+template <int R, int KT>
+__device__ void converter(const Launch& p, const Ctx& c, uint32_t tmem, int n_units, bool box) {
+  using L = Lay<KT>;
   constexpr int kGp = kRows / R;  // rows per copy of the group
   const int ct = threadIdx.x - 11 * 32;  // 0..127
   const int warp = threadIdx.x >> 5, lane = ct & 31;
@@ -511,21 +549,40 @@ __device__ void converter(const Launch& p, const Ctx& c, uint32_t tmem, int n_un
       const int rs = g % L::kRawStages, os = g % L::kStages;
       if (!wait_w(kRawFull0 + rs, (g / L::kRawStages) & 1)) return;
       if (!wait_w(kEmpty0 + os, ((g / L::kStages) & 1) ^ 1)) return;
-      const uint8_t* raw = c.smem + L::kRawOffset + rs * kRawStageBytes;
+      const uint8_t* raw = c.smem + L::kRawOffset + rs * L::kRawStageBytes;
       uint8_t* op = c.smem + L::kStageOffset + os * kStageBytes;
 #pragma unroll
       for (int kv = 0; kv < 2; ++kv) {
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           const int row = r0 + 16 * q4;
-          const uint4 b = *reinterpret_cast<const uint4*>(raw + kv * kRawTileBytes + row * kD +
-                                                          jj * 16);
-          const uint32_t wb[4] = {b.x, b.y, b.z, b.w};
-          uint32_t h[8];
+          uint32_t h[8];  // f16 pairs of dims 16 jj .. 16 jj + 15, in order
+          if constexpr (KT == 2) {
+            // sixteen E2M1 codes and their one E4M3 block scale (byte jj of
+            // the head's eight), each exact in f16, multiplied exactly
+            const uint2 cw = *reinterpret_cast<const uint2*>(raw + kv * L::kRawCodeBytes +
+                                                             row * (kD / 2) + jj * 8);
+            const int srow = box ? row * 16 : (row >> 2) * 128 + (row & 3) * 16;
+            const uint32_t sb = raw[2 * L::kRawCodeBytes + kv * L::kRawScaleBytes + srow +
+                                    (x.h & 1) * 8 + jj];
+            const uint32_t s2 = __byte_perm(e4m3x2_to_f16x2(sb), 0, 0x1010);
+            uint32_t lo4[4], hi4[4];
+            e2m1x8_to_f16x2(cw.x, lo4);
+            e2m1x8_to_f16x2(cw.y, hi4);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            h[2 * e] = e4m3x2_to_f16x2(wb[e]);
-            h[2 * e + 1] = e4m3x2_to_f16x2(wb[e] >> 16);
+            for (int e = 0; e < 4; ++e) {
+              h[e] = hmul2(lo4[e], s2);
+              h[4 + e] = hmul2(hi4[e], s2);
+            }
+          } else {
+            const uint4 b = *reinterpret_cast<const uint4*>(raw + kv * L::kRawCodeBytes +
+                                                            row * kD + jj * 16);
+            const uint32_t wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              h[2 * e] = e4m3x2_to_f16x2(wb[e]);
+              h[2 * e + 1] = e4m3x2_to_f16x2(wb[e] >> 16);
+            }
           }
           // dims 16 jj .. +7 and +8 .. +15: region jj / 4, chunks 2 (jj % 4) and +1
           uint8_t* rbase = op + kv * kTileBytes + (jj >> 2) * kRegion + row * 128;
@@ -549,9 +606,10 @@ __device__ void converter(const Launch& p, const Ctx& c, uint32_t tmem, int n_un
 // the softmax of tile g: warp 10 issues the S MMAs, warp kPvWarp the P.V
 // MMAs.  A tcgen05.commit tracks the MMAs of its own thread, so each thread's
 // commits free exactly what its MMAs read.
-template <bool Q8>
+template <int KT>
 __device__ void mma_s(const Launch& p, const Ctx& c, uint32_t tmem, int n_units) {
-  using L = Lay<Q8>;
+  constexpr bool Q8 = KT != 0;  // a quantized cache (E4M3 or NVFP4)
+  using L = Lay<KT>;
   constexpr int kStages = L::kStages;
   constexpr uint32_t kIdescS = idesc_s<Q8>();
   // Q in a Q buffer is ready: copied (bf16), or written to tensor memory (E4M3)
@@ -598,9 +656,10 @@ __device__ void mma_s(const Launch& p, const Ctx& c, uint32_t tmem, int n_units)
 
 // O += P(g) V(g): P sits over the K tile of stage g % kStages (the softmax
 // wrote it once S(g) had read that tile), V after it.
-template <bool Q8>
+template <int KT>
 __device__ void mma_pv(const Launch& p, const Ctx& c, uint32_t tmem, int n_units) {
-  using L = Lay<Q8>;
+  constexpr bool Q8 = KT != 0;  // a quantized cache (E4M3 or NVFP4)
+  using L = Lay<KT>;
   constexpr int kStages = L::kStages;
   static_assert(kStages <= 4, "the four P slots cover the softmax's lead");
   constexpr uint32_t kIdescO = idesc_o<Q8>();
@@ -644,9 +703,10 @@ __device__ void mma_pv(const Launch& p, const Ctx& c, uint32_t tmem, int n_units
 // order, the combine arithmetic of the split/merge step:
 //     M = max_c m_c,  L = sum_c 2^(m_c - M) l_c,  O = sum_c 2^(m_c - M) O_c / L.
 // All of it depends only on the unit's own data.
-template <int R, bool Q8>
+template <int R, int KT>
 __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int n_units) {
-  using L = Lay<Q8>;
+  constexpr bool Q8 = KT != 0;  // a quantized cache (E4M3 or NVFP4)
+  using L = Lay<KT>;
   constexpr int kGp = kRows / R;              // rows per copy
   constexpr int kCpt = kT / R;                // entries of a tile per copy
   constexpr int kCopiesPerWarp = kGp < 32 ? 32 / kGp : 1;
@@ -675,7 +735,7 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
     const TcUnit x = tc_unit(p, u);
     const int n_sub = (x.t_end - x.t_begin + kT - 1) / kT;
     const int ob = nq & 1;
-    // E4M3 cache: the row's Q was prescaled by 2^e into f16 (the converter
+    // quantized cache: the row's Q was prescaled by 2^e into f16 (the converter
     // derives e from the same 128 values, see q_prescale_exp), so its scores
     // carry that factor; the row takes it back in its softmax scale
     float row_scale = p.scale_log2;
@@ -793,8 +853,9 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
 // and write O / L (bf16 output of a single-split row, else the fp32 partial
 // and its LSE in log2 units).  Thread t of the group, for each 32-column
 // chunk, sums the R copies of head t % Gp over 32/R of the columns.
-template <int R, bool Q8>
+template <int R, int KT>
 __device__ void epilogue_warps(const Launch& p, const Ctx& c, uint32_t tmem, int n_units) {
+  constexpr bool Q8 = KT != 0;  // a quantized cache (E4M3 or NVFP4)
   constexpr int kGp = kRows / R;
   constexpr int kCols = 32 / R;  // columns of a chunk a thread sums
   const int q = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
@@ -835,7 +896,7 @@ __device__ void epilogue_warps(const Launch& p, const Ctx& c, uint32_t tmem, int
     const float f = (m_row == -INFINITY) ? 0.f : ex2(m_row - M);
     const bool writer = jt < G;
     const int hq = x.h * G + jt;
-    // (an E4M3 cache's V scale multiplies the output once, here)
+    // (a quantized cache's V scale multiplies the output once, here)
     const float inv = ((L > 0.f) ? 1.f / L : 0.f) * (Q8 ? p.v_scale : 1.f);
 #pragma unroll 1
     for (int ch = 0; ch < kD / 32; ++ch) {
@@ -889,10 +950,11 @@ __device__ void epilogue_warps(const Launch& p, const Ctx& c, uint32_t tmem, int
   }
 }
 
-template <int R, bool Q8>
-__global__ void __launch_bounds__(Lay<Q8>::kThreads, 1)
+template <int R, int KT>
+__global__ void __launch_bounds__(Lay<KT>::kThreads, 1)
     split_gqa_tc_kernel(Launch p, const __grid_constant__ Maps maps, int box) {
-  using L = Lay<Q8>;
+  using L = Lay<KT>;
+  constexpr bool Q8 = KT != 0;
   constexpr int kThreads = L::kThreads;
   extern __shared__ __align__(1024) uint8_t smem[];
   Ctx c;
@@ -928,7 +990,7 @@ __global__ void __launch_bounds__(Lay<Q8>::kThreads, 1)
           (i >= kEpiReady0 && i < kEpiReady0 + 2) || (i >= kOFree0 && i < kOFree0 + 2))
         count = 4;  // the four softmax (or, for kOFree, epilogue) warps
       if (i == kDrain) count = 2;  // the S and the P.V issuing threads
-      // E4M3 cache: the four converter warps fill the operand stages, free
+      // quantized cache: the four converter warps fill the operand stages, free
       // the raw stages and report each converted Q buffer
       if (Q8 && ((i >= kFull0 && i < kFull0 + kMaxStages) ||
                  (i >= kRawEmpty0 && i < kRawEmpty0 + kMaxStages) ||
@@ -949,23 +1011,23 @@ __global__ void __launch_bounds__(Lay<Q8>::kThreads, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
 
   if (warp < 4) {
-    softmax_warps<R, Q8>(p, c, tmem, n_units);
+    softmax_warps<R, KT>(p, c, tmem, n_units);
   } else if (warp < 8) {
-    epilogue_warps<R, Q8>(p, c, tmem, n_units);
+    epilogue_warps<R, KT>(p, c, tmem, n_units);
   } else if (warp < 10) {
-    producer<Q8>(p, c, maps, n_units, box != 0, R);
+    producer<KT>(p, c, maps, n_units, box != 0, R);
   } else if (warp == 10 || warp == L::kPvWarp) {
     if ((threadIdx.x & 31) == 0) {
       if (warp == 10)
-        mma_s<Q8>(p, c, tmem, n_units);
+        mma_s<KT>(p, c, tmem, n_units);
       else
-        mma_pv<Q8>(p, c, tmem, n_units);
+        mma_pv<KT>(p, c, tmem, n_units);
       // drain (one commit per issuing thread): its arrival means every MMA
       // this thread issued has completed
       umma::commit(bar_addr(c, kDrain));
     }
   } else if constexpr (Q8) {
-    converter<R>(p, c, tmem, n_units);
+    converter<R, KT>(p, c, tmem, n_units, box != 0);
   }
   umma::fence_before_sync();
   __syncthreads();
@@ -1002,10 +1064,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// A map of `rank` dims (dim 0 = the 128 elements of a head row), zero fill
-// past the bounds: bf16 elements with the 128-byte swizzle (operands copied
-// straight into the tensor core's layout), or bytes without swizzle (E4M3
-// rows for the converter).
+// A map of `rank` dims (dim 0 = a head row), zero fill past the bounds: bf16
+// elements with the 128-byte swizzle (operands copied straight into the
+// tensor core's layout), or bytes without swizzle (E4M3 rows, NVFP4 code and
+// scale rows, for the converter).
 bool encode(CUtensorMap* tm, const void* base, int rank, const cuuint64_t* dims,
             const cuuint64_t* strides, const cuuint32_t* box, bool bytes) {
   const PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
@@ -1024,45 +1086,46 @@ int copies_for(int G) {
   return kRows / gp;
 }
 
-template <int R, bool Q8>
+template <int R, int KT>
 cudaError_t set_smem() {
   static const cudaError_t e =
-      cudaFuncSetAttribute(split_gqa_tc_kernel<R, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Lay<Q8>::kSmemBytes);
+      cudaFuncSetAttribute(split_gqa_tc_kernel<R, KT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Lay<KT>::kSmemBytes);
   return e;
 }
 
 int tc_ctas_per_sm() {
   static const int n = [] {
-    if (set_smem<1, false>() != cudaSuccess) return 1;
+    if (set_smem<1, 0>() != cudaSuccess) return 1;
     int c = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, split_gqa_tc_kernel<1, false>,
-                                                      Lay<false>::kThreads,
-                                                      Lay<false>::kSmemBytes) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, split_gqa_tc_kernel<1, 0>,
+                                                      Lay<0>::kThreads,
+                                                      Lay<0>::kSmemBytes) != cudaSuccess ||
         c < 1)
       c = 1;
     return c;
   }();
   return n;
 }
-static_assert(Lay<true>::kSmemBytes > 232448 / 2 && Lay<false>::kSmemBytes > 232448 / 2,
-              "both layouts run one CTA per SM (the grid is sized from one)");
+static_assert(Lay<0>::kSmemBytes > 232448 / 2 && Lay<1>::kSmemBytes > 232448 / 2 &&
+                  Lay<2>::kSmemBytes > 232448 / 2,
+              "every layout runs one CTA per SM (the grid is sized from one)");
 
-template <int R, bool Q8>
+template <int R, int KT>
 cudaError_t launch_r(const Launch& p, const Maps& m, int box, int grid, cudaStream_t stream) {
-  const cudaError_t e = set_smem<R, Q8>();
+  const cudaError_t e = set_smem<R, KT>();
   if (e != cudaSuccess) return e;
-  return launch_after(split_gqa_tc_kernel<R, Q8>, dim3(grid), dim3(Lay<Q8>::kThreads),
-                      (size_t)Lay<Q8>::kSmemBytes, stream, p, m, box);
+  return launch_after(split_gqa_tc_kernel<R, KT>, dim3(grid), dim3(Lay<KT>::kThreads),
+                      (size_t)Lay<KT>::kSmemBytes, stream, p, m, box);
 }
 
-template <bool Q8>
+template <int KT>
 cudaError_t launch_q(const Launch& p, const Maps& m, int box, int grid, cudaStream_t stream) {
   switch (copies_for(p.H_q / p.H_kv)) {
-    case 8: return launch_r<8, Q8>(p, m, box, grid, stream);
-    case 4: return launch_r<4, Q8>(p, m, box, grid, stream);
-    case 2: return launch_r<2, Q8>(p, m, box, grid, stream);
-    default: return launch_r<1, Q8>(p, m, box, grid, stream);
+    case 8: return launch_r<8, KT>(p, m, box, grid, stream);
+    case 4: return launch_r<4, KT>(p, m, box, grid, stream);
+    case 2: return launch_r<2, KT>(p, m, box, grid, stream);
+    default: return launch_r<1, KT>(p, m, box, grid, stream);
   }
 }
 
@@ -1074,10 +1137,13 @@ int gqa_tc_resident_ctas(int sms) { return tc_ctas_per_sm() * sms; }
 
 cudaError_t launch_split_gqa_tc(const Launch& p, int grid, cudaStream_t stream) {
   const int G = p.H_q / p.H_kv;
-  // bf16 or E4M3 caches (kv_type 0 or 1), one source
-  if (!gqa_tc_supported(G, p.D_qk) || p.D_v != kD || p.extra_k || (p.kv_type != 0 && p.kv_type != 1))
+  // bf16, E4M3 or NVFP4 caches (kv_type 0, 1, 2; NVFP4 with an even number
+  // of KV heads: its scale rows are copied in pairs of heads), one source
+  if (!gqa_tc_supported(G, p.D_qk) || p.D_v != kD || p.extra_k || p.kv_type < 0 ||
+      p.kv_type > 2 || (p.kv_type == 2 && p.H_kv % 2 != 0))
     return cudaErrorInvalidValue;
-  const bool q8 = p.kv_type == 1;
+  const int kt = p.kv_type;
+  const bool q8 = kt != 0;
   const long long rows = (p.layout == DA_KV_CONTIGUOUS) ? (long long)p.B * p.width
                          : (p.layout == DA_KV_PAGED)    ? p.num_blocks * p.page_size
                                                         : p.num_blocks;
@@ -1096,16 +1162,18 @@ cudaError_t launch_split_gqa_tc(const Launch& p, int grid, cudaStream_t stream) 
     if (cudaGetSymbolAddress(&z, g_zero_tile) != cudaSuccess) return cudaErrorInvalidValue;
     kb = vb = z;
     r = 1;
-    heads = 1;
+    heads = kt == 2 ? 2 : 1;  // NVFP4: 16-byte scale rows
   }
   if (r * heads >= (1ll << 31)) return cudaErrorInvalidValue;  // signed TMA coordinates
-  const cuuint64_t es = q8 ? 1 : 2;  // bytes per cache element
-  const cuuint64_t d3[3] = {(cuuint64_t)kD, (cuuint64_t)heads, (cuuint64_t)r};
-  const cuuint64_t s3[2] = {(cuuint64_t)kD * es, (cuuint64_t)heads * kD * es};
-  const cuuint32_t b3[3] = {q8 ? 128u : 64u, 1, 16};
-  const cuuint64_t d2[2] = {(cuuint64_t)kD, (cuuint64_t)(r * heads)};
-  const cuuint64_t s2[1] = {(cuuint64_t)kD * es};
-  const cuuint32_t b2[2] = {q8 ? 128u : 64u, 1};
+  // elements of a head row in the map (NVFP4: its 64 code bytes) and bytes each
+  const cuuint64_t row = kt == 2 ? kD / 2 : kD, es = kt == 0 ? 2 : 1;
+  const cuuint32_t bx = kt == 0 ? 64u : (cuuint32_t)row;  // box: a 128-byte swizzle span or a row
+  const cuuint64_t d3[3] = {row, (cuuint64_t)heads, (cuuint64_t)r};
+  const cuuint64_t s3[2] = {row * es, (cuuint64_t)heads * row * es};
+  const cuuint32_t b3[3] = {bx, 1, 16};
+  const cuuint64_t d2[2] = {row, (cuuint64_t)(r * heads)};
+  const cuuint64_t s2[1] = {row * es};
+  const cuuint32_t b2[2] = {bx, 1};
   const cuuint64_t dq[2] = {(cuuint64_t)kD, (cuuint64_t)p.B * p.H_q};
   const cuuint64_t sq[1] = {(cuuint64_t)kD * 2};
   const cuuint32_t bq[2] = {64, (cuuint32_t)kQBoxRows};
@@ -1113,8 +1181,19 @@ cudaError_t launch_split_gqa_tc(const Launch& p, int grid, cudaStream_t stream) 
       !encode(&m.k2, kb, 2, d2, s2, b2, q8) || !encode(&m.v2, vb, 2, d2, s2, b2, q8) ||
       !encode(&m.q, p.q, 2, dq, sq, bq, false))
     return cudaErrorInvalidValue;
-  return q8 ? launch_q<true>(p, m, box ? 1 : 0, grid, stream)
-            : launch_q<false>(p, m, box ? 1 : 0, grid, stream);
+  if (kt == 2) {  // block scales [rows][H_kv * 8] bytes, after the codes
+    const uint8_t* ks = static_cast<const uint8_t*>(kb) + r * heads * row;
+    const uint8_t* vs = static_cast<const uint8_t*>(vb) + r * heads * row;
+    const cuuint64_t ds[2] = {(cuuint64_t)heads * 8, (cuuint64_t)r};
+    const cuuint64_t ss[1] = {(cuuint64_t)heads * 8};
+    const cuuint32_t bs[2] = {16, 16}, bs1[2] = {16, 1};
+    if (!encode(&m.ks, ks, 2, ds, ss, bs, true) || !encode(&m.vs, vs, 2, ds, ss, bs, true) ||
+        !encode(&m.ks2, ks, 2, ds, ss, bs1, true) || !encode(&m.vs2, vs, 2, ds, ss, bs1, true))
+      return cudaErrorInvalidValue;
+    return launch_q<2>(p, m, box ? 1 : 0, grid, stream);
+  }
+  return q8 ? launch_q<1>(p, m, box ? 1 : 0, grid, stream)
+            : launch_q<0>(p, m, box ? 1 : 0, grid, stream);
 }
 
 }  // namespace da

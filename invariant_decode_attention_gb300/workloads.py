@@ -645,6 +645,13 @@ def gqa16_paged_fp8(seed=1007):
     return quantize_fp8(gqa16_paged(seed), name="gqa16_paged_fp8_b32_h128x8_d128_p16")
 
 
+def gqa16_paged_nvfp4(seed=1007):
+    """The 16-heads-per-KV-head GQA paged workload (32 rows, 128/8 heads,
+    d = 128, page 16) with NVFP4 KV caches (global scales 1/2)."""
+    return nvfp4_kv(gqa16_paged(seed), seed=seed + 31,
+                    name="gqa16_paged_nvfp4_b32_h128x8_d128_p16")
+
+
 def gqa_paged_fp8(seed=1001):
     """The GQA paged workload (32 rows, 32/8 heads, d = 128, page 16, lengths
     512..8192) with an E4M3 KV cache, scales 1/64."""

@@ -36,6 +36,9 @@ def _workloads():
                          page_size=16, seed=72),
         "gqa_tc_fp8": W.quantize_fp8(W.make(W.PAGED, [40, 300, 1500, 5000], H_q=64, H_kv=2,
                                             D_qk=128, page_size=16, seed=73)),
+        "gqa_tc_nvfp4": W.nvfp4_kv(W.make(W.PAGED, [40, 300, 1500, 5000], H_q=64, H_kv=2,
+                                          D_qk=128, page_size=16, seed=74, draw_kv=False),
+                                   seed=75),
     }
 
 
@@ -50,7 +53,7 @@ def test_flag_validation(api):
 
 
 @gpu
-@pytest.mark.parametrize("kind", ["mla", "gqa_tc", "gqa_tc_fp8"])
+@pytest.mark.parametrize("kind", ["mla", "gqa_tc", "gqa_tc_fp8", "gqa_tc_nvfp4"])
 def test_stall_times_out_and_context_stays_usable(api, kind):
     wl = _workloads()[kind]
     g = wl.to("cuda")
