@@ -183,6 +183,8 @@ def build_workload(name, rank=0):
         return W.tiny(seed=1000 + seed_shift)
     if name == "mla_sparse":
         return W.mla_sparse(seed=1002 + seed_shift)
+    if name == "mla_sparse_fp8":
+        return W.mla_sparse_fp8(seed=1002 + seed_shift)
     if name == "gqa_paged_fp8":
         return W.gqa_paged_fp8(seed=1001 + seed_shift)
     if name == "long_context_fp8":
@@ -565,7 +567,8 @@ def main():
     ap.add_argument("--workload", default="long_context",
                     choices=["gqa_paged", "long_context", "tiny", "mla_sparse", "gqa_paged_fp8",
                              "long_context_fp8", "gqa_paged_nvfp4", "long_context_nvfp4",
-                             "gqa16_paged", "gqa16_paged_fp8", "gqa16_paged_nvfp4"])
+                             "gqa16_paged", "gqa16_paged_fp8", "gqa16_paged_nvfp4",
+                             "mla_sparse_fp8"])
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the secondary workloads and the CPU baseline")
     ap.add_argument("--nvfp4-only", type=int, nargs="+", metavar="ROWS",
@@ -648,7 +651,7 @@ def main():
         line["roofline_tensor"] = rec["roofline_tensor"]
     if not args.no_extra:
         extra = {}
-        for name in ("gqa_paged", "mla_sparse", "gqa16_paged", "gqa16_paged_fp8",
+        for name in ("gqa_paged", "mla_sparse", "mla_sparse_fp8", "gqa16_paged", "gqa16_paged_fp8",
                      "gqa16_paged_nvfp4", "tiny",
                      "gqa_paged_fp8",
                      "long_context_fp8", "gqa_paged_nvfp4", "long_context_nvfp4",

@@ -76,9 +76,11 @@ extern "C" {
  * gllm issue #98, Observation: NVFP4 Nemotron) but name no cache format;
  * this is the library's reading.  The kernel converts each byte exactly to
  * fp32, applies k_scale to the softmax scale and v_scale to a unit's output
- * (fixed roundings, independent of the batch).  One KV source only, no
- * shared latent (DA_ERR_UNSUPPORTED otherwise); DA_VARIANT_GQA_TC for groups
- * of 16 or more heads at D = 128, else DA_VARIANT_FMA.                     */
+ * (fixed roundings, independent of the batch).  One KV source only
+ * (DA_ERR_UNSUPPORTED otherwise).  DA_VARIANT_MLA for a shared latent cache
+ * (576/512: scores from k_scale * the row's 576 bytes, values from v_scale *
+ * its first 512), DA_VARIANT_GQA_TC for groups of 16 or more heads at
+ * D = 128, else DA_VARIANT_FMA.                                            */
 #define DA_KV_FP8_E4M3 1
 /* NVFP4: each head's row of D elements is stored as D/2 bytes of 4-bit E2M1
  * codes (element 2j in the low nibble of byte j; magnitudes 0, 0.5, 1, 1.5,
@@ -97,7 +99,9 @@ extern "C" {
 
 /* ---- kernel variants (chosen from the head config only, never B) ----- */
 #define DA_VARIANT_FMA 0 /* CUDA-core fp32 FMA, H_q/H_kv in 1..128, D in {64,128}    */
-#define DA_VARIANT_MLA 1 /* tcgen05 tensor cores, shared latent 576/512, 16..128 heads */
+/* tcgen05 tensor cores, shared latent 576/512, 16..128 heads (bf16, or E4M3
+ * converted to f16 in shared memory with one KV source)                     */
+#define DA_VARIANT_MLA 1
 /* tcgen05 tensor cores, separate K and V (bf16, or E4M3 or NVFP4 converted
  * to f16 in shared memory; NVFP4 with an even H_kv), 16..128 query heads per
  * KV head, D = 128, one KV source (other configs of >= 16 heads:
@@ -205,7 +209,9 @@ int decode_attn_plan(const da_problem* prob, int32_t policy, const int32_t* d_le
 
 /* The split kernel: every (row, split, KV head) partial.
  *   q:       bf16 [B, H_q, D_qk], 16-byte aligned
- *   k, v:    bf16 caches in prob->layout (v NULL when shared_latent), 16-byte aligned
+ *   k, v:    caches in prob->layout of prob->kv_dtype (bf16, E4M3 bytes, or
+ *            NVFP4 codes then block scales); v NULL when shared_latent;
+ *            16-byte aligned
  *   table:   int32 [B, width] page ids / slot indices (NULL for contiguous)
  *   lengths: the same int32[B] device array given to decode_attn_plan
  *   out:     bf16 [B, H_q, D_v]; lse: float [B, H_q] (natural log)

@@ -54,8 +54,9 @@ int check_problem(const da_problem* p) {
 // The kernel variant follows from the head configuration alone -- never from
 // the batch size or the lengths.
 int select_variant(const da_problem* p, Variant* v) {
-  // quantized caches: CUDA-core variant, one KV source
-  if (p->kv_dtype != DA_KV_BF16 && (p->shared_latent || p->extra_width > 0))
+  // quantized caches: one KV source; a shared latent cache in E4M3 only
+  if (p->kv_dtype != DA_KV_BF16 &&
+      (p->extra_width > 0 || (p->shared_latent && p->kv_dtype != DA_KV_FP8_E4M3)))
     return DA_ERR_UNSUPPORTED;
   if (p->shared_latent) {
     if (p->head_dim_qk == 576 && p->head_dim_v == 512 && p->num_kv_heads == 1 &&

@@ -224,39 +224,6 @@ __device__ __forceinline__ bool wait_bar(const Ctx& c, int i, uint32_t parity,
   }
 }
 
-// ---- quantized cache: f16 operands ----------------------------------------
-// Every E4M3 value is an f16 value, and so is every NVFP4 element (an E2M1
-// code, at most two significant bits, times an E4M3 block scale, at most
-// four, with magnitudes from 2^-10 to 2688), so K and V convert exactly; Q (bf16) is
-// brought into f16's range per row by a power of two: with m the row's
-// largest magnitude and 2^k <= m < 2^(k+1), the row is multiplied by
-// 2^e, e = 14 - k (clamped to [-113, 120]), so its largest element lies in
-// [2^14, 2^15).  Elements below 2^-14 of that (after scaling) become f16
-// subnormals, an absolute error of at most 2^-25 * 2^-e, far below the fp32
-// accumulation's.  The softmax divides the row's scores by 2^e again.
-__device__ __forceinline__ int q_prescale_exp(float maxabs) {
-  const uint32_t bits = __float_as_uint(maxabs);
-  const int biased = (int)((bits >> 23) & 0xff);
-  if (maxabs == 0.f || biased == 0xff) return 0;  // zero row, or inf / NaN: no scaling
-  const int k = (biased == 0) ? -127 : biased - 127;
-  return min(120, max(-113, 14 - k));
-}
-
-// 2^e for e in [-126, 127].
-__device__ __forceinline__ float exp2_int(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
-
-// Largest magnitude of eight bf16 values.
-__device__ __forceinline__ float bf16x8_absmax(uint4 w) {
-  const uint32_t v[4] = {w.x, w.y, w.z, w.w};
-  float m = 0.f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    m = fmaxf(m, fabsf(__uint_as_float(v[i] << 16)));
-    m = fmaxf(m, fabsf(__uint_as_float(v[i] & 0xffff0000u)));
-  }
-  return m;
-}
-
 // A unit: KV head h of one (row, split) item.
 struct TcUnit {
   int slot, b, h, t_begin, t_end;

@@ -41,6 +41,22 @@
 //              unit's Q dims 256..575 come by TMA tile copies at its start.
 //   warp 8     S MMA issue (one thread) and TMEM allocation.
 //   warp 9     P.V MMA issue (one thread).
+//   warps 10-13  E4M3 cache only: the converter (below).
+//
+// E4M3 latent cache (one byte per element, one fp32 scale for the scores
+// and one for the values).  Every E4M3 value is an f16 value, so the MMAs
+// run on f16 operands: the softmax warps write each Q row, prescaled by a
+// power of two into f16's range, into TMEM (dims 0..255) and into the
+// shared-memory Q regions (dims 256..575) themselves; the producer gathers
+// the 64-byte pieces of the 576-byte rows, region by region, into the upper
+// half of the operand stage (region j's 64 rows x 64 bytes at 36 KB + 4 KB j);
+// the converter warps widen them in place into the same 128-byte-swizzled f16
+// layout, regions 0..8 in order.  f16 region j covers [8 KB j, 8 KB j + 8 KB),
+// which overlaps only raw regions 2j - 9 and 2j - 8: already converted, except
+// for region 8 (its own raw bytes), so the raw bytes of regions 4..8 are read
+// into registers and the four warps meet at a barrier before any of those
+// regions is written.  The copy volume per tile halves; the number of copies
+// stays the same.
 // Every wait on an mbarrier is bounded; on time-out the kernel records
 // DA_DEVERR_TIMEOUT, every role leaves its loop, outstanding tensor-core work
 // is drained (bounded) and TMEM is freed.
@@ -79,7 +95,8 @@ enum { kFull0 = 0, kEmpty0 = kFull0 + kStages, kSFull0 = kEmpty0 + kStages,
        kSFree0 = kSFull0 + 2, kPFull0 = kSFree0 + 2, kODone0 = kPFull0 + 2,
        kOFree = kODone0 + 2, kQFull, kQTFull, kQFree, kDrain,
        kStall,  // never signalled: the time-out test hook waits on it
-       kNumBars };
+       kRawFull0,  // E4M3 cache: a stage's raw bytes landed (kFull: converted)
+       kNumBars = kRawFull0 + kStages };
 constexpr int kTmemSlot = kBarOffset + kNumBars * 8;
 static_assert(kStageOffset % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle atoms 1024-aligned");
 constexpr int kAbortSlot = kTmemSlot + 4;
@@ -94,7 +111,17 @@ __host__ __device__ constexpr int p_offset_in_stage(int half) {
 }
 static_assert(2 * kStageRegion == kPBytes, "P fills two regions");
 
-constexpr int kThreads = 320;
+// E4M3 cache: the raw bytes of a tile in the upper half of its stage,
+// region-major (region j: 64 rows x 64 bytes)
+constexpr int kRawInStage = kStageBytes / 2;  // 36864
+constexpr int kRawRegion = kSub * 64;         // 4096
+static_assert(kRawInStage + kRegions * kRawRegion == kStageBytes, "raw bytes fill the upper half");
+constexpr int kRawTileBytes = kSub * kDqk;    // 36864 bytes copied per tile
+constexpr int kConvBar = 1;                   // named barrier of the converter warps
+
+// KT: 0 bf16 cache, 1 E4M3 cache (four more warps: the converter)
+template <int KT>
+constexpr int threads_for() { return KT ? 448 : 320; }
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSCol = kQTCols;  // S buffers at [128, 192) and [192, 256)
 constexpr int kKSteps = kDqk / 16;   // 36 MMAs of K = 16 per S tile
@@ -103,8 +130,16 @@ constexpr uint32_t kOCol = 256;      // O accumulator columns [256, 512)
 static_assert(kSCol + 2 * kSub == kOCol && kOCol + kDvHalf == kTmemCols, "TMEM budget");
 constexpr float kRescaleLog2 = 8.f;
 
-constexpr uint32_t kIdescS = umma::idesc_bf16_f32(kHeads, kSub, false);
-constexpr uint32_t kIdescO = umma::idesc_bf16_f32(kHeads, kDvHalf, true);
+// bf16 operands (bf16 cache) or f16 operands (E4M3 cache)
+template <int KT>
+constexpr uint32_t idesc_s() {
+  return KT ? umma::idesc_f16_f32(kHeads, kSub, false) : umma::idesc_bf16_f32(kHeads, kSub, false);
+}
+template <int KT>
+constexpr uint32_t idesc_o() {
+  return KT ? umma::idesc_f16_f32(kHeads, kDvHalf, true)
+            : umma::idesc_bf16_f32(kHeads, kDvHalf, true);
+}
 
 // TMA copies from a 2-D tensor map (dim 0 = the 576 dims of a row, dim 1 =
 // rows) into this CTA's own shared memory, 128-byte swizzle applied by the
@@ -145,7 +180,7 @@ struct Ctx {
   uint32_t sbase;  // shared address of smem[0]
   volatile int* abort_flag;
   int32_t* hdr;
-  const CUtensorMap* tm_k;  // main cache as [rows, 576], box {64, 1}
+  const CUtensorMap* tm_k;  // main cache as [rows, 576], box {64, 1} (elements or E4M3 bytes)
   const CUtensorMap* tm_x;  // second source as [slots, 576], box {64, 1}
   const CUtensorMap* tm_q;  // q as [B * H_q, 576], box {64, 16}
 };
@@ -244,7 +279,9 @@ __device__ __forceinline__ bool latent_decode(const Launch& p, int b, int tok, i
 }
 
 // ---------------------------------------------------------------- producer
+template <int KT>
 __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
+  constexpr int kRowBytes = KT ? kDqk : 2 * kDqk;  // bytes of a cache row
   const int pt = threadIdx.x - 128;  // 0..127
   const int pw = pt >> 5, pl = pt & 31;
   uint32_t g = 0, n_ne = 0;
@@ -263,14 +300,18 @@ __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
     // Q dims 256..575 of row b into shared memory once the previous unit's S
     // MMAs are done: q_boxes 16-row boxes per 64-dim region, spread over the
     // four warps (rows past H_q belong to other rows or read as zeros; those
-    // heads' results are never written)
-    if (!wait_w(kQFree, (n_ne & 1) ^ 1)) break;
-    if (pt == 0) mbar_arrive_expect_tx(bar_addr(c, kQFull), kQSRegions * q_boxes * kQBoxRows * 128);
-    __syncwarp();
-    for (int i = pt; i < kQSRegions * q_boxes; i += 128) {
-      const int j = i / q_boxes, rb = i % q_boxes;
-      tma_tile(c.sbase + j * (kHeads * 128) + rb * (kQBoxRows * 128), c.tm_q, kQT + 64 * j,
-               x.b * p.H_q + rb * kQBoxRows, bar_addr(c, kQFull));
+    // heads' results are never written).  E4M3 cache: the softmax warps
+    // write them (as prescaled f16).
+    if constexpr (KT == 0) {
+      if (!wait_w(kQFree, (n_ne & 1) ^ 1)) break;
+      if (pt == 0)
+        mbar_arrive_expect_tx(bar_addr(c, kQFull), kQSRegions * q_boxes * kQBoxRows * 128);
+      __syncwarp();
+      for (int i = pt; i < kQSRegions * q_boxes; i += 128) {
+        const int j = i / q_boxes, rb = i % q_boxes;
+        tma_tile(c.sbase + j * (kHeads * 128) + rb * (kQBoxRows * 128), c.tm_q, kQT + 64 * j,
+                 x.b * p.H_q + rb * kQBoxRows, bar_addr(c, kQFull));
+      }
     }
     // warm L2 with the next unit's query rows (its softmax warps load them
     // into tensor memory at its start)
@@ -320,8 +361,9 @@ __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
         alive = false;
         break;
       }
-      const uint32_t full = bar_addr(c, kFull0 + stage);
-      if (pt == 0) mbar_arrive_expect_tx(full, kStageBytes);
+      // (E4M3 cache: the raw bytes' own barrier; the converter signals kFull)
+      const uint32_t full = bar_addr(c, (KT ? kRawFull0 : kFull0) + stage);
+      if (pt == 0) mbar_arrive_expect_tx(full, KT ? kRawTileBytes : kStageBytes);
       // lane q < 4 copies the group of entries 16*pw + 4q .. 16*pw + 4q + 3
       int r[4], sr[4];
 #pragma unroll
@@ -329,7 +371,15 @@ __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
         r[i] = __shfl_sync(0xffffffffu, my_row, (4 * pl + i) & 31);
         sr[i] = __shfl_sync(0xffffffffu, my_src, (4 * pl + i) & 31);
       }
-      if (pl < 4) {
+      if (KT == 1 && pl < 4) {
+        // E4M3 cache (one source): the group's 64-byte pieces of region j
+        // at raw region j, rows 16 pw + 4 pl .. + 3
+        const uint32_t dst = c.sbase + kStageOffset + stage * kStageBytes + kRawInStage +
+                             (kEntPerWarp * pw + 4 * pl) * 64;
+#pragma unroll 1
+        for (int j = 0; j < kRegions; ++j)
+          tma_gather4(dst + j * kRawRegion, c.tm_k, 64 * j, r[0], r[1], r[2], r[3], full);
+      } else if (pl < 4) {
         const uint32_t dst = c.sbase + kStageOffset + stage * kStageBytes +
                              (kEntPerWarp * pw + 4 * pl) * 128;
         if (sr[0] == sr[1] && sr[0] == sr[2] && sr[0] == sr[3]) {
@@ -351,7 +401,9 @@ __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
       if (t0 + kSub < x.t_end) decode(t0 + kSub, nx_word, nx_row, nx_src, nx_live);
       if (t0 + 2 * kSub < x.t_end) nx_word = fetch(t0 + 2 * kSub);
       if (nx_live && t0 + kSub < x.t_end)
-        prefetch_l2((nx_src ? p.extra_k : p.k) + (size_t)nx_row * kDqk, kDqk * 2);
+        prefetch_l2(reinterpret_cast<const uint8_t*>(nx_src ? p.extra_k : p.k) +
+                        (size_t)nx_row * kRowBytes,
+                    kRowBytes);
       my_row = nx_row;
       my_src = nx_src;
       my_live = nx_live;
@@ -364,10 +416,11 @@ __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
   if (pt == 0) {
     for (int st = 0; st < kStages; ++st) {
       const int last = (int)g - 1 - (((int)g - 1 - st) % kStages + kStages) % kStages;
-      if (last >= 0 && !mbar_wait(bar_addr(c, kFull0 + st), (last / kStages) & 1))
+      if (last >= 0 &&
+          !mbar_wait(bar_addr(c, (KT ? kRawFull0 : kFull0) + st), (last / kStages) & 1))
         set_error(p.hdr, DA_DEVERR_TIMEOUT);
     }
-    if (n_ne > 0 && !mbar_wait(bar_addr(c, kQFull), (n_ne - 1) & 1))
+    if (KT == 0 && n_ne > 0 && !mbar_wait(bar_addr(c, kQFull), (n_ne - 1) & 1))
       set_error(p.hdr, DA_DEVERR_TIMEOUT);
   }
 }
@@ -380,7 +433,9 @@ __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
 // read.  The softmax can lead the P.V thread by at most one tile (S(g) needs
 // stage g's copy, which needs P.V(g - 2) done), so the per-parity P-ready and
 // P.V-done barriers stay within one phase of every wait.
+template <int KT>
 __device__ void mma_s(const Launch& p, const Ctx& c, uint32_t tmem, int n_units, uint32_t& n_ne) {
+  constexpr uint32_t kIdescS = idesc_s<KT>();
   // base descriptors; per-MMA ones differ only by a constant start offset
   const uint64_t b_stage0 =  // K tile, K-major, 128-byte swizzle
       umma::smem_desc(c.sbase + kStageOffset, 16, 1024, umma::kSwizzle128B);
@@ -393,8 +448,10 @@ __device__ void mma_s(const Launch& p, const Ctx& c, uint32_t tmem, int n_units,
     const MlaUnit x = mla_unit(p, u);
     if (x.empty) continue;
     const int n_sub = (x.t_end - x.t_begin + kSub - 1) / kSub;
-    if (!wait_bar(c, kQFull, n_ne & 1)) return;   // Q dims 256.. in shared memory
-    fence_proxy_async();
+    if (KT == 0) {  // Q dims 256.. in shared memory (E4M3 cache: with kQTFull)
+      if (!wait_bar(c, kQFull, n_ne & 1)) return;
+      fence_proxy_async();
+    }
     if (!wait_bar(c, kQTFull, n_ne & 1)) return;  // Q dims 0..255 in TMEM
     umma::fence_after_sync();
     for (int i = 0; i < n_sub; ++i, ++g) {
@@ -425,7 +482,9 @@ __device__ void mma_s(const Launch& p, const Ctx& c, uint32_t tmem, int n_units,
 }
 
 // O += P(g) V(g): P and V both sit in the stage of tile g.
+template <int KT>
 __device__ void mma_pv(const Launch& p, const Ctx& c, uint32_t tmem, int n_units, uint32_t& g) {
+  constexpr uint32_t kIdescO = idesc_o<KT>();
   const uint64_t b_stage0 =
       umma::smem_desc(c.sbase + kStageOffset, 16, 1024, umma::kSwizzle128B);
   const uint64_t b_v0 =      // V = leading dims of the K tile, MN-major
@@ -454,6 +513,15 @@ __device__ void mma_pv(const Launch& p, const Ctx& c, uint32_t tmem, int n_units
 }
 
 // ---------------------------------------------------------------- softmax + epilogue
+// bf16 pair (low half = lower dim) times 2^e as an f16 pair (exact but for
+// f16 subnormals, see q_prescale_exp).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t v, float sc) {
+  const __half2 h = __floats2half2_rn(__uint_as_float(v << 16) * sc,
+                                      __uint_as_float(v & 0xffff0000u) * sc);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+template <int KT>
 __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int n_units) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = threadIdx.x;  // head = tensor-memory lane
@@ -471,32 +539,78 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
   };
   // Q dims 0..255 of head `row` of row b into TMEM columns [0, 128): two bf16
   // per column, the lower dim in the low half; then signal the MMA thread.
-  auto load_q = [&](int b) {
+  // E4M3 cache: the row times 2^e as f16 (e from the row's largest
+  // magnitude, q_prescale_exp), dims 0..255 into TMEM the same way and dims
+  // 256..575 into the shared-memory Q regions (128-byte-swizzled rows);
+  // returns e (0 for a bf16 cache).
+  auto load_q = [&](int b) -> int {
     const bool ok = row < p.H_q;
     const uint4* qrow = reinterpret_cast<const uint4*>(p.q + ((size_t)b * p.H_q + row) * kDqk);
+    if constexpr (KT == 1) {
+      float mx = 0.f;
+      if (ok) {
+#pragma unroll 8
+        for (int i = 0; i < kDqk / 8; ++i) mx = fmaxf(mx, bf16x8_absmax(__ldg(qrow + i)));
+      }
+      const int e = q_prescale_exp(mx);
+      const float sc = exp2_int(e);
 #pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
-      uint4 w[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) w[i] = ok ? __ldg(qrow + half * 16 + i) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
+      for (int ch = 0; ch < kQT / 64; ++ch) {  // 64 dims = 32 columns
         uint32_t r32[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          r32[4 * i + 0] = w[ch * 8 + i].x;
-          r32[4 * i + 1] = w[ch * 8 + i].y;
-          r32[4 * i + 2] = w[ch * 8 + i].z;
-          r32[4 * i + 3] = w[ch * 8 + i].w;
+          const uint4 w = ok ? __ldg(qrow + ch * 8 + i) : make_uint4(0, 0, 0, 0);
+          r32[4 * i + 0] = bf16x2_to_f16x2_scaled(w.x, sc);
+          r32[4 * i + 1] = bf16x2_to_f16x2_scaled(w.y, sc);
+          r32[4 * i + 2] = bf16x2_to_f16x2_scaled(w.z, sc);
+          r32[4 * i + 3] = bf16x2_to_f16x2_scaled(w.w, sc);
         }
-        umma::st_32x32b_x32_u(lane_base + (half * 2 + ch) * 32, r32);
+        umma::st_32x32b_x32_u(lane_base + ch * 32, r32);
       }
+#pragma unroll 1
+      for (int j = 0; j < kQSRegions; ++j) {
+        uint8_t* qdst = c.smem + j * (kHeads * 128) + row * 128;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {  // 8 dims (16 bytes) per chunk
+          const uint4 w = ok ? __ldg(qrow + kQT / 8 + j * 8 + cc) : make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(qdst + ((cc ^ (row & 7)) << 4)) =
+              make_uint4(bf16x2_to_f16x2_scaled(w.x, sc), bf16x2_to_f16x2_scaled(w.y, sc),
+                         bf16x2_to_f16x2_scaled(w.z, sc), bf16x2_to_f16x2_scaled(w.w, sc));
+        }
+      }
+      fence_proxy_async();  // the S MMAs read these rows
+      umma::wait_st();
+      umma::fence_before_sync();
+      arrive_w(kQTFull);
+      return e;
+    } else {
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        uint4 w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          w[i] = ok ? __ldg(qrow + half * 16 + i) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          uint32_t r32[32];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            r32[4 * i + 0] = w[ch * 8 + i].x;
+            r32[4 * i + 1] = w[ch * 8 + i].y;
+            r32[4 * i + 2] = w[ch * 8 + i].z;
+            r32[4 * i + 3] = w[ch * 8 + i].w;
+          }
+          umma::st_32x32b_x32_u(lane_base + (half * 2 + ch) * 32, r32);
+        }
+      }
+      umma::wait_st();
+      umma::fence_before_sync();
+      arrive_w(kQTFull);
+      return 0;
     }
-    umma::wait_st();
-    umma::fence_before_sync();
-    arrive_w(kQTFull);
   };
   bool q_ready = false;  // Q of the coming unit already in TMEM
+  int e_next = 0;        // its prescale exponent (E4M3 cache)
   for (int u = blockIdx.x; u < n_units; u = next_unit(u)) {
     const MlaUnit x = mla_unit(p, u);
     const bool head_ok = row < p.H_q;
@@ -509,14 +623,17 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
       continue;
     }
     const int n_sub = (x.t_end - x.t_begin + kSub - 1) / kSub;
+    int e_q = e_next;
     if (!q_ready) {
       // (first unit only: later units get their Q while the previous unit's
       // epilogue is still ahead, see below)
       if (!wait_w(kQFree, (n_ne & 1) ^ 1)) return;
       umma::fence_after_sync();
-      load_q(x.b);
+      e_q = load_q(x.b);
     }
     q_ready = false;
+    // E4M3 cache: the scores carry Q's factor 2^e; the row takes it back here
+    const float row_scale = KT ? p.scale_log2 * exp2_int(-e_q) : p.scale_log2;
     float m_used = -INFINITY, l = 0.f;
     for (int i = 0; i < n_sub; ++i, ++g) {
       const int sb = g & 1;
@@ -537,7 +654,7 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
       float mt = -INFINITY;
 #pragma unroll
       for (int j = 0; j < kSub; ++j) {
-        s[j] = (j < n_valid) ? s[j] * p.scale_log2 : -INFINITY;
+        s[j] = (j < n_valid) ? s[j] * row_scale : -INFINITY;
         mt = fmaxf(mt, s[j]);
       }
       // the max used for the exponentials moves only when the tile max
@@ -551,8 +668,13 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
         const float p0 = ex2(s[j] - m_new), p1 = ex2(s[j + 1] - m_new);
         sum += p0;
         sum += p1;
-        const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-        pk[j / 2] = *reinterpret_cast<const uint32_t*>(&h);
+        if constexpr (KT == 1) {  // f16 operands
+          const __half2 h = __floats2half2_rn(p0, p1);
+          pk[j / 2] = *reinterpret_cast<const uint32_t*>(&h);
+        } else {
+          const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+          pk[j / 2] = *reinterpret_cast<const uint32_t*>(&h);
+        }
       }
       l = (i == 0) ? sum : fmaf(l, alpha, sum);
       // O is rescaled only when some head's max moved; the PV of the previous
@@ -592,7 +714,7 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
           if (x2.empty) continue;
           if (!wait_w(kQFree, n_ne & 1)) return;
           umma::fence_after_sync();
-          load_q(x2.b);
+          e_next = load_q(x2.b);
           q_ready = true;
           break;
         }
@@ -601,7 +723,8 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
     // epilogue: O / l for this half of the value dims
     if (!wait_w(kODone0 + ((g - 1) & 1), ((g - 1) >> 1) & 1)) return;
     umma::fence_after_sync();
-    const float inv = (l > 0.f) ? 1.f / l : 0.f;
+    // (an E4M3 cache's value scale multiplies the output once, here)
+    const float inv = ((l > 0.f) ? 1.f / l : 0.f) * (KT ? p.v_scale : 1.f);
 #pragma unroll 1
     for (int ch = 0; ch < kDvHalf / 32; ++ch) {
       float o[32];
@@ -646,7 +769,64 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// ---------------------------------------------------------------- converter
+// E4M3 cache only: warps 10-13.  Per tile, once its raw bytes have landed,
+// thread t widens 32 bytes of row t / 2 (dims 32 (t % 2) .. + 31 of each
+// region) into four 16-byte f16 chunks of the swizzled row, regions 0..3
+// first (below the raw bytes), then reads the raw bytes of regions 4..8,
+// meets the other three warps at a named barrier and writes those regions
+// (see the E4M3 note at the top).  The four warps decide together whether to
+// go on (a bounded wait that ran out in one of them ends all four), so none
+// is ever left at the barrier.
+__device__ void converter(const Launch& p, const Ctx& c, int n_units) {
+  const int ct = threadIdx.x - 320;  // 0..127
+  const int lane = ct & 31;
+  const int row = ct >> 1, hh = ct & 1;
+  uint32_t g = 0;
+  for (int u = blockIdx.x; u < n_units; u = next_unit(u)) {
+    const MlaUnit x = mla_unit(p, u);
+    if (x.empty) continue;
+    const int n_sub = (x.t_end - x.t_begin + kSub - 1) / kSub;
+    for (int i = 0; i < n_sub; ++i, ++g) {
+      const int stage = g % kStages;
+      int ok = 1;
+      if (lane == 0) ok = wait_bar(c, kRawFull0 + stage, (g / kStages) & 1) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (named_bar_or(kConvBar, 128, ok == 0)) return;
+      uint8_t* st = c.smem + kStageOffset + stage * kStageBytes;
+      const uint8_t* raw = st + kRawInStage + row * 64 + hh * 32;
+      uint8_t* dst = st + row * 128;
+      // 32 E4M3 bytes (a, b) -> chunks 4 hh .. 4 hh + 3 of the row in region j
+      auto put = [&](int j, uint4 a, uint4 b) {
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          *reinterpret_cast<uint4*>(dst + j * kStageRegion + (((4 * hh + k) ^ (row & 7)) << 4)) =
+              make_uint4(e4m3x2_to_f16x2(w[2 * k]), e4m3x2_to_f16x2(w[2 * k] >> 16),
+                         e4m3x2_to_f16x2(w[2 * k + 1]), e4m3x2_to_f16x2(w[2 * k + 1] >> 16));
+      };
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        put(j, *reinterpret_cast<const uint4*>(raw + j * kRawRegion),
+            *reinterpret_cast<const uint4*>(raw + j * kRawRegion + 16));
+      uint4 ra[kRegions - 4], rb[kRegions - 4];
+#pragma unroll
+      for (int j = 4; j < kRegions; ++j) {
+        ra[j - 4] = *reinterpret_cast<const uint4*>(raw + j * kRawRegion);
+        rb[j - 4] = *reinterpret_cast<const uint4*>(raw + j * kRawRegion + 16);
+      }
+      named_bar_sync(kConvBar, 128);  // every raw byte of the tile is read
+#pragma unroll
+      for (int j = 4; j < kRegions; ++j) put(j, ra[j - 4], rb[j - 4]);
+      fence_proxy_async();  // the MMAs read the stage
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_addr(c, kFull0 + stage));
+    }
+  }
+}
+
+template <int KT>
+__global__ void __launch_bounds__(threads_for<KT>(), 1)
     split_mla_kernel(Launch p, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_x,
                      const __grid_constant__ CUtensorMap tm_q) {
@@ -676,6 +856,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           i == kOFree || i == kQTFull)
         count = 4;                                                   // softmax warps
       if (i == kDrain) count = 2;                                    // the two issuing threads
+      if (KT == 1 && i >= kFull0 && i < kFull0 + kStages) count = 4;  // the converter warps
       mbar_init(bar_addr(c, i), count);
     }
     *c.abort_flag = 0;
@@ -694,15 +875,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   // tiles whose P.V and units whose S MMAs the issuing threads got through
   volatile uint32_t* done = reinterpret_cast<volatile uint32_t*>(smem + kAbortSlot + 4);
   if (warp < 4) {
-    softmax_warps(p, c, tmem, n_units);
+    softmax_warps<KT>(p, c, tmem, n_units);
   } else if (warp < 8) {
-    producer(p, c, n_units);
+    producer<KT>(p, c, n_units);
+  } else if (warp >= 10) {
+    if constexpr (KT == 1) converter(p, c, n_units);
   } else if ((threadIdx.x & 31) == 0) {
     uint32_t count = 0;
     if (warp == 8)
-      mma_s(p, c, tmem, n_units, count);
+      mma_s<KT>(p, c, tmem, n_units, count);
     else
-      mma_pv(p, c, tmem, n_units, count);
+      mma_pv<KT>(p, c, tmem, n_units, count);
     done[warp - 8] = count;
     // drain (one commit per issuing thread): its arrival means every MMA the
     // thread issued has completed, so tensor memory can be freed
@@ -741,7 +924,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Stands in for an empty cache: dummy copies of masked entries read it.
-__device__ __nv_bfloat16 g_zero_row[kDqk];
+__device__ __align__(16) __nv_bfloat16 g_zero_row[kDqk];
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
@@ -756,33 +939,41 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// `rows` rows of 576 bf16 at `base` (16-byte aligned), box {64, box_rows},
-// 128-byte swizzle.
-bool encode_rows(CUtensorMap* tm, const void* base, long long rows, int box_rows) {
+// `rows` rows of 576 elements at `base` (16-byte aligned), box {64, box_rows}:
+// bf16 with the 128-byte swizzle, or E4M3 bytes without swizzle (`bytes`).
+bool encode_rows(CUtensorMap* tm, const void* base, long long rows, int box_rows,
+                 bool bytes = false) {
   const PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn || rows < 1 || rows > (1ll << 32)) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)kDqk, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)kDqk * 2};
+  const cuuint64_t strides[1] = {(cuuint64_t)kDqk * (bytes ? 1 : 2)};
   const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   const cuuint32_t elem[2] = {1, 1};
-  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  return fn(tm, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            const_cast<void*>(base), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            bytes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int KT>
+cudaError_t set_smem() {
+  static const cudaError_t e = cudaFuncSetAttribute(
+      split_mla_kernel<KT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  return e;
 }
 
 }  // namespace
 
 bool mla_supported(int H_q) { return H_q >= 16 && H_q <= kHeads; }
 
-// Persistent CTAs: as many as can be resident at once (one per SM), rounded
-// down to an even number (units are dealt to pairs of CTAs).
+// Persistent CTAs: as many as can be resident at once (one per SM: both
+// instantiations take nearly all of the shared memory), rounded down to an
+// even number (units are dealt to pairs of CTAs).
 int mla_resident_ctas(int sms) {
   static const int per_sm = [] {
-    if (cudaFuncSetAttribute(split_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes) != cudaSuccess)
-      return 1;
+    if (set_smem<0>() != cudaSuccess) return 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, split_mla_kernel, kThreads,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, split_mla_kernel<0>, threads_for<0>(),
                                                       kSmemBytes) != cudaSuccess || n < 1)
       n = 1;
     return n;
@@ -792,8 +983,10 @@ int mla_resident_ctas(int sms) {
 }
 
 cudaError_t launch_split_mla(const Launch& p, int grid, cudaStream_t stream) {
-  static const cudaError_t attr = cudaFuncSetAttribute(
-      split_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  // bf16 or E4M3 (kv_type 0 or 1; E4M3 with one source)
+  const int kt = p.kv_type;
+  if (kt < 0 || kt > 1 || (kt == 1 && p.extra_k)) return cudaErrorInvalidValue;
+  const cudaError_t attr = kt ? set_smem<1>() : set_smem<0>();
   if (attr != cudaSuccess) return attr;
   // rows addressable in the main cache under its layout
   const long long rows = (p.layout == DA_KV_CONTIGUOUS) ? (long long)p.B * p.width
@@ -804,10 +997,11 @@ cudaError_t launch_split_mla(const Launch& p, int grid, cudaStream_t stream) {
   memset(&tm_x, 0, sizeof tm_x);
   memset(&tm_q, 0, sizeof tm_q);
   if (rows >= 1) {
-    if (!encode_rows(&tm_k, p.k, rows, 1)) return cudaErrorInvalidValue;
+    if (!encode_rows(&tm_k, p.k, rows, 1, kt == 1)) return cudaErrorInvalidValue;
   } else {  // every entry is out of range: dummy copies read one zero row
     void* z = nullptr;
-    if (cudaGetSymbolAddress(&z, g_zero_row) != cudaSuccess || !encode_rows(&tm_k, z, 1, 1))
+    if (cudaGetSymbolAddress(&z, g_zero_row) != cudaSuccess ||
+        !encode_rows(&tm_k, z, 1, 1, kt == 1))
       return cudaErrorInvalidValue;
   }
   if (p.extra_k && p.extra_num_blocks >= 1 && !encode_rows(&tm_x, p.extra_k, p.extra_num_blocks, 1))
@@ -816,8 +1010,11 @@ cudaError_t launch_split_mla(const Launch& p, int grid, cudaStream_t stream) {
       !encode_rows(&tm_q, p.q, (long long)p.B * p.H_q, kQBoxRows))
     return cudaErrorInvalidValue;
   if (grid < 2 || (grid & 1)) return cudaErrorInvalidValue;  // whole pairs only
-  return launch_after(split_mla_kernel, dim3(grid), dim3(kThreads), (size_t)kSmemBytes, stream,
-                      p, tm_k, tm_x, tm_q);
+  if (kt == 1)
+    return launch_after(split_mla_kernel<1>, dim3(grid), dim3(threads_for<1>()),
+                        (size_t)kSmemBytes, stream, p, tm_k, tm_x, tm_q);
+  return launch_after(split_mla_kernel<0>, dim3(grid), dim3(threads_for<0>()), (size_t)kSmemBytes,
+                      stream, p, tm_k, tm_x, tm_q);
 }
 
 }  // namespace da

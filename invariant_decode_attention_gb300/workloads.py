@@ -492,7 +492,12 @@ class RaggedSweepLatent:
     lists are random (possibly repeated) slots."""
 
     def __init__(self, sizes, device="cuda", seed=1008, extra=False, num_slots=65536,
-                 width=2048, extra_slots=16384, extra_width=512):
+                 width=2048, extra_slots=16384, extra_width=512, kv_fp8=False):
+        # kv_fp8: an E4M3 latent cache (one source), scores at scale 1/64 and
+        # values at 1/32 of the stored bytes
+        assert not (kv_fp8 and extra), "E4M3 latent cache: one source"
+        self.kv_fp8 = kv_fp8
+        self.k_scale, self.v_scale = (1.0 / 64, 1.0 / 32) if kv_fp8 else (1.0, 1.0)
         self.sizes = list(sizes)
         self.device = device
         self.seed = seed
@@ -508,6 +513,9 @@ class RaggedSweepLatent:
                                 dtype=torch.bfloat16)
         self.xpool = (torch.randn((extra_slots, 1, 576), generator=gd, device=device,
                                   dtype=torch.bfloat16) if extra else None)
+        if kv_fp8:
+            self.k_t = _e4m3_bytes(self.k_t, self.k_scale)
+            self.pool = _e4m3_bytes(self.pool, self.k_scale)
         self._qt, self._kt = self.q_t.to(device), self.k_t.to(device)
         self._xkt = self.xk_t.to(device) if extra else None
 
@@ -521,7 +529,12 @@ class RaggedSweepLatent:
                          extra_lengths=torch.tensor([LATENT_TARGET_EXTRA], dtype=torch.int32))
         return Workload("latent_solo", INDEXED, self.q_t[None], self.k_t, None,
                         torch.tensor([LATENT_TARGET_LEN], dtype=torch.int32), table, 0, 128, 1,
-                        576, 512, 576 ** -0.5, **extra)
+                        576, 512, 576 ** -0.5, **extra, **self._fp8_kw())
+
+    def _fp8_kw(self):
+        if not self.kv_fp8:
+            return {}
+        return dict(kv_fp8=True, k_scale=self.k_scale, v_scale=self.v_scale)
 
     def solo(self):
         return self.solo_cpu().to(self.device)
@@ -557,7 +570,8 @@ class RaggedSweepLatent:
             extra = dict(extra_k=self.xpool, extra_v=None, extra_table=xt.to(self.device),
                          extra_lengths=el.to(self.device))
         wl = Workload(f"latent_ragged_b{B}", INDEXED, q, self.pool, None, lens.to(self.device),
-                      table.to(self.device), 0, 128, 1, 576, 512, 576 ** -0.5, **extra)
+                      table.to(self.device), 0, 128, 1, 576, 512, 576 ** -0.5, **extra,
+                      **self._fp8_kw())
         return wl, pos
 
 
@@ -589,13 +603,14 @@ def mla_sparse_extra(seed=1005):
 
 def quantize_fp8(wl, k_scale=1.0 / 64, v_scale=1.0 / 64, name=None):
     """The same workload with its K and V caches stored as E4M3 bytes:
-    ``bytes = float8_e4m3fn(value / scale)`` (torch's conversion, round to
+    ``bytes = float8_e4m3fn(value / k_scale)`` (torch's conversion, round to
     nearest even).  With N(0, 1) data and scale 1/64 every value stays far
-    inside the format's range (|value / scale| < 448)."""
-    assert wl.v is not None and wl.extra_k is None, "separate K and V, one source"
-    def q8(t, scale):
-        return (t.float() / scale).to(torch.float8_e4m3fn).view(torch.uint8)
-    return dataclasses.replace(wl, k=q8(wl.k, k_scale), v=q8(wl.v, v_scale), kv_fp8=True,
+    inside the format's range (|value / scale| < 448).  A shared latent
+    cache (v None) is one byte array: its scores use k_scale, its values (the
+    leading D_v bytes of each row) v_scale."""
+    assert wl.extra_k is None, "one source"
+    v = None if wl.v is None else _e4m3_bytes(wl.v, v_scale)
+    return dataclasses.replace(wl, k=_e4m3_bytes(wl.k, k_scale), v=v, kv_fp8=True,
                                k_scale=float(k_scale), v_scale=float(v_scale),
                                name=name or wl.name + "_fp8")
 
@@ -643,6 +658,12 @@ def gqa16_paged_fp8(seed=1007):
     """The 16-heads-per-KV-head GQA paged workload (32 rows, 128/8 heads,
     d = 128, page 16) with an E4M3 KV cache, scales 1/64."""
     return quantize_fp8(gqa16_paged(seed), name="gqa16_paged_fp8_b32_h128x8_d128_p16")
+
+
+def mla_sparse_fp8(seed=1002):
+    """The MLA-style sparse workload (64 rows, 128 heads, 576/512 latent,
+    top-k <= 2048 of 65536 slots) with an E4M3 latent cache, scales 1/64."""
+    return quantize_fp8(mla_sparse(seed), name="mla_sparse_fp8_b64_h128_d576_topk2048")
 
 
 def gqa16_paged_nvfp4(seed=1007):

@@ -76,8 +76,12 @@ def oracle_for(wl, rows=None, heads=None):
                         scale=wl.scale, layout=wl.layout, table=table,
                         page_size=wl.page_size, d_v=wl.D_v, rows=rows, heads=heads)
     if getattr(wl, "kv_fp8", False):
+        # a shared latent cache: values are the leading D_v bytes of each row,
+        # decoded at the value scale
+        v = (Fp8Cache(wl.k[..., :wl.D_v], wl.v_scale) if wl.v is None
+             else Fp8Cache(wl.v, wl.v_scale))
         return A.attend(wl.q.double().numpy(), Fp8Cache(wl.k, wl.k_scale),
-                        Fp8Cache(wl.v, wl.v_scale), wl.lengths.numpy(), scale=wl.scale,
+                        v, wl.lengths.numpy(), scale=wl.scale,
                         layout=wl.layout, table=table, page_size=wl.page_size, d_v=wl.D_v,
                         rows=rows, heads=heads)
     extra = {}

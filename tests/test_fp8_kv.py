@@ -77,7 +77,8 @@ def test_fp8_argument_rules(api):
         (_prob(api, k_scale=0.0), 1), (_prob(api, v_scale=float("nan")), 1),
         (_prob(api, kv_dtype=7), 1),
         (_prob(api, num_q_heads=128, num_kv_heads=1, head_dim_qk=576, head_dim_v=512,
-               shared_latent=True, layout="indexed"), 2),   # tensor-core variant: unsupported
+               shared_latent=True, layout="indexed", extra_width=16, extra_num_blocks=4),
+         2),                                                  # second latent source: unsupported
         (_prob(api, extra_width=16, extra_num_blocks=4), 2),  # second source: unsupported
     ]
     import ctypes

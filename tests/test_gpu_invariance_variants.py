@@ -11,8 +11,8 @@ itself matches the fp64 oracle, and repeated runs must be identical.
 Families: the E4M3 (one-byte cache) instantiation of the CUDA-core kernel,
 the CUDA-core kernel with a second KV source, the CUDA-core kernel on groups
 it cuts into head chunks (8 and 3 query heads per KV head at d = 128), the
-tensor-core shared-latent kernel, and the tensor-core kernel with a second
-latent source.
+tensor-core shared-latent kernel on bf16 and on E4M3 latent caches, and the
+tensor-core kernel with a second latent source.
 """
 
 import pytest
@@ -72,4 +72,9 @@ def test_latent_ragged_sweep_bitwise(api):
 
 def test_latent_extra_source_ragged_sweep_bitwise(api):
     sweep = W.RaggedSweepLatent(SIZES, extra=True)
+    _sweep(api, sweep, sweep.solo_cpu())
+
+
+def test_latent_fp8_ragged_sweep_bitwise(api):
+    sweep = W.RaggedSweepLatent(SIZES, kv_fp8=True)
     _sweep(api, sweep, sweep.solo_cpu())

@@ -32,6 +32,9 @@ def _workloads():
     return {
         "mla": W.make(W.INDEXED, [40, 300, 1500, 2048], H_q=128, H_kv=1, D_qk=576, D_v=512,
                       latent=True, num_slots=4096, seed=71),
+        "mla_fp8": W.quantize_fp8(W.make(W.INDEXED, [40, 300, 1500, 2048], H_q=128, H_kv=1,
+                                         D_qk=576, D_v=512, latent=True, num_slots=4096,
+                                         seed=76)),
         "gqa_tc": W.make(W.PAGED, [40, 300, 1500, 5000], H_q=64, H_kv=2, D_qk=128,
                          page_size=16, seed=72),
         "gqa_tc_fp8": W.quantize_fp8(W.make(W.PAGED, [40, 300, 1500, 5000], H_q=64, H_kv=2,
@@ -53,13 +56,13 @@ def test_flag_validation(api):
 
 
 @gpu
-@pytest.mark.parametrize("kind", ["mla", "gqa_tc", "gqa_tc_fp8", "gqa_tc_nvfp4"])
+@pytest.mark.parametrize("kind", ["mla", "mla_fp8", "gqa_tc", "gqa_tc_fp8", "gqa_tc_nvfp4"])
 def test_stall_times_out_and_context_stays_usable(api, kind):
     wl = _workloads()[kind]
     g = wl.to("cuda")
     prob = api.problem_for(g)
     variant = api.split_constants(prob)[0]
-    assert variant == (api.VARIANT_MLA if kind == "mla" else api.VARIANT_GQA_TC)
+    assert variant == (api.VARIANT_MLA if kind.startswith("mla") else api.VARIANT_GQA_TC)
     o_ref, l_ref = [t.clone() for t in api.run_workload(g)]
 
     prob.flags = api.FLAG_TEST_STALL
