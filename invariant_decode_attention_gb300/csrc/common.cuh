@@ -250,6 +250,18 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
+// Arrive on the mbarrier at shared address `bar` once every cp.async this
+// thread has issued so far has landed.  The arrival is not added to the
+// barrier's pending count: its initial count includes it.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Wait until every cp.async this thread has issued has landed.
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
@@ -353,6 +365,23 @@ __device__ __forceinline__ float bf16x8_absmax(uint4 w) {
     m = fmaxf(m, fabsf(__uint_as_float(v[i] & 0xffff0000u)));
   }
   return m;
+}
+
+// Running maximum of bf16 magnitudes as integers: the magnitude bits of a
+// bf16 (sign cleared) order like the values for every non-NaN value, so
+// `acc` keeps, per 16-bit half, the largest magnitude's bits seen so far
+// (a NaN's bits sort above infinity's; q_prescale_exp treats both alike).
+__device__ __forceinline__ uint32_t bf16x8_absmax_bits(uint32_t acc, uint4 w) {
+  acc = __vmaxu2(acc, w.x & 0x7fff7fffu);
+  acc = __vmaxu2(acc, w.y & 0x7fff7fffu);
+  acc = __vmaxu2(acc, w.z & 0x7fff7fffu);
+  return __vmaxu2(acc, w.w & 0x7fff7fffu);
+}
+
+// The fp32 value of the larger of the two magnitudes held by `acc`.
+__device__ __forceinline__ float bf16_absmax_value(uint32_t acc) {
+  const uint32_t m = max(acc & 0xffffu, acc >> 16);
+  return __uint_as_float(m << 16);
 }
 
 // Barrier over `n` threads that also returns the OR of `pred` across them.

@@ -45,18 +45,20 @@
 //
 // E4M3 latent cache (one byte per element, one fp32 scale for the scores
 // and one for the values).  Every E4M3 value is an f16 value, so the MMAs
-// run on f16 operands: the softmax warps write each Q row, prescaled by a
-// power of two into f16's range, into TMEM (dims 0..255) and into the
-// shared-memory Q regions (dims 256..575) themselves; the producer gathers
-// the 64-byte pieces of the 576-byte rows, region by region, into the upper
-// half of the operand stage (region j's 64 rows x 64 bytes at 36 KB + 4 KB j);
-// the converter warps widen them in place into the same 128-byte-swizzled f16
-// layout, regions 0..8 in order.  f16 region j covers [8 KB j, 8 KB j + 8 KB),
-// which overlaps only raw regions 2j - 9 and 2j - 8: already converted, except
-// for region 8 (its own raw bytes), so the raw bytes of regions 4..8 are read
-// into registers and the four warps meet at a barrier before any of those
-// regions is written.  The copy volume per tile halves; the number of copies
-// stays the same.
+// run on f16 operands.  Q: dims 256..575 arrive by TMA as for bf16 and the
+// softmax warps rescale them in place, dims 0..255 go to TMEM as f16 -- the
+// row times 2^e, e from its largest magnitude, so it lies in f16's range.
+// K: the four producer warps copy each row's 576 bytes with 16-byte cp.async
+// (consecutive threads take consecutive runs of a row, so a row's copies
+// coalesce) into the upper half of the operand stage as three 192-byte
+// pieces, piece c of rows 0..63 back to back at 36 KB + 12 KB c; each thread
+// arrives on the stage's barrier once its copies have landed.  (Gathers
+// through the TMA unit of rows at random addresses proved to be bound by the
+// unit's per-request cost, not by HBM.)  The converter warps widen the bytes
+// in place into the 128-byte-swizzled f16 layout.  Piece 0 becomes f16 regions
+// 0..2, below the raw bytes; pieces 1 and 2 are read into registers and the
+// four warps meet at a barrier before regions 3..8 (which cover the raw
+// bytes) are written.
 // Every wait on an mbarrier is bounded; on time-out the kernel records
 // DA_DEVERR_TIMEOUT, every role leaves its loop, outstanding tensor-core work
 // is drained (bounded) and TMEM is freed.
@@ -100,7 +102,10 @@ enum { kFull0 = 0, kEmpty0 = kFull0 + kStages, kSFull0 = kEmpty0 + kStages,
 constexpr int kTmemSlot = kBarOffset + kNumBars * 8;
 static_assert(kStageOffset % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle atoms 1024-aligned");
 constexpr int kAbortSlot = kTmemSlot + 4;
-constexpr int kSmemBytes = kAbortSlot + 12;
+// the global address of each entry's cache row, two tiles' worth
+// (producer lanes -> all producer threads)
+constexpr int kRowsSlot = (kAbortSlot + 12 + 15) / 16 * 16;
+constexpr int kSmemBytes = kRowsSlot + 2 * 64 * 8;
 static_assert(kSmemBytes <= 232448, "fits the 227 KB per-block limit");
 
 // P of a tile sits in its stage over K dims that only S reads: regions 4-5
@@ -111,13 +116,19 @@ __host__ __device__ constexpr int p_offset_in_stage(int half) {
 }
 static_assert(2 * kStageRegion == kPBytes, "P fills two regions");
 
-// E4M3 cache: the raw bytes of a tile in the upper half of its stage,
-// region-major (region j: 64 rows x 64 bytes)
+// E4M3 cache: the raw bytes of a tile in the upper half of its stage, as
+// three pieces of 192 bytes per row (dims 192 c .. 192 c + 191), piece c of
+// the 64 rows back to back
 constexpr int kRawInStage = kStageBytes / 2;  // 36864
-constexpr int kRawRegion = kSub * 64;         // 4096
-static_assert(kRawInStage + kRegions * kRawRegion == kStageBytes, "raw bytes fill the upper half");
-constexpr int kRawTileBytes = kSub * kDqk;    // 36864 bytes copied per tile
+constexpr int kRawPiece = 192;                // bytes of a row per copy
+constexpr int kRawPieces = kDqk / kRawPiece;  // 3
+constexpr int kRawPieceBytes = kSub * kRawPiece;  // 12288
+static_assert(kRawInStage + kRawPieces * kRawPieceBytes == kStageBytes,
+              "raw bytes fill the upper half");
+static_assert((kRawPiece / 64) * kStageRegion <= kRawInStage,
+              "piece 0's f16 regions end below the raw bytes");
 constexpr int kConvBar = 1;                   // named barrier of the converter warps
+constexpr int kProdBar = 2;                   // named barrier of the producer warps
 
 // KT: 0 bf16 cache, 1 E4M3 cache (four more warps: the converter)
 template <int KT>
@@ -146,16 +157,6 @@ constexpr uint32_t idesc_o() {
 // copy engine from the shared-memory address; each completes its bytes on the
 // mbarrier at shared address `bar`.
 
-// Box {64, 1} at rows r0..r3: four 128-byte rows land at dst + 128 * i.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* tm, int col, int r0,
-                                            int r1, int r2, int r3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-      : "memory");
-}
-
 // One box of the map (its box dims) at (col, row).
 __device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap* tm, int col, int row,
                                          uint32_t bar) {
@@ -180,8 +181,6 @@ struct Ctx {
   uint32_t sbase;  // shared address of smem[0]
   volatile int* abort_flag;
   int32_t* hdr;
-  const CUtensorMap* tm_k;  // main cache as [rows, 576], box {64, 1} (elements or E4M3 bytes)
-  const CUtensorMap* tm_x;  // second source as [slots, 576], box {64, 1}
   const CUtensorMap* tm_q;  // q as [B * H_q, 576], box {64, 16}
 };
 
@@ -278,10 +277,24 @@ __device__ __forceinline__ bool latent_decode(const Launch& p, int b, int tok, i
   return word >= 0 && word < p.num_blocks;
 }
 
+// Stands in for an empty cache: dummy copies of masked entries read it.
+__device__ __align__(16) __nv_bfloat16 g_zero_row[kDqk];
+
 // ---------------------------------------------------------------- producer
+// The four warps copy a tile with 16-byte cp.async, consecutive threads
+// taking consecutive 16-byte runs of a row (so a row's copies coalesce); each
+// thread arrives on the stage's barrier once its own copies have landed.
+// (TMA gathers of rows at random addresses proved bound by the copy unit's
+// per-request cost, not by HBM.)  The warps meet at a named barrier per tile
+// (the entries' row addresses pass through shared memory), so every wait is
+// decided together -- a bounded wait that ran out in one warp ends all four
+// -- and none is ever left at the barrier.
 template <int KT>
 __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
   constexpr int kRowBytes = KT ? kDqk : 2 * kDqk;  // bytes of a cache row
+  constexpr int kRunsPerRow = kRowBytes / 16;      // 16-byte runs of a row
+  constexpr int kRunsPerThread = kSub * kRunsPerRow / 128;
+  static_assert(kSub * kRunsPerRow % 128 == 0, "a tile's runs split evenly over 128 threads");
   const int pt = threadIdx.x - 128;  // 0..127
   const int pw = pt >> 5, pl = pt & 31;
   uint32_t g = 0, n_ne = 0;
@@ -291,8 +304,14 @@ __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
   auto wait_w = [&](int bar, uint32_t parity) -> bool {
     int ok = 1;
     if (pl == 0) ok = wait_bar(c, bar, parity) ? 1 : 0;
-    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    return !named_bar_or(kProdBar, 128, ok == 0);
   };
+  // the main cache (or the zero row standing in for an empty one) and the
+  // second source
+  const uint8_t* kmain = p.kv_rows < 1 ? reinterpret_cast<const uint8_t*>(g_zero_row)
+                                       : reinterpret_cast<const uint8_t*>(p.k);
+  const uint8_t* kextra = reinterpret_cast<const uint8_t*>(p.extra_k);
   const int q_boxes = (min(p.H_q, kHeads) + kQBoxRows - 1) / kQBoxRows;  // per region
   for (int u = blockIdx.x; u < n_units && alive; u = next_unit(u)) {
     const MlaUnit x = mla_unit(p, u);
@@ -301,17 +320,14 @@ __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
     // MMAs are done: q_boxes 16-row boxes per 64-dim region, spread over the
     // four warps (rows past H_q belong to other rows or read as zeros; those
     // heads' results are never written).  E4M3 cache: the softmax warps
-    // write them (as prescaled f16).
-    if constexpr (KT == 0) {
-      if (!wait_w(kQFree, (n_ne & 1) ^ 1)) break;
-      if (pt == 0)
-        mbar_arrive_expect_tx(bar_addr(c, kQFull), kQSRegions * q_boxes * kQBoxRows * 128);
-      __syncwarp();
-      for (int i = pt; i < kQSRegions * q_boxes; i += 128) {
-        const int j = i / q_boxes, rb = i % q_boxes;
-        tma_tile(c.sbase + j * (kHeads * 128) + rb * (kQBoxRows * 128), c.tm_q, kQT + 64 * j,
-                 x.b * p.H_q + rb * kQBoxRows, bar_addr(c, kQFull));
-      }
+    // then rescale them into f16 in place.
+    if (!wait_w(kQFree, (n_ne & 1) ^ 1)) break;
+    if (pt == 0) mbar_arrive_expect_tx(bar_addr(c, kQFull), kQSRegions * q_boxes * kQBoxRows * 128);
+    __syncwarp();
+    for (int i = pt; i < kQSRegions * q_boxes; i += 128) {
+      const int j = i / q_boxes, rb = i % q_boxes;
+      tma_tile(c.sbase + j * (kHeads * 128) + rb * (kQBoxRows * 128), c.tm_q, kQT + 64 * j,
+               x.b * p.H_q + rb * kQBoxRows, bar_addr(c, kQFull));
     }
     // warm L2 with the next unit's query rows (its softmax warps load them
     // into tensor memory at its start)
@@ -363,39 +379,26 @@ __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
       }
       // (E4M3 cache: the raw bytes' own barrier; the converter signals kFull)
       const uint32_t full = bar_addr(c, (KT ? kRawFull0 : kFull0) + stage);
-      if (pt == 0) mbar_arrive_expect_tx(full, KT ? kRawTileBytes : kStageBytes);
-      // lane q < 4 copies the group of entries 16*pw + 4q .. 16*pw + 4q + 3
-      int r[4], sr[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        r[i] = __shfl_sync(0xffffffffu, my_row, (4 * pl + i) & 31);
-        sr[i] = __shfl_sync(0xffffffffu, my_src, (4 * pl + i) & 31);
+      // the row addresses of the tile's entries into shared memory, then run
+      // k of the tile (row k / kRunsPerRow, bytes 16 (k % kRunsPerRow) ..)
+      // by thread k % 128
+      const uint8_t** rows_s = reinterpret_cast<const uint8_t**>(c.smem + kRowsSlot) + (g & 1) * kSub;
+      if (pl < kEntPerWarp)
+        rows_s[kEntPerWarp * pw + pl] = (my_src ? kextra : kmain) + (size_t)my_row * kRowBytes;
+      named_bar_sync(kProdBar, 128);
+      const uint32_t st = c.sbase + kStageOffset + stage * kStageBytes;
+#pragma unroll 6
+      for (int i = 0; i < kRunsPerThread; ++i) {
+        const int k = pt + 128 * i;
+        const int rr = k / kRunsPerRow, q = k % kRunsPerRow;
+        // E4M3: raw piece q / 12, rows back to back; bf16: 64-dim region
+        // q / 8, chunk q % 8 of the row, 128-byte swizzle
+        const uint32_t dst =
+            KT ? st + kRawInStage + (q / 12) * kRawPieceBytes + rr * kRawPiece + (q % 12) * 16
+               : st + (q >> 3) * kStageRegion + rr * 128 + (((q & 7) ^ (rr & 7)) << 4);
+        cp_async16(dst, rows_s[rr] + q * 16);
       }
-      if (KT == 1 && pl < 4) {
-        // E4M3 cache (one source): the group's 64-byte pieces of region j
-        // at raw region j, rows 16 pw + 4 pl .. + 3
-        const uint32_t dst = c.sbase + kStageOffset + stage * kStageBytes + kRawInStage +
-                             (kEntPerWarp * pw + 4 * pl) * 64;
-#pragma unroll 1
-        for (int j = 0; j < kRegions; ++j)
-          tma_gather4(dst + j * kRawRegion, c.tm_k, 64 * j, r[0], r[1], r[2], r[3], full);
-      } else if (pl < 4) {
-        const uint32_t dst = c.sbase + kStageOffset + stage * kStageBytes +
-                             (kEntPerWarp * pw + 4 * pl) * 128;
-        if (sr[0] == sr[1] && sr[0] == sr[2] && sr[0] == sr[3]) {
-          const CUtensorMap* tm = sr[0] ? c.tm_x : c.tm_k;
-#pragma unroll 1
-          for (int j = 0; j < kRegions; ++j)
-            tma_gather4(dst + j * kStageRegion, tm, 64 * j, r[0], r[1], r[2], r[3], full);
-        } else {  // the group straddles the two sources: one row per copy
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-#pragma unroll 1
-            for (int j = 0; j < kRegions; ++j)
-              tma_tile(dst + i * 128 + j * kStageRegion, sr[i] ? c.tm_x : c.tm_k, 64 * j, r[i],
-                       full);
-        }
-      }
+      cp_async_mbar_arrive(full);
       // decode the next tile's words (loaded an iteration ago), load the
       // words of the tile after it, and start the next tile's rows towards L2
       if (t0 + kSub < x.t_end) decode(t0 + kSub, nx_word, nx_row, nx_src, nx_live);
@@ -413,16 +416,9 @@ __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
   if (bad) set_error(p.hdr, DA_DEVERR_INDEX);
   // leave no copy in flight into this CTA's shared memory (on the normal path
   // every stage was consumed and these waits return at once)
-  if (pt == 0) {
-    for (int st = 0; st < kStages; ++st) {
-      const int last = (int)g - 1 - (((int)g - 1 - st) % kStages + kStages) % kStages;
-      if (last >= 0 &&
-          !mbar_wait(bar_addr(c, (KT ? kRawFull0 : kFull0) + st), (last / kStages) & 1))
-        set_error(p.hdr, DA_DEVERR_TIMEOUT);
-    }
-    if (KT == 0 && n_ne > 0 && !mbar_wait(bar_addr(c, kQFull), (n_ne - 1) & 1))
-      set_error(p.hdr, DA_DEVERR_TIMEOUT);
-  }
+  cp_async_wait_all();
+  if (pt == 0 && n_ne > 0 && !mbar_wait(bar_addr(c, kQFull), (n_ne - 1) & 1))
+    set_error(p.hdr, DA_DEVERR_TIMEOUT);
 }
 
 // ---------------------------------------------------------------- MMA issue
@@ -448,7 +444,7 @@ __device__ void mma_s(const Launch& p, const Ctx& c, uint32_t tmem, int n_units,
     const MlaUnit x = mla_unit(p, u);
     if (x.empty) continue;
     const int n_sub = (x.t_end - x.t_begin + kSub - 1) / kSub;
-    if (KT == 0) {  // Q dims 256.. in shared memory (E4M3 cache: with kQTFull)
+    if (KT == 0) {  // Q dims 256.. in shared memory (E4M3 cache: rescaled, with kQTFull)
       if (!wait_bar(c, kQFull, n_ne & 1)) return;
       fence_proxy_async();
     }
@@ -540,49 +536,76 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
   // Q dims 0..255 of head `row` of row b into TMEM columns [0, 128): two bf16
   // per column, the lower dim in the low half; then signal the MMA thread.
   // E4M3 cache: the row times 2^e as f16 (e from the row's largest
-  // magnitude, q_prescale_exp), dims 0..255 into TMEM the same way and dims
-  // 256..575 into the shared-memory Q regions (128-byte-swizzled rows);
-  // returns e (0 for a bf16 cache).
-  auto load_q = [&](int b) -> int {
+  // magnitude, q_prescale_exp) -- dims 0..255 into TMEM the same way, dims
+  // 256..575 rescaled in place in the shared-memory Q regions once their TMA
+  // copy (kQFull, phase parity `qpar`) has landed; `e` gets the exponent (0
+  // for a bf16 cache).  False when a bounded wait ran out.
+  auto load_q = [&](int b, uint32_t qpar, int& e) -> bool {
     const bool ok = row < p.H_q;
     const uint4* qrow = reinterpret_cast<const uint4*>(p.q + ((size_t)b * p.H_q + row) * kDqk);
+    e = 0;
     if constexpr (KT == 1) {
-      float mx = 0.f;
-      if (ok) {
-#pragma unroll 8
-        for (int i = 0; i < kDqk / 8; ++i) mx = fmaxf(mx, bf16x8_absmax(__ldg(qrow + i)));
-      }
-      const int e = q_prescale_exp(mx);
-      const float sc = exp2_int(e);
+      if (!wait_w(kQFull, qpar)) return false;
+      // (the loops stay rolled: this runs once per unit, and its code is
+      // fetched cold each time)
+      uint8_t* qs = c.smem + row * 128;  // + region j * kHeads * 128 + swizzled chunk
+      uint32_t mb = 0;                   // magnitude bits, see bf16x8_absmax_bits
+      // dims 0..255: into TMEM as bf16 pairs (as for a bf16 cache) while
+      // taking the maximum; rescaled there below
 #pragma unroll 1
-      for (int ch = 0; ch < kQT / 64; ++ch) {  // 64 dims = 32 columns
+      for (int half = 0; half < 2; ++half) {
+        uint4 w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          w[i] = ok ? __ldg(qrow + half * 16 + i) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          uint32_t r32[32];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint4 v = w[ch * 8 + i];
+            mb = bf16x8_absmax_bits(mb, v);
+            r32[4 * i + 0] = v.x;
+            r32[4 * i + 1] = v.y;
+            r32[4 * i + 2] = v.z;
+            r32[4 * i + 3] = v.w;
+          }
+          umma::st_32x32b_x32_u(lane_base + (half * 2 + ch) * 32, r32);
+        }
+      }
+#pragma unroll 1
+      for (int j = 0; j < kQSRegions; ++j)
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+          mb = bf16x8_absmax_bits(mb, *reinterpret_cast<const uint4*>(
+                                          qs + j * (kHeads * 128) + ((cc ^ (row & 7)) << 4)));
+      e = q_prescale_exp(bf16_absmax_value(mb));
+      const float sc = exp2_int(e);
+      umma::wait_st();
+#pragma unroll 1
+      for (int ch = 0; ch < kQTCols / 32; ++ch) {
+        float f[32];
+        umma::ld_32x32b_x32(lane_base + ch * 32, f);
+        umma::wait_ld();
         uint32_t r32[32];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 w = ok ? __ldg(qrow + ch * 8 + i) : make_uint4(0, 0, 0, 0);
-          r32[4 * i + 0] = bf16x2_to_f16x2_scaled(w.x, sc);
-          r32[4 * i + 1] = bf16x2_to_f16x2_scaled(w.y, sc);
-          r32[4 * i + 2] = bf16x2_to_f16x2_scaled(w.z, sc);
-          r32[4 * i + 3] = bf16x2_to_f16x2_scaled(w.w, sc);
-        }
+        for (int i = 0; i < 32; ++i) r32[i] = bf16x2_to_f16x2_scaled(__float_as_uint(f[i]), sc);
         umma::st_32x32b_x32_u(lane_base + ch * 32, r32);
       }
 #pragma unroll 1
-      for (int j = 0; j < kQSRegions; ++j) {
-        uint8_t* qdst = c.smem + j * (kHeads * 128) + row * 128;
+      for (int j = 0; j < kQSRegions; ++j)
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {  // 8 dims (16 bytes) per chunk
-          const uint4 w = ok ? __ldg(qrow + kQT / 8 + j * 8 + cc) : make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(qdst + ((cc ^ (row & 7)) << 4)) =
-              make_uint4(bf16x2_to_f16x2_scaled(w.x, sc), bf16x2_to_f16x2_scaled(w.y, sc),
-                         bf16x2_to_f16x2_scaled(w.z, sc), bf16x2_to_f16x2_scaled(w.w, sc));
+        for (int cc = 0; cc < 8; ++cc) {  // 8 dims (16 bytes) per chunk, own row only
+          uint4* q16 = reinterpret_cast<uint4*>(qs + j * (kHeads * 128) + ((cc ^ (row & 7)) << 4));
+          const uint4 v = *q16;
+          *q16 = make_uint4(bf16x2_to_f16x2_scaled(v.x, sc), bf16x2_to_f16x2_scaled(v.y, sc),
+                            bf16x2_to_f16x2_scaled(v.z, sc), bf16x2_to_f16x2_scaled(v.w, sc));
         }
-      }
       fence_proxy_async();  // the S MMAs read these rows
       umma::wait_st();
       umma::fence_before_sync();
       arrive_w(kQTFull);
-      return e;
+      return true;
     } else {
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
@@ -606,7 +629,7 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
       umma::wait_st();
       umma::fence_before_sync();
       arrive_w(kQTFull);
-      return 0;
+      return true;
     }
   };
   bool q_ready = false;  // Q of the coming unit already in TMEM
@@ -629,7 +652,7 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
       // epilogue is still ahead, see below)
       if (!wait_w(kQFree, (n_ne & 1) ^ 1)) return;
       umma::fence_after_sync();
-      e_q = load_q(x.b);
+      if (!load_q(x.b, n_ne & 1, e_q)) return;
     }
     q_ready = false;
     // E4M3 cache: the scores carry Q's factor 2^e; the row takes it back here
@@ -714,7 +737,7 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
           if (x2.empty) continue;
           if (!wait_w(kQFree, n_ne & 1)) return;
           umma::fence_after_sync();
-          e_next = load_q(x2.b);
+          if (!load_q(x2.b, (n_ne + 1) & 1, e_next)) return;
           q_ready = true;
           break;
         }
@@ -771,13 +794,13 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
 
 // ---------------------------------------------------------------- converter
 // E4M3 cache only: warps 10-13.  Per tile, once its raw bytes have landed,
-// thread t widens 32 bytes of row t / 2 (dims 32 (t % 2) .. + 31 of each
-// region) into four 16-byte f16 chunks of the swizzled row, regions 0..3
-// first (below the raw bytes), then reads the raw bytes of regions 4..8,
-// meets the other three warps at a named barrier and writes those regions
-// (see the E4M3 note at the top).  The four warps decide together whether to
-// go on (a bounded wait that ran out in one of them ends all four), so none
-// is ever left at the barrier.
+// thread t widens the bytes 96 (t % 2) .. + 95 of row t / 2's three pieces
+// (six 16-byte runs of 16 dims each) into the row's 16-byte f16 chunks,
+// 128-byte-swizzled: piece 0 first (f16 regions 0..2, below the raw bytes),
+// then it reads pieces 1 and 2, meets the other three warps at a named
+// barrier and writes regions 3..8 (see the E4M3 note at the top).  The four
+// warps decide together whether to go on (a bounded wait that ran out in one
+// of them ends all four), so none is ever left at the barrier.
 __device__ void converter(const Launch& p, const Ctx& c, int n_units) {
   const int ct = threadIdx.x - 320;  // 0..127
   const int lane = ct & 31;
@@ -794,30 +817,33 @@ __device__ void converter(const Launch& p, const Ctx& c, int n_units) {
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (named_bar_or(kConvBar, 128, ok == 0)) return;
       uint8_t* st = c.smem + kStageOffset + stage * kStageBytes;
-      const uint8_t* raw = st + kRawInStage + row * 64 + hh * 32;
+      const uint8_t* raw = st + kRawInStage + row * kRawPiece + hh * 96;
       uint8_t* dst = st + row * 128;
-      // 32 E4M3 bytes (a, b) -> chunks 4 hh .. 4 hh + 3 of the row in region j
-      auto put = [&](int j, uint4 a, uint4 b) {
-        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          *reinterpret_cast<uint4*>(dst + j * kStageRegion + (((4 * hh + k) ^ (row & 7)) << 4)) =
-              make_uint4(e4m3x2_to_f16x2(w[2 * k]), e4m3x2_to_f16x2(w[2 * k] >> 16),
-                         e4m3x2_to_f16x2(w[2 * k + 1]), e4m3x2_to_f16x2(w[2 * k + 1] >> 16));
+      // 16 E4M3 bytes of dims d0 .. d0 + 15 (d0 a multiple of 16) -> two f16 chunks
+      auto put = [&](int d0, uint4 v) {
+        uint8_t* rd = dst + (d0 >> 6) * kStageRegion;
+        const int k0 = (d0 & 63) >> 3;
+        *reinterpret_cast<uint4*>(rd + ((k0 ^ (row & 7)) << 4)) =
+            make_uint4(e4m3x2_to_f16x2(v.x), e4m3x2_to_f16x2(v.x >> 16), e4m3x2_to_f16x2(v.y),
+                       e4m3x2_to_f16x2(v.y >> 16));
+        *reinterpret_cast<uint4*>(rd + (((k0 + 1) ^ (row & 7)) << 4)) =
+            make_uint4(e4m3x2_to_f16x2(v.z), e4m3x2_to_f16x2(v.z >> 16), e4m3x2_to_f16x2(v.w),
+                       e4m3x2_to_f16x2(v.w >> 16));
       };
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        put(j, *reinterpret_cast<const uint4*>(raw + j * kRawRegion),
-            *reinterpret_cast<const uint4*>(raw + j * kRawRegion + 16));
-      uint4 ra[kRegions - 4], rb[kRegions - 4];
+      for (int q = 0; q < 6; ++q)
+        put(96 * hh + 16 * q, *reinterpret_cast<const uint4*>(raw + 16 * q));
+      uint4 rv[2][6];
 #pragma unroll
-      for (int j = 4; j < kRegions; ++j) {
-        ra[j - 4] = *reinterpret_cast<const uint4*>(raw + j * kRawRegion);
-        rb[j - 4] = *reinterpret_cast<const uint4*>(raw + j * kRawRegion + 16);
-      }
+      for (int cc = 1; cc < kRawPieces; ++cc)
+#pragma unroll
+        for (int q = 0; q < 6; ++q)
+          rv[cc - 1][q] = *reinterpret_cast<const uint4*>(raw + cc * kRawPieceBytes + 16 * q);
       named_bar_sync(kConvBar, 128);  // every raw byte of the tile is read
 #pragma unroll
-      for (int j = 4; j < kRegions; ++j) put(j, ra[j - 4], rb[j - 4]);
+      for (int cc = 1; cc < kRawPieces; ++cc)
+#pragma unroll
+        for (int q = 0; q < 6; ++q) put(kRawPiece * cc + 96 * hh + 16 * q, rv[cc - 1][q]);
       fence_proxy_async();  // the MMAs read the stage
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_addr(c, kFull0 + stage));
@@ -827,8 +853,7 @@ __device__ void converter(const Launch& p, const Ctx& c, int n_units) {
 
 template <int KT>
 __global__ void __launch_bounds__(threads_for<KT>(), 1)
-    split_mla_kernel(Launch p, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_x,
+    split_mla_kernel(Launch p,
                      const __grid_constant__ CUtensorMap tm_q) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Ctx c;
@@ -836,8 +861,6 @@ __global__ void __launch_bounds__(threads_for<KT>(), 1)
   c.sbase = smem_addr(smem);
   c.abort_flag = reinterpret_cast<volatile int*>(smem + kAbortSlot);
   c.hdr = p.hdr;
-  c.tm_k = &tm_k;
-  c.tm_x = &tm_x;
   c.tm_q = &tm_q;
   const int warp = threadIdx.x >> 5;
   wait_prior_grid();  // the plan kernel's outputs
@@ -856,7 +879,10 @@ __global__ void __launch_bounds__(threads_for<KT>(), 1)
           i == kOFree || i == kQTFull)
         count = 4;                                                   // softmax warps
       if (i == kDrain) count = 2;                                    // the two issuing threads
-      if (KT == 1 && i >= kFull0 && i < kFull0 + kStages) count = 4;  // the converter warps
+      // a stage's copies: one cp.async arrival per producer thread (E4M3
+      // cache: on the raw barrier; kFull then counts the converter warps)
+      if (i >= kFull0 && i < kFull0 + kStages) count = KT ? 4 : 128;
+      if (KT == 1 && i >= kRawFull0 && i < kRawFull0 + kStages) count = 128;
       mbar_init(bar_addr(c, i), count);
     }
     *c.abort_flag = 0;
@@ -923,8 +949,6 @@ __global__ void __launch_bounds__(threads_for<KT>(), 1)
   }
 }
 
-// Stands in for an empty cache: dummy copies of masked entries read it.
-__device__ __align__(16) __nv_bfloat16 g_zero_row[kDqk];
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
@@ -939,19 +963,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// `rows` rows of 576 elements at `base` (16-byte aligned), box {64, box_rows}:
-// bf16 with the 128-byte swizzle, or E4M3 bytes without swizzle (`bytes`).
-bool encode_rows(CUtensorMap* tm, const void* base, long long rows, int box_rows,
-                 bool bytes = false) {
+// `rows` rows of 576 bf16 at `base` (16-byte aligned), box {64, box_rows},
+// 128-byte swizzle.
+bool encode_rows(CUtensorMap* tm, const void* base, long long rows, int box_rows) {
   const PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn || rows < 1 || rows > (1ll << 32)) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)kDqk, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)kDqk * (bytes ? 1 : 2)};
+  const cuuint64_t strides[1] = {(cuuint64_t)kDqk * 2};
   const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   const cuuint32_t elem[2] = {1, 1};
-  return fn(tm, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-            const_cast<void*>(base), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            bytes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -988,33 +1010,23 @@ cudaError_t launch_split_mla(const Launch& p, int grid, cudaStream_t stream) {
   if (kt < 0 || kt > 1 || (kt == 1 && p.extra_k)) return cudaErrorInvalidValue;
   const cudaError_t attr = kt ? set_smem<1>() : set_smem<0>();
   if (attr != cudaSuccess) return attr;
-  // rows addressable in the main cache under its layout
-  const long long rows = (p.layout == DA_KV_CONTIGUOUS) ? (long long)p.B * p.width
-                         : (p.layout == DA_KV_PAGED)    ? p.num_blocks * p.page_size
-                                                        : p.num_blocks;
-  alignas(64) CUtensorMap tm_k, tm_x, tm_q;
-  memset(&tm_k, 0, sizeof tm_k);
-  memset(&tm_x, 0, sizeof tm_x);
+  // rows addressable in the main cache under its layout (none: the kernel
+  // reads a zero row for every masked entry instead)
+  Launch lp = p;
+  lp.kv_rows = (p.layout == DA_KV_CONTIGUOUS) ? (long long)p.B * p.width
+               : (p.layout == DA_KV_PAGED)    ? p.num_blocks * p.page_size
+                                              : p.num_blocks;
+  alignas(64) CUtensorMap tm_q;
   memset(&tm_q, 0, sizeof tm_q);
-  if (rows >= 1) {
-    if (!encode_rows(&tm_k, p.k, rows, 1, kt == 1)) return cudaErrorInvalidValue;
-  } else {  // every entry is out of range: dummy copies read one zero row
-    void* z = nullptr;
-    if (cudaGetSymbolAddress(&z, g_zero_row) != cudaSuccess ||
-        !encode_rows(&tm_k, z, 1, 1, kt == 1))
-      return cudaErrorInvalidValue;
-  }
-  if (p.extra_k && p.extra_num_blocks >= 1 && !encode_rows(&tm_x, p.extra_k, p.extra_num_blocks, 1))
-    return cudaErrorInvalidValue;
   if ((long long)p.B * p.H_q >= kQBoxRows &&
       !encode_rows(&tm_q, p.q, (long long)p.B * p.H_q, kQBoxRows))
     return cudaErrorInvalidValue;
   if (grid < 2 || (grid & 1)) return cudaErrorInvalidValue;  // whole pairs only
   if (kt == 1)
     return launch_after(split_mla_kernel<1>, dim3(grid), dim3(threads_for<1>()),
-                        (size_t)kSmemBytes, stream, p, tm_k, tm_x, tm_q);
+                        (size_t)kSmemBytes, stream, lp, tm_q);
   return launch_after(split_mla_kernel<0>, dim3(grid), dim3(threads_for<0>()), (size_t)kSmemBytes,
-                      stream, p, tm_k, tm_x, tm_q);
+                      stream, lp, tm_q);
 }
 
 }  // namespace da
