@@ -18,13 +18,14 @@
 // than 2^8 (then its O row is rescaled in TMEM), a decision that depends only
 // on the unit's own scores.
 //
-// Memory.  Shared: two Q buffers (the next unit's Q loads while the current
-// one runs) and four 64-entry stages of K and V, each tile in the
-// 128-byte-swizzled layout the tensor core reads (two 64-dim regions of
-// 64 rows x 128 bytes).  P of a tile (128 heads x 64 entries, bf16) is
-// written over its stage's K tile once S has read it.  TMEM: two S buffers
-// and two O accumulators (the next unit's first P.V does not wait for the
-// previous unit's epilogue).
+// Memory.  Shared: six 64-entry stages of K and V (bf16 cache; three for a
+// quantized cache, plus its raw stages), each tile in the 128-byte-swizzled
+// layout the tensor core reads (two 64-dim regions of 64 rows x 128 bytes).
+// P of a tile (128 heads x 64 entries, 16-bit) is written over its stage's K
+// tile once S has read it.  TMEM: two S buffers, two O accumulators (the
+// next unit's first P.V does not wait for the previous unit's epilogue) and
+// two Q buffers (the S MMAs' A operand; the next unit's Q is written while
+// the current one runs).
 //
 // Loads (TMA).  For a contiguous cache and for pages of a multiple of 16
 // entries, each 16-entry group of a tile is 16 consecutive cache rows: one
@@ -38,9 +39,9 @@
 // or index lookups ahead of the copies, TMA issue; for a bf16 cache the two
 // warps take alternate tiles, so one issues copies while the other waits for
 // its next stage; for a quantized cache warp 8 alone); warp 10 the S MMAs
-// (one thread) and TMEM allocation; quantized cache: warps 11-14 converter;
-// last warp
-// the P.V MMAs (one thread).  Every mbarrier wait is bounded; on time-out the
+// (one thread) and TMEM allocation; warps 11-14 converter (Q into tensor
+// memory; quantized cache: K and V into the operand stages); warp 15 the
+// P.V MMAs (one thread).  Every mbarrier wait is bounded; on time-out the
 // kernel records DA_DEVERR_TIMEOUT, every role leaves its loop, outstanding
 // tensor-core work is drained (bounded) and TMEM is freed.
 //
@@ -63,23 +64,22 @@ static_assert(kT == 64, "one 128-byte swizzle row of P per head");
 constexpr int kRegion = kT * 128;           // 64 rows x 64 dims (16-bit elements)
 constexpr int kTileBytes = 2 * kRegion;     // K (or V) of a tile: 16 KB
 constexpr int kStageBytes = 2 * kTileBytes;  // K, then V
-constexpr int kQRegion = kRows * 128;       // 128 rows x 64 dims
-constexpr int kQBytes = 2 * kQRegion;       // 32 KB
 
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 6;     // operand stages
+constexpr int kMaxRawStages = 8;  // raw stages (quantized caches)
 enum {
   kFull0 = 0, kEmpty0 = kFull0 + kMaxStages,  // operand stages: ready / free
   kRawFull0 = kEmpty0 + kMaxStages,           // quantized cache: copies landed
-  kRawEmpty0 = kRawFull0 + kMaxStages,        // quantized cache: converted, reusable
-  kQConv0 = kRawEmpty0 + kMaxStages,          // quantized cache: Q in tensor memory
-  kQFull0 = kQConv0 + 2, kQFree0 = kQFull0 + 2,
-  // P ready and P.V done: four slots each (tile g uses slot g % 4, phase
-  // g / 4).  The S and P.V MMAs are issued by two threads, so the softmax can
-  // run up to three tiles ahead of the P.V thread (S(g) needs stage g's copy,
-  // which needs P.V(g - kStages) done); four slots keep every parity wait
-  // within one phase of its barrier.
-  kSFull0 = kQFree0 + 2, kSFree0 = kSFull0 + 2, kPFull0 = kSFree0 + 2, kPVDone0 = kPFull0 + 4,
-  kODone0 = kPVDone0 + 4, kEpiReady0 = kODone0 + 2, kOFree0 = kEpiReady0 + 2,
+  kRawEmpty0 = kRawFull0 + kMaxRawStages,     // quantized cache: converted, reusable
+  kQConv0 = kRawEmpty0 + kMaxRawStages,       // Q written to tensor memory
+  kQFree0 = kQConv0 + 2,
+  // P ready and P.V done: eight slots each (tile g uses slot g % 8, phase
+  // g / 8).  The S and P.V MMAs are issued by two threads, so the softmax can
+  // run up to kStages - 1 tiles ahead of the P.V thread (S(g) needs stage g's
+  // copy, which needs P.V(g - kStages) done); eight slots keep every parity
+  // wait within one phase of its barrier.
+  kSFull0 = kQFree0 + 2, kSFree0 = kSFull0 + 2, kPFull0 = kSFree0 + 2, kPVDone0 = kPFull0 + 8,
+  kODone0 = kPVDone0 + 8, kEpiReady0 = kODone0 + 2, kOFree0 = kEpiReady0 + 2,
   kDrain = kOFree0 + 2,
   kStall,  // never signalled: the time-out test hook waits on it
   kNumBars
@@ -87,18 +87,19 @@ enum {
 
 // Shared-memory map.  KT: 0 bf16 cache, 1 E4M3 (one byte per element), 2
 // NVFP4 (E2M1 codes and E4M3 block scales); Q8: a quantized cache (1 or 2).
-// bf16: two Q buffers (TMA copies, the S MMAs' A operand) and four operand
-// stages that TMA fills directly.  Quantized: Q lives in tensor memory
-// instead (the converter writes it there), TMA copies the cache bytes into
-// raw stages (one producer warp) and the converter warpgroup writes them, as
-// f16, into three operand stages (the MMAs then run on f16 operands, see the
-// converter).  Seven E4M3 raw stages keep 112 KB of the cache in flight per
-// SM, as many entries as 224 KB of bf16; eight NVFP4 stages keep 80 KB (512
-// entries, where the bf16 path has 256).
+// Q lives in tensor memory (the converter warps write it there, two buffers),
+// so shared memory holds only the cache.  bf16: six operand stages that TMA
+// fills directly (192 KB in flight per SM: a stage stays busy from its copy,
+// ≈ 3–4k cycles to land, through its S, softmax and P.V).  Quantized: TMA
+// copies the cache bytes into raw stages (one producer warp) and the
+// converter warpgroup writes them, as f16, into three operand stages (the
+// MMAs then run on f16 operands, see the converter).  Seven E4M3 raw stages
+// keep 112 KB of the cache in flight per SM; eight NVFP4 stages keep 80 KB
+// (512 entries).
 template <int KT>
 struct Lay {
   static constexpr bool Q8 = KT != 0;  // a quantized cache: the f16 converter path
-  static constexpr int kStages = Q8 ? 3 : 4;     // operand stages (K, V as 16-bit)
+  static constexpr int kStages = Q8 ? 3 : 6;     // operand stages (K, V as 16-bit)
   // Raw stage: E4M3 -- K rows, then V rows, 128 bytes each (16 KB); NVFP4 --
   // K codes, V codes (64 bytes a row), then K and V block scales (16 bytes a
   // row: the scale rows of two neighbouring heads, copied together) in 2 KB
@@ -110,7 +111,7 @@ struct Lay {
   static constexpr int kRawStageBytes = 2 * kRawCodeBytes + 2 * kRawScaleBytes;
   static constexpr int kRawTxBytes = 2 * kRawCodeBytes + (KT == 2 ? 2 * kT * 16 : 0);  // copied
   static constexpr int kRawStages = KT == 2 ? 8 : Q8 ? 7 : 0;
-  static constexpr int kStageOffset = Q8 ? 0 : 2 * kQBytes;
+  static constexpr int kStageOffset = 0;
   static constexpr int kRawOffset = kStageOffset + kStages * kStageBytes;
   static constexpr int kBarOffset = kRawOffset + kRawStages * kRawStageBytes;
   static_assert(kRawStageBytes % 1024 == 0, "raw stages keep 1 KB alignment");
@@ -122,20 +123,20 @@ struct Lay {
   static constexpr int kMergeOffset = (kAbortSlot + 4 + 15) / 16 * 16;
   static constexpr int kSmemBytes = kMergeOffset + (2 * 2 * kRows + kRows * 33) * 4;
   // warps 0-3 softmax, 4-7 epilogue, 8-9 producer, 10 S MMAs, 11-14
-  // converter (quantized cache), then the P.V MMAs' warp
-  static constexpr int kPvWarp = Q8 ? 15 : 11;
+  // converter (Q into tensor memory; quantized cache: K and V too), 15 the
+  // P.V MMAs
+  static constexpr int kPvWarp = 15;
   static constexpr int kThreads = (kPvWarp + 1) * 32;
   static_assert(kStageOffset % 1024 == 0 && kRawOffset % 1024 == 0, "aligned stages");
-  static_assert(kStages <= kMaxStages && kRawStages <= kMaxStages, "barrier slots");
+  static_assert(kStages <= kMaxStages && kRawStages <= kMaxRawStages, "barrier slots");
   static_assert(kSmemBytes <= 232448, "fits the 227 KB per-block limit");
 };
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSCol = 0;    // S buffers [0, 64) and [64, 128)
 constexpr uint32_t kOCol = 128;  // O accumulators [128, 256) and [256, 384)
-constexpr uint32_t kQCol = 384;  // quantized cache: two f16 Q buffers [384, 448), [448, 512)
+constexpr uint32_t kQCol = 384;  // two Q buffers [384, 448), [448, 512) (bf16 or f16 pairs)
 constexpr float kRescaleLog2 = 8.f;
-constexpr int kQBoxRows = 16;
 
 // bf16 operands (bf16 cache); f16 operands (quantized cache: E4M3 values and
 // NVFP4 code x block-scale products are f16 values, and Q is prescaled by a
@@ -191,7 +192,6 @@ struct Maps {
   // NVFP4 block scales as bytes [rows][H_kv * 8]: box {16, 16} (box path) and
   // {16, 1} (gather path) -- the 8-byte scale rows of heads 2i and 2i + 1
   CUtensorMap ks, vs, ks2, vs2;
-  CUtensorMap q;       // [B * H_q][128], box {64, 16}
 };
 
 struct Ctx {
@@ -265,10 +265,7 @@ __device__ void producer(const Launch& p, const Ctx& c, const Maps& m, int n_uni
   const int lane = threadIdx.x & 31;
   const int pw = (threadIdx.x >> 5) - 8;  // producer warp 0 or 1: tiles of its parity
   if (pw >= kWarpsCopying) return;
-  const int G = p.H_q / p.H_kv;
-  const int q_boxes = (G + kQBoxRows - 1) / kQBoxRows;
-  const int gp = kRows / R;  // rows per copy of the group
-  uint32_t g = 0, nq = 0;
+  uint32_t g = 0;
   bool bad = false;
   // table word holding entry `tok` (0 past the split or for a contiguous cache)
   auto word_of = [&](const TcUnit& x, int tok) -> int {
@@ -300,25 +297,11 @@ __device__ void producer(const Launch& p, const Ctx& c, const Maps& m, int n_uni
   bool alive = true;
   TcUnit x = tc_unit(p, blockIdx.x);  // blockIdx.x < n_units (the kernel checked)
   int w_first = box ? batch_word(x, 0) : 0;
-  for (int u = blockIdx.x; u < n_units && alive; u += gridDim.x, ++nq) {
+  for (int u = blockIdx.x; u < n_units && alive; u += gridDim.x) {
     const int u_next = u + (int)gridDim.x;
     const bool has_next = u_next < n_units;
     const TcUnit xn = has_next ? tc_unit(p, u_next) : x;  // in flight during this unit
     const int n_sub = (x.t_end - x.t_begin + kT - 1) / kT;
-    // Q of the unit's heads into Q buffer nq & 1 once the unit that used it
-    // last has finished its S MMAs
-    const int qb = nq & 1;
-    if (!Q8 && pw == 0 && !wait_w(kQFree0 + qb, ((nq >> 1) & 1) ^ 1)) break;
-    if (!Q8 && pw == 0 && lane == 0) {
-      const uint32_t qfull = bar_addr(c, kQFull0 + qb);
-      mbar_arrive_expect_tx(qfull, R * q_boxes * 2 * kQBoxRows * 128);
-      const uint32_t qdst = c.sbase + qb * kQBytes;
-      for (int cp = 0; cp < R; ++cp)  // every copy of the group's rows
-        for (int rb = 0; rb < q_boxes; ++rb)
-          for (int half = 0; half < 2; ++half)
-            tma_box2(qdst + half * kQRegion + (cp * gp + rb * kQBoxRows) * 128, &m.q, 64 * half,
-                     x.b * p.H_q + x.h * G + rb * kQBoxRows, qfull);
-    }
     int w_cur = w_first, w_nxt = 0, w_n0 = 0;
     if (box && n_sub > 8) w_nxt = batch_word(x, 1);
     // gather path: this lane's four words of the current and the next tile
@@ -420,10 +403,9 @@ __device__ void producer(const Launch& p, const Ctx& c, const Maps& m, int n_uni
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(p.hdr, DA_DEVERR_INDEX);
   // leave no copy in flight into this CTA's shared memory (on the normal path
-  // every stage and Q buffer was consumed and these waits return at once).
-  // A warp waits only for its own copies: tiles t < g of its parity (after a
-  // time-out, g is the tile it did not copy), which fill the stages of its
-  // parity; Q buffers are copied by warp 0 alone.
+  // every stage was consumed and these waits return at once).  A warp waits
+  // only for its own copies: tiles t < g of its parity (after a time-out, g
+  // is the tile it did not copy), which fill the stages of its parity.
   static_assert(kNS % kWarpsCopying == 0, "a stage is filled by one producer warp");
   if (lane == 0) {
     for (int st = pw; st < kNS; st += kWarpsCopying) {
@@ -431,20 +413,17 @@ __device__ void producer(const Launch& p, const Ctx& c, const Maps& m, int n_uni
       if (last >= 0 && !mbar_wait(bar_addr(c, kFullB + st), (last / kNS) & 1))
         set_error(p.hdr, DA_DEVERR_TIMEOUT);
     }
-    for (int qb = 0; qb < 2 && pw == 0 && !Q8; ++qb) {
-      const int last = (int)nq - 1 - (((int)nq - 1 - qb) % 2 + 2) % 2;
-      if (last >= 0 && !mbar_wait(bar_addr(c, kQFull0 + qb), (last >> 1) & 1))
-        set_error(p.hdr, DA_DEVERR_TIMEOUT);
-    }
   }
 }
 
 // ---------------------------------------------------------------- converter
-// Quantized cache only: warps 11-14.  Per unit, once the S MMAs of the unit two
-// back have released Q buffer qb (kQFree), each thread writes one MMA row of
-// Q into tensor memory -- warp w owns lanes 32 (w % 4) .. + 31 -- as f16
-// pairs, prescaled (q_prescale_exp; rows past the group are zeros), and the
-// MMA thread is told (kQConv).  Per tile, once its bytes are in raw stage
+// Warps 11-14.  Per unit, once the S MMAs of the unit two back have released
+// Q buffer qb (kQFree), each thread writes one MMA row of Q into tensor
+// memory -- warp w owns lanes 32 (w % 4) .. + 31 -- as bf16 pairs (bf16
+// cache) or as f16 pairs prescaled (quantized cache, q_prescale_exp); rows
+// past the group are zeros; then the MMA thread is told (kQConv).  The Q of
+// the next unit is written while the current one runs.  Quantized cache
+// only: per tile, once its bytes are in raw stage
 // g % kRawStages and operand stage g % 3 is free (the PV three tiles back
 // completed), K and V are written as f16 into the operand stage (NVFP4: each
 // code times its block scale, multiplied in f16) in the 128-byte-swizzled
@@ -456,6 +435,7 @@ __device__ void producer(const Launch& p, const Ctx& c, const Maps& m, int n_uni
 template <int R, int KT>
 __device__ void converter(const Launch& p, const Ctx& c, uint32_t tmem, int n_units, bool box) {
   using L = Lay<KT>;
+  constexpr bool Q8 = KT != 0;
   constexpr int kGp = kRows / R;  // rows per copy of the group
   const int ct = threadIdx.x - 11 * 32;  // 0..127
   const int warp = threadIdx.x >> 5, lane = ct & 31;
@@ -483,12 +463,15 @@ __device__ void converter(const Launch& p, const Ctx& c, uint32_t tmem, int n_un
     {
       const uint4* src = reinterpret_cast<const uint4*>(
           p.q + ((size_t)x.b * p.H_q + (size_t)x.h * G + (jq < G ? jq : 0)) * kD);
-      float mx = 0.f;
-      if (jq < G) {
+      float sc = 1.f;
+      if constexpr (Q8) {
+        float mx = 0.f;
+        if (jq < G) {
 #pragma unroll 4
-        for (int i = 0; i < kD / 8; ++i) mx = fmaxf(mx, bf16x8_absmax(__ldg(src + i)));
+          for (int i = 0; i < kD / 8; ++i) mx = fmaxf(mx, bf16x8_absmax(__ldg(src + i)));
+        }
+        sc = exp2_int(q_prescale_exp(mx));
       }
-      const float sc = exp2_int(q_prescale_exp(mx));
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
         uint32_t r32[32];
@@ -498,9 +481,13 @@ __device__ void converter(const Launch& p, const Ctx& c, uint32_t tmem, int n_un
           const uint32_t v[4] = {wi.x, wi.y, wi.z, wi.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const __half2 hh = __floats2half2_rn(__uint_as_float(v[e] << 16) * sc,
-                                                 __uint_as_float(v[e] & 0xffff0000u) * sc);
-            r32[4 * i + e] = *reinterpret_cast<const uint32_t*>(&hh);
+            if constexpr (Q8) {
+              const __half2 hh = __floats2half2_rn(__uint_as_float(v[e] << 16) * sc,
+                                                   __uint_as_float(v[e] & 0xffff0000u) * sc);
+              r32[4 * i + e] = *reinterpret_cast<const uint32_t*>(&hh);
+            } else {
+              r32[4 * i + e] = v[e];  // the bf16 pair as it is
+            }
           }
         }
         umma::st_32x32b_x32_u(lane_base + kQCol + qb * 64 + half * 32, r32);
@@ -509,61 +496,63 @@ __device__ void converter(const Launch& p, const Ctx& c, uint32_t tmem, int n_un
     }
     umma::fence_before_sync();
     arrive_w(kQConv0 + qb);
-    // ---- K and V of every tile
-    const int jj = ct & 7;        // 16-byte piece (dims 16 jj .. 16 jj + 15) of a row
-    const int r0 = ct >> 3;       // rows r0, r0 + 16, r0 + 32, r0 + 48 of a tile
-    for (int i = 0; i < n_sub; ++i, ++g) {
-      const int rs = g % L::kRawStages, os = g % L::kStages;
-      if (!wait_w(kRawFull0 + rs, (g / L::kRawStages) & 1)) return;
-      if (!wait_w(kEmpty0 + os, ((g / L::kStages) & 1) ^ 1)) return;
-      const uint8_t* raw = c.smem + L::kRawOffset + rs * L::kRawStageBytes;
-      uint8_t* op = c.smem + L::kStageOffset + os * kStageBytes;
-#pragma unroll
-      for (int kv = 0; kv < 2; ++kv) {
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int row = r0 + 16 * q4;
-          uint32_t h[8];  // f16 pairs of dims 16 jj .. 16 jj + 15, in order
-          if constexpr (KT == 2) {
-            // sixteen E2M1 codes and their one E4M3 block scale (byte jj of
-            // the head's eight), each exact in f16, multiplied exactly
-            const uint2 cw = *reinterpret_cast<const uint2*>(raw + kv * L::kRawCodeBytes +
-                                                             row * (kD / 2) + jj * 8);
-            const int srow = box ? row * 16 : (row >> 2) * 128 + (row & 3) * 16;
-            const uint32_t sb = raw[2 * L::kRawCodeBytes + kv * L::kRawScaleBytes + srow +
-                                    (x.h & 1) * 8 + jj];
-            const uint32_t s2 = __byte_perm(e4m3x2_to_f16x2(sb), 0, 0x1010);
-            uint32_t lo4[4], hi4[4];
-            e2m1x8_to_f16x2(cw.x, lo4);
-            e2m1x8_to_f16x2(cw.y, hi4);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              h[e] = hmul2(lo4[e], s2);
-              h[4 + e] = hmul2(hi4[e], s2);
+    if constexpr (Q8) {  // (bf16: TMA fills the operand stages)
+      // ---- K and V of every tile
+      const int jj = ct & 7;        // 16-byte piece (dims 16 jj .. 16 jj + 15) of a row
+      const int r0 = ct >> 3;       // rows r0, r0 + 16, r0 + 32, r0 + 48 of a tile
+      for (int i = 0; i < n_sub; ++i, ++g) {
+        const int rs = g % L::kRawStages, os = g % L::kStages;
+        if (!wait_w(kRawFull0 + rs, (g / L::kRawStages) & 1)) return;
+        if (!wait_w(kEmpty0 + os, ((g / L::kStages) & 1) ^ 1)) return;
+        const uint8_t* raw = c.smem + L::kRawOffset + rs * L::kRawStageBytes;
+        uint8_t* op = c.smem + L::kStageOffset + os * kStageBytes;
+  #pragma unroll
+        for (int kv = 0; kv < 2; ++kv) {
+  #pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int row = r0 + 16 * q4;
+            uint32_t h[8];  // f16 pairs of dims 16 jj .. 16 jj + 15, in order
+            if constexpr (KT == 2) {
+              // sixteen E2M1 codes and their one E4M3 block scale (byte jj of
+              // the head's eight), each exact in f16, multiplied exactly
+              const uint2 cw = *reinterpret_cast<const uint2*>(raw + kv * L::kRawCodeBytes +
+                                                               row * (kD / 2) + jj * 8);
+              const int srow = box ? row * 16 : (row >> 2) * 128 + (row & 3) * 16;
+              const uint32_t sb = raw[2 * L::kRawCodeBytes + kv * L::kRawScaleBytes + srow +
+                                      (x.h & 1) * 8 + jj];
+              const uint32_t s2 = __byte_perm(e4m3x2_to_f16x2(sb), 0, 0x1010);
+              uint32_t lo4[4], hi4[4];
+              e2m1x8_to_f16x2(cw.x, lo4);
+              e2m1x8_to_f16x2(cw.y, hi4);
+  #pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                h[e] = hmul2(lo4[e], s2);
+                h[4 + e] = hmul2(hi4[e], s2);
+              }
+            } else {
+              const uint4 b = *reinterpret_cast<const uint4*>(raw + kv * L::kRawCodeBytes +
+                                                              row * kD + jj * 16);
+              const uint32_t wb[4] = {b.x, b.y, b.z, b.w};
+  #pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                h[2 * e] = e4m3x2_to_f16x2(wb[e]);
+                h[2 * e + 1] = e4m3x2_to_f16x2(wb[e] >> 16);
+              }
             }
-          } else {
-            const uint4 b = *reinterpret_cast<const uint4*>(raw + kv * L::kRawCodeBytes +
-                                                            row * kD + jj * 16);
-            const uint32_t wb[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              h[2 * e] = e4m3x2_to_f16x2(wb[e]);
-              h[2 * e + 1] = e4m3x2_to_f16x2(wb[e] >> 16);
-            }
+            // dims 16 jj .. +7 and +8 .. +15: region jj / 4, chunks 2 (jj % 4) and +1
+            uint8_t* rbase = op + kv * kTileBytes + (jj >> 2) * kRegion + row * 128;
+            const int ch = 2 * (jj & 3);
+            const int sw = jj >> 2;  // 0: chunk ch first, 1: chunk ch + 1 first
+            const uint4 lo = make_uint4(h[0], h[1], h[2], h[3]);
+            const uint4 hi = make_uint4(h[4], h[5], h[6], h[7]);
+            *reinterpret_cast<uint4*>(rbase + (((ch + sw) ^ (row & 7)) << 4)) = sw ? hi : lo;
+            *reinterpret_cast<uint4*>(rbase + (((ch + 1 - sw) ^ (row & 7)) << 4)) = sw ? lo : hi;
           }
-          // dims 16 jj .. +7 and +8 .. +15: region jj / 4, chunks 2 (jj % 4) and +1
-          uint8_t* rbase = op + kv * kTileBytes + (jj >> 2) * kRegion + row * 128;
-          const int ch = 2 * (jj & 3);
-          const int sw = jj >> 2;  // 0: chunk ch first, 1: chunk ch + 1 first
-          const uint4 lo = make_uint4(h[0], h[1], h[2], h[3]);
-          const uint4 hi = make_uint4(h[4], h[5], h[6], h[7]);
-          *reinterpret_cast<uint4*>(rbase + (((ch + sw) ^ (row & 7)) << 4)) = sw ? hi : lo;
-          *reinterpret_cast<uint4*>(rbase + (((ch + 1 - sw) ^ (row & 7)) << 4)) = sw ? lo : hi;
         }
+        fence_proxy_async();
+        arrive_w(kFull0 + os);
+        arrive_w(kRawEmpty0 + rs);
       }
-      fence_proxy_async();
-      arrive_w(kFull0 + os);
-      arrive_w(kRawEmpty0 + rs);
     }
   }
 }
@@ -579,12 +568,9 @@ __device__ void mma_s(const Launch& p, const Ctx& c, uint32_t tmem, int n_units)
   using L = Lay<KT>;
   constexpr int kStages = L::kStages;
   constexpr uint32_t kIdescS = idesc_s<Q8>();
-  // Q in a Q buffer is ready: copied (bf16), or written to tensor memory (E4M3)
-  constexpr int kQReady0 = Q8 ? kQConv0 : kQFull0;
   // K-major tiles, 128-byte swizzle: 8-row groups 1024 bytes apart
   const uint64_t b_k0 =
       umma::smem_desc(c.sbase + L::kStageOffset, 16, 1024, umma::kSwizzle128B);
-  const uint64_t a_q0 = umma::smem_desc(c.sbase, 16, 1024, umma::kSwizzle128B);
   uint32_t g = 0, nq = 0;
   // time-out test hook: a wait that runs out, then the abort path
   if (p.test_stall && !wait_bar(c, kStall, 0, kTestStallNs)) return;
@@ -592,7 +578,7 @@ __device__ void mma_s(const Launch& p, const Ctx& c, uint32_t tmem, int n_units)
     const TcUnit x = tc_unit(p, u);
     const int n_sub = (x.t_end - x.t_begin + kT - 1) / kT;
     const int qb = nq & 1;
-    if (!wait_bar(c, kQReady0 + qb, (nq >> 1) & 1)) return;
+    if (!wait_bar(c, kQConv0 + qb, (nq >> 1) & 1)) return;  // Q in tensor memory
     fence_proxy_async();
     for (int i = 0; i < n_sub; ++i, ++g) {
       const int st = g % kStages;
@@ -602,18 +588,12 @@ __device__ void mma_s(const Launch& p, const Ctx& c, uint32_t tmem, int n_units)
       if (!wait_bar(c, kSFree0 + sb, ((g >> 1) & 1) ^ 1)) return;  // S(g-2) was read
       umma::fence_after_sync();
       const uint64_t b0 = b_k0 + (uint64_t)((st * kStageBytes) >> 4);
-      const uint64_t a0 = a_q0 + (uint64_t)((qb * kQBytes) >> 4);
 #pragma unroll
       for (int k = 0; k < kD / 16; ++k) {  // dims 16k .. 16k + 15
         const uint32_t off = (k / 4) * kRegion + (k % 4) * 32;
-        if constexpr (Q8) {  // A = Q in tensor memory (8 columns per 16 dims)
-          umma::mma_bf16_ta(tmem + kSCol + sb * kT, tmem + kQCol + qb * 64 + k * 8,
-                            b0 + (uint64_t)(off >> 4), kIdescS, k ? 1u : 0u);
-        } else {
-          const uint32_t offq = (k / 4) * kQRegion + (k % 4) * 32;
-          umma::mma_bf16(tmem + kSCol + sb * kT, a0 + (uint64_t)(offq >> 4),
-                         b0 + (uint64_t)(off >> 4), kIdescS, k ? 1u : 0u);
-        }
+        // A = Q in tensor memory (8 columns per 16 dims)
+        umma::mma_bf16_ta(tmem + kSCol + sb * kT, tmem + kQCol + qb * 64 + k * 8,
+                          b0 + (uint64_t)(off >> 4), kIdescS, k ? 1u : 0u);
       }
       umma::commit(bar_addr(c, kSFull0 + sb));
       if (i == n_sub - 1) umma::commit(bar_addr(c, kQFree0 + qb));
@@ -628,7 +608,7 @@ __device__ void mma_pv(const Launch& p, const Ctx& c, uint32_t tmem, int n_units
   constexpr bool Q8 = KT != 0;  // a quantized cache (E4M3 or NVFP4)
   using L = Lay<KT>;
   constexpr int kStages = L::kStages;
-  static_assert(kStages <= 4, "the four P slots cover the softmax's lead");
+  static_assert(kStages <= 7, "the eight P slots cover the softmax's lead");
   constexpr uint32_t kIdescO = idesc_o<Q8>();
   const uint64_t b_k0 =
       umma::smem_desc(c.sbase + L::kStageOffset, 16, 1024, umma::kSwizzle128B);
@@ -642,7 +622,7 @@ __device__ void mma_pv(const Launch& p, const Ctx& c, uint32_t tmem, int n_units
     const int n_sub = (x.t_end - x.t_begin + kT - 1) / kT;
     const int ob = nq & 1;
     for (int i = 0; i < n_sub; ++i, ++g) {
-      if (!wait_bar(c, kPFull0 + (g & 3), (g >> 2) & 1)) return;
+      if (!wait_bar(c, kPFull0 + (g & 7), (g >> 3) & 1)) return;
       if (i == 0 && !wait_bar(c, kOFree0 + ob, ((nq >> 1) & 1) ^ 1)) return;
       umma::fence_after_sync();
       const uint32_t st = (g % kStages) * kStageBytes;
@@ -652,7 +632,7 @@ __device__ void mma_pv(const Launch& p, const Ctx& c, uint32_t tmem, int n_units
       for (int kk = 0; kk < kT / 16; ++kk)
         umma::mma_bf16(tmem + kOCol + ob * kD, ap + (uint64_t)((kk * 32) >> 4),
                        bv + (uint64_t)((kk * 2048) >> 4), kIdescO, (i == 0 && kk == 0) ? 0u : 1u);
-      umma::commit(bar_addr(c, kPVDone0 + (g & 3)));
+      umma::commit(bar_addr(c, kPVDone0 + (g & 7)));
       umma::commit(bar_addr(c, kEmpty0 + (g % kStages)));
     }
     umma::commit(bar_addr(c, kODone0 + ob));  // the unit's O is complete
@@ -774,7 +754,7 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
       // rescale the row's O when its reference value moved; the previous P.V
       // must have landed first
       if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        if (!wait_w(kPVDone0 + ((g - 1) & 3), ((g - 1) >> 2) & 1)) return;
+        if (!wait_w(kPVDone0 + ((g - 1) & 7), ((g - 1) >> 3) & 1)) return;
         umma::fence_after_sync();
 #pragma unroll 1
         for (int ch = 0; ch < kD / 32; ++ch) {
@@ -802,7 +782,7 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
       }
       fence_proxy_async();
       umma::fence_before_sync();
-      arrive_w(kPFull0 + (g & 3));
+      arrive_w(kPFull0 + (g & 7));
     }
     // hand the rows' (m, l) to the epilogue warps once the epilogue of the
     // unit that used this O buffer before has read its own
@@ -953,15 +933,15 @@ __global__ void __launch_bounds__(Lay<KT>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t count = 1;  // tcgen05.commit or the producer's expect_tx arrive
-      if ((i >= kSFree0 && i < kSFree0 + 2) || (i >= kPFull0 && i < kPFull0 + 4) ||
+      if ((i >= kSFree0 && i < kSFree0 + 2) || (i >= kPFull0 && i < kPFull0 + 8) ||
           (i >= kEpiReady0 && i < kEpiReady0 + 2) || (i >= kOFree0 && i < kOFree0 + 2))
         count = 4;  // the four softmax (or, for kOFree, epilogue) warps
       if (i == kDrain) count = 2;  // the S and the P.V issuing threads
       // quantized cache: the four converter warps fill the operand stages, free
       // the raw stages and report each converted Q buffer
-      if (Q8 && ((i >= kFull0 && i < kFull0 + kMaxStages) ||
-                 (i >= kRawEmpty0 && i < kRawEmpty0 + kMaxStages) ||
-                 (i >= kQConv0 && i < kQConv0 + 2)))
+      if ((Q8 && ((i >= kFull0 && i < kFull0 + kMaxStages) ||
+                  (i >= kRawEmpty0 && i < kRawEmpty0 + kMaxRawStages))) ||
+          (i >= kQConv0 && i < kQConv0 + 2))
         count = 4;
       mbar_init(bar_addr(c, i), count);
     }
@@ -993,7 +973,7 @@ __global__ void __launch_bounds__(Lay<KT>::kThreads, 1)
       // this thread issued has completed
       umma::commit(bar_addr(c, kDrain));
     }
-  } else if constexpr (Q8) {
+  } else {
     converter<R, KT>(p, c, tmem, n_units, box != 0);
   }
   umma::fence_before_sync();
@@ -1141,12 +1121,8 @@ cudaError_t launch_split_gqa_tc(const Launch& p, int grid, cudaStream_t stream) 
   const cuuint64_t d2[2] = {row, (cuuint64_t)(r * heads)};
   const cuuint64_t s2[1] = {row * es};
   const cuuint32_t b2[2] = {bx, 1};
-  const cuuint64_t dq[2] = {(cuuint64_t)kD, (cuuint64_t)p.B * p.H_q};
-  const cuuint64_t sq[1] = {(cuuint64_t)kD * 2};
-  const cuuint32_t bq[2] = {64, (cuuint32_t)kQBoxRows};
   if (!encode(&m.k3, kb, 3, d3, s3, b3, q8) || !encode(&m.v3, vb, 3, d3, s3, b3, q8) ||
-      !encode(&m.k2, kb, 2, d2, s2, b2, q8) || !encode(&m.v2, vb, 2, d2, s2, b2, q8) ||
-      !encode(&m.q, p.q, 2, dq, sq, bq, false))
+      !encode(&m.k2, kb, 2, d2, s2, b2, q8) || !encode(&m.v2, vb, 2, d2, s2, b2, q8))
     return cudaErrorInvalidValue;
   if (kt == 2) {  // block scales [rows][H_kv * 8] bytes, after the codes
     const uint8_t* ks = static_cast<const uint8_t*>(kb) + r * heads * row;
