@@ -92,14 +92,15 @@ enum {
 // fills directly (192 KB in flight per SM: a stage stays busy from its copy,
 // ≈ 3–4k cycles to land, through its S, softmax and P.V).  Quantized: TMA
 // copies the cache bytes into raw stages (one producer warp) and the
-// converter warpgroup writes them, as f16, into three operand stages (the
-// MMAs then run on f16 operands, see the converter).  Seven E4M3 raw stages
-// keep 112 KB of the cache in flight per SM; eight NVFP4 stages keep 80 KB
-// (512 entries).
+// converter warpgroup writes them, as f16, into four operand stages (the
+// MMAs then run on f16 operands, see the converter).  Five E4M3 raw stages
+// keep 80 KB of the cache in flight per SM, six NVFP4 stages 72 KB; measured
+// against 3 operand + 7 (E4M3) / 8 (NVFP4) raw stages and 5 + 3 / 4, the
+// converter, which waits for a free operand stage, is held up least here.
 template <int KT>
 struct Lay {
   static constexpr bool Q8 = KT != 0;  // a quantized cache: the f16 converter path
-  static constexpr int kStages = Q8 ? 3 : 6;     // operand stages (K, V as 16-bit)
+  static constexpr int kStages = Q8 ? 4 : 6;     // operand stages (K, V as 16-bit)
   // Raw stage: E4M3 -- K rows, then V rows, 128 bytes each (16 KB); NVFP4 --
   // K codes, V codes (64 bytes a row), then K and V block scales (16 bytes a
   // row: the scale rows of two neighbouring heads, copied together) in 2 KB
@@ -110,7 +111,7 @@ struct Lay {
   static constexpr int kRawScaleBytes = KT == 2 ? (kT / 4) * 128 : 0;    // K (or V) scales
   static constexpr int kRawStageBytes = 2 * kRawCodeBytes + 2 * kRawScaleBytes;
   static constexpr int kRawTxBytes = 2 * kRawCodeBytes + (KT == 2 ? 2 * kT * 16 : 0);  // copied
-  static constexpr int kRawStages = KT == 2 ? 8 : Q8 ? 7 : 0;
+  static constexpr int kRawStages = KT == 2 ? 6 : Q8 ? 5 : 0;
   static constexpr int kStageOffset = 0;
   static constexpr int kRawOffset = kStageOffset + kStages * kStageBytes;
   static constexpr int kBarOffset = kRawOffset + kRawStages * kRawStageBytes;
@@ -424,8 +425,8 @@ __device__ void producer(const Launch& p, const Ctx& c, const Maps& m, int n_uni
 // past the group are zeros; then the MMA thread is told (kQConv).  The Q of
 // the next unit is written while the current one runs.  Quantized cache
 // only: per tile, once its bytes are in raw stage
-// g % kRawStages and operand stage g % 3 is free (the PV three tiles back
-// completed), K and V are written as f16 into the operand stage (NVFP4: each
+// g % kRawStages and operand stage g % kStages is free (the PV kStages
+// tiles back completed), K and V are written as f16 into the operand stage (NVFP4: each
 // code times its block scale, multiplied in f16) in the 128-byte-swizzled
 // K-major layout the tensor core reads -- eight lanes per row, so every load
 // reads four whole rows, and lanes jj and
