@@ -29,16 +29,17 @@
 // more than 2^8), after the PV before it has landed.  The producer prefetches
 // the next tile's rows into L2 while the current stage is in use.
 //
-// Roles inside a CTA (320 threads):
+// Roles inside a CTA (320 threads; 448 with the E4M3 converter):
 //   warps 0-3  softmax: thread i owns head i = TMEM lane i.  It loads its row
 //              of Q dims 0..255 into TMEM at the start of a unit, reads its
 //              row of S, keeps the running max and sum in fp32, writes P
 //              (bf16) into the stage and writes its row of the result.
-//   warps 4-7  producer: looks up each entry's cache row and has the TMA unit
-//              gather the 1152-byte latent rows four at a time
-//              (tile::gather4, 64 dims x 4 rows per copy) into the
+//   warps 4-7  producer: looks up each entry's cache row and copies the
+//              1152-byte latent rows with 16-byte cp.async runs into the
 //              128-byte-swizzled K-major layout the tensor core reads; the
-//              unit's Q dims 256..575 come by TMA tile copies at its start.
+//              unit's Q dims 256..575 come by TMA tile copies, issued after
+//              the unit's first tile (whose index words were loaded during
+//              the previous unit) and once the previous unit's S is done.
 //   warp 8     S MMA issue (one thread) and TMEM allocation.
 //   warp 9     P.V MMA issue (one thread).
 //   warps 10-13  E4M3 cache only: the converter (below).
@@ -313,64 +314,66 @@ __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
                                        : reinterpret_cast<const uint8_t*>(p.k);
   const uint8_t* kextra = reinterpret_cast<const uint8_t*>(p.extra_k);
   const int q_boxes = (min(p.H_q, kHeads) + kQBoxRows - 1) / kQBoxRows;  // per region
-  for (int u = blockIdx.x; u < n_units && alive; u = next_unit(u)) {
-    const MlaUnit x = mla_unit(p, u);
-    if (x.empty) continue;
-    // Q dims 256..575 of row b into shared memory once the previous unit's S
-    // MMAs are done: q_boxes 16-row boxes per 64-dim region, spread over the
-    // four warps (rows past H_q belong to other rows or read as zeros; those
-    // heads' results are never written).  E4M3 cache: the softmax warps
-    // then rescale them into f16 in place.
-    if (!wait_w(kQFree, (n_ne & 1) ^ 1)) break;
-    if (pt == 0) mbar_arrive_expect_tx(bar_addr(c, kQFull), kQSRegions * q_boxes * kQBoxRows * 128);
-    __syncwarp();
-    for (int i = pt; i < kQSRegions * q_boxes; i += 128) {
-      const int j = i / q_boxes, rb = i % q_boxes;
-      tma_tile(c.sbase + j * (kHeads * 128) + rb * (kQBoxRows * 128), c.tm_q, kQT + 64 * j,
-               x.b * p.H_q + rb * kQBoxRows, bar_addr(c, kQFull));
+  // Lane e < 16 of producer warp pw handles entry 16*pw + e of a tile.
+  // Table words are loaded two tiles ahead and decoded one tile ahead (the
+  // decoded rows of the next tile are prefetched into L2), so the index
+  // load's latency stays off the copy path; a unit's first two tiles' words
+  // are loaded during the previous unit's last tile.
+  // src: 0 = main cache, 1 = second source.  Masked entries (past the end
+  // of the split) and bad indices read row 0 of the main cache, so every
+  // stage byte holds real data; masked scores are dropped by the softmax.
+  const int e_lane = kEntPerWarp * pw + pl;
+  auto fetch = [&](const MlaUnit& xu, int t0) -> int {
+    const int tok = t0 + e_lane;
+    return (pl < kEntPerWarp && tok < xu.t_end) ? latent_fetch(p, xu.b, tok, xu.l_main) : 0;
+  };
+  auto decode = [&](const MlaUnit& xu, int t0, int word, int& row, int& src, bool& live) {
+    row = 0;
+    src = 0;
+    live = false;
+    const int tok = t0 + e_lane;
+    if (pl < kEntPerWarp && tok < xu.t_end) {
+      long long r;
+      int sr;
+      const bool good = latent_decode(p, xu.b, tok, xu.l_main, word, &r, &sr);
+      bad |= !good;
+      if (good) {
+        row = (int)r;
+        src = sr;
+        live = true;
+      }
     }
+  };
+  // the next unit with tiles at or after u
+  auto next_live = [&](int u) -> int {
+    while (u < n_units && mla_unit(p, u).empty) u = next_unit(u);
+    return u;
+  };
+  uint32_t nq_issued = 0;  // units whose Q copy was issued
+  int u = next_live(blockIdx.x);
+  MlaUnit x = mla_unit(p, u < n_units ? u : 0);
+  int pre_w0 = 0, pre_w1 = 0;  // the unit's first two tiles' words
+  if (u < n_units) {
+    pre_w0 = fetch(x, x.t_begin);
+    pre_w1 = (x.t_begin + kSub < x.t_end) ? fetch(x, x.t_begin + kSub) : 0;
+  }
+  while (u < n_units && alive) {
+    const int un = next_live(next_unit(u));
+    const bool has_next = un < n_units;
+    const MlaUnit xn = has_next ? mla_unit(p, un) : x;
     // warm L2 with the next unit's query rows (its softmax warps load them
     // into tensor memory at its start)
-    if (next_unit(u) < n_units) {
-      const MlaUnit nx = mla_unit(p, next_unit(u));
-      const char* qn = reinterpret_cast<const char*>(p.q + (size_t)nx.b * p.H_q * kDqk);
+    if (has_next) {
+      const char* qn = reinterpret_cast<const char*>(p.q + (size_t)xn.b * p.H_q * kDqk);
       const int lines = min(p.H_q, kHeads) * kDqk * 2 / 128;
       for (int i = pt; i < lines; i += 128)
         asm volatile("prefetch.global.L2 [%0];" ::"l"(qn + (size_t)i * 128));
     }
-    // Lane e < 16 of producer warp pw handles entry 16*pw + e of a tile.
-    // Table words are loaded two tiles ahead and decoded one tile ahead (the
-    // decoded rows of the next tile are prefetched into L2), so the index
-    // load's latency stays off the copy path.
-    // src: 0 = main cache, 1 = second source.  Masked entries (past the end
-    // of the split) and bad indices read row 0 of the main cache, so every
-    // stage byte holds real data; masked scores are dropped by the softmax.
-    const int e_lane = kEntPerWarp * pw + pl;
-    auto fetch = [&](int t0) -> int {
-      const int tok = t0 + e_lane;
-      return (pl < kEntPerWarp && tok < x.t_end) ? latent_fetch(p, x.b, tok, x.l_main) : 0;
-    };
-    auto decode = [&](int t0, int word, int& row, int& src, bool& live) {
-      row = 0;
-      src = 0;
-      live = false;
-      const int tok = t0 + e_lane;
-      if (pl < kEntPerWarp && tok < x.t_end) {
-        long long r;
-        int sr;
-        const bool good = latent_decode(p, x.b, tok, x.l_main, word, &r, &sr);
-        bad |= !good;
-        if (good) {
-          row = (int)r;
-          src = sr;
-          live = true;
-        }
-      }
-    };
     int my_row, my_src, nx_row = 0, nx_src = 0;
     bool my_live, nx_live = false;
-    int nx_word = (x.t_begin + kSub < x.t_end) ? fetch(x.t_begin + kSub) : 0;
-    decode(x.t_begin, fetch(x.t_begin), my_row, my_src, my_live);
+    int nx_word = pre_w1;
+    decode(x, x.t_begin, pre_w0, my_row, my_src, my_live);
+    bool pre_fetched = false;  // the next unit's first words are loaded
     for (int t0 = x.t_begin; t0 < x.t_end; t0 += kSub, ++g) {
       const int stage = g % kStages;
       if (!wait_w(kEmpty0 + stage, ((g / kStages) & 1) ^ 1)) {
@@ -399,10 +402,48 @@ __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
         cp_async16(dst, rows_s[rr] + q * 16);
       }
       cp_async_mbar_arrive(full);
+      // Q dims 256..575 of row b into shared memory once the previous
+      // unit's S MMAs are done (after this unit's first tile is on its way):
+      // q_boxes 16-row boxes per 64-dim region, spread over the four warps
+      // (rows past H_q belong to other rows or read as zeros; those heads'
+      // results are never written).  E4M3 cache: the softmax warps then
+      // rescale them into f16 in place.
+      if (t0 == x.t_begin) {
+        if (!wait_w(kQFree, (n_ne & 1) ^ 1)) {
+          alive = false;
+          break;
+        }
+        if (pt == 0)
+          mbar_arrive_expect_tx(bar_addr(c, kQFull), kQSRegions * q_boxes * kQBoxRows * 128);
+        __syncwarp();
+        for (int i = pt; i < kQSRegions * q_boxes; i += 128) {
+          const int j = i / q_boxes, rb = i % q_boxes;
+          tma_tile(c.sbase + j * (kHeads * 128) + rb * (kQBoxRows * 128), c.tm_q, kQT + 64 * j,
+                   x.b * p.H_q + rb * kQBoxRows, bar_addr(c, kQFull));
+        }
+        ++nq_issued;
+      }
       // decode the next tile's words (loaded an iteration ago), load the
       // words of the tile after it, and start the next tile's rows towards L2
-      if (t0 + kSub < x.t_end) decode(t0 + kSub, nx_word, nx_row, nx_src, nx_live);
-      if (t0 + 2 * kSub < x.t_end) nx_word = fetch(t0 + 2 * kSub);
+      if (t0 + kSub < x.t_end) decode(x, t0 + kSub, nx_word, nx_row, nx_src, nx_live);
+      if (t0 + 2 * kSub < x.t_end) nx_word = fetch(x, t0 + 2 * kSub);
+      // the next unit: its first two tiles' words during this unit's
+      // second-to-last tile (or its only one), its first tile's rows towards
+      // L2 during the last
+      if (has_next && t0 + kSub >= x.t_end && pre_fetched) {
+        int r0, s0;
+        bool l0;
+        decode(xn, xn.t_begin, pre_w0, r0, s0, l0);
+        if (l0)
+          prefetch_l2(reinterpret_cast<const uint8_t*>(s0 ? p.extra_k : p.k) +
+                          (size_t)r0 * kRowBytes,
+                      kRowBytes);
+      }
+      if (has_next && t0 + 2 * kSub >= x.t_end && !pre_fetched) {
+        pre_w0 = fetch(xn, xn.t_begin);
+        pre_w1 = (xn.t_begin + kSub < xn.t_end) ? fetch(xn, xn.t_begin + kSub) : 0;
+        pre_fetched = true;
+      }
       if (nx_live && t0 + kSub < x.t_end)
         prefetch_l2(reinterpret_cast<const uint8_t*>(nx_src ? p.extra_k : p.k) +
                         (size_t)nx_row * kRowBytes,
@@ -411,13 +452,16 @@ __device__ void producer(const Launch& p, const Ctx& c, int n_units) {
       my_src = nx_src;
       my_live = nx_live;
     }
+    if (!alive) break;
     ++n_ne;
+    u = un;
+    x = xn;
   }
   if (bad) set_error(p.hdr, DA_DEVERR_INDEX);
   // leave no copy in flight into this CTA's shared memory (on the normal path
   // every stage was consumed and these waits return at once)
   cp_async_wait_all();
-  if (pt == 0 && n_ne > 0 && !mbar_wait(bar_addr(c, kQFull), (n_ne - 1) & 1))
+  if (pt == 0 && nq_issued > 0 && !mbar_wait(bar_addr(c, kQFull), (nq_issued - 1) & 1))
     set_error(p.hdr, DA_DEVERR_TIMEOUT);
 }
 
