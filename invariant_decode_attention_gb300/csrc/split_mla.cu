@@ -584,9 +584,26 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
   // 256..575 rescaled in place in the shared-memory Q regions once their TMA
   // copy (kQFull, phase parity `qpar`) has landed; `e` gets the exponent (0
   // for a bf16 cache).  False when a bounded wait ran out.
+  // 32-byte loads when q allows them (a row's 1152 bytes keep the alignment):
+  // each load instruction touches as many rows as a 16-byte one, for twice
+  // the bytes
+  const bool q32 = (reinterpret_cast<uintptr_t>(p.q) & 31) == 0;
   auto load_q = [&](int b, uint32_t qpar, int& e) -> bool {
     const bool ok = row < p.H_q;
     const uint4* qrow = reinterpret_cast<const uint4*>(p.q + ((size_t)b * p.H_q + row) * kDqk);
+    // dims 128 half .. 128 half + 127 of the row (zeros past the heads)
+    auto load_half = [&](int half, uint4 (&w)[16]) {
+      if (!ok) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = make_uint4(0, 0, 0, 0);
+      } else if (q32) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ldg_v8(qrow + half * 16 + 2 * i, w[2 * i], w[2 * i + 1]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = __ldg(qrow + half * 16 + i);
+      }
+    };
     e = 0;
     if constexpr (KT == 1) {
       if (!wait_w(kQFull, qpar)) return false;
@@ -599,9 +616,7 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
         uint4 w[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          w[i] = ok ? __ldg(qrow + half * 16 + i) : make_uint4(0, 0, 0, 0);
+        load_half(half, w);
 #pragma unroll
         for (int ch = 0; ch < 2; ++ch) {
           uint32_t r32[32];
@@ -654,9 +669,7 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
         uint4 w[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          w[i] = ok ? __ldg(qrow + half * 16 + i) : make_uint4(0, 0, 0, 0);
+        load_half(half, w);
 #pragma unroll
         for (int ch = 0; ch < 2; ++ch) {
           uint32_t r32[32];

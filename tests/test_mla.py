@@ -145,6 +145,26 @@ def test_mla_row_solo_vs_batch(api):
 
 
 @gpu
+@pytest.mark.parametrize("fp8", [False, True])
+def test_mla_q_alignment_does_not_change_bits(api, fp8):
+    """q 32-byte aligned (32-byte row loads) or only 16-byte aligned (16-byte
+    loads): the same bits."""
+    wl = W.make(W.INDEXED, [300, 1500, 2048], H_q=128, H_kv=1, D_qk=576, D_v=512, latent=True,
+                num_slots=4000, width=2048, seed=45)
+    if fp8:
+        wl = W.quantize_fp8(wl)
+    g = wl.to("cuda")
+    o32, l32 = [t.clone() for t in api.run_workload(g)]
+    assert g.q.data_ptr() % 32 == 0
+    store = torch.empty(g.q.numel() + 16, dtype=torch.bfloat16, device="cuda")
+    q16 = store[8:8 + g.q.numel()].view_as(g.q)
+    q16.copy_(g.q)
+    assert q16.data_ptr() % 32 == 16
+    o16, l16 = api.run_workload(dataclasses.replace(g, q=q16))
+    assert torch.equal(o16, o32) and torch.equal(l16, l32)
+
+
+@gpu
 @pytest.mark.parametrize("name", ["mla_sparse", "mla_sparse_extra"])
 def test_mla_repeated_runs_bitwise(api, name):
     """The same inputs give the same bits on every run, one workspace reused
