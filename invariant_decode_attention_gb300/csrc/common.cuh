@@ -250,15 +250,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
-// 32 bytes from global memory (read-only path) as two 16-byte halves; the
-// address is 32-byte aligned.
-__device__ __forceinline__ void ldg_v8(const void* src, uint4& lo, uint4& hi) {
-  asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-               : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y),
-                 "=r"(hi.z), "=r"(hi.w)
-               : "l"(src));
-}
-
 // Arrive on the mbarrier at shared address `bar` once every cp.async this
 // thread has issued so far has landed.  The arrival is not added to the
 // barrier's pending count: its initial count includes it.

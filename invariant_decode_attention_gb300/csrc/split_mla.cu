@@ -168,6 +168,15 @@ __device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap* tm, in
       : "memory");
 }
 
+// 32 bytes from global memory (read-only path) as two 16-byte halves; the
+// address is 32-byte aligned.
+__device__ __forceinline__ void ldg_v8(const void* src, uint4& lo, uint4& hi) {
+  asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y),
+                 "=r"(hi.z), "=r"(hi.w)
+               : "l"(src));
+}
+
 // Start pulling `bytes` (a multiple of 16) at a 16-byte-aligned address into L2.
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
