@@ -1,12 +1,14 @@
 // C ABI of the decode attention library: argument checks, workspace layout,
 // plan construction and kernel launches.  Allocates nothing; synchronises the
 // host only in the two documented read-back calls.
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
 
 #include "common.cuh"
+#include "merge.cuh"
 
 namespace da {
 bool mla_supported(int H_q);
@@ -166,6 +168,20 @@ Launch make_launch(const da_plan* plan) {
                                                 : pr.num_blocks;
   }
   return L;
+}
+
+// The most splits any row of `plan` can have: under INVARIANT a row of L
+// entries has ceil(tiles / tps) splits with tps >= min_tiles_per_split and
+// tiles <= ceil(capacity / tile), so n <= ceil(that / min_tiles_per_split);
+// BALANCED may cut any row into max_splits.
+int split_bound(const da_plan* plan) {
+  if (plan->policy != DA_POLICY_INVARIANT) return plan->max_splits;
+  const da_problem& pr = plan->prob;
+  long long cap = row_capacity(pr.layout, pr.width, pr.page_size);
+  if (plan->has_extra) cap += pr.extra_width;
+  const long long tiles = (cap + plan->tile_tokens - 1) / plan->tile_tokens;
+  const long long n = (tiles + plan->min_tiles_per_split - 1) / plan->min_tiles_per_split;
+  return (int)std::min<long long>(std::max<long long>(n, 1), plan->max_splits);
 }
 
 int check_plan(const da_plan* plan) {
@@ -406,8 +422,9 @@ int decode_attn_combine(const da_plan* plan, void* out, float* lse, void* stream
   Launch L = make_launch(plan);
   L.out = static_cast<__nv_bfloat16*>(out);
   L.lse = lse;
-  return launch_combine(L, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DA_OK
-                                                                               : DA_ERR_CUDA;
+  return launch_combine(L, split_bound(plan), static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? DA_OK
+             : DA_ERR_CUDA;
 }
 
 int decode_attn_forward(const da_problem* prob, int32_t policy, const void* q, const void* k,

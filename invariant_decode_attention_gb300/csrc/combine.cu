@@ -5,11 +5,13 @@
 // so the addends and their order are the same in any batch.
 //
 // One CTA per (row, head): every thread owns up to four value dims (d,
-// d + 128, ...).  It loads its values of a batch of kBatch splits first (all
-// those loads in flight at once: a row of 64 splits costs four round trips to
-// L2, not 64; the first batch is issued before warp 0 forms the weights),
-// then advances its FMA chains through the batch; each chain runs in split
-// order from zero, as merge.cuh states.
+// d + 128, ...).  It loads its values of a batch of NB splits first (all
+// those loads in flight at once; the first batch is issued before warp 0
+// forms the weights), then advances its FMA chains through the batch; each
+// chain runs in split order from zero, as merge.cuh states.  NB is the
+// bound on any row's split count that the plan implies (16 or 64 for one
+// value dim per thread), so a row costs one round trip to L2 without holding
+// registers for splits no row can have.
 #include "common.cuh"
 #include "merge.cuh"
 
@@ -18,12 +20,12 @@ namespace {
 
 constexpr int kCombineThreads = 128;
 constexpr int kMaxDimsPerThread = 4;  // D_v <= 512
-constexpr int kBatch = 16;            // splits whose loads are issued together
 constexpr int kMaxSplitsAny = kFmaMaxSplits > kMlaMaxSplits ? kFmaMaxSplits : kMlaMaxSplits;
 static_assert(kMaxSplitsAny <= 64, "two split weights per lane of warp 0");
 
-// DPT: value dims per thread (1 when D_v <= 128, else up to 4).
-template <int DPT>
+// DPT: value dims per thread (1 when D_v <= 128, else up to 4); NB: splits
+// whose loads are issued together.
+template <int DPT, int NB>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Launch p) {
   __shared__ float coef[kMaxSplitsAny];
   __shared__ float lse_out;
@@ -36,10 +38,10 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Launch p) {
   const size_t stride = (size_t)p.H_q * Dv;
   const float* o0 = p.o_part + (slot0 * p.H_q + j) * (size_t)Dv + threadIdx.x;
   const int nk = (Dv - (int)threadIdx.x + kCombineThreads - 1) / kCombineThreads;  // own dims
-  float v[kBatch][DPT];
+  float v[NB][DPT];
   auto load = [&](int s0) {
 #pragma unroll
-    for (int i = 0; i < kBatch; ++i)
+    for (int i = 0; i < NB; ++i)
 #pragma unroll
       for (int k = 0; k < DPT; ++k)
         v[i][k] = (s0 + i < n && k < nk)
@@ -55,10 +57,10 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Launch p) {
   float acc[DPT];
 #pragma unroll
   for (int k = 0; k < DPT; ++k) acc[k] = 0.f;
-  for (int s0 = 0; s0 < n; s0 += kBatch) {
+  for (int s0 = 0; s0 < n; s0 += NB) {
     if (s0 > 0) load(s0);
 #pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
+    for (int i = 0; i < NB; ++i) {
       if (s0 + i < n) {
         const float c = coef[s0 + i];
 #pragma unroll
@@ -77,102 +79,120 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Launch p) {
 // The tensor-core variant's partials are head-interleaved: value dims in
 // groups of four, heads innermost -- element (slot, head j, dim d) at
 // ((slot * 128 + d / 4) * H_q + j) * 4 + d % 4 -- so that its epilogue's
-// stores coalesce.  Its combine takes one CTA per (row, value half, 32 dims)
-// and one thread per head: each thread forms its head's weights alone with
-// the same operations in the same order as merge_weights (its weights sit in
-// a shared-memory column; the split LSEs are loaded together), and its loads
-// of a split's 4-dim group coalesce across the heads.  The loads of two
-// splits are issued before their FMAs, the first two before the weights are
-// formed.
-constexpr int kMlaGroupsPerCta = 8;  // 4-dim groups: 32 value dims
-constexpr int kMlaBatch = 2;         // splits whose loads are issued together
+// stores coalesce.  Its combine takes one thread per (row, head, two 4-dim
+// groups): a warp's load of one split's group covers 32 consecutive heads
+// (512 contiguous bytes).  Every thread forms its head's weights itself with
+// the operations and order of merge_weights (its LSEs staged in its own
+// shared-memory column), and the loads of a whole batch of splits, together
+// with the split LSEs, are in flight at once: a row with up to kMlaBatch
+// splits costs one round trip to L2.
+constexpr int kMlaThreads = 256;
+constexpr int kMlaGroupsPerThread = 2;  // 4-dim groups: 8 value dims
+constexpr int kMlaGroupsPerCta = (kMlaThreads / 128) * kMlaGroupsPerThread;
+constexpr int kMlaBatch = 4;  // splits whose loads are issued together
 
-__global__ void __launch_bounds__(kCombineThreads) combine_mla_kernel(Launch p) {
+__global__ void __launch_bounds__(kMlaThreads) combine_mla_kernel(Launch p) {
+  __shared__ float col[kMlaMaxSplits][kMlaThreads];  // thread t's column: its LSEs, then weights
   wait_prior_grid();  // the split kernel's partials
-  constexpr int kBlocksPerRow = 512 / 4 / kMlaGroupsPerCta;  // 16
-  const int b = blockIdx.x / kBlocksPerRow, cb = blockIdx.x % kBlocksPerRow;
+  constexpr int kCtasPerRow = 512 / 4 / kMlaGroupsPerCta;
+  const int b = blockIdx.x / kCtasPerRow, cb = blockIdx.x % kCtasPerRow;
   const int n = p.n_splits[b];
-  const int j = threadIdx.x;
+  const int t = threadIdx.x, j = t & 127;
   if (n <= 1 || j >= p.H_q) return;
+  const int g0 = cb * kMlaGroupsPerCta + (t >> 7) * kMlaGroupsPerThread;
   const size_t slot0 = (size_t)b * p.max_splits;
-  __shared__ float coef_s[kMlaMaxSplits][kCombineThreads];
-  const float4* base = reinterpret_cast<const float4*>(p.o_part) +
-                       (slot0 * 128 + cb * kMlaGroupsPerCta) * p.H_q + j;
-  float4 v[kMlaBatch][kMlaGroupsPerCta];
+  const size_t split_stride = (size_t)128 * p.H_q;  // float4s per split
+  const float4* base = reinterpret_cast<const float4*>(p.o_part) + (slot0 * 128 + g0) * p.H_q + j;
+  float4 v[kMlaBatch][kMlaGroupsPerThread];
   auto load = [&](int s0) {
 #pragma unroll
-    for (int i = 0; i < kMlaBatch; ++i) {
-      const float4* src = base + (size_t)(s0 + i) * 128 * p.H_q;
+    for (int i = 0; i < kMlaBatch; ++i)
 #pragma unroll
-      for (int gi = 0; gi < kMlaGroupsPerCta; ++gi)
-        v[i][gi] = (s0 + i < n) ? __ldcg(src + gi * p.H_q) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+      for (int e = 0; e < kMlaGroupsPerThread; ++e)
+        v[i][e] = (s0 + i < n) ? __ldcg(base + (size_t)(s0 + i) * split_stride + e * p.H_q)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
   };
-  load(0);  // in flight while the weights are formed
-  // the split LSEs, all loads issued together
-  float ls[kMlaMaxSplits];
-#pragma unroll
-  for (int s = 0; s < kMlaMaxSplits; ++s)
-    ls[s] = (s < n) ? __ldcg(p.lse_part + (slot0 + s) * p.H_q + j) : -INFINITY;
+  load(0);  // in flight with the LSE loads
+  // weights: M = max of the split LSEs, w_s = 2^(lse_s - M), W = sum in
+  // split order, coefficient w_s / W (merge_weights' arithmetic)
+  const float* lse = p.lse_part + slot0 * p.H_q + j;
   float M = -INFINITY;
+  for (int s0 = 0; s0 < n; s0 += 8) {
+    float ls[8];
 #pragma unroll
-  for (int s = 0; s < kMlaMaxSplits; ++s) M = fmaxf(M, ls[s]);
-  float W = 0.f;
+    for (int i = 0; i < 8; ++i) ls[i] = (s0 + i < n) ? __ldcg(lse + (size_t)(s0 + i) * p.H_q) : -INFINITY;
 #pragma unroll
-  for (int s = 0; s < kMlaMaxSplits; ++s) {
-    if (s < n) {
-      coef_s[s][j] = (M == -INFINITY) ? 0.f : ex2(ls[s] - M);
-      W += coef_s[s][j];
+    for (int i = 0; i < 8; ++i) {
+      if (s0 + i < n) col[s0 + i][t] = ls[i];
+      M = fmaxf(M, ls[i]);
     }
   }
-  for (int s = 0; s < n; ++s) coef_s[s][j] = (W > 0.f) ? coef_s[s][j] / W : 0.f;
-  float4 acc[kMlaGroupsPerCta];
+  float W = 0.f;
+  for (int s = 0; s < n; ++s) {
+    const float w = (M == -INFINITY) ? 0.f : ex2(col[s][t] - M);
+    col[s][t] = w;
+    W += w;
+  }
+  for (int s = 0; s < n; ++s) col[s][t] = (W > 0.f) ? col[s][t] / W : 0.f;
+  float4 acc[kMlaGroupsPerThread];
 #pragma unroll
-  for (int gi = 0; gi < kMlaGroupsPerCta; ++gi) acc[gi] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int e = 0; e < kMlaGroupsPerThread; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int s0 = 0; s0 < n; s0 += kMlaBatch) {
     if (s0 > 0) load(s0);
 #pragma unroll
     for (int i = 0; i < kMlaBatch; ++i) {
       if (s0 + i < n) {
-        const float c = coef_s[s0 + i][j];
+        const float c = col[s0 + i][t];
 #pragma unroll
-        for (int gi = 0; gi < kMlaGroupsPerCta; ++gi) {
-          acc[gi].x = fmaf(c, v[i][gi].x, acc[gi].x);
-          acc[gi].y = fmaf(c, v[i][gi].y, acc[gi].y);
-          acc[gi].z = fmaf(c, v[i][gi].z, acc[gi].z);
-          acc[gi].w = fmaf(c, v[i][gi].w, acc[gi].w);
+        for (int e = 0; e < kMlaGroupsPerThread; ++e) {
+          acc[e].x = fmaf(c, v[i][e].x, acc[e].x);
+          acc[e].y = fmaf(c, v[i][e].y, acc[e].y);
+          acc[e].z = fmaf(c, v[i][e].z, acc[e].z);
+          acc[e].w = fmaf(c, v[i][e].w, acc[e].w);
         }
       }
     }
   }
-  __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(
-      p.out + ((size_t)b * p.H_q + j) * 512 + cb * kMlaGroupsPerCta * 4);
+  uint32_t w[2 * kMlaGroupsPerThread];
 #pragma unroll
-  for (int gi = 0; gi < kMlaGroupsPerCta; ++gi) {
-    dst[2 * gi] = __floats2bfloat162_rn(acc[gi].x, acc[gi].y);
-    dst[2 * gi + 1] = __floats2bfloat162_rn(acc[gi].z, acc[gi].w);
+  for (int e = 0; e < kMlaGroupsPerThread; ++e) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[e].x, acc[e].y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[e].z, acc[e].w);
+    w[2 * e] = *reinterpret_cast<const uint32_t*>(&lo);
+    w[2 * e + 1] = *reinterpret_cast<const uint32_t*>(&hi);
   }
-  if (cb == 0) p.lse[(size_t)b * p.H_q + j] = (W > 0.f) ? (M + lg2(W)) * kLn2 : -INFINITY;
+  static_assert(kMlaGroupsPerThread == 2, "one 16-byte store of 8 value dims");
+  *reinterpret_cast<uint4*>(p.out + ((size_t)b * p.H_q + j) * 512 + g0 * 4) =
+      make_uint4(w[0], w[1], w[2], w[3]);
+  if (cb == 0 && t < 128) p.lse[(size_t)b * p.H_q + j] = (W > 0.f) ? (M + lg2(W)) * kLn2 : -INFINITY;
 }
 
 }  // namespace
 
-cudaError_t launch_combine(const Launch& p, cudaStream_t stream) {
+cudaError_t launch_combine(const Launch& p, int n_bound, cudaStream_t stream) {
   if (p.o_part_mla) {
-    if (p.D_v != 512 || p.H_q > kCombineThreads) return cudaErrorInvalidValue;
+    if (p.D_v != 512 || p.H_q > 128) return cudaErrorInvalidValue;
     const long long blocks = (long long)p.B * (512 / 4 / kMlaGroupsPerCta);
     if (blocks == 0) return cudaSuccess;
-    return launch_after(combine_mla_kernel, dim3((unsigned)blocks), dim3(kCombineThreads), 0,
-                        stream, p);
+    return launch_after(combine_mla_kernel, dim3((unsigned)blocks), dim3(kMlaThreads), 0, stream,
+                        p);
   }
   if (p.D_v > kCombineThreads * kMaxDimsPerThread) return cudaErrorInvalidValue;
   const long long blocks = (long long)p.B * p.H_q;
   if (blocks == 0) return cudaSuccess;
-  if (p.D_v <= kCombineThreads)
-    return launch_after(combine_kernel<1>, dim3((unsigned)blocks), dim3(kCombineThreads), 0,
+  if (p.D_v <= kCombineThreads) {
+    if (n_bound <= 16)
+      return launch_after(combine_kernel<1, 16>, dim3((unsigned)blocks), dim3(kCombineThreads), 0,
+                          stream, p);
+    return launch_after(combine_kernel<1, 64>, dim3((unsigned)blocks), dim3(kCombineThreads), 0,
                         stream, p);
-  return launch_after(combine_kernel<kMaxDimsPerThread>, dim3((unsigned)blocks),
+  }
+  return launch_after(combine_kernel<kMaxDimsPerThread, 16>, dim3((unsigned)blocks),
                       dim3(kCombineThreads), 0, stream, p);
+}
+
+cudaError_t launch_combine(const Launch& p, cudaStream_t stream) {
+  return launch_combine(p, p.max_splits, stream);
 }
 
 }  // namespace da

@@ -50,4 +50,9 @@ __device__ __forceinline__ float merge_weights(const float* lse, size_t stride, 
   return (W > 0.f) ? (M + lg2(W)) * kLn2 : -INFINITY;
 }
 
+// The combine launch for partials whose rows have at most n_bound splits
+// each (a bound the plan implies: its kernel then keeps no registers for
+// splits beyond it).
+cudaError_t launch_combine(const Launch& p, int n_bound, cudaStream_t stream);
+
 }  // namespace da

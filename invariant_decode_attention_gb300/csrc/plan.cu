@@ -135,14 +135,21 @@ __global__ void __launch_bounds__(kPlanThreads) plan_invariant_kernel(PlanLaunch
     if (threadIdx.x == 0) p.hdr[kHdrNWork] = total;
   }
   __syncthreads();
-  // pass 2: place every item in its bucket (order within a bucket is free)
+  // pass 2: place every item in its bucket (order within a bucket is free).
+  // All splits of a row but the last have tps tiles, so a row takes n - 1
+  // consecutive places of that key with one atomic and its last split one
+  // place of its own key; the stores then need no further atomics.
   for (int b = threadIdx.x; b < p.B; b += kPlanThreads) {
     const RowSplits r = (b == (int)threadIdx.x) ? mine
                                                 : invariant_splits(p, row_length_quiet(p, b));
+    const int last0 = (r.n - 1) * r.tps;  // first tile of the last split
+    const int pos_full = (r.n > 1) ? atomicAdd(&bucket[sort_key(r.tps)], r.n - 1) : 0;
+    const int pos_last = atomicAdd(&bucket[sort_key(r.n_tiles - last0)], 1);
     for (int s = 0; s < r.n; ++s) {
       const int slot = b * p.max_splits + s;
-      const int t0 = min(s * r.tps, r.n_tiles), t1 = min((s + 1) * r.tps, r.n_tiles);
-      const int pos = atomicAdd(&bucket[sort_key(t1 - t0)], 1);
+      const bool is_last = s == r.n - 1;
+      const int pos = is_last ? pos_last : pos_full + s;
+      const int t0 = s * r.tps, t1 = is_last ? r.n_tiles : t0 + r.tps;
       p.work[pos] = slot;
       reinterpret_cast<int4*>(p.item_desc)[pos] = make_int4(r.n == 1 ? ~slot : slot, t0, t1, r.len);
     }

@@ -615,13 +615,13 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
     };
     e = 0;
     if constexpr (KT == 1) {
-      if (!wait_w(kQFull, qpar)) return false;
       // (the loops stay rolled: this runs once per unit, and its code is
       // fetched cold each time)
       uint8_t* qs = c.smem + row * 128;  // + region j * kHeads * 128 + swizzled chunk
       uint32_t mb = 0;                   // magnitude bits, see bf16x8_absmax_bits
       // dims 0..255: into TMEM as bf16 pairs (as for a bf16 cache) while
-      // taking the maximum; rescaled there below
+      // taking the maximum (the TMA copy of dims 256..575 lands meanwhile);
+      // rescaled there below
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
         uint4 w[16];
@@ -641,6 +641,7 @@ __device__ void softmax_warps(const Launch& p, const Ctx& c, uint32_t tmem, int 
           umma::st_32x32b_x32_u(lane_base + (half * 2 + ch) * 32, r32);
         }
       }
+      if (!wait_w(kQFull, qpar)) return false;  // dims 256..575 in shared memory
 #pragma unroll 1
       for (int j = 0; j < kQSRegions; ++j)
 #pragma unroll
