@@ -171,12 +171,17 @@ __device__ __forceinline__ int unit_of(const Launch& p, int ord, int n_static) {
 
 // Position of the prefetch stream: a (unit, tile) pair; ord is the unit's
 // ordinal in this CTA's sequence.  The descriptor of the next unit is loaded
-// one unit ahead.
+// one unit ahead.  In the PF instantiation (a paged cache whose pages hold 16
+// or 32 entries, so that the four warps' slices of a tile lie in different
+// pages or page halves) the page of this warp's slice is loaded as soon as
+// the cursor stands on the tile, a whole slice before its copies are issued;
+// otherwise load_slice looks it up itself.
 struct Cursor {
   Unit x;
   int ord, k;
   int4 next;
-  bool valid;
+  int page;  // page-table entry of the warp's slice (when `paged` is set)
+  bool valid, paged;
 };
 
 template <int Gc, bool X>
@@ -203,9 +208,23 @@ __device__ __forceinline__ void cursor_next(const Launch& p, Cursor& c, const vo
   cursor_seek<Gc, X>(p, c, c.ord + 1, c.next, ring, n_units);
 }
 
+// PF: load the page of warp `warp`'s slice of the cursor's tile when every
+// live entry of the slice sits in one page of the main source (then the page
+// table is the slice's only address lookup).
+template <bool X, bool PF>
+__device__ __forceinline__ void cursor_page(const Launch& p, Cursor& c, int warp) {
+  c.paged = false;
+  if (!PF || !c.valid || p.layout != DA_KV_PAGED || (p.page_size & 15) != 0) return;
+  const int t0 = c.k * kFmaTile + warp * (kFmaTile / 4);
+  if (t0 >= c.x.L || (X && min(t0 + kFmaTile / 4, c.x.L) > c.x.l_main)) return;
+  const int pi = (p.page_shift >= 0) ? (t0 >> p.page_shift) : (t0 / p.page_size);
+  c.page = __ldg(p.table + (size_t)c.x.b * p.width + pi);
+  c.paged = true;
+}
+
 // Issue this warp's copies for the cursor's tile into ring slot `slot`, then
 // close the cp.async group (always, so group counting stays uniform).
-template <int G, int D, bool X, int KT>
+template <int G, int D, bool X, int KT, bool PF>
 __device__ __forceinline__ void load_slice(const Launch& p, const Cursor& c, uint8_t* smem,
                                            int slot, int warp, int lane) {
   using S = FmaShape<G, D, KT>;
@@ -223,7 +242,12 @@ __device__ __forceinline__ void load_slice(const Launch& p, const Cursor& c, uin
       if (p.layout == DA_KV_CONTIGUOUS) {
         uniform = true;
         base_row = (long long)c.x.b * p.width + t0;
-      } else if (p.layout == DA_KV_PAGED && (p.page_size & 15) == 0) {
+      } else if (PF && c.paged) {  // the page was loaded when the cursor reached the slice
+        uniform = true;
+        const int pi = (p.page_shift >= 0) ? (t0 >> p.page_shift) : (t0 / p.page_size);
+        base_ok = c.page >= 0 && c.page < p.num_blocks;
+        base_row = (long long)c.page * p.page_size + (t0 - pi * p.page_size);
+      } else if (!PF && p.layout == DA_KV_PAGED && (p.page_size & 15) == 0) {
         uniform = true;
         const int pi = (p.page_shift >= 0) ? (t0 >> p.page_shift) : (t0 / p.page_size);
         const int page = __ldg(p.table + (size_t)c.x.b * p.width + pi);
@@ -551,7 +575,7 @@ __device__ __forceinline__ void consume_slice(const uint8_t* ks, int lane, int n
   }
 }
 
-template <int G, int D, bool X, int KT>
+template <int G, int D, bool X, int KT, bool PF>
 __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Launch p) {
   using S = FmaShape<G, D, KT>;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -582,10 +606,12 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
     cursor_seek<G, X>(p, pf, 0, load_desc(p, ring[0]), ring, n_units);
   else
     pf.valid = false;
+  cursor_page<X, PF>(p, pf, warp);
 #pragma unroll
   for (int s = 0; s < S::kStages - 1; ++s) {
-    load_slice<G, D, X, KT>(p, pf, smem, s, warp, lane);
+    load_slice<G, D, X, KT, PF>(p, pf, smem, s, warp, lane);
     cursor_next<G, X>(p, pf, ring, n_units);
+    cursor_page<X, PF>(p, pf, warp);
   }
 
   int slot = 0;
@@ -620,8 +646,10 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
         named_bar_sync(1, S::kThreads);
       }
       // refill the slot consumed in the previous iteration
-      load_slice<G, D, X, KT>(p, pf, smem, (slot + S::kStages - 1) % S::kStages, warp, lane);
+      load_slice<G, D, X, KT, PF>(p, pf, smem, (slot + S::kStages - 1) % S::kStages, warp,
+                                  lane);
       cursor_next<G, X>(p, pf, ring, n_units);
+      cursor_page<X, PF>(p, pf, warp);
       const uint8_t* ks = smem + (slot * S::kWarps + warp) * S::kWarpSlotBytes;
       const int n_valid = min(S::kTokPerWarp, x.L - k * S::kTile - warp * S::kTokPerWarp);
       if (n_valid >= S::kTokPerWarp)
@@ -730,18 +758,19 @@ __global__ void __launch_bounds__(FmaShape<G, D>::kThreads) split_fma_kernel(Lau
   }
 }
 
-template <int G, int D, bool X, int KT>
+template <int G, int D, bool X, int KT, bool PF = false>
 cudaError_t launch_x(const Launch& p, int grid, cudaStream_t stream) {
   using S = FmaShape<G, D, KT>;
-  static const cudaError_t attr = cudaFuncSetAttribute(
-      split_fma_kernel<G, D, X, KT>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
+  static const cudaError_t attr =
+      cudaFuncSetAttribute(split_fma_kernel<G, D, X, KT, PF>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
   if (attr != cudaSuccess) return attr;
-  return launch_after(split_fma_kernel<G, D, X, KT>, dim3(grid), dim3(S::kThreads), S::kSmemBytes,
-                      stream, p);
+  return launch_after(split_fma_kernel<G, D, X, KT, PF>, dim3(grid), dim3(S::kThreads),
+                      S::kSmemBytes, stream, p);
 }
 
-// Instantiations: bf16 with one or two KV sources; E4M3 and NVFP4 caches
-// with one source.
+// Instantiations: bf16 with one or two KV sources (one source: also the PF
+// form for small pages); E4M3 and NVFP4 caches with one source.
 template <int G, int D>
 cudaError_t launch_one(const Launch& p, int grid, cudaStream_t stream) {
   if (p.kv_type != kKvBf16) {
@@ -750,18 +779,21 @@ cudaError_t launch_one(const Launch& p, int grid, cudaStream_t stream) {
     if (p.kv_type == kKvFp4) return launch_x<G, D, false, kKvFp4>(p, grid, stream);
     return cudaErrorInvalidValue;
   }
-  return p.extra_k ? launch_x<G, D, true, kKvBf16>(p, grid, stream)
-                   : launch_x<G, D, false, kKvBf16>(p, grid, stream);
+  if (p.extra_k) return launch_x<G, D, true, kKvBf16>(p, grid, stream);
+  // pages of 16 or 32 entries: the page lookups go one slice ahead
+  if (p.layout == DA_KV_PAGED && (p.page_size == 16 || p.page_size == 32))
+    return launch_x<G, D, false, kKvBf16, true>(p, grid, stream);
+  return launch_x<G, D, false, kKvBf16>(p, grid, stream);
 }
 
 template <int G, int D>
 int ctas_one() {
   using S = FmaShape<G, D>;
   static int n = [] {
-    cudaFuncSetAttribute(split_fma_kernel<G, D, false, kKvBf16>,
+    cudaFuncSetAttribute(split_fma_kernel<G, D, false, kKvBf16, false>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmemBytes);
     int c = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, split_fma_kernel<G, D, false, kKvBf16>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, split_fma_kernel<G, D, false, kKvBf16, false>,
                                                       S::kThreads,
                                                       S::kSmemBytes) != cudaSuccess)
       c = 1;

@@ -61,7 +61,7 @@ def test_any_group_size_fp8_and_extra(api, g):
         assert_parity(out, lse, ro, rl)
 
 
-@pytest.mark.parametrize("page_size", [1, 8, 16, 64, 100])
+@pytest.mark.parametrize("page_size", [1, 8, 16, 32, 64, 100])
 def test_page_sizes(api, page_size):
     wl = W.make(W.PAGED, [1, 99, 700, 2100], H_q=8, H_kv=2, D_qk=128, page_size=page_size,
                 seed=page_size)
@@ -108,7 +108,26 @@ def test_layouts_give_identical_bits(api):
                         128, 128, paged.scale)
     indexed = W.Workload("i", W.INDEXED, paged.q, flat_k.contiguous(), flat_v.contiguous(),
                          paged.lengths, idx, 0, 16, 4, 128, 128, paged.scale)
-    res = [api.run_workload(w.to("cuda")) for w in (paged, contig, indexed)]
+    # the same lists again in pages of 32 and 64 entries (shuffled tables):
+    # small pages take the kernel form whose page lookups run a slice ahead
+    repaged = []
+    for P in (32, 64):
+        n_pages = [-(-L // P) for L in lens]
+        perm = torch.randperm(sum(n_pages), generator=torch.Generator().manual_seed(P))
+        kp = torch.zeros((sum(n_pages), P, 4, 128), dtype=torch.bfloat16)
+        vp = torch.zeros_like(kp)
+        table = torch.zeros((B, max(n_pages)), dtype=torch.int32)
+        first = 0
+        for b, L in enumerate(lens):
+            for i in range(n_pages[b]):
+                pg = int(perm[first + i])
+                table[b, i] = pg
+                n = min(P, L - i * P)
+                kp[pg, :n], vp[pg, :n] = kc[b, i * P:i * P + n], vc[b, i * P:i * P + n]
+            first += n_pages[b]
+        repaged.append(W.Workload(f"p{P}", W.PAGED, paged.q, kp, vp, paged.lengths, table, P, 16,
+                                  4, 128, 128, paged.scale))
+    res = [api.run_workload(w.to("cuda")) for w in (paged, contig, indexed, *repaged)]
     for o, l in res[1:]:
         assert torch.equal(o, res[0][0]) and torch.equal(l, res[0][1])
     ro, rl = oracle_for(paged)
