@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Launch p) {
 // The tensor-core variant's partials are head-interleaved: value dims in
 // groups of four, heads innermost -- element (slot, head j, dim d) at
 // ((slot * 128 + d / 4) * H_q + j) * 4 + d % 4 -- so that its epilogue's
-// stores coalesce.  Its combine takes one thread per (row, head, two 4-dim
+// stores coalesce.  Its combine takes one thread per (row, head, four 4-dim
 // groups): a warp's load of one split's group covers 32 consecutive heads
 // (512 contiguous bytes).  Every thread forms its head's weights itself with
 // the operations and order of merge_weights (its LSEs staged in its own
@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Launch p) {
 // with the split LSEs, are in flight at once: a row with up to kMlaBatch
 // splits costs one round trip to L2.
 constexpr int kMlaThreads = 256;
-constexpr int kMlaGroupsPerThread = 2;  // 4-dim groups: 8 value dims
+constexpr int kMlaGroupsPerThread = 4;  // 4-dim groups: 16 value dims, one 32-byte sector of out
 constexpr int kMlaGroupsPerCta = (kMlaThreads / 128) * kMlaGroupsPerThread;
 constexpr int kMlaBatch = 4;  // splits whose loads are issued together
 
@@ -161,9 +161,9 @@ __global__ void __launch_bounds__(kMlaThreads) combine_mla_kernel(Launch p) {
     w[2 * e] = *reinterpret_cast<const uint32_t*>(&lo);
     w[2 * e + 1] = *reinterpret_cast<const uint32_t*>(&hi);
   }
-  static_assert(kMlaGroupsPerThread == 2, "one 16-byte store of 8 value dims");
-  *reinterpret_cast<uint4*>(p.out + ((size_t)b * p.H_q + j) * 512 + g0 * 4) =
-      make_uint4(w[0], w[1], w[2], w[3]);
+  uint4* dsto = reinterpret_cast<uint4*>(p.out + ((size_t)b * p.H_q + j) * 512 + g0 * 4);
+  dsto[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  dsto[1] = make_uint4(w[4], w[5], w[6], w[7]);
   if (cb == 0 && t < 128) p.lse[(size_t)b * p.H_q + j] = (W > 0.f) ? (M + lg2(W)) * kLn2 : -INFINITY;
 }
 
