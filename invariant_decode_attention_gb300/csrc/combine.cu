@@ -11,7 +11,10 @@
 // chain runs in split order from zero, as merge.cuh states.  NB is the
 // bound on any row's split count that the plan implies (16 or 64 for one
 // value dim per thread), so a row costs one round trip to L2 without holding
-// registers for splits no row can have.
+// registers for splits no row can have.  Rows of at most 16 splits with
+// D_v <= 128 take combine_warp_kernel instead: one warp per (row, head),
+// a lane per four value dims, so a split's values are one 16-byte load per
+// lane and four heads share a CTA.
 #include "common.cuh"
 #include "merge.cuh"
 
@@ -74,6 +77,56 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(Launch p) {
     if (d < Dv) p.out[((size_t)b * p.H_q + j) * Dv + d] = __float2bfloat16_rn(acc[k]);
   }
   if (threadIdx.x == 0) p.lse[(size_t)b * p.H_q + j] = lse_out;
+}
+
+// One warp per (row, head), for D_v <= 128 and rows of at most NB splits
+// (the plan's bound): lane l owns value dims 4l .. 4l + 3, so one 16-byte
+// load per lane takes a split's whole row of values for the head, and the
+// loads of every split are in flight while the warp forms the weights.  Per
+// value dim the FMA chain is combine_kernel's: split order from zero.  (A
+// row with more than NB splits, which the plan rules out, would still be
+// merged in order by the loop after the batch.)
+constexpr int kCombineWarps = kCombineThreads / 32;
+
+template <int NB>
+__global__ void __launch_bounds__(kCombineThreads) combine_warp_kernel(Launch p) {
+  __shared__ float coef[kCombineWarps][kMaxSplitsAny];
+  wait_prior_grid();  // the split kernel's partials
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long item = (long long)blockIdx.x * kCombineWarps + warp;
+  if (item >= (long long)p.B * p.H_q) return;
+  const int b = (int)(item / p.H_q), j = (int)(item % p.H_q);
+  const int n = p.n_splits[b];
+  if (n <= 1) return;  // written final by the split kernel
+  const size_t slot0 = (size_t)b * p.max_splits;
+  const int Dv = p.D_v;
+  const bool mine = 4 * lane < Dv;
+  const size_t stride4 = (size_t)p.H_q * Dv / 4;  // float4s per split
+  const float4* o0 = reinterpret_cast<const float4*>(p.o_part + (slot0 * p.H_q + j) * Dv) + lane;
+  float4 v[NB];
+#pragma unroll
+  for (int s = 0; s < NB; ++s)
+    v[s] = (s < n && mine) ? __ldcg(o0 + (size_t)s * stride4) : make_float4(0.f, 0.f, 0.f, 0.f);
+  const float lse = merge_weights(p.lse_part + slot0 * p.H_q + j, p.H_q, n, coef[warp], lane);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  auto fma4 = [&](float c, const float4& x) {
+    acc.x = fmaf(c, x.x, acc.x);
+    acc.y = fmaf(c, x.y, acc.y);
+    acc.z = fmaf(c, x.z, acc.z);
+    acc.w = fmaf(c, x.w, acc.w);
+  };
+#pragma unroll
+  for (int s = 0; s < NB; ++s)
+    if (s < n) fma4(coef[warp][s], v[s]);
+  for (int s = NB; s < n; ++s)
+    fma4(coef[warp][s], mine ? __ldcg(o0 + (size_t)s * stride4) : make_float4(0.f, 0.f, 0.f, 0.f));
+  if (mine) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+    *reinterpret_cast<uint2*>(p.out + ((size_t)b * p.H_q + j) * Dv + 4 * lane) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+  }
+  if (lane == 0) p.lse[(size_t)b * p.H_q + j] = lse;
 }
 
 // The tensor-core variant's partials are head-interleaved: value dims in
@@ -180,6 +233,14 @@ cudaError_t launch_combine(const Launch& p, int n_bound, cudaStream_t stream) {
   if (p.D_v > kCombineThreads * kMaxDimsPerThread) return cudaErrorInvalidValue;
   const long long blocks = (long long)p.B * p.H_q;
   if (blocks == 0) return cudaSuccess;
+  if (p.D_v <= kCombineThreads && p.D_v % 4 == 0 && n_bound <= 16) {
+    const long long warp_blocks = (blocks + kCombineWarps - 1) / kCombineWarps;
+    if (n_bound <= 8)
+      return launch_after(combine_warp_kernel<8>, dim3((unsigned)warp_blocks),
+                          dim3(kCombineThreads), 0, stream, p);
+    return launch_after(combine_warp_kernel<16>, dim3((unsigned)warp_blocks),
+                        dim3(kCombineThreads), 0, stream, p);
+  }
   if (p.D_v <= kCombineThreads) {
     if (n_bound <= 16)
       return launch_after(combine_kernel<1, 16>, dim3((unsigned)blocks), dim3(kCombineThreads), 0,
