@@ -269,30 +269,49 @@ def time_steps(case, steps, warmup, split_events=True, flush=False):
     return total, per_step, split
 
 
+def packed_views(buf, specs):
+    """Views of one contiguous byte buffer: specs is a list of (shape, dtype);
+    each piece starts on a 256-byte boundary.  Returns the views in order."""
+    views, off = [], 0
+    for shape, dtype in specs:
+        n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        views.append(buf[off:off + n].view(dtype).view(shape))
+        off += (n + 255) // 256 * 256
+    return views
+
+
+def packed_bytes(specs):
+    """Size of the buffer packed_views lays `specs` out in."""
+    return sum((int(np.prod(s)) * torch.empty((), dtype=d).element_size() + 255) // 256 * 256
+               for s, d in specs)
+
+
 def e2e_steps(case, steps, warmup):
     """Same step through the public C entry point with host buffers: per step
     the step inputs (q, lengths, page table) go host->device from pinned
-    memory and (out, lse) come back; the KV cache stays resident."""
+    memory and (out, lse) come back; the KV cache stays resident.  As a
+    caller would, the inputs are staged in one pinned buffer and the outputs
+    written into one device buffer, so each direction is one copy."""
     api, w = case.api, case.wl
-    h_q = case.cpu.q.pin_memory()
-    h_len = case.cpu.lengths.pin_memory()
-    h_tab = None if case.cpu.table is None else case.cpu.table.pin_memory()
-    h_out = torch.empty(case.out.shape, dtype=torch.bfloat16).pin_memory()
-    h_lse = torch.empty(case.lse.shape, dtype=torch.float32).pin_memory()
-    d_q, d_len = torch.empty_like(w.q), torch.empty_like(w.lengths)
-    d_tab = None if w.table is None else torch.empty_like(w.table)
-    h2d = h_q.numel() * 2 + h_len.numel() * 4 + (0 if h_tab is None else h_tab.numel() * 4)
-    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+    ins = [case.cpu.q, case.cpu.lengths] + ([] if case.cpu.table is None else [case.cpu.table])
+    in_specs = [(tuple(t.shape), t.dtype) for t in ins]
+    out_specs = [(tuple(case.out.shape), torch.bfloat16), (tuple(case.lse.shape), torch.float32)]
+    h_in = torch.empty(packed_bytes(in_specs), dtype=torch.uint8).pin_memory()
+    for v, t in zip(packed_views(h_in, in_specs), ins):
+        v.copy_(t)
+    d_in = torch.empty_like(h_in, device=case.out.device)
+    d_views = packed_views(d_in, in_specs)
+    d_q, d_len = d_views[0], d_views[1]
+    d_tab = d_views[2] if len(d_views) > 2 else None
+    d_outbuf = torch.empty(packed_bytes(out_specs), dtype=torch.uint8, device=case.out.device)
+    d_out, d_lse = packed_views(d_outbuf, out_specs)
+    h_outbuf = torch.empty(d_outbuf.numel(), dtype=torch.uint8).pin_memory()
+    h2d, d2h = h_in.numel(), h_outbuf.numel()
 
     def one():
-        d_q.copy_(h_q, non_blocking=True)
-        d_len.copy_(h_len, non_blocking=True)
-        if d_tab is not None:
-            d_tab.copy_(h_tab, non_blocking=True)
-        api.forward(case.prob, case.policy, d_q, w.k, w.v, d_tab, d_len, case.ws, case.out,
-                    case.lse)
-        h_out.copy_(case.out, non_blocking=True)
-        h_lse.copy_(case.lse, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
+        api.forward(case.prob, case.policy, d_q, w.k, w.v, d_tab, d_len, case.ws, d_out, d_lse)
+        h_outbuf.copy_(d_outbuf, non_blocking=True)
 
     for _ in range(warmup):
         one()
@@ -303,7 +322,12 @@ def e2e_steps(case, steps, warmup):
         one()
     b.record()
     torch.cuda.synchronize()
-    return a.elapsed_time(b) / steps, h2d, d2h
+    # the staged result is the device step's result, bit for bit
+    h_out, h_lse = packed_views(h_outbuf, out_specs)
+    case.step()
+    torch.cuda.synchronize()
+    same = torch.equal(h_out, case.out.cpu()) and torch.equal(h_lse, case.lse.cpu())
+    return a.elapsed_time(b) / steps, h2d, d2h, same
 
 
 # ----------------------------------------------------------------- NVFP4 weight matmul
@@ -610,7 +634,7 @@ def main():
     rec = measure(case, peak, peak_kind, args.steps, args.warmup, world, dev, clocks)
     ms_per_step = rec["ms_per_step"]
     value = replica_value(kv_bytes, world, ms_per_step) / 1e9
-    e2e_ms, h2d, d2h = e2e_steps(case, max(20, args.steps // 4), args.warmup)
+    e2e_ms, h2d, d2h, e2e_same = e2e_steps(case, max(20, args.steps // 4), args.warmup)
     e2e_ms = max_over_ranks(e2e_ms, dev)
 
     if rank != 0:
@@ -643,7 +667,10 @@ def main():
         "e2e": {"value": round(replica_value(kv_bytes, world, e2e_ms) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "resident": "KV cache",
-                "api": "decode_attn_forward"},
+                "api": "decode_attn_forward",
+                "staging": "inputs in one pinned buffer, outputs in one device buffer: "
+                           "one copy each way per step",
+                "result_equals_device_step": e2e_same},
         "gpu_launches": 3 * args.steps,
         "clocks": clocks.summary(),
     }

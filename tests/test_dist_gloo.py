@@ -59,6 +59,26 @@ def test_replica_value_is_whole_job_throughput():
     assert bench.replica_value(1000, 2, 2.0) == pytest.approx(1e6)
 
 
+def test_e2e_staging_views_round_trip():
+    # the end-to-end leg stages q, lengths and the page table in one buffer
+    # (one copy per step): every view must land on a 256-byte boundary and
+    # read back exactly what was written into it
+    sys.path.insert(0, ROOT)
+    import torch
+    import bench
+    specs = [((8, 32, 128), torch.bfloat16), ((8,), torch.int32), ((3, 1000), torch.int32)]
+    buf = torch.zeros(bench.packed_bytes(specs), dtype=torch.uint8)
+    src = [torch.randn(8, 32, 128).to(torch.bfloat16), torch.arange(8, dtype=torch.int32),
+           torch.randint(-5, 100, (3, 1000), dtype=torch.int32)]
+    for v, t in zip(bench.packed_views(buf, specs), src):
+        v.copy_(t)
+    views = bench.packed_views(buf, specs)
+    for v, t in zip(views, src):
+        assert v.is_contiguous() and v.dtype == t.dtype and torch.equal(v, t)
+        assert (v.data_ptr() - buf.data_ptr()) % 256 == 0
+    assert buf.numel() == 65536 + 256 + 12032  # 32 B and 12000 B pieces padded to 256
+
+
 def test_reference_arm_under_torchrun_prints_one_line():
     port = _free_port()
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
