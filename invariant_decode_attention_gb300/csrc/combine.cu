@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_warp_kernel(Launch p)
 // shared-memory column), and the loads of a whole batch of splits, together
 // with the split LSEs, are in flight at once: a row with up to kMlaBatch
 // splits costs one round trip to L2.
-constexpr int kMlaThreads = 256;
+constexpr int kMlaThreads = 128;
 constexpr int kMlaGroupsPerThread = 4;  // 4-dim groups: 16 value dims, one 32-byte sector of out
 constexpr int kMlaGroupsPerCta = (kMlaThreads / 128) * kMlaGroupsPerThread;
 constexpr int kMlaBatch = 4;  // splits whose loads are issued together
